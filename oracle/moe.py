@@ -1,0 +1,224 @@
+"""The fused NVFP4 MoE layer, step by step, in float64 on the CPU.
+
+Test infrastructure only (see the package docstring for who may import it).
+
+Steps follow "vLLM on the NVIDIA DGX Spark: A Complete Technical Guide",
+section 7.1 (router -> quantise/dispatch -> permute, experts, unpermute ->
+combine) and section 4.3 (dispatch, two GEMMs with SwiGLU between them, top-k
+weight reduction; BF16 input quantised to FP4 on the W4A4 path), with one
+shared expert that every token uses ("Serving Solar Open 2 on DGX Spark",
+"Solar Open 2 in brief").
+
+Readings adopted where the pages are silent:
+
+* the router's logits are an input; softmax over all routed experts, top-k by
+  logit (ties to the lower expert index), weights renormalised over the k;
+* the shared expert's output is added with weight 1 and no gate;
+* each expert's gate, up and down matrices carry their own global scale;
+* ``h = silu(g) * u`` with ``silu(z) = z / (1 + exp(-z))``;
+* W4A4: X is quantised with one global scale over the whole ``[T, H]``
+  tensor; h is rounded to bf16 (the activation precision) and quantised with
+  one global scale over all rows (routed pairs and shared rows together).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import nvfp4
+
+F32 = np.float32
+
+
+def bf16_round(x):
+    """float -> nearest bf16 value (ties to even), returned as float32.
+
+    bf16 keeps the top 16 bits of an fp32; rounding adds half of the dropped
+    part with the tie going to an even kept part. Pinned by: torch's bf16
+    conversion (tests).
+    """
+    f = np.asarray(x, dtype=np.float64).astype(F32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    u = (u + 0x7FFF + lsb) >> 16 << 16
+    out = u.astype(np.uint32).view(F32)
+    return np.where(np.isnan(f), f, out)
+
+
+def route(logits, k):
+    """Router: softmax over experts, top-k, renormalised weights.
+
+    ``logits`` ``[T, E]`` fp32 -> ``(ids [T, k] int32, w [T, k] fp32)``. The k
+    slots are ordered by rank: higher logit first, equal logits (including
+    -0 and +0) by lower expert index. The weights are the softmax
+    probabilities of the chosen experts divided by their sum, computed in
+    float64 and stored as fp32.
+    Pinned by: brute-force selection on tiny inputs; weights summing to 1;
+    constructed ties; k = E returning every expert in rank order.
+    """
+    logits = np.asarray(logits, dtype=F32)
+    T, E = logits.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    l64 = logits.astype(np.float64)
+    p = np.exp(l64 - l64.max(axis=1, keepdims=True))
+    p = p / p.sum(axis=1, keepdims=True)
+    # Stable sort on the negated logit keeps ascending expert order among ties.
+    order = np.argsort(-l64, axis=1, kind="stable")
+    ids = order[:, :k]
+    pk = np.take_along_axis(p, ids, axis=1)
+    w = pk / pk.sum(axis=1, keepdims=True)
+    return ids.astype(np.int32), w.astype(F32)
+
+
+def permute(ids, E):
+    """Group the T*k (token, slot) pairs by expert with a stable counting sort.
+
+    Pair ``p = t*k + j`` goes to expert ``ids[t, j]``. Returns
+    ``counts [E]``, ``offsets [E+1]`` (exclusive prefix sum, ``offsets[E] =
+    T*k``), ``perm [T*k]`` (sorted position -> pair) and ``inv_perm [T*k]``
+    (pair -> sorted position). Inside an expert's group pairs keep ascending
+    ``p``. The shared expert's rows follow at ``T*k .. T*k + T - 1`` in token
+    order and are not listed.
+    Pinned by: inv_perm(perm) = identity, counts summing to T*k, offsets as
+    the exclusive scan, and stability against Python's sorted().
+    """
+    ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+    P = ids.size
+    if P and (ids.min() < 0 or ids.max() >= E):
+        raise ValueError("expert id out of range")
+    counts = np.zeros(E, dtype=np.int64)
+    for e in ids:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    cursor = offsets[:-1].copy()
+    perm = np.empty(P, dtype=np.int64)
+    inv_perm = np.empty(P, dtype=np.int64)
+    for p in range(P):
+        e = ids[p]
+        perm[cursor[e]] = p
+        inv_perm[p] = cursor[e]
+        cursor[e] += 1
+    return (counts.astype(np.int32), offsets.astype(np.int32),
+            perm.astype(np.int32), inv_perm.astype(np.int32))
+
+
+def silu(z):
+    """SiLU, ``z / (1 + exp(-z))``, float64. Pinned by: torch's silu (tests)."""
+    z = np.asarray(z, dtype=np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+class QuantWeight:
+    """One NVFP4 weight matrix ``[N, K]``: unpacked codes, E4M3 scales, gs."""
+
+    def __init__(self, codes, sf, gs):
+        self.codes = np.asarray(codes, dtype=np.uint8)
+        self.sf = np.asarray(sf, dtype=np.uint8)
+        self.gs = F32(gs)
+
+    @classmethod
+    def from_dense(cls, w):
+        return cls(*nvfp4.quantize(np.asarray(w, dtype=F32)))
+
+    def dequantize(self):
+        return nvfp4.dequantize(self.codes, self.sf, self.gs)
+
+
+def gate_up_swiglu(x_rows, gate, up):
+    """First GEMM pair and SwiGLU on a block of rows: ``h = silu(x Wg^T) * (x Wu^T)``.
+
+    ``x_rows`` are float64 rows already in the GEMM's input precision (bf16
+    values on W4A16, dequantised NVFP4 on W4A4); ``gate``/``up`` are
+    ``QuantWeight``. Returns ``h`` float64.
+    Pinned by: the dense one-expert reduction against torch.matmul and
+    torch's silu; brute force on tiny sizes (tests).
+    """
+    g = x_rows @ gate.dequantize().T
+    u = x_rows @ up.dequantize().T
+    return silu(g) * u
+
+
+def down_proj(h_rows, down):
+    """Second GEMM: ``y = h Wd^T`` in float64."""
+    return h_rows @ down.dequantize().T
+
+
+def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False):
+    """The whole layer for ``T`` tokens, float64.
+
+    ``x`` ``[T, H]`` (bf16 values), ``logits`` ``[T, E]`` fp32, ``experts`` a
+    list of E ``(gate, up, down)`` QuantWeight triples, ``shared`` one triple
+    or None. Returns ``out [T, H]`` float64 (and a dict of intermediates when
+    ``return_parts``):
+
+        out[t] = sum_j w[t, j] * y[(t, j)] + y_shared[t]
+
+    W4A16: ``x`` enters the GEMMs as is. W4A4: ``x`` is quantised (one global
+    scale) and dequantised first; ``h`` is rounded to bf16, quantised over all
+    rows with one global scale, and dequantised before the down GEMM.
+    Pinned by: a dense formulation (every expert on every token, weighted by a
+    T x E routing matrix) on tiny sizes, the identical-experts invariant, and
+    the one-expert dense reduction (tests).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, H = x.shape
+    E = len(experts)
+    ids, w = route(logits, k)
+    counts, offsets, perm, inv_perm = permute(ids, E)
+    parts = {"ids": ids, "w": w, "counts": counts, "offsets": offsets,
+             "perm": perm, "inv_perm": inv_perm}
+    if mode == "w4a4":
+        xq, xsf, xgs = nvfp4.quantize(x.astype(F32))
+        parts.update(xq=xq, xsf=xsf, xgs=xgs)
+        x_in = nvfp4.dequantize(xq, xsf, xgs)
+    elif mode == "w4a16":
+        x_in = x
+    else:
+        raise ValueError(mode)
+    # Rows in the order the layer lays them out: routed pairs grouped by
+    # expert (sorted order), then the shared expert's rows in token order.
+    groups = [(experts[e], perm[offsets[e]:offsets[e + 1]] // k) for e in range(E)]
+    if shared is not None:
+        groups.append((shared, np.arange(T)))
+    hs = [gate_up_swiglu(x_in[toks], gate, up) for (gate, up, _), toks in groups]
+    if mode == "w4a4":
+        sizes = [h.shape[0] for h in hs]
+        allh = np.concatenate(hs, axis=0)
+        allh_bf = bf16_round(allh)
+        hq, hsf, hgs = nvfp4.quantize(allh_bf)
+        parts.update(h_bf16=allh_bf, hq=hq, hsf=hsf, hgs=hgs)
+        hs = np.split(nvfp4.dequantize(hq, hsf, hgs), np.cumsum(sizes)[:-1], axis=0)
+    ys = [down_proj(h, trip[2]) for h, (trip, _) in zip(hs, groups)]
+    y_routed = np.concatenate(ys[:E], axis=0) if E else np.zeros((0, H))
+    out = np.zeros((T, H), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            out[t] += np.float64(w[t, j]) * y_routed[inv_perm[t * k + j]]
+    if shared is not None:
+        out += ys[E]
+    parts.update(h=hs, y_routed=y_routed)
+    if return_parts:
+        return out, parts
+    return out
+
+
+def token_outputs_w4a16(x_tokens, ids, w, expert_weights, shared):
+    """W4A16 outputs of a few tokens, one at a time, from their routing.
+
+    ``x_tokens`` ``[n, H]``, ``ids``/``w`` ``[n, k]`` from ``route``;
+    ``expert_weights(e)`` returns expert e's ``(gate, up, down)`` triple.
+    ``out[t] = sum_j w[t, j] * expert_{ids[t, j]}(x_t) + shared(x_t)``. Used to
+    check sampled tokens of workloads too large for ``layer``.
+    """
+    x_tokens = np.asarray(x_tokens, dtype=np.float64)
+    out = np.zeros_like(x_tokens)
+    for t in range(x_tokens.shape[0]):
+        xt = x_tokens[t:t + 1]
+        for j in range(ids.shape[1]):
+            g, u, d = expert_weights(int(ids[t, j]))
+            out[t] += np.float64(w[t, j]) * down_proj(gate_up_swiglu(xt, g, u), d)[0]
+        if shared is not None:
+            g, u, d = shared
+            out[t] += down_proj(gate_up_swiglu(xt, g, u), d)[0]
+    return out

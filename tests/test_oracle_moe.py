@@ -1,0 +1,203 @@
+"""Pins of the oracle's routing, permutation and layer to facts outside itself:
+brute force, invariants, library routines (torch.matmul, torch silu) and a
+dense reformulation of the layer that never permutes."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic_inputs as si
+from oracle import moe, nvfp4
+
+
+def test_route_brute_force_tiny():
+    rng = np.random.default_rng(0)
+    for T, E, k in [(5, 4, 1), (7, 6, 3), (3, 8, 8), (9, 16, 4)]:
+        logits = rng.integers(-3, 4, size=(T, E)).astype(np.float32)  # many exact ties
+        ids, w = moe.route(logits, k)
+        for t in range(T):
+            brute = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))[:k]
+            assert ids[t].tolist() == brute
+            ex = np.exp(logits[t].astype(np.float64) - logits[t].max())
+            ref = ex[brute] / ex[brute].sum()
+            assert np.abs(w[t] - ref).max() <= 1e-7
+        assert np.abs(w.astype(np.float64).sum(axis=1) - 1).max() <= 1e-6
+
+
+def test_route_ties_and_signed_zero():
+    logits = np.array([[0.0, -0.0, 0.0, -1.0, 0.0]], dtype=np.float32)
+    ids, w = moe.route(logits, 3)
+    assert ids.tolist() == [[0, 1, 2]]
+    assert np.allclose(w, 1 / 3)
+    logits = np.array([[1.0, 2.0, 2.0, 2.0]], dtype=np.float32)
+    ids, _ = moe.route(logits, 2)
+    assert ids.tolist() == [[1, 2]]
+
+
+def test_route_k_equals_e_is_full_rank_order():
+    logits = np.array([[0.3, -1.0, 2.0, 0.3, 5.0]], dtype=np.float32)
+    ids, w = moe.route(logits, 5)
+    assert ids.tolist() == [[4, 2, 0, 3, 1]]
+    p = torch.softmax(torch.tensor(logits, dtype=torch.float64), dim=1).numpy()
+    assert np.abs(w[0] - p[0, ids[0]]).max() <= 1e-7
+
+
+def test_silu_matches_torch():
+    z = np.linspace(-30, 30, 10001)
+    ref = torch.nn.functional.silu(torch.tensor(z, dtype=torch.float64)).numpy()
+    assert np.abs(moe.silu(z) - ref).max() <= 1e-12
+
+
+def test_permute_invariants_and_stability():
+    rng = np.random.default_rng(1)
+    for T, E, k in [(1, 1, 1), (16, 8, 2), (50, 7, 3), (33, 40, 5)]:
+        ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        counts, offsets, perm, inv = moe.permute(ids, E)
+        P = T * k
+        assert counts.sum() == P
+        assert offsets[0] == 0 and offsets[-1] == P
+        assert (np.diff(offsets) == counts).all()
+        assert (inv[perm] == np.arange(P)).all() and (perm[inv] == np.arange(P)).all()
+        flat = ids.reshape(-1)
+        ref = sorted(range(P), key=lambda p: (flat[p], p))   # Python's stable sort
+        assert perm.tolist() == ref
+        for e in range(E):
+            assert (flat[perm[offsets[e]:offsets[e + 1]]] == e).all()
+
+
+def test_permute_empty_and_out_of_range():
+    counts, offsets, perm, inv = moe.permute(np.zeros((0, 4), dtype=np.int32), 5)
+    assert counts.sum() == 0 and offsets.tolist() == [0] * 6 and perm.size == 0
+    with pytest.raises(ValueError):
+        moe.permute(np.array([[0, 5]]), 5)
+
+
+def _tiny_layer(cfg):
+    W = si.make_layer_weights(cfg)
+    qw = {e: tuple(moe.QuantWeight.from_dense(m.float().numpy()) for m in W[e]) for e in W}
+    x = si.make_x(cfg).float().numpy()
+    logits = si.make_logits(cfg).numpy()
+    return x, logits, [qw[e] for e in range(cfg.E)], qw[cfg.E]
+
+
+def _ffn_torch(x, trip, hq=None):
+    g, u, d = (torch.tensor(m.dequantize()) for m in trip)
+    xt = torch.tensor(x, dtype=torch.float64)
+    h = torch.nn.functional.silu(torch.matmul(xt, g.T)) * torch.matmul(xt, u.T)
+    return h.numpy(), d.numpy()
+
+
+def test_layer_matches_dense_formulation_w4a16():
+    cfg = si.CONFIGS["tiny"]
+    x, logits, experts, shared = _tiny_layer(cfg)
+    out = moe.layer(x, logits, experts, shared, cfg.k)
+    ids, w = moe.route(logits, cfg.k)
+    R = np.zeros((cfg.T, cfg.E))
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            R[t, ids[t, j]] += w[t, j]
+    dense = np.zeros_like(out)
+    for e in range(cfg.E):
+        h, d = _ffn_torch(x, experts[e])
+        dense += R[:, e:e + 1] * (torch.tensor(h) @ torch.tensor(d).T).numpy()
+    h, d = _ffn_torch(x, shared)
+    dense += (torch.tensor(h) @ torch.tensor(d).T).numpy()
+    assert np.abs(out - dense).max() <= 1e-12 * max(1.0, np.abs(dense).max())
+
+
+def test_layer_matches_dense_formulation_w4a4():
+    cfg = si.CONFIGS["tiny"]
+    x, logits, experts, shared = _tiny_layer(cfg)
+    out, parts = moe.layer(x, logits, experts, shared, cfg.k, mode="w4a4", return_parts=True)
+    ids, w = moe.route(logits, cfg.k)
+    xq, xsf, xgs = nvfp4.quantize(x.astype(np.float32))
+    xd = nvfp4.dequantize(xq, xsf, xgs)
+    # h of every routed (token, expert) pair and of the shared rows; one global
+    # scale over all of them; each row quantises on its own given that scale.
+    rows = {}
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            rows[(t, int(ids[t, j]))] = _ffn_torch(xd[t:t + 1], experts[ids[t, j]])[0][0]
+    hs_shared = _ffn_torch(xd, shared)[0]
+    allh = np.concatenate([np.stack(list(rows.values())), hs_shared])
+    hb = torch.tensor(allh, dtype=torch.float32).to(torch.bfloat16).float().numpy()
+    amax = np.abs(hb).max()
+    gs = np.float32(2688.0) / np.float32(amax)
+    assert gs == parts["hgs"]
+    dense = np.zeros_like(out)
+    for i, ((t, e), h) in enumerate(rows.items()):
+        q, sf, _ = nvfp4.quantize(np.concatenate([hb[i:i + 1], [[amax] + [0] * (hb.shape[1] - 1)]]))
+        hd = nvfp4.dequantize(q[:1], sf[:1], gs)
+        d = torch.tensor(experts[e][2].dequantize())
+        wt = w[t, list(ids[t]).index(e)]
+        dense[t] += wt * (torch.tensor(hd) @ d.T).numpy()[0]
+    for t in range(cfg.T):
+        i = len(rows) + t
+        q, sf, _ = nvfp4.quantize(np.concatenate([hb[i:i + 1], [[amax] + [0] * (hb.shape[1] - 1)]]))
+        hd = nvfp4.dequantize(q[:1], sf[:1], gs)
+        dense[t] += (torch.tensor(hd) @ torch.tensor(shared[2].dequantize()).T).numpy()[0]
+    assert np.abs(out - dense).max() <= 1e-12 * max(1.0, np.abs(dense).max())
+
+
+def test_identical_experts_invariant():
+    cfg = si.LayerConfig("same", T=12, H=64, I=32, I_s=48, E=6, k=3)
+    W = si.make_layer_weights(cfg, experts=[0, cfg.E])
+    e0 = tuple(moe.QuantWeight.from_dense(m.float().numpy()) for m in W[0])
+    sh = tuple(moe.QuantWeight.from_dense(m.float().numpy()) for m in W[cfg.E])
+    x = si.make_x(cfg).float().numpy()
+    for trial in range(3):
+        logits = np.random.default_rng(trial).standard_normal((cfg.T, cfg.E)).astype(np.float32)
+        out = moe.layer(x, logits, [e0] * cfg.E, sh, cfg.k)
+        h, d = _ffn_torch(x, e0)
+        hs, ds = _ffn_torch(x, sh)
+        ref = h @ d.T + hs @ ds.T
+        # routing weights sum to 1 (to fp32 rounding), so the mixture is the expert
+        assert np.abs(out - ref).max() <= 1e-6 * max(1.0, np.abs(ref).max())
+
+
+def test_one_expert_reduces_to_dense_ffn():
+    cfg = si.LayerConfig("one", T=10, H=128, I=64, I_s=64, E=1, k=1)
+    W = si.make_layer_weights(cfg, experts=[0])
+    e0 = tuple(moe.QuantWeight.from_dense(m.float().numpy()) for m in W[0])
+    x = si.make_x(cfg).float().numpy()
+    logits = si.make_logits(cfg).numpy()
+    out = moe.layer(x, logits, [e0], None, 1)
+    g, u, d = (torch.tensor(m.dequantize()) for m in e0)
+    xt = torch.tensor(x, dtype=torch.float64)
+    ref = torch.matmul(torch.nn.functional.silu(xt @ g.T) * (xt @ u.T), d.T).numpy()
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_token_outputs_match_layer():
+    cfg = si.CONFIGS["tiny"]
+    x, logits, experts, shared = _tiny_layer(cfg)
+    out = moe.layer(x, logits, experts, shared, cfg.k)
+    ids, w = moe.route(logits, cfg.k)
+    sel = [0, 5, 15]
+    got = moe.token_outputs_w4a16(x[sel], ids[sel], w[sel], lambda e: experts[e], shared)
+    assert np.abs(got - out[sel]).max() <= 1e-12
+
+
+def test_brute_force_gemm_tiny():
+    # plain Python loops over a few outputs of the tiny layer
+    cfg = si.CONFIGS["tiny"]
+    x, logits, experts, shared = _tiny_layer(cfg)
+    out = moe.layer(x, logits, experts, shared, cfg.k)
+    ids, w = moe.route(logits, cfg.k)
+    t = 3
+
+    def ffn_point(trip, xt, f):
+        g, u, d = trip
+        wg, wu, wd = g.dequantize(), u.dequantize(), d.dequantize()
+        acc = 0.0
+        for i in range(wg.shape[0]):
+            gi = sum(float(xt[c]) * float(wg[i, c]) for c in range(len(xt)))
+            ui = sum(float(xt[c]) * float(wu[i, c]) for c in range(len(xt)))
+            acc += gi / (1.0 + np.exp(-gi)) * ui * float(wd[f, i])
+        return acc
+
+    for f in (0, 77, 255):
+        ref = sum(float(w[t, j]) * ffn_point(experts[ids[t, j]], x[t], f) for j in range(cfg.k))
+        ref += ffn_point(shared, x[t], f)
+        assert abs(out[t, f] - ref) <= 1e-12
