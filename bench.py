@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Benchmark of the fused NVFP4 MoE layer on GB300.
+
+One step = one full pass of the layer (route, permute, [quantise x], gate/up
+GEMM + SwiGLU, [quantise h], down GEMM + routing weight, combine) over one
+batch of seeded synthetic input, through the C ABI ``moe_nvfp4_forward``.
+The default workload is the decode-shaped layer (8 tokens, hidden 4096,
+expert intermediate 1536, 320 routed experts top-8 + 1 shared, W4A16).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica of the same workload (the layer does not shard here:
+replicas only) and ``value`` is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and % of roofline (HBM GB/s decode, FP4/BF16 TFLOP/s prefill)"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--batches", type=int, default=4, help="distinct input batches rotated over steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sus": p.get("bf16_tflops_sustained"),
+                "source": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+def algorithmic(cfg, ids_list):
+    """Per-step algorithmic bytes/FLOPs averaged over the batches' routings."""
+    import numpy as np
+    w13 = 2 * cfg.I * cfg.H * 9 // 16     # packed e2m1 + one E4M3 per 16
+    w2 = cfg.H * cfg.I * 9 // 16
+    rows = cfg.T * cfg.k + cfg.T
+    touched = [len(np.unique(ids)) + 1 for ids in ids_list]  # + shared expert
+    t = statistics.mean(touched)
+    act = 2 if cfg.mode == "w4a16" else 2  # bf16 x in, bf16 out
+    gemm1_bytes = t * w13 + cfg.T * cfg.H * act + rows * cfg.I * 2
+    layer_bytes = t * (w13 + w2) + cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4 + cfg.T * cfg.H * 2
+    gemm1_flops = rows * 2 * (2 * cfg.I) * cfg.H
+    layer_flops = rows * 6 * cfg.H * cfg.I
+    return {"touched_experts": t, "gemm1_bytes": gemm1_bytes, "layer_bytes": layer_bytes,
+            "gemm1_flops": gemm1_flops, "layer_flops": layer_flops, "w13_bytes": w13, "w2_bytes": w2}
+
+
+def config_dict(cfg, nb, flush):
+    return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} I_shared={cfg.I_s} E={cfg.E} k={cfg.k} "
+                        f"{cfg.mode.upper()} +1 shared expert",
+            "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k, "mode": cfg.mode,
+            "batches": nb, "l2": flush, "weights": "seeded N(0,0.02) bf16 -> NVFP4 (g16, E4M3, fp32 gs)"}
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg, x, logits, n_rows, pool_threads=8):
+    """Times the CPU oracle on the first ``n_rows`` (token, expert) rows of a
+    batch (routed slots in rank order, then the shared expert). Returns
+    (seconds, rows_done, cpu_seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import synthetic_inputs as si
+    from oracle import moe as omoe
+
+    xs = x.float().numpy()
+    ids, w = omoe.route(logits.numpy(), cfg.k)
+    plan = []
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            plan.append((t, int(ids[t, j]), float(w[t, j])))
+        plan.append((t, cfg.E, 1.0))
+    plan = plan[:n_rows]
+    need = sorted({e for _, e, _ in plan})
+
+    def prep(e):
+        mats = [si.make_expert_weight(cfg, e, m) for m in ("gate", "up", "down")]
+        return e, tuple(omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats)
+
+    with ThreadPoolExecutor(pool_threads) as ex:
+        qw = dict(ex.map(prep, need))
+    out = np.zeros((cfg.T, cfg.H))
+    c0, t0 = time.process_time(), time.perf_counter()
+    for t, e, wt in plan:
+        g, u, d = qw[e]
+        out[t] += wt * omoe.down_proj(omoe.gate_up_swiglu(xs[t:t + 1], g, u), d)[0]
+    wall = time.perf_counter() - t0
+    return wall, len(plan), time.process_time() - c0
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synthetic_inputs as si
+    cfg = si.CONFIGS[args.config]
+    x = si.make_x(cfg)
+    logits = si.make_logits(cfg)
+    rows_per_token = cfg.k + 1
+    # one (token, expert) row per step unless K is small enough for whole tokens
+    est = oracle_sample(cfg, x, logits, 1)[0]
+    per_step = rows_per_token if (args.steps + args.warmup) * est * rows_per_token < 150 else 1
+    total_rows = min((args.steps + args.warmup) * per_step, cfg.T * rows_per_token)
+    times = []
+    # warm-up + timed steps each run `per_step` rows (rows repeat once the batch is exhausted)
+    for i in range(args.warmup + args.steps):
+        wall, n, cpu = oracle_sample(cfg, x, logits, per_step if i else per_step)
+        if i >= args.warmup:
+            times.append((wall, n, cpu))
+    wall = sum(t[0] for t in times)
+    rows = sum(t[1] for t in times)
+    cpu = sum(t[2] for t in times)
+    tokens = rows / rows_per_token
+    value = tokens / wall
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, len(times)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(cfg, 1, "n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": round(cpu / wall, 2),
+                             "kind": "oracle",
+                             "sample": f"{per_step} (token, expert) rows per step of the {cfg.name} batch; "
+                                       f"{rows} rows = {tokens:.2f} tokens timed; oracle weights prepared "
+                                       f"untimed"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    del total_rows
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synthetic_inputs as si
+    from nvfp4_mixture_experts_moe_gb300 import MOE_W4A4, MOE_W4A16, Nvfp4MoeLayer
+    from nvfp4_mixture_experts_moe_gb300 import binding as B
+
+    cfg = si.CONFIGS[args.config]
+    mode = MOE_W4A4 if cfg.mode == "w4a4" else MOE_W4A16
+    t_setup = time.perf_counter()
+    layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mode=mode, I_shared=cfg.I_s, device=dev)
+    chunk = 32
+    for e0 in range(0, cfg.E + 1, chunk):
+        W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + chunk))), threads=16)
+        for e, mats in W.items():
+            layer.set_expert(e, *mats)
+        del W
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    # distinct batches (seeds) rotated over the steps, resident in HBM
+    nb = max(1, args.batches)
+    batches = []
+    for b in range(nb):
+        c = si.LayerConfig(cfg.name, cfg.T, cfg.H, cfg.I, cfg.I_s, cfg.E, cfg.k, cfg.mode, cfg.logits,
+                           cfg.outliers, seed=cfg.seed + 1000 * b + rank)
+        batches.append((si.make_x(c).to(dev), si.make_logits(c).to(dev)))
+    ids_list = [__import__("oracle").moe.route(lg.cpu().numpy(), cfg.k)[0] for _, lg in batches]
+    alg = algorithmic(cfg, ids_list)
+
+    ws = layer.workspace()
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    desc = layer.desc()
+
+    def step(i, stage_events=None):
+        x, lg = batches[i % nb]
+        if stage_events is not None:
+            B.moe_set_stage_events(stage_events)
+        B.moe_nvfp4_forward(desc, x, lg, out, None, ws, stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    if B.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(B.MOE_STAGE_COUNT)] for _ in range(K)]
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    sampler = ClockSampler(bus if isinstance(bus, str) else None)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    launches0 = B.moe_kernel_launches()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        step(i, ev[i])
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    launches = B.moe_kernel_launches() - launches0
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
+    stage_ms = [[e[s].elapsed_time(e[s + 1]) for e in ev] for s in range(B.MOE_STAGE_COUNT - 1)]
+    ms = statistics.mean(step_ms)
+    if dist:
+        tm = torch.tensor([ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    if B.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status set during the timed steps")
+    value = cfg.T * world / (ms / 1e3)
+
+    # end to end: pinned host inputs copied in, result read back, every step
+    hx = [b[0].cpu().pin_memory() for b in batches]
+    hl = [b[1].cpu().pin_memory() for b in batches]
+    hout = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(batches[0][0])
+    dl = torch.empty_like(batches[0][1])
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(args.warmup + K):
+        flush.zero_()
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][0].record(stream)
+        dx.copy_(hx[i % nb], non_blocking=True)
+        dl.copy_(hl[i % nb], non_blocking=True)
+        B.moe_nvfp4_forward(desc, dx, dl, out, None, ws, stream)
+        hout.copy_(out, non_blocking=True)
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    if dist:
+        tm = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tm.item())
+    h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
+    d2h = hout.numel() * hout.element_size()
+
+    pk = peaks()
+    per_stage = {name: statistics.mean(stage_ms[i]) for i, name in enumerate(B.STAGES)}
+    g1_ms = per_stage["gemm1_gate_up_swiglu"]
+    if cfg.mode == "w4a16" and cfg.T <= 64:
+        bound, unit = "hbm", "GB/s"
+        achieved = alg["gemm1_bytes"] / (g1_ms / 1e3) / 1e9
+        peak = pk["hbm"]
+        traffic = None
+    else:
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = alg["gemm1_flops"] / (g1_ms / 1e3) / 1e12
+        peak = pk["bf16"] * (6.0 if cfg.mode == "w4a4" else 1.0)
+        traffic = None
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic, "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU epilogue)",
+                "peak_source": pk["source"]}
+    layer_time_hbm = alg["layer_bytes"] / (pk["hbm"] * 1e9)
+    layer_time_tc = alg["layer_flops"] / (peak * 1e12 if bound == "tensor" else pk["bf16"] * 1e12)
+    layer_roof_ms = 1e3 * max(layer_time_hbm, layer_time_tc)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp4xf16" if cfg.mode == "w4a16" else "fp4",
+            "data": "synthetic",
+            "config": config_dict(cfg, nb, "flushed: 258 MB write between timed steps"),
+            "roofline": roofline,
+            "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
+                               "bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
+                               "touched_experts": alg["touched_experts"]},
+            "stages_ms": per_stage,
+            "e2e": {"value": cfg.T * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "host_wall_s": t1 - t0, "setup_s": setup_s}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x0, l0 = batches[0][0].cpu(), batches[0][1].cpu()
+        n_rows = args.cpu_sample_tokens * (cfg.k + 1)
+        wall, rows, cpu = oracle_sample(cfg, x0, l0, n_rows, pool_threads=16)
+        line["cpu_baseline"] = {"value": rows / (cfg.k + 1) / wall, "unit": "tokens/s",
+                                "cores": round(cpu / wall, 2), "kind": "oracle",
+                                "sample": f"first {rows} (token, expert) rows = {rows / (cfg.k + 1):.0f} tokens "
+                                          f"of batch 0 through the float64 oracle; weights prepared untimed"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

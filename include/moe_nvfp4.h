@@ -1,0 +1,271 @@
+/*
+ * moe_nvfp4.h -- C ABI of the fused NVFP4 Mixture-of-Experts layer for one
+ * GB300 GPU (sm_103a).
+ *
+ * The layer (pages: "vLLM on the NVIDIA DGX Spark: A Complete Technical
+ * Guide", sections 4.3, 6.1 and 7.1; "Serving Solar Open 2 on DGX Spark",
+ * "Solar Open 2 in brief" and "The fix"):
+ *
+ *   route     softmax over E routed experts, top-k, weights renormalised
+ *   permute   (token, slot) pairs grouped by expert, stable
+ *   quantise  BF16 -> NVFP4 (W4A4 only)
+ *   GEMM 1    [gate | up] = x W13^T over NVFP4 weights, SwiGLU epilogue
+ *   GEMM 2    y = h W2^T, routing weight in the epilogue
+ *   combine   out[t] = sum_j y[(t, j)] + y_shared[t]
+ *
+ * NVFP4 ("vLLM on the NVIDIA DGX Spark", section 6.1): e2m1 elements packed
+ * two per byte (element 2j in the low nibble of byte j), one FP8 E4M3 block
+ * scale per 16 consecutive elements along K, one fp32 global scale per
+ * tensor. Global scales cross this ABI in the *quant* convention
+ * gs = (448 * 6) / amax ("GLM-5.3-Flash-NVFP4 #4" discussion, follow-up on
+ * the MoE fault); a value decodes as e2m1 * e4m3 / gs.
+ *
+ * Conventions for every call:
+ *  - Pointers are device pointers unless a comment says "host". The caller
+ *    owns every buffer; no call allocates or frees device memory on the
+ *    compute path. Scratch comes from a caller-provided workspace.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream). Argument errors are found on the host and returned
+ *    before anything is enqueued. Anomalies only visible on the device
+ *    (an expert id out of range, say) set an error word inside the
+ *    workspace; moe_get_device_status() reads it. A workspace's first 256
+ *    bytes must be zero before its first use; the library keeps them so.
+ *  - Only sm_103 devices are supported; anything else returns
+ *    MOE_ERR_UNSUPPORTED. No call traps or aborts the process.
+ *  - Matrices are row-major with the contraction dimension K contiguous.
+ *    bf16 values travel as uint16_t bit patterns.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad pointer, size, scale or layout */
+  MOE_ERR_UNSUPPORTED = 2, /* size outside the kernels' limits, or not sm_103 */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed (see moe_last_cuda_error) */
+  MOE_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded device wait gave up */
+  MOE_ERR_DEVICE = 6       /* the device flagged bad data (e.g. expert id out of range) */
+} moe_status;
+
+typedef enum {
+  MOE_W4A16 = 0, /* NVFP4 weights, bf16 activations (weight-only) */
+  MOE_W4A4 = 1   /* NVFP4 weights and activations (block-scaled FP4 MMA) */
+} moe_mode;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* The last CUDA error string seen by this library in this thread (static). */
+const char* moe_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------
+ * Router.  "Serving Solar Open 2 on DGX Spark", "Solar Open 2 in brief"
+ * (top-k routing over routed experts); "vLLM on the NVIDIA DGX Spark",
+ * section 7.1 ([Router] stage).
+ *
+ * logits   fp32 [T, E]
+ * topk_ids int32 [T, k] out: experts by rank; higher logit first, equal
+ *          logits by lower expert index
+ * topk_w   fp32 [T, k] out: softmax probabilities of the chosen experts
+ *          renormalised to sum to 1
+ * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0 (T = 0 is a no-op).
+ * NaN logits are outside the contract (results unspecified, no fault).
+ */
+moe_status moe_route_topk(const float* logits, int T, int E, int k,
+                          int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Permutation into expert-contiguous groups.  "vLLM on the NVIDIA DGX
+ * Spark", section 4.3 (token dispatch) and section 7.1
+ * ([Permute-Experts-Unpermute]).
+ *
+ * Pair p = t*k + j is routed to expert topk_ids[p]. Outputs:
+ * counts   int32 [E]    pairs per expert
+ * offsets  int32 [E+1]  exclusive prefix sum of counts; offsets[E] = T*k
+ * perm     int32 [T*k]  sorted position -> pair; ascending p within a group
+ * inv_perm int32 [T*k]  pair -> sorted position
+ * ws       scratch of at least moe_permute_workspace_size(T, k, E) bytes
+ * An id outside [0, E) sets MOE_ERR_DEVICE in the workspace status word
+ * (read it with moe_get_device_status); such pairs are dropped.
+ */
+size_t moe_permute_workspace_size(int T, int k, int E);
+moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E,
+                       int32_t* counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv_perm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * BF16 -> NVFP4 quantisation with a dynamic per-tensor global scale.
+ * "vLLM on the NVIDIA DGX Spark", sections 4.3 (BF16 input quantised to FP4
+ * inside the fused kernel) and 6.1 (format); the 448 clamp of the block
+ * scale is from "Serving Solar Open 2 on DGX Spark", "Supporting real NVFP4
+ * checkpoints".
+ *
+ * Steps, each a correctly rounded fp32 operation:
+ *   amax = max |x|; gs = 2688 / amax (gs = 1 when amax = 0)
+ *   per 16-element block: s = (max|x_i| / 6) * gs; sf = E4M3(s), round to
+ *   nearest even, saturating at 448; if sf = 0 the codes are 0, otherwise
+ *   code_i = e2m1(x_i * (gs / sf)), nearest even, saturating at 6, sign kept.
+ *
+ * x      bf16 [rows, K], K % 16 == 0
+ * q      uint8 [rows, K/2] out, packed codes (element 2j in the low nibble)
+ * sf     uint8 [rows, K/16] out, E4M3 block scales
+ * gs_out fp32 [1] out (device)
+ * ws     scratch of at least moe_quantize_workspace_size() bytes
+ */
+size_t moe_quantize_workspace_size(void);
+moe_status moe_nvfp4_quantize(const uint16_t* x, int rows, int K, uint8_t* q,
+                              uint8_t* sf, float* gs_out, void* ws, size_t ws_bytes,
+                              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Weight preparation (one-time, synchronous).  "Serving Solar Open 2 on DGX
+ * Spark", "Supporting real NVFP4 checkpoints" (checkpoint weights are
+ * converted once into the kernels' tile layout, with gate/up ordering).
+ *
+ * Converts one linear NVFP4 matrix into the opaque tile layout the GEMMs
+ * read. codes uint8 [N, K/2] (packed), sf uint8 [N, K/16] (E4M3), both
+ * device. gs is a HOST array of fp32 global scales (quant convention): one
+ * entry for a plain matrix, two (gate, up) when gate_up != 0, in which case
+ * the N rows are [gate (N/2 rows); up (N/2 rows)]. out must hold
+ * moe_prepare_size(N, K, mode, gate_up) bytes, 256-byte aligned.
+ * Errors: gs <= 0 or non-finite (a zero scale would silently zero every
+ * expert output, the failure described in "GLM-5.3-Flash-NVFP4 #4"), a block
+ * scale with its sign bit set or a NaN code, N % 128 != 0 (N/2 % 64 for
+ * gate_up), K % 64 != 0 -> MOE_ERR_INVALID_ARG. The call synchronises the
+ * stream.
+ */
+size_t moe_prepare_size(int N, int K, moe_mode mode, int gate_up);
+moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf,
+                                     const float* gs, int N, int K, moe_mode mode,
+                                     int gate_up, void* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped GEMM over prepared NVFP4 weights.  "vLLM on the NVIDIA DGX
+ * Spark", section 4.3 (the two GEMMs of the fused MoE, SwiGLU and top-k
+ * weight reduction fused) and section 6.1 (alpha = 1 / (gs_a * gs_w)).
+ *
+ * Output row r belongs to group g when group_offsets[g] <= r <
+ * group_offsets[g+1]; group g multiplies by prepared block g of `weights`
+ * (blocks are moe_prepare_size(N, K, mode, gate_up) bytes apart), except
+ * that the last group uses `last_weights` when it is not NULL (the shared
+ * expert). Row r reads A row a_row_index[r] (or r when NULL).
+ *
+ * gate_up = 1: the weights are a prepared [gate; up] pair (N = 2*I); the
+ *   epilogue writes h = silu(x Wg^T / gs) * (x Wu^T / gs) as bf16 [rows, I].
+ * gate_up = 0: the epilogue writes y = (x W^T / gs) * row_scale[r] as bf16
+ *   [rows, N] (row_scale NULL means 1).
+ * W4A16: a is bf16 [a_rows, K]. W4A4: a is packed NVFP4 [a_rows, K/2] with
+ *   E4M3 scales a_sf [a_rows, K/16] and device global scale a_gs.
+ * out_amax (nullable, device fp32, must start at 0): atomically maxed with
+ *   |out| (as stored), to feed the next quantisation.
+ * ws: scratch of at least moe_gemm_workspace_size(num_groups) bytes.
+ * Limits: K % 64 == 0, N % 128 == 0, num_groups <= 1025.
+ */
+typedef struct {
+  moe_mode mode;
+  int gate_up;
+  int num_groups;
+  int N, K;
+  const void* weights;
+  const void* last_weights;
+  const int32_t* group_offsets;
+  const void* a;
+  const uint8_t* a_sf;
+  const float* a_gs;
+  const int32_t* a_row_index;
+  const float* row_scale;
+  uint16_t* out;
+  float* out_amax;
+} moe_gemm_args;
+
+size_t moe_gemm_workspace_size(int num_groups);
+moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * SwiGLU on a materialised gate/up product ("vLLM on the NVIDIA DGX Spark",
+ * section 4.3). gu fp32 [rows, 2*I] with gate in columns [0, I) and up in
+ * [I, 2I); h bf16 [rows, I] = silu(gate) * up, silu(z) = z / (1 + e^-z).
+ * The fused path does this inside GEMM 1's epilogue; this call is the
+ * standalone step.
+ */
+moe_status moe_swiglu(const float* gu, int rows, int I, uint16_t* h,
+                      moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine back to token order ("vLLM on the NVIDIA DGX Spark", section 7.1
+ * [Combine]; section 4.3 top-k weight reduction). Deterministic: fp32 sums
+ * in the fixed order j = 0..k-1, then the shared row, rounded once to bf16.
+ *
+ * y        bf16 [T*k (+T), H]: routed rows in sorted order, then (if
+ *          y_shared_rows != 0) the shared expert's T rows
+ * inv_perm int32 [T*k] pair -> sorted row
+ * topk_w   fp32 [T, k] or NULL: multiplies row (t, j) (NULL when GEMM 2
+ *          already applied the routing weight)
+ * out      bf16 [T, H]
+ */
+moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
+                       int y_shared_rows, int T, int k, int H, uint16_t* out,
+                       moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The whole layer. Weights come prepared (moe_nvfp4_prepare_weights):
+ * w13 holds E gate/up blocks, w2 E down blocks, back to back; the shared
+ * expert's blocks are separate and may be NULL (no shared expert).
+ */
+typedef struct {
+  int T, H, I, I_shared, E, k;
+  moe_mode mode;
+  const void* w13;
+  const void* w2;
+  const void* w13_shared;
+  const void* w2_shared;
+} moe_layer_desc;
+
+/* Workspace bytes moe_nvfp4_forward needs for this descriptor. */
+size_t moe_workspace_size(const moe_layer_desc* L);
+
+/* x bf16 [T, H], logits fp32 [T, E] -> out bf16 [T, H]; topk_ids_out
+ * (nullable) int32 [T, k] receives the routing. ws must hold
+ * moe_workspace_size(L) bytes, 256-byte aligned. */
+moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const float* logits,
+                             uint16_t* out, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/* Synchronises `stream`, returns and clears the device status word kept in
+ * the first bytes of a workspace used by the calls above. */
+moe_status moe_get_device_status(void* ws, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Measurement hooks (no counterpart in the pages; used by the benchmark).
+ *
+ * moe_set_stage_events: `events` is a HOST array of n >= MOE_STAGE_COUNT
+ * cudaEvent_t handles owned by the caller. The next moe_nvfp4_forward call
+ * on this host thread records events[0] before its first kernel and
+ * events[i] after stage i (route, permute, quantise x, GEMM 1, quantise h,
+ * GEMM 2, combine; a stage the mode does not run records at the same point
+ * as the previous one), all on the call's stream; the setting is then
+ * cleared. Pass NULL to clear it explicitly.
+ *
+ * moe_kernel_launches: number of kernels this library has launched in this
+ * process so far (all threads).
+ */
+#define MOE_STAGE_COUNT 8
+moe_status moe_set_stage_events(void* const* events, int n);
+unsigned long long moe_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,452 @@
+// C ABI entry points: argument validation on the host, workspace carving,
+// and the launch sequence of the fused layer. Declarations and the contract
+// of every call are in include/moe_nvfp4.h.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+static thread_local char g_last_cuda_error[256] = "no CUDA error";
+static std::atomic<unsigned long long> g_launches{0};
+static thread_local cudaEvent_t g_stage_events[MOE_STAGE_COUNT];
+static thread_local bool g_stage_events_set = false;
+
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+// Records stage event i of the current forward, if the caller asked for them.
+static void stage_mark(int i, cudaStream_t s) {
+  if (g_stage_events_set && i < MOE_STAGE_COUNT) cudaEventRecord(g_stage_events[i], s);
+}
+
+moe_status cuda_ok(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+// sm_103 only. Checked once per device.
+static moe_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_ok(e);
+  static std::mutex mu;
+  static int known[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (known[dev] == 0) {
+      int major = 0, minor = 0;
+      e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+      if (e != cudaSuccess) return cuda_ok(e);
+      e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+      if (e != cudaSuccess) return cuda_ok(e);
+      known[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return known[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+  }
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Carves consecutive 256-byte aligned pieces out of a workspace.
+struct Carver {
+  uint8_t* base;
+  size_t off;
+  template <class T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off = align_up(off + count * sizeof(T));
+    return p;
+  }
+};
+
+// Everything the fused forward keeps in its workspace.
+struct ForwardWs {
+  WsHeader* hdr;
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;   // [E+1]
+  int32_t* gofs;      // [E+2] group offsets: routed groups, then the shared rows [P, P+T)
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* row_token;
+  float* row_weight;
+  void* perm_scratch;
+  uint16_t* h;        // [rows, I]
+  uint16_t* y;        // [rows, H]
+  uint8_t* xq;        // W4A4: [T, H/2]
+  uint8_t* xsf;       // W4A4: [T, H/16]
+  float* xgs;
+  uint8_t* hq;        // W4A4: [rows, I/2]
+  uint8_t* hsf;       // W4A4: [rows, I/16]
+  float* hgs;
+  size_t bytes;
+};
+
+static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
+  const size_t P = (size_t)L.T * L.k;
+  const size_t shared = L.w13_shared ? (size_t)L.T : 0;
+  const size_t rows = P + shared;
+  Carver c{static_cast<uint8_t*>(ws), 0};
+  ForwardWs f;
+  f.hdr = c.take<WsHeader>(1);
+  f.ids = c.take<int32_t>(P);
+  f.w = c.take<float>(P);
+  f.counts = c.take<int32_t>(L.E);
+  f.offsets = c.take<int32_t>(L.E + 1);
+  f.gofs = c.take<int32_t>(L.E + 2);
+  f.perm = c.take<int32_t>(P);
+  f.inv_perm = c.take<int32_t>(P);
+  f.row_token = c.take<int32_t>(P + L.T);   // routed rows, then one per token
+  f.row_weight = c.take<float>(P + L.T);
+  f.perm_scratch = c.take<uint8_t>(permute_scratch_bytes(L.T, L.k, L.E));
+  f.h = c.take<uint16_t>(rows * L.I);
+  f.y = c.take<uint16_t>(rows * L.H);
+  if (L.mode == MOE_W4A4) {
+    f.xq = c.take<uint8_t>((size_t)L.T * L.H / 2);
+    f.xsf = c.take<uint8_t>((size_t)L.T * L.H / 16);
+    f.xgs = c.take<float>(1);
+    f.hq = c.take<uint8_t>(rows * L.I / 2);
+    f.hsf = c.take<uint8_t>(rows * L.I / 16);
+    f.hgs = c.take<float>(1);
+  } else {
+    f.xq = f.xsf = f.hq = f.hsf = nullptr;
+    f.xgs = f.hgs = nullptr;
+  }
+  f.bytes = c.off;
+  return f;
+}
+
+static size_t prep_size(int N, int K, moe_mode mode, int gate_up) {
+  (void)gate_up;
+  if (mode == MOE_W4A16) return sizeof(PrepHeader) + w4a16_data_bytes(N, K) + w4a16_sf_bytes(N, K);
+  return sizeof(PrepHeader) + (size_t)N * K / 2 + prepare_w4a4_sf_bytes(N, K);
+}
+
+static moe_status validate_layer(const moe_layer_desc* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (L->T < 0 || L->H <= 0 || L->I <= 0 || L->E < 1 || L->k < 1) return MOE_ERR_INVALID_ARG;
+  if (L->mode != MOE_W4A16 && L->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (L->E > 1024 || L->k > 32 || L->k > L->E) return MOE_ERR_UNSUPPORTED;
+  if (L->H % 128 || L->I % 64) return MOE_ERR_UNSUPPORTED;
+  if (L->w13 == nullptr || L->w2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((L->w13_shared == nullptr) != (L->w2_shared == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (L->w13_shared && L->I_shared != L->I) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(L->w13, kAlign) || !aligned(L->w2, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (L->w13_shared && (!aligned(L->w13_shared, kAlign) || !aligned(L->w2_shared, kAlign)))
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)L->T * L->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                          moe_stream_t stream) {
+  if (T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || k > 32 || k > E) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_route_topk(logits, T, E, k, topk_ids, topk_w, (cudaStream_t)stream);
+}
+
+size_t moe_permute_workspace_size(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return sizeof(WsHeader) + permute_scratch_bytes(T, k, E);
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                       int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || (long long)T * k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !perm || !inv_perm)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < moe_permute_workspace_size(T, k, E)) return MOE_ERR_WORKSPACE;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  auto* hdr = static_cast<WsHeader*>(ws);
+  return launch_permute(topk_ids, T, k, E, counts, offsets, perm, inv_perm, &hdr->status,
+                        static_cast<uint8_t*>(ws) + sizeof(WsHeader), nullptr, nullptr, nullptr, nullptr,
+                        (cudaStream_t)stream);
+}
+
+size_t moe_quantize_workspace_size(void) { return sizeof(WsHeader); }
+
+moe_status moe_nvfp4_quantize(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t* sf, float* gs_out,
+                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 16) return MOE_ERR_INVALID_ARG;
+  if (!gs_out) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!x || !q || !sf)) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!aligned(x, 16) || !aligned(q, 8))) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < moe_quantize_workspace_size()) return MOE_ERR_WORKSPACE;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  auto* hdr = static_cast<WsHeader*>(ws);
+  st = cuda_ok(cudaMemsetAsync(&hdr->amax[0], 0, sizeof(float), s));
+  if (st != MOE_OK) return st;
+  st = launch_amax_bf16(x, (size_t)rows * K, &hdr->amax[0], s);
+  if (st != MOE_OK) return st;
+  return launch_quantize_bf16(x, rows, K, &hdr->amax[0], q, sf, gs_out, s);
+}
+
+size_t moe_prepare_size(int N, int K, moe_mode mode, int gate_up) {
+  if (N <= 0 || K <= 0) return 0;
+  return prep_size(N, K, mode, gate_up);
+}
+
+static __device__ int g_prepare_flag;
+
+moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf, const float* gs, int N, int K,
+                                     moe_mode mode, int gate_up, void* out, moe_stream_t stream) {
+  if (!codes || !sf || !gs || !out) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_W4A16 && mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 64 || N % 128) return MOE_ERR_INVALID_ARG;
+  if (gate_up && (N / 2) % 64) return MOE_ERR_INVALID_ARG;
+  if (!aligned(out, kAlign)) return MOE_ERR_INVALID_ARG;
+  const int ngs = gate_up ? 2 : 1;
+  for (int i = 0; i < ngs; ++i)
+    if (!(gs[i] > 0.0f) || !std::isfinite(gs[i])) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  PrepHeader h;
+  std::memset(&h, 0, sizeof(h));
+  h.magic = kPrepMagic;
+  h.mode = mode;
+  h.gate_up = gate_up;
+  h.N = N;
+  h.K = K;
+  h.alpha[0] = 1.0f / gs[0];
+  h.alpha[1] = gate_up ? 1.0f / gs[1] : 0.0f;
+  uint8_t* o = static_cast<uint8_t*>(out);
+  st = cuda_ok(cudaMemcpyAsync(o, &h, sizeof(h), cudaMemcpyHostToDevice, s));
+  if (st != MOE_OK) return st;
+  int* flag = nullptr;
+  st = cuda_ok(cudaGetSymbolAddress(reinterpret_cast<void**>(&flag), g_prepare_flag));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaMemsetAsync(flag, 0, sizeof(int), s));
+  if (st != MOE_OK) return st;
+  uint8_t* data = o + sizeof(PrepHeader);
+  if (mode == MOE_W4A16)
+    st = launch_prepare_w4a16(codes, sf, N, K, gate_up, data, data + w4a16_data_bytes(N, K), flag, s);
+  else
+    st = launch_prepare_w4a4(codes, sf, N, K, gate_up, data, data + (size_t)N * K / 2, flag, s);
+  if (st != MOE_OK) return st;
+  int hflag = 0;
+  st = cuda_ok(cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, s));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaStreamSynchronize(s));
+  if (st != MOE_OK) return st;
+  return hflag ? MOE_ERR_INVALID_ARG : MOE_OK;
+}
+
+size_t moe_gemm_workspace_size(int num_groups) {
+  (void)num_groups;
+  return sizeof(WsHeader);
+}
+
+static moe_status run_gemm(const GemmPlan& p, cudaStream_t s) {
+  if (p.mode == MOE_W4A16) return launch_gemm_small_w4a16(p, 0x7fffffff, s);
+  return MOE_ERR_UNSUPPORTED;
+}
+
+moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!a) return MOE_ERR_INVALID_ARG;
+  if (a->mode != MOE_W4A16 && a->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (a->num_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (a->num_groups == 0) return MOE_OK;
+  if (a->num_groups > 1025) return MOE_ERR_UNSUPPORTED;
+  if (a->K <= 0 || a->N <= 0 || a->K % 64 || a->N % 128) return MOE_ERR_UNSUPPORTED;
+  if (a->gate_up && (a->N / 2) % 64) return MOE_ERR_UNSUPPORTED;
+  if (!a->weights || !a->group_offsets || !a->a || !a->out) return MOE_ERR_INVALID_ARG;
+  if (a->mode == MOE_W4A4 && (!a->a_sf || !a->a_gs)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a->weights, kAlign) || (a->last_weights && !aligned(a->last_weights, kAlign)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(a->a, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < moe_gemm_workspace_size(a->num_groups)) return MOE_ERR_WORKSPACE;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  GemmPlan p;
+  p.mode = a->mode;
+  p.gate_up = a->gate_up;
+  p.num_groups = a->num_groups;
+  p.N = a->N;
+  p.K = a->K;
+  p.weights = static_cast<const uint8_t*>(a->weights);
+  p.weight_stride = prep_size(a->N, a->K, a->mode, a->gate_up);
+  p.last_weights = static_cast<const uint8_t*>(a->last_weights);
+  p.group_offsets = a->group_offsets;
+  p.a = a->a;
+  p.a_sf = a->a_sf;
+  p.a_gs = a->a_gs;
+  p.a_row_index = a->a_row_index;
+  p.row_scale = a->row_scale;
+  p.out = a->out;
+  p.out_amax = a->out_amax;
+  p.status = &static_cast<WsHeader*>(ws)->status;
+  p.max_rows = 1 << 30;
+  return run_gemm(p, (cudaStream_t)stream);
+}
+
+moe_status moe_swiglu(const float* gu, int rows, int I, uint16_t* h, moe_stream_t stream) {
+  if (rows < 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!gu || !h) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_swiglu(gu, rows, I, h, (cudaStream_t)stream);
+}
+
+moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int y_shared_rows,
+                       int T, int k, int H, uint16_t* out, moe_stream_t stream) {
+  if (T < 0 || k < 1 || H <= 0 || H % 8) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y || !inv_perm || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_combine(y, inv_perm, topk_w, y_shared_rows ? 1 : 0, T, k, H, out, (cudaStream_t)stream);
+}
+
+size_t moe_workspace_size(const moe_layer_desc* L) {
+  if (validate_layer(L) != MOE_OK) return 0;
+  return carve_forward(*L, nullptr).bytes;
+}
+
+moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const float* logits, uint16_t* out,
+                             int32_t* topk_ids_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = validate_layer(L);
+  if (st != MOE_OK) return st;
+  if (L->T == 0) return MOE_OK;
+  if (!x || !logits || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_WORKSPACE;
+  ForwardWs f = carve_forward(*L, ws);
+  if (ws_bytes < f.bytes) return MOE_ERR_WORKSPACE;
+  st = check_device();
+  if (st != MOE_OK) return st;
+  if (L->mode == MOE_W4A4) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int T = L->T, k = L->k, E = L->E, H = L->H, I = L->I;
+  const int P = T * k;
+  const bool has_shared = L->w13_shared != nullptr;
+  const int rows = P + (has_shared ? T : 0);
+  int32_t* ids = topk_ids_out ? topk_ids_out : f.ids;
+  struct StageGuard {  // the events apply to one forward call only
+    ~StageGuard() { g_stage_events_set = false; }
+  } guard;
+
+  stage_mark(0, s);
+  st = launch_route_topk(logits, T, E, k, ids, f.w, s);
+  if (st != MOE_OK) return st;
+  stage_mark(1, s);
+  st = launch_permute(ids, T, k, E, f.counts, f.offsets, f.perm, f.inv_perm, &f.hdr->status, f.perm_scratch,
+                      f.row_token, f.row_weight, f.w, f.gofs, s);
+  if (st != MOE_OK) return st;
+  stage_mark(2, s);
+  stage_mark(3, s);  // quantise x: W4A4 only
+
+  const int G = E + (has_shared ? 1 : 0);
+  GemmPlan g1;
+  std::memset(&g1, 0, sizeof(g1));
+  g1.mode = L->mode;
+  g1.gate_up = 1;
+  g1.num_groups = G;
+  g1.N = 2 * I;
+  g1.K = H;
+  g1.weights = static_cast<const uint8_t*>(L->w13);
+  g1.weight_stride = prep_size(2 * I, H, L->mode, 1);
+  g1.last_weights = has_shared ? static_cast<const uint8_t*>(L->w13_shared) : nullptr;
+  g1.group_offsets = f.gofs;
+  g1.a = x;
+  g1.a_row_index = f.row_token;
+  g1.out = f.h;
+  g1.status = &f.hdr->status;
+  g1.max_rows = rows;
+  st = run_gemm(g1, s);
+  if (st != MOE_OK) return st;
+  stage_mark(4, s);
+  stage_mark(5, s);  // quantise h: W4A4 only
+
+  GemmPlan g2 = g1;
+  g2.gate_up = 0;
+  g2.N = H;
+  g2.K = I;
+  g2.weights = static_cast<const uint8_t*>(L->w2);
+  g2.weight_stride = prep_size(H, I, L->mode, 0);
+  g2.last_weights = has_shared ? static_cast<const uint8_t*>(L->w2_shared) : nullptr;
+  g2.a = f.h;
+  g2.a_row_index = nullptr;
+  g2.row_scale = f.row_weight;
+  g2.out = f.y;
+  st = run_gemm(g2, s);
+  if (st != MOE_OK) return st;
+  stage_mark(6, s);
+  st = launch_combine(f.y, f.inv_perm, nullptr, has_shared ? 1 : 0, T, k, H, out, s);
+  if (st != MOE_OK) return st;
+  stage_mark(7, s);
+  return MOE_OK;
+}
+
+moe_status moe_set_stage_events(void* const* events, int n) {
+  if (events == nullptr) {
+    g_stage_events_set = false;
+    return MOE_OK;
+  }
+  if (n < MOE_STAGE_COUNT) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_STAGE_COUNT; ++i) {
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_stage_events_set = true;
+  return MOE_OK;
+}
+
+unsigned long long moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_get_device_status(void* ws, moe_stream_t stream) {
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0;
+  moe_status st = cuda_ok(cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaMemsetAsync(ws, 0, sizeof(int), s));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaStreamSynchronize(s));
+  if (st != MOE_OK) return st;
+  return (moe_status)v;
+}
+
+}  // extern "C"

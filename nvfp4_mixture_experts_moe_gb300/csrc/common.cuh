@@ -1,0 +1,123 @@
+// Shared device/host helpers of the CUDA path (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe_nvfp4.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Workspace header: every workspace starts with this 256-byte block. The
+// first word is the device status (0 = OK, otherwise a moe_status code).
+struct WsHeader {
+  int status;
+  int pad0;
+  float amax[4];     // atomic-max slots for dynamic global scales
+  int pad[58];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr size_t kAlign = 256;
+__host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Prepared weight block header (first 256 bytes of every prepared matrix).
+constexpr uint32_t kPrepMagic = 0x3446564Eu;  // "NVF4"
+struct PrepHeader {
+  uint32_t magic;
+  int mode;      // moe_mode
+  int gate_up;   // 1: [gate; up] pair, rows interleaved by 8
+  int N, K;
+  float alpha[2];  // 1/gs (gate, up) or (w, unused)
+  int pad[57];
+};
+static_assert(sizeof(PrepHeader) == 256, "prepared header is 256 bytes");
+
+// W4A16 layout after the header: fragment-ordered codes, N/16 x K/64 blocks
+// of 512 bytes ([row tile][k block]); then the E4M3 scales, same blocks of
+// 64 bytes. Within a data block, lane L = 4*g + t of a warp owns bytes
+// [16L, 16L+16): word s (k16 step s of the block) holds, byte by byte, the
+// code pairs of (row g, k 16s+2t..+1), (row g+8, same k), (row g, k+8..+9),
+// (row g+8, k+8..+9) -- the A-fragment order of an m16n8k16 MMA. Within a
+// scale block, group g owns bytes [8g, 8g+8): scales of row g for the four
+// k16 groups, then those of row g+8.
+__host__ __device__ inline size_t w4a16_data_bytes(int N, int K) { return (size_t)N * K / 2; }
+__host__ __device__ inline size_t w4a16_sf_bytes(int N, int K) { return (size_t)N * K / 16; }
+
+// ---------------------------------------------------------------------------
+// Small device helpers.
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// Four e2m1 pairs (the four bytes of w) to four f16x2 words.
+__device__ __forceinline__ void cvt_e2m1x8_f16(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) to f16x2; exact.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  uint16_t h = (uint16_t)two_bytes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint2 ldg_stream2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (the hardware conversion).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// atomic max of a non-negative float via its integer bit pattern (exact and
+// order-independent).
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
+  atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
+}
+
+__device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace moe

@@ -1,0 +1,66 @@
+// Internal launchers shared between the translation units of the library.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Records the CUDA error string for moe_last_cuda_error() and maps it.
+moe_status cuda_ok(cudaError_t e);
+
+// Adds n to the process-wide count of kernels this library launched.
+void count_launches(int n);
+
+constexpr int kPermSingleMax = 8192;  // pairs handled by the one-CTA permutation
+
+moe_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                             cudaStream_t s);
+
+size_t permute_scratch_bytes(int T, int k, int E);
+moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* inv_perm, int* status, void* scratch,
+                          int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
+                          cudaStream_t s);
+
+// Quantisation: amax into *amax (must be zeroed first), then codes.
+moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s);
+moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float* amax, uint8_t* q,
+                                uint8_t* sf, float* gs_out, cudaStream_t s);
+
+moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStream_t s);
+moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
+                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s);
+
+// Weight preparation (device part; the host validates sizes and scales).
+moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
+                                uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s);
+moe_status launch_prepare_w4a4(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
+                               uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s);
+size_t prepare_w4a4_sf_bytes(int N, int K);
+
+// Grouped GEMMs.
+struct GemmPlan {
+  moe_mode mode;
+  int gate_up;
+  int num_groups;           // G
+  int N, K;
+  const uint8_t* weights;   // block 0
+  size_t weight_stride;     // bytes between blocks
+  const uint8_t* last_weights;  // block used by group G-1 (may equal weights + (G-1)*stride)
+  const int32_t* group_offsets; // [G+1]
+  const void* a;
+  const uint8_t* a_sf;
+  const float* a_gs;
+  const int32_t* a_row_index;
+  const float* row_scale;
+  uint16_t* out;
+  float* out_amax;
+  int* status;
+  int max_rows;             // upper bound of group_offsets[G] (sizes launches)
+};
+
+// Small-group path: mma.sync m16n8k16 over register-dequantised weights; one
+// pass of up to 8 rows per weight tile. Handles groups with rows <= max_rows.
+moe_status launch_gemm_small_w4a16(const GemmPlan& p, int rows_limit, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,80 @@
+// One-time weight preparation: linear NVFP4 matrices -> the tile layouts the
+// GEMM kernels read. "Serving Solar Open 2 on DGX Spark", "Supporting real
+// NVFP4 checkpoints" (pre-quantised checkpoint weights are converted once
+// into the kernel's MMA tile layout, including the fused gate/up ordering).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+// Source row of output row o. For a gate/up pair the N rows arrive as
+// [gate (N/2); up (N/2)] and leave interleaved by 8: output rows 16j..16j+7
+// are gate rows 8j..8j+7 and 16j+8..16j+15 are up rows 8j..8j+7, so one
+// 16-row MMA tile holds the gate and up rows of the same 8 features.
+__device__ __forceinline__ int src_row(int o, int N, int gate_up) {
+  if (!gate_up) return o;
+  const int j = o >> 4, w = o & 15;
+  return w < 8 ? 8 * j + w : N / 2 + 8 * j + (w - 8);
+}
+
+__device__ __forceinline__ void check_sf(uint8_t v, int* flag) {
+  if ((v & 0x80u) || v == 0x7fu) atomicOr(flag, 1);
+}
+
+// One thread per output byte of the fragment-ordered codes.
+__global__ void prepare_w4a16_data_kernel(const uint8_t* __restrict__ codes, int N, int K, int gate_up,
+                                          uint8_t* __restrict__ out) {
+  const size_t total = (size_t)N * K / 2;
+  const int kblocks = K / 64;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t blk = i / 512;
+    const int within = (int)(i % 512);
+    const int mb = (int)(blk / kblocks), kb = (int)(blk % kblocks);
+    const int lane = within / 16, s = (within / 4) % 4, b = within % 4;
+    const int g = lane >> 2, t = lane & 3;
+    const int r = 16 * mb + g + ((b & 1) ? 8 : 0);
+    const int k = 64 * kb + 16 * s + 2 * t + ((b & 2) ? 8 : 0);
+    out[i] = codes[(size_t)src_row(r, N, gate_up) * (K / 2) + k / 2];
+  }
+}
+
+__global__ void prepare_w4a16_sf_kernel(const uint8_t* __restrict__ sf, int N, int K, int gate_up,
+                                        uint8_t* __restrict__ out, int* flag) {
+  const size_t total = (size_t)N * K / 16;
+  const int kblocks = K / 64;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t blk = i / 64;
+    const int within = (int)(i % 64);
+    const int mb = (int)(blk / kblocks), kb = (int)(blk % kblocks);
+    const int g = within / 8, half = (within / 4) & 1, j = within & 3;
+    const int r = 16 * mb + g + 8 * half;
+    const uint8_t v = sf[(size_t)src_row(r, N, gate_up) * (K / 16) + 4 * kb + j];
+    check_sf(v, flag);
+    out[i] = v;
+  }
+}
+
+moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
+                                uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s) {
+  prepare_w4a16_data_kernel<<<1024, 256, 0, s>>>(codes, N, K, gate_up, out_data);
+  count_launches(1);
+  prepare_w4a16_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out_sf, flag);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// W4A4 tile layout: not built yet; the launcher reports it as unsupported.
+size_t prepare_w4a4_sf_bytes(int N, int K) { return (size_t)N * K / 16; }
+
+moe_status launch_prepare_w4a4(const uint8_t*, const uint8_t*, int, int, int, uint8_t*, uint8_t*, int*,
+                               cudaStream_t) {
+  return MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace moe

@@ -1,0 +1,215 @@
+// BF16 -> NVFP4 quantisation, standalone SwiGLU and the deterministic
+// combine.
+//
+// Quantisation: "vLLM on the NVIDIA DGX Spark: A Complete Technical Guide",
+// section 4.3 (BF16 input quantised to FP4 inside the fused kernel) and
+// section 6.1 (e2m1 elements, one E4M3 scale per 16 along K, one fp32
+// global scale); the 448 clamp of the block scale is named in "Serving
+// Solar Open 2 on DGX Spark", "Supporting real NVFP4 checkpoints"; the
+// global scale is the quant-convention (448*6)/amax ("GLM-5.3-Flash-NVFP4 #4"
+// discussion, follow-up on the MoE fault).
+// Combine: same guide, section 7.1 ([Combine]) and section 4.3 (top-k weight
+// reduction).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// amax = max |x| over n bf16 values. 16-byte loads, grid-stride; one atomic
+// per block on the float's bit pattern (exact and order-independent).
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x, size_t n,
+                                                        float* __restrict__ amax) {
+  uint32_t m = 0;  // running max of |x| as a bf16 bit pattern (monotonic in magnitude)
+  const size_t nvec = n / 8;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = ldg_stream(xv + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = max(m, w[j] & 0x7fffu);
+      m = max(m, (w[j] >> 16) & 0x7fffu);
+    }
+  }
+  for (size_t i = nvec * 8 + blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    m = max(m, (uint32_t)(x[i] & 0x7fffu));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = max(m, red[i]);
+    // NaN bit patterns (> 0x7f80) are outside the contract; keep them out of
+    // the max so the scale stays finite.
+    if (m > 0x7f80u) m = 0x7f80u;
+    atomic_max_nonneg(amax, __uint_as_float(m << 16));
+  }
+}
+
+moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s) {
+  if (n == 0) return MOE_OK;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  size_t want = (n / 8 + 255) / 256;
+  size_t cap = (size_t)sms * 8;
+  int blocks = (int)(want == 0 ? 1 : (want < cap ? want : cap));
+  amax_bf16_kernel<<<blocks, 256, 0, s>>>(x, n, amax);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+// e2m1 code of |y| (0..7), round to nearest with ties to the even code,
+// saturating at 6: the thresholds are the midpoints of the grid
+// {0, .5, 1, 1.5, 2, 3, 4, 6}; at a midpoint the even code wins, so the
+// comparison is strict where the lower neighbour is even and non-strict where
+// the upper one is.
+__device__ __forceinline__ uint32_t e2m1_code_mag(float a) {
+  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+}
+
+// E4M3 (fn) encoding of a non-negative fp32, nearest-even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_encode_sat(float s) {
+  uint16_t r;
+  // both halves get s, so the byte order of the packed result does not matter
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(s), "f"(s));
+  return r & 0xffu;
+}
+
+__device__ __forceinline__ float e4m3_decode(uint32_t code) {
+  const uint32_t h2 = cvt_e4m3x2_f16x2((code & 0xffu) * 0x101u);  // same byte in both halves
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+// One thread per 16-element block: 32 bytes of bf16 in, 8 bytes of codes and
+// 1 scale byte out.
+__global__ void __launch_bounds__(256) quantize_bf16_kernel(const uint16_t* __restrict__ x, int rows, int K,
+                                                            const float* __restrict__ amax_p,
+                                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                            float* __restrict__ gs_out) {
+  const float amax = *amax_p;
+  const float gs = amax > 0.0f ? 2688.0f / amax : 1.0f;
+  const size_t nblk = (size_t)rows * (K / 16);
+  const size_t b = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (b == 0 && gs_out != nullptr) *gs_out = gs;
+  if (b >= nblk) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + b * 16);
+  const uint4 v0 = ldg_stream(src), v1 = ldg_stream(src + 1);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float f[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+  float bmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
+  const float s = __fmul_rn(__fdiv_rn(bmax, 6.0f), gs);
+  const uint32_t code = e4m3_encode_sat(s);
+  const float sval = e4m3_decode(code);
+  uint32_t lo = 0, hi = 0;
+  if (sval > 0.0f) {
+    const float r = __fdiv_rn(gs, sval);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float y = __fmul_rn(f[j], r);
+      const uint32_t c = e2m1_code_mag(fabsf(y)) | (signbit(y) ? 8u : 0u);
+      if (j < 8) lo |= c << (4 * j);
+      else hi |= c << (4 * (j - 8));
+    }
+  }
+  *reinterpret_cast<uint2*>(q + b * 8) = make_uint2(lo, hi);
+  sf[b] = (uint8_t)code;
+}
+
+moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float* amax, uint8_t* q,
+                                uint8_t* sf, float* gs_out, cudaStream_t s) {
+  const size_t nblk = (size_t)rows * (K / 16);
+  const int blocks = (int)((nblk + 255) / 256);
+  quantize_bf16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(x, rows, K, amax, q, sf, gs_out);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// h = silu(gate) * up, gate in columns [0, I), up in [I, 2I).
+__global__ void swiglu_kernel(const float* __restrict__ gu, int rows, int I, uint16_t* __restrict__ h) {
+  const size_t n = (size_t)rows * I;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / I, c = i % I;
+    const float g = gu[r * 2 * I + c];
+    const float u = gu[r * 2 * I + I + c];
+    h[i] = float_to_bf16_bits(silu(g) * u);
+  }
+}
+
+moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStream_t s) {
+  const size_t n = (size_t)rows * I;
+  if (n == 0) return MOE_OK;
+  const size_t want = (n + 255) / 256;
+  const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+  swiglu_kernel<<<blocks, 256, 0, s>>>(gu, rows, I, h);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// out[t] = sum_j y[inv_perm[t*k + j]] (* topk_w[t, j]) + y[T*k + t], fp32 in
+// that fixed order, rounded once to bf16. One thread per 8 outputs (16-byte
+// loads and stores); a grid of (H/8/64) x T blocks of 64 threads.
+__global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict__ y,
+                                                     const int32_t* __restrict__ inv_perm,
+                                                     const float* __restrict__ topk_w, int shared, int T,
+                                                     int k, int H, uint16_t* __restrict__ out) {
+  const int t = blockIdx.y;
+  const int c8 = blockIdx.x * blockDim.x + threadIdx.x;  // chunk of 8 columns
+  if (c8 * 8 >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  const size_t P = (size_t)T * k;
+  for (int j = 0; j < k; ++j) {
+    const int row = __ldg(inv_perm + (size_t)t * k + j);
+    if (row < 0) continue;
+    const float wt = topk_w != nullptr ? __ldg(topk_w + (size_t)t * k + j) : 1.0f;
+    const uint4 v = ldg_stream(y + (size_t)row * H + (size_t)c8 * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __uint_as_float(w[i] << 16) * wt;
+      acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u) * wt;
+    }
+  }
+  if (shared) {
+    const uint4 v = ldg_stream(y + (P + t) * H + (size_t)c8 * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __uint_as_float(w[i] << 16);
+      acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = (uint32_t)float_to_bf16_bits(acc[2 * i]) | ((uint32_t)float_to_bf16_bits(acc[2 * i + 1]) << 16);
+  *reinterpret_cast<uint4*>(out + (size_t)t * H + (size_t)c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
+                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  const int chunks = H / 8;
+  dim3 grid((chunks + 63) / 64, T);
+  combine_kernel<<<grid, 64, 0, s>>>(y, inv_perm, topk_w, y_shared_rows, T, k, H, out);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -1,0 +1,367 @@
+// Router top-k and the stable expert permutation.
+//
+// Router: "Serving Solar Open 2 on DGX Spark", "Solar Open 2 in brief"
+// (320 routed experts + 1 shared, top-8); "vLLM on the NVIDIA DGX Spark: A
+// Complete Technical Guide", section 7.1 ([Router] stage).
+// Permutation: same guide, section 4.3 (token dispatch) and section 7.1
+// ([Permute-Experts-Unpermute]).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// One warp per token. Lane l holds logits l, l+32, l+64, ... in registers.
+// k rounds of a warp-wide argmax pick the experts by rank: a larger logit
+// wins, equal logits go to the lower expert index. The weights are
+// exp(l_j - l_max) / sum over the chosen j (fp32), i.e. the softmax
+// probabilities renormalised over the top k.
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                         int k, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (token >= T) return;
+  const float* row = logits + (size_t)token * E;
+  float v[PER_LANE];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(row + e) : 0.0f;
+    if (e >= E) taken |= 1u << i;
+  }
+  float my_val = 0.0f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      if (!(taken & (1u << i))) {
+        // ascending index within a lane: strict '>' keeps the lower index on ties
+        if (bi == 0x7fffffff || v[i] > bv) {
+          bv = v[i];
+          bi = lane + 32 * i;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      const bool other_valid = oi != 0x7fffffff;
+      const bool mine_valid = bi != 0x7fffffff;
+      if (other_valid && (!mine_valid || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi == 0x7fffffff) bi = 0;  // only reachable with NaN logits (outside the contract)
+    if ((bi & 31) == lane && bi < E) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_val = bv;
+      my_id = bi;
+    }
+  }
+  const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
+  float ex = lane < k ? expf(my_val - vmax) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids[(size_t)token * k + lane] = my_id;
+    w[(size_t)token * k + lane] = ex / sum;
+  }
+}
+
+moe_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                             cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  const int threads = 256;
+  const int blocks = (int)(((size_t)T * 32 + threads - 1) / threads);
+  const int per = (E + 31) / 32;
+#define MOE_ROUTE_CASE(P)                                                             \
+  if (per <= P) {                                                                     \
+    route_topk_kernel<P><<<blocks, threads, 0, s>>>(logits, T, E, k, ids, w);         \
+    count_launches(1);                                                                \
+    return cuda_ok(cudaGetLastError());                                               \
+  }
+  MOE_ROUTE_CASE(1)
+  MOE_ROUTE_CASE(2)
+  MOE_ROUTE_CASE(4)
+  MOE_ROUTE_CASE(8)
+  MOE_ROUTE_CASE(16)
+  MOE_ROUTE_CASE(32)
+#undef MOE_ROUTE_CASE
+  return MOE_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// Stable counting sort of the P = T*k pairs by expert.
+//
+// Phase 1 (count): per chunk of pairs, a shared-memory histogram.
+// Phase 2 (scan):  offsets[e] = sum of counts below e; the base of chunk b
+//                  inside expert e's group = offsets[e] + counts of e in
+//                  chunks before b.
+// Phase 3 (scatter): per chunk, one warp walks its pairs in order, 32 at a
+//                  time; lanes holding the same expert (match_any) take
+//                  consecutive slots in lane order, so a pair's slot grows
+//                  with its index p (stability).
+// Small problems run all three phases in one CTA (one launch); large ones use
+// three launches with one CTA per chunk.
+
+constexpr int kPermChunk = 4096;  // pairs per chunk in the multi-CTA path
+
+__device__ __forceinline__ void scatter_warp(const int32_t* __restrict__ ids, int p0, int p1, int E,
+                                             int* cursor /* smem [E] */, int32_t* perm,
+                                             int32_t* inv_perm, int* status) {
+  const int lane = threadIdx.x & 31;
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    const bool in = p < p1;
+    int e = in ? __ldg(ids + p) : -1;
+    const bool valid = in && e >= 0 && e < E;
+    if (in && !valid) set_status(status, MOE_ERR_DEVICE);
+    const int key = valid ? e : -1 - lane;  // invalid lanes never match each other
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const unsigned lt = (1u << lane) - 1u;
+    const int rank = __popc(peers & lt);
+    int slot = 0;
+    if (valid) slot = cursor[e] + rank;
+    __syncwarp();
+    if (valid) {
+      perm[slot] = p;
+      inv_perm[p] = slot;
+      // highest lane of the peer group advances the cursor
+      if ((peers >> lane) == 1u) cursor[e] += __popc(peers);
+    } else if (in) {
+      inv_perm[p] = -1;
+    }
+    __syncwarp();
+  }
+}
+
+// Extra per-row outputs for the fused forward: the A-row (token) of each
+// sorted row and its routing weight; shared rows follow the routed ones.
+struct RowInfoOut {
+  int32_t* row_token;    // [P + T] or nullptr
+  float* row_weight;     // [P + T] or nullptr
+  const float* topk_w;   // [P]
+  int k, T;
+  int32_t* gofs;         // [E+2] or nullptr: offsets[0..E-1], then P, then P + T
+};
+
+__device__ void write_row_info(const RowInfoOut& ri, const int32_t* perm, int P) {
+  if (ri.row_token == nullptr) return;
+  for (int r = threadIdx.x; r < P + ri.T; r += blockDim.x) {
+    if (r < P) {
+      const int p = perm[r];
+      const bool ok = p >= 0 && p < P;
+      ri.row_token[r] = ok ? p / ri.k : 0;
+      ri.row_weight[r] = ok ? ri.topk_w[p] : 0.0f;
+    } else {
+      ri.row_token[r] = r - P;
+      ri.row_weight[r] = 1.0f;
+    }
+  }
+}
+
+// Block-wide exclusive scan of n <= blockDim.x * 4 ints in shared memory.
+__device__ void block_exclusive_scan(int* data, int n, int* tmp /* smem [32] */) {
+  const int tid = threadIdx.x;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int idx = tid * per + i;
+    if (idx < n) local += data[idx];
+  }
+  int incl = local;
+  const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) tmp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = (blockDim.x + 31) / 32;
+    int v = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += o;
+    }
+    if (lane < nw) tmp[lane] = v;
+  }
+  __syncthreads();
+  int run = incl - local + (wid > 0 ? tmp[wid - 1] : 0);
+  for (int i = 0; i < per; ++i) {
+    const int idx = tid * per + i;
+    if (idx < n) {
+      const int d = data[idx];
+      data[idx] = run;
+      run += d;
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __restrict__ ids, int P,
+                                                              int E, int32_t* counts, int32_t* offsets,
+                                                              int32_t* perm, int32_t* inv_perm,
+                                                              int* status, RowInfoOut ri) {
+  extern __shared__ int smem[];
+  int* cnt = smem;            // [E]
+  int* cursor = smem + E;     // [E]
+  int* tmp = smem + 2 * E;    // [32]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) perm[p] = -1;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = __ldg(ids + p);
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    counts[e] = cnt[e];
+    cursor[e] = cnt[e];
+  }
+  __syncthreads();
+  block_exclusive_scan(cursor, E, tmp);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    offsets[e] = cursor[e];
+    if (ri.gofs) ri.gofs[e] = cursor[e];
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = cursor[E - 1] + cnt[E - 1];
+    if (ri.gofs) {
+      ri.gofs[E] = P;
+      ri.gofs[E + 1] = P + ri.T;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) scatter_warp(ids, 0, P, E, cursor, perm, inv_perm, status);
+  __syncthreads();
+  __threadfence_block();
+  write_row_info(ri, perm, P);
+}
+
+__global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                             int32_t* chunk_hist /* [nchunks][E] */,
+                                                             int32_t* perm) {
+  extern __shared__ int cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kPermChunk;
+  const int p1 = min(P, p0 + kPermChunk);
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = __ldg(ids + p);
+    perm[p] = -1;
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* chunk_hist, int nchunks, int E, int P,
+                                                            int32_t* counts, int32_t* offsets,
+                                                            int32_t* gofs, int T) {
+  extern __shared__ int smem[];
+  int* tot = smem;         // [E]
+  int* tmp = smem + E;     // [32]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nchunks; ++b) {
+      const int c = chunk_hist[(size_t)b * E + e];
+      chunk_hist[(size_t)b * E + e] = run;  // becomes the base within the group
+      run += c;
+    }
+    tot[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  int last = 0;
+  if (threadIdx.x == 0) last = tot[E - 1];
+  block_exclusive_scan(tot, E, tmp);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    offsets[e] = tot[e];
+    if (gofs) gofs[e] = tot[e];
+    for (int b = 0; b < nchunks; ++b) chunk_hist[(size_t)b * E + e] += tot[e];
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = tot[E - 1] + last;
+    if (gofs) {
+      gofs[E] = P;
+      gofs[E + 1] = P + T;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                               const int32_t* chunk_base, int32_t* perm,
+                                                               int32_t* inv_perm, int* status) {
+  extern __shared__ int cursor[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cursor[e] = chunk_base[(size_t)blockIdx.x * E + e];
+  __syncthreads();
+  const int p0 = blockIdx.x * kPermChunk;
+  const int p1 = min(P, p0 + kPermChunk);
+  if (threadIdx.x < 32) scatter_warp(ids, p0, p1, E, cursor, perm, inv_perm, status);
+}
+
+__global__ void row_info_kernel(const int32_t* perm, int P, RowInfoOut ri) {
+  // grid-stride version of write_row_info
+  const int n = P + ri.T;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
+    if (r < P) {
+      const int p = perm[r];
+      const bool ok = p >= 0 && p < P;
+      ri.row_token[r] = ok ? p / ri.k : 0;
+      ri.row_weight[r] = ok ? ri.topk_w[p] : 0.0f;
+    } else {
+      ri.row_token[r] = r - P;
+      ri.row_weight[r] = 1.0f;
+    }
+  }
+}
+
+size_t permute_scratch_bytes(int T, int k, int E) {
+  const size_t P = (size_t)T * k;
+  if (P <= (size_t)kPermSingleMax) return 0;
+  const size_t nchunks = (P + kPermChunk - 1) / kPermChunk;
+  return align_up(nchunks * (size_t)E * sizeof(int32_t));
+}
+
+moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* inv_perm, int* status, void* scratch,
+                          int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
+                          cudaStream_t s) {
+  const int P = T * k;
+  RowInfoOut ri{row_token, row_weight, topk_w, k, T, gofs};
+  if (P <= kPermSingleMax) {
+    const size_t smem = (2 * (size_t)E + 32) * sizeof(int);
+    permute_single_kernel<<<1, 1024, smem, s>>>(ids, P, E, counts, offsets, perm, inv_perm, status, ri);
+    count_launches(1);
+    return cuda_ok(cudaGetLastError());
+  }
+  const int nchunks = (P + kPermChunk - 1) / kPermChunk;
+  int32_t* hist = static_cast<int32_t*>(scratch);
+  permute_count_kernel<<<nchunks, 1024, (size_t)E * sizeof(int), s>>>(ids, P, E, hist, perm);
+  count_launches(1);
+  permute_scan_kernel<<<1, 1024, ((size_t)E + 32) * sizeof(int), s>>>(hist, nchunks, E, P, counts, offsets,
+                                                                      gofs, T);
+  count_launches(1);
+  permute_scatter_kernel<<<nchunks, 32, (size_t)E * sizeof(int), s>>>(ids, P, E, hist, perm, inv_perm,
+                                                                      status);
+  count_launches(1);
+  if (row_token != nullptr) {
+    const int n = P + T;
+    row_info_kernel<<<(n + 255) / 256, 256, 0, s>>>(perm, P, ri);
+    count_launches(1);
+  }
+  return cuda_ok(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -1,0 +1,100 @@
+"""Device-side setup of one MoE layer through the C ABI.
+
+``Nvfp4MoeLayer`` quantises bf16 weight matrices to NVFP4 with the
+library's own quantiser (``moe_nvfp4_quantize``), converts them into the
+kernels' tile layout (``moe_nvfp4_prepare_weights``), keeps them resident in
+device memory and runs the fused forward (``moe_nvfp4_forward``). torch is
+used only to allocate device memory; every step of the layer runs in the
+CUDA library.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+def _empty_bytes(n, device):
+    # 256-byte aligned (the caching allocator aligns to 512)
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def quantize_bf16(x, device="cuda"):
+    """bf16 ``[rows, K]`` on the device -> (packed codes, E4M3 scales, gs tensor)."""
+    rows, K = x.shape
+    q = torch.empty(rows, K // 2, dtype=torch.uint8, device=device)
+    sf = torch.empty(rows, K // 16, dtype=torch.uint8, device=device)
+    gs = torch.empty(1, dtype=torch.float32, device=device)
+    ws = _empty_bytes(B.moe_quantize_workspace_size(), device)
+    B.moe_nvfp4_quantize(x, rows, K, q, sf, gs, ws)
+    return q, sf, gs
+
+
+class Nvfp4MoeLayer:
+    """NVFP4 weights of E routed experts (+ optional shared expert) on one GPU."""
+
+    def __init__(self, T, H, I, E, k, mode=B.MOE_W4A16, I_shared=None, shared=True, device="cuda"):
+        self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.I_shared = I if I_shared is None else I_shared
+        self.mode = mode
+        self.shared = shared
+        self.device = device
+        self.s13 = B.moe_prepare_size(2 * I, H, mode, 1)
+        self.s2 = B.moe_prepare_size(H, I, mode, 0)
+        self.w13 = _empty_bytes(E * self.s13, device)
+        self.w2 = _empty_bytes(E * self.s2, device)
+        if shared:
+            self.w13_s = _empty_bytes(B.moe_prepare_size(2 * self.I_shared, H, mode, 1), device)
+            self.w2_s = _empty_bytes(B.moe_prepare_size(H, self.I_shared, mode, 0), device)
+        else:
+            self.w13_s = self.w2_s = None
+        self.gs = {}  # (expert, matrix) -> quant-convention global scale (float)
+
+    def _slot(self, expert, which):
+        if expert == self.E:
+            return self.w13_s if which == 13 else self.w2_s
+        if which == 13:
+            return self.w13[expert * self.s13:(expert + 1) * self.s13]
+        return self.w2[expert * self.s2:(expert + 1) * self.s2]
+
+    def set_expert(self, expert, gate, up, down):
+        """bf16 gate ``[I, H]``, up ``[I, H]``, down ``[H, I]`` (any device); expert E = shared."""
+        dev = self.device
+        gate, up, down = (t.to(dev, torch.bfloat16).contiguous() for t in (gate, up, down))
+        qg, sg, gg = quantize_bf16(gate, dev)
+        qu, su, gu = quantize_bf16(up, dev)
+        qd, sd, gd = quantize_bf16(down, dev)
+        gsv = torch.cat([gg, gu, gd]).cpu().tolist()
+        self.gs[(expert, "gate")], self.gs[(expert, "up")], self.gs[(expert, "down")] = gsv
+        inter = gate.shape[0]
+        codes13 = torch.cat([qg, qu])
+        sf13 = torch.cat([sg, su])
+        B.moe_nvfp4_prepare_weights(codes13, sf13, gsv[:2], 2 * inter, self.H, self.mode, 1,
+                                    self._slot(expert, 13))
+        B.moe_nvfp4_prepare_weights(qd, sd, gsv[2:], self.H, inter, self.mode, 0, self._slot(expert, 2))
+        return (qg, sg, gsv[0]), (qu, su, gsv[1]), (qd, sd, gsv[2])
+
+    def desc(self, T=None):
+        d = B.MoeLayerDesc()
+        d.T = self.T if T is None else T
+        d.H, d.I, d.I_shared, d.E, d.k = self.H, self.I, self.I_shared, self.E, self.k
+        d.mode = self.mode
+        d.w13, d.w2 = self.w13.data_ptr(), self.w2.data_ptr()
+        d.w13_shared = self.w13_s.data_ptr() if self.shared else None
+        d.w2_shared = self.w2_s.data_ptr() if self.shared else None
+        return d
+
+    def workspace(self, T=None):
+        # the first 256 bytes hold the device status word and must start at zero
+        ws = _empty_bytes(B.moe_workspace_size(self.desc(T)), self.device)
+        ws[:256].zero_()
+        return ws
+
+    def forward(self, x, logits, out=None, topk_ids=None, ws=None, stream=None):
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        if ws is None:
+            ws = self.workspace(T)
+        B.moe_nvfp4_forward(self.desc(T), x, logits, out, topk_ids, ws, stream)
+        return out

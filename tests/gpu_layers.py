@@ -1,0 +1,47 @@
+"""Builders shared by the GPU parity tests: one seeded layer, prepared once on
+the device through the C ABI, and the oracle's view of the same weights."""
+import functools
+
+import numpy as np
+import torch
+
+import synthetic_inputs as si
+from oracle import moe as omoe
+from oracle import nvfp4 as onv
+
+
+@functools.lru_cache(maxsize=4)
+def device_layer(name, T=None):
+    """(cfg, Nvfp4MoeLayer) with every expert of workload ``name`` prepared."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from nvfp4_mixture_experts_moe_gb300 import Nvfp4MoeLayer, MOE_W4A16, MOE_W4A4
+    cfg = si.CONFIGS[name]
+    if T is not None:
+        cfg = cfg.with_tokens(T)
+    mode = MOE_W4A4 if cfg.mode == "w4a4" else MOE_W4A16
+    layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mode=mode, I_shared=cfg.I_s, device="cuda")
+    chunk = 16
+    for e0 in range(0, cfg.E + 1, chunk):
+        W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + chunk))))
+        for e, (g, u, d) in W.items():
+            layer.set_expert(e, g, u, d)
+    torch.cuda.synchronize()
+    return cfg, layer
+
+
+class OracleWeights:
+    """Lazily quantised (by the oracle) experts of a workload, cached."""
+
+    def __init__(self, cfg):
+        self.cfg = cfg
+        self.cache = {}
+
+    def __call__(self, e):
+        if e not in self.cache:
+            mats = [si.make_expert_weight(self.cfg, e, m) for m in ("gate", "up", "down")]
+            self.cache[e] = tuple(omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats)
+        return self.cache[e]
+
+    def all(self):
+        return [self(e) for e in range(self.cfg.E)], self(self.cfg.E)

@@ -1,0 +1,74 @@
+"""The C ABI library builds, loads and exports every declared symbol; host-side
+argument validation answers before any device work (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from nvfp4_mixture_experts_moe_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return B.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(moe_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "moe_nvfp4_forward" in names and len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert B.status_string(0) == "MOE_OK"
+    assert B.status_string(6) == "MOE_ERR_DEVICE"
+
+
+def test_host_validation_before_device_work(lib):
+    L = lib
+    assert L.moe_route_topk(None, 4, 0, 1, None, None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_route_topk(None, 4, 8, 9, None, None, None) == B.MOE_ERR_UNSUPPORTED
+    assert L.moe_route_topk(None, 4, 2048, 2, None, None, None) == B.MOE_ERR_UNSUPPORTED
+    assert L.moe_route_topk(None, 0, 8, 2, None, None, None) == B.MOE_OK  # empty batch: no-op
+    assert L.moe_permute(256, 4, 2, 8, 256, 256, 256, 256, None, 0, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_permute(256, 4, 2, 8, 256, 256, 256, 256, 256 * 3, 0, None) == B.MOE_ERR_WORKSPACE
+    # a zero or non-finite global scale is refused (it would silently zero an expert)
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        gs = (ctypes.c_float * 1)(bad)
+        assert L.moe_nvfp4_prepare_weights(256, 256, ctypes.cast(gs, ctypes.c_void_p), 128, 64, 0, 0, 256,
+                                           None) == B.MOE_ERR_INVALID_ARG
+    gs = (ctypes.c_float * 1)(1.0)
+    assert L.moe_nvfp4_prepare_weights(256, 256, ctypes.cast(gs, ctypes.c_void_p), 100, 64, 0, 0, 256,
+                                       None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_nvfp4_quantize(256, 4, 24, 256, 256, 256, 256, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(256, 256, None, 1, 4, 2, 12, 256, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_sizes(lib):
+    assert B.moe_prepare_size(3072, 4096, 0, 1) == 256 + 3072 * 4096 * 9 // 16
+    d = B.MoeLayerDesc(T=8, H=4096, I=1536, I_shared=1536, E=320, k=8, mode=0, w13=256, w2=256,
+                       w13_shared=256, w2_shared=256)
+    n8 = B.moe_workspace_size(d)
+    d.T = 4096
+    n4096 = B.moe_workspace_size(d)
+    assert 0 < n8 < n4096
+    d.H = 100
+    assert B.moe_workspace_size(d) == 0

@@ -1,0 +1,183 @@
+"""CUDA path against the CPU oracle, through the C ABI, on seeded inputs.
+
+Integer results (routing ids, counts, offsets, permutation, NVFP4 codes and
+scales, global scales) must match bit for bit; float results within the
+bars of tests/tolerance.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic_inputs as si
+from oracle import moe as omoe
+from oracle import nvfp4 as onv
+from tests.gpu_layers import OracleWeights, device_layer
+from tests.tolerance import TOPK_W_ABS, check_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def B():
+    from nvfp4_mixture_experts_moe_gb300 import binding
+    return binding
+
+
+def route_gpu(logits, k):
+    T, E = logits.shape
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    B().moe_route_topk(logits.cuda(), T, E, k, ids, w)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,E,k,kind", [
+    (16, 8, 2, "normal"), (8, 320, 8, "normal"), (4096, 320, 8, "normal"), (2048, 320, 8, "zipf"),
+    (16384, 256, 8, "normal"), (5, 1024, 32, "normal"), (3, 7, 7, "normal"), (33, 40, 1, "ties")])
+def test_route_topk(T, E, k, kind):
+    g = torch.Generator().manual_seed(T * 31 + E)
+    if kind == "ties":
+        logits = torch.randint(-2, 3, (T, E), generator=g).float()
+        logits[0, :] = 0.0
+        logits[0, ::2] = -0.0
+    else:
+        cfg = si.LayerConfig("r", T=T, H=16, I=16, I_s=16, E=E, k=k, logits=kind)
+        logits = si.make_logits(cfg)
+    ids, w = route_gpu(logits, k)
+    rids, rw = omoe.route(logits.numpy(), k)
+    assert (ids == rids).all()
+    assert np.abs(w - rw).max() <= TOPK_W_ABS
+
+
+@pytest.mark.parametrize("T,k,E", [(16, 2, 8), (8, 8, 320), (4096, 8, 320), (2048, 8, 320),
+                                   (16384, 8, 256), (1, 1, 1), (7, 3, 1024), (0, 8, 320)])
+def test_permute(T, k, E):
+    g = torch.Generator().manual_seed(T + 7 * E)
+    if E == 320 and T == 2048:
+        cfg = si.LayerConfig("z", T=T, H=16, I=16, I_s=16, E=E, k=k, logits="zipf")
+        ids_cpu = torch.from_numpy(omoe.route(si.make_logits(cfg).numpy(), k)[0])
+    else:
+        ids_cpu = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    P = T * k
+    ids = ids_cpu.cuda()
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(max(P, 1), dtype=torch.int32, device="cuda")
+    inv = torch.empty(max(P, 1), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(B().moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
+    B().moe_permute(ids, T, k, E, counts, offsets, perm, inv, ws)
+    assert B().moe_get_device_status(ws) == 0
+    rc, ro, rp, ri = omoe.permute(ids_cpu.numpy(), E)
+    assert (counts.cpu().numpy() == rc).all()
+    assert (offsets.cpu().numpy() == ro).all()
+    assert (perm.cpu().numpy()[:P] == rp).all()
+    assert (inv.cpu().numpy()[:P] == ri).all()
+
+
+def test_permute_flags_out_of_range_ids():
+    ids = torch.tensor([[0, 1], [9, 2]], dtype=torch.int32, device="cuda")
+    counts = torch.empty(4, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(5, dtype=torch.int32, device="cuda")
+    perm = torch.empty(4, dtype=torch.int32, device="cuda")
+    inv = torch.empty(4, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(B().moe_permute_workspace_size(2, 2, 4), dtype=torch.uint8, device="cuda")
+    B().moe_permute(ids, 2, 2, 4, counts, offsets, perm, inv, ws)
+    assert B().moe_get_device_status(ws) == B().MOE_ERR_DEVICE
+    assert B().moe_get_device_status(ws) == 0      # cleared by the read
+    assert counts.cpu().tolist() == [1, 1, 1, 0]
+    assert inv.cpu().tolist()[2] == -1
+
+
+def quant_gpu(x_bf16):
+    from nvfp4_mixture_experts_moe_gb300 import quantize_bf16
+    q, sf, gs = quantize_bf16(x_bf16.cuda())
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), sf.cpu().numpy(), np.float32(gs.item())
+
+
+@pytest.mark.parametrize("rows,K,scale,outliers", [(16, 256, 1.0, False), (64, 4096, 0.02, False),
+                                                   (257, 7168, 1.0, True), (3, 16, 1e-3, False)])
+def test_quantize_bit_exact(rows, K, scale, outliers):
+    g = torch.Generator().manual_seed(rows * K)
+    x = torch.randn(rows, K, generator=g) * scale
+    if outliers:
+        m = torch.rand(rows, K, generator=g) < 0.001
+        x = torch.where(m, x * 20, x)
+    x = x.to(torch.bfloat16)
+    q, sf, gs = quant_gpu(x)
+    rq, rsf, rgs = onv.quantize(x.float().numpy())
+    assert gs == rgs
+    assert (sf == rsf).all()
+    assert (q == onv.pack(rq)).all()
+
+
+def test_quantize_ties_and_edges():
+    # values constructed to land exactly on e2m1 and e4m3 rounding midpoints
+    vals = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, -0.25, -5.0, 0.0, -0.0, 4.0, 3.0, 1.0, 0.5]
+    x = torch.tensor([vals, [v * 0.37 for v in vals], [1e-30] * 16, [0.0] * 16], dtype=torch.float32)
+    x[0, 7] = 6.0  # block amax 6 -> gs/sf chosen by the quantiser
+    x = x.to(torch.bfloat16)
+    q, sf, gs = quant_gpu(x)
+    rq, rsf, rgs = onv.quantize(x.float().numpy())
+    assert gs == rgs and (sf == rsf).all() and (q == onv.pack(rq)).all()
+    z = torch.zeros(2, 32, dtype=torch.bfloat16)
+    q, sf, gs = quant_gpu(z)
+    assert gs == 1.0 and (q == 0).all() and (sf == 0).all()
+
+
+def run_forward(name, T=None):
+    cfg, layer = device_layer(name, T)
+    x = si.make_x(cfg)
+    logits = si.make_logits(cfg)
+    ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device="cuda")
+    ws = layer.workspace()
+    out = layer.forward(x.cuda(), logits.cuda(), topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    from nvfp4_mixture_experts_moe_gb300 import binding
+    assert binding.moe_get_device_status(ws) == 0
+    return cfg, layer, x, logits, out.float().cpu().numpy(), ids.cpu().numpy()
+
+
+def test_forward_tiny_full_check():
+    cfg, layer, x, logits, out, ids = run_forward("tiny")
+    ow = OracleWeights(cfg)
+    experts, shared = ow.all()
+    ref, parts = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k, return_parts=True)
+    assert (ids == parts["ids"]).all()
+    check_outputs(out, ref, what="tiny")
+
+
+def test_forward_tiny_is_deterministic():
+    cfg, layer = device_layer("tiny")
+    x = si.make_x(cfg).cuda()
+    logits = si.make_logits(cfg).cuda()
+    outs = [layer.forward(x, logits).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_forward_decode_full_check():
+    cfg, layer, x, logits, out, ids = run_forward("decode")
+    ow = OracleWeights(cfg)
+    rids, rw = omoe.route(logits.numpy(), cfg.k)
+    assert (ids == rids).all()
+    ref = omoe.token_outputs_w4a16(x.float().numpy(), rids, rw, ow, ow(cfg.E))
+    check_outputs(out, ref, what="decode")
+
+
+@pytest.mark.parametrize("name,tokens", [("prefill", [0, 1, 2047, 4095]), ("skewed", [0, 777, 2047])])
+def test_forward_large_sampled_tokens(name, tokens):
+    cfg, layer, x, logits, out, ids = run_forward(name)
+    rids, rw = omoe.route(logits.numpy(), cfg.k)
+    assert (ids == rids).all()
+    ow = OracleWeights(cfg)
+    ref = omoe.token_outputs_w4a16(x.float().numpy()[tokens], rids[tokens], rw[tokens], ow, ow(cfg.E))
+    check_outputs(out[tokens], ref, what=name)
+    # every token: finite and of the oracle's overall magnitude
+    assert np.isfinite(out).all()
