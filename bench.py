@@ -273,6 +273,10 @@ def run_ours(args):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(B.MOE_STAGE_COUNT)] for _ in range(K)]
+    for row in ev:  # torch creates the underlying CUDA events on first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(dev)
     bus = getattr(props, "pci_bus_id", None)
     sampler = ClockSampler(bus if isinstance(bus, str) else None)

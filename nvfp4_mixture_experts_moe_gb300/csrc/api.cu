@@ -138,6 +138,7 @@ static moe_status validate_layer(const moe_layer_desc* L) {
   if (L->mode != MOE_W4A16 && L->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
   if (L->E > 1024 || L->k > 32 || L->k > L->E) return MOE_ERR_UNSUPPORTED;
   if (L->H % 128 || L->I % 64) return MOE_ERR_UNSUPPORTED;
+  if (L->mode == MOE_W4A4 && (L->H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
   if (L->w13 == nullptr || L->w2 == nullptr) return MOE_ERR_INVALID_ARG;
   if ((L->w13_shared == nullptr) != (L->w2_shared == nullptr)) return MOE_ERR_INVALID_ARG;
   if (L->w13_shared && L->I_shared != L->I) return MOE_ERR_UNSUPPORTED;
@@ -277,9 +278,14 @@ size_t moe_gemm_workspace_size(int num_groups) {
   return sizeof(WsHeader);
 }
 
-static moe_status run_gemm(const GemmPlan& p, cudaStream_t s) {
-  if (p.mode == MOE_W4A16) return launch_gemm_small_w4a16(p, 0x7fffffff, s);
-  return MOE_ERR_UNSUPPORTED;
+// Small groups (decode-sized) stream weights through registers into
+// mma.sync; large groups go to the tcgen05 kernel. `max_group_rows` is an
+// upper bound on any group's rows (skips the tcgen05 launch when small).
+static moe_status run_gemm(const GemmPlan& p, long long max_group_rows, cudaStream_t s) {
+  if (p.mode == MOE_W4A4) return launch_gemm_tc_w4a4(p, s);
+  moe_status st = launch_gemm_small_w4a16(p, kSmallGroupRows, s);
+  if (st != MOE_OK || max_group_rows <= kSmallGroupRows) return st;
+  return launch_gemm_tc_w4a16(p, kSmallGroupRows, s);
 }
 
 moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -292,6 +298,7 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   if (a->gate_up && (a->N / 2) % 64) return MOE_ERR_UNSUPPORTED;
   if (!a->weights || !a->group_offsets || !a->a || !a->out) return MOE_ERR_INVALID_ARG;
   if (a->mode == MOE_W4A4 && (!a->a_sf || !a->a_gs)) return MOE_ERR_INVALID_ARG;
+  if (a->mode == MOE_W4A4 && a->K % 256) return MOE_ERR_UNSUPPORTED;
   if (!aligned(a->weights, kAlign) || (a->last_weights && !aligned(a->last_weights, kAlign)))
     return MOE_ERR_INVALID_ARG;
   if (!aligned(a->a, 16)) return MOE_ERR_INVALID_ARG;
@@ -317,7 +324,7 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   p.out_amax = a->out_amax;
   p.status = &static_cast<WsHeader*>(ws)->status;
   p.max_rows = 1 << 30;
-  return run_gemm(p, (cudaStream_t)stream);
+  return run_gemm(p, 1LL << 30, (cudaStream_t)stream);
 }
 
 moe_status moe_swiglu(const float* gu, int rows, int I, uint16_t* h, moe_stream_t stream) {
@@ -357,8 +364,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   if (ws_bytes < f.bytes) return MOE_ERR_WORKSPACE;
   st = check_device();
   if (st != MOE_OK) return st;
-  if (L->mode == MOE_W4A4) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
+  const bool fp4 = L->mode == MOE_W4A4;
   const int T = L->T, k = L->k, E = L->E, H = L->H, I = L->I;
   const int P = T * k;
   const bool has_shared = L->w13_shared != nullptr;
@@ -376,7 +383,15 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
                       f.row_token, f.row_weight, f.w, f.gofs, s);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
-  stage_mark(3, s);  // quantise x: W4A4 only
+  if (fp4) {  // dynamic per-tensor quantisation of x (W4A4)
+    st = cuda_ok(cudaMemsetAsync(&f.hdr->amax[0], 0, 2 * sizeof(float), s));
+    if (st != MOE_OK) return st;
+    st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s);
+    if (st != MOE_OK) return st;
+    st = launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq, f.xsf, f.xgs, s);
+    if (st != MOE_OK) return st;
+  }
+  stage_mark(3, s);
 
   const int G = E + (has_shared ? 1 : 0);
   GemmPlan g1;
@@ -390,15 +405,22 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.weight_stride = prep_size(2 * I, H, L->mode, 1);
   g1.last_weights = has_shared ? static_cast<const uint8_t*>(L->w13_shared) : nullptr;
   g1.group_offsets = f.gofs;
-  g1.a = x;
+  g1.a = fp4 ? static_cast<const void*>(f.xq) : static_cast<const void*>(x);
+  g1.a_sf = fp4 ? f.xsf : nullptr;
+  g1.a_gs = fp4 ? f.xgs : nullptr;
   g1.a_row_index = f.row_token;
   g1.out = f.h;
+  g1.out_amax = fp4 ? &f.hdr->amax[1] : nullptr;
   g1.status = &f.hdr->status;
   g1.max_rows = rows;
-  st = run_gemm(g1, s);
+  st = run_gemm(g1, T, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
-  stage_mark(5, s);  // quantise h: W4A4 only
+  if (fp4) {  // h -> NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue)
+    st = launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf, f.hgs, s);
+    if (st != MOE_OK) return st;
+  }
+  stage_mark(5, s);
 
   GemmPlan g2 = g1;
   g2.gate_up = 0;
@@ -407,11 +429,14 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g2.weights = static_cast<const uint8_t*>(L->w2);
   g2.weight_stride = prep_size(H, I, L->mode, 0);
   g2.last_weights = has_shared ? static_cast<const uint8_t*>(L->w2_shared) : nullptr;
-  g2.a = f.h;
+  g2.a = fp4 ? static_cast<const void*>(f.hq) : static_cast<const void*>(f.h);
+  g2.a_sf = fp4 ? f.hsf : nullptr;
+  g2.a_gs = fp4 ? f.hgs : nullptr;
+  g2.out_amax = nullptr;
   g2.a_row_index = nullptr;
   g2.row_scale = f.row_weight;
   g2.out = f.y;
-  st = run_gemm(g2, s);
+  st = run_gemm(g2, T, s);
   if (st != MOE_OK) return st;
   stage_mark(6, s);
   st = launch_combine(f.y, f.inv_perm, nullptr, has_shared ? 1 : 0, T, k, H, out, s);

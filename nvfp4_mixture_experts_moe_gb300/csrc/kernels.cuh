@@ -63,4 +63,14 @@ struct GemmPlan {
 // pass of up to 8 rows per weight tile. Handles groups with rows <= max_rows.
 moe_status launch_gemm_small_w4a16(const GemmPlan& p, int rows_limit, cudaStream_t s);
 
+// Large-group path: tcgen05 MMA with TMEM accumulators. Handles groups with
+// rows > rows_min.
+moe_status launch_gemm_tc_w4a16(const GemmPlan& p, int rows_min, cudaStream_t s);
+
+// W4A4: block-scaled FP4 tcgen05 kernel (every non-empty group).
+moe_status launch_gemm_tc_w4a4(const GemmPlan& p, cudaStream_t s);
+
+// Groups with at most this many rows take the small-group path.
+constexpr int kSmallGroupRows = 32;
+
 }  // namespace moe

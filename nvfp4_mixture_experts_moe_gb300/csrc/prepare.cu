@@ -69,12 +69,58 @@ moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, 
 
 namespace moe {
 
-// W4A4 tile layout: not built yet; the launcher reports it as unsupported.
+// W4A4 layout after the header: for every (128-row tile mt, 256-wide K stage
+// ks) the 16 KB shared-memory image the block-scaled MMA reads (row r of the
+// tile at r * 128 bytes, its 16-byte chunks XOR-swizzled by r % 8), then, in
+// a second region, for every (mt, ks) four 512-byte scale-factor atoms (one
+// per 64-wide K step; byte m0 * 16 + m1 * 4 + j holds scale j of row
+// 32 * m1 + m0).
 size_t prepare_w4a4_sf_bytes(int N, int K) { return (size_t)N * K / 16; }
 
-moe_status launch_prepare_w4a4(const uint8_t*, const uint8_t*, int, int, int, uint8_t*, uint8_t*, int*,
-                               cudaStream_t) {
-  return MOE_ERR_UNSUPPORTED;
+__global__ void prepare_w4a4_data_kernel(const uint8_t* __restrict__ codes, int N, int K, int gate_up,
+                                         uint8_t* __restrict__ out) {
+  const size_t total = (size_t)N * K / 2;
+  const int KS = K / 256;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t tile = i / 16384;
+    const int within = (int)(i % 16384);
+    const int mt = (int)(tile / KS), ks = (int)(tile % KS);
+    const int r = within / 128;
+    const int phys_chunk = (within % 128) / 16;
+    const int c = ((phys_chunk ^ (r & 7)) << 4) + (within % 16);  // logical byte column
+    const int o = mt * 128 + r;
+    out[i] = codes[(size_t)src_row(o, N, gate_up) * (K / 2) + ks * 128 + c];
+  }
+}
+
+__global__ void prepare_w4a4_sf_kernel(const uint8_t* __restrict__ sf, int N, int K, int gate_up,
+                                       uint8_t* __restrict__ out, int* flag) {
+  const size_t total = (size_t)N * K / 16;
+  const int KS = K / 256;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t tile = i / 2048;
+    const int within = (int)(i % 2048);
+    const int mt = (int)(tile / KS), ks = (int)(tile % KS);
+    const int kk = within / 512, a = within % 512;
+    const int m0 = a / 16, m1 = (a % 16) / 4, jj = a % 4;
+    const int r = 32 * m1 + m0;
+    const int o = mt * 128 + r;
+    const uint8_t v = sf[(size_t)src_row(o, N, gate_up) * (K / 16) + ks * 16 + kk * 4 + jj];
+    check_sf(v, flag);
+    out[i] = v;
+  }
+}
+
+moe_status launch_prepare_w4a4(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
+                               uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s) {
+  if (K % 256) return MOE_ERR_INVALID_ARG;
+  prepare_w4a4_data_kernel<<<1024, 256, 0, s>>>(codes, N, K, gate_up, out_data);
+  count_launches(1);
+  prepare_w4a4_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out_sf, flag);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
 }
 
 }  // namespace moe

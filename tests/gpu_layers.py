@@ -10,20 +10,21 @@ from oracle import moe as omoe
 from oracle import nvfp4 as onv
 
 
-@functools.lru_cache(maxsize=4)
+@functools.lru_cache(maxsize=3)
 def device_layer(name, T=None):
-    """(cfg, Nvfp4MoeLayer) with every expert of workload ``name`` prepared."""
+    """(cfg, Nvfp4MoeLayer) with every expert of workload ``name`` (a CONFIGS
+    key or a LayerConfig) prepared on the device."""
     import __graft_entry__
     __graft_entry__.build()
     from nvfp4_mixture_experts_moe_gb300 import Nvfp4MoeLayer, MOE_W4A16, MOE_W4A4
-    cfg = si.CONFIGS[name]
+    cfg = si.CONFIGS[name] if isinstance(name, str) else name
     if T is not None:
         cfg = cfg.with_tokens(T)
     mode = MOE_W4A4 if cfg.mode == "w4a4" else MOE_W4A16
     layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mode=mode, I_shared=cfg.I_s, device="cuda")
-    chunk = 16
+    chunk = 32
     for e0 in range(0, cfg.E + 1, chunk):
-        W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + chunk))))
+        W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + chunk))), threads=16)
         for e, (g, u, d) in W.items():
             layer.set_expert(e, g, u, d)
     torch.cuda.synchronize()
@@ -45,3 +46,15 @@ class OracleWeights:
 
     def all(self):
         return [self(e) for e in range(self.cfg.E)], self(self.cfg.E)
+
+    def prefetch(self, experts, threads=16):
+        from concurrent.futures import ThreadPoolExecutor
+        todo = [e for e in set(experts) if e not in self.cache]
+
+        def one(e):
+            mats = [si.make_expert_weight(self.cfg, e, m) for m in ("gate", "up", "down")]
+            return e, tuple(omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats)
+
+        with ThreadPoolExecutor(threads) as ex:
+            for e, w in ex.map(one, todo):
+                self.cache[e] = w

@@ -181,3 +181,65 @@ def test_forward_large_sampled_tokens(name, tokens):
     check_outputs(out[tokens], ref, what=name)
     # every token: finite and of the oracle's overall magnitude
     assert np.isfinite(out).all()
+
+
+def _prepared_groups(G, N, K, gate_up, seed):
+    """G prepared NVFP4 matrices (device) + the oracle's QuantWeights of the same bf16 values."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd, quantize_bf16
+    g = torch.Generator().manual_seed(seed)
+    size = Bd.moe_prepare_size(N, K, 0, gate_up)
+    buf = torch.empty(G * size, dtype=torch.uint8, device="cuda")
+    oracle_w = []
+    for i in range(G):
+        if gate_up:
+            mats = [(torch.randn(N // 2, K, generator=g) * 0.02).to(torch.bfloat16) for _ in range(2)]
+        else:
+            mats = [(torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)]
+        qs = [quantize_bf16(m.cuda()) for m in mats]
+        codes = torch.cat([q[0] for q in qs])
+        sfs = torch.cat([q[1] for q in qs])
+        gss = [q[2].item() for q in qs]
+        Bd.moe_nvfp4_prepare_weights(codes, sfs, gss, N, K, 0, gate_up, buf[i * size:(i + 1) * size])
+        oracle_w.append([omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats])
+    return buf, oracle_w
+
+
+@pytest.mark.parametrize("gate_up", [1, 0])
+def test_grouped_gemm_entry_tile_edges(gate_up):
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd
+    rows = [0, 40, 300, 7, 129, 33, 1, 256]
+    G = len(rows)
+    N, K = (256, 512) if gate_up else (384, 256)
+    buf, ow = _prepared_groups(G, N, K, gate_up, seed=11 + gate_up)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    total = int(off[-1])
+    g = torch.Generator().manual_seed(5)
+    src_rows = total + 3
+    a = torch.randn(src_rows, K, generator=g).to(torch.bfloat16)
+    idx = torch.randperm(src_rows, generator=g)[:total].to(torch.int32)
+    rs = torch.rand(total, generator=g) + 0.5
+    out_cols = N // 2 if gate_up else N
+    out = torch.full((total, out_cols), float("nan"), dtype=torch.bfloat16, device="cuda")
+    args = Bd.MoeGemmArgs(mode=0, gate_up=gate_up, num_groups=G, N=N, K=K)
+    offs_d = torch.from_numpy(off).cuda()
+    a_d, idx_d, rs_d = a.cuda(), idx.cuda(), rs.cuda()
+    args.weights = buf.data_ptr()
+    args.group_offsets = offs_d.data_ptr()
+    args.a = a_d.data_ptr()
+    args.a_row_index = idx_d.data_ptr()
+    args.row_scale = None if gate_up else rs_d.data_ptr()
+    args.out = out.data_ptr()
+    ws = torch.zeros(Bd.moe_gemm_workspace_size(G), dtype=torch.uint8, device="cuda")
+    Bd.moe_nvfp4_grouped_gemm(args, ws)
+    assert Bd.moe_get_device_status(ws) == 0
+    got = out.float().cpu().numpy()
+    xa = a.float().numpy()[idx.numpy()]
+    for gi in range(G):
+        r0, r1 = off[gi], off[gi + 1]
+        if r1 == r0:
+            continue
+        if gate_up:
+            ref = omoe.gate_up_swiglu(xa[r0:r1], ow[gi][0], ow[gi][1])
+        else:
+            ref = omoe.down_proj(xa[r0:r1], ow[gi][0]) * rs.numpy()[r0:r1, None]
+        check_outputs(got[r0:r1], ref, what=f"group {gi} ({r1 - r0} rows)")

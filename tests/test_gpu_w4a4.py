@@ -1,0 +1,154 @@
+"""W4A4 path (NVFP4 weights and activations, block-scaled FP4 MMA on tcgen05)
+against the CPU oracle through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic_inputs as si
+from oracle import moe as omoe
+from oracle import nvfp4 as onv
+from tests.gpu_layers import OracleWeights, device_layer
+from tests.tolerance import check_outputs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = si.LayerConfig("w4a4_small", T=64, H=512, I=256, I_s=256, E=8, k=2, mode="w4a4", outliers=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _run(cfg):
+    cfg, layer = device_layer(cfg)
+    x = si.make_x(cfg)
+    logits = si.make_logits(cfg)
+    ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device="cuda")
+    ws = layer.workspace()
+    out = layer.forward(x.cuda(), logits.cuda(), topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    from nvfp4_mixture_experts_moe_gb300 import binding
+    assert binding.moe_get_device_status(ws) == 0
+    return cfg, layer, x, logits, out.float().cpu().numpy(), ids.cpu().numpy()
+
+
+def test_w4a4_small_layer_full_check():
+    cfg, layer, x, logits, out, ids = _run(SMALL)
+    ow = OracleWeights(cfg)
+    experts, shared = ow.all()
+    ref, parts = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k, mode="w4a4",
+                            return_parts=True)
+    assert (ids == parts["ids"]).all()
+    check_outputs(out, ref, what="w4a4 small")
+
+
+def test_w4a4_small_deterministic():
+    cfg, layer = device_layer(SMALL)
+    x = si.make_x(cfg).cuda()
+    lg = si.make_logits(cfg).cuda()
+    o = [layer.forward(x, lg).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(o[0], t) for t in o[1:])
+
+
+def _fp4_groups(G, N, K, gate_up, seed):
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd, quantize_bf16
+    g = torch.Generator().manual_seed(seed)
+    size = Bd.moe_prepare_size(N, K, 1, gate_up)
+    buf = torch.empty(G * size, dtype=torch.uint8, device="cuda")
+    ow = []
+    for i in range(G):
+        shapes = [(N // 2, K)] * 2 if gate_up else [(N, K)]
+        mats = [(torch.randn(*sh, generator=g) * 0.02).to(torch.bfloat16) for sh in shapes]
+        qs = [quantize_bf16(m.cuda()) for m in mats]
+        Bd.moe_nvfp4_prepare_weights(torch.cat([q[0] for q in qs]), torch.cat([q[1] for q in qs]),
+                                     [q[2].item() for q in qs], N, K, 1, gate_up,
+                                     buf[i * size:(i + 1) * size])
+        ow.append([omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats])
+    return buf, ow
+
+
+@pytest.mark.parametrize("gate_up", [1, 0])
+def test_w4a4_grouped_gemm_tile_edges(gate_up):
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd, quantize_bf16
+    rows = [0, 40, 300, 7, 129, 128, 1]
+    G = len(rows)
+    N, K = (256, 512) if gate_up else (384, 256)
+    buf, ow = _fp4_groups(G, N, K, gate_up, seed=21 + gate_up)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    total = int(off[-1])
+    g = torch.Generator().manual_seed(9)
+    src = total + 5
+    a = torch.randn(src, K, generator=g).to(torch.bfloat16)
+    aq, asf, ags = quantize_bf16(a.cuda())
+    idx = torch.randperm(src, generator=g)[:total].to(torch.int32)
+    rs = torch.rand(total, generator=g) + 0.5
+    out = torch.full((total, N // 2 if gate_up else N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    offs_d, idx_d, rs_d = torch.from_numpy(off).cuda(), idx.cuda(), rs.cuda()
+    args = Bd.MoeGemmArgs(mode=1, gate_up=gate_up, num_groups=G, N=N, K=K)
+    args.weights = buf.data_ptr()
+    args.group_offsets = offs_d.data_ptr()
+    args.a, args.a_sf, args.a_gs = aq.data_ptr(), asf.data_ptr(), ags.data_ptr()
+    args.a_row_index = idx_d.data_ptr()
+    args.row_scale = None if gate_up else rs_d.data_ptr()
+    args.out = out.data_ptr()
+    args.out_amax = amax.data_ptr() if gate_up else None
+    ws = torch.zeros(Bd.moe_gemm_workspace_size(G), dtype=torch.uint8, device="cuda")
+    Bd.moe_nvfp4_grouped_gemm(args, ws)
+    assert Bd.moe_get_device_status(ws) == 0
+    got = out.float().cpu().numpy()
+    q, sf, gs = onv.quantize(a.float().numpy())
+    assert gs == np.float32(ags.item())
+    xa = onv.dequantize(q, sf, gs)[idx.numpy()]
+    for gi in range(G):
+        r0, r1 = off[gi], off[gi + 1]
+        if r1 == r0:
+            continue
+        if gate_up:
+            ref = omoe.gate_up_swiglu(xa[r0:r1], ow[gi][0], ow[gi][1])
+        else:
+            ref = omoe.down_proj(xa[r0:r1], ow[gi][0]) * rs.numpy()[r0:r1, None]
+        check_outputs(got[r0:r1], ref, what=f"group {gi} ({r1 - r0} rows)")
+    if gate_up:
+        assert amax.item() == float(np.abs(got).max())
+
+
+@pytest.mark.slow
+def test_w4a4_full_size_properties():
+    """The W4A4 workload at full size (16384 tokens, hidden 7168, 256 experts):
+    routing exact; X quantisation bit-exact; sampled tokens within the bound
+    that NVFP4 quantisation of h can introduce (valid for any global scale of
+    h): |out - out_h_unquantised| <= sum_i |W2 col i| * delta_i, where delta_i
+    = (block amax / 6) * (1 + 2**-4) is the round-trip bound of one element."""
+    cfg, layer, x, logits, out, ids = _run("w4a4")
+    rids, rw = omoe.route(logits.numpy(), cfg.k)
+    assert (ids == rids).all()
+    from nvfp4_mixture_experts_moe_gb300 import quantize_bf16
+    q, sf, gs = quantize_bf16(x.cuda())
+    xs = x.float().numpy()
+    rq, rsf, rgs = onv.quantize(xs)
+    assert np.float32(gs.item()) == rgs
+    assert (sf.cpu().numpy() == rsf).all() and (q.cpu().numpy() == onv.pack(rq)).all()
+    xd = onv.dequantize(rq, rsf, rgs)
+    tokens = [0, 9999]
+    ow = OracleWeights(cfg)
+    ow.prefetch([int(e) for t in tokens for e in rids[t]] + [cfg.E])
+    for t in tokens:
+        ref = np.zeros(cfg.H)
+        bound = np.zeros(cfg.H)
+        slots = [(int(rids[t, j]), float(rw[t, j])) for j in range(cfg.k)] + [(cfg.E, 1.0)]
+        for e, wt in slots:
+            g_, u_, d_ = ow(e)
+            h = omoe.bf16_round(omoe.gate_up_swiglu(xd[t:t + 1], g_, u_)).astype(np.float64)
+            blocks = np.abs(h.reshape(-1, 16)).max(axis=1)
+            delta = np.repeat(blocks / 6 * (1 + 2 ** -4), 16)
+            wd = d_.dequantize()
+            ref += wt * (h @ wd.T)[0]
+            bound += wt * (np.abs(wd) @ delta)
+        err = np.abs(out[t] - ref)
+        assert (err <= bound + 2e-2 + 2 ** -7 * np.abs(ref)).all(), (t, float((err - bound).max()))
+        # the quantisation error is random in sign: far below the worst case
+        assert np.linalg.norm(out[t] - ref) <= 0.25 * np.linalg.norm(bound)
