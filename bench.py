@@ -125,6 +125,22 @@ def algorithmic(cfg, ids_list):
             "gemm1_flops": gemm1_flops, "layer_flops": layer_flops, "w13_bytes": w13, "w2_bytes": w2}
 
 
+def max_over_ranks(v, dist, device):
+    """The largest of every rank's ``v`` (the job's step time is its slowest
+    rank's); identity without a process group."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_per_step):
+    """Whole-job throughput: every rank processes its own batch of tokens."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def config_dict(cfg, nb, flush):
     return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} I_shared={cfg.I_s} E={cfg.E} k={cfg.k} "
                         f"{cfg.mode.upper()} +1 shared expert",
@@ -133,18 +149,16 @@ def config_dict(cfg, nb, flush):
 
 
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg, x, logits, n_rows, pool_threads=8):
-    """Times the CPU oracle on the first ``n_rows`` (token, expert) rows of a
-    batch (routed slots in rank order, then the shared expert). Returns
-    (seconds, rows_done, cpu_seconds)."""
+def oracle_prepare(cfg, x, logits, n_rows, pool_threads=8):
+    """The (token, expert) rows of one batch in order (each token's routed
+    slots by rank, then its shared-expert row), the first ``n_rows`` of them,
+    and the oracle's NVFP4 weights of the experts they touch (quantised by the
+    oracle, untimed)."""
     from concurrent.futures import ThreadPoolExecutor
-
-    import numpy as np
 
     import synthetic_inputs as si
     from oracle import moe as omoe
 
-    xs = x.float().numpy()
     ids, w = omoe.route(logits.numpy(), cfg.k)
     plan = []
     for t in range(cfg.T):
@@ -152,58 +166,68 @@ def oracle_sample(cfg, x, logits, n_rows, pool_threads=8):
             plan.append((t, int(ids[t, j]), float(w[t, j])))
         plan.append((t, cfg.E, 1.0))
     plan = plan[:n_rows]
-    need = sorted({e for _, e, _ in plan})
 
     def prep(e):
         mats = [si.make_expert_weight(cfg, e, m) for m in ("gate", "up", "down")]
         return e, tuple(omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats)
 
     with ThreadPoolExecutor(pool_threads) as ex:
-        qw = dict(ex.map(prep, need))
-    out = np.zeros((cfg.T, cfg.H))
+        qw = dict(ex.map(prep, sorted({e for _, e, _ in plan})))
+    return plan, qw, x.float().numpy()
+
+
+def oracle_rows(plan, qw, xs, out):
+    """Runs the oracle (float64) on the given rows, accumulating into ``out``.
+    Returns (wall seconds, process CPU seconds)."""
+    from oracle import moe as omoe
     c0, t0 = time.process_time(), time.perf_counter()
     for t, e, wt in plan:
         g, u, d = qw[e]
         out[t] += wt * omoe.down_proj(omoe.gate_up_swiglu(xs[t:t + 1], g, u), d)[0]
-    wall = time.perf_counter() - t0
-    return wall, len(plan), time.process_time() - c0
+    return time.perf_counter() - t0, time.process_time() - c0
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import numpy as np
+
     import synthetic_inputs as si
     cfg = si.CONFIGS[args.config]
     x = si.make_x(cfg)
     logits = si.make_logits(cfg)
     rows_per_token = cfg.k + 1
-    # one (token, expert) row per step unless K is small enough for whole tokens
-    est = oracle_sample(cfg, x, logits, 1)[0]
-    per_step = rows_per_token if (args.steps + args.warmup) * est * rows_per_token < 150 else 1
-    total_rows = min((args.steps + args.warmup) * per_step, cfg.T * rows_per_token)
-    times = []
-    # warm-up + timed steps each run `per_step` rows (rows repeat once the batch is exhausted)
-    for i in range(args.warmup + args.steps):
-        wall, n, cpu = oracle_sample(cfg, x, logits, per_step if i else per_step)
+    all_rows = cfg.T * rows_per_token
+    steps = args.warmup + args.steps
+    plan, qw, xs = oracle_prepare(cfg, x, logits, min(all_rows, max(steps, rows_per_token)), pool_threads=16)
+    out = np.zeros((cfg.T, cfg.H))
+    est, _ = oracle_rows(plan[:1], qw, xs, out)
+    # whole tokens per step if that keeps the run short, else one row per step
+    per_step = rows_per_token if steps * est * rows_per_token < 150 else 1
+    if per_step > 1:
+        plan, qw, xs = oracle_prepare(cfg, x, logits, all_rows, pool_threads=16)
+    wall = cpu = 0.0
+    rows = 0
+    for i in range(steps):
+        sel = [plan[(i * per_step + r) % len(plan)] for r in range(per_step)]
+        w_, c_ = oracle_rows(sel, qw, xs, out)
         if i >= args.warmup:
-            times.append((wall, n, cpu))
-    wall = sum(t[0] for t in times)
-    rows = sum(t[1] for t in times)
-    cpu = sum(t[2] for t in times)
+            wall += w_
+            cpu += c_
+            rows += len(sel)
     tokens = rows / rows_per_token
     value = tokens / wall
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, len(times)),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(cfg, 1, "n/a (CPU)"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": round(cpu / wall, 2),
                              "kind": "oracle",
-                             "sample": f"{per_step} (token, expert) rows per step of the {cfg.name} batch; "
-                                       f"{rows} rows = {tokens:.2f} tokens timed; oracle weights prepared "
-                                       f"untimed"},
+                             "sample": f"{per_step} (token, expert) row(s) per step of the {cfg.name} batch "
+                                       f"({rows} rows = {tokens:.2f} tokens timed); oracle weights "
+                                       f"quantised untimed"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    del total_rows
     print(json.dumps(line), flush=True)
     return 0
 
@@ -298,14 +322,10 @@ def run_ours(args):
     clocks = sampler.stop()
     step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
     stage_ms = [[e[s].elapsed_time(e[s + 1]) for e in ev] for s in range(B.MOE_STAGE_COUNT - 1)]
-    ms = statistics.mean(step_ms)
-    if dist:
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
     if B.moe_get_device_status(ws) != 0:
         raise RuntimeError("device status set during the timed steps")
-    value = cfg.T * world / (ms / 1e3)
+    value = job_tokens_per_s(cfg.T, world, ms)
 
     # end to end: pinned host inputs copied in, result read back, every step
     hx = [b[0].cpu().pin_memory() for b in batches]
@@ -325,11 +345,7 @@ def run_ours(args):
         if i >= args.warmup:
             e2e_ev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    if dist:
-        tm = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tm.item())
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dist, dev)
     h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
     d2h = hout.numel() * hout.element_size()
 
@@ -363,7 +379,7 @@ def run_ours(args):
                                "bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
                                "touched_experts": alg["touched_experts"]},
             "stages_ms": per_stage,
-            "e2e": {"value": cfg.T * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches),
             "clocks": clocks,
@@ -371,8 +387,10 @@ def run_ours(args):
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x0, l0 = batches[0][0].cpu(), batches[0][1].cpu()
-        n_rows = args.cpu_sample_tokens * (cfg.k + 1)
-        wall, rows, cpu = oracle_sample(cfg, x0, l0, n_rows, pool_threads=16)
+        n_rows = min(cfg.T, args.cpu_sample_tokens) * (cfg.k + 1)
+        plan, qw, xs = oracle_prepare(cfg, x0, l0, n_rows, pool_threads=16)
+        wall, cpu = oracle_rows(plan, qw, xs, np.zeros((cfg.T, cfg.H)))
+        rows = len(plan)
         line["cpu_baseline"] = {"value": rows / (cfg.k + 1) / wall, "unit": "tokens/s",
                                 "cores": round(cpu / wall, 2), "kind": "oracle",
                                 "sample": f"first {rows} (token, expert) rows = {rows / (cfg.k + 1):.0f} tokens "
