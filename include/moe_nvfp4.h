@@ -265,6 +265,36 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream);
 moe_status moe_set_stage_events(void* const* events, int n);
 unsigned long long moe_kernel_launches(void);
 
+/* ------------------------------------------------------------------------
+ * moe_permute_noalloc: the permutation of moe_permute for callers that
+ * cannot allocate device memory when they call it (the pages have no
+ * counterpart). Some callers own all device memory themselves: a serving
+ * engine that reserves one pool at start-up and hands kernels only fixed
+ * buffers, or a plug-in running inside a host program that gives it no
+ * allocator. Such callers cannot size and provide a workspace per call.
+ *
+ * This entry point allocates nothing (no cudaMalloc, cudaFree or any
+ * allocating routine): its scratch is one fixed device array of 64 KiB
+ * that every GPU loading the library holds until the process exits.
+ * Inputs and outputs are as in moe_permute; device_status (nullable, device int32) receives MOE_OK or
+ * MOE_ERR_DEVICE (an expert id outside [0, E); such pairs are dropped and
+ * get inv_perm = -1). A problem whose scratch would exceed the array
+ * (T*k above 8192 pairs with more than 16320 histogram entries, e.g. more
+ * than about 200k pairs at E = 320) returns MOE_ERR_UNSUPPORTED before
+ * anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture. Every call on a device shares the one array and
+ * leaves its contents behind; each call clears the status word it needs.
+ * Calls that overlap on the GPU (on different streams, say) race on the
+ * array: order them on one stream or with events.
+ */
+moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k, int E,
+                               int32_t* counts, int32_t* offsets, int32_t* perm,
+                               int32_t* inv_perm, int32_t* device_status,
+                               moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,7 @@ _SIGS = {
     "moe_get_device_status": (_I, [_P, _P]),
     "moe_set_stage_events": (_I, [ctypes.POINTER(ctypes.c_void_p), _I]),
     "moe_kernel_launches": (ctypes.c_ulonglong, []),
+    "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 }
 
 MOE_STAGE_COUNT = 8
@@ -206,3 +207,10 @@ def moe_set_stage_events(events):
 
 def moe_kernel_launches():
     return int(lib().moe_kernel_launches())
+
+
+def moe_permute_noalloc(topk_ids, T, k, E, counts, offsets, perm, inv_perm, device_status=None, stream=None):
+    """moe_permute without a workspace (fixed device scratch inside the library)."""
+    _check(lib().moe_permute_noalloc(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm),
+                                     _ptr(inv_perm), _ptr(device_status), _stream(stream)),
+           "moe_permute_noalloc")
