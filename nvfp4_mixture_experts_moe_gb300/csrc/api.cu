@@ -324,6 +324,8 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   p.out_amax = a->out_amax;
   p.status = &static_cast<WsHeader*>(ws)->status;
   p.max_rows = 1 << 30;
+  p.pdl = false;
+  p.early_weights = false;
   return run_gemm(p, 1LL << 30, (cudaStream_t)stream);
 }
 
@@ -375,20 +377,30 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     ~StageGuard() { g_stage_events_set = false; }
   } guard;
 
+  // Kernels after the first use programmatic dependent launch (each waits for
+  // its predecessor's results in-kernel) unless stage events are recorded.
+  const bool pdl = !g_stage_events_set;
   stage_mark(0, s);
-  st = launch_route_topk(logits, T, E, k, ids, f.w, s);
-  if (st != MOE_OK) return st;
-  stage_mark(1, s);
-  st = launch_permute(ids, T, k, E, f.counts, f.offsets, f.perm, f.inv_perm, &f.hdr->status, f.perm_scratch,
-                      f.row_token, f.row_weight, f.w, f.gofs, s);
-  if (st != MOE_OK) return st;
+  if (P <= kFusedRoutePermuteMax) {  // route + permute in one CTA
+    st = launch_route_permute_small(logits, T, E, k, ids, f.w, f.counts, f.offsets, f.perm, f.inv_perm,
+                                    &f.hdr->status, f.row_token, f.row_weight, f.gofs, s);
+    if (st != MOE_OK) return st;
+    stage_mark(1, s);
+  } else {
+    st = launch_route_topk(logits, T, E, k, ids, f.w, s);
+    if (st != MOE_OK) return st;
+    stage_mark(1, s);
+    st = launch_permute(ids, T, k, E, f.counts, f.offsets, f.perm, f.inv_perm, &f.hdr->status, f.perm_scratch,
+                        f.row_token, f.row_weight, f.w, f.gofs, s, pdl);
+    if (st != MOE_OK) return st;
+  }
   stage_mark(2, s);
   if (fp4) {  // dynamic per-tensor quantisation of x (W4A4)
     st = cuda_ok(cudaMemsetAsync(&f.hdr->amax[0], 0, 2 * sizeof(float), s));
     if (st != MOE_OK) return st;
-    st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s);
+    st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s, pdl);
     if (st != MOE_OK) return st;
-    st = launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq, f.xsf, f.xgs, s);
+    st = launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq, f.xsf, f.xgs, s, pdl);
     if (st != MOE_OK) return st;
   }
   stage_mark(3, s);
@@ -413,11 +425,13 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.out_amax = fp4 ? &f.hdr->amax[1] : nullptr;
   g1.status = &f.hdr->status;
   g1.max_rows = rows;
+  g1.pdl = pdl;
+  g1.early_weights = false;
   st = run_gemm(g1, T, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
   if (fp4) {  // h -> NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue)
-    st = launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf, f.hgs, s);
+    st = launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf, f.hgs, s, pdl);
     if (st != MOE_OK) return st;
   }
   stage_mark(5, s);
@@ -433,13 +447,14 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g2.a_sf = fp4 ? f.hsf : nullptr;
   g2.a_gs = fp4 ? f.hgs : nullptr;
   g2.out_amax = nullptr;
+  g2.early_weights = true;  // group offsets come from the permutation, two launches back
   g2.a_row_index = nullptr;
   g2.row_scale = f.row_weight;
   g2.out = f.y;
   st = run_gemm(g2, T, s);
   if (st != MOE_OK) return st;
   stage_mark(6, s);
-  st = launch_combine(f.y, f.inv_perm, nullptr, has_shared ? 1 : 0, T, k, H, out, s);
+  st = launch_combine(f.y, f.inv_perm, nullptr, has_shared ? 1 : 0, T, k, H, out, s, pdl);
   if (st != MOE_OK) return st;
   stage_mark(7, s);
   return MOE_OK;

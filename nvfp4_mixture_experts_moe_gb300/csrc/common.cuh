@@ -44,8 +44,9 @@ static_assert(sizeof(PrepHeader) == 256, "prepared header is 256 bytes");
 // [16L, 16L+16): word s (k16 step s of the block) holds, byte by byte, the
 // code pairs of (row g, k 16s+2t..+1), (row g+8, same k), (row g, k+8..+9),
 // (row g+8, k+8..+9) -- the A-fragment order of an m16n8k16 MMA. Within a
-// scale block, group g owns bytes [8g, 8g+8): scales of row g for the four
-// k16 groups, then those of row g+8.
+// scale block, group g owns bytes [8g, 8g+8): for k16 step s = 0..3 the pair
+// (scale of row g, scale of row g+8), so one e4m3x2 conversion yields both
+// rows' scales of a step.
 __host__ __device__ inline size_t w4a16_data_bytes(int N, int K) { return (size_t)N * K / 2; }
 __host__ __device__ inline size_t w4a16_sf_bytes(int N, int K) { return (size_t)N * K / 16; }
 

@@ -8,35 +8,47 @@
 //
 // At a few rows per expert the layer is bound by the bytes of the touched
 // experts' weights ("Seven Months of GB10 Field Notes": decode re-reads the
-// active weights). So this kernel streams each weight tile from HBM exactly
-// once, straight into registers (no shared-memory round trip), turns the
-// e2m1 codes into f16 MMA fragments with the hardware e2m1x2 conversion,
-// multiplies in the E4M3 block scale (e2m1 * e4m3 is exact in f16) and feeds
-// mma.sync m16n8k16 with the group's rows (up to 8) as the N side.
+// active weights). Each weight byte is read from HBM once. One producer warp
+// streams the weight tiles with bulk copies (cp.async.bulk, completion on
+// mbarriers) into a ring of shared-memory stages, keeping ~100 KB in flight
+// per SM; eight MMA warps each own one 16-row tile of a 128-row item for the
+// whole K. A warp loads its 16-byte A fragment per 64-wide K block from
+// shared memory, turns the e2m1 codes into f16 with the hardware e2m1x2
+// conversion, multiplies in the E4M3 block scales (e2m1 * e4m3 is exact in
+// f16) and feeds mma.sync m16n8k16 with the group's rows (up to 8) as N.
 //
-// Activations enter as f16: each row is scaled by a power of two 2^s so
-// that its largest magnitude lands in [2^14, 2^15); bf16 values are then
-// exact in f16 (apart from magnitudes below 2^-24 of the row's maximum,
-// which flush), and the epilogue multiplies by 2^-s again.
+// Activations enter as f16: each row is scaled by a power of two 2^s so that
+// its largest magnitude lands in [2^14, 2^15); bf16 values are then exact in
+// f16 (apart from magnitudes below 2^-24 of the row's maximum, which flush),
+// and the epilogue multiplies by 2^-s again. The gate/up tile holds the gate
+// and up rows of the same 8 features (prepared interleave), so SwiGLU is
+// applied in registers.
 //
-// Work item = (group, chunk of 8 rows, 128 weight rows). Each of the 8 warps
-// of a CTA owns every 8th 64-wide K block (split-K inside the CTA) and all
-// eight 16-row MMA tiles of the item; partial sums meet in shared memory.
-// CTAs are persistent and take contiguous item ranges.
+// Work item = (group, chunk of 8 rows, 128 weight rows). CTAs are persistent
+// (one per SM) and take contiguous item ranges. Every wait is bounded; on a
+// timeout the kernel records MOE_ERR_TIMEOUT and returns.
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+using namespace tc;
+
+constexpr int kMmaWarps = 8;
+constexpr int kThreads = (kMmaWarps + 1) * 32;  // + one producer warp
 constexpr int kRowsPerPass = 8;
-constexpr int kTileRows = 128;     // weight rows per item
+constexpr int kTileRows = 128;                   // weight rows per item
 constexpr int kMaxGroups = 1025;
+constexpr int kBlocksPerStage = 8;               // 64-wide K blocks per stage (512 K)
+constexpr int kStageData = kMmaWarps * kBlocksPerStage * 512;  // 32 KB
+constexpr int kStageSf = kMmaWarps * kBlocksPerStage * 64;     // 4 KB
+constexpr int kStageBytes = kStageData + kStageSf;
+constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
 
 struct SmallArgs {
   const uint8_t* weights;
@@ -49,6 +61,17 @@ struct SmallArgs {
   const float* row_scale;
   uint16_t* out;
   int rows_limit;
+  int stages;
+  int early_weights;  // stream weights before the dependency wait (offsets already final)
+  int* status;
+};
+
+struct SmallSmem {
+  uint64_t full[8];
+  uint64_t empty[8];
+  int abort;
+  float row_mul[kRowsPerPass];
+  int row_out[kRowsPerPass];
 };
 
 __device__ __forceinline__ int group_items(const int32_t* off, int g, int mt_count, int limit) {
@@ -57,36 +80,62 @@ __device__ __forceinline__ int group_items(const int32_t* off, int g, int mt_cou
   return ((rows + kRowsPerPass - 1) / kRowsPerPass) * mt_count;
 }
 
+__device__ __forceinline__ int find_group(const int* pref, int G, int item) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Named barrier over the eight MMA warps only (the producer never joins).
+__device__ __forceinline__ void mma_warps_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kMmaWarps * 32)); }
+
 template <bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, 2) gemm_small_kernel(SmallArgs p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   const int K = p.K, N = p.N;
-  const int xs_stride = K + 8;  // f16 elements per staged row (16-byte pad: no bank conflicts)
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);                                  // [8][K+8]
-  float* red = reinterpret_cast<float*>(smem_raw + (size_t)kRowsPerPass * xs_stride * 2);  // [8][8][32][4]
-  int* pref = reinterpret_cast<int*>(red + kWarps * 8 * 32 * 4);                          // [G+1]
-  __shared__ float row_mul[kRowsPerPass];   // 2^-s per staged row
-  __shared__ int row_out[kRowsPerPass];     // output row index, -1 if padding
-  __shared__ int warp_tmp[32];
+  const int S = p.stages;
+  const int xs_stride = K + 8;  // f16 elements per staged row (16-byte pad: conflict-free ldmatrix)
+  uint8_t* stages = smem_raw;                                                   // S x kStageBytes
+  uint16_t* xs = reinterpret_cast<uint16_t*>(stages + (size_t)S * kStageBytes);  // [8][K+8]
+  SmallSmem* sm = reinterpret_cast<SmallSmem*>(xs + (size_t)kRowsPerPass * xs_stride);
+  int* pref = reinterpret_cast<int*>(sm + 1);                                   // [G+1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int mt_count = N / kTileRows;
   const int G = p.G;
+  const int kblocks = K / 64;
+  const int nstage = (kblocks + kBlocksPerStage - 1) / kBlocksPerStage;
+  if (!p.early_weights) pdl_wait();
 
-  // Item prefix sums over groups (each CTA computes its own copy).
   for (int g = tid; g < G; g += kThreads) pref[g + 1] = group_items(p.group_offsets, g, mt_count, p.rows_limit);
-  if (tid == 0) pref[0] = 0;
+  if (tid == 0) {
+    pref[0] = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&sm->full[i], 1);
+      mbar_init(&sm->empty[i], kMmaWarps);
+    }
+    sm->abort = 0;
+    fence_barrier_init();
+  }
   __syncthreads();
-  if (tid < 32) {
-    // serial-by-warp inclusive scan in chunks of 32
+  if (warp == 0) {
     int carry = 0;
-    for (int base = 1; base <= G; base += 32) {
-      const int i = base + lane;
+    for (int b0 = 1; b0 <= G; b0 += 32) {
+      const int i = b0 + lane;
       int v = i <= G ? pref[i] : 0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += o;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
       }
       if (i <= G) pref[i] = v + carry;
       carry += __shfl_sync(0xffffffffu, v, 31);
@@ -96,26 +145,57 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_small_kernel(SmallArgs p) {
   const int total = pref[G];
   const int i0 = (int)((long long)total * blockIdx.x / gridDim.x);
   const int i1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  volatile int* abort = &sm->abort;
 
-  const int kblocks = K / 64;
-  int cur_g = -1, cur_c = -1;
-  for (int item = i0; item < i1; ++item) {
-    // group of this item: last g with pref[g] <= item
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pref[mid] <= item) lo = mid; else hi = mid - 1;
+  if (warp == kMmaWarps) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      int j = 0;
+      for (int item = i0; item < i1 && !*abort; ++item) {
+        const int g = find_group(pref, G, item);
+        const int mt = (item - pref[g]) % mt_count;
+        const uint8_t* blk = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
+                                                                      : p.weights + (size_t)g * p.stride;
+        const uint8_t* data = blk + sizeof(PrepHeader);
+        const uint8_t* sfp = data + w4a16_data_bytes(N, K);
+        for (int st = 0; st < nstage; ++st, ++j) {
+          const int slot = j % S;
+          if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, kWaitLimit)) break;
+          const int kb0 = st * kBlocksPerStage;
+          const int nkb = min(kBlocksPerStage, kblocks - kb0);
+          mbar_arrive_expect_tx(&sm->full[slot], (uint32_t)(kMmaWarps * nkb * (512 + 64)));
+          uint8_t* sd = stages + (size_t)slot * kStageBytes;
+          for (int w = 0; w < kMmaWarps; ++w) {
+            const size_t b = (size_t)(mt * 8 + w) * kblocks + kb0;
+            bulk_g2s(smem_u32(sd + w * kBlocksPerStage * 512), data + b * 512, nkb * 512, &sm->full[slot]);
+            bulk_g2s(smem_u32(sd + kStageData + w * kBlocksPerStage * 64), sfp + b * 64, nkb * 64,
+                     &sm->full[slot]);
+          }
+        }
+      }
     }
-    const int g = lo;
+    return;
+  }
+
+  // ------------------------------------------------------------- MMA warps
+  if (p.early_weights) pdl_wait();  // the activation rows come from the predecessor
+  const int g8 = lane >> 2, t4 = lane & 3;
+  int cur_g = -1, cur_c = -1;
+  int j = 0;
+  // ldmatrix row address of this lane: matrix q = lane / 8 covers the 8
+  // staged rows at k offset 8 * q (two k16 steps per ldmatrix.x4)
+  const int lrow = lane & 7, lq = lane >> 3;
+  for (int item = i0; item < i1; ++item) {
+    const int g = find_group(pref, G, item);
     const int local = item - pref[g];
     const int c = local / mt_count, mt = local % mt_count;
     const int row0 = p.group_offsets[g] + c * kRowsPerPass;
     const int nrows = min(kRowsPerPass, p.group_offsets[g + 1] - row0);
 
     if (g != cur_g || c != cur_c) {
-      __syncthreads();  // everyone is done with the previous rows
-      // warp w stages row w: max |x|, power-of-two scale, f16 conversion
-      const int r = warp;
+      if (*abort) break;
+      mma_warps_sync();  // everyone is done with the previous rows
+      const int r = warp;  // warp w stages row w
       uint16_t* dst = xs + (size_t)r * xs_stride;
       if (r < nrows) {
         const int orow = row0 + r;
@@ -126,134 +206,122 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_small_kernel(SmallArgs p) {
           const uint4 v = __ldg(src + i);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+          for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-        // m = bf16 bits of the row max; its exponent e gives max in [2^(e-127), 2^(e-126))
-        const int e = (int)(m >> 7);  // biased exponent (0 for zero/subnormal rows)
+        if (m > 0x7f80u) m = 0x7f80u;  // NaN patterns are outside the contract
+        // m = bf16 bits of the row max; its exponent e puts the max in [2^(e-127), 2^(e-126))
+        const int e = (int)(m >> 7);
         int sh = (m == 0) ? 0 : 141 - max(e, 1);  // 2^(e-127+sh) = 2^14
-        sh = max(-113, min(sh, 126));             // keeps 2^sh and 2^-sh normal floats
+        sh = max(-113, min(sh, 126));             // 2^sh and 2^-sh stay normal floats
         const float up = __int_as_float((127 + sh) << 23);
         for (int i = lane; i < K / 8; i += 32) {
           const uint4 v = __ldg(src + i);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float f0 = __uint_as_float(w[j] << 16) * up;
-            const float f1 = __uint_as_float(w[j] & 0xffff0000u) * up;
-            const __half2 h = __floats2half2_rn(f0, f1);
-            o[j] = *reinterpret_cast<const uint32_t*>(&h);
+          for (int q = 0; q < 4; ++q) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * up,
+                                                __uint_as_float(w[q] & 0xffff0000u) * up);
+            o[q] = *reinterpret_cast<const uint32_t*>(&h);
           }
           *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         if (lane == 0) {
-          row_mul[r] = __int_as_float((127 - sh) << 23);
-          row_out[r] = orow;
+          sm->row_mul[r] = __int_as_float((127 - sh) << 23);
+          sm->row_out[r] = orow;
         }
       } else {
         for (int i = lane; i < K / 8; i += 32) *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(0, 0, 0, 0);
         if (lane == 0) {
-          row_mul[r] = 0.0f;
-          row_out[r] = -1;
+          sm->row_mul[r] = 0.0f;
+          sm->row_out[r] = -1;
         }
       }
       cur_g = g;
       cur_c = c;
-      __syncthreads();
+      mma_warps_sync();
     }
 
-    const uint8_t* blk = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
-                                                                  : p.weights + (size_t)g * p.stride;
-    const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(blk);
-    const uint8_t* data = blk + sizeof(PrepHeader);
-    const uint8_t* sfp = data + w4a16_data_bytes(N, K);
-
-    float acc[8][4];
+    // one accumulator per k16 step of a block: four independent MMA chains
+    float acc4[4][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-
-    const int g8 = lane >> 2, t4 = lane & 3;
-    const uint16_t* xrow = xs + (size_t)g8 * xs_stride + 2 * t4;
-    for (int kb = warp; kb < kblocks; kb += kWarps) {
-      uint4 wq[8];
-      uint2 sq[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const size_t b = (size_t)(mt * 8 + i) * kblocks + kb;
-        wq[i] = ldg_stream(data + b * 512 + lane * 16);
-        sq[i] = ldg_stream2(sfp + b * 64 + g8 * 8);
-      }
-      uint32_t bf[4][2];
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        bf[s][0] = *reinterpret_cast<const uint32_t*>(xrow + kb * 64 + 16 * s);
-        bf[s][1] = *reinterpret_cast<const uint32_t*>(xrow + kb * 64 + 16 * s + 8);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t wv[4] = {wq[i].x, wq[i].y, wq[i].z, wq[i].w};
+    for (int s = 0; s < 4; ++s) acc4[s][0] = acc4[s][1] = acc4[s][2] = acc4[s][3] = 0.f;
+    const uint32_t xbase = smem_u32(xs) + (uint32_t)(lrow * xs_stride + 8 * lq) * 2;
+    bool ok = true;
+    for (int st = 0; st < nstage; ++st, ++j) {
+      const int slot = j % S;
+      if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, kWaitLimit)) { ok = false; break; }
+      const int kb0 = st * kBlocksPerStage;
+      const int nkb = min(kBlocksPerStage, kblocks - kb0);
+      const uint8_t* sd = stages + (size_t)slot * kStageBytes;
+      const uint8_t* my_data = sd + warp * kBlocksPerStage * 512 + lane * 16;
+      const uint8_t* my_sf = sd + kStageData + warp * kBlocksPerStage * 64 + g8 * 8;
+#pragma unroll 2
+      for (int kb = 0; kb < nkb; ++kb) {
+        const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * 512);
+        const uint2 sq = *reinterpret_cast<const uint2*>(my_sf + kb * 64);
+        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+        // B fragments of the 4 k16 steps: two ldmatrix.x4 (steps 0-1, 2-3)
+        uint32_t bf[8];
+        const uint32_t xa = xbase + (uint32_t)((kb0 + kb) * 64) * 2;
+        ldsm_x4(xa, bf[0], bf[1], bf[2], bf[3]);
+        ldsm_x4(xa + 64, bf[4], bf[5], bf[6], bf[7]);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           uint32_t a[4];
           cvt_e2m1x8_f16(wv[s], a);
-          // block scales of rows g and g+8 for k16 group s, each duplicated
-          // into both halves so the MMA fragments multiply element-wise
-          const uint32_t sg = cvt_e4m3x2_f16x2(__byte_perm(sq[i].x, 0, s | (s << 4)));
-          const uint32_t s8 = cvt_e4m3x2_f16x2(__byte_perm(sq[i].y, 0, s | (s << 4)));
-          a[0] = hmul2_u32(a[0], sg);
-          a[1] = hmul2_u32(a[1], s8);
-          a[2] = hmul2_u32(a[2], sg);
-          a[3] = hmul2_u32(a[3], s8);
-          mma_f16_16816(acc[i], a, bf[s][0], bf[s][1]);
+          // (scale of row g, scale of row g+8) for step s
+          const uint32_t pr = cvt_e4m3x2_f16x2(((s < 2 ? sq.x : sq.y) >> (16 * (s & 1))) & 0xffffu);
+          const __half2 sp = *reinterpret_cast<const __half2*>(&pr);
+          const __half2 sg = __low2half2(sp), s8 = __high2half2(sp);
+          __half2* ah = reinterpret_cast<__half2*>(a);
+          ah[0] = __hmul2(ah[0], sg);
+          ah[1] = __hmul2(ah[1], s8);
+          ah[2] = __hmul2(ah[2], sg);
+          ah[3] = __hmul2(ah[3], s8);
+          mma_f16_16816(acc4[s], a, bf[2 * s], bf[2 * s + 1]);
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->empty[slot]);
     }
+    if (!ok) break;
+    float acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = (acc4[0][q] + acc4[1][q]) + (acc4[2][q] + acc4[3][q]);
 
-    // Cross-warp reduction of the split-K partial sums.
-    float* my = red + ((size_t)warp * 8 * 32) * 4;
+    // Epilogue: c0,c1 = row g (tokens 2t, 2t+1); c2,c3 = row g+8.
+    const uint8_t* blk = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
+                                                                  : p.weights + (size_t)g * p.stride;
+    const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(blk);
+    const int mb = mt * 8 + warp;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<float4*>(my + ((size_t)i * 32 + lane) * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    __syncthreads();
-    {
-      const int i = tid >> 5;  // 16-row tile within the item
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float4 v = *reinterpret_cast<const float4*>(red + (((size_t)w * 8 + i) * 32 + lane) * 4);
-        c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
-      }
-      const int mb = mt * 8 + i;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int n = 2 * t4 + q;  // staged row
-        if (n >= nrows) continue;
-        const int orow = row_out[n];
-        const float rm = row_mul[n];
-        if (GATE_UP) {
-          const float gv = c[q] * rm * hdr->alpha[0];
-          const float uv = c[2 + q] * rm * hdr->alpha[1];
-          const int f = 8 * mb + g8;
-          p.out[(size_t)orow * (N / 2) + f] = float_to_bf16_bits(silu(gv) * uv);
-        } else {
-          const float rs = p.row_scale ? p.row_scale[orow] : 1.0f;
-          const int hr = 16 * mb + g8;
-          p.out[(size_t)orow * N + hr] = float_to_bf16_bits(c[q] * rm * hdr->alpha[0] * rs);
-          p.out[(size_t)orow * N + hr + 8] = float_to_bf16_bits(c[2 + q] * rm * hdr->alpha[0] * rs);
-        }
+    for (int q = 0; q < 2; ++q) {
+      const int n = 2 * t4 + q;
+      if (n >= nrows) continue;
+      const int orow = sm->row_out[n];
+      const float rm = sm->row_mul[n];
+      if (GATE_UP) {
+        const float gv = acc[q] * rm * hdr->alpha[0];
+        const float uv = acc[2 + q] * rm * hdr->alpha[1];
+        p.out[(size_t)orow * (N / 2) + 8 * mb + g8] = float_to_bf16_bits(silu(gv) * uv);
+      } else {
+        const float rs = p.row_scale ? p.row_scale[orow] : 1.0f;
+        const int hr = 16 * mb + g8;
+        p.out[(size_t)orow * N + hr] = float_to_bf16_bits(acc[q] * rm * hdr->alpha[0] * rs);
+        p.out[(size_t)orow * N + hr + 8] = float_to_bf16_bits(acc[2 + q] * rm * hdr->alpha[0] * rs);
       }
     }
-    __syncthreads();
   }
-  (void)warp_tmp;
+  if (lane == 0 && sm->abort) set_status(p.status, MOE_ERR_TIMEOUT);
 }
 
 }  // namespace
 
-size_t gemm_small_smem_bytes(int K, int G) {
-  return (size_t)kRowsPerPass * (K + 8) * 2 + (size_t)kWarps * 8 * 32 * 4 * 4 + (size_t)(G + 1) * 4;
+static size_t small_smem_bytes(int K, int G, int S) {
+  return (size_t)S * kStageBytes + (size_t)kRowsPerPass * (K + 8) * 2 + sizeof(SmallSmem) + (size_t)(G + 1) * 4;
 }
 
 moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStream_t s) {
@@ -272,27 +340,26 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStrea
   a.row_scale = pl.row_scale;
   a.out = pl.out;
   a.rows_limit = rows_limit;
-  const size_t smem = gemm_small_smem_bytes(pl.K, pl.num_groups);
-  if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
-  int dev = 0, sms = 152;
+  a.status = pl.status;
+  a.early_weights = pl.pdl && pl.early_weights ? 1 : 0;
+  const size_t limit = 227 * 1024;
+  int S = 6;
+  while (S > 2 && small_smem_bytes(pl.K, pl.num_groups, S) > limit) --S;
+  const size_t smem = small_smem_bytes(pl.K, pl.num_groups, S);
+  if (smem > limit) return MOE_ERR_UNSUPPORTED;
+  a.stages = S;
+  int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int per_sm = smem <= 110 * 1024 ? 2 : 1;
   // upper bound on items: every row its own chunk
   const long long max_items = (long long)((pl.max_rows + kRowsPerPass - 1) / kRowsPerPass + pl.num_groups) *
                               (pl.N / kTileRows);
-  const int grid = (int)std::max<long long>(1, std::min<long long>((long long)sms * per_sm, max_items));
-  if (pl.gate_up) {
-    auto k = gemm_small_kernel<true>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kThreads, smem, s>>>(a);
-    count_launches(1);
-  } else {
-    auto k = gemm_small_kernel<false>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kThreads, smem, s>>>(a);
-    count_launches(1);
-  }
+  const int grid = (int)std::max<long long>(1, std::min<long long>((long long)sms, max_items));
+  auto k = pl.gate_up ? gemm_small_kernel<true> : gemm_small_kernel<false>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(grid), dim3(kThreads), smem, s, a);
+  if (e != cudaSuccess) return cuda_ok(e);
+  count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
 

@@ -38,12 +38,12 @@ using namespace tc;
 constexpr int kM = 128;            // weight rows per tile
 constexpr int kRowBytes = 128;     // bytes per operand row per stage (64 bf16)
 constexpr int kBK = 64;            // K elements per stage
-constexpr int kStages = 4;
-constexpr int kMaxBN = 256;
-constexpr int kLookahead = 2;      // cp.async groups in flight per producer thread
+constexpr int kStages = 6;
+constexpr int kMaxBN = 128;
+constexpr int kLookahead = 4;      // cp.async groups in flight per producer thread
 constexpr int kThreads = 288;
 constexpr int kProducers = 128;
-constexpr int kAccCols = 256;      // TMEM columns per accumulator buffer
+constexpr int kAccCols = 128;      // TMEM columns per accumulator buffer
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;  // cycles (~2 s) before giving up
 
 constexpr int kATileBytes = kM * kRowBytes;              // 16 KB
@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
   const int G = p.G, K = p.K, N = p.N;
   const int MT = N / kM;
   const int KS = K / kBK;
+  pdl_wait();
 
   // Item prefix over groups.
   for (int g = tid; g < G; g += kThreads) {
@@ -185,8 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
       const uint32_t at = smem_u32(a_tiles + slot * kATileBytes);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const uint32_t sg = cvt_e4m3x2_f16x2(__byte_perm(sw.x, 0, s | (s << 4)));
-        const uint32_t s8 = cvt_e4m3x2_f16x2(__byte_perm(sw.y, 0, s | (s << 4)));
+        // (scale of row g, scale of row g+8) for step s -> each in both halves
+        const uint32_t pair = cvt_e4m3x2_f16x2(((s < 2 ? sw.x : sw.y) >> (16 * (s & 1))) & 0xffffu);
+        const uint32_t sg = __byte_perm(pair, 0, 0x1010);
+        const uint32_t s8 = __byte_perm(pair, 0, 0x3232);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const uint32_t scale = (b & 1) ? s8 : sg;
@@ -392,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a4_kernel(TcFp4Args p) 
   const int G = p.G, K = p.K, N = p.N;
   const int MT = N / kM;
   const int KS = K / kFp4BK;
+  pdl_wait();
 
   for (int g = tid; g < G; g += kThreads) {
     const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
@@ -627,15 +631,10 @@ moe_status launch_gemm_tc_w4a16(const GemmPlan& pl, int rows_min, cudaStream_t s
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (pl.gate_up) {
-    auto k = gemm_tc_w4a16_kernel<true>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<sms, kThreads, smem, s>>>(a);
-  } else {
-    auto k = gemm_tc_w4a16_kernel<false>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<sms, kThreads, smem, s>>>(a);
-  }
+  auto k = pl.gate_up ? gemm_tc_w4a16_kernel<true> : gemm_tc_w4a16_kernel<false>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(kThreads), smem, s, a);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
@@ -672,15 +671,10 @@ moe_status launch_gemm_tc_w4a4(const GemmPlan& pl, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (pl.gate_up) {
-    auto k = gemm_tc_w4a4_kernel<true>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<sms, kThreads, smem, s>>>(a);
-  } else {
-    auto k = gemm_tc_w4a4_kernel<false>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<sms, kThreads, smem, s>>>(a);
-  }
+  auto k = pl.gate_up ? gemm_tc_w4a4_kernel<true> : gemm_tc_w4a4_kernel<false>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(kThreads), smem, s, a);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }

@@ -1,9 +1,28 @@
 // Internal launchers shared between the translation units of the library.
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
+
+// Launches `kernel`, with programmatic dependent launch when `pdl` is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Records the CUDA error string for moe_last_cuda_error() and maps it.
 moe_status cuda_ok(cudaError_t e);
@@ -12,6 +31,18 @@ moe_status cuda_ok(cudaError_t e);
 void count_launches(int n);
 
 constexpr int kPermSingleMax = 8192;  // pairs handled by the one-CTA permutation
+constexpr int kFusedRoutePermuteMax = 2048;  // pairs routed and permuted by one CTA in one launch
+
+// Programmatic dependent launch: a kernel launched with it may start before
+// its predecessor in the stream finishes; it must call pdl_wait() before it
+// reads anything the predecessor writes. Without the attribute the wait
+// returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+moe_status launch_route_permute_small(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                      int* status, int32_t* row_token, float* row_weight, int32_t* gofs,
+                                      cudaStream_t s);
 
 moe_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                              cudaStream_t s);
@@ -20,16 +51,17 @@ size_t permute_scratch_bytes(int T, int k, int E);
 moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* inv_perm, int* status, void* scratch,
                           int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
-                          cudaStream_t s);
+                          cudaStream_t s, bool pdl = false);
 
 // Quantisation: amax into *amax (must be zeroed first), then codes.
-moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s);
+moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s, bool pdl = false);
 moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float* amax, uint8_t* q,
-                                uint8_t* sf, float* gs_out, cudaStream_t s);
+                                uint8_t* sf, float* gs_out, cudaStream_t s, bool pdl = false);
 
 moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStream_t s);
 moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
-                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s);
+                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s,
+                          bool pdl = false);
 
 // Weight preparation (device part; the host validates sizes and scales).
 moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
@@ -57,6 +89,9 @@ struct GemmPlan {
   float* out_amax;
   int* status;
   int max_rows;             // upper bound of group_offsets[G] (sizes launches)
+  bool pdl;                 // programmatic dependent launch (inside the fused forward)
+  bool early_weights;       // group offsets are final before the predecessor ends: weights may
+                            // stream before the dependency wait (only with pdl)
 };
 
 // Small-group path: mma.sync m16n8k16 over register-dequantised weights; one

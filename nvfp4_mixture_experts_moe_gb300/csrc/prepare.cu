@@ -48,7 +48,8 @@ __global__ void prepare_w4a16_sf_kernel(const uint8_t* __restrict__ sf, int N, i
     const size_t blk = i / 64;
     const int within = (int)(i % 64);
     const int mb = (int)(blk / kblocks), kb = (int)(blk % kblocks);
-    const int g = within / 8, half = (within / 4) & 1, j = within & 3;
+    // group g owns 8 bytes: (row g, row g+8) pairs for k16 steps 0..3
+    const int g = within / 8, j = (within / 2) & 3, half = within & 1;
     const int r = 16 * mb + g + 8 * half;
     const uint8_t v = sf[(size_t)src_row(r, N, gate_up) * (K / 16) + 4 * kb + j];
     check_sf(v, flag);

@@ -20,6 +20,7 @@ namespace moe {
 // per block on the float's bit pattern (exact and order-independent).
 __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x, size_t n,
                                                         float* __restrict__ amax) {
+  pdl_wait();
   uint32_t m = 0;  // running max of |x| as a bf16 bit pattern (monotonic in magnitude)
   const size_t nvec = n / 8;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restri
   }
 }
 
-moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s) {
+moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s, bool pdl) {
   if (n == 0) return MOE_OK;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
@@ -58,7 +59,8 @@ moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream
   size_t want = (n / 8 + 255) / 256;
   size_t cap = (size_t)sms * 8;
   int blocks = (int)(want == 0 ? 1 : (want < cap ? want : cap));
-  amax_bf16_kernel<<<blocks, 256, 0, s>>>(x, n, amax);
+  cudaError_t e = launch_ex(pdl, amax_bf16_kernel, dim3(blocks), dim3(256), 0, s, x, n, amax);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(256) quantize_bf16_kernel(const uint16_t* __re
                                                             const float* __restrict__ amax_p,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                             float* __restrict__ gs_out) {
+  pdl_wait();
   const float amax = *amax_p;
   const float gs = amax > 0.0f ? 2688.0f / amax : 1.0f;
   const size_t nblk = (size_t)rows * (K / 16);
@@ -129,10 +132,12 @@ __global__ void __launch_bounds__(256) quantize_bf16_kernel(const uint16_t* __re
 }
 
 moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float* amax, uint8_t* q,
-                                uint8_t* sf, float* gs_out, cudaStream_t s) {
+                                uint8_t* sf, float* gs_out, cudaStream_t s, bool pdl) {
   const size_t nblk = (size_t)rows * (K / 16);
   const int blocks = (int)((nblk + 255) / 256);
-  quantize_bf16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(x, rows, K, amax, q, sf, gs_out);
+  cudaError_t e = launch_ex(pdl, quantize_bf16_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s, x, rows,
+                            K, amax, q, sf, gs_out);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ inv_perm,
                                                      const float* __restrict__ topk_w, int shared, int T,
                                                      int k, int H, uint16_t* __restrict__ out) {
+  pdl_wait();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;  // chunk of 8 columns
   if (c8 * 8 >= H) return;
@@ -203,11 +209,13 @@ __global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict_
 }
 
 moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
-                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s) {
+                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s, bool pdl) {
   if (T == 0) return MOE_OK;
   const int chunks = H / 8;
   dim3 grid((chunks + 63) / 64, T);
-  combine_kernel<<<grid, 64, 0, s>>>(y, inv_perm, topk_w, y_shared_rows, T, k, H, out);
+  cudaError_t e = launch_ex(pdl, combine_kernel, grid, dim3(64), 0, s, y, inv_perm, topk_w, y_shared_rows, T, k,
+                            H, out);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }

@@ -17,12 +17,9 @@ namespace moe {
 // exp(l_j - l_max) / sum over the chosen j (fp32), i.e. the softmax
 // probabilities renormalised over the top k.
 template <int PER_LANE>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
-                                                         int k, int32_t* __restrict__ ids,
-                                                         float* __restrict__ w) {
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int token, int E, int k,
+                                            int32_t* __restrict__ ids, float* __restrict__ w) {
   const int lane = threadIdx.x & 31;
-  const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (token >= T) return;
   const float* row = logits + (size_t)token * E;
   float v[PER_LANE];
   uint32_t taken = 0;
@@ -74,6 +71,15 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     ids[(size_t)token * k + lane] = my_id;
     w[(size_t)token * k + lane] = ex / sum;
   }
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                         int k, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w) {
+  const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (token >= T) return;
+  route_token<PER_LANE>(logits, token, E, k, ids, w);
 }
 
 moe_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -209,10 +215,9 @@ __device__ void block_exclusive_scan(int* data, int n, int* tmp /* smem [32] */)
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __restrict__ ids, int P,
-                                                              int E, int32_t* counts, int32_t* offsets,
-                                                              int32_t* perm, int32_t* inv_perm,
-                                                              int* status, RowInfoOut ri) {
+__device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int E, int32_t* counts,
+                                    int32_t* offsets, int32_t* perm, int32_t* inv_perm, int* status,
+                                    const RowInfoOut& ri) {
   extern __shared__ int smem[];
   int* cnt = smem;            // [E]
   int* cursor = smem + E;     // [E]
@@ -249,9 +254,56 @@ __global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __r
   write_row_info(ri, perm, P);
 }
 
+__global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __restrict__ ids, int P,
+                                                              int E, int32_t* counts, int32_t* offsets,
+                                                              int32_t* perm, int32_t* inv_perm,
+                                                              int* status, RowInfoOut ri) {
+  pdl_wait();
+  permute_single_body(ids, P, E, counts, offsets, perm, inv_perm, status, ri);
+}
+
+// Small batches: route and permute in one CTA (one launch). Warp w routes
+// tokens w, w + 32, ...; the permutation starts once every id is written.
+template <int PER_LANE>
+__global__ void __launch_bounds__(1024) route_permute_small_kernel(const float* __restrict__ logits, int T,
+                                                                   int E, int k, int32_t* ids, float* w,
+                                                                   int32_t* counts, int32_t* offsets,
+                                                                   int32_t* perm, int32_t* inv_perm,
+                                                                   int* status, RowInfoOut ri) {
+  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5) route_token<PER_LANE>(logits, t, E, k, ids, w);
+  __syncthreads();
+  __threadfence_block();
+  permute_single_body(ids, T * k, E, counts, offsets, perm, inv_perm, status, ri);
+}
+
+moe_status launch_route_permute_small(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                      int* status, int32_t* row_token, float* row_weight, int32_t* gofs,
+                                      cudaStream_t s) {
+  RowInfoOut ri{row_token, row_weight, w, k, T, gofs};
+  const size_t smem = (2 * (size_t)E + 32) * sizeof(int);
+  const int per = (E + 31) / 32;
+#define MOE_RP_CASE(PL)                                                                                  \
+  if (per <= PL) {                                                                                       \
+    route_permute_small_kernel<PL><<<1, 1024, smem, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, \
+                                                         inv_perm, status, ri);                          \
+    count_launches(1);                                                                                   \
+    return cuda_ok(cudaGetLastError());                                                                  \
+  }
+  MOE_RP_CASE(1)
+  MOE_RP_CASE(2)
+  MOE_RP_CASE(4)
+  MOE_RP_CASE(8)
+  MOE_RP_CASE(16)
+  MOE_RP_CASE(32)
+#undef MOE_RP_CASE
+  return MOE_ERR_UNSUPPORTED;
+}
+
 __global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                              int32_t* chunk_hist /* [nchunks][E] */,
                                                              int32_t* perm) {
+  pdl_wait();
   extern __shared__ int cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -269,6 +321,7 @@ __global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __re
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* chunk_hist, int nchunks, int E, int P,
                                                             int32_t* counts, int32_t* offsets,
                                                             int32_t* gofs, int T) {
+  pdl_wait();
   extern __shared__ int smem[];
   int* tot = smem;         // [E]
   int* tmp = smem + E;     // [32]
@@ -303,6 +356,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* chunk_hist,
 __global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                                const int32_t* chunk_base, int32_t* perm,
                                                                int32_t* inv_perm, int* status) {
+  pdl_wait();
   extern __shared__ int cursor[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cursor[e] = chunk_base[(size_t)blockIdx.x * E + e];
   __syncthreads();
@@ -312,6 +366,7 @@ __global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __
 }
 
 __global__ void row_info_kernel(const int32_t* perm, int P, RowInfoOut ri) {
+  pdl_wait();
   // grid-stride version of write_row_info
   const int n = P + ri.T;
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
@@ -337,28 +392,35 @@ size_t permute_scratch_bytes(int T, int k, int E) {
 moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* inv_perm, int* status, void* scratch,
                           int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool pdl) {
   const int P = T * k;
   RowInfoOut ri{row_token, row_weight, topk_w, k, T, gofs};
   if (P <= kPermSingleMax) {
     const size_t smem = (2 * (size_t)E + 32) * sizeof(int);
-    permute_single_kernel<<<1, 1024, smem, s>>>(ids, P, E, counts, offsets, perm, inv_perm, status, ri);
+    cudaError_t e = launch_ex(pdl, permute_single_kernel, dim3(1), dim3(1024), smem, s, ids, P, E, counts,
+                              offsets, perm, inv_perm, status, ri);
+    if (e != cudaSuccess) return cuda_ok(e);
     count_launches(1);
     return cuda_ok(cudaGetLastError());
   }
   const int nchunks = (P + kPermChunk - 1) / kPermChunk;
   int32_t* hist = static_cast<int32_t*>(scratch);
-  permute_count_kernel<<<nchunks, 1024, (size_t)E * sizeof(int), s>>>(ids, P, E, hist, perm);
+  cudaError_t e = launch_ex(pdl, permute_count_kernel, dim3(nchunks), dim3(1024), (size_t)E * sizeof(int), s,
+                            ids, P, E, hist, perm);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
-  permute_scan_kernel<<<1, 1024, ((size_t)E + 32) * sizeof(int), s>>>(hist, nchunks, E, P, counts, offsets,
-                                                                      gofs, T);
+  e = launch_ex(pdl, permute_scan_kernel, dim3(1), dim3(1024), ((size_t)E + 32) * sizeof(int), s, hist,
+                nchunks, E, P, counts, offsets, gofs, T);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
-  permute_scatter_kernel<<<nchunks, 32, (size_t)E * sizeof(int), s>>>(ids, P, E, hist, perm, inv_perm,
-                                                                      status);
+  e = launch_ex(pdl, permute_scatter_kernel, dim3(nchunks), dim3(32), (size_t)E * sizeof(int), s, ids, P, E,
+                (const int32_t*)hist, perm, inv_perm, status);
+  if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   if (row_token != nullptr) {
     const int n = P + T;
-    row_info_kernel<<<(n + 255) / 256, 256, 0, s>>>(perm, P, ri);
+    e = launch_ex(pdl, row_info_kernel, dim3((n + 255) / 256), dim3(256), 0, s, (const int32_t*)perm, P, ri);
+    if (e != cudaSuccess) return cuda_ok(e);
     count_launches(1);
   }
   return cuda_ok(cudaGetLastError());
