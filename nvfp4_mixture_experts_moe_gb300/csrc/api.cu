@@ -83,6 +83,10 @@ struct ForwardWs {
   void* perm_scratch;
   uint16_t* h;        // [rows, I]
   uint16_t* y;        // [rows, H]
+  uint16_t* xf;       // W4A16, T above the small-group limit: f16 copy of x [T, H]
+  float* xmul;        // [T]
+  uint16_t* hf;       // f16 copy of h [rows, I]
+  float* hmul;        // [rows]
   uint8_t* xq;        // W4A4: [T, H/2]
   uint8_t* xsf;       // W4A4: [T, H/16]
   float* xgs;
@@ -111,6 +115,15 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
   f.perm_scratch = c.take<uint8_t>(permute_scratch_bytes(L.T, L.k, L.E));
   f.h = c.take<uint16_t>(rows * L.I);
   f.y = c.take<uint16_t>(rows * L.H);
+  if (L.mode == MOE_W4A16 && L.T > kSmallGroupRows) {
+    f.xf = c.take<uint16_t>((size_t)L.T * L.H);
+    f.xmul = c.take<float>(L.T);
+    f.hf = c.take<uint16_t>(rows * L.I);
+    f.hmul = c.take<float>(rows);
+  } else {
+    f.xf = f.hf = nullptr;
+    f.xmul = f.hmul = nullptr;
+  }
   if (L.mode == MOE_W4A4) {
     f.xq = c.take<uint8_t>((size_t)L.T * L.H / 2);
     f.xsf = c.take<uint8_t>((size_t)L.T * L.H / 16);
@@ -285,6 +298,7 @@ static moe_status run_gemm(const GemmPlan& p, long long max_group_rows, cudaStre
   if (p.mode == MOE_W4A4) return launch_gemm_tc_w4a4(p, s);
   moe_status st = launch_gemm_small_w4a16(p, kSmallGroupRows, s);
   if (st != MOE_OK || max_group_rows <= kSmallGroupRows) return st;
+  if (p.a_f16 != nullptr) return launch_gemm_tc_f16(p, kSmallGroupRows, s);
   return launch_gemm_tc_w4a16(p, kSmallGroupRows, s);
 }
 
@@ -326,6 +340,8 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   p.max_rows = 1 << 30;
   p.pdl = false;
   p.early_weights = false;
+  p.a_f16 = nullptr;
+  p.a_mul = nullptr;
   return run_gemm(p, 1LL << 30, (cudaStream_t)stream);
 }
 
@@ -403,6 +419,10 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     st = launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq, f.xsf, f.xgs, s, pdl);
     if (st != MOE_OK) return st;
   }
+  if (f.xf) {  // f16 copy of x for the large-group tensor-core GEMM
+    st = launch_rows_to_f16(x, T, H, f.xf, f.xmul, s, pdl);
+    if (st != MOE_OK) return st;
+  }
   stage_mark(3, s);
 
   const int G = E + (has_shared ? 1 : 0);
@@ -423,6 +443,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.a_row_index = f.row_token;
   g1.out = f.h;
   g1.out_amax = fp4 ? &f.hdr->amax[1] : nullptr;
+  g1.a_f16 = f.xf;
+  g1.a_mul = f.xmul;
   g1.status = &f.hdr->status;
   g1.max_rows = rows;
   g1.pdl = pdl;
@@ -432,6 +454,9 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   stage_mark(4, s);
   if (fp4) {  // h -> NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue)
     st = launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf, f.hgs, s, pdl);
+    if (st != MOE_OK) return st;
+  } else if (f.hf) {
+    st = launch_rows_to_f16(f.h, rows, I, f.hf, f.hmul, s, pdl);
     if (st != MOE_OK) return st;
   }
   stage_mark(5, s);
@@ -447,6 +472,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g2.a_sf = fp4 ? f.hsf : nullptr;
   g2.a_gs = fp4 ? f.hgs : nullptr;
   g2.out_amax = nullptr;
+  g2.a_f16 = f.hf;
+  g2.a_mul = f.hmul;
   g2.early_weights = true;  // group offsets come from the permutation, two launches back
   g2.a_row_index = nullptr;
   g2.row_scale = f.row_weight;

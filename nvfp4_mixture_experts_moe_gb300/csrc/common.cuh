@@ -7,7 +7,7 @@
 #include <stdint.h>
 #include <stddef.h>
 
-#include "../../include/moe_nvfp4.h"
+#include "moe_nvfp4.h"  // from include/, on the compiler include path
 
 namespace moe {
 

@@ -210,6 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
                                                                          : p.weights + (size_t)it.g * p.stride;
       const uint8_t* wdata = wblk + sizeof(PrepHeader);
       const uint8_t* wsf = wdata + w4a16_data_bytes(N, K);
+      // this thread's activation rows of the tile (chunk tau & 7 of rows tau/8 + 16q), loaded once
+      const uint16_t* asrc[kMaxBN / 16];
+#pragma unroll
+      for (int q = 0; q < kMaxBN / 16; ++q) {
+        const int n = (tau >> 3) + 16 * q;
+        asrc[q] = nullptr;
+        if (n < it.rows) {
+          const int r = it.row0 + n;
+          const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
+          asrc[q] = p.a + (size_t)arow * K + (tau & 7) * 8;
+        }
+      }
       for (int ks = 0; ks < KS; ++ks, ++j) {
         const int slot = j % kStages;
         if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) break;
@@ -221,15 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
                      "l"(wsf + bidx * 64 + g8 * 8)
                      : "memory");
         const uint32_t bt = smem_u32(b_tiles + slot * kBTileBytes);
-        for (int c = tau; c < it.bn * 8; c += kProducers) {
-          const int n = c >> 3, ch = c & 7;
-          const uint32_t dst = bt + n * kRowBytes + ((ch ^ (n & 7)) << 4);
-          if (n < it.rows) {
-            const int r = it.row0 + n;
-            const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
-            cp_async_16(dst, p.a + (size_t)arow * K + ks * kBK + ch * 8, 16);
-          } else {
-            cp_async_16(dst, p.a, 0);  // zero fill
+#pragma unroll
+        for (int q = 0; q < kMaxBN / 16; ++q) {
+          const int n = (tau >> 3) + 16 * q, ch = tau & 7;
+          if (n < it.bn) {
+            const uint32_t dst = bt + n * kRowBytes + ((ch ^ (n & 7)) << 4);
+            if (asrc[q] != nullptr) cp_async_16(dst, asrc[q] + ks * kBK, 16);
+            else cp_async_16(dst, p.a, 0);  // zero fill
           }
         }
         cp_async_commit();
@@ -255,10 +265,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
                                                                          : p.weights + (size_t)it.g * p.stride;
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wblk);
       const float a0 = hdr->alpha[0], a1 = hdr->alpha[1];
+      // routing weights of the tile's rows: lane l holds rows l, l + 32, ...
+      float rsv[kMaxBN / 32];
+#pragma unroll
+      for (int i = 0; i < kMaxBN / 32; ++i) {
+        const int n = 32 * i + lane;
+        rsv[i] = (!GATE_UP && p.row_scale && n < it.rows) ? __ldg(p.row_scale + it.row0 + n) : 1.0f;
+      }
       for (int c0 = 0; c0 < it.bn; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols + c0, r);
         tmem_ld_wait();
+        float rs_chunk = 1.0f;
+#pragma unroll
+        for (int i = 0; i < kMaxBN / 32; ++i)
+          if ((c0 >> 5) == i) rs_chunk = rsv[i];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const float v = __uint_as_float(r[c]);
@@ -270,10 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
               const float h = silu(v * a0) * (up * a1);
               p.out[(size_t)(it.row0 + n) * (N / 2) + f] = float_to_bf16_bits(h);
             }
-          } else if (n < it.rows) {
-            const int r0 = it.row0 + n;
-            const float rs = p.row_scale ? __ldg(p.row_scale + r0) : 1.0f;
-            p.out[(size_t)r0 * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0 * rs);
+          } else {
+            const float rs = __shfl_sync(0xffffffffu, rs_chunk, n & 31);
+            if (n < it.rows)
+              p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0 * rs);
           }
         }
       }
@@ -454,6 +475,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a4_kernel(TcFp4Args p) 
                                                                          : p.weights + (size_t)it.g * p.stride;
       const uint8_t* wdata = wblk + sizeof(PrepHeader);
       const uint8_t* wsf = wdata + (size_t)N * K / 2;
+      // this thread's activation rows (codes: chunk tau & 7 of rows tau/8 + 16q; scales: row tau)
+      const uint8_t* asrc[kFp4MaxBN / 16];
+#pragma unroll
+      for (int q = 0; q < kFp4MaxBN / 16; ++q) {
+        const int n = (tau >> 3) + 16 * q;
+        asrc[q] = nullptr;
+        if (n < it.rows) {
+          const int r = it.row0 + n;
+          const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
+          asrc[q] = p.a + (size_t)arow * (K / 2) + (tau & 7) * 16;
+        }
+      }
+      const uint8_t* sfsrc = nullptr;
+      if (tau < it.rows) {
+        const int r = it.row0 + tau;
+        const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
+        sfsrc = p.a_sf + (size_t)arow * (K / 16);
+      }
       for (int ks = 0; ks < KS; ++ks, ++j) {
         const int slot = j % kStages;
         if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) break;
@@ -470,33 +509,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a4_kernel(TcFp4Args p) 
         }
         // activation codes: bn rows x 8 chunks of 16 bytes
         const uint32_t bt = smem_u32(b_t);
-        for (int c = tau; c < it.bn * 8; c += kProducers) {
-          const int n = c >> 3, ch = c & 7;
-          const uint32_t dst = bt + n * kRowBytes + ((ch ^ (n & 7)) << 4);
-          if (n < it.rows) {
-            const int r = it.row0 + n;
-            const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
-            cp_async_16(dst, p.a + (size_t)arow * (K / 2) + ks * kRowBytes + ch * 16, 16);
-          } else {
-            cp_async_16(dst, p.a, 0);
+#pragma unroll
+        for (int q = 0; q < kFp4MaxBN / 16; ++q) {
+          const int n = (tau >> 3) + 16 * q, ch = tau & 7;
+          if (n < it.bn) {
+            const uint32_t dst = bt + n * kRowBytes + ((ch ^ (n & 7)) << 4);
+            if (asrc[q] != nullptr) cp_async_16(dst, asrc[q] + ks * kRowBytes, 16);
+            else cp_async_16(dst, p.a, 0);
           }
         }
-        cp_async_commit();
-        // activation scales: 16 per row per stage -> 4 bytes into each atom
+        // activation scales: 16 per row per stage, 4 bytes into each atom (async)
         if (tau < kFp4MaxBN) {
-          const int n = tau;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (n < it.rows) {
-            const int r = it.row0 + n;
-            const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
-            v = __ldg(reinterpret_cast<const uint4*>(p.a_sf + (size_t)arow * (K / 16) + ks * 16));
+          const int off = (tau & 31) * 16 + (tau >> 5) * 4;
+          if (sfsrc != nullptr) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sfb + kk * kSfAtom + off)),
+                           "l"(sfsrc + ks * 16 + 4 * kk)
+                           : "memory");
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) *reinterpret_cast<uint32_t*>(sfb + kk * kSfAtom + off) = 0u;
           }
-          const int off = (n & 31) * 16 + (n >> 5) * 4;
-          *reinterpret_cast<uint32_t*>(sfb + 0 * kSfAtom + off) = v.x;
-          *reinterpret_cast<uint32_t*>(sfb + 1 * kSfAtom + off) = v.y;
-          *reinterpret_cast<uint32_t*>(sfb + 2 * kSfAtom + off) = v.z;
-          *reinterpret_cast<uint32_t*>(sfb + 3 * kSfAtom + off) = v.w;
         }
+        cp_async_commit();  // codes and scales of this stage form one group
         if (j - fin >= kLookahead) {
           cp_async_wait<kLookahead>();
           finalize(fin++);
@@ -521,10 +557,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a4_kernel(TcFp4Args p) 
                                                                          : p.weights + (size_t)it.g * p.stride;
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wblk);
       const float a0 = hdr->alpha[0] * inv_gs_a, a1 = hdr->alpha[1] * inv_gs_a;
+      float rsv[kFp4MaxBN / 32];
+#pragma unroll
+      for (int i = 0; i < kFp4MaxBN / 32; ++i) {
+        const int n = 32 * i + lane;
+        rsv[i] = (!GATE_UP && p.row_scale && n < it.rows) ? __ldg(p.row_scale + it.row0 + n) : 1.0f;
+      }
       for (int c0 = 0; c0 < it.bn; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * kAccColsFp4 + c0, r);
         tmem_ld_wait();
+        float rs_chunk = 1.0f;
+#pragma unroll
+        for (int i = 0; i < kFp4MaxBN / 32; ++i)
+          if ((c0 >> 5) == i) rs_chunk = rsv[i];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const float v = __uint_as_float(r[c]);
@@ -537,10 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a4_kernel(TcFp4Args p) 
               p.out[(size_t)(it.row0 + n) * (N / 2) + f] = hb;
               amax = fmaxf(amax, fabsf(bf16_bits_to_float(hb)));
             }
-          } else if (n < it.rows) {
-            const int r0 = it.row0 + n;
-            const float rs = p.row_scale ? __ldg(p.row_scale + r0) : 1.0f;
-            p.out[(size_t)r0 * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0 * rs);
+          } else {
+            const float rs = __shfl_sync(0xffffffffu, rs_chunk, n & 31);
+            if (n < it.rows)
+              p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0 * rs);
           }
         }
       }

@@ -87,6 +87,8 @@ struct GemmPlan {
   const float* row_scale;
   uint16_t* out;
   float* out_amax;
+  const uint16_t* a_f16;    // W4A16 large groups: f16 copy of the A rows (rows_to_f16), or null
+  const float* a_mul;       // its per-row multipliers 2^-s
   int* status;
   int max_rows;             // upper bound of group_offsets[G] (sizes launches)
   bool pdl;                 // programmatic dependent launch (inside the fused forward)
@@ -101,6 +103,15 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& p, int rows_limit, cudaStream
 // Large-group path: tcgen05 MMA with TMEM accumulators. Handles groups with
 // rows > rows_min.
 moe_status launch_gemm_tc_w4a16(const GemmPlan& p, int rows_min, cudaStream_t s);
+
+// Large-group W4A16 path with the dequantised weights in TMEM; needs the f16
+// copy of the activation rows (a_f16, a_mul).
+moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
+
+// bf16 rows -> f16 rows scaled by a power of two so that each row's largest
+// magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it.
+moe_status launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, float* mul, cudaStream_t s,
+                              bool pdl = false);
 
 // W4A4: block-scaled FP4 tcgen05 kernel (every non-empty group).
 moe_status launch_gemm_tc_w4a4(const GemmPlan& p, cudaStream_t s);

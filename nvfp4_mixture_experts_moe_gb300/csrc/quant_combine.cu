@@ -143,6 +143,56 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
 }
 
 // ---------------------------------------------------------------------------
+// bf16 rows -> f16 rows with a power-of-two row scale (one warp per row).
+// With the row's largest magnitude in [2^14, 2^15) every bf16 value is exact
+// in f16 except magnitudes below 2^-24 of that maximum, which flush.
+__global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __restrict__ src, int rows, int K,
+                                                          uint16_t* __restrict__ dst, float* __restrict__ mul) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  if (row >= rows) return;
+  const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)row * K);
+  uint4* d = reinterpret_cast<uint4*>(dst + (size_t)row * K);
+  uint32_t m = 0;
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = __ldg(s + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (m > 0x7f80u) m = 0x7f80u;
+  const int e = (int)(m >> 7);
+  int sh = (m == 0) ? 0 : 141 - max(e, 1);
+  sh = max(-113, min(sh, 126));
+  const float up = __int_as_float((127 + sh) << 23);
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = __ldg(s + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * up, __uint_as_float(w[q] & 0xffff0000u) * up);
+      o[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    d[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) mul[row] = __int_as_float((127 - sh) << 23);
+}
+
+moe_status launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, float* mul, cudaStream_t s,
+                              bool pdl) {
+  if (rows == 0) return MOE_OK;
+  const int blocks = (int)(((size_t)rows * 32 + 255) / 256);
+  cudaError_t e = launch_ex(pdl, rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, rows, K, dst, mul);
+  if (e != cudaSuccess) return cuda_ok(e);
+  count_launches(1);
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
 // h = silu(gate) * up, gate in columns [0, I), up in [I, 2I).
 __global__ void swiglu_kernel(const float* __restrict__ gu, int rows, int I, uint16_t* __restrict__ h) {
   const size_t n = (size_t)rows * I;

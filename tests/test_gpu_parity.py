@@ -162,6 +162,20 @@ def test_forward_tiny_is_deterministic():
     assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
+@pytest.mark.parametrize("cfg", [
+    si.LayerConfig("mid4", T=300, H=512, I=256, I_s=256, E=4, k=2),     # groups ~150 rows: tensor-core path
+    si.LayerConfig("mid16", T=300, H=256, I=128, I_s=128, E=16, k=2),   # groups ~37 rows: both paths
+    si.LayerConfig("midz", T=160, H=256, I=192, I_s=192, E=24, k=4, logits="zipf"),  # skewed, empty groups
+])
+def test_forward_mid_full_check(cfg):
+    cfg, layer, x, logits, out, ids = run_forward(cfg)
+    ow = OracleWeights(cfg)
+    experts, shared = ow.all()
+    ref, parts = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k, return_parts=True)
+    assert (ids == parts["ids"]).all()
+    check_outputs(out, ref, what=cfg.name)
+
+
 def test_forward_decode_full_check():
     cfg, layer, x, logits, out, ids = run_forward("decode")
     ow = OracleWeights(cfg)
