@@ -116,8 +116,8 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
   f.h = c.take<uint16_t>(rows * L.I);
   f.y = c.take<uint16_t>(rows * L.H);
   if (L.mode == MOE_W4A16 && L.T > kSmallGroupRows) {
-    f.xf = c.take<uint16_t>((size_t)L.T * L.H);
-    f.xmul = c.take<float>(L.T);
+    f.xf = c.take<uint16_t>(rows * L.H);  // x rows in group order
+    f.xmul = c.take<float>(rows);
     f.hf = c.take<uint16_t>(rows * L.I);
     f.hmul = c.take<float>(rows);
   } else {
@@ -141,7 +141,7 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
 
 static size_t prep_size(int N, int K, moe_mode mode, int gate_up) {
   (void)gate_up;
-  if (mode == MOE_W4A16) return sizeof(PrepHeader) + w4a16_data_bytes(N, K) + w4a16_sf_bytes(N, K);
+  if (mode == MOE_W4A16) return sizeof(PrepHeader) + w4a16_bytes(N, K);
   return sizeof(PrepHeader) + (size_t)N * K / 2 + prepare_w4a4_sf_bytes(N, K);
 }
 
@@ -274,7 +274,7 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf, co
   if (st != MOE_OK) return st;
   uint8_t* data = o + sizeof(PrepHeader);
   if (mode == MOE_W4A16)
-    st = launch_prepare_w4a16(codes, sf, N, K, gate_up, data, data + w4a16_data_bytes(N, K), flag, s);
+    st = launch_prepare_w4a16(codes, sf, N, K, gate_up, data, flag, s);
   else
     st = launch_prepare_w4a4(codes, sf, N, K, gate_up, data, data + (size_t)N * K / 2, flag, s);
   if (st != MOE_OK) return st;
@@ -419,8 +419,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     st = launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq, f.xsf, f.xgs, s, pdl);
     if (st != MOE_OK) return st;
   }
-  if (f.xf) {  // f16 copy of x for the large-group tensor-core GEMM
-    st = launch_rows_to_f16(x, T, H, f.xf, f.xmul, s, pdl);
+  if (f.xf) {  // f16 copy of x, rows in group order, for the large-group tensor-core GEMM
+    st = launch_rows_to_f16(x, f.row_token, rows, H, f.xf, f.xmul, s, pdl);
     if (st != MOE_OK) return st;
   }
   stage_mark(3, s);
@@ -445,6 +445,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.out_amax = fp4 ? &f.hdr->amax[1] : nullptr;
   g1.a_f16 = f.xf;
   g1.a_mul = f.xmul;
+  g1.a_rows = rows;
   g1.status = &f.hdr->status;
   g1.max_rows = rows;
   g1.pdl = pdl;
@@ -456,7 +457,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     st = launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf, f.hgs, s, pdl);
     if (st != MOE_OK) return st;
   } else if (f.hf) {
-    st = launch_rows_to_f16(f.h, rows, I, f.hf, f.hmul, s, pdl);
+    st = launch_rows_to_f16(f.h, nullptr, rows, I, f.hf, f.hmul, s, pdl);
     if (st != MOE_OK) return st;
   }
   stage_mark(5, s);

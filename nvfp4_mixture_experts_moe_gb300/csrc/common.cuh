@@ -38,17 +38,21 @@ struct PrepHeader {
 };
 static_assert(sizeof(PrepHeader) == 256, "prepared header is 256 bytes");
 
-// W4A16 layout after the header: fragment-ordered codes, N/16 x K/64 blocks
-// of 512 bytes ([row tile][k block]); then the E4M3 scales, same blocks of
-// 64 bytes. Within a data block, lane L = 4*g + t of a warp owns bytes
+// W4A16 layout after the header: one chunk of 4608 bytes per (128-row tile
+// mt, 64-wide K block kb), at ((mt * K/64) + kb) * 4608, so that a tile's K
+// blocks follow one another: eight 512-byte blocks of fragment-ordered codes
+// (16-row blocks b = 0..7 of the tile, at 512 b), then their eight 64-byte
+// blocks of E4M3 scales (at 4096 + 64 b). Within a data block, lane L = 4*g + t of a warp owns bytes
 // [16L, 16L+16): word s (k16 step s of the block) holds, byte by byte, the
 // code pairs of (row g, k 16s+2t..+1), (row g+8, same k), (row g, k+8..+9),
 // (row g+8, k+8..+9) -- the A-fragment order of an m16n8k16 MMA. Within a
 // scale block, group g owns bytes [8g, 8g+8): for k16 step s = 0..3 the pair
 // (scale of row g, scale of row g+8), so one e4m3x2 conversion yields both
 // rows' scales of a step.
-__host__ __device__ inline size_t w4a16_data_bytes(int N, int K) { return (size_t)N * K / 2; }
-__host__ __device__ inline size_t w4a16_sf_bytes(int N, int K) { return (size_t)N * K / 16; }
+constexpr int kW16Chunk = 4608;   // bytes of one (128-row tile, 64-wide K block) chunk
+constexpr int kW16SfOff = 4096;   // scale blocks within a chunk
+__host__ __device__ inline size_t w4a16_bytes(int N, int K) { return (size_t)N * K / 2 + (size_t)N * K / 16; }
+__host__ __device__ inline size_t w4a16_chunk(int mt, int kb, int KB) { return ((size_t)mt * KB + kb) * kW16Chunk; }
 
 // ---------------------------------------------------------------------------
 // Small device helpers.

@@ -45,9 +45,7 @@ constexpr int kRowsPerPass = 8;
 constexpr int kTileRows = 128;                   // weight rows per item
 constexpr int kMaxGroups = 1025;
 constexpr int kBlocksPerStage = 8;               // 64-wide K blocks per stage (512 K)
-constexpr int kStageData = kMmaWarps * kBlocksPerStage * 512;  // 32 KB
-constexpr int kStageSf = kMmaWarps * kBlocksPerStage * 64;     // 4 KB
-constexpr int kStageBytes = kStageData + kStageSf;
+constexpr int kStageBytes = kBlocksPerStage * kW16Chunk;     // 36 KB: the item's chunks of 8 K blocks
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
 
 struct SmallArgs {
@@ -157,20 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
         const uint8_t* blk = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
                                                                       : p.weights + (size_t)g * p.stride;
         const uint8_t* data = blk + sizeof(PrepHeader);
-        const uint8_t* sfp = data + w4a16_data_bytes(N, K);
         for (int st = 0; st < nstage; ++st, ++j) {
           const int slot = j % S;
           if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, kWaitLimit)) break;
           const int kb0 = st * kBlocksPerStage;
           const int nkb = min(kBlocksPerStage, kblocks - kb0);
-          mbar_arrive_expect_tx(&sm->full[slot], (uint32_t)(kMmaWarps * nkb * (512 + 64)));
-          uint8_t* sd = stages + (size_t)slot * kStageBytes;
-          for (int w = 0; w < kMmaWarps; ++w) {
-            const size_t b = (size_t)(mt * 8 + w) * kblocks + kb0;
-            bulk_g2s(smem_u32(sd + w * kBlocksPerStage * 512), data + b * 512, nkb * 512, &sm->full[slot]);
-            bulk_g2s(smem_u32(sd + kStageData + w * kBlocksPerStage * 64), sfp + b * 64, nkb * 64,
-                     &sm->full[slot]);
-          }
+          const uint32_t bytes = (uint32_t)(nkb * kW16Chunk);
+          mbar_arrive_expect_tx(&sm->full[slot], bytes);
+          bulk_g2s(smem_u32(stages + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, kblocks), bytes,
+                   &sm->full[slot]);
         }
       }
     }
@@ -256,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       const int kb0 = st * kBlocksPerStage;
       const int nkb = min(kBlocksPerStage, kblocks - kb0);
       const uint8_t* sd = stages + (size_t)slot * kStageBytes;
-      const uint8_t* my_data = sd + warp * kBlocksPerStage * 512 + lane * 16;
-      const uint8_t* my_sf = sd + kStageData + warp * kBlocksPerStage * 64 + g8 * 8;
+      const uint8_t* my_data = sd + warp * 512 + lane * 16;
+      const uint8_t* my_sf = sd + kW16SfOff + warp * 64 + g8 * 8;
 #pragma unroll 2
       for (int kb = 0; kb < nkb; ++kb) {
-        const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * 512);
-        const uint2 sq = *reinterpret_cast<const uint2*>(my_sf + kb * 64);
+        const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * kW16Chunk);
+        const uint2 sq = *reinterpret_cast<const uint2*>(my_sf + kb * kW16Chunk);
         const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
         // B fragments of the 4 k16 steps: two ldmatrix.x4 (steps 0-1, 2-3)
         uint32_t bf[8];

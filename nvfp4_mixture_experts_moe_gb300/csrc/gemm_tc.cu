@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
       const uint8_t* wblk = (it.g == G - 1 && p.last_weights != nullptr) ? p.last_weights
                                                                          : p.weights + (size_t)it.g * p.stride;
       const uint8_t* wdata = wblk + sizeof(PrepHeader);
-      const uint8_t* wsf = wdata + w4a16_data_bytes(N, K);
       // this thread's activation rows of the tile (chunk tau & 7 of rows tau/8 + 16q), loaded once
       const uint16_t* asrc[kMaxBN / 16];
 #pragma unroll
@@ -226,11 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_w4a16_kernel(TcArgs p) {
         const int slot = j % kStages;
         if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) break;
         uint8_t* rw = raw + slot * kRawBytes;
-        const size_t bidx = (size_t)(it.mt * 8 + blk) * KS + ks;
-        cp_async_16(smem_u32(rw + blk * 512 + L * 16), wdata + bidx * 512 + L * 16, 16);
-        cp_async_16(smem_u32(rw + blk * 512 + L * 16 + 16), wdata + bidx * 512 + L * 16 + 16, 16);
+        const uint8_t* chunk = wdata + w4a16_chunk(it.mt, ks, KS);
+        cp_async_16(smem_u32(rw + blk * 512 + L * 16), chunk + blk * 512 + L * 16, 16);
+        cp_async_16(smem_u32(rw + blk * 512 + L * 16 + 16), chunk + blk * 512 + L * 16 + 16, 16);
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(rw + kRawData + tau * 8)),
-                     "l"(wsf + bidx * 64 + g8 * 8)
+                     "l"(chunk + kW16SfOff + blk * 64 + g8 * 8)
                      : "memory");
         const uint32_t bt = smem_u32(b_tiles + slot * kBTileBytes);
 #pragma unroll

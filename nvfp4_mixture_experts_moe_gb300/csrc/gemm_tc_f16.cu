@@ -7,27 +7,39 @@
 // 16-bit inside the GEMM) and section 6.1 (alpha = 1/gs).
 //
 // Swap-AB tile: 128 weight rows are the MMA's M side, up to 128 rows of one
-// expert group its N side. Producer warp q (lanes 32q..32q+31 of TMEM) owns
-// 32 weight rows: each thread copies its row's raw e2m1 codes and E4M3
-// scales for a 64-wide K stage into shared memory (cp.async), rebuilds the
-// row from the m16n8k16 fragment layout with one register exchange with its
-// partner row (lane ^ 8), converts to f16 with the hardware e2m1x2
-// conversion, multiplies by the block scale (exact in f16) and writes the 32
-// columns straight into TMEM with tcgen05.st. The MMA (kind::f16) reads A
-// from TMEM and the activation rows from 128B-swizzled shared memory, so the
-// dequantised weights never cross shared memory.
+// expert group its N side, K in stages of 128 (two 64-wide halves).
 //
-// The activation rows are f16 with a power-of-two row scale (the f16 copy
-// from rows_to_f16); the epilogue multiplies by the row's 2^-s, alpha, and
-// the routing weight (GEMM 2) or applies SwiGLU (GEMM 1).
+// * Two loader warps move each stage with the tensor-memory-access engine:
+//   one copies the stage's two 4608-byte chunks of raw e2m1 codes and E4M3
+//   scales (one bulk copy) into a ring of eight raw slots; the other loads the
+//   group's activation rows, one box per K half (16, 32, 64 or 128 rows, the
+//   smallest that covers the tile, through tensor maps over the f16
+//   activation matrix, whose rows are in group order; 128-byte swizzle). Box
+//   rows past the end of the matrix read as zero; rows of the next group that
+//   fill a box are computed and not stored. A TMA or bulk instruction costs
+//   its issuing thread tens of cycles and an mbarrier wait more than a
+//   hundred, so a stage is few large copies and a 128-wide K step.
+// * Eight dequant warps (two sets of four that take alternate stages; warp q
+//   of a set owns TMEM lanes 32q..32q+31) rebuild their weight row from the
+//   m16n8k16 fragment layout with one register exchange with the partner row
+//   (lane ^ 8), convert with the hardware e2m1x2 conversion, multiply by the
+//   block scale (exact in f16) and write the stage's 64 columns into TMEM
+//   with tcgen05.st.
+// * One thread issues tcgen05.mma (kind::f16, A from TMEM, B from shared
+//   memory, fp32 accumulators in TMEM): one wait, eight MMAs and one commit
+//   per stage.
+// * Four epilogue warps read the accumulators (tcgen05.ld), multiply by the
+//   activation row's 2^-s (the f16 copy's power-of-two scale), alpha and the
+//   routing weight (GEMM 2) or apply SwiGLU (GEMM 1), and store bf16.
 //
-// Warps: 0-7 producers in two sets of four that take alternate stages (the
-// dependent chain load -> exchange -> convert -> tcgen05.st of one stage is
-// long; two warps per scheduler overlap it), 8-11 epilogue (TMEM lane
-// quarters), 12 MMA. Eight pipeline stages, two accumulator buffers of 128
-// columns, eight A stages of 32 columns in TMEM. Every wait
-// is bounded; on a timeout the kernel records MOE_ERR_TIMEOUT, drains, frees
-// TMEM and exits.
+// TMEM: two accumulator buffers of 128 columns and four A stages of 64
+// columns. Every wait is bounded; on a timeout the kernel records
+// MOE_ERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
@@ -38,23 +50,31 @@ namespace {
 using namespace tc;
 
 constexpr int kM = 128;
-constexpr int kBK = 64;
-constexpr int kRowBytes = 128;       // one B row per stage: 64 f16
-constexpr int kStages = 8;
-constexpr int kLookahead = 3;        // per producer set; two sets alternate stages
+constexpr int kBK = 128;                     // K per stage
+constexpr int kHalf = 64;                    // K per box / per 128-byte swizzled row
+constexpr int kRowBytes = 128;
+constexpr int kStages = 4;                   // activation tiles and TMEM A stages
+constexpr int kRawSlots = 8;                 // raw weight stages
 constexpr int kMaxBN = 128;
-constexpr int kProducerWarps = 8;    // two sets of four (one TMEM lane quarter each)
-constexpr int kEpiWarp0 = kProducerWarps;
-constexpr int kMmaWarp = kProducerWarps + 4;
+constexpr int kWLoadWarp = 0;
+constexpr int kBLoadWarp = 1;
+constexpr int kDeqWarp0 = 2;                 // warps 2..9: two dequant sets
+constexpr int kEpiWarp0 = 10;                // warps 10..13
+constexpr int kMmaWarp = 14;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kProducers = 128;      // threads per producer set
-constexpr int kBTile = kMaxBN * kRowBytes;  // 16 KB
-constexpr int kRawPerThread = 48;           // 32 B codes + 8 B scales, padded to 16
-constexpr int kRawStage = kProducers * kRawPerThread;
-static_assert(2 * kLookahead < kStages, "both sets' copies in flight must fit the ring");
+constexpr int kBHalf = kMaxBN * kRowBytes;   // 16 KB: one K half of the activation tile
+constexpr int kBStage = 2 * kBHalf;
+constexpr int kRawStage = 2 * kW16Chunk;     // two (128-row, 64-K) chunks
 constexpr uint32_t kAccCols = 128;
-constexpr uint32_t kAcol0 = 256;            // A stages: columns [256, 256 + 32 * kStages)
+constexpr uint32_t kAcol0 = 256;             // A stages: columns [256, 256 + 64 * kStages)
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
+static_assert(kAcol0 + 64 * kStages <= 512, "TMEM columns");
+
+// Tensor maps over the f16 activation matrix with boxes of 16, 32, 64 and
+// 128 rows (64 columns each).
+struct BoxMaps {
+  CUtensorMap m[4];
+};
 
 struct Args {
   const uint8_t* weights;
@@ -62,9 +82,7 @@ struct Args {
   const uint8_t* last_weights;
   int G, N, K;
   const int32_t* group_offsets;
-  const uint16_t* a;       // f16 rows [*, K]
-  const float* a_mul;      // per A row multiplier (2^-s)
-  const int32_t* a_row_index;
+  const float* a_mul;      // per A row multiplier (2^-s), group order
   const float* row_scale;
   uint16_t* out;
   int rows_min;
@@ -72,8 +90,10 @@ struct Args {
 };
 
 struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t w_full[kRawSlots];   // raw weights of the stage landed
+  uint64_t w_empty[kRawSlots];  // the dequant set is done reading them
+  uint64_t ready[kStages];      // activation rows landed (bytes) and the four dequant warps done
+  uint64_t empty[kStages];      // the stage's MMAs completed (activation tile and TMEM A free)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -103,21 +123,31 @@ __device__ __forceinline__ Item decode_item(int idx, const int* pref, int G, int
   return it;
 }
 
-__device__ __forceinline__ uint32_t byte_of(uint32_t w, int b) { return (w >> (8 * b)) & 0xffu; }
+__device__ __forceinline__ const uint8_t* weight_block(const Args& p, int g) {
+  return (g == p.G - 1 && p.last_weights != nullptr) ? p.last_weights : p.weights + (size_t)g * p.stride;
+}
+
+// Bounded wait that ignores the abort flag (draining after a timeout).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitLimit) {
+  }
+}
 
 template <bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_constant__ BoxMaps maps, Args p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* b_tiles = base;                               // kStages x 16 KB
-  uint8_t* raw = b_tiles + kStages * kBTile;             // kStages x 6 KB
-  Smem* sm = reinterpret_cast<Smem*>(raw + kStages * kRawStage);
+  uint8_t* b_tiles = base;                               // kStages x 32 KB
+  uint8_t* raw = b_tiles + kStages * kBStage;            // kRawSlots x 9 KB
+  Smem* sm = reinterpret_cast<Smem*>(raw + kRawSlots * kRawStage);
   int* pref = reinterpret_cast<int*>(sm + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G, K = p.K, N = p.N;
   const int MT = N / kM;
-  const int KS = K / kBK;
+  const int KS = (K + kBK - 1) / kBK;     // the last stage has one half when K % 128 == 64
+  const int KB64 = K / kHalf;
   pdl_wait();
 
   for (int g = tid; g < G; g += kThreads) {
@@ -126,8 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
   }
   if (tid == 0) {
     pref[0] = 0;
+    for (int i = 0; i < kRawSlots; ++i) {
+      mbar_init(&sm->w_full[i], 1);
+      mbar_init(&sm->w_empty[i], 4);
+    }
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm->full[i], kProducers);
+      mbar_init(&sm->ready[i], 4 + 1);
       mbar_init(&sm->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -161,107 +195,121 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
   const int total = pref[G];
   volatile int* abort = &sm->abort;
 
-  if (warp < kProducerWarps) {
-    // ------------------------------------------------------------- producers
-    const int set = warp >> 2;                   // this set takes the stages j with j % 2 == set
-    const int tau = tid & (kProducers - 1);      // TMEM lane = weight row in the tile
-    const int blk = tau >> 4, g8 = tau & 7, hi = (tau >> 3) & 1;
-    const uint32_t lane_taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    // byte selectors: the partner needs bytes (1-hi) and (3-hi) of my two
-    // fragment words, I keep bytes hi and 2+hi
-    const uint32_t sel_send = (uint32_t)((1 - hi) | ((5 - hi) << 4) | ((3 - hi) << 8) | ((7 - hi) << 12));
-    const uint32_t sel_keep = (uint32_t)(hi | ((4 + hi) << 4) | ((2 + hi) << 8) | ((6 + hi) << 12));
-    int j = 0, fin = set, pending = 0;
-    auto finalize = [&](int i) {
-      const int slot = i % kStages;
-      const uint8_t* rw = raw + slot * kRawStage + tau * kRawPerThread;
-      const uint4 wa4 = *reinterpret_cast<const uint4*>(rw);        // fragment lane 4g + 2hi
-      const uint4 wb4 = *reinterpret_cast<const uint4*>(rw + 16);   // fragment lane 4g + 2hi + 1
-      const uint2 sc = *reinterpret_cast<const uint2*>(rw + 32);
-      const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
-      const uint32_t wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
-      uint32_t col[32];
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint32_t keep = __byte_perm(wa[s], wb[s], sel_keep);
-        const uint32_t recv = __shfl_xor_sync(0xffffffffu, __byte_perm(wa[s], wb[s], sel_send), 8);
-        // bytes of lanes t = 0..3 for k 16s + 2t (lo) and 16s + 8 + 2t (hi)
-        const uint32_t lo = hi ? __byte_perm(recv, keep, 0x5410) : __byte_perm(keep, recv, 0x5410);
-        const uint32_t hh = hi ? __byte_perm(recv, keep, 0x7632) : __byte_perm(keep, recv, 0x7632);
-        const int sb = 2 * (s & 1) + hi;  // my scale byte of step s
-        const uint32_t sw = s < 2 ? sc.x : sc.y;
-        const uint32_t scale = cvt_e4m3x2_f16x2(__byte_perm(sw, 0, sb | (sb << 4)));
-        uint32_t flo[4], fhi[4];
-        cvt_e2m1x8_f16(lo, flo);
-        cvt_e2m1x8_f16(hh, fhi);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          col[8 * s + t] = hmul2_u32(flo[t], scale);
-          col[8 * s + 4 + t] = hmul2_u32(fhi[t], scale);
+  if (warp == kWLoadWarp) {
+    // --------------------------------------------------------- weight loader
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        const Item it = decode_item(item, pref, G, MT, p.group_offsets);
+        const uint8_t* wdata = weight_block(p, it.g) + sizeof(PrepHeader);
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int rs = j % kRawSlots;
+          if (!mbar_wait(&sm->w_empty[rs], ((j / kRawSlots) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          const uint32_t bytes = (uint32_t)(min(2, KB64 - 2 * ks) * kW16Chunk);
+          mbar_arrive_expect_tx(&sm->w_full[rs], bytes);
+          bulk_g2s(smem_u32(raw + rs * kRawStage), wdata + w4a16_chunk(it.mt, 2 * ks, KB64), bytes, &sm->w_full[rs]);
         }
+        if (!ok) break;
       }
-      tmem_st32(lane_taddr + kAcol0 + slot * 32, col);
-      fence_proxy_async_smem();  // the cp.async activation rows of this stage, for the tensor core
-      tc_fence_before();
-      mbar_arrive(&sm->full[slot]);
-    };
-    for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-      const Item it = decode_item(item, pref, G, MT, p.group_offsets);
-      const uint8_t* wblk = (it.g == G - 1 && p.last_weights != nullptr) ? p.last_weights
-                                                                         : p.weights + (size_t)it.g * p.stride;
-      const uint8_t* wdata = wblk + sizeof(PrepHeader);
-      const uint8_t* wsf = wdata + w4a16_data_bytes(N, K);
-      const uint16_t* asrc[kMaxBN / 16];
-#pragma unroll
-      for (int q = 0; q < kMaxBN / 16; ++q) {
-        const int n = (tau >> 3) + 16 * q;
-        asrc[q] = nullptr;
-        if (n < it.rows) {
-          const int r = it.row0 + n;
-          const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
-          asrc[q] = p.a + (size_t)arow * K + (tau & 7) * 8;
+      if (*abort)  // let copies in flight land before the shared memory is released
+        for (int i = max(0, j - kRawSlots); i < j; ++i) drain_wait(&sm->w_full[i % kRawSlots], (i / kRawSlots) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kBLoadWarp) {
+    // ----------------------------------------------------- activation loader
+    if (lane < 4) tma_prefetch_map(&maps.m[lane]);
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        const Item it = decode_item(item, pref, G, MT, p.group_offsets);
+        const int q = 32 - __clz((it.bn >> 4) - 1);   // box of 16 << q >= bn rows
+        const uint32_t half_bytes = (uint32_t)((16 << q) * kRowBytes);
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kStages;
+          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          const int nh = min(2, KB64 - 2 * ks);
+          mbar_arrive_expect_tx(&sm->ready[slot], nh * half_bytes);
+          const uint32_t dst = smem_u32(b_tiles + slot * kBStage);
+          for (int h = 0; h < nh; ++h)
+            tma_load_2d(dst + h * kBHalf, &maps.m[q], (2 * ks + h) * kHalf, it.row0, &sm->ready[slot]);
         }
+        if (!ok) break;
       }
-      for (int ks = 0; ks < KS; ++ks, ++j) {
-        if ((j & 1) != set) continue;
-        const int slot = j % kStages;
-        if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) break;
-        uint8_t* rw = raw + slot * kRawStage + tau * kRawPerThread;
-        const size_t bidx = (size_t)(it.mt * 8 + blk) * KS + ks;
-        const uint8_t* src = wdata + bidx * 512 + (4 * g8 + 2 * hi) * 16;
-        cp_async_16(smem_u32(rw), src, 16);
-        cp_async_16(smem_u32(rw + 16), src + 16, 16);
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(rw + 32)),
-                     "l"(wsf + bidx * 64 + g8 * 8)
-                     : "memory");
-        const uint32_t bt = smem_u32(b_tiles + slot * kBTile);
-#pragma unroll
-        for (int q = 0; q < kMaxBN / 16; ++q) {
-          const int n = (tau >> 3) + 16 * q, ch = tau & 7;
-          if (n < it.bn) {
-            const uint32_t dst = bt + n * kRowBytes + ((ch ^ (n & 7)) << 4);
-            if (asrc[q] != nullptr) cp_async_16(dst, asrc[q] + ks * kBK, 16);
-            else cp_async_16(dst, p.a, 0);  // zero fill
-          }
-        }
-        cp_async_commit();
-        if (++pending > kLookahead) {
-          cp_async_wait<kLookahead>();
-          finalize(fin);
-          fin += 2;
-          --pending;
+      if (*abort) {  // the boxes share their barrier with the dequant warps: allow them ~0.1 ms to land
+        const long long t0 = clock64();
+        while (clock64() - t0 < 200000) {
         }
       }
     }
-    cp_async_wait_all();
-    while (pending > 0) {
-      finalize(fin);
-      fin += 2;
-      --pending;
+    __syncwarp();
+  } else if (warp < kEpiWarp0) {
+    // --------------------------------------------------------------- dequant
+    const int set = (warp - kDeqWarp0) >> 2;     // takes the stages j with j % 2 == set
+    const int q = warp & 3;                      // TMEM lane quarter of this warp
+    const int tau = q * 32 + lane;               // weight row of the tile
+    const int blk = tau >> 4, g8 = tau & 7, hi = (tau >> 3) & 1;
+    const uint32_t lane_taddr = tmem + ((uint32_t)(q * 32) << 16);
+    // the partner row needs bytes (1-hi) and (3-hi) of my two fragment words;
+    // I keep bytes hi and 2+hi
+    const uint32_t sel_send = (uint32_t)((1 - hi) | ((5 - hi) << 4) | ((3 - hi) << 8) | ((7 - hi) << 12));
+    const uint32_t sel_keep = (uint32_t)(hi | ((4 + hi) << 4) | ((2 + hi) << 8) | ((6 + hi) << 12));
+    int j = 0;
+    for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+      bool ok = true;
+      for (int ks = 0; ks < KS; ++ks, ++j) {
+        if ((j & 1) != set) continue;
+        const int slot = j % kStages, rslot = j % kRawSlots;
+        if (!mbar_wait(&sm->w_full[rslot], (j / kRawSlots) & 1, abort, kWaitLimit) ||
+            !mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int nh = min(2, KB64 - 2 * ks);
+        for (int h = 0; h < nh; ++h) {
+          const uint8_t* rs = raw + rslot * kRawStage + h * kW16Chunk;
+          const uint4 wa4 = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16);
+          const uint4 wb4 = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16 + 16);
+          const uint2 sc = *reinterpret_cast<const uint2*>(rs + kW16SfOff + blk * 64 + g8 * 8);
+          if (h == nh - 1) {  // raw slot read completely
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm->w_empty[rslot]);
+          }
+          const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
+          const uint32_t wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
+          uint32_t col[32];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint32_t keep = __byte_perm(wa[s], wb[s], sel_keep);
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, __byte_perm(wa[s], wb[s], sel_send), 8);
+            // bytes of fragment lanes t = 0..3 for k 16s + 2t (lo) and 16s + 8 + 2t (hh)
+            const uint32_t lo = hi ? __byte_perm(recv, keep, 0x5410) : __byte_perm(keep, recv, 0x5410);
+            const uint32_t hh = hi ? __byte_perm(recv, keep, 0x7632) : __byte_perm(keep, recv, 0x7632);
+            const int sb = 2 * (s & 1) + hi;  // my scale byte of step s
+            const uint32_t sw = s < 2 ? sc.x : sc.y;
+            const uint32_t scale = cvt_e4m3x2_f16x2(__byte_perm(sw, 0, sb | (sb << 4)));
+            uint32_t flo[4], fhi[4];
+            cvt_e2m1x8_f16(lo, flo);
+            cvt_e2m1x8_f16(hh, fhi);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              col[8 * s + t] = hmul2_u32(flo[t], scale);
+              col[8 * s + 4 + t] = hmul2_u32(fhi[t], scale);
+            }
+          }
+          tmem_st32(lane_taddr + kAcol0 + slot * 64 + h * 32, col);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->ready[slot]);
+      }
+      if (!ok) break;
     }
   } else if (warp < kMmaWarp) {
     // -------------------------------------------------------------- epilogue
-    const int q = warp - kEpiWarp0;
+    const int q = warp & 3;
     const int rho = q * 32 + lane;
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
@@ -275,17 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
         float m = 0.0f;
         if (n < it.rows) {
           const int r = it.row0 + n;
-          const int arow = p.a_row_index ? __ldg(p.a_row_index + r) : r;
-          m = __ldg(p.a_mul + arow);
+          m = __ldg(p.a_mul + r);
           if (!GATE_UP && p.row_scale) m *= __ldg(p.row_scale + r);
         }
         mulv[i] = m;
       }
       if (!mbar_wait(&sm->tfull[acc], (itc >> 1) & 1, abort, kWaitLimit)) break;
       tc_fence_after();
-      const uint8_t* wblk = (it.g == G - 1 && p.last_weights != nullptr) ? p.last_weights
-                                                                         : p.weights + (size_t)it.g * p.stride;
-      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wblk);
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
       const float a0 = hdr->alpha[0], a1 = hdr->alpha[1];
       for (int c0 = 0; c0 < it.bn; c0 += 16) {
         uint32_t r[16];
@@ -317,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
   } else {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
+      const uint64_t bdesc0 = smem_desc(smem_u32(b_tiles), 16, 1024, kSwizzle128B);  // + 2 per 32-byte K step
       int j = 0, itc = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
         const Item it = decode_item(item, pref, G, MT, p.group_offsets);
@@ -328,14 +374,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->full[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, kWaitLimit)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t bs = smem_u32(b_tiles + slot * kBTile);
-          const uint32_t a_t = tmem + kAcol0 + slot * 32;
+          const uint64_t bd = bdesc0 + (uint64_t)((slot * kBStage) >> 4);
+          const uint32_t a_t = tmem + kAcol0 + slot * 64;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
-            mma_f16_tmem_a(d, a_t + kk * 8, bd, idesc, (ks | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) mma_f16_tmem_a(d, a_t + kk * 8, bd + 2 * kk, idesc, (ks | kk) != 0);
+          if (2 * ks + 1 < KB64) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_tmem_a(d, a_t + 32 + kk * 8, bd + (kBHalf >> 4) + 2 * kk, idesc, 1);
           }
           tc_commit(&sm->empty[slot]);
         }
@@ -343,9 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
         tc_commit(&sm->tfull[acc]);
       }
       tc_commit(&sm->drain);
-      const long long t0 = clock64();
-      while (!mbar_try_wait(&sm->drain, 0) && clock64() - t0 < kWaitLimit) {
-      }
+      drain_wait(&sm->drain, 0);
     }
     __syncwarp();
   }
@@ -356,15 +405,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(Args p) {
   if (tid == 0 && sm->abort) set_status(p.status, MOE_ERR_TIMEOUT);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
 }  // namespace
 
 static size_t smem_bytes(int G) {
-  return 1024 + (size_t)kStages * (kBTile + kRawStage) + sizeof(Smem) + (size_t)(G + 1) * 4;
+  return 1024 + (size_t)kStages * kBStage + (size_t)kRawSlots * kRawStage + sizeof(Smem) + (size_t)(G + 1) * 4;
 }
 
 moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) {
   if (pl.num_groups <= 0) return MOE_OK;
-  if (pl.a_f16 == nullptr || pl.a_mul == nullptr) return MOE_ERR_INVALID_ARG;
+  if (pl.a_f16 == nullptr || pl.a_mul == nullptr || pl.a_rows <= 0) return MOE_ERR_INVALID_ARG;
+  auto encode = encode_tiled();
+  if (encode == nullptr) return MOE_ERR_CUDA;
+  // the f16 activation matrix [a_rows, K] in group order: boxes of 16..128 rows x 64 elements, 128-byte swizzle
+  BoxMaps maps;
+  for (int q = 0; q < 4; ++q) {
+    const cuuint64_t dims[2] = {(cuuint64_t)pl.K, (cuuint64_t)pl.a_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pl.K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kHalf, (cuuint32_t)(16 << q)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&maps.m[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(pl.a_f16), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_ERR_INVALID_ARG;
+  }
   Args a;
   a.weights = pl.weights;
   a.stride = pl.weight_stride;
@@ -373,9 +450,7 @@ moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) 
   a.N = pl.N;
   a.K = pl.K;
   a.group_offsets = pl.group_offsets;
-  a.a = pl.a_f16;
   a.a_mul = pl.a_mul;
-  a.a_row_index = pl.a_row_index;
   a.row_scale = pl.row_scale;
   a.out = pl.out;
   a.rows_min = rows_min;
@@ -387,7 +462,7 @@ moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   auto k = pl.gate_up ? gemm_tc_f16_kernel<true> : gemm_tc_f16_kernel<false>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(kThreads), smem, s, a);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(kThreads), smem, s, maps, a);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;

@@ -65,7 +65,7 @@ moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const floa
 
 // Weight preparation (device part; the host validates sizes and scales).
 moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
-                                uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s);
+                                uint8_t* out, int* flag, cudaStream_t s);
 moe_status launch_prepare_w4a4(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
                                uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s);
 size_t prepare_w4a4_sf_bytes(int N, int K);
@@ -87,8 +87,10 @@ struct GemmPlan {
   const float* row_scale;
   uint16_t* out;
   float* out_amax;
-  const uint16_t* a_f16;    // W4A16 large groups: f16 copy of the A rows (rows_to_f16), or null
+  const uint16_t* a_f16;    // W4A16 large groups: f16 copy of the A rows in group order
+                            // (row r of the grouped layout; rows_to_f16), or null
   const float* a_mul;       // its per-row multipliers 2^-s
+  int a_rows;               // rows of a_f16
   int* status;
   int max_rows;             // upper bound of group_offsets[G] (sizes launches)
   bool pdl;                 // programmatic dependent launch (inside the fused forward)
@@ -109,9 +111,10 @@ moe_status launch_gemm_tc_w4a16(const GemmPlan& p, int rows_min, cudaStream_t s)
 moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
 
 // bf16 rows -> f16 rows scaled by a power of two so that each row's largest
-// magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it.
-moe_status launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, float* mul, cudaStream_t s,
-                              bool pdl = false);
+// magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it. Row r of dst is
+// row src_index[r] of src (row r when src_index is null).
+moe_status launch_rows_to_f16(const uint16_t* src, const int32_t* src_index, int rows, int K, uint16_t* dst,
+                              float* mul, cudaStream_t s, bool pdl = false);
 
 // W4A4: block-scaled FP4 tcgen05 kernel (every non-empty group).
 moe_status launch_gemm_tc_w4a4(const GemmPlan& p, cudaStream_t s);

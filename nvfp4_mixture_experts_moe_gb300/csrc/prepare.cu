@@ -21,7 +21,7 @@ __device__ __forceinline__ void check_sf(uint8_t v, int* flag) {
   if ((v & 0x80u) || v == 0x7fu) atomicOr(flag, 1);
 }
 
-// One thread per output byte of the fragment-ordered codes.
+// One thread per byte of fragment-ordered codes (block mb = 16 rows, kb).
 __global__ void prepare_w4a16_data_kernel(const uint8_t* __restrict__ codes, int N, int K, int gate_up,
                                           uint8_t* __restrict__ out) {
   const size_t total = (size_t)N * K / 2;
@@ -35,7 +35,8 @@ __global__ void prepare_w4a16_data_kernel(const uint8_t* __restrict__ codes, int
     const int g = lane >> 2, t = lane & 3;
     const int r = 16 * mb + g + ((b & 1) ? 8 : 0);
     const int k = 64 * kb + 16 * s + 2 * t + ((b & 2) ? 8 : 0);
-    out[i] = codes[(size_t)src_row(r, N, gate_up) * (K / 2) + k / 2];
+    out[w4a16_chunk(mb >> 3, kb, kblocks) + (mb & 7) * 512 + within] =
+        codes[(size_t)src_row(r, N, gate_up) * (K / 2) + k / 2];
   }
 }
 
@@ -53,15 +54,15 @@ __global__ void prepare_w4a16_sf_kernel(const uint8_t* __restrict__ sf, int N, i
     const int r = 16 * mb + g + 8 * half;
     const uint8_t v = sf[(size_t)src_row(r, N, gate_up) * (K / 16) + 4 * kb + j];
     check_sf(v, flag);
-    out[i] = v;
+    out[w4a16_chunk(mb >> 3, kb, kblocks) + kW16SfOff + (mb & 7) * 64 + within] = v;
   }
 }
 
 moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
-                                uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s) {
-  prepare_w4a16_data_kernel<<<1024, 256, 0, s>>>(codes, N, K, gate_up, out_data);
+                                uint8_t* out, int* flag, cudaStream_t s) {
+  prepare_w4a16_data_kernel<<<1024, 256, 0, s>>>(codes, N, K, gate_up, out);
   count_launches(1);
-  prepare_w4a16_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out_sf, flag);
+  prepare_w4a16_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out, flag);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }

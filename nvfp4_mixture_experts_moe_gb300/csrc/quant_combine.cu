@@ -143,16 +143,19 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
 }
 
 // ---------------------------------------------------------------------------
-// bf16 rows -> f16 rows with a power-of-two row scale (one warp per row).
+// bf16 rows -> f16 rows with a power-of-two row scale (one warp per row);
+// dst row r comes from src row src_index[r] (r when src_index is null).
 // With the row's largest magnitude in [2^14, 2^15) every bf16 value is exact
 // in f16 except magnitudes below 2^-24 of that maximum, which flush.
-__global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __restrict__ src, int rows, int K,
+__global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __restrict__ src,
+                                                          const int32_t* __restrict__ src_index, int rows, int K,
                                                           uint16_t* __restrict__ dst, float* __restrict__ mul) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   if (row >= rows) return;
-  const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)row * K);
+  const int srow = src_index ? __ldg(src_index + row) : row;
+  const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)srow * K);
   uint4* d = reinterpret_cast<uint4*>(dst + (size_t)row * K);
   uint32_t m = 0;
   for (int i = lane; i < K / 8; i += 32) {
@@ -182,11 +185,12 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __rest
   if (lane == 0) mul[row] = __int_as_float((127 - sh) << 23);
 }
 
-moe_status launch_rows_to_f16(const uint16_t* src, int rows, int K, uint16_t* dst, float* mul, cudaStream_t s,
-                              bool pdl) {
+moe_status launch_rows_to_f16(const uint16_t* src, const int32_t* src_index, int rows, int K, uint16_t* dst,
+                              float* mul, cudaStream_t s, bool pdl) {
   if (rows == 0) return MOE_OK;
   const int blocks = (int)(((size_t)rows * 32 + 255) / 256);
-  cudaError_t e = launch_ex(pdl, rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, rows, K, dst, mul);
+  cudaError_t e = launch_ex(pdl, rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, src_index, rows, K, dst,
+                            mul);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;

@@ -176,6 +176,29 @@ def test_forward_mid_full_check(cfg):
     check_outputs(out, ref, what=cfg.name)
 
 
+def test_forward_group_sizes_cover_tile_shapes():
+    # top-1 routing forced by the logits: groups of 33..200 rows give every
+    # 16-row residue of the 128-row token tiles of the large-group GEMMs
+    sizes = [33, 40, 70, 90, 100, 128, 129, 200]
+    cfg = si.LayerConfig("groups8", T=sum(sizes), H=256, I=128, I_s=128, E=len(sizes), k=1)
+    _, layer = device_layer(cfg)
+    rng = np.random.default_rng(7)
+    expert_of = rng.permutation(np.repeat(np.arange(len(sizes)), sizes))
+    logits = torch.from_numpy(rng.standard_normal((cfg.T, cfg.E)).astype(np.float32))
+    logits[torch.arange(cfg.T), torch.from_numpy(expert_of)] += 10.0
+    x = si.make_x(cfg)
+    ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device="cuda")
+    ws = layer.workspace()
+    out = layer.forward(x.cuda(), logits.cuda(), topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    from nvfp4_mixture_experts_moe_gb300 import binding
+    assert binding.moe_get_device_status(ws) == 0
+    assert (ids.cpu().numpy()[:, 0] == expert_of).all()
+    experts, shared = OracleWeights(cfg).all()
+    ref = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k)
+    check_outputs(out.float().cpu().numpy(), ref, what="groups8")
+
+
 def test_forward_decode_full_check():
     cfg, layer, x, logits, out, ids = run_forward("decode")
     ow = OracleWeights(cfg)
