@@ -11,7 +11,7 @@
 //
 // * Two loader warps move each stage with the tensor-memory-access engine:
 //   one copies the stage's two 4608-byte chunks of raw e2m1 codes and E4M3
-//   scales (one bulk copy) into a ring of eight raw slots; the other loads the
+//   scales (one bulk copy) into a ring of four raw slots; the other loads the
 //   group's activation rows, one box per K half (16, 32, 64 or 128 rows, the
 //   smallest that covers the tile, through tensor maps over the f16
 //   activation matrix, whose rows are in group order; 128-byte swizzle). Box
@@ -32,8 +32,8 @@
 //   activation row's 2^-s (the f16 copy's power-of-two scale), alpha and the
 //   routing weight (GEMM 2) or apply SwiGLU (GEMM 1), and store bf16.
 //
-// TMEM: two accumulator buffers of 128 columns and four A stages of 64
-// columns. Every wait is bounded; on a timeout the kernel records
+// Two CTAs share an SM (kCtasPerSm). TMEM per CTA: one accumulator of 128
+// columns and two A stages of 64 columns. Every wait is bounded; on a timeout the kernel records
 // MOE_ERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -53,22 +53,29 @@ constexpr int kM = 128;
 constexpr int kBK = 128;                     // K per stage
 constexpr int kHalf = 64;                    // K per box / per 128-byte swizzled row
 constexpr int kRowBytes = 128;
-constexpr int kStages = 4;                   // activation tiles and TMEM A stages
-constexpr int kRawSlots = 8;                 // raw weight stages
+// Two CTAs per SM: one thread issues a CTA's MMAs and each stage costs that
+// thread a few hundred cycles of barrier and commit latency in which its
+// tensor core would idle; two independent issuers keep it fed, and while one
+// CTA drains its accumulator in the epilogue the other one's MMAs run.
+constexpr int kCtasPerSm = 2;
+constexpr int kStages = 2;                   // activation tiles and TMEM A stages
+constexpr int kRawSlots = 4;                 // raw weight stages
+constexpr int kTmemCols = 256;               // per CTA
 constexpr int kMaxBN = 128;
-constexpr int kWLoadWarp = 0;
-constexpr int kBLoadWarp = 1;
-constexpr int kDeqWarp0 = 2;                 // warps 2..9: two dequant sets
-constexpr int kEpiWarp0 = 10;                // warps 10..13
-constexpr int kMmaWarp = 14;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+// Warp roles. The epilogue warps are the oldest: the schedulers favour them
+// over the ALU-heavy dequant warps, so an accumulator drains quickly.
+constexpr int kEpiWarp0 = 0;                 // warps 0..3
+constexpr int kMmaWarp = 4;
+constexpr int kWLoadWarp = 5;
+constexpr int kBLoadWarp = 6;
+constexpr int kDeqWarp0 = 7;                 // warps 7..14: two dequant sets
+constexpr int kThreads = (kDeqWarp0 + 8) * 32;
 constexpr int kBHalf = kMaxBN * kRowBytes;   // 16 KB: one K half of the activation tile
 constexpr int kBStage = 2 * kBHalf;
 constexpr int kRawStage = 2 * kW16Chunk;     // two (128-row, 64-K) chunks
-constexpr uint32_t kAccCols = 128;
-constexpr uint32_t kAcol0 = 256;             // A stages: columns [256, 256 + 64 * kStages)
+constexpr uint32_t kAcol0 = 128;             // accumulator: columns [0, 128); A stages from 128
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
-static_assert(kAcol0 + 64 * kStages <= 512, "TMEM columns");
+static_assert(kAcol0 + 64 * kStages <= kTmemCols, "TMEM columns");
 
 // Tensor maps over the f16 activation matrix with boxes of 16, 32, 64 and
 // 128 rows (64 columns each).
@@ -94,8 +101,9 @@ struct Smem {
   uint64_t w_empty[kRawSlots];  // the dequant set is done reading them
   uint64_t ready[kStages];      // activation rows landed (bytes) and the four dequant warps done
   uint64_t empty[kStages];      // the stage's MMAs completed (activation tile and TMEM A free)
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull;
+  uint64_t tempty;
+  float rowmul[4][kMaxBN];      // epilogue: per-row factors of the tile, one copy per epilogue warp
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -135,7 +143,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_constant__ BoxMaps maps, Args p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const __grid_constant__ BoxMaps maps, Args p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_tiles = base;                               // kStages x 32 KB
@@ -164,10 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
       mbar_init(&sm->ready[i], 4 + 1);
       mbar_init(&sm->empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm->tfull[i], 1);
-      mbar_init(&sm->tempty[i], 128);
-    }
+    mbar_init(&sm->tfull, 1);
+    mbar_init(&sm->tempty, 128);
     mbar_init(&sm->drain, 1);
     sm->abort = 0;
     fence_barrier_init();
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
-  if (warp == kMmaWarp) tmem_alloc(&sm->tmem_base, 512);
+  if (warp == kMmaWarp) tmem_alloc(&sm->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
       }
     }
     __syncwarp();
-  } else if (warp < kEpiWarp0) {
+  } else if (warp >= kDeqWarp0) {
     // --------------------------------------------------------------- dequant
     const int set = (warp - kDeqWarp0) >> 2;     // takes the stages j with j % 2 == set
     const int q = warp & 3;                      // TMEM lane quarter of this warp
@@ -307,16 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
       }
       if (!ok) break;
     }
-  } else if (warp < kMmaWarp) {
+  } else if (warp < kEpiWarp0 + 4) {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int rho = q * 32 + lane;
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
       const Item it = decode_item(item, pref, G, MT, p.group_offsets);
-      const int acc = itc & 1;
-      // per-row factors of the tile: lane l holds rows l, l + 32, ...
-      float mulv[kMaxBN / 32];
+      // per-row factors of the tile into this warp's shared copy (no cross-warp sync)
+      float* rowmul = sm->rowmul[q];
+      __syncwarp();  // done reading the previous item's factors
 #pragma unroll
       for (int i = 0; i < kMaxBN / 32; ++i) {
         const int n = 32 * i + lane;
@@ -326,38 +332,57 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
           m = __ldg(p.a_mul + r);
           if (!GATE_UP && p.row_scale) m *= __ldg(p.row_scale + r);
         }
-        mulv[i] = m;
+        rowmul[n] = m;
       }
-      if (!mbar_wait(&sm->tfull[acc], (itc >> 1) & 1, abort, kWaitLimit)) break;
+      __syncwarp();
+      if (!mbar_wait(&sm->tfull, itc & 1, abort, kWaitLimit)) break;
       tc_fence_after();
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
       const float a0 = hdr->alpha[0], a1 = hdr->alpha[1];
-      for (int c0 = 0; c0 < it.bn; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols + c0, r);
+      const bool gate_lane = (rho & 8) == 0;   // rows 16j..16j+7 gate, 16j+8..16j+15 up (interleave by 8)
+      const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
+      for (int c0 = 0; c0 < it.bn; c0 += 32) {  // columns past bn are read (within the buffer) and not stored
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
         tmem_ld_wait();
-        float m_chunk = 0.0f;
+        if (GATE_UP) {
+          // the gate lane finishes columns c0..c0+15 and its up partner (lane ^ 8)
+          // columns c0+16..c0+31: one exchange of 16 raw values, 16 SiLUs each
+          const int cb = gate_lane ? 0 : 16;  // first column this lane finishes
+          float other[16];
 #pragma unroll
-        for (int i = 0; i < kMaxBN / 32; ++i)
-          if ((c0 >> 5) == i) m_chunk = mulv[i];
+          for (int c = 0; c < 16; ++c)
+            other[c] = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? r[16 + c] : r[c]), 8);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int n = c0 + c;
-          const float m = __shfl_sync(0xffffffffu, m_chunk, n & 31);
-          const float v = __uint_as_float(r[c]) * m;
-          if (GATE_UP) {
-            const float up = __shfl_down_sync(0xffffffffu, v, 8);
-            if ((rho & 15) < 8 && n < it.rows) {
-              const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
-              p.out[(size_t)(it.row0 + n) * (N / 2) + f] = float_to_bf16_bits(silu(v * a0) * (up * a1));
+          for (int c4 = 0; c4 < 16; c4 += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + cb + c4);  // broadcast read
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int c = c4 + t;
+              const float own = __uint_as_float(gate_lane ? r[c] : r[16 + c]);
+              const float g = (gate_lane ? own : other[c]) * mv[t];
+              const float u = (gate_lane ? other[c] : own) * mv[t];
+              const int n = c0 + cb + c;
+              if (n < it.rows) p.out[(size_t)(it.row0 + n) * (N / 2) + f] = float_to_bf16_bits(silu(g * a0) * (u * a1));
             }
-          } else if (n < it.rows) {
-            p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0);
+          }
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < 32; c4 += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + c4);  // broadcast read
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int n = c0 + c4 + t;
+              const float v = __uint_as_float(r[c4 + t]) * mv[t];
+              if (n < it.rows) p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0);
+            }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm->tempty[acc]);
+      mbar_arrive(&sm->tempty);
     }
   } else {
     // ------------------------------------------------------------------ MMA
@@ -366,11 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
       int j = 0, itc = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
         const Item it = decode_item(item, pref, G, MT, p.group_offsets);
-        const int acc = itc & 1;
-        if (!mbar_wait(&sm->tempty[acc], ((itc >> 1) & 1) ^ 1, abort, kWaitLimit)) break;
+        if (!mbar_wait(&sm->tempty, (itc & 1) ^ 1, abort, kWaitLimit)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(kM, it.bn, 0);
-        const uint32_t d = tmem + acc * kAccCols;
+        const uint32_t d = tmem;
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
@@ -391,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
           tc_commit(&sm->empty[slot]);
         }
         if (!ok) break;
-        tc_commit(&sm->tfull[acc]);
+        tc_commit(&sm->tfull);
       }
       tc_commit(&sm->drain);
       drain_wait(&sm->drain, 0);
@@ -401,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_f16_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (tid == 0 && sm->abort) set_status(p.status, MOE_ERR_TIMEOUT);
 }
 
@@ -462,7 +486,7 @@ moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   auto k = pl.gate_up ? gemm_tc_f16_kernel<true> : gemm_tc_f16_kernel<false>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(kThreads), smem, s, maps, a);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * kCtasPerSm), dim3(kThreads), smem, s, maps, a);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;
