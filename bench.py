@@ -127,6 +127,23 @@ def algorithmic(cfg, ids_list):
             "gemm1_flops": gemm1_flops, "layer_flops": layer_flops, "w13_bytes": w13, "w2_bytes": w2}
 
 
+def ncu_traffic(workload_key):
+    """DRAM bytes per launch of the reported kernel from the committed ncu
+    summary (profiles/ncu_traffic.json), or None when there is none for this
+    workload or the kernel's sources changed since the capture."""
+    import hashlib
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "ncu_traffic.json")
+    try:
+        rec = json.load(open(path))[workload_key]
+        h = hashlib.sha256()
+        root = os.path.dirname(path)
+        for f in rec["sources"]:
+            h.update(open(os.path.join(root, "..", f), "rb").read())
+        return rec["bytes"] if h.hexdigest() == rec["sources_sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def max_over_ranks(v, dist, device):
     """The largest of every rank's ``v`` (the job's step time is its slowest
     rank's); identity without a process group."""
@@ -380,7 +397,7 @@ def run_ours(args):
         bound, unit = "hbm", "GB/s"
         achieved = alg["gemm1_bytes"] / (g1_ms / 1e3) / 1e9
         peak = pk["hbm"]
-        traffic = None
+        traffic = ncu_traffic("decode") if cfg.name == "decode" else None
     else:
         bound, unit = "tensor", "TFLOP/s"
         achieved = alg["gemm1_flops"] / (g1_ms / 1e3) / 1e12
