@@ -39,7 +39,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kMmaWarps = 8;
+constexpr int kBlockWarps = 8;                   // one per 16-row block of a 128-row item
+constexpr int kHalves = 2;                       // K split: half h takes the stages st with st % 2 == h
+constexpr int kMmaWarps = kBlockWarps * kHalves;
 constexpr int kThreads = (kMmaWarps + 1) * 32;  // + one producer warp
 constexpr int kRowsPerPass = 8;
 constexpr int kTileRows = 128;                   // weight rows per item
@@ -67,9 +69,13 @@ struct SmallArgs {
 struct SmallSmem {
   uint64_t full[8];
   uint64_t empty[8];
+  uint64_t xsync;                  // the MMA warps' barrier around x staging (one arrival per warp)
+  uint64_t red_full[kBlockWarps];  // half 1 -> half 0: partial sums of block b written
+  uint64_t red_empty[kBlockWarps]; // half 0 -> half 1: read
   int abort;
   float row_mul[kRowsPerPass];
   int row_out[kRowsPerPass];
+  float4 red[kBlockWarps][32];     // half 1's partial sums (per lane: acc of rows g, g+8 x 2 columns)
 };
 
 __device__ __forceinline__ int group_items(const int32_t* off, int g, int mt_count, int limit) {
@@ -93,8 +99,16 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
-// Named barrier over the eight MMA warps only (the producer never joins).
-__device__ __forceinline__ void mma_warps_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kMmaWarps * 32)); }
+// Barrier over the MMA warps (the producer never joins) on an mbarrier, with
+// a bounded wait: every warp arrives once per use and waits for the phase.
+__device__ __forceinline__ bool mma_warps_sync(uint64_t* bar, uint32_t& phase, volatile int* abort) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase, abort, kWaitLimit);
+  phase ^= 1u;
+  __syncwarp();
+  return ok;
+}
 
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
@@ -119,7 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     pref[0] = 0;
     for (int i = 0; i < S; ++i) {
       mbar_init(&sm->full[i], 1);
-      mbar_init(&sm->empty[i], kMmaWarps);
+      mbar_init(&sm->empty[i], kBlockWarps);  // the eight warps of the half that read the stage
+    }
+    mbar_init(&sm->xsync, kMmaWarps);
+    for (int b = 0; b < kBlockWarps; ++b) {
+      mbar_init(&sm->red_full[b], 1);
+      mbar_init(&sm->red_empty[b], 1);
     }
     sm->abort = 0;
     fence_barrier_init();
@@ -172,9 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
 
   // ------------------------------------------------------------- MMA warps
   if (p.early_weights) pdl_wait();  // the activation rows come from the predecessor
+  const int blk = warp % kBlockWarps, half = warp / kBlockWarps;
   const int g8 = lane >> 2, t4 = lane & 3;
   int cur_g = -1, cur_c = -1;
   int j = 0;
+  uint32_t xphase = 0, rphase = 0;
   // ldmatrix row address of this lane: matrix q = lane / 8 covers the 8
   // staged rows at k offset 8 * q (two k16 steps per ldmatrix.x4)
   const int lrow = lane & 7, lq = lane >> 3;
@@ -186,55 +207,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     const int nrows = min(kRowsPerPass, p.group_offsets[g + 1] - row0);
 
     if (g != cur_g || c != cur_c) {
-      if (*abort) break;
-      mma_warps_sync();  // everyone is done with the previous rows
-      const int r = warp;  // warp w stages row w
-      uint16_t* dst = xs + (size_t)r * xs_stride;
-      if (r < nrows) {
-        const int orow = row0 + r;
-        const int arow = p.a_row_index ? p.a_row_index[orow] : orow;
-        const uint4* src = reinterpret_cast<const uint4*>(p.a + (size_t)arow * K);
-        uint32_t m = 0;
-        for (int i = lane; i < K / 8; i += 32) {
-          const uint4 v = __ldg(src + i);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      if (!mma_warps_sync(&sm->xsync, xphase, abort)) break;  // everyone is done with the previous rows
+      if (warp < kRowsPerPass) {
+        const int r = warp;  // warp w stages row w
+        uint16_t* dst = xs + (size_t)r * xs_stride;
+        if (r < nrows) {
+          const int orow = row0 + r;
+          const int arow = p.a_row_index ? p.a_row_index[orow] : orow;
+          const uint4* src = reinterpret_cast<const uint4*>(p.a + (size_t)arow * K);
+          uint32_t m = 0;
+          for (int i = lane; i < K / 8; i += 32) {
+            const uint4 v = __ldg(src + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (m > 0x7f80u) m = 0x7f80u;  // NaN patterns are outside the contract
-        // m = bf16 bits of the row max; its exponent e puts the max in [2^(e-127), 2^(e-126))
-        const int e = (int)(m >> 7);
-        int sh = (m == 0) ? 0 : 141 - max(e, 1);  // 2^(e-127+sh) = 2^14
-        sh = max(-113, min(sh, 126));             // 2^sh and 2^-sh stay normal floats
-        const float up = __int_as_float((127 + sh) << 23);
-        for (int i = lane; i < K / 8; i += 32) {
-          const uint4 v = __ldg(src + i);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * up,
-                                                __uint_as_float(w[q] & 0xffff0000u) * up);
-            o[q] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
           }
-          *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (lane == 0) {
-          sm->row_mul[r] = __int_as_float((127 - sh) << 23);
-          sm->row_out[r] = orow;
-        }
-      } else {
-        for (int i = lane; i < K / 8; i += 32) *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(0, 0, 0, 0);
-        if (lane == 0) {
-          sm->row_mul[r] = 0.0f;
-          sm->row_out[r] = -1;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if (m > 0x7f80u) m = 0x7f80u;  // NaN patterns are outside the contract
+          // m = bf16 bits of the row max; its exponent e puts the max in [2^(e-127), 2^(e-126))
+          const int e = (int)(m >> 7);
+          int sh = (m == 0) ? 0 : 141 - max(e, 1);  // 2^(e-127+sh) = 2^14
+          sh = max(-113, min(sh, 126));             // 2^sh and 2^-sh stay normal floats
+          const float up = __int_as_float((127 + sh) << 23);
+          for (int i = lane; i < K / 8; i += 32) {
+            const uint4 v = __ldg(src + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * up,
+                                                  __uint_as_float(w[q] & 0xffff0000u) * up);
+              o[q] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+          if (lane == 0) {
+            sm->row_mul[r] = __int_as_float((127 - sh) << 23);
+            sm->row_out[r] = orow;
+          }
+        } else {
+          for (int i = lane; i < K / 8; i += 32) *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(0, 0, 0, 0);
+          if (lane == 0) {
+            sm->row_mul[r] = 0.0f;
+            sm->row_out[r] = -1;
+          }
         }
       }
       cur_g = g;
       cur_c = c;
-      mma_warps_sync();
+      if (!mma_warps_sync(&sm->xsync, xphase, abort)) break;
     }
 
     // one accumulator per k16 step of a block: four independent MMA chains
@@ -244,13 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     const uint32_t xbase = smem_u32(xs) + (uint32_t)(lrow * xs_stride + 8 * lq) * 2;
     bool ok = true;
     for (int st = 0; st < nstage; ++st, ++j) {
+      if ((st % kHalves) != half) continue;  // the other half's stage
       const int slot = j % S;
       if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, kWaitLimit)) { ok = false; break; }
       const int kb0 = st * kBlocksPerStage;
       const int nkb = min(kBlocksPerStage, kblocks - kb0);
       const uint8_t* sd = stages + (size_t)slot * kStageBytes;
-      const uint8_t* my_data = sd + warp * 512 + lane * 16;
-      const uint8_t* my_sf = sd + kW16SfOff + warp * 64 + g8 * 8;
+      const uint8_t* my_data = sd + blk * 512 + lane * 16;
+      const uint8_t* my_sf = sd + kW16SfOff + blk * 64 + g8 * 8;
 #pragma unroll 2
       for (int kb = 0; kb < nkb; ++kb) {
         const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * kW16Chunk);
@@ -285,11 +308,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = (acc4[0][q] + acc4[1][q]) + (acc4[2][q] + acc4[3][q]);
 
+    // split-K reduction: half 1 hands its partial sums to half 0 (fixed order:
+    // half 0's stages + half 1's stages)
+    if (half == 1) {
+      if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, kWaitLimit)) break;
+      sm->red[blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->red_full[blk]);
+      rphase ^= 1u;
+      continue;
+    }
+    if (!mbar_wait(&sm->red_full[blk], rphase, abort, kWaitLimit)) break;
+    {
+      const float4 o = sm->red[blk][lane];
+      acc[0] += o.x;
+      acc[1] += o.y;
+      acc[2] += o.z;
+      acc[3] += o.w;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->red_empty[blk]);
+    rphase ^= 1u;
+
     // Epilogue: c0,c1 = row g (tokens 2t, 2t+1); c2,c3 = row g+8.
-    const uint8_t* blk = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
-                                                                  : p.weights + (size_t)g * p.stride;
-    const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(blk);
-    const int mb = mt * 8 + warp;
+    const uint8_t* wb = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
+                                                                 : p.weights + (size_t)g * p.stride;
+    const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wb);
+    const int mb = mt * 8 + blk;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int n = 2 * t4 + q;
