@@ -9,12 +9,14 @@
 // At a few rows per expert the layer is bound by the bytes of the touched
 // experts' weights ("Seven Months of GB10 Field Notes": decode re-reads the
 // active weights). Each weight byte is read from HBM once. One producer warp
-// streams the weight tiles with bulk copies (cp.async.bulk, completion on
-// mbarriers) into a ring of shared-memory stages, keeping ~100 KB in flight
-// per SM; eight MMA warps each own one 16-row tile of a 128-row item for the
-// whole K. A warp loads its 16-byte A fragment per 64-wide K block from
-// shared memory, turns the e2m1 codes into f16 with the hardware e2m1x2
-// conversion, multiplies in the E4M3 block scales (e2m1 * e4m3 is exact in
+// streams the weight tiles with bulk copies (cp.async.bulk, one 36 KB copy
+// per stage, completion on mbarriers) into a ring of shared-memory stages,
+// keeping ~140 KB in flight per SM. Sixteen MMA warps: warp b of part h owns
+// the 16-row block b of a 128-row item for the stages j with j % 2 == h, and
+// part 1 hands its partial sums to part 0 at the end of the item (more warps
+// per scheduler hide the conversion -> multiply -> MMA latency chains). A
+// warp loads its 16-byte A fragment per 64-wide K block from shared memory,
+// turns the e2m1 codes into f16 with the hardware e2m1x2 conversion, multiplies in the E4M3 block scales (e2m1 * e4m3 is exact in
 // f16) and feeds mma.sync m16n8k16 with the group's rows (up to 8) as N.
 //
 // Activations enter as f16: each row is scaled by a power of two 2^s so that
@@ -40,7 +42,12 @@ namespace {
 using namespace tc;
 
 constexpr int kBlockWarps = 8;                   // one per 16-row block of a 128-row item
-constexpr int kHalves = 2;                       // K split: half h takes the stages st with st % 2 == h
+// K split: part h takes the ring stages j with j % kHalves == h (j counts the
+// stages of all items in order). A part waits for stage j only after it
+// consumed stage j - kHalves, so with at least kHalves ring slots it never
+// waits on a slot two phases ahead (an mbarrier parity wait cannot tell those
+// apart).
+constexpr int kHalves = 2;
 constexpr int kMmaWarps = kBlockWarps * kHalves;
 constexpr int kThreads = (kMmaWarps + 1) * 32;  // + one producer warp
 constexpr int kRowsPerPass = 8;
@@ -70,12 +77,12 @@ struct SmallSmem {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t xsync;                  // the MMA warps' barrier around x staging (one arrival per warp)
-  uint64_t red_full[kBlockWarps];  // half 1 -> half 0: partial sums of block b written
-  uint64_t red_empty[kBlockWarps]; // half 0 -> half 1: read
+  uint64_t red_full[kBlockWarps];  // parts 1.. -> part 0: partial sums of block b written
+  uint64_t red_empty[kBlockWarps]; // part 0 -> parts 1..: read
   int abort;
   float row_mul[kRowsPerPass];
   int row_out[kRowsPerPass];
-  float4 red[kBlockWarps][32];     // half 1's partial sums (per lane: acc of rows g, g+8 x 2 columns)
+  float4 red[kHalves - 1][kBlockWarps][32];  // parts 1..'s partial sums (per lane: rows g, g+8 x 2 columns)
 };
 
 __device__ __forceinline__ int group_items(const int32_t* off, int g, int mt_count, int limit) {
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     }
     mbar_init(&sm->xsync, kMmaWarps);
     for (int b = 0; b < kBlockWarps; ++b) {
-      mbar_init(&sm->red_full[b], 1);
+      mbar_init(&sm->red_full[b], kHalves - 1);
       mbar_init(&sm->red_empty[b], 1);
     }
     sm->abort = 0;
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     const uint32_t xbase = smem_u32(xs) + (uint32_t)(lrow * xs_stride + 8 * lq) * 2;
     bool ok = true;
     for (int st = 0; st < nstage; ++st, ++j) {
-      if ((st % kHalves) != half) continue;  // the other half's stage
+      if ((j % kHalves) != half) continue;  // another part's stage
       const int slot = j % S;
       if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, kWaitLimit)) { ok = false; break; }
       const int kb0 = st * kBlocksPerStage;
@@ -308,19 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = (acc4[0][q] + acc4[1][q]) + (acc4[2][q] + acc4[3][q]);
 
-    // split-K reduction: half 1 hands its partial sums to half 0 (fixed order:
-    // half 0's stages + half 1's stages)
-    if (half == 1) {
+    // split-K reduction: parts 1.. hand their partial sums to part 0, which
+    // adds them in a fixed order (part 0, 1, 2, ...)
+    if (half != 0) {
       if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, kWaitLimit)) break;
-      sm->red[blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      sm->red[half - 1][blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->red_full[blk]);
       rphase ^= 1u;
       continue;
     }
     if (!mbar_wait(&sm->red_full[blk], rphase, abort, kWaitLimit)) break;
-    {
-      const float4 o = sm->red[blk][lane];
+#pragma unroll
+    for (int h = 0; h < kHalves - 1; ++h) {
+      const float4 o = sm->red[h][blk][lane];
       acc[0] += o.x;
       acc[1] += o.y;
       acc[2] += o.z;
@@ -339,7 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     for (int q = 0; q < 2; ++q) {
       const int n = 2 * t4 + q;
       if (n >= nrows) continue;
-      const int orow = sm->row_out[n];
+      const int orow = row0 + n;
+      if (sm->row_out[n] != orow) {  // the staged rows must be this item's (a desync would be a bug)
+        set_status(p.status, MOE_ERR_DEVICE);
+        continue;
+      }
       const float rm = sm->row_mul[n];
       if (GATE_UP) {
         const float gv = acc[q] * rm * hdr->alpha[0];
@@ -382,9 +394,9 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStrea
   a.early_weights = pl.pdl && pl.early_weights ? 1 : 0;
   const size_t limit = 227 * 1024;
   int S = 6;
-  while (S > 2 && small_smem_bytes(pl.K, pl.num_groups, S) > limit) --S;
+  while (S > kHalves && small_smem_bytes(pl.K, pl.num_groups, S) > limit) --S;
   const size_t smem = small_smem_bytes(pl.K, pl.num_groups, S);
-  if (smem > limit) return MOE_ERR_UNSUPPORTED;
+  if (smem > limit) return MOE_ERR_UNSUPPORTED;  // K too large for the staged rows and kHalves slots
   a.stages = S;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);

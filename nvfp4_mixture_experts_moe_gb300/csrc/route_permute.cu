@@ -127,7 +127,7 @@ __device__ __forceinline__ void scatter_warp(const int32_t* __restrict__ ids, in
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     const bool in = p < p1;
-    int e = in ? __ldg(ids + p) : -1;
+    int e = in ? __ldcg(ids + p) : -1;  // L2 load: ids may have been written earlier in this kernel
     const bool valid = in && e >= 0 && e < E;
     if (in && !valid) set_status(status, MOE_ERR_DEVICE);
     const int key = valid ? e : -1 - lane;  // invalid lanes never match each other
@@ -226,7 +226,7 @@ __device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int 
   for (int p = threadIdx.x; p < P; p += blockDim.x) perm[p] = -1;
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int e = __ldg(ids + p);
+    const int e = __ldcg(ids + p);  // L2 load: ids may have been written earlier in this kernel
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
