@@ -87,11 +87,12 @@ struct ForwardWs {
   float* xmul;        // [T]
   uint16_t* hf;       // f16 copy of h [rows, I]
   float* hmul;        // [rows]
-  uint8_t* xq;        // W4A4: [T, H/2]
-  uint8_t* xsf;       // W4A4: [T, H/16]
+  uint8_t* xq;        // W4A4: [rows, H/2], x quantised in group order
+  uint8_t* xsf;       // W4A4: scale atoms per (128-row tile, 256-wide K stage): [tiles, H/256, 2048]
   float* xgs;
   uint8_t* hq;        // W4A4: [rows, I/2]
-  uint8_t* hsf;       // W4A4: [rows, I/16]
+  uint8_t* hsf;       // W4A4: [tiles, I/256, 2048]
+  int tiles;          // W4A4: bound on the 128-row tiles of all groups
   float* hgs;
   size_t bytes;
 };
@@ -125,15 +126,17 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
     f.xmul = f.hmul = nullptr;
   }
   if (L.mode == MOE_W4A4) {
-    f.xq = c.take<uint8_t>((size_t)L.T * L.H / 2);
-    f.xsf = c.take<uint8_t>((size_t)L.T * L.H / 16);
+    f.tiles = (int)(rows / 128) + L.E + 1;  // sum over groups of ceil(rows_g / 128)
+    f.xq = c.take<uint8_t>(rows * L.H / 2);
+    f.xsf = c.take<uint8_t>((size_t)f.tiles * (L.H / 256) * 2048);
     f.xgs = c.take<float>(1);
     f.hq = c.take<uint8_t>(rows * L.I / 2);
-    f.hsf = c.take<uint8_t>(rows * L.I / 16);
+    f.hsf = c.take<uint8_t>((size_t)f.tiles * (L.I / 256) * 2048);
     f.hgs = c.take<float>(1);
   } else {
     f.xq = f.xsf = f.hq = f.hsf = nullptr;
     f.xgs = f.hgs = nullptr;
+    f.tiles = 0;
   }
   f.bytes = c.off;
   return f;
@@ -416,7 +419,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     if (st != MOE_OK) return st;
     st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s, pdl);
     if (st != MOE_OK) return st;
-    st = launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq, f.xsf, f.xgs, s, pdl);
+    st = launch_quantize_tiles(x, T, H, f.inv_perm, k, has_shared ? P : -1, f.gofs, E + (has_shared ? 1 : 0),
+                               &f.hdr->amax[0], f.xq, f.xsf, (size_t)f.tiles * (H / 256) * 2048, f.xgs, s, pdl);
     if (st != MOE_OK) return st;
   }
   if (f.xf) {  // f16 copy of x, rows in group order, for the large-group tensor-core GEMM
@@ -450,11 +454,12 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.max_rows = rows;
   g1.pdl = pdl;
   g1.early_weights = false;
-  st = run_gemm(g1, T, s);
+  st = fp4 ? launch_gemm_tc_fp4(g1, s) : run_gemm(g1, T, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
   if (fp4) {  // h -> NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue)
-    st = launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf, f.hgs, s, pdl);
+    st = launch_quantize_tiles(f.h, rows, I, nullptr, 0, -1, f.gofs, G, &f.hdr->amax[1], f.hq, f.hsf,
+                               (size_t)f.tiles * (I / 256) * 2048, f.hgs, s, pdl);
     if (st != MOE_OK) return st;
   } else if (f.hf) {
     st = launch_rows_to_f16(f.h, nullptr, rows, I, f.hf, f.hmul, s, pdl);
@@ -479,7 +484,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g2.a_row_index = nullptr;
   g2.row_scale = f.row_weight;
   g2.out = f.y;
-  st = run_gemm(g2, T, s);
+  st = fp4 ? launch_gemm_tc_fp4(g2, s) : run_gemm(g2, T, s);
   if (st != MOE_OK) return st;
   stage_mark(6, s);
   st = launch_combine(f.y, f.inv_perm, nullptr, has_shared ? 1 : 0, T, k, H, out, s, pdl);

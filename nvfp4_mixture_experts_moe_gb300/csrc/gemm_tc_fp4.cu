@@ -1,0 +1,416 @@
+// Grouped NVFP4 x NVFP4 GEMM (W4A4) of the fused forward: block-scaled FP4
+// tensor-core MMA with UE4M3 scales, both operands moved by the copy engine.
+//
+// "vLLM on the NVIDIA DGX Spark: A Complete Technical Guide", section 6.1
+// (NVFP4 needs block-scaled tensor-core MMA: e2m1 values, one E4M3 scale per
+// 16, fp32 global scales) and section 4.3 (the BF16 input quantised to FP4
+// before the expert GEMMs; SwiGLU and the top-k weight in the epilogues).
+//
+// Swap-AB tile: 128 weight rows on the MMA's M side, up to 128 rows of one
+// expert group on N, K in stages of 256 (four kind::mxf4nvf4 MMAs of K 64).
+// * A weight-loader warp copies the stage's prepared weight tile (the exact
+//   128-byte-swizzled shared-memory image, 16 KB) and its four scale-factor
+//   atoms (2 KB) with two bulk copies.
+// * An activation-loader warp copies the group's FP4 rows with one
+//   tensor-map box (16/32/64/128 rows x 128 bytes, 128-byte swizzle) and the
+//   tile's four scale-factor atoms, written in that layout by the quantiser
+//   (rows past the group carry scale 0), with one bulk copy.
+// * One thread moves the eight atoms into tensor memory (tcgen05.cp
+//   32x128b.warpx4) and issues the MMAs; four epilogue warps apply alpha and
+//   the activations' 1/gs, SwiGLU (gate/up, with the amax of h for its
+//   quantisation) or the routing weight (down), and store bf16.
+// Two CTAs share an SM: each has one accumulator (128 TMEM columns) and
+// three stages of scale factors (32 columns each), so while one drains its
+// accumulator the other's MMAs run, and the two MMA issuers overlap their
+// per-stage wait/commit latency. Every wait is bounded; on a timeout the
+// kernel records MOE_ERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM
+// and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int kCtasPerSm = 2;
+constexpr int kM = 128;
+constexpr int kBK = 256;                    // K per stage
+constexpr int kRowBytes = 128;              // one operand row per stage: 256 FP4
+constexpr int kStages = 3;
+constexpr int kMaxBN = 128;
+constexpr int kTile = kM * kRowBytes;       // 16 KB (A; B at most the same)
+constexpr int kSfStage = 4 * 512;           // four atoms
+constexpr int kStageBytes = 2 * kTile + 2 * kSfStage;
+constexpr int kEpiWarp0 = 0;                // warps 0..3
+constexpr int kMmaWarp = 4;
+constexpr int kALoadWarp = 5;
+constexpr int kBLoadWarp = 6;
+constexpr int kThreads = 7 * 32;
+constexpr int kTmemCols = 256;
+constexpr uint32_t kSfCol0 = 128;           // accumulator [0, 128); scale factors 32 columns per stage
+static_assert(kSfCol0 + 32 * kStages <= kTmemCols, "TMEM columns");
+constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
+
+struct BoxMaps {
+  CUtensorMap m[4];
+};
+
+struct Args {
+  const uint8_t* weights;
+  size_t stride;
+  const uint8_t* last_weights;
+  int G, N, K;
+  const int32_t* group_offsets;
+  const uint8_t* b_sf_tiles;   // activation scale atoms per (tile, stage)
+  const float* b_gs;           // activation global scale
+  const float* row_scale;
+  uint16_t* out;
+  float* out_amax;
+  int* status;
+};
+
+struct Smem {
+  uint64_t ready[kStages];  // both loaders' bytes landed (two expect_tx arrivals)
+  uint64_t empty[kStages];  // the stage's MMAs completed
+  uint64_t tfull;
+  uint64_t tempty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Item {
+  int g, row0, rows, bn, mt, tile;
+};
+
+// pref[g]: first item of group g; tb[g]: its first 128-row activation tile
+__device__ __forceinline__ Item decode_item(int idx, const int* pref, const int* tb, int G, int MT,
+                                            const int32_t* off) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  Item it;
+  it.g = lo;
+  const int local = idx - pref[lo];
+  const int nt = local / MT;
+  it.mt = local % MT;
+  const int grows = off[lo + 1] - off[lo];
+  it.row0 = off[lo] + nt * kMaxBN;
+  it.rows = min(kMaxBN, grows - nt * kMaxBN);
+  it.bn = (it.rows + 15) & ~15;
+  it.tile = tb[lo] + nt;
+  return it;
+}
+
+__device__ __forceinline__ const uint8_t* weight_block(const Args& p, int g) {
+  return (g == p.G - 1 && p.last_weights != nullptr) ? p.last_weights : p.weights + (size_t)g * p.stride;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitLimit) {
+  }
+}
+
+template <bool GATE_UP>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const __grid_constant__ BoxMaps maps,
+                                                                           Args p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // per stage: A tile | B tile | SFA atoms | SFB atoms
+  Smem* sm = reinterpret_cast<Smem*>(base + kStages * kStageBytes);
+  int* pref = reinterpret_cast<int*>(sm + 1);   // [G + 1]
+  int* tb = pref + (p.G + 1);                   // [G + 1]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.G, K = p.K, N = p.N;
+  const int MT = N / kM;
+  const int KS = K / kBK;
+  pdl_wait();
+
+  for (int g = tid; g < G; g += kThreads) {
+    const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
+    const int nt = rows > 0 ? (rows + kMaxBN - 1) / kMaxBN : 0;
+    pref[g + 1] = nt * MT;
+    tb[g + 1] = nt;
+  }
+  if (tid == 0) {
+    pref[0] = 0;
+    tb[0] = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm->ready[i], 2);
+      mbar_init(&sm->empty[i], 1);
+    }
+    mbar_init(&sm->tfull, 1);
+    mbar_init(&sm->tempty, 128);
+    mbar_init(&sm->drain, 1);
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp < 2) {  // inclusive scans of pref (warp 0) and tb (warp 1)
+    int* arr = warp == 0 ? pref : tb;
+    int carry = 0;
+    for (int b0 = 1; b0 <= G; b0 += 32) {
+      const int i = b0 + lane;
+      int v = i <= G ? arr[i] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (i <= G) arr[i] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  if (warp == kMmaWarp) tmem_alloc(&sm->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  const int total = pref[G];
+  volatile int* abort = &sm->abort;
+
+  if (warp == kALoadWarp) {
+    // --------------------------------------------------------- weight loader
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
+        const uint8_t* wdata = weight_block(p, it.g) + sizeof(PrepHeader);
+        const uint8_t* wsf = wdata + (size_t)N * K / 2;
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kStages;
+          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          uint8_t* st = base + slot * kStageBytes;
+          const size_t tile = (size_t)it.mt * KS + ks;
+          mbar_arrive_expect_tx(&sm->ready[slot], kTile + kSfStage);
+          bulk_g2s(smem_u32(st), wdata + tile * kTile, kTile, &sm->ready[slot]);
+          bulk_g2s(smem_u32(st + 2 * kTile), wsf + tile * kSfStage, kSfStage, &sm->ready[slot]);
+        }
+        if (!ok) break;
+      }
+      if (*abort) {  // copies in flight land before the shared memory is released
+        const long long t0 = clock64();
+        while (clock64() - t0 < 200000) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kBLoadWarp) {
+    // ----------------------------------------------------- activation loader
+    if (lane < 4) tma_prefetch_map(&maps.m[lane]);
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
+        const int q = 32 - __clz((it.bn >> 4) - 1);   // box of 16 << q >= bn rows
+        const uint32_t bytes = (uint32_t)((16 << q) * kRowBytes + kSfStage);
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kStages;
+          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          uint8_t* st = base + slot * kStageBytes;
+          mbar_arrive_expect_tx(&sm->ready[slot], bytes);
+          tma_load_2d(smem_u32(st + kTile), &maps.m[q], ks * kRowBytes, it.row0, &sm->ready[slot]);
+          bulk_g2s(smem_u32(st + 2 * kTile + kSfStage), p.b_sf_tiles + ((size_t)it.tile * KS + ks) * kSfStage,
+                   kSfStage, &sm->ready[slot]);
+        }
+        if (!ok) break;
+      }
+      if (*abort) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 200000) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < kEpiWarp0 + 4) {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int rho = q * 32 + lane;
+    const float inv_gs_b = 1.0f / *p.b_gs;
+    float amax = 0.0f;
+    int itc = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
+      const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
+      float rsv[kMaxBN / 32];
+#pragma unroll
+      for (int i = 0; i < kMaxBN / 32; ++i) {
+        const int n = 32 * i + lane;
+        rsv[i] = (!GATE_UP && p.row_scale && n < it.rows) ? __ldg(p.row_scale + it.row0 + n) : 1.0f;
+      }
+      if (!mbar_wait(&sm->tfull, itc & 1, abort, kWaitLimit)) break;
+      tc_fence_after();
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
+      const float a0 = hdr->alpha[0] * inv_gs_b, a1 = hdr->alpha[1] * inv_gs_b;
+      const bool gate_lane = (rho & 8) == 0;  // rows 16j..16j+7 gate, 16j+8..16j+15 up (interleave by 8)
+      const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
+      for (int c0 = 0; c0 < it.bn; c0 += 32) {  // columns past bn are read (within the buffer) and not stored
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
+        tmem_ld_wait();
+        if (GATE_UP) {
+          // the gate lane finishes columns c0..c0+15, its up partner (lane ^ 8) c0+16..c0+31
+          const int cb = gate_lane ? 0 : 16;
+          float other[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            other[c] = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? r[16 + c] : r[c]), 8);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float own = __uint_as_float(gate_lane ? r[c] : r[16 + c]);
+            const float g = gate_lane ? own : other[c];
+            const float u = gate_lane ? other[c] : own;
+            const int n = c0 + cb + c;
+            if (n < it.rows) {
+              const uint16_t hb = float_to_bf16_bits(silu(g * a0) * (u * a1));
+              p.out[(size_t)(it.row0 + n) * (N / 2) + f] = hb;
+              amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)hb << 16)));
+            }
+          }
+        } else {
+          float rs_chunk = 1.0f;
+#pragma unroll
+          for (int i = 0; i < kMaxBN / 32; ++i)
+            if ((c0 >> 5) == i) rs_chunk = rsv[i];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int n = c0 + c;
+            const float rs = __shfl_sync(0xffffffffu, rs_chunk, c);
+            if (n < it.rows)
+              p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(__uint_as_float(r[c]) * a0 * rs);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm->tempty);
+    }
+    if (GATE_UP && p.out_amax != nullptr) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) atomic_max_nonneg(p.out_amax, amax);
+    }
+  } else {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      int j = 0, itc = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
+        const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
+        if (!mbar_wait(&sm->tempty, (itc & 1) ^ 1, abort, kWaitLimit)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_nvf4(kM, it.bn);
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kStages;
+          if (!mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t as = smem_u32(base + slot * kStageBytes);
+          const uint32_t bs = as + kTile;
+          const uint32_t sfa = as + 2 * kTile;
+          const uint32_t sfb = sfa + kSfStage;
+          const uint32_t sf_col = tmem + kSfCol0 + slot * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
+            tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
+            mma_nvf4(tmem, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4, (ks | kk) != 0);
+          }
+          tc_commit(&sm->empty[slot]);
+        }
+        if (!ok) break;
+        tc_commit(&sm->tfull);
+      }
+      tc_commit(&sm->drain);
+      drain_wait(&sm->drain, 0);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0 && sm->abort) set_status(p.status, MOE_ERR_TIMEOUT);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+static size_t fp4_smem_bytes(int G) {
+  return 1024 + (size_t)kStages * kStageBytes + sizeof(Smem) + (size_t)(G + 1) * 8;
+}
+
+moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
+  if (pl.num_groups <= 0) return MOE_OK;
+  if (pl.K % kBK || pl.N % kM) return MOE_ERR_UNSUPPORTED;
+  if (pl.a == nullptr || pl.a_sf == nullptr || pl.a_gs == nullptr || pl.a_rows <= 0) return MOE_ERR_INVALID_ARG;
+  auto encode = encode_tiled();
+  if (encode == nullptr) return MOE_ERR_CUDA;
+  // the FP4 activation codes [a_rows, K/2] in group order: boxes of 16..128 rows x 128 bytes, 128-byte swizzle
+  BoxMaps maps;
+  for (int q = 0; q < 4; ++q) {
+    const cuuint64_t dims[2] = {(cuuint64_t)pl.K / 2, (cuuint64_t)pl.a_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pl.K / 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kRowBytes, (cuuint32_t)(16 << q)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&maps.m[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pl.a), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_ERR_INVALID_ARG;
+  }
+  Args a;
+  a.weights = pl.weights;
+  a.stride = pl.weight_stride;
+  a.last_weights = pl.last_weights;
+  a.G = pl.num_groups;
+  a.N = pl.N;
+  a.K = pl.K;
+  a.group_offsets = pl.group_offsets;
+  a.b_sf_tiles = pl.a_sf;
+  a.b_gs = pl.a_gs;
+  a.row_scale = pl.row_scale;
+  a.out = pl.out;
+  a.out_amax = pl.out_amax;
+  a.status = pl.status;
+  const size_t smem = fp4_smem_bytes(pl.num_groups);
+  if (smem > 113 * 1024) return MOE_ERR_UNSUPPORTED;  // two CTAs per SM
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  auto k = pl.gate_up ? gemm_tc_fp4_kernel<true> : gemm_tc_fp4_kernel<false>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * kCtasPerSm), dim3(kThreads), smem, s, maps, a);
+  if (e != cudaSuccess) return cuda_ok(e);
+  count_launches(1);
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -110,6 +110,16 @@ moe_status launch_gemm_tc_w4a16(const GemmPlan& p, int rows_min, cudaStream_t s)
 // copy of the activation rows (a_f16, a_mul).
 moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
 
+// bf16 rows -> NVFP4 codes [rows, K/2] of the grouped layout and scale-factor
+// atoms per (128-row tile of a group, 256-wide K stage), zeroed first
+// (sf_bytes); gs = 2688 / amax as moe_nvfp4_quantize. With `dest` (inverse
+// permutation, [src_rows * k]) token t's row goes to dest[t*k + j] and, with
+// shared_base >= 0, to shared_base + t; without it source row r is row r.
+moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
+                                 int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
+                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, cudaStream_t s,
+                                 bool pdl = false);
+
 // bf16 rows -> f16 rows scaled by a power of two so that each row's largest
 // magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it. Row r of dst is
 // row src_index[r] of src (row r when src_index is null).
@@ -118,6 +128,11 @@ moe_status launch_rows_to_f16(const uint16_t* src, const int32_t* src_index, int
 
 // W4A4: block-scaled FP4 tcgen05 kernel (every non-empty group).
 moe_status launch_gemm_tc_w4a4(const GemmPlan& p, cudaStream_t s);
+
+// W4A4 GEMM of the fused forward: activation codes in group order (a, a_rows
+// rows) loaded as tensor-map boxes, their scales as per-tile atoms (a_sf, from
+// launch_quantize_tiles), two CTAs per SM.
+moe_status launch_gemm_tc_fp4(const GemmPlan& p, cudaStream_t s);
 
 // Groups with at most this many rows take the small-group path.
 constexpr int kSmallGroupRows = 32;

@@ -10,6 +10,8 @@
 // discussion, follow-up on the MoE fault).
 // Combine: same guide, section 7.1 ([Combine]) and section 4.3 (top-k weight
 // reduction).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -137,6 +139,145 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
   const int blocks = (int)((nblk + 255) / 256);
   cudaError_t e = launch_ex(pdl, quantize_bf16_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s, x, rows,
                             K, amax, q, sf, gs_out);
+  if (e != cudaSuccess) return cuda_ok(e);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Quantisation of the block-scaled GEMM's activation rows straight into the
+// layout its loaders copy. Row r of the grouped layout gets its codes at
+// q[r][K/2] (row-major, so 2-D tensor-map boxes of a group's rows are plain
+// tiles) and its E4M3 scales in the scale-factor atoms of its 128-row tile:
+// the tiles of group g are numbered from tile_base[g] = sum over g' < g of
+// ceil(rows(g') / 128), and tile t, 256-wide K stage ks, 64-wide step kk hold
+// one 512-byte atom at ((t * K/256 + ks) * 4 + kk) * 512 whose byte
+// m0 * 16 + m1 * 4 + j is scale j of tile row 32 * m1 + m0 (the layout
+// tcgen05.cp 32x128b.warpx4 moves into tensor memory). The atoms start zeroed
+// (tile rows past a group's end keep scale 0, so whatever codes a box brings
+// for them contribute nothing).
+//
+// One warp per source row, quantised once: with `dest` (the inverse
+// permutation, [rows_src * k]) the row of token t goes to dest[t*k + j] for
+// each j with a valid slot and, with `shared_base` >= 0, to row
+// shared_base + t; without it, source row r is row r. A lane takes 4
+// consecutive 16-blocks (one 4-byte scale word per destination). The
+// arithmetic per 16-block is quantize_bf16_kernel's.
+constexpr int kQtWarps = 8;
+constexpr int kQtMaxDest = 33;
+
+__device__ __forceinline__ void quant_block16(const uint16_t* src, float gs, uint32_t& lo4, uint32_t& hi4,
+                                              uint32_t& code) {
+  const uint4 v0 = ldg_stream(reinterpret_cast<const uint4*>(src));
+  const uint4 v1 = ldg_stream(reinterpret_cast<const uint4*>(src) + 1);
+  const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float f[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f[2 * j] = __uint_as_float(wv[j] << 16);
+    f[2 * j + 1] = __uint_as_float(wv[j] & 0xffff0000u);
+  }
+  float bmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
+  const float sc = __fmul_rn(__fdiv_rn(bmax, 6.0f), gs);
+  code = e4m3_encode_sat(sc);
+  const float sval = e4m3_decode(code);
+  lo4 = hi4 = 0;
+  if (sval > 0.0f) {
+    const float rr = __fdiv_rn(gs, sval);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float y = __fmul_rn(f[j], rr);
+      const uint32_t c = e2m1_code_mag(fabsf(y)) | (signbit(y) ? 8u : 0u);
+      if (j < 8) lo4 |= c << (4 * j);
+      else hi4 |= c << (4 * (j - 8));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
+    const uint16_t* __restrict__ x, int src_rows, int K, const int32_t* __restrict__ dest, int k, int shared_base,
+    const int32_t* __restrict__ gofs, int G, const float* __restrict__ amax_p, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sf_tiles, float* __restrict__ gs_out) {
+  pdl_wait();
+  extern __shared__ int tile_base[];  // [G + 1]
+  if (threadIdx.x < 32) {  // exclusive prefix of ceil(rows / 128) over the groups
+    int carry = 0;
+    for (int g0 = 0; g0 <= G; g0 += 32) {
+      const int g = g0 + (int)threadIdx.x;
+      const int v = g < G ? (gofs[g + 1] - gofs[g] + 127) / 128 : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((int)threadIdx.x >= o) incl += t;
+      }
+      if (g <= G) tile_base[g] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+  const float amax = *amax_p;
+  const float gs = amax > 0.0f ? 2688.0f / amax : 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && gs_out != nullptr) *gs_out = gs;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kQtWarps + (threadIdx.x >> 5);
+  if (row >= src_rows) return;
+  // destinations of this source row: lane d < ndest holds (row r, tile t, tile row m)
+  const int ndest = dest ? k + (shared_base >= 0 ? 1 : 0) : 1;
+  int my_r = -1, my_t = 0, my_m = 0;
+  if (lane < ndest) {
+    my_r = dest ? (lane < k ? dest[(size_t)row * k + lane] : shared_base + row) : row;
+    if (my_r >= 0) {
+      int lo = 0, hi = G - 1;  // group of row my_r: the last g with gofs[g] <= my_r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(gofs + mid) <= my_r) lo = mid; else hi = mid - 1;
+      }
+      const int local = my_r - __ldg(gofs + lo);
+      my_t = tile_base[lo] + local / 128;
+      my_m = local % 128;
+    }
+  }
+  const int KB16 = K / 16, KS = K / 256;
+  const uint16_t* src = x + (size_t)row * K;
+  for (int qd = lane; qd < KB16 / 4; qd += 32) {  // 4 consecutive 16-blocks
+    uint32_t c4[8], sw = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t code;
+      quant_block16(src + (size_t)(4 * qd + i) * 16, gs, c4[2 * i], c4[2 * i + 1], code);
+      sw |= code << (8 * i);
+    }
+    const int kb = 4 * qd, ks = kb / 16, kk = (kb / 4) & 3;
+    for (int d = 0; d < ndest; ++d) {
+      const int r = __shfl_sync(0xffffffffu, my_r, d);
+      const int t = __shfl_sync(0xffffffffu, my_t, d);
+      const int m = __shfl_sync(0xffffffffu, my_m, d);
+      if (r < 0) continue;
+      uint4* qd_dst = reinterpret_cast<uint4*>(q + (size_t)r * (K / 2) + (size_t)kb * 8);
+      qd_dst[0] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+      qd_dst[1] = make_uint4(c4[4], c4[5], c4[6], c4[7]);
+      *reinterpret_cast<uint32_t*>(sf_tiles + (((size_t)t * KS + ks) * 4 + kk) * 512 + (m & 31) * 16 +
+                                   (m >> 5) * 4) = sw;
+    }
+  }
+}
+
+moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
+                                 int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
+                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, cudaStream_t s, bool pdl) {
+  if (K % 256 || G <= 0 || (dest && k + 1 > kQtMaxDest)) return MOE_ERR_UNSUPPORTED;
+  if (src_rows == 0) return MOE_OK;
+  moe_status st = cuda_ok(cudaMemsetAsync(sf_tiles, 0, sf_bytes, s));
+  if (st != MOE_OK) return st;
+  const int blocks = (src_rows + kQtWarps - 1) / kQtWarps;
+  const size_t smem = (size_t)(G + 1) * sizeof(int);
+  // after the memset the kernel is an ordinary stream successor (no programmatic launch)
+  (void)pdl;
+  cudaError_t e = launch_ex(false, quantize_tiles_kernel, dim3(blocks), dim3(kQtWarps * 32), smem, s, x, src_rows, K,
+                            dest, k, shared_base, gofs, G, amax, q, sf_tiles, gs_out);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
