@@ -123,9 +123,11 @@ __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
 
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
 
-// SiLU z * sigmoid(z) with the hardware exp2 approximation and a rounded
-// reciprocal: relative error a few ulp of fp32, far below the bf16 rounding
-// of the result. Large negative z gives exp -> inf and a result of -0.
-__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+// SiLU z * sigmoid(z) with the hardware exp2 approximation and the fast
+// division (relative error a few ulp of fp32, far below the bf16 rounding of
+// the result). The IEEE reciprocal or division costs tens of instructions per
+// element and dominated the GEMM epilogues. Large negative z gives exp -> inf
+// and a result of -0.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 }  // namespace moe

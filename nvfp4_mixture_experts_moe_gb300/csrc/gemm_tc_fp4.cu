@@ -15,8 +15,10 @@
 //   tensor-map box (16/32/64/128 rows x 128 bytes, 128-byte swizzle) and the
 //   tile's four scale-factor atoms, written in that layout by the quantiser
 //   (rows past the group carry scale 0), with one bulk copy.
-// * One thread moves the eight atoms into tensor memory (tcgen05.cp
-//   32x128b.warpx4) and issues the MMAs; four epilogue warps apply alpha and
+// * One thread moves the stage's eight atoms into tensor memory (tcgen05.cp
+//   32x128b.warpx4) and commits them; another issues the four MMAs (each
+//   tcgen05 instruction costs its issuing thread tens of cycles, so the two
+//   streams run in parallel); four epilogue warps apply alpha and
 //   the activations' 1/gs, SwiGLU (gate/up, with the amax of h for its
 //   quantisation) or the routing weight (down), and store bf16.
 // Two CTAs share an SM: each has one accumulator (128 TMEM columns) and
@@ -52,7 +54,8 @@ constexpr int kEpiWarp0 = 0;                // warps 0..3
 constexpr int kMmaWarp = 4;
 constexpr int kALoadWarp = 5;
 constexpr int kBLoadWarp = 6;
-constexpr int kThreads = 7 * 32;
+constexpr int kSfWarp = 7;
+constexpr int kThreads = 8 * 32;
 constexpr int kTmemCols = 256;
 constexpr uint32_t kSfCol0 = 128;           // accumulator [0, 128); scale factors 32 columns per stage
 static_assert(kSfCol0 + 32 * kStages <= kTmemCols, "TMEM columns");
@@ -78,10 +81,12 @@ struct Args {
 
 struct Smem {
   uint64_t ready[kStages];  // both loaders' bytes landed (two expect_tx arrivals)
+  uint64_t sf_full[kStages];  // the stage's scale factors are in tensor memory
   uint64_t empty[kStages];  // the stage's MMAs completed
   uint64_t tfull;
   uint64_t tempty;
   uint64_t drain;
+  uint64_t drain_sf;
   uint32_t tmem_base;
   int abort;
 };
@@ -148,11 +153,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
     tb[0] = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm->ready[i], 2);
+      mbar_init(&sm->sf_full[i], 1);
       mbar_init(&sm->empty[i], 1);
     }
     mbar_init(&sm->tfull, 1);
     mbar_init(&sm->tempty, 128);
     mbar_init(&sm->drain, 1);
+    mbar_init(&sm->drain_sf, 1);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -235,6 +242,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
       }
     }
     __syncwarp();
+  } else if (warp == kSfWarp) {
+    // ------------------------------------------------- scale factors -> TMEM
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kStages;
+          // the slot's previous MMAs completed before its loads were issued, so
+          // its TMEM columns are free once the new data has landed
+          if (!mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sfa = smem_u32(base + slot * kStageBytes) + 2 * kTile;
+          const uint32_t sfb = sfa + kSfStage;
+          const uint32_t sf_col = tmem + kSfCol0 + slot * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
+            tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
+          }
+          tc_commit(&sm->sf_full[slot]);
+        }
+        if (!ok) break;
+      }
+      tc_commit(&sm->drain_sf);
+      drain_wait(&sm->drain_sf, 0);
+    }
+    __syncwarp();
   } else if (warp < kEpiWarp0 + 4) {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;
@@ -313,18 +348,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->sf_full[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
           tc_fence_after();
           const uint32_t as = smem_u32(base + slot * kStageBytes);
           const uint32_t bs = as + kTile;
-          const uint32_t sfa = as + 2 * kTile;
-          const uint32_t sfb = sfa + kSfStage;
           const uint32_t sf_col = tmem + kSfCol0 + slot * 32;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
-            tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
-          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
