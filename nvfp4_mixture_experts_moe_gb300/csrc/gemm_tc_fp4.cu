@@ -41,11 +41,10 @@ namespace {
 
 using namespace tc;
 
-constexpr int kCtasPerSm = 2;
 constexpr int kM = 128;
 constexpr int kBK = 256;                    // K per stage
 constexpr int kRowBytes = 128;              // one operand row per stage: 256 FP4
-constexpr int kStages = 3;
+constexpr int kMaxStages = 6;
 constexpr int kMaxBN = 128;
 constexpr int kTile = kM * kRowBytes;       // 16 KB (A; B at most the same)
 constexpr int kSfStage = 4 * 512;           // four atoms
@@ -56,10 +55,22 @@ constexpr int kALoadWarp = 5;
 constexpr int kBLoadWarp = 6;
 constexpr int kSfWarp = 7;
 constexpr int kThreads = 8 * 32;
-constexpr int kTmemCols = 256;
-constexpr uint32_t kSfCol0 = 128;           // accumulator [0, 128); scale factors 32 columns per stage
-static_assert(kSfCol0 + 32 * kStages <= kTmemCols, "TMEM columns");
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
+
+// Two shapes: two CTAs per SM, each with one accumulator and three stages
+// (two independent MMA issuers; a CTA's MMAs stall while its accumulator
+// drains), or one CTA per SM with two accumulators and six stages (the
+// epilogue overlaps the next tile's MMAs). TMEM: accumulators of 128 columns,
+// then 32 columns of scale factors per stage.
+template <int CTAS>
+struct Shape {
+  static constexpr int kStages = CTAS == 2 ? 3 : 6;
+  static constexpr int kAcc = CTAS == 2 ? 1 : 2;
+  static constexpr int kTmemCols = CTAS == 2 ? 256 : 512;
+  static constexpr uint32_t kSfCol0 = 128 * kAcc;
+  static_assert(kSfCol0 + 32 * kStages <= kTmemCols, "TMEM columns");
+  static_assert(kStages <= kMaxStages, "stages");
+};
 
 struct BoxMaps {
   CUtensorMap m[4];
@@ -80,11 +91,11 @@ struct Args {
 };
 
 struct Smem {
-  uint64_t ready[kStages];  // both loaders' bytes landed (two expect_tx arrivals)
-  uint64_t sf_full[kStages];  // the stage's scale factors are in tensor memory
-  uint64_t empty[kStages];  // the stage's MMAs completed
-  uint64_t tfull;
-  uint64_t tempty;
+  uint64_t ready[kMaxStages];    // both loaders' bytes landed (two expect_tx arrivals)
+  uint64_t sf_full[kMaxStages];  // the stage's scale factors are in tensor memory
+  uint64_t empty[kMaxStages];    // the stage's MMAs completed
+  uint64_t tfull[2];
+  uint64_t tempty[2];
   uint64_t drain;
   uint64_t drain_sf;
   uint32_t tmem_base;
@@ -126,9 +137,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const __grid_constant__ BoxMaps maps,
-                                                                           Args p) {
+template <bool GATE_UP, int CTAS>
+__global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __grid_constant__ BoxMaps maps, Args p) {
+  constexpr int kStages = Shape<CTAS>::kStages;
+  constexpr int kAcc = Shape<CTAS>::kAcc;
+  constexpr int kTmemCols = Shape<CTAS>::kTmemCols;
+  constexpr uint32_t kSfCol0 = Shape<CTAS>::kSfCol0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // per stage: A tile | B tile | SFA atoms | SFB atoms
@@ -156,8 +170,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
       mbar_init(&sm->sf_full[i], 1);
       mbar_init(&sm->empty[i], 1);
     }
-    mbar_init(&sm->tfull, 1);
-    mbar_init(&sm->tempty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm->tfull[i], 1);
+      mbar_init(&sm->tempty[i], 128);
+    }
     mbar_init(&sm->drain, 1);
     mbar_init(&sm->drain_sf, 1);
     sm->abort = 0;
@@ -285,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
         const int n = 32 * i + lane;
         rsv[i] = (!GATE_UP && p.row_scale && n < it.rows) ? __ldg(p.row_scale + it.row0 + n) : 1.0f;
       }
-      if (!mbar_wait(&sm->tfull, itc & 1, abort, kWaitLimit)) break;
+      const int acc = itc % kAcc;
+      if (!mbar_wait(&sm->tfull[acc], (itc / kAcc) & 1, abort, kWaitLimit)) break;
       tc_fence_after();
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
       const float a0 = hdr->alpha[0] * inv_gs_b, a1 = hdr->alpha[1] * inv_gs_b;
@@ -293,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
       const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
       for (int c0 = 0; c0 < it.bn; c0 += 32) {  // columns past bn are read (within the buffer) and not stored
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * 128 + c0, r);
         tmem_ld_wait();
         if (GATE_UP) {
           // the gate lane finishes columns c0..c0+15, its up partner (lane ^ 8) c0+16..c0+31
@@ -329,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm->tempty);
+      mbar_arrive(&sm->tempty[acc]);
     }
     if (GATE_UP && p.out_amax != nullptr) {
 #pragma unroll
@@ -342,7 +359,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
       int j = 0, itc = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
         const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
-        if (!mbar_wait(&sm->tempty, (itc & 1) ^ 1, abort, kWaitLimit)) break;
+        const int acc = itc % kAcc;
+        if (!mbar_wait(&sm->tempty[acc], ((itc / kAcc) & 1) ^ 1, abort, kWaitLimit)) break;
+        const uint32_t d = tmem + acc * 128;
         tc_fence_after();
         const uint32_t idesc = idesc_nvf4(kM, it.bn);
         bool ok = true;
@@ -357,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_fp4_kernel(const
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
-            mma_nvf4(tmem, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4, (ks | kk) != 0);
+            mma_nvf4(d, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4, (ks | kk) != 0);
           }
           tc_commit(&sm->empty[slot]);
         }
         if (!ok) break;
-        tc_commit(&sm->tfull);
+        tc_commit(&sm->tfull[acc]);
       }
       tc_commit(&sm->drain);
       drain_wait(&sm->drain, 0);
@@ -392,8 +411,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 
 }  // namespace
 
-static size_t fp4_smem_bytes(int G) {
-  return 1024 + (size_t)kStages * kStageBytes + sizeof(Smem) + (size_t)(G + 1) * 8;
+static size_t fp4_smem_bytes(int G, int stages) {
+  return 1024 + (size_t)stages * kStageBytes + sizeof(Smem) + (size_t)(G + 1) * 8;
 }
 
 moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
@@ -428,14 +447,16 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   a.out = pl.out;
   a.out_amax = pl.out_amax;
   a.status = pl.status;
-  const size_t smem = fp4_smem_bytes(pl.num_groups);
-  if (smem > 113 * 1024) return MOE_ERR_UNSUPPORTED;  // two CTAs per SM
+  const int ctas = pl.ctas_per_sm == 1 ? 1 : 2;
+  const size_t smem = fp4_smem_bytes(pl.num_groups, ctas == 2 ? Shape<2>::kStages : Shape<1>::kStages);
+  if (smem > (ctas == 2 ? 113 : 227) * 1024) return MOE_ERR_UNSUPPORTED;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  auto k = pl.gate_up ? gemm_tc_fp4_kernel<true> : gemm_tc_fp4_kernel<false>;
+  auto k = ctas == 2 ? (pl.gate_up ? gemm_tc_fp4_kernel<true, 2> : gemm_tc_fp4_kernel<false, 2>)
+                     : (pl.gate_up ? gemm_tc_fp4_kernel<true, 1> : gemm_tc_fp4_kernel<false, 1>);
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * kCtasPerSm), dim3(kThreads), smem, s, maps, a);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * ctas), dim3(kThreads), smem, s, maps, a);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;

@@ -96,6 +96,7 @@ struct GemmPlan {
   bool pdl;                 // programmatic dependent launch (inside the fused forward)
   bool early_weights;       // group offsets are final before the predecessor ends: weights may
                             // stream before the dependency wait (only with pdl)
+  int ctas_per_sm;          // W4A4 tile GEMM shape: 2 (default) or 1 (two accumulators)
 };
 
 // Small-group path: mma.sync m16n8k16 over register-dequantised weights; one
