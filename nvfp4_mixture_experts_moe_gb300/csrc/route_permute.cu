@@ -18,7 +18,8 @@ namespace moe {
 // probabilities renormalised over the top k.
 template <int PER_LANE>
 __device__ __forceinline__ void route_token(const float* __restrict__ logits, int token, int E, int k,
-                                            int32_t* __restrict__ ids, float* __restrict__ w) {
+                                            int32_t* __restrict__ ids, float* __restrict__ w,
+                                            int32_t* sids = nullptr, float* sw = nullptr) {
   const int lane = threadIdx.x & 31;
   const float* row = logits + (size_t)token * E;
   float v[PER_LANE];
@@ -70,6 +71,10 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
   if (lane < k) {
     ids[(size_t)token * k + lane] = my_id;
     w[(size_t)token * k + lane] = ex / sum;
+    if (sids != nullptr) {  // shared-memory copies for the fused single-CTA kernel
+      sids[token * k + lane] = my_id;
+      sw[token * k + lane] = ex / sum;
+    }
   }
 }
 
@@ -122,12 +127,14 @@ constexpr int kPermChunk = 4096;  // pairs per chunk in the multi-CTA path
 
 __device__ __forceinline__ void scatter_warp(const int32_t* __restrict__ ids, int p0, int p1, int E,
                                              int* cursor /* smem [E] */, int32_t* perm,
-                                             int32_t* inv_perm, int* status) {
+                                             int32_t* inv_perm, int* status, const int32_t* lids = nullptr,
+                                             int32_t* lperm = nullptr) {
   const int lane = threadIdx.x & 31;
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     const bool in = p < p1;
-    int e = in ? __ldcg(ids + p) : -1;  // L2 load: ids may have been written earlier in this kernel
+    // ids written earlier in the same kernel: the shared copy, else an L2 load
+    int e = in ? (lids ? lids[p] : __ldcg(ids + p)) : -1;
     const bool valid = in && e >= 0 && e < E;
     if (in && !valid) set_status(status, MOE_ERR_DEVICE);
     const int key = valid ? e : -1 - lane;  // invalid lanes never match each other
@@ -140,6 +147,7 @@ __device__ __forceinline__ void scatter_warp(const int32_t* __restrict__ ids, in
     if (valid) {
       perm[slot] = p;
       inv_perm[p] = slot;
+      if (lperm) lperm[slot] = p;
       // highest lane of the peer group advances the cursor
       if ((peers >> lane) == 1u) cursor[e] += __popc(peers);
     } else if (in) {
@@ -159,14 +167,15 @@ struct RowInfoOut {
   int32_t* gofs;         // [E+2] or nullptr: offsets[0..E-1], then P, then P + T
 };
 
-__device__ void write_row_info(const RowInfoOut& ri, const int32_t* perm, int P) {
+__device__ void write_row_info(const RowInfoOut& ri, const int32_t* perm, int P, const int32_t* lperm = nullptr,
+                               const float* lw = nullptr) {
   if (ri.row_token == nullptr) return;
   for (int r = threadIdx.x; r < P + ri.T; r += blockDim.x) {
     if (r < P) {
-      const int p = perm[r];
+      const int p = lperm ? lperm[r] : perm[r];
       const bool ok = p >= 0 && p < P;
       ri.row_token[r] = ok ? p / ri.k : 0;
-      ri.row_weight[r] = ok ? ri.topk_w[p] : 0.0f;
+      ri.row_weight[r] = ok ? (lw ? lw[p] : ri.topk_w[p]) : 0.0f;
     } else {
       ri.row_token[r] = r - P;
       ri.row_weight[r] = 1.0f;
@@ -217,16 +226,21 @@ __device__ void block_exclusive_scan(int* data, int n, int* tmp /* smem [32] */)
 
 __device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int E, int32_t* counts,
                                     int32_t* offsets, int32_t* perm, int32_t* inv_perm, int* status,
-                                    const RowInfoOut& ri) {
+                                    const RowInfoOut& ri, const int32_t* lids = nullptr, const float* lw = nullptr,
+                                    int32_t* lperm = nullptr) {
   extern __shared__ int smem[];
   int* cnt = smem;            // [E]
   int* cursor = smem + E;     // [E]
   int* tmp = smem + 2 * E;    // [32]
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-  for (int p = threadIdx.x; p < P; p += blockDim.x) perm[p] = -1;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    perm[p] = -1;
+    if (lperm) lperm[p] = -1;
+  }
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int e = __ldcg(ids + p);  // L2 load: ids may have been written earlier in this kernel
+    // ids written earlier in the same kernel: the shared copy, else an L2 load
+    const int e = lids ? lids[p] : __ldcg(ids + p);
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
@@ -248,10 +262,10 @@ __device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int 
     }
   }
   __syncthreads();
-  if (threadIdx.x < 32) scatter_warp(ids, 0, P, E, cursor, perm, inv_perm, status);
+  if (threadIdx.x < 32) scatter_warp(ids, 0, P, E, cursor, perm, inv_perm, status, lids, lperm);
   __syncthreads();
   __threadfence_block();
-  write_row_info(ri, perm, P);
+  write_row_info(ri, perm, P, lperm, lw);
 }
 
 __global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __restrict__ ids, int P,
@@ -270,10 +284,16 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(const float* 
                                                                    int32_t* counts, int32_t* offsets,
                                                                    int32_t* perm, int32_t* inv_perm,
                                                                    int* status, RowInfoOut ri) {
-  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5) route_token<PER_LANE>(logits, t, E, k, ids, w);
+  extern __shared__ int smem_rp[];
+  const int P = T * k;
+  // after the permutation's own shared arrays ([2E + 32] ints): ids, weights, perm of the pairs
+  int32_t* sids = smem_rp + 2 * E + 32;
+  float* sw = reinterpret_cast<float*>(sids + P);
+  int32_t* sperm = reinterpret_cast<int32_t*>(sw + P);
+  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5)
+    route_token<PER_LANE>(logits, t, E, k, ids, w, sids, sw);
   __syncthreads();
-  __threadfence_block();
-  permute_single_body(ids, T * k, E, counts, offsets, perm, inv_perm, status, ri);
+  permute_single_body(ids, P, E, counts, offsets, perm, inv_perm, status, ri, sids, sw, sperm);
 }
 
 moe_status launch_route_permute_small(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -281,7 +301,8 @@ moe_status launch_route_permute_small(const float* logits, int T, int E, int k, 
                                       int* status, int32_t* row_token, float* row_weight, int32_t* gofs,
                                       cudaStream_t s) {
   RowInfoOut ri{row_token, row_weight, w, k, T, gofs};
-  const size_t smem = (2 * (size_t)E + 32) * sizeof(int);
+  const size_t smem = (2 * (size_t)E + 32 + 3 * (size_t)T * k) * sizeof(int);
+  if (smem > 48 * 1024) return MOE_ERR_UNSUPPORTED;
   const int per = (E + 31) / 32;
 #define MOE_RP_CASE(PL)                                                                                  \
   if (per <= PL) {                                                                                       \
@@ -294,6 +315,7 @@ moe_status launch_route_permute_small(const float* logits, int T, int E, int k, 
   MOE_RP_CASE(2)
   MOE_RP_CASE(4)
   MOE_RP_CASE(8)
+  MOE_RP_CASE(10)
   MOE_RP_CASE(16)
   MOE_RP_CASE(32)
 #undef MOE_RP_CASE
