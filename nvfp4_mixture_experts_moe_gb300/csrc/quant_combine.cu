@@ -67,14 +67,15 @@ moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream
   return cuda_ok(cudaGetLastError());
 }
 
-// e2m1 code of |y| (0..7), round to nearest with ties to the even code,
-// saturating at 6: the thresholds are the midpoints of the grid
-// {0, .5, 1, 1.5, 2, 3, 4, 6}; at a midpoint the even code wins, so the
-// comparison is strict where the lower neighbour is even and non-strict where
-// the upper one is.
-__device__ __forceinline__ uint32_t e2m1_code_mag(float a) {
-  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+// e2m1 codes of two fp32 values with the hardware conversion: round to
+// nearest, ties to the even code, saturating at 6, the sign kept (also on a
+// zero result); `lo` lands in bits 0-3 of the byte, `hi` in bits 4-7.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("{\n .reg .b8 b;\n cvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n cvt.u16.u8 %0, b;\n}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r & 0xffu;
 }
 
 // E4M3 (fn) encoding of a non-negative fp32, nearest-even, saturating at 448.
@@ -122,11 +123,10 @@ __global__ void __launch_bounds__(256) quantize_bf16_kernel(const uint16_t* __re
   if (sval > 0.0f) {
     const float r = __fdiv_rn(gs, sval);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float y = __fmul_rn(f[j], r);
-      const uint32_t c = e2m1_code_mag(fabsf(y)) | (signbit(y) ? 8u : 0u);
-      if (j < 8) lo |= c << (4 * j);
-      else hi |= c << (4 * (j - 8));
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t b = e2m1x2_rn(__fmul_rn(f[2 * j], r), __fmul_rn(f[2 * j + 1], r));
+      if (j < 4) lo |= b << (8 * j);
+      else hi |= b << (8 * (j - 4));
     }
   }
   *reinterpret_cast<uint2*>(q + b * 8) = make_uint2(lo, hi);
@@ -187,11 +187,10 @@ __device__ __forceinline__ void quant_block16(const uint16_t* src, float gs, uin
   if (sval > 0.0f) {
     const float rr = __fdiv_rn(gs, sval);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float y = __fmul_rn(f[j], rr);
-      const uint32_t c = e2m1_code_mag(fabsf(y)) | (signbit(y) ? 8u : 0u);
-      if (j < 8) lo4 |= c << (4 * j);
-      else hi4 |= c << (4 * (j - 8));
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t b = e2m1x2_rn(__fmul_rn(f[2 * j], rr), __fmul_rn(f[2 * j + 1], rr));
+      if (j < 4) lo4 |= b << (8 * j);
+      else hi4 |= b << (8 * (j - 4));
     }
   }
 }
