@@ -115,6 +115,13 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Two floats -> two bf16 (round to nearest even) in one conversion: `lo` in
+// bits 0-15, `hi` in bits 16-31.
+__device__ __forceinline__ uint32_t float2_to_bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // atomic max of a non-negative float via its integer bit pattern (exact and
 // order-independent).
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {

@@ -358,13 +358,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
             const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + cb + c4);  // broadcast read
             const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int c = c4 + t;
-              const float own = __uint_as_float(gate_lane ? r[c] : r[16 + c]);
-              const float g = (gate_lane ? own : other[c]) * mv[t];
-              const float u = (gate_lane ? other[c] : own) * mv[t];
-              const int n = c0 + cb + c;
-              if (n < it.rows) p.out[(size_t)(it.row0 + n) * (N / 2) + f] = float_to_bf16_bits(silu(g * a0) * (u * a1));
+            for (int t = 0; t < 4; t += 2) {  // two tokens per bf16 conversion
+              float h2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int c = c4 + t + e;
+                const float own = __uint_as_float(gate_lane ? r[c] : r[16 + c]);
+                const float g = (gate_lane ? own : other[c]) * mv[t + e];
+                const float u = (gate_lane ? other[c] : own) * mv[t + e];
+                h2[e] = silu(g * a0) * (u * a1);
+              }
+              const uint32_t hb = float2_to_bf16x2_bits(h2[0], h2[1]);
+              const int n = c0 + cb + c4 + t;
+              uint16_t* o = p.out + (size_t)(it.row0 + n) * (N / 2) + f;
+              if (n < it.rows) o[0] = (uint16_t)(hb & 0xffffu);
+              if (n + 1 < it.rows) o[N / 2] = (uint16_t)(hb >> 16);
             }
           }
         } else {
@@ -373,10 +381,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
             const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + c4);  // broadcast read
             const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
+            for (int t = 0; t < 4; t += 2) {  // two tokens per bf16 conversion
+              const uint32_t yb = float2_to_bf16x2_bits(__uint_as_float(r[c4 + t]) * mv[t] * a0,
+                                                        __uint_as_float(r[c4 + t + 1]) * mv[t + 1] * a0);
               const int n = c0 + c4 + t;
-              const float v = __uint_as_float(r[c4 + t]) * mv[t];
-              if (n < it.rows) p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(v * a0);
+              uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
+              if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
+              if (n + 1 < it.rows) o[N] = (uint16_t)(yb >> 16);
             }
           }
         }
