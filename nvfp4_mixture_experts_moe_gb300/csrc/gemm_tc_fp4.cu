@@ -320,15 +320,25 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
           for (int c = 0; c < 16; ++c)
             other[c] = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? r[16 + c] : r[c]), 8);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float own = __uint_as_float(gate_lane ? r[c] : r[16 + c]);
-            const float g = gate_lane ? own : other[c];
-            const float u = gate_lane ? other[c] : own;
+          for (int c = 0; c < 16; c += 2) {  // two tokens per bf16 conversion
+            float h2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float own = __uint_as_float(gate_lane ? r[c + e] : r[16 + c + e]);
+              const float g = gate_lane ? own : other[c + e];
+              const float u = gate_lane ? other[c + e] : own;
+              h2[e] = silu(g * a0) * (u * a1);
+            }
+            const uint32_t hb = float2_to_bf16x2_bits(h2[0], h2[1]);
             const int n = c0 + cb + c;
+            uint16_t* o = p.out + (size_t)(it.row0 + n) * (N / 2) + f;
             if (n < it.rows) {
-              const uint16_t hb = float_to_bf16_bits(silu(g * a0) * (u * a1));
-              p.out[(size_t)(it.row0 + n) * (N / 2) + f] = hb;
-              amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)hb << 16)));
+              o[0] = (uint16_t)(hb & 0xffffu);
+              amax = fmaxf(amax, fabsf(__uint_as_float(hb << 16)));
+            }
+            if (n + 1 < it.rows) {
+              o[N / 2] = (uint16_t)(hb >> 16);
+              amax = fmaxf(amax, fabsf(__uint_as_float(hb & 0xffff0000u)));
             }
           }
         } else {
@@ -337,11 +347,15 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
           for (int i = 0; i < kMaxBN / 32; ++i)
             if ((c0 >> 5) == i) rs_chunk = rsv[i];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < 32; c += 2) {  // two tokens per bf16 conversion
             const int n = c0 + c;
-            const float rs = __shfl_sync(0xffffffffu, rs_chunk, c);
-            if (n < it.rows)
-              p.out[(size_t)(it.row0 + n) * N + it.mt * kM + rho] = float_to_bf16_bits(__uint_as_float(r[c]) * a0 * rs);
+            const float rs0 = __shfl_sync(0xffffffffu, rs_chunk, c);
+            const float rs1 = __shfl_sync(0xffffffffu, rs_chunk, c + 1);
+            const uint32_t yb = float2_to_bf16x2_bits(__uint_as_float(r[c]) * a0 * rs0,
+                                                      __uint_as_float(r[c + 1]) * a0 * rs1);
+            uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
+            if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
+            if (n + 1 < it.rows) o[N] = (uint16_t)(yb >> 16);
           }
         }
       }
