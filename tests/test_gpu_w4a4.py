@@ -44,6 +44,24 @@ def test_w4a4_small_layer_full_check():
     check_outputs(out, ref, what="w4a4 small")
 
 
+# skewed routing at a small size: empty groups, groups of several 128-row
+# tiles and ragged last tiles through the fused forward's tile quantiser and
+# its block-scaled GEMMs
+GROUPS = si.LayerConfig("w4a4_groups", T=300, H=512, I=256, I_s=256, E=24, k=4, mode="w4a4", logits="zipf")
+
+
+def test_w4a4_skewed_groups_full_check():
+    cfg, layer, x, logits, out, ids = _run(GROUPS)
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    assert (counts == 0).any() and counts.max() > 128  # the cases this test is for
+    ow = OracleWeights(cfg)
+    experts, shared = ow.all()
+    ref, parts = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k, mode="w4a4",
+                            return_parts=True)
+    assert (ids == parts["ids"]).all()
+    check_outputs(out, ref, what="w4a4 skewed groups")
+
+
 def test_w4a4_small_deterministic():
     cfg, layer = device_layer(SMALL)
     x = si.make_x(cfg).cuda()
