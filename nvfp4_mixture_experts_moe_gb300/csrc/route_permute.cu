@@ -375,16 +375,40 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* chunk_hist,
   }
 }
 
-__global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                                               const int32_t* chunk_base, int32_t* perm,
-                                                               int32_t* inv_perm, int* status) {
+// Phase 3 inside a chunk: kScatterWarps warps take consecutive sub-chunks;
+// each counts its own pairs per expert, the counts are scanned across the
+// warps on top of the chunk's base, and every warp then scatters its
+// sub-chunk in order (stable: earlier sub-chunks get the lower slots).
+constexpr int kScatterWarps = 8;
+
+__global__ void __launch_bounds__(kScatterWarps * 32) permute_scatter_kernel(const int32_t* __restrict__ ids, int P,
+                                                                            int E, const int32_t* chunk_base,
+                                                                            int32_t* perm, int32_t* inv_perm,
+                                                                            int* status) {
   pdl_wait();
-  extern __shared__ int cursor[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cursor[e] = chunk_base[(size_t)blockIdx.x * E + e];
+  extern __shared__ int cursor[];  // [kScatterWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) cursor[i] = 0;
   __syncthreads();
   const int p0 = blockIdx.x * kPermChunk;
   const int p1 = min(P, p0 + kPermChunk);
-  if (threadIdx.x < 32) scatter_warp(ids, p0, p1, E, cursor, perm, inv_perm, status);
+  constexpr int kSub = kPermChunk / kScatterWarps;
+  const int q0 = min(p1, p0 + warp * kSub), q1 = min(p1, q0 + kSub);
+  for (int p = q0 + lane; p < q1; p += 32) {
+    const int e = __ldg(ids + p);
+    if (e >= 0 && e < E) atomicAdd(&cursor[warp * E + e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = chunk_base[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int c = cursor[w * E + e];
+      cursor[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (q0 < q1) scatter_warp(ids, q0, q1, E, cursor + warp * E, perm, inv_perm, status);
 }
 
 __global__ void row_info_kernel(const int32_t* perm, int P, RowInfoOut ri) {
@@ -435,8 +459,8 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
                 nchunks, E, P, counts, offsets, gofs, T);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
-  e = launch_ex(pdl, permute_scatter_kernel, dim3(nchunks), dim3(32), (size_t)E * sizeof(int), s, ids, P, E,
-                (const int32_t*)hist, perm, inv_perm, status);
+  e = launch_ex(pdl, permute_scatter_kernel, dim3(nchunks), dim3(kScatterWarps * 32),
+                (size_t)kScatterWarps * E * sizeof(int), s, ids, P, E, (const int32_t*)hist, perm, inv_perm, status);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   if (row_token != nullptr) {
