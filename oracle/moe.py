@@ -144,7 +144,22 @@ def down_proj(h_rows, down):
     return h_rows @ down.dequantize().T
 
 
-def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False):
+def router_logits(x, w_router):
+    """Router GEMM: ``logits = x W_router^T`` in float64.
+
+    ``x`` ``[T, H]`` and ``w_router`` ``[E, H]`` hold bf16 values (exact in
+    float64). The pages name the router as the step ahead of top-k ("vLLM on
+    the NVIDIA DGX Spark", section 7.1, [Router]); the router matrix stays in
+    16-bit, outside the NVFP4 expert weights.
+    Pinned by: exact rational dot products (fractions) on tiny sizes; one-hot
+    router rows that pick out a scaled column of x exactly (tests).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w_router, dtype=np.float64)
+    return x @ w.T
+
+
+def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=None, h_gs=None):
     """The whole layer for ``T`` tokens, float64.
 
     ``x`` ``[T, H]`` (bf16 values), ``logits`` ``[T, E]`` fp32, ``experts`` a
@@ -156,10 +171,13 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False):
 
     W4A16: ``x`` enters the GEMMs as is. W4A4: ``x`` is quantised (one global
     scale) and dequantised first; ``h`` is rounded to bf16, quantised over all
-    rows with one global scale, and dequantised before the down GEMM.
+    rows with one global scale, and dequantised before the down GEMM. The two
+    W4A4 global scales are dynamic (from the tensors' amax) unless ``x_gs`` /
+    ``h_gs`` give static calibrated ones (quant convention).
     Pinned by: a dense formulation (every expert on every token, weighted by a
-    T x E routing matrix) on tiny sizes, the identical-experts invariant, and
-    the one-expert dense reduction (tests).
+    T x E routing matrix) on tiny sizes, the identical-experts invariant, the
+    one-expert dense reduction, and (static scales) the dynamic result when
+    the static scales equal the dynamic ones (tests).
     """
     x = np.asarray(x, dtype=np.float64)
     T, H = x.shape
@@ -169,7 +187,7 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False):
     parts = {"ids": ids, "w": w, "counts": counts, "offsets": offsets,
              "perm": perm, "inv_perm": inv_perm}
     if mode == "w4a4":
-        xq, xsf, xgs = nvfp4.quantize(x.astype(F32))
+        xq, xsf, xgs = nvfp4.quantize(x.astype(F32), gs=x_gs)
         parts.update(xq=xq, xsf=xsf, xgs=xgs)
         x_in = nvfp4.dequantize(xq, xsf, xgs)
     elif mode == "w4a16":
@@ -186,7 +204,7 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False):
         sizes = [h.shape[0] for h in hs]
         allh = np.concatenate(hs, axis=0)
         allh_bf = bf16_round(allh)
-        hq, hsf, hgs = nvfp4.quantize(allh_bf)
+        hq, hsf, hgs = nvfp4.quantize(allh_bf, gs=h_gs)
         parts.update(h_bf16=allh_bf, hq=hq, hsf=hsf, hgs=hgs)
         hs = np.split(nvfp4.dequantize(hq, hsf, hgs), np.cumsum(sizes)[:-1], axis=0)
     ys = [down_proj(h, trip[2]) for h, (trip, _) in zip(hs, groups)]

@@ -125,14 +125,19 @@ def global_scale(amax):
     return F32(QUANT_RANGE / amax)
 
 
-def quantize(x):
+def quantize(x, gs=None):
     """Quantise a 2-D tensor to NVFP4 with one per-tensor global scale.
 
     ``x`` is ``[rows, K]`` with ``K % 16 == 0``, given in any dtype whose values
     are exact in fp32 (bf16 activations and weights). Steps, each a correctly
     rounded fp32 operation:
 
-    1. ``amax = max |x|`` over the whole tensor, ``gs = 2688 / amax``;
+    1. ``amax = max |x|`` over the whole tensor, ``gs = 2688 / amax``; a
+       static (calibrated) ``gs`` given by the caller replaces this step
+       ("Serving Solar Open 2 on DGX Spark", "The fix": static and dynamic
+       W4A4 paths; "GLM-5.3-Flash-NVFP4 #4", calibrated per-projection input
+       scales). With a static scale a block can exceed the range: its scale
+       saturates at 448 and its codes at 6;
     2. per block of 16 along K: ``amax_b = max |x_i|``,
        ``s = (amax_b / 6) * gs``, ``sf = E4M3(s)`` (nearest even, clamp 448);
     3. if ``sf`` decodes to 0 the 16 codes are 0; otherwise
@@ -140,23 +145,32 @@ def quantize(x):
 
     Returns ``(codes [rows, K] uint8 unpacked, sf [rows, K/16] uint8, gs fp32)``.
     Pinned by: the golden worked scale; round-trip error bounds; g16 block
-    independence; the tie tables of the two encoders (tests).
+    independence; the tie tables of the two encoders; static scale: the
+    dynamic result when the static scale equals the dynamic one, the exponent
+    shift of the block scales under a power-of-two scale, the saturation of
+    out-of-range blocks (tests).
     """
     x = np.asarray(x, dtype=F32)
     rows, K = x.shape
     if K % 16:
         raise ValueError("K must be a multiple of 16")
-    amax = F32(np.max(np.abs(x))) if x.size else F32(0)
-    gs = global_scale(amax)
+    if gs is None:
+        amax = F32(np.max(np.abs(x))) if x.size else F32(0)
+        gs = global_scale(amax)
+    else:
+        gs = F32(gs)
+        if not (np.isfinite(gs) and gs > 0):
+            raise ValueError("a static global scale is positive and finite")
     blocks = x.reshape(rows, K // 16, 16)
     amax_b = np.max(np.abs(blocks), axis=2).astype(F32)
-    s = (amax_b / F32(E2M1_MAX)).astype(F32) * gs
-    s = s.astype(F32)
+    with np.errstate(over="ignore"):
+        s = ((amax_b / F32(E2M1_MAX)).astype(F32) * gs).astype(F32)
     sf = e4m3_encode(s).astype(np.uint8)
     sf_val = e4m3_decode(sf).astype(F32)
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.where(sf_val > 0, gs / np.where(sf_val > 0, sf_val, F32(1)), F32(0)).astype(F32)
-    y = (blocks * r[:, :, None]).astype(F32)
+    with np.errstate(over="ignore"):
+        y = (blocks * r[:, :, None]).astype(F32)
     codes = e2m1_encode(y)
     codes = np.where((sf_val > 0)[:, :, None], codes, np.uint8(0)).astype(np.uint8)
     return codes.reshape(rows, K), sf, gs
@@ -187,3 +201,57 @@ def unpack(packed):
     out[:, 0::2] = packed & 0xF
     out[:, 1::2] = packed >> 4
     return out
+
+
+# ---------------------------------------------------------------------------
+# Checkpoint import ("Serving Solar Open 2 on DGX Spark", "Supporting real
+# NVFP4 checkpoints"; "GLM-5.3-Flash-NVFP4 #4" discussion, follow-up on the
+# MoE fault).
+
+#: How a checkpoint stores a tensor's global scale. ModelOpt keeps the dequant
+#: scale amax/(448*6) (``weight_scale_2``, ``input_scale``); compressed-tensors
+#: keeps the quant scale (448*6)/amax (``global_scale``).
+SCALE_FORMATS = ("quant", "dequant")
+
+
+def import_global_scale(value, fmt):
+    """A checkpoint's stored global scale -> the quant-convention ``gs`` (fp32).
+
+    ``fmt`` is "quant" (the value already is ``gs``) or "dequant" (the value is
+    ``amax / 2688`` and ``gs`` is its fp32 reciprocal, correctly rounded). A
+    value that is not positive and finite is refused: a zero scale multiplies
+    every expert by zero without any error, the fault the GLM thread traces.
+    Pinned by: the worked pair 4.650297705666162e-05 <-> 21504.0 (golden
+    file); exact powers of two; the round trip within one ulp (tests).
+    """
+    if fmt not in SCALE_FORMATS:
+        raise ValueError(fmt)
+    v = F32(value)
+    if not (np.isfinite(v) and v > 0):
+        raise ValueError("a global scale is positive and finite")
+    return v if fmt == "quant" else F32(F32(1.0) / v)
+
+
+def fold_block_scales(sf, ratio):
+    """Re-round E4M3 block scales by a factor: ``E4M3(e4m3[sf] * ratio)``.
+
+    Moving a matrix from global scale ``gs_old`` to ``gs_new`` keeps its
+    dequantised values ``e2m1 * sf / gs`` when every block scale is multiplied
+    by ``ratio = gs_new / gs_old``; the product (one correctly rounded fp32
+    multiply) is rounded back to E4M3, nearest even, clamped at 448. A scale
+    that underflows to code 0 zeroes its block. Sign-bit and NaN codes are
+    refused.
+    Pinned by: ratio 1 is the identity on every finite code; a power-of-two
+    ratio adds its exponent to the code's exponent field; every code times a
+    few ratios against torch's float8_e4m3fn rounding, saturating at 448
+    (tests).
+    """
+    sf = np.asarray(sf, dtype=np.uint8)
+    if np.any(sf & 0x80) or np.any((sf & 0x7F) == 0x7F):
+        raise ValueError("block scales are non-negative and finite")
+    ratio = F32(ratio)
+    if not (np.isfinite(ratio) and ratio > 0):
+        raise ValueError("the fold ratio is positive and finite")
+    with np.errstate(over="ignore"):
+        prod = (e4m3_decode(sf).astype(F32) * ratio).astype(F32)
+    return e4m3_encode(prod).astype(np.uint8)

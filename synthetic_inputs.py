@@ -12,6 +12,8 @@ Recipe (fixed draw order, everything on the CPU with ``torch.Generator``):
   expert ``e`` (rank ``r = e + 1``) adds ``3 * ln(r**-1.2 / sum_q q**-1.2)``;
 * activations ``X [T, H]`` ~ N(0, 1) rounded to bf16; for the W4A4 workload
   each element is independently multiplied by 20 with probability 0.001;
+* router weights ``W_router [E, H]`` ~ N(0, 1/H) rounded to bf16, so that
+  ``x W_router^T`` has the N(0, 1) logits of the workloads;
 * weights per expert ``e`` (routed ``0..E-1``, the shared expert is ``E``)
   and per matrix (gate ``[I, H]``, up ``[I, H]``, down ``[H, I]``) ~
   N(0, 0.02) rounded to bf16, each drawn from its own generator seeded from
@@ -27,8 +29,8 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["LayerConfig", "CONFIGS", "make_logits", "make_x", "make_expert_weight",
-           "make_layer_weights", "weight_seed"]
+__all__ = ["LayerConfig", "CONFIGS", "make_logits", "make_x", "make_router_weight",
+           "make_expert_weight", "make_layer_weights", "weight_seed"]
 
 
 @dataclass(frozen=True)
@@ -106,6 +108,13 @@ def make_x(cfg: LayerConfig, rows: slice | None = None) -> torch.Tensor:
     if rows is not None:
         x = x[rows]
     return x.contiguous()
+
+
+def make_router_weight(cfg: LayerConfig) -> torch.Tensor:
+    """Router matrix ``[E, H]`` bf16, entries ~ N(0, 1/H)."""
+    g = _gen(cfg.seed * 7919 + 4)
+    w = torch.randn(cfg.E, cfg.H, generator=g, dtype=torch.float32) / math.sqrt(cfg.H)
+    return w.to(torch.bfloat16).contiguous()
 
 
 def make_expert_weight(cfg: LayerConfig, expert: int, matrix: str) -> torch.Tensor:
