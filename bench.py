@@ -419,6 +419,40 @@ def run_ours(args):
     h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
     d2h = hout.numel() * hout.element_size()
 
+    # The router GEMM ahead of the top-k (logits = x W_router^T) on this
+    # workload's shapes: alone, and inside the forward (which then takes x
+    # only). The headline step above takes the logits as an input.
+    w_router = si.make_router_weight(cfg).to(dev)
+    rlog = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    layer.set_router(w_router)
+    desc_r = layer.desc()
+    layer.set_router(None)
+    ws_r = torch.empty(B.moe_workspace_size(desc_r), dtype=torch.uint8, device=dev)
+    ws_r[:256].zero_()
+    for i in range(args.warmup + K):
+        flush.zero_()
+        if i >= args.warmup:
+            rev[i - args.warmup][0].record(stream)
+        B.moe_router_gemm(batches[i % nb][0], w_router, cfg.T, cfg.H, cfg.E, rlog, stream)
+        if i >= args.warmup:
+            rev[i - args.warmup][1].record(stream)
+    for i in range(args.warmup + K):
+        flush.zero_()
+        if i >= args.warmup:
+            fev[i - args.warmup][0].record(stream)
+        B.moe_nvfp4_forward(desc_r, batches[i % nb][0], None, out, None, ws_r, stream)
+        if i >= args.warmup:
+            fev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    if B.moe_get_device_status(ws_r) != 0:
+        raise RuntimeError("device status set in the forward with the router GEMM")
+    r_ms = statistics.mean(a.elapsed_time(b) for a, b in rev)
+    fr_ms = statistics.mean(a.elapsed_time(b) for a, b in fev)
+    r_bytes = cfg.E * cfg.H * 2 + cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4
+    r_flops = 2 * cfg.T * cfg.H * cfg.E
+
     pk = peaks()
     per_stage = {name: statistics.mean(stage_ms[i]) for i, name in enumerate(B.STAGES)}
     g1_ms = per_stage["gemm1_gate_up_swiglu"]
@@ -435,6 +469,17 @@ def run_ours(args):
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": traffic, "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU epilogue)",
                 "peak_source": pk["source"]}
+    if cfg.T <= 16:
+        r_roof = {"bound": "hbm", "unit": "GB/s", "achieved": r_bytes / (r_ms / 1e3) / 1e9, "peak": pk["hbm"],
+                  "kernel": "router_gemv_kernel"}
+    else:
+        r_roof = {"bound": "tensor", "unit": "TFLOP/s", "achieved": r_flops / (r_ms / 1e3) / 1e12,
+                  "peak": pk["bf16"], "kernel": "router_mma_kernel (mma.sync bf16)"}
+    r_roof["frac"] = r_roof["achieved"] / r_roof["peak"]
+    router = dict(ms=r_ms, bytes=r_bytes, flops=r_flops, **r_roof,
+                  forward_with_router_ms=fr_ms,
+                  note="logits = x W_router^T (bf16 [E, H] router, seeded N(0, 1/H)); timed alone and inside "
+                       "moe_nvfp4_forward (x only), L2 flushed between launches")
     layer_time_hbm = alg["layer_bytes"] / (pk["hbm"] * 1e9)
     layer_time_tc = alg["layer_flops"] / (peak * 1e12 if bound == "tensor" else pk["bf16"] * 1e12)
     layer_roof_ms = 1e3 * max(layer_time_hbm, layer_time_tc)
@@ -454,6 +499,7 @@ def run_ours(args):
             "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "graph_replay": graph,
+            "router_gemm": router,
             "gpu_launches": int(launches),
             "clocks": clocks,
             "host_wall_s": t1 - t0, "setup_s": setup_s}

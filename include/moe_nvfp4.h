@@ -85,6 +85,24 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k,
                           int32_t* topk_ids, float* topk_w, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Router GEMM ahead of the top-k ("vLLM on the NVIDIA DGX Spark", section
+ * 7.1, the [Router] stage): logits = x . W_router^T.
+ *
+ * x        bf16 [T, H], 16-byte aligned (device)
+ * w_router bf16 [E, H], 16-byte aligned (device); the router matrix is kept
+ *          16-bit, it is not one of the NVFP4 expert weights
+ * logits   fp32 [T, E] out (device)
+ * Products are exact in fp32 and summed in fp32 in an order fixed by the
+ * shapes (the same bits on every run; the order differs from a sequential
+ * sum, so values differ from one by accumulated fp32 rounding).
+ * Errors: T < 0, H <= 0, E < 1, a NULL pointer -> MOE_ERR_INVALID_ARG;
+ * H % 8 != 0 or misaligned rows -> MOE_ERR_INVALID_ARG; T = 0 -> MOE_OK with
+ * nothing enqueued.
+ */
+moe_status moe_router_gemm(const uint16_t* x, const uint16_t* w_router, int T, int H, int E,
+                           float* logits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Permutation into expert-contiguous groups.  "vLLM on the NVIDIA DGX
  * Spark", section 4.3 (token dispatch) and section 7.1
  * ([Permute-Experts-Unpermute]).
@@ -127,6 +145,54 @@ size_t moe_quantize_workspace_size(void);
 moe_status moe_nvfp4_quantize(const uint16_t* x, int rows, int K, uint8_t* q,
                               uint8_t* sf, float* gs_out, void* ws, size_t ws_bytes,
                               moe_stream_t stream);
+
+/* The same quantisation with a static (calibrated) global scale gs in place
+ * of the dynamic 2688 / amax ("Serving Solar Open 2 on DGX Spark", "The
+ * fix": static and dynamic NVFP4 W4A4 paths; "GLM-5.3-Flash-NVFP4 #4":
+ * calibrated per-projection input scales). gs is a host float in the quant
+ * convention (moe_import_global_scale turns a checkpoint's stored value into
+ * it). Blocks whose (max|x_i| / 6) * gs exceeds 448 saturate: the block scale
+ * clamps at 448 and the codes at 6. Errors: gs <= 0 or non-finite, and the
+ * size and pointer errors of moe_nvfp4_quantize -> MOE_ERR_INVALID_ARG.
+ */
+moe_status moe_nvfp4_quantize_static(const uint16_t* x, int rows, int K, float gs,
+                                     uint8_t* q, uint8_t* sf, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Checkpoint import ("Serving Solar Open 2 on DGX Spark", "Supporting real
+ * NVFP4 checkpoints"; "GLM-5.3-Flash-NVFP4 #4" discussion, follow-up on the
+ * MoE fault).
+ *
+ * Checkpoints store a tensor's global scale in one of two conventions:
+ * ModelOpt keeps the dequant scale amax / (448*6) (weight_scale_2,
+ * input_scale), compressed-tensors the quant scale (448*6) / amax
+ * (global_scale). This library takes the quant convention everywhere.
+ *
+ * moe_import_global_scale (host only, no GPU work): gs_out = stored for
+ * MOE_SCALE_QUANT, the fp32 reciprocal 1 / stored (correctly rounded) for
+ * MOE_SCALE_DEQUANT. stored <= 0 or non-finite -> MOE_ERR_INVALID_ARG (a zero
+ * scale silently zeroes every expert, the fault of the GLM thread); an
+ * unknown format -> MOE_ERR_INVALID_ARG.
+ *
+ * moe_nvfp4_fold_scales (one-time, synchronous): moves n E4M3 block scales
+ * to another global scale, sf_out[i] = E4M3(e4m3[sf_in[i]] * ratio) with one
+ * correctly rounded fp32 multiply, nearest even, clamped at 448; use ratio =
+ * gs_new / gs_old to express a matrix in the global scale gs_new (for
+ * example one scale shared by a fused gate/up pair). A scale that underflows
+ * becomes 0 and zeroes its block. sf_in and sf_out are device arrays (they
+ * may be the same array). Errors: a NULL pointer, ratio <= 0 or non-finite,
+ * or any input code with its sign bit set or a NaN code (0x7F/0xFF) ->
+ * MOE_ERR_INVALID_ARG (sf_out then holds the converted codes with the bad
+ * ones copied unchanged). n = 0 -> MOE_OK. The call synchronises the stream.
+ */
+typedef enum {
+  MOE_SCALE_QUANT = 0,   /* stored value is (448*6) / amax */
+  MOE_SCALE_DEQUANT = 1  /* stored value is amax / (448*6) */
+} moe_scale_format;
+
+moe_status moe_import_global_scale(float stored, moe_scale_format format, float* gs_out);
+moe_status moe_nvfp4_fold_scales(const uint8_t* sf_in, size_t n, float ratio, uint8_t* sf_out,
+                                 moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Weight preparation (one-time, synchronous).  "Serving Solar Open 2 on DGX
@@ -223,6 +289,14 @@ moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* 
  * The whole layer. Weights come prepared (moe_nvfp4_prepare_weights):
  * w13 holds E gate/up blocks, w2 E down blocks, back to back; the shared
  * expert's blocks are separate and may be NULL (no shared expert).
+ *
+ * w_router (nullable): bf16 [E, H] router matrix, 16-byte aligned. When it
+ *   is set the forward computes the logits itself (moe_router_gemm) and its
+ *   `logits` argument may be NULL (it is ignored).
+ * x_global_scale, h_global_scale (W4A4 only; 0 = dynamic): static
+ *   calibrated global scales (quant convention) for the two activation
+ *   quantisations, x before GEMM 1 and h before GEMM 2, in place of the
+ *   dynamic 2688 / amax. Must be 0 on W4A16 layers.
  */
 typedef struct {
   int T, H, I, I_shared, E, k;
@@ -231,14 +305,20 @@ typedef struct {
   const void* w2;
   const void* w13_shared;
   const void* w2_shared;
+  const uint16_t* w_router;
+  float x_global_scale;
+  float h_global_scale;
 } moe_layer_desc;
 
 /* Workspace bytes moe_nvfp4_forward needs for this descriptor. */
 size_t moe_workspace_size(const moe_layer_desc* L);
 
-/* x bf16 [T, H], logits fp32 [T, E] -> out bf16 [T, H]; topk_ids_out
- * (nullable) int32 [T, k] receives the routing. ws must hold
- * moe_workspace_size(L) bytes, 256-byte aligned. */
+/* x bf16 [T, H], logits fp32 [T, E] (or NULL with L->w_router) -> out bf16
+ * [T, H]; topk_ids_out (nullable) int32 [T, k] receives the routing. ws must
+ * hold moe_workspace_size(L) bytes, 256-byte aligned. Errors: a scale in
+ * x_global_scale / h_global_scale that is negative or non-finite, or nonzero
+ * on a W4A16 layer -> MOE_ERR_INVALID_ARG; a misaligned w_router or H % 8 != 0
+ * with it -> MOE_ERR_INVALID_ARG. */
 moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const float* logits,
                              uint16_t* out, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
                              moe_stream_t stream);
@@ -255,7 +335,8 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream);
  * on this host thread records events[0] before its first kernel and
  * events[i] after stage i (route, permute, quantise x, GEMM 1, quantise h,
  * GEMM 2, combine; a stage the mode does not run records at the same point
- * as the previous one), all on the call's stream; the setting is then
+ * as the previous one; with w_router the router GEMM belongs to the route
+ * stage), all on the call's stream; the setting is then
  * cleared. Pass NULL to clear it explicitly.
  *
  * moe_kernel_launches: number of kernels this library has launched in this

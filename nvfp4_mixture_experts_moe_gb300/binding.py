@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_nvfp4.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_ERR_WORKSPACE, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
 MOE_W4A16, MOE_W4A4 = 0, 1
+MOE_SCALE_QUANT, MOE_SCALE_DEQUANT = 0, 1
 
 _lib = None
 
@@ -35,7 +36,9 @@ class MoeLayerDesc(ctypes.Structure):
                 ("I_shared", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
                 ("mode", ctypes.c_int),
                 ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
-                ("w13_shared", ctypes.c_void_p), ("w2_shared", ctypes.c_void_p)]
+                ("w13_shared", ctypes.c_void_p), ("w2_shared", ctypes.c_void_p),
+                ("w_router", ctypes.c_void_p),
+                ("x_global_scale", ctypes.c_float), ("h_global_scale", ctypes.c_float)]
 
 
 class MoeGemmArgs(ctypes.Structure):
@@ -55,6 +58,10 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_router_gemm": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_nvfp4_quantize_static": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
+    "moe_import_global_scale": (_I, [ctypes.c_float, _I, ctypes.POINTER(ctypes.c_float)]),
+    "moe_nvfp4_fold_scales": (_I, [_P, _Z, ctypes.c_float, _P, _P]),
     "moe_permute_workspace_size": (_Z, [_I, _I, _I]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_quantize_workspace_size": (_Z, []),
@@ -128,6 +135,11 @@ def moe_route_topk(logits, T, E, k, topk_ids, topk_w, stream=None):
            "moe_route_topk")
 
 
+def moe_router_gemm(x, w_router, T, H, E, logits, stream=None):
+    _check(lib().moe_router_gemm(_ptr(x), _ptr(w_router), T, H, E, _ptr(logits), _stream(stream)),
+           "moe_router_gemm")
+
+
 def moe_permute_workspace_size(T, k, E):
     return lib().moe_permute_workspace_size(T, k, E)
 
@@ -146,6 +158,23 @@ def moe_nvfp4_quantize(x, rows, K, q, sf, gs_out, ws, stream=None):
     _check(lib().moe_nvfp4_quantize(_ptr(x), rows, K, _ptr(q), _ptr(sf), _ptr(gs_out), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)),
            "moe_nvfp4_quantize")
+
+
+def moe_nvfp4_quantize_static(x, rows, K, gs, q, sf, stream=None):
+    _check(lib().moe_nvfp4_quantize_static(_ptr(x), rows, K, float(gs), _ptr(q), _ptr(sf), _stream(stream)),
+           "moe_nvfp4_quantize_static")
+
+
+def moe_import_global_scale(stored, fmt):
+    """A checkpoint's stored global scale -> the quant-convention gs (host only)."""
+    out = ctypes.c_float(0.0)
+    _check(lib().moe_import_global_scale(float(stored), int(fmt), ctypes.byref(out)), "moe_import_global_scale")
+    return out.value
+
+
+def moe_nvfp4_fold_scales(sf_in, n, ratio, sf_out, stream=None):
+    _check(lib().moe_nvfp4_fold_scales(_ptr(sf_in), n, float(ratio), _ptr(sf_out), _stream(stream)),
+           "moe_nvfp4_fold_scales")
 
 
 def moe_prepare_size(N, K, mode, gate_up):

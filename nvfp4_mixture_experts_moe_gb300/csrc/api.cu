@@ -73,6 +73,7 @@ struct ForwardWs {
   WsHeader* hdr;
   int32_t* ids;
   float* w;
+  float* logits;      // [T, E] when the forward runs the router GEMM
   int32_t* counts;
   int32_t* offsets;   // [E+1]
   int32_t* gofs;      // [E+2] group offsets: routed groups, then the shared rows [P, P+T)
@@ -106,6 +107,7 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
   f.hdr = c.take<WsHeader>(1);
   f.ids = c.take<int32_t>(P);
   f.w = c.take<float>(P);
+  f.logits = L.w_router ? c.take<float>((size_t)L.T * L.E) : nullptr;
   f.counts = c.take<int32_t>(L.E);
   f.offsets = c.take<int32_t>(L.E + 1);
   f.gofs = c.take<int32_t>(L.E + 2);
@@ -162,6 +164,10 @@ static moe_status validate_layer(const moe_layer_desc* L) {
   if (L->w13_shared && (!aligned(L->w13_shared, kAlign) || !aligned(L->w2_shared, kAlign)))
     return MOE_ERR_INVALID_ARG;
   if ((long long)L->T * L->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  if (L->w_router && !aligned(L->w_router, 16)) return MOE_ERR_INVALID_ARG;
+  const float sx = L->x_global_scale, sh = L->h_global_scale;
+  if (!(sx >= 0.0f) || !(sh >= 0.0f) || !std::isfinite(sx) || !std::isfinite(sh)) return MOE_ERR_INVALID_ARG;
+  if (L->mode == MOE_W4A16 && (sx != 0.0f || sh != 0.0f)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -195,6 +201,17 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
   moe_status st = check_device();
   if (st != MOE_OK) return st;
   return launch_route_topk(logits, T, E, k, topk_ids, topk_w, (cudaStream_t)stream);
+}
+
+moe_status moe_router_gemm(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, float* logits,
+                           moe_stream_t stream) {
+  if (T < 0 || H <= 0 || E < 1 || H % 8) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !logits) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_router_gemm(x, w_router, T, H, E, logits, (cudaStream_t)stream);
 }
 
 size_t moe_permute_workspace_size(int T, int k, int E) {
@@ -235,7 +252,56 @@ moe_status moe_nvfp4_quantize(const uint16_t* x, int rows, int K, uint8_t* q, ui
   if (st != MOE_OK) return st;
   st = launch_amax_bf16(x, (size_t)rows * K, &hdr->amax[0], s);
   if (st != MOE_OK) return st;
-  return launch_quantize_bf16(x, rows, K, &hdr->amax[0], q, sf, gs_out, s);
+  return launch_quantize_bf16(x, rows, K, &hdr->amax[0], q, sf, gs_out, 0.0f, s);
+}
+
+moe_status moe_nvfp4_quantize_static(const uint16_t* x, int rows, int K, float gs, uint8_t* q, uint8_t* sf,
+                                     moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 16) return MOE_ERR_INVALID_ARG;
+  if (!(gs > 0.0f) || !std::isfinite(gs)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !sf || !aligned(x, 16) || !aligned(q, 8)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_quantize_bf16(x, rows, K, nullptr, q, sf, nullptr, gs, (cudaStream_t)stream);
+}
+
+moe_status moe_import_global_scale(float stored, moe_scale_format format, float* gs_out) {
+  if (!gs_out) return MOE_ERR_INVALID_ARG;
+  if (!(stored > 0.0f) || !std::isfinite(stored)) return MOE_ERR_INVALID_ARG;
+  if (format == MOE_SCALE_QUANT) {
+    *gs_out = stored;
+  } else if (format == MOE_SCALE_DEQUANT) {
+    *gs_out = 1.0f / stored;  // IEEE fp32 division, correctly rounded
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+static __device__ int g_fold_flag;
+
+moe_status moe_nvfp4_fold_scales(const uint8_t* sf_in, size_t n, float ratio, uint8_t* sf_out,
+                                 moe_stream_t stream) {
+  if (!(ratio > 0.0f) || !std::isfinite(ratio)) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!sf_in || !sf_out) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* flag = nullptr;
+  st = cuda_ok(cudaGetSymbolAddress(reinterpret_cast<void**>(&flag), g_fold_flag));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaMemsetAsync(flag, 0, sizeof(int), s));
+  if (st != MOE_OK) return st;
+  st = launch_fold_scales(sf_in, n, ratio, sf_out, flag, s);
+  if (st != MOE_OK) return st;
+  int hflag = 0;
+  st = cuda_ok(cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, s));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaStreamSynchronize(s));
+  if (st != MOE_OK) return st;
+  return hflag ? MOE_ERR_INVALID_ARG : MOE_OK;
 }
 
 size_t moe_prepare_size(int N, int K, moe_mode mode, int gate_up) {
@@ -378,8 +444,9 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   moe_status st = validate_layer(L);
   if (st != MOE_OK) return st;
   if (L->T == 0) return MOE_OK;
-  if (!x || !logits || !out) return MOE_ERR_INVALID_ARG;
+  if (!x || !out || (!logits && !L->w_router)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (L->w_router && L->H % 8) return MOE_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, kAlign)) return MOE_ERR_WORKSPACE;
   ForwardWs f = carve_forward(*L, ws);
   if (ws_bytes < f.bytes) return MOE_ERR_WORKSPACE;
@@ -400,6 +467,11 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   // its predecessor's results in-kernel) unless stage events are recorded.
   const bool pdl = !g_stage_events_set;
   stage_mark(0, s);
+  if (L->w_router) {  // router GEMM: the logits come from x
+    st = launch_router_gemm(x, L->w_router, T, H, E, f.logits, s);
+    if (st != MOE_OK) return st;
+    logits = f.logits;
+  }
   if (P <= kFusedRoutePermuteMax) {  // route + permute in one CTA
     st = launch_route_permute_small(logits, T, E, k, ids, f.w, f.counts, f.offsets, f.perm, f.inv_perm,
                                     &f.hdr->status, f.row_token, f.row_weight, f.gofs, s);
@@ -414,13 +486,17 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     if (st != MOE_OK) return st;
   }
   stage_mark(2, s);
-  if (fp4) {  // dynamic per-tensor quantisation of x (W4A4)
+  const float x_static = L->x_global_scale, h_static = L->h_global_scale;
+  if (fp4) {  // per-tensor quantisation of x (W4A4): dynamic amax, or a static scale
     st = cuda_ok(cudaMemsetAsync(&f.hdr->amax[0], 0, 2 * sizeof(float), s));
     if (st != MOE_OK) return st;
-    st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s, pdl);
-    if (st != MOE_OK) return st;
+    if (x_static == 0.0f) {
+      st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s, pdl);
+      if (st != MOE_OK) return st;
+    }
     st = launch_quantize_tiles(x, T, H, f.inv_perm, k, has_shared ? P : -1, f.gofs, E + (has_shared ? 1 : 0),
-                               &f.hdr->amax[0], f.xq, f.xsf, (size_t)f.tiles * (H / 256) * 2048, f.xgs, s, pdl);
+                               &f.hdr->amax[0], f.xq, f.xsf, (size_t)f.tiles * (H / 256) * 2048, f.xgs,
+                               x_static, s, pdl);
     if (st != MOE_OK) return st;
   }
   if (f.xf) {  // f16 copy of x, rows in group order, for the large-group tensor-core GEMM
@@ -446,7 +522,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.a_gs = fp4 ? f.xgs : nullptr;
   g1.a_row_index = f.row_token;
   g1.out = f.h;
-  g1.out_amax = fp4 ? &f.hdr->amax[1] : nullptr;
+  g1.out_amax = (fp4 && h_static == 0.0f) ? &f.hdr->amax[1] : nullptr;
   g1.a_f16 = f.xf;
   g1.a_mul = f.xmul;
   g1.a_rows = rows;
@@ -459,7 +535,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   stage_mark(4, s);
   if (fp4) {  // h -> NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue)
     st = launch_quantize_tiles(f.h, rows, I, nullptr, 0, -1, f.gofs, G, &f.hdr->amax[1], f.hq, f.hsf,
-                               (size_t)f.tiles * (I / 256) * 2048, f.hgs, s, pdl);
+                               (size_t)f.tiles * (I / 256) * 2048, f.hgs, h_static, s, pdl);
     if (st != MOE_OK) return st;
   } else if (f.hf) {
     st = launch_rows_to_f16(f.h, nullptr, rows, I, f.hf, f.hmul, s, pdl);

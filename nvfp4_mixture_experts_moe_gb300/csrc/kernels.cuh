@@ -53,10 +53,20 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
                           int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
                           cudaStream_t s, bool pdl = false);
 
-// Quantisation: amax into *amax (must be zeroed first), then codes.
+// Quantisation: amax into *amax (must be zeroed first), then codes. A
+// gs_static > 0 replaces the dynamic 2688 / amax (amax is then not read).
 moe_status launch_amax_bf16(const uint16_t* x, size_t n, float* amax, cudaStream_t s, bool pdl = false);
 moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float* amax, uint8_t* q,
-                                uint8_t* sf, float* gs_out, cudaStream_t s, bool pdl = false);
+                                uint8_t* sf, float* gs_out, float gs_static, cudaStream_t s, bool pdl = false);
+
+// E4M3 block scales re-rounded by a ratio (checkpoint import); sign-bit or
+// NaN codes set *flag.
+moe_status launch_fold_scales(const uint8_t* in, size_t n, float ratio, uint8_t* out, int* flag, cudaStream_t s);
+
+// Router GEMM: logits fp32 [T, E] = x bf16 [T, H] . w bf16 [E, H]^T, fp32
+// accumulation in a fixed order (H % 8 == 0, 16-byte aligned rows).
+moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits,
+                              cudaStream_t s, bool pdl = false);
 
 moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStream_t s);
 moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
@@ -113,13 +123,14 @@ moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
 
 // bf16 rows -> NVFP4 codes [rows, K/2] of the grouped layout and scale-factor
 // atoms per (128-row tile of a group, 256-wide K stage), zeroed first
-// (sf_bytes); gs = 2688 / amax as moe_nvfp4_quantize. With `dest` (inverse
+// (sf_bytes); gs = 2688 / amax as moe_nvfp4_quantize, or gs_static when it is
+// > 0. With `dest` (inverse
 // permutation, [src_rows * k]) token t's row goes to dest[t*k + j] and, with
 // shared_base >= 0, to shared_base + t; without it source row r is row r.
 moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
                                  int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
-                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, cudaStream_t s,
-                                 bool pdl = false);
+                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, float gs_static,
+                                 cudaStream_t s, bool pdl = false);
 
 // bf16 rows -> f16 rows scaled by a power of two so that each row's largest
 // magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it. Row r of dst is

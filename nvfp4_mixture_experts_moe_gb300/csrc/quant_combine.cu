@@ -91,15 +91,22 @@ __device__ __forceinline__ float e4m3_decode(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
 }
 
+// The global scale of a quantisation: a static (calibrated) one when
+// gs_static > 0, else the dynamic 2688 / amax (1 when amax is 0).
+__device__ __forceinline__ float global_scale_of(const float* amax_p, float gs_static) {
+  if (gs_static > 0.0f) return gs_static;
+  const float amax = *amax_p;
+  return amax > 0.0f ? 2688.0f / amax : 1.0f;
+}
+
 // One thread per 16-element block: 32 bytes of bf16 in, 8 bytes of codes and
 // 1 scale byte out.
 __global__ void __launch_bounds__(256) quantize_bf16_kernel(const uint16_t* __restrict__ x, int rows, int K,
                                                             const float* __restrict__ amax_p,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                            float* __restrict__ gs_out) {
+                                                            float* __restrict__ gs_out, float gs_static) {
   pdl_wait();
-  const float amax = *amax_p;
-  const float gs = amax > 0.0f ? 2688.0f / amax : 1.0f;
+  const float gs = global_scale_of(amax_p, gs_static);
   const size_t nblk = (size_t)rows * (K / 16);
   const size_t b = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   if (b == 0 && gs_out != nullptr) *gs_out = gs;
@@ -134,11 +141,11 @@ __global__ void __launch_bounds__(256) quantize_bf16_kernel(const uint16_t* __re
 }
 
 moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float* amax, uint8_t* q,
-                                uint8_t* sf, float* gs_out, cudaStream_t s, bool pdl) {
+                                uint8_t* sf, float* gs_out, float gs_static, cudaStream_t s, bool pdl) {
   const size_t nblk = (size_t)rows * (K / 16);
   const int blocks = (int)((nblk + 255) / 256);
   cudaError_t e = launch_ex(pdl, quantize_bf16_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s, x, rows,
-                            K, amax, q, sf, gs_out);
+                            K, amax, q, sf, gs_out, gs_static);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
@@ -198,7 +205,7 @@ __device__ __forceinline__ void quant_block16(const uint16_t* src, float gs, uin
 __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
     const uint16_t* __restrict__ x, int src_rows, int K, const int32_t* __restrict__ dest, int k, int shared_base,
     const int32_t* __restrict__ gofs, int G, const float* __restrict__ amax_p, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ sf_tiles, float* __restrict__ gs_out) {
+    uint8_t* __restrict__ sf_tiles, float* __restrict__ gs_out, float gs_static) {
   pdl_wait();
   extern __shared__ int tile_base[];  // [G + 1]
   if (threadIdx.x < 32) {  // exclusive prefix of ceil(rows / 128) over the groups
@@ -217,8 +224,7 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
     }
   }
   __syncthreads();
-  const float amax = *amax_p;
-  const float gs = amax > 0.0f ? 2688.0f / amax : 1.0f;
+  const float gs = global_scale_of(amax_p, gs_static);
   if (blockIdx.x == 0 && threadIdx.x == 0 && gs_out != nullptr) *gs_out = gs;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kQtWarps + (threadIdx.x >> 5);
@@ -266,7 +272,8 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
 
 moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
                                  int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
-                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, cudaStream_t s, bool pdl) {
+                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, float gs_static,
+                                 cudaStream_t s, bool pdl) {
   if (K % 256 || G <= 0 || (dest && k + 1 > kQtMaxDest)) return MOE_ERR_UNSUPPORTED;
   if (src_rows == 0) return MOE_OK;
   moe_status st = cuda_ok(cudaMemsetAsync(sf_tiles, 0, sf_bytes, s));
@@ -276,8 +283,41 @@ moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const i
   // after the memset the kernel is an ordinary stream successor (no programmatic launch)
   (void)pdl;
   cudaError_t e = launch_ex(false, quantize_tiles_kernel, dim3(blocks), dim3(kQtWarps * 32), smem, s, x, src_rows, K,
-                            dest, k, shared_base, gofs, G, amax, q, sf_tiles, gs_out);
+                            dest, k, shared_base, gofs, G, amax, q, sf_tiles, gs_out, gs_static);
   if (e != cudaSuccess) return cuda_ok(e);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Re-rounding E4M3 block scales by a global-scale ratio (checkpoint import,
+// "Serving Solar Open 2 on DGX Spark", "Supporting real NVFP4 checkpoints":
+// reciprocal global scales folded into the FP8 block scales with
+// re-rounding, clamped at 448): out = E4M3(e4m3[in] * ratio), one correctly
+// rounded fp32 multiply, then nearest even with saturation at 448. A code
+// with the sign bit set or a NaN code sets *flag and is copied unchanged.
+// One code per thread, grid-stride.
+// `in` and `out` may be the same array (no __restrict__): each element is read
+// and then written by one thread.
+__global__ void __launch_bounds__(256) fold_scales_kernel(const uint8_t* in, size_t n, float ratio, uint8_t* out,
+                                                          int* flag) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+    const uint32_t c = in[i];
+    if ((c & 0x80u) || (c & 0x7fu) == 0x7fu) {
+      atomicOr(flag, 1);
+      out[i] = (uint8_t)c;
+      continue;
+    }
+    out[i] = (uint8_t)e4m3_encode_sat(__fmul_rn(e4m3_decode(c), ratio));
+  }
+}
+
+moe_status launch_fold_scales(const uint8_t* in, size_t n, float ratio, uint8_t* out, int* flag, cudaStream_t s) {
+  if (n == 0) return MOE_OK;
+  const size_t want = (n + 255) / 256;
+  const int blocks = (int)(want < 152 * 8 ? want : 152 * 8);
+  fold_scales_kernel<<<blocks, 256, 0, s>>>(in, n, ratio, out, flag);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }

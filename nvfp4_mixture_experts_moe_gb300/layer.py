@@ -1,11 +1,14 @@
 """Device-side setup of one MoE layer through the C ABI.
 
 ``Nvfp4MoeLayer`` quantises bf16 weight matrices to NVFP4 with the
-library's own quantiser (``moe_nvfp4_quantize``), converts them into the
-kernels' tile layout (``moe_nvfp4_prepare_weights``), keeps them resident in
-device memory and runs the fused forward (``moe_nvfp4_forward``). torch is
-used only to allocate device memory; every step of the layer runs in the
-CUDA library.
+library's own quantiser (``moe_nvfp4_quantize``) or takes pre-quantised
+checkpoint matrices (``import_expert``: the stored global scale is converted
+with ``moe_import_global_scale``), converts them into the kernels' tile
+layout (``moe_nvfp4_prepare_weights``), keeps them resident in device memory
+and runs the fused forward (``moe_nvfp4_forward``), optionally with its own
+router GEMM (``set_router``) and static W4A4 activation scales
+(``set_static_scales``). torch is used only to allocate device memory; every
+step of the layer runs in the CUDA library.
 """
 from __future__ import annotations
 
@@ -49,6 +52,8 @@ class Nvfp4MoeLayer:
         else:
             self.w13_s = self.w2_s = None
         self.gs = {}  # (expert, matrix) -> quant-convention global scale (float)
+        self.w_router = None
+        self.x_gs = self.h_gs = 0.0
 
     def _slot(self, expert, which):
         if expert == self.E:
@@ -74,6 +79,34 @@ class Nvfp4MoeLayer:
         B.moe_nvfp4_prepare_weights(qd, sd, gsv[2:], self.H, inter, self.mode, 0, self._slot(expert, 2))
         return (qg, sg, gsv[0]), (qu, su, gsv[1]), (qd, sd, gsv[2])
 
+    def import_expert(self, expert, gate, up, down, fmt):
+        """Pre-quantised checkpoint matrices of one expert (expert E = shared).
+
+        ``gate``, ``up`` (``[I, H]``) and ``down`` (``[H, I]``) are each a
+        triple (packed codes uint8 ``[N, K/2]``, E4M3 scales uint8
+        ``[N, K/16]``, stored global scale) with the scale stored in ``fmt``
+        (``MOE_SCALE_QUANT``: compressed-tensors; ``MOE_SCALE_DEQUANT``:
+        ModelOpt). Returns the three quant-convention global scales.
+        """
+        dev = self.device
+        gs = [B.moe_import_global_scale(m[2], fmt) for m in (gate, up, down)]
+        (qg, sg, _), (qu, su, _), (qd, sd, _) = (
+            (m[0].to(dev).contiguous(), m[1].to(dev).contiguous(), m[2]) for m in (gate, up, down))
+        self.gs[(expert, "gate")], self.gs[(expert, "up")], self.gs[(expert, "down")] = gs
+        inter = qg.shape[0]
+        B.moe_nvfp4_prepare_weights(torch.cat([qg, qu]), torch.cat([sg, su]), gs[:2], 2 * inter, self.H,
+                                    self.mode, 1, self._slot(expert, 13))
+        B.moe_nvfp4_prepare_weights(qd, sd, gs[2:], self.H, inter, self.mode, 0, self._slot(expert, 2))
+        return gs
+
+    def set_router(self, w_router):
+        """bf16 router matrix ``[E, H]``; the forward then computes its own logits."""
+        self.w_router = None if w_router is None else w_router.to(self.device, torch.bfloat16).contiguous()
+
+    def set_static_scales(self, x_gs=0.0, h_gs=0.0):
+        """W4A4 static global scales (quant convention) for x and h; 0 = dynamic."""
+        self.x_gs, self.h_gs = float(x_gs), float(h_gs)
+
     def desc(self, T=None):
         d = B.MoeLayerDesc()
         d.T = self.T if T is None else T
@@ -82,6 +115,8 @@ class Nvfp4MoeLayer:
         d.w13, d.w2 = self.w13.data_ptr(), self.w2.data_ptr()
         d.w13_shared = self.w13_s.data_ptr() if self.shared else None
         d.w2_shared = self.w2_s.data_ptr() if self.shared else None
+        d.w_router = None if self.w_router is None else self.w_router.data_ptr()
+        d.x_global_scale, d.h_global_scale = self.x_gs, self.h_gs
         return d
 
     def workspace(self, T=None):
@@ -90,7 +125,8 @@ class Nvfp4MoeLayer:
         ws[:256].zero_()
         return ws
 
-    def forward(self, x, logits, out=None, topk_ids=None, ws=None, stream=None):
+    def forward(self, x, logits=None, out=None, topk_ids=None, ws=None, stream=None):
+        """``logits`` may be None when a router matrix is set."""
         T = x.shape[0]
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)

@@ -72,3 +72,60 @@ def test_sizes(lib):
     assert 0 < n8 < n4096
     d.H = 100
     assert B.moe_workspace_size(d) == 0
+
+
+def test_import_global_scale_host_only(lib):
+    # host-only entry point: runs here without a GPU; checked against the
+    # worked pair of the GLM thread (golden file) and the oracle
+    import numpy as np
+    from oracle import nvfp4
+    gold = {}
+    with open(os.path.join(ROOT, "tests", "golden", "global_scale_worked_example.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, val = line.split()
+                gold[key] = float(val)
+    assert B.moe_import_global_scale(gold["dequant_scale"], B.MOE_SCALE_DEQUANT) == gold["quant_scale"]
+    assert B.moe_import_global_scale(gold["quant_scale"], B.MOE_SCALE_QUANT) == gold["quant_scale"]
+    vals = np.random.default_rng(3).uniform(1e-7, 1e5, 500).astype(np.float32)
+    for v in vals:
+        got = np.float32(B.moe_import_global_scale(float(v), B.MOE_SCALE_DEQUANT))
+        assert got == nvfp4.import_global_scale(v, "dequant")
+    out = ctypes.c_float(0)
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.moe_import_global_scale(bad, B.MOE_SCALE_DEQUANT, ctypes.byref(out)) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_import_global_scale(1.0, 7, ctypes.byref(out)) == B.MOE_ERR_INVALID_ARG
+
+
+def test_new_entry_points_validate_on_host(lib):
+    L = lib
+    # router GEMM: H must be a multiple of 8, pointers set; T = 0 is a no-op
+    assert L.moe_router_gemm(256, 256, 4, 12, 8, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_gemm(None, None, 0, 64, 8, None, None) == B.MOE_OK
+    assert L.moe_router_gemm(None, 256, 4, 64, 8, 256, None) == B.MOE_ERR_INVALID_ARG
+    # static quantisation: the scale must be positive and finite
+    for bad in (0.0, -2.0, float("inf"), float("nan")):
+        assert L.moe_nvfp4_quantize_static(256, 4, 64, bad, 256, 256, None) == B.MOE_ERR_INVALID_ARG
+    # fold: ratio must be positive and finite; n = 0 is a no-op
+    for bad in (0.0, -1.0, float("inf")):
+        assert L.moe_nvfp4_fold_scales(256, 16, bad, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_nvfp4_fold_scales(256, 0, 1.0, 256, None) == B.MOE_OK
+    # static scales on a W4A16 layer, or negative ones, are refused
+    d = B.MoeLayerDesc(T=8, H=4096, I=1536, I_shared=1536, E=320, k=8, mode=0, w13=256, w2=256,
+                       w13_shared=256, w2_shared=256)
+    assert B.moe_workspace_size(d) > 0
+    d.x_global_scale = 100.0
+    assert B.moe_workspace_size(d) == 0
+    d.mode = 1
+    d.H, d.I = 4096, 1536
+    assert B.moe_workspace_size(d) > 0
+    d.h_global_scale = -1.0
+    assert B.moe_workspace_size(d) == 0
+    d.h_global_scale = 0.0
+    # the router matrix adds the [T, E] logits to the workspace
+    n0 = B.moe_workspace_size(d)
+    d.w_router = 256
+    assert B.moe_workspace_size(d) >= n0 + 8 * 320 * 4
+    d.w_router = 258
+    assert B.moe_workspace_size(d) == 0
