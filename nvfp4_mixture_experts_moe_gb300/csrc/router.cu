@@ -10,8 +10,11 @@
 // so two plain kernels cover it:
 // * few tokens (T <= 16): the weight rows stream from HBM once; one CTA per
 //   expert row, its four warps take a quarter of K each, every lane holds one
-//   fp32 sum per token, and the partial sums are added in a fixed order
-//   (lanes by a shuffle tree, then warps 0..3);
+//   fp32 sum per token (its chunks in a fixed order), and the partial sums
+//   are added in a fixed order (lanes by a shuffle tree, then warps 0..3).
+//   Measured at 8 tokens, E = 320, H = 4096: about 11 us per launch after an
+//   L2 flush, far from the 0.4 us the 2.7 MB would take at HBM speed; the
+//   kernel is latency-bound (sixteen warps per row measured no faster);
 // * more tokens: mma.sync m16n8k16 (bf16 in, fp32 accumulate) over 64 x 64
 //   (token x expert) tiles, K in 64-wide stages moved by cp.async into a
 //   4-deep ring of XOR-swizzled shared-memory tiles read by ldmatrix.
@@ -33,6 +36,7 @@ using tc::smem_u32;
 // Few tokens.
 constexpr int kGemvMaxT = 16;
 constexpr int kGemvWarps = 4;
+constexpr int kGemvBatch = 4;
 
 __device__ __forceinline__ void bf16x8_to_float(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -56,17 +60,35 @@ __global__ void __launch_bounds__(kGemvWarps * 32) router_gemv_kernel(const uint
 #pragma unroll
   for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.0f;
   const uint4* wrow = reinterpret_cast<const uint4*>(w + (size_t)e * H);
-#pragma unroll 4
-  for (int c = c0 + lane; c < c1; c += 32) {
-    float wf[8];
-    bf16x8_to_float(ldg_stream(wrow + c), wf);
+  // kGemvBatch chunks per lane per round: their weight loads (HBM) are issued
+  // together; then, chunk by chunk, the matching x chunks of every token (L2)
+  // are issued together before they are used, so a round costs one HBM
+  // latency plus one L2 latency per chunk instead of one per chunk and token
+  for (int cb = c0 + lane; cb < c1; cb += 32 * kGemvBatch) {
+    uint4 wv[kGemvBatch];
 #pragma unroll
-    for (int t = 0; t < kGemvMaxT; ++t) {
-      if (t < T) {
-        float xf[8];
-        bf16x8_to_float(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c), xf);
+    for (int u = 0; u < kGemvBatch; ++u) {
+      const int c = cb + 32 * u;
+      wv[u] = c < c1 ? ldg_stream(wrow + c) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[t] = fmaf(xf[i], wf[i], acc[t]);
+    for (int u = 0; u < kGemvBatch; ++u) {
+      const int c = cb + 32 * u;
+      if (c >= c1) break;
+      uint4 xv[kGemvMaxT];
+#pragma unroll
+      for (int t = 0; t < kGemvMaxT; ++t)
+        xv[t] = t < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c) : make_uint4(0, 0, 0, 0);
+      float wf[8];
+      bf16x8_to_float(wv[u], wf);
+#pragma unroll
+      for (int t = 0; t < kGemvMaxT; ++t) {
+        if (t < T) {
+          float xf[8];
+          bf16x8_to_float(xv[t], xf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[t] = fmaf(xf[i], wf[i], acc[t]);
+        }
       }
     }
   }
