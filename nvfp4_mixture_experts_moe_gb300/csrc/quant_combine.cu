@@ -167,9 +167,10 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
 // One warp per source row, quantised once: with `dest` (the inverse
 // permutation, [rows_src * k]) the row of token t goes to dest[t*k + j] for
 // each j with a valid slot and, with `shared_base` >= 0, to row
-// shared_base + t; without it, source row r is row r. A lane takes 4
-// consecutive 16-blocks (one 4-byte scale word per destination). The
-// arithmetic per 16-block is quantize_bf16_kernel's.
+// shared_base + t; without it, source row r is row r. A lane takes one
+// 16-block per round of 32 (coalesced loads and code stores; four lanes'
+// scales make one 4-byte atom word). The group offsets and the tile prefix
+// sit in shared memory. The arithmetic per 16-block is quantize_bf16_kernel's.
 constexpr int kQtWarps = 8;
 constexpr int kQtMaxDest = 33;
 
@@ -207,12 +208,16 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
     const int32_t* __restrict__ gofs, int G, const float* __restrict__ amax_p, uint8_t* __restrict__ q,
     uint8_t* __restrict__ sf_tiles, float* __restrict__ gs_out, float gs_static) {
   pdl_wait();
-  extern __shared__ int tile_base[];  // [G + 1]
+  extern __shared__ int smem_i[];
+  int* s_gofs = smem_i;               // [G + 1] group offsets
+  int* tile_base = smem_i + (G + 1);  // [G + 1] first tile of each group
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) s_gofs[g] = gofs[g];
+  __syncthreads();
   if (threadIdx.x < 32) {  // exclusive prefix of ceil(rows / 128) over the groups
     int carry = 0;
     for (int g0 = 0; g0 <= G; g0 += 32) {
       const int g = g0 + (int)threadIdx.x;
-      const int v = g < G ? (gofs[g + 1] - gofs[g] + 127) / 128 : 0;
+      const int v = g < G ? (s_gofs[g + 1] - s_gofs[g] + 127) / 128 : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -238,34 +243,37 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
       int lo = 0, hi = G - 1;  // group of row my_r: the last g with gofs[g] <= my_r
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(gofs + mid) <= my_r) lo = mid; else hi = mid - 1;
+        if (s_gofs[mid] <= my_r) lo = mid; else hi = mid - 1;
       }
-      const int local = my_r - __ldg(gofs + lo);
+      const int local = my_r - s_gofs[lo];
       my_t = tile_base[lo] + local / 128;
       my_m = local % 128;
     }
   }
   const int KB16 = K / 16, KS = K / 256;
   const uint16_t* src = x + (size_t)row * K;
-  for (int qd = lane; qd < KB16 / 4; qd += 32) {  // 4 consecutive 16-blocks
-    uint32_t c4[8], sw = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t code;
-      quant_block16(src + (size_t)(4 * qd + i) * 16, gs, c4[2 * i], c4[2 * i + 1], code);
-      sw |= code << (8 * i);
-    }
-    const int kb = 4 * qd, ks = kb / 16, kk = (kb / 4) & 3;
+  // 32 consecutive 16-blocks per round, one per lane: the warp's loads and
+  // code stores are contiguous; the four scales of lanes 4i..4i+3 (one
+  // 4-byte word of a scale atom) are gathered into lane 4i, which stores it
+#pragma unroll 2
+  for (int kb0 = 0; kb0 < KB16; kb0 += 32) {
+    const int kb = kb0 + lane;
+    const bool valid = kb < KB16;
+    uint32_t lo = 0, hi = 0, code = 0;
+    if (valid) quant_block16(src + (size_t)kb * 16, gs, lo, hi, code);
+    uint32_t sw = code << (8 * (lane & 3));
+    sw |= __shfl_xor_sync(0xffffffffu, sw, 1);
+    sw |= __shfl_xor_sync(0xffffffffu, sw, 2);
+    const int ks = kb >> 4, kk = (kb >> 2) & 3;
     for (int d = 0; d < ndest; ++d) {
       const int r = __shfl_sync(0xffffffffu, my_r, d);
       const int t = __shfl_sync(0xffffffffu, my_t, d);
       const int m = __shfl_sync(0xffffffffu, my_m, d);
-      if (r < 0) continue;
-      uint4* qd_dst = reinterpret_cast<uint4*>(q + (size_t)r * (K / 2) + (size_t)kb * 8);
-      qd_dst[0] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
-      qd_dst[1] = make_uint4(c4[4], c4[5], c4[6], c4[7]);
-      *reinterpret_cast<uint32_t*>(sf_tiles + (((size_t)t * KS + ks) * 4 + kk) * 512 + (m & 31) * 16 +
-                                   (m >> 5) * 4) = sw;
+      if (r < 0 || !valid) continue;
+      *reinterpret_cast<uint2*>(q + (size_t)r * (K / 2) + (size_t)kb * 8) = make_uint2(lo, hi);
+      if ((lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(sf_tiles + (((size_t)t * KS + ks) * 4 + kk) * 512 + (m & 31) * 16 +
+                                     (m >> 5) * 4) = sw;
     }
   }
 }
@@ -279,7 +287,7 @@ moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const i
   moe_status st = cuda_ok(cudaMemsetAsync(sf_tiles, 0, sf_bytes, s));
   if (st != MOE_OK) return st;
   const int blocks = (src_rows + kQtWarps - 1) / kQtWarps;
-  const size_t smem = (size_t)(G + 1) * sizeof(int);
+  const size_t smem = (size_t)2 * (G + 1) * sizeof(int);
   // after the memset the kernel is an ordinary stream successor (no programmatic launch)
   (void)pdl;
   cudaError_t e = launch_ex(false, quantize_tiles_kernel, dim3(blocks), dim3(kQtWarps * 32), smem, s, x, src_rows, K,
