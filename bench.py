@@ -474,7 +474,7 @@ def run_ours(args):
                   "kernel": "router_gemv_kernel"}
     else:
         r_roof = {"bound": "tensor", "unit": "TFLOP/s", "achieved": r_flops / (r_ms / 1e3) / 1e12,
-                  "peak": pk["bf16"], "kernel": "router_mma_kernel (mma.sync bf16)"}
+                  "peak": pk["bf16"], "kernel": "router_tc_kernel (tcgen05 kind::f16, bf16)"}
     r_roof["frac"] = r_roof["achieved"] / r_roof["peak"]
     router = dict(ms=r_ms, bytes=r_bytes, flops=r_flops, **r_roof,
                   forward_with_router_ms=fr_ms,

@@ -15,13 +15,11 @@
 //   Measured at 8 tokens, E = 320, H = 4096: about 11 us per launch after an
 //   L2 flush, far from the 0.4 us the 2.7 MB would take at HBM speed; the
 //   kernel is latency-bound (sixteen warps per row measured no faster);
-// * more tokens: mma.sync m16n8k16 (bf16 in, fp32 accumulate) over 64 x 64
-//   (token x expert) tiles, K in 64-wide stages moved by cp.async into a
-//   4-deep ring of XOR-swizzled shared-memory tiles read by ldmatrix.
+// * more tokens: tcgen05.mma (bf16 in, fp32 accumulate in TMEM) over
+//   128-expert x 128-token tiles, described below.
 // Both reduce in an order fixed by the shapes, so the logits are the same
 // bits on every run. Rows past T or E and the K tail past H are zero-filled
-// by the copies; every store is bounds-checked. Neither kernel waits on
-// anything but its own copies.
+// by the copies; every store is bounds-checked.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
@@ -110,149 +108,163 @@ __global__ void __launch_bounds__(kGemvWarps * 32) router_gemv_kernel(const uint
 }
 
 // ---------------------------------------------------------------------------
-// Many tokens: 64 tokens x 64 experts per CTA, four warps of 32 x 32.
-constexpr int kBM = 64;
-constexpr int kBN = 64;
-constexpr int kBK = 64;                    // bf16 per row per stage (128 bytes)
-constexpr int kRing = 4;
-constexpr int kMmaThreads = 128;
-constexpr int kTileBytes = kBM * kBK * 2;  // 8 KB (A and B tiles are the same size)
-constexpr int kSlotBytes = 2 * kTileBytes;
-constexpr int kRouterSmem = kRing * kSlotBytes;  // 64 KB
-static_assert(kBM == kBN, "A and B tiles share the copy loop");
+// Many tokens on the 5th-generation tensor cores: one 128-expert x 128-token
+// tile per CTA (swap-AB: router rows on the MMA's M side, so TMEM lane = expert
+// and the epilogue's stores are coalesced along E). Warps 0-3 copy both
+// operands with cp.async into a 6-deep ring of 128-byte-swizzled K-major
+// tiles (64 K per stage; four stages in flight per thread, since the copy
+// rate is set by the bytes in flight) and then read the accumulator back; lane 0 of warp 4
+// issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in TMEM), four per
+// stage. Every wait is bounded: on a timeout the tile's logits are written as
+// NaN, the status word (when given) gets MOE_ERR_TIMEOUT, copies and MMAs
+// drain and TMEM is freed.
+constexpr int kTcM = 128;                   // experts per tile
+constexpr int kTcN = 128;                   // tokens per tile
+constexpr int kTcStages = 6;
+constexpr int kTcTile = 128 * 128;          // bytes of one operand tile (128 rows x 64 bf16)
+constexpr int kTcStageBytes = 2 * kTcTile;  // A (router rows) then B (token rows)
+constexpr int kTcLookahead = 4;             // stages a producer keeps in flight before publishing
+constexpr int kTcThreads = 160;
+constexpr int kTcCols = 128;                // TMEM columns (one fp32 accumulator of N <= 128)
+constexpr long long kTcWaitLimit = 2ll * 1000 * 1000 * 1000;  // cycles (~1 s)
+static_assert(kTcStages >= kTcLookahead + 1, "a producer must publish a stage before it reuses its slot");
 
-// Byte offset of 16-byte chunk `ch` (0..7) of tile row `row`: the chunk index
-// is XORed with the row's low three bits, so the eight rows an ldmatrix phase
-// reads sit in eight different bank groups.
-__device__ __forceinline__ uint32_t swz(int row, int ch) { return (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4)); }
+struct TcSmem {
+  uint64_t full[kTcStages];
+  uint64_t empty[kTcStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kTcSmemBytes = 1024 + (size_t)kTcStages * kTcStageBytes + sizeof(TcSmem);
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__global__ void __launch_bounds__(kMmaThreads) router_mma_kernel(const uint16_t* __restrict__ x,
-                                                                 const uint16_t* __restrict__ w, int T, int H,
-                                                                 int E, float* __restrict__ logits) {
+__global__ void __launch_bounds__(kTcThreads, 1) router_tc_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint16_t* __restrict__ w, int T, int H,
+                                                                  int E, float* __restrict__ logits,
+                                                                  int* __restrict__ status) {
+  using namespace tc;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcSmem* sm = reinterpret_cast<TcSmem*>(base + kTcStages * kTcStageBytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e0 = blockIdx.x * kTcM, t0 = blockIdx.y * kTcN;
+  const int C = H / 8, KT = (C + 7) / 8;
+  const int bn = (min(kTcN, T - t0) + 15) & ~15;  // the MMA's N: tokens of the tile rounded up to 16
   pdl_wait();
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sbase = smem_u32(smem);
-  const int n0 = blockIdx.x * kBN;  // first expert of the tile
-  const int m0 = blockIdx.y * kBM;  // first token of the tile
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wm = warp & 1, wn = warp >> 1;  // 32-token x 32-expert quarter of the tile
-  const int C = H / 8;
-  const int KT = (C + 7) / 8;
-
-  // stage kt -> ring slot: A (x rows) at 0, B (router rows) at kTileBytes
-  auto load = [&](int kt, int slot) {
-    const uint32_t a_s = sbase + (uint32_t)(slot * kSlotBytes);
-    const uint32_t b_s = a_s + kTileBytes;
-#pragma unroll
-    for (int j = 0; j < (kBM * 8) / kMmaThreads; ++j) {
-      const int idx = tid + j * kMmaThreads;
-      const int row = idx >> 3, ch = idx & 7;
-      const int kc = kt * 8 + ch;
-      const int tok = m0 + row, ex = n0 + row;
-      const bool kin = kc < C;
-      const bool va = kin && tok < T, vb = kin && ex < E;
-      cp_async16(a_s + swz(row, ch), va ? (const void*)(x + (size_t)tok * H + (size_t)kc * 8) : (const void*)x, va);
-      cp_async16(b_s + swz(row, ch), vb ? (const void*)(w + (size_t)ex * H + (size_t)kc * 8) : (const void*)w, vb);
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&sm->full[i], 128);
+      mbar_init(&sm->empty[i], 1);
     }
-  };
-
-  float acc[2][4][4];
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni) acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0.0f;
-
-#pragma unroll
-  for (int s = 0; s < kRing - 1; ++s) {
-    if (s < KT) load(s, s);
-    cp_async_commit();
+    mbar_init(&sm->done, 1);
+    sm->abort = 0;
+    fence_barrier_init();
   }
-  for (int kt = 0; kt < KT; ++kt) {
-    cp_async_wait<kRing - 2>();  // stage kt has landed (this thread's copies) ...
-    __syncthreads();             // ... everyone's, and slot (kt - 1) % kRing is free again
-    const int nk = kt + kRing - 1;
-    if (nk < KT) load(nk, nk % kRing);
-    cp_async_commit();
-    const uint32_t a_s = sbase + (uint32_t)((kt % kRing) * kSlotBytes);
-    const uint32_t b_s = a_s + kTileBytes;
-#pragma unroll
-    for (int ks = 0; ks < kBK / 16; ++ks) {
-      uint32_t a[2][4], b[2][4];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        // matrices: rows 0-7 / 8-15 (lane bit 3) x k 0-7 / 8-15 (lane bit 4)
-        const int row = wm * 32 + mi * 16 + (lane & 15);
-        ldsm4(a_s + swz(row, ks * 2 + (lane >> 4)), a[mi]);
-      }
-#pragma unroll
-      for (int nj = 0; nj < 2; ++nj) {
-        // matrices: k 0-7 / 8-15 (lane bit 3) x experts 0-7 / 8-15 (lane bit 4)
-        const int row = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
-        ldsm4(b_s + swz(row, ks * 2 + ((lane >> 3) & 1)), b[nj]);
-      }
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni)
-          mma_bf16_16816(acc[mi][ni], a[mi], b[ni >> 1][(ni & 1) * 2], b[ni >> 1][(ni & 1) * 2 + 1]);
-    }
-  }
-  cp_async_wait<0>();
+  __syncthreads();
+  if (warp == 4) tmem_alloc(&sm->tmem_base, kTcCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort = &sm->abort;
 
+  if (warp < 4) {
+    // ------------------------------------------------ copies, then epilogue
+    int issued = 0, fin = 0;
+    for (int kt = 0; kt < KT; ++kt) {
+      const int slot = kt % kTcStages;
+      if (!mbar_wait(&sm->empty[slot], ((kt / kTcStages) & 1) ^ 1, abort, kTcWaitLimit)) break;
+      const uint32_t a_s = smem_u32(base + slot * kTcStageBytes);
+      const uint32_t b_s = a_s + kTcTile;
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int tok = m0 + wm * 32 + mi * 16 + (lane >> 2) + half * 8;
-      if (tok >= T) continue;
-      float* dst = logits + (size_t)tok * E;
-#pragma unroll
-      for (int ni = 0; ni < 4; ++ni) {
-        const int ex = n0 + wn * 32 + ni * 8 + 2 * (lane & 3);
-        if (ex < E) dst[ex] = acc[mi][ni][2 * half];
-        if (ex + 1 < E) dst[ex + 1] = acc[mi][ni][2 * half + 1];
+      for (int j = 0; j < 8; ++j) {
+        const int idx = tid + 128 * j;
+        const int row = idx >> 3, ch = idx & 7;
+        const int kc = kt * 8 + ch;
+        const bool kin = kc < C;
+        const int ex = e0 + row, tok = t0 + row;
+        const bool va = kin && ex < E, vb = kin && tok < T;
+        const uint32_t off = (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
+        cp_async_16(a_s + off, va ? (const void*)(w + (size_t)ex * H + (size_t)kc * 8) : (const void*)w,
+                    va ? 16u : 0u);
+        cp_async_16(b_s + off, vb ? (const void*)(x + (size_t)tok * H + (size_t)kc * 8) : (const void*)x,
+                    vb ? 16u : 0u);
+      }
+      cp_async_commit();
+      ++issued;
+      if (issued - fin > kTcLookahead) {
+        cp_async_wait<kTcLookahead>();
+        fence_proxy_async_smem();
+        mbar_arrive(&sm->full[fin % kTcStages]);
+        ++fin;
       }
     }
+    cp_async_wait_all();
+    while (fin < issued) {
+      fence_proxy_async_smem();
+      mbar_arrive(&sm->full[fin % kTcStages]);
+      ++fin;
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm->done, 0, abort, kTcWaitLimit) && !*abort);
+    tc_fence_after();
+    const int ex = e0 + warp * 32 + lane;  // TMEM lane = router row
+    for (int c0 = 0; c0 < bn; c0 += 16) {
+      uint32_t r[16];
+      if (ok) {
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+        tmem_ld_wait();
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int tok = t0 + c0 + c;
+        if (ex < E && tok < T) logits[(size_t)tok * E + ex] = ok ? __uint_as_float(r[c]) : __int_as_float(0x7fc00000);
+      }
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------------ MMA
+    const uint32_t idesc = idesc_f16(kTcM, bn, 1);
+    for (int kt = 0; kt < KT; ++kt) {
+      const int slot = kt % kTcStages;
+      if (!mbar_wait(&sm->full[slot], (kt / kTcStages) & 1, abort, kTcWaitLimit)) break;
+      tc_fence_after();
+      const uint32_t as = smem_u32(base + slot * kTcStageBytes);
+      const uint32_t bs = as + kTcTile;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
+        const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
+        mma_f16(tmem, ad, bd, idesc, (kt | kk) != 0);
+      }
+      tc_commit(&sm->empty[slot]);
+    }
+    // `done` arrives once every MMA issued above has completed (also after an abort)
+    tc_commit(&sm->done);
+    const long long c0 = clock64();
+    while (!mbar_try_wait(&sm->done, 0) && clock64() - c0 < kTcWaitLimit) {
+    }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, kTcCols);
+  if (tid == 0 && sm->abort && status != nullptr) set_status(status, MOE_ERR_TIMEOUT);
 }
 
 }  // namespace
 
 moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits,
-                              cudaStream_t s, bool pdl) {
+                              cudaStream_t s, bool pdl, int* status) {
   if (T == 0) return MOE_OK;
   cudaError_t e;
   if (T <= kGemvMaxT) {
     e = launch_ex(pdl, router_gemv_kernel, dim3(E), dim3(kGemvWarps * 32), 0, s, x, w, T, H, E, logits);
   } else {
-    const int mtiles = (T + kBM - 1) / kBM;
-    if (mtiles > 65535) return MOE_ERR_UNSUPPORTED;
-    e = cudaFuncSetAttribute(router_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmem);
+    const int ntiles = (T + kTcN - 1) / kTcN;
+    if (ntiles > 65535) return MOE_ERR_UNSUPPORTED;
+    e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
     if (e != cudaSuccess) return cuda_ok(e);
-    const dim3 grid((E + kBN - 1) / kBN, mtiles);
-    e = launch_ex(pdl, router_mma_kernel, grid, dim3(kMmaThreads), (size_t)kRouterSmem, s, x, w, T, H, E, logits);
+    const dim3 grid((E + kTcM - 1) / kTcM, ntiles);
+    e = launch_ex(pdl, router_tc_kernel, grid, dim3(kTcThreads), kTcSmemBytes, s, x, w, T, H, E, logits, status);
   }
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);

@@ -39,9 +39,9 @@ def _gpu_logits(x, w):
 
 
 # (T, H, E): few-token path (T <= 16) and tiled path; ragged T, E and a K tail
-# (H % 64 != 0); the decode and prefill router shapes
+# (H % 64 != 0); the decode and prefill router shapes and the W4A4 layer's H, E
 ROUTER_CASES = [(1, 256, 8), (8, 4096, 320), (16, 264, 33), (17, 264, 33), (130, 520, 65), (300, 512, 320),
-                (4096, 4096, 320)]
+                (4096, 4096, 320), (300, 7168, 256)]
 
 
 @pytest.mark.parametrize("T,H,E", ROUTER_CASES)
