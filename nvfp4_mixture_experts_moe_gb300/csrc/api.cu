@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "router.cuh"
 
 namespace moe {
 
@@ -468,7 +469,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   const bool pdl = !g_stage_events_set;
   stage_mark(0, s);
   if (L->w_router) {  // router GEMM: the logits come from x
-    st = launch_router_gemm(x, L->w_router, T, H, E, f.logits, s, false, &f.hdr->status);
+    st = launch_router_gemm_status(x, L->w_router, T, H, E, f.logits, s, false, &f.hdr->status);
     if (st != MOE_OK) return st;
     logits = f.logits;
   }

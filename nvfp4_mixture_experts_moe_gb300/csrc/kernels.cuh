@@ -64,11 +64,9 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
 moe_status launch_fold_scales(const uint8_t* in, size_t n, float ratio, uint8_t* out, int* flag, cudaStream_t s);
 
 // Router GEMM: logits fp32 [T, E] = x bf16 [T, H] . w bf16 [E, H]^T, fp32
-// accumulation in a fixed order (H % 8 == 0, 16-byte aligned rows). A bounded
-// wait that gives up writes NaN logits for its tile and MOE_ERR_TIMEOUT into
-// *status (when status is not null).
+// accumulation in a fixed order (H % 8 == 0, 16-byte aligned rows).
 moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits,
-                              cudaStream_t s, bool pdl = false, int* status = nullptr);
+                              cudaStream_t s, bool pdl = false);
 
 moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStream_t s);
 moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,

@@ -22,6 +22,7 @@
 // by the copies; every store is bounds-checked.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "router.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -252,8 +253,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) router_tc_kernel(const uint16_t
 
 }  // namespace
 
-moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits,
-                              cudaStream_t s, bool pdl, int* status) {
+moe_status launch_router_gemm_status(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits,
+                                     cudaStream_t s, bool pdl, int* status) {
   if (T == 0) return MOE_OK;
   cudaError_t e;
   if (T <= kGemvMaxT) {
@@ -269,6 +270,11 @@ moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
+}
+
+moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H, int E, float* logits,
+                              cudaStream_t s, bool pdl) {
+  return launch_router_gemm_status(x, w, T, H, E, logits, s, pdl, nullptr);
 }
 
 }  // namespace moe
