@@ -22,6 +22,8 @@ Sources (web pages, cited by title and section):
 * "GLM-5.3-Flash-NVFP4 #4" discussion, the follow-up on the MoE fault (the
   global scale is a reciprocal: dequant scale amax/(448*6) versus quant scale
   (448*6)/amax; worked value 4.650297705666162e-05 against 21504.0).
+* the same guide, section 6.4 (MXFP4: e2m1 elements, blocks of 32, E8M0
+  scales), for ``mxfp4``.
 
 Precision: everything is float64 except the quantiser, whose decisions are
 integer codes and are therefore taken in fp32 with correctly rounded IEEE
@@ -29,4 +31,4 @@ operations, the precision the CUDA kernels use.
 
 Parity status of each function is stated in its docstring ("pinned by ...").
 """
-from . import nvfp4, moe  # noqa: F401
+from . import nvfp4, moe, mxfp4  # noqa: F401
