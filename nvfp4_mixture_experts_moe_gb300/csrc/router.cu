@@ -7,7 +7,7 @@
 //
 // The product is small next to the experts (E x H weights, T x E x H
 // multiply-adds: 2.6 MB and 10.7 GFLOP for E = 320, H = 4096 at 4096 tokens),
-// so two plain kernels cover it:
+// and two kernels cover it:
 // * few tokens (T <= 16): the weight rows stream from HBM once; one CTA per
 //   expert row, its four warps take a quarter of K each, every lane holds one
 //   fp32 sum per token (its chunks in a fixed order), and the partial sums
