@@ -129,3 +129,13 @@ def test_new_entry_points_validate_on_host(lib):
     assert B.moe_workspace_size(d) >= n0 + 8 * 320 * 4
     d.w_router = 258
     assert B.moe_workspace_size(d) == 0
+
+
+def test_empty_batches_are_host_no_ops(lib):
+    # T = 0 (or rows = 0) returns MOE_OK before any device work
+    d = B.MoeLayerDesc(T=0, H=4096, I=1536, I_shared=1536, E=320, k=8, mode=0, w13=256, w2=256,
+                       w13_shared=256, w2_shared=256)
+    assert lib.moe_nvfp4_forward(ctypes.byref(d), None, None, None, None, None, 0, None) == B.MOE_OK
+    assert lib.moe_nvfp4_quantize_static(None, 0, 64, 1.0, None, None, None) == B.MOE_OK
+    assert lib.moe_combine(None, None, None, 1, 0, 8, 4096, None, None) == B.MOE_OK
+    assert lib.moe_swiglu(None, 0, 128, None, None) == B.MOE_OK
