@@ -201,3 +201,26 @@ def test_brute_force_gemm_tiny():
         ref = sum(float(w[t, j]) * ffn_point(experts[ids[t, j]], x[t], f) for j in range(cfg.k))
         ref += ffn_point(shared, x[t], f)
         assert abs(out[t, f] - ref) <= 1e-12
+
+
+def test_w4a4_golden_script_equals_layer():
+    """The full-size W4A4 golden values come from tests/golden/make_w4a4_full.py,
+    which computes a few tokens' outputs from the batch-wide global scales
+    instead of running oracle.moe.layer on all 16384 tokens at once; on a small
+    W4A4 layer the two must agree to float64 rounding, with the same scales."""
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "make_w4a4_full.py")
+    spec = importlib.util.spec_from_file_location("make_w4a4_full", path)
+    mk = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mk)
+    cfg = si.LayerConfig("w4a4_pin", T=64, H=512, I=256, I_s=256, E=8, k=2, mode="w4a4", outliers=True)
+    toks = np.array([0, 5, 17, 40, 63])
+    out, gs_x, amax_h, gs_h, ids, w = mk.golden_rows(cfg, toks, threads=4, log=lambda m: None)
+    W = {e: tuple(moe.QuantWeight.from_dense(si.make_expert_weight(cfg, e, m).float().numpy())
+                  for m in ("gate", "up", "down")) for e in range(cfg.E + 1)}
+    ref, parts = moe.layer(si.make_x(cfg).float().numpy(), si.make_logits(cfg).numpy(),
+                           [W[e] for e in range(cfg.E)], W[cfg.E], cfg.k, mode="w4a4", return_parts=True)
+    assert gs_x == parts["xgs"] and gs_h == parts["hgs"]
+    assert amax_h == np.float32(np.max(np.abs(parts["h_bf16"])))
+    assert np.abs(out - ref[toks]).max() <= 1e-12 * max(1.0, np.abs(ref).max())
