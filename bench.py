@@ -12,7 +12,11 @@ expert intermediate 1536, 320 routed experts top-8 + 1 shared, W4A16).
 
 Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
 independent replica of the same workload (the layer does not shard here:
-replicas only) and ``value`` is the sum over ranks.
+replicas only) and ``value`` is the sum over ranks. On one GPU the line also
+carries ``configs``: the same measurement (step time, tokens/s, roofline of
+the dominant kernel, layer roofline, end-to-end number, CPU baseline) for
+every other workload (tiny, prefill, skewed, W4A4), run in the same process
+after the headline; ``--only`` skips them.
 """
 from __future__ import annotations
 
@@ -44,6 +48,7 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=None, help="override T (a smaller case, e.g. for ncu)")
     ap.add_argument("--experts", type=int, default=None, help="override E (a smaller case, e.g. for ncu)")
+    ap.add_argument("--only", action="store_true", help="measure the chosen workload only (no 'configs' key)")
     return ap.parse_args()
 
 
@@ -206,6 +211,26 @@ def oracle_rows(plan, qw, xs, out):
     return time.perf_counter() - t0, time.process_time() - c0
 
 
+def oracle_rows_w4a4(plan, qw, xs, gs_x, out):
+    """W4A4 rows through the oracle: x quantised with the tensor's global
+    scale, h rounded to bf16 and quantised (one global scale over the sampled
+    rows), down GEMM. Returns (wall seconds, process CPU seconds)."""
+    import numpy as np
+    from oracle import moe as omoe
+    from oracle import nvfp4 as onv
+    c0, t0 = time.process_time(), time.perf_counter()
+    hs = []
+    for t, e, wt in plan:
+        g, u, d = qw[e]
+        xq, xsf, _ = onv.quantize(xs[t:t + 1], gs=gs_x)
+        hs.append(omoe.bf16_round(omoe.gate_up_swiglu(onv.dequantize(xq, xsf, gs_x), g, u)))
+    gs_h = onv.global_scale(np.float32(max(float(np.abs(h).max()) for h in hs)))
+    for (t, e, wt), h in zip(plan, hs):
+        hq, hsf, _ = onv.quantize(h.astype(np.float32), gs=gs_h)
+        out[t] += wt * omoe.down_proj(onv.dequantize(hq, hsf, gs_h), qw[e][2])[0]
+    return time.perf_counter() - t0, time.process_time() - c0
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -263,40 +288,60 @@ def workload(args):
     return cfg
 
 
-def run_ours(args):
-    import numpy as np
+def build_layer(cfg, dev):
+    """A device layer with every expert of the workload prepared (seeded weights)."""
     import torch
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    import __graft_entry__
-    __graft_entry__.build()
     import synthetic_inputs as si
     from nvfp4_mixture_experts_moe_gb300 import MOE_W4A4, MOE_W4A16, Nvfp4MoeLayer
-    from nvfp4_mixture_experts_moe_gb300 import binding as B
-
-    cfg = workload(args)
     mode = MOE_W4A4 if cfg.mode == "w4a4" else MOE_W4A16
-    t_setup = time.perf_counter()
     layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mode=mode, I_shared=cfg.I_s, device=dev)
-    chunk = 32
-    for e0 in range(0, cfg.E + 1, chunk):
-        W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + chunk))), threads=16)
+    for e0 in range(0, cfg.E + 1, 32):
+        W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + 32))), threads=16)
         for e, mats in W.items():
             layer.set_expert(e, *mats)
         del W
     torch.cuda.synchronize()
-    setup_s = time.perf_counter() - t_setup
+    return layer
 
-    # distinct batches (seeds) rotated over the steps, resident in HBM
+
+def decode_fused(cfg):
+    """The forward runs this workload as the single-kernel decode path."""
+    return cfg.mode == "w4a16" and cfg.T <= 8
+
+
+def cpu_baseline(cfg, x0, l0, n_tokens):
+    """The float64 oracle on the first ``n_tokens`` tokens of a batch, timed on
+    the host cores (weights quantised by the oracle beforehand, untimed)."""
+    import numpy as np
+    from oracle import nvfp4 as onv
+    n_rows = min(cfg.T, n_tokens) * (cfg.k + 1)
+    plan, qw, xs = oracle_prepare(cfg, x0, l0, n_rows, pool_threads=16)
+    if cfg.mode == "w4a4":
+        wall, cpu = oracle_rows_w4a4(plan, qw, xs, onv.global_scale(np.float32(np.abs(xs).max())),
+                                     np.zeros((cfg.T, cfg.H)))
+        how = ("x rows quantised with the tensor's global scale, h of the sampled rows with the "
+               "sample's own global scale")
+    else:
+        wall, cpu = oracle_rows(plan, qw, xs, np.zeros((cfg.T, cfg.H)))
+        how = "W4A16"
+    rows = len(plan)
+    return {"value": rows / (cfg.k + 1) / wall, "unit": "tokens/s", "cores": round(cpu / wall, 2),
+            "kind": "oracle",
+            "sample": f"first {rows} (token, expert) rows = {rows / (cfg.k + 1):.0f} token(s) of batch 0 through "
+                      f"the float64 oracle ({how}); weights prepared untimed"}
+
+
+def measure(cfg, layer, args, dev, dist, world, rank, headline):
+    """Times the forward on ``cfg`` (K steps after W warm-up steps, L2 flushed
+    between steps) and returns the fields of a result line. ``headline`` adds
+    the clock record, CUDA-graph replay and the router GEMM."""
+    import numpy as np
+    import torch
+
+    import synthetic_inputs as si
+    from nvfp4_mixture_experts_moe_gb300 import binding as B
+
     nb = max(1, args.batches)
     batches = []
     for b in range(nb):
@@ -306,11 +351,11 @@ def run_ours(args):
     ids_list = [__import__("oracle").moe.route(lg.cpu().numpy(), cfg.k)[0] for _, lg in batches]
     alg = algorithmic(cfg, ids_list)
 
-    ws = layer.workspace()
+    ws = layer.workspace(cfg.T)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    desc = layer.desc()
+    desc = layer.desc(cfg.T)
 
     def step(i, stage_events=None):
         x, lg = batches[i % nb]
@@ -323,26 +368,28 @@ def run_ours(args):
         step(i)
     torch.cuda.synchronize()
     if B.moe_get_device_status(ws) != 0:
-        raise RuntimeError("device status set during warm-up")
+        raise RuntimeError(f"{cfg.name}: device status set during warm-up")
 
     K = args.steps
-    # Pass 1 (the headline): K steps, one event pair per step, nothing else
-    # inside the forward (kernels chain with programmatic dependent launch).
+    # Pass 1 (the measurement): K steps, one event pair per step, nothing else
+    # inside the forward. Pass 2: the same K steps with the library recording
+    # an event between every stage, for the per-kernel durations.
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    # Pass 2: the same K steps with the library recording an event between
-    # every stage, for the per-kernel durations of the roofline.
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(B.MOE_STAGE_COUNT)] for _ in range(K)]
     for e in [x for pair in ev for x in pair] + [x for row in sev for x in row]:
         e.record(stream)  # torch creates the underlying CUDA events on first record
     torch.cuda.synchronize()
-    props = torch.cuda.get_device_properties(dev)
-    bus = getattr(props, "pci_bus_id", None)
-    sampler = ClockSampler(bus if isinstance(bus, str) else None)
+    sampler = None
+    if headline:
+        props = torch.cuda.get_device_properties(dev)
+        bus = getattr(props, "pci_bus_id", None)
+        sampler = ClockSampler(bus if isinstance(bus, str) else None)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.2)
+    if sampler:
+        sampler.start()
+        time.sleep(0.2)
     launches0 = B.moe_kernel_launches()
     t0 = time.perf_counter()
     for i in range(K):
@@ -355,7 +402,7 @@ def run_ours(args):
     launches = B.moe_kernel_launches() - launches0
     if dist:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
     for i in range(K):
         flush.zero_()
@@ -365,7 +412,7 @@ def run_ours(args):
     staged_step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in sev)
     ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
     if B.moe_get_device_status(ws) != 0:
-        raise RuntimeError("device status set during the timed steps")
+        raise RuntimeError(f"{cfg.name}: device status set during the timed steps")
     value = job_tokens_per_s(cfg.T, world, ms)
 
     # end to end: pinned host inputs copied in, result read back, every step
@@ -387,10 +434,73 @@ def run_ours(args):
             e2e_ev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dist, dev)
+    h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
+    d2h = hout.numel() * hout.element_size()
 
-    # the same forward captured once as a CUDA graph and replayed (batch 0's
-    # inputs, L2 flushed between replays outside the graph)
-    graph = None
+    pk = peaks()
+    per_stage = {name: statistics.mean(stage_ms[i]) for i, name in enumerate(B.STAGES)}
+    if decode_fused(cfg):
+        # one kernel is the whole layer: its roofline is the layer's bytes
+        k_ms = per_stage["route"]
+        bound, unit, peak = "hbm", "GB/s", pk["hbm"]
+        achieved = alg["layer_bytes"] / (k_ms / 1e3) / 1e9
+        kernel = "decode_fused_kernel (whole layer: route, permute, gate/up GEMM + SwiGLU, down GEMM, combine)"
+        traffic = ncu_traffic(cfg.name)
+        per_unit = "touched experts x (W13 + W2 NVFP4 bytes) + x in + out + logits"
+    else:
+        k_ms = per_stage["gemm1_gate_up_swiglu"]
+        kernel = "gemm1 (gate/up grouped GEMM + SwiGLU epilogue)"
+        if cfg.mode == "w4a16" and cfg.T <= 64:
+            bound, unit, peak = "hbm", "GB/s", pk["hbm"]
+            achieved = alg["gemm1_bytes"] / (k_ms / 1e3) / 1e9
+            per_unit = "touched experts x W13 NVFP4 bytes + x rows in + h out"
+        else:
+            bound, unit = "tensor", "TFLOP/s"
+            achieved = alg["gemm1_flops"] / (k_ms / 1e3) / 1e12
+            peak = pk["bf16"] * (6.0 if cfg.mode == "w4a4" else 1.0)
+            per_unit = "rows x 2 x 2I x H FLOPs"
+        traffic = ncu_traffic(cfg.name)
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic, "kernel": kernel, "kernel_ms": k_ms, "per_launch": per_unit,
+                "peak_source": pk["source"] + (" (fp4 = 6 x measured bf16, the nominal ratio)"
+                                               if cfg.mode == "w4a4" and bound == "tensor" else "")}
+    layer_time_hbm = alg["layer_bytes"] / (pk["hbm"] * 1e9)
+    tc_peak = pk["bf16"] * (6.0 if cfg.mode == "w4a4" else 1.0)
+    layer_time_tc = alg["layer_flops"] / (tc_peak * 1e12)
+    layer_roof_ms = 1e3 * max(layer_time_hbm, layer_time_tc)
+    res = {"ms_per_step": ms, "value": value, "unit": "tokens/s",
+           "config": config_dict(cfg, nb, "flushed: 258 MB write between timed steps"),
+           "roofline": roofline,
+           "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
+                              "bound": "hbm" if layer_time_hbm >= layer_time_tc else "tensor",
+                              "bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
+                              "touched_experts": alg["touched_experts"]},
+           "stages_ms": per_stage,
+           "stages_note": ("single-kernel decode path: 'route' is the whole fused kernel"
+                           if decode_fused(cfg) else
+                           "per-stage CUDA events recorded by the library in a second pass of the same K steps")
+                          + f" (that pass: {staged_step_ms:.4f} ms/step, stages serialised)",
+           "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+           "gpu_launches": int(launches), "host_wall_s": t1 - t0}
+    if clocks is not None:
+        res["clocks"] = clocks
+    if headline:
+        res["graph_replay"] = graph_replay(desc, batches, out, ws, flush, stream, args, dist, dev, world, cfg)
+        res["router_gemm"] = router_gemm(cfg, layer, batches, out, flush, stream, args, dev, pk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok = {"tiny": 16, "w4a4": 1}.get(cfg.name, args.cpu_sample_tokens)
+        res["cpu_baseline"] = cpu_baseline(cfg, batches[0][0].cpu(), batches[0][1].cpu(), n_tok)
+    return res
+
+
+def graph_replay(desc, batches, out, ws, flush, stream, args, dist, dev, world, cfg):
+    """The same forward captured once as a CUDA graph and replayed (batch 0's
+    inputs, L2 flushed between replays outside the graph)."""
+    import torch
+
+    from nvfp4_mixture_experts_moe_gb300 import binding as B
+    K = args.steps
     try:
         gx, gl = batches[0]
         g = torch.cuda.CUDAGraph()
@@ -410,24 +520,29 @@ def run_ours(args):
                 gev[i - args.warmup][1].record(stream)
         torch.cuda.synchronize()
         g_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in gev), dist, dev)
-        graph = {"ms_per_step": g_ms, "value": job_tokens_per_s(cfg.T, world, g_ms), "unit": "tokens/s",
-                 "note": "moe_nvfp4_forward captured once in a CUDA graph, replayed K times"}
         if B.moe_get_device_status(ws) != 0:
             raise RuntimeError("device status set during graph replay")
+        return {"ms_per_step": g_ms, "value": job_tokens_per_s(cfg.T, world, g_ms), "unit": "tokens/s",
+                "note": "moe_nvfp4_forward captured once in a CUDA graph, replayed K times"}
     except RuntimeError as exc:  # capture not possible here: report why
-        graph = {"error": str(exc).splitlines()[0][:200]}
-    h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
-    d2h = hout.numel() * hout.element_size()
+        return {"error": str(exc).splitlines()[0][:200]}
 
-    # The router GEMM ahead of the top-k (logits = x W_router^T) on this
-    # workload's shapes: alone, and inside the forward (which then takes x
-    # only). The headline step above takes the logits as an input.
+
+def router_gemm(cfg, layer, batches, out, flush, stream, args, dev, pk):
+    """The router GEMM ahead of the top-k (logits = x W_router^T) on this
+    workload's shapes: alone, and inside the forward (which then takes x
+    only). The measured step takes the logits as an input."""
+    import torch
+
+    import synthetic_inputs as si
+    from nvfp4_mixture_experts_moe_gb300 import binding as B
+    K, nb = args.steps, len(batches)
     w_router = si.make_router_weight(cfg).to(dev)
     rlog = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
     rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     layer.set_router(w_router)
-    desc_r = layer.desc()
+    desc_r = layer.desc(cfg.T)
     layer.set_router(None)
     ws_r = torch.empty(B.moe_workspace_size(desc_r), dtype=torch.uint8, device=dev)
     ws_r[:256].zero_()
@@ -452,23 +567,6 @@ def run_ours(args):
     fr_ms = statistics.mean(a.elapsed_time(b) for a, b in fev)
     r_bytes = cfg.E * cfg.H * 2 + cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4
     r_flops = 2 * cfg.T * cfg.H * cfg.E
-
-    pk = peaks()
-    per_stage = {name: statistics.mean(stage_ms[i]) for i, name in enumerate(B.STAGES)}
-    g1_ms = per_stage["gemm1_gate_up_swiglu"]
-    if cfg.mode == "w4a16" and cfg.T <= 64:
-        bound, unit = "hbm", "GB/s"
-        achieved = alg["gemm1_bytes"] / (g1_ms / 1e3) / 1e9
-        peak = pk["hbm"]
-        traffic = ncu_traffic("decode") if cfg.name == "decode" else None
-    else:
-        bound, unit = "tensor", "TFLOP/s"
-        achieved = alg["gemm1_flops"] / (g1_ms / 1e3) / 1e12
-        peak = pk["bf16"] * (6.0 if cfg.mode == "w4a4" else 1.0)
-        traffic = None
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": traffic, "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU epilogue)",
-                "peak_source": pk["source"]}
     if cfg.T <= 16:
         r_roof = {"bound": "hbm", "unit": "GB/s", "achieved": r_bytes / (r_ms / 1e3) / 1e9, "peak": pk["hbm"],
                   "kernel": "router_gemv_kernel"}
@@ -476,44 +574,62 @@ def run_ours(args):
         r_roof = {"bound": "tensor", "unit": "TFLOP/s", "achieved": r_flops / (r_ms / 1e3) / 1e12,
                   "peak": pk["bf16"], "kernel": "router_tc_kernel (tcgen05 kind::f16, bf16)"}
     r_roof["frac"] = r_roof["achieved"] / r_roof["peak"]
-    router = dict(ms=r_ms, bytes=r_bytes, flops=r_flops, **r_roof,
-                  forward_with_router_ms=fr_ms,
-                  note="logits = x W_router^T (bf16 [E, H] router, seeded N(0, 1/H)); timed alone and inside "
-                       "moe_nvfp4_forward (x only), L2 flushed between launches")
-    layer_time_hbm = alg["layer_bytes"] / (pk["hbm"] * 1e9)
-    layer_time_tc = alg["layer_flops"] / (peak * 1e12 if bound == "tensor" else pk["bf16"] * 1e12)
-    layer_roof_ms = 1e3 * max(layer_time_hbm, layer_time_tc)
+    return dict(ms=r_ms, bytes=r_bytes, flops=r_flops, **r_roof, forward_with_router_ms=fr_ms,
+                note="logits = x W_router^T (bf16 [E, H] router, seeded N(0, 1/H)); timed alone and inside "
+                     "moe_nvfp4_forward (x only), L2 flushed between launches")
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp4xf16" if cfg.mode == "w4a16" else "fp4",
-            "data": "synthetic",
-            "config": config_dict(cfg, nb, "flushed: 258 MB write between timed steps"),
-            "roofline": roofline,
-            "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
-                               "bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
-                               "touched_experts": alg["touched_experts"]},
-            "stages_ms": per_stage,
-            "stages_note": "per-stage CUDA events recorded by the library in a second pass of the same K steps "
-                           f"(that pass: {staged_step_ms:.4f} ms/step, stages serialised)",
-            "e2e": {"value": job_tokens_per_s(cfg.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "graph_replay": graph,
-            "router_gemm": router,
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-            "host_wall_s": t1 - t0, "setup_s": setup_s}
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        x0, l0 = batches[0][0].cpu(), batches[0][1].cpu()
-        n_rows = min(cfg.T, args.cpu_sample_tokens) * (cfg.k + 1)
-        plan, qw, xs = oracle_prepare(cfg, x0, l0, n_rows, pool_threads=16)
-        wall, cpu = oracle_rows(plan, qw, xs, np.zeros((cfg.T, cfg.H)))
-        rows = len(plan)
-        line["cpu_baseline"] = {"value": rows / (cfg.k + 1) / wall, "unit": "tokens/s",
-                                "cores": round(cpu / wall, 2), "kind": "oracle",
-                                "sample": f"first {rows} (token, expert) rows = {rows / (cfg.k + 1):.0f} tokens "
-                                          f"of batch 0 through the float64 oracle; weights prepared untimed"}
+def run_ours(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import synthetic_inputs as si
+
+    cfg = workload(args)
+    t_setup = time.perf_counter()
+    layer = build_layer(cfg, dev)
+    setup_s = time.perf_counter() - t_setup
+    res = measure(cfg, layer, args, dev, dist, world, rank, headline=True)
+    line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp4xf16" if cfg.mode == "w4a16" else "fp4",
+            "data": "synthetic"}
+    line.update({k: v for k, v in res.items() if k not in ("value", "ms_per_step", "unit")})
+    line["setup_s"] = setup_s
+
+    # every other workload in the same process (one GPU only): its own step
+    # time, roofline, end-to-end number and CPU baseline
+    if world == 1 and not args.only and args.tokens is None and args.experts is None:
+        configs = {}
+        same_layer = (cfg.H, cfg.I, cfg.I_s, cfg.E, cfg.k, cfg.mode, cfg.seed)
+        for name, c in si.CONFIGS.items():
+            if name == cfg.name:
+                continue
+            if (c.H, c.I, c.I_s, c.E, c.k, c.mode, c.seed) != same_layer:
+                del layer
+                torch.cuda.empty_cache()
+                t_setup = time.perf_counter()
+                layer = build_layer(c, dev)
+                same_layer = (c.H, c.I, c.I_s, c.E, c.k, c.mode, c.seed)
+                setup = time.perf_counter() - t_setup
+            else:
+                setup = 0.0
+            r = measure(c, layer, args, dev, None, 1, 0, headline=False)
+            r["setup_s"] = setup
+            configs[name] = r
+        line["configs"] = configs
+
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

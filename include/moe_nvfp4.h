@@ -59,7 +59,11 @@ typedef enum {
 
 typedef enum {
   MOE_W4A16 = 0, /* NVFP4 weights, bf16 activations (weight-only) */
-  MOE_W4A4 = 1   /* NVFP4 weights and activations (block-scaled FP4 MMA) */
+  MOE_W4A4 = 1,  /* NVFP4 weights and activations (block-scaled FP4 MMA) */
+  MOE_MXFP4 = 2  /* MXFP4 weights and activations: e2m1 with one power-of-two
+                    E8M0 scale per 32 along K, no global scale ("vLLM on the
+                    NVIDIA DGX Spark", section 6.4 "NVFP4 vs MXFP4");
+                    block-scaled FP4 MMA with UE8M0 scales */
 } moe_mode;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -159,6 +163,24 @@ moe_status moe_nvfp4_quantize_static(const uint16_t* x, int rows, int K, float g
                                      uint8_t* q, uint8_t* sf, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * BF16 -> MXFP4 ("vLLM on the NVIDIA DGX Spark", section 6.4 "NVFP4 vs
+ * MXFP4": e2m1 elements, blocks of 32 along K, one E8M0 power-of-two scale
+ * per block, no per-tensor scale). Per block: e = floor(log2 max|x_i|) - 2,
+ * clamped to [-127, 127] (so max|x_i| / 2^e lies in [4, 8)); an all-zero
+ * block takes e = -127 and zero codes; sf = e + 127; code_i = e2m1(x_i *
+ * 2^-e), nearest even, saturating at 6, sign kept (the multiply is exact).
+ *
+ * x  bf16 [rows, K], K % 32 == 0, 16-byte aligned
+ * q  uint8 [rows, K/2] out, packed codes (element 2j in the low nibble),
+ *    16-byte aligned
+ * sf uint8 [rows, K/32] out, E8M0 scale codes
+ * Errors: K % 32 != 0, a NULL or misaligned pointer -> MOE_ERR_INVALID_ARG;
+ * rows = 0 -> MOE_OK with nothing enqueued.
+ */
+moe_status moe_mxfp4_quantize(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t* sf,
+                              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Checkpoint import ("Serving Solar Open 2 on DGX Spark", "Supporting real
  * NVFP4 checkpoints"; "GLM-5.3-Flash-NVFP4 #4" discussion, follow-up on the
  * MoE fault).
@@ -205,6 +227,8 @@ moe_status moe_nvfp4_fold_scales(const uint8_t* sf_in, size_t n, float ratio, ui
  * entry for a plain matrix, two (gate, up) when gate_up != 0, in which case
  * the N rows are [gate (N/2 rows); up (N/2 rows)]. out must hold
  * moe_prepare_size(N, K, mode, gate_up) bytes, 256-byte aligned.
+ * MOE_MXFP4: sf is uint8 [N, K/32] E8M0 codes (moe_mxfp4_quantize), gs is
+ * not read (may be NULL), K % 256 == 0, and code 0xFF (NaN) is refused.
  * Errors: gs <= 0 or non-finite (a zero scale would silently zero every
  * expert output, the failure described in "GLM-5.3-Flash-NVFP4 #4"), a block
  * scale with its sign bit set or a NaN code, N % 128 != 0 (N/2 % 64 for
@@ -236,7 +260,8 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf,
  * out_amax (nullable, device fp32, must start at 0): atomically maxed with
  *   |out| (as stored), to feed the next quantisation.
  * ws: scratch of at least moe_gemm_workspace_size(num_groups) bytes.
- * Limits: K % 64 == 0, N % 128 == 0, num_groups <= 1025.
+ * Limits: K % 64 == 0, N % 128 == 0, num_groups <= 1025. MOE_MXFP4 ->
+ * MOE_ERR_UNSUPPORTED here (MXFP4 layers run through moe_nvfp4_forward).
  */
 typedef struct {
   moe_mode mode;
@@ -274,15 +299,21 @@ moe_status moe_swiglu(const float* gu, int rows, int I, uint16_t* h,
  * [Combine]; section 4.3 top-k weight reduction). Deterministic: fp32 sums
  * in the fixed order j = 0..k-1, then the shared row, rounded once to bf16.
  *
- * y        bf16 [T*k (+T), H]: routed rows in sorted order, then (if
- *          y_shared_rows != 0) the shared expert's T rows
- * inv_perm int32 [T*k] pair -> sorted row
+ * y        bf16 [T*k, H]: the routed rows in sorted (grouped) order
+ * inv_perm int32 [T*k] pair -> sorted row; a negative entry (a dropped pair)
+ *          contributes nothing
  * topk_w   fp32 [T, k] or NULL: multiplies row (t, j) (NULL when GEMM 2
  *          already applied the routing weight)
+ * y_shared fp32 [T, H] or NULL: the shared expert's rows, added with weight
+ *          1 (kept in fp32: with weight 1 their bf16 rounding would be the
+ *          largest single error term of the output)
  * out      bf16 [T, H]
+ * Errors: T < 0, k < 1, H <= 0 or H % 8 != 0, a NULL y / inv_perm / out, or
+ * a pointer that is not 16-byte aligned -> MOE_ERR_INVALID_ARG; T = 0 ->
+ * MOE_OK with nothing enqueued.
  */
 moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
-                       int y_shared_rows, int T, int k, int H, uint16_t* out,
+                       const float* y_shared, int T, int k, int H, uint16_t* out,
                        moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -296,7 +327,23 @@ moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* 
  * x_global_scale, h_global_scale (W4A4 only; 0 = dynamic): static
  *   calibrated global scales (quant convention) for the two activation
  *   quantisations, x before GEMM 1 and h before GEMM 2, in place of the
- *   dynamic 2688 / amax. Must be 0 on W4A16 layers.
+ *   dynamic 2688 / amax. Must be 0 on W4A16 and MXFP4 layers.
+ * expert_offset, local_experts (expert parallelism; "Serving Solar Open 2
+ *   on DGX Spark", "Adding Expert Parallelism to b12x": each node holds a
+ *   contiguous shard of the experts, global expert ids are remapped to
+ *   shard-local ones and out-of-shard pairs are filtered out): the router
+ *   still ranks all E experts (logits [T, E], topk_ids_out global ids), but
+ *   only pairs routed to experts [expert_offset, expert_offset +
+ *   local_experts) are computed, with w13 / w2 holding just those
+ *   local_experts blocks. out is then this shard's partial output: the sum
+ *   over the shard's pairs (with their routing weights) plus the shared
+ *   expert if this shard carries one (give the shared expert to exactly one
+ *   shard). Summing the shards' outputs gives the layer's output. With
+ *   dynamic W4A4 scales the h scale is the shard's own (the amax of its rows).
+ *   local_experts = 0 means all E experts (expert_offset must be 0).
+ * mode MOE_MXFP4: weights prepared with MOE_MXFP4; x and h (rounded to bf16)
+ *   are quantised to MXFP4 (moe_mxfp4_quantize's steps) and both GEMMs run
+ *   block-scaled FP4 MMA with UE8M0 scales; H % 256 == 0 and I % 256 == 0.
  */
 typedef struct {
   int T, H, I, I_shared, E, k;
@@ -308,6 +355,9 @@ typedef struct {
   const uint16_t* w_router;
   float x_global_scale;
   float h_global_scale;
+  int expert_offset;   /* expert parallelism: this forward computes experts  */
+  int local_experts;   /* [expert_offset, expert_offset + local_experts) of E; */
+                       /* 0 = all E (no sharding)                             */
 } moe_layer_desc;
 
 /* Workspace bytes moe_nvfp4_forward needs for this descriptor. */
@@ -318,7 +368,16 @@ size_t moe_workspace_size(const moe_layer_desc* L);
  * hold moe_workspace_size(L) bytes, 256-byte aligned. Errors: a scale in
  * x_global_scale / h_global_scale that is negative or non-finite, or nonzero
  * on a W4A16 layer -> MOE_ERR_INVALID_ARG; a misaligned w_router or H % 8 != 0
- * with it -> MOE_ERR_INVALID_ARG. */
+ * with it -> MOE_ERR_INVALID_ARG.
+ *
+ * Decode batches (W4A16, T <= 8) run as one kernel ("micro path", "Serving
+ * Solar Open 2 on DGX Spark", "The fix"; "vLLM on the NVIDIA DGX Spark",
+ * section 4.3): routing, permutation, both GEMMs and the combine in a single
+ * cooperative launch of one CTA per SM, after one small memset of its
+ * counters (plus the router GEMM first when w_router is set). It needs the
+ * whole GPU: another kernel occupying SMs at launch time makes the launch
+ * fail with MOE_ERR_CUDA rather than wait. Its output equals the
+ * multi-kernel path's bit for bit. */
 moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const float* logits,
                              uint16_t* out, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
                              moe_stream_t stream);
@@ -337,7 +396,9 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream);
  * GEMM 2, combine; a stage the mode does not run records at the same point
  * as the previous one; with w_router the router GEMM belongs to the route
  * stage), all on the call's stream; the setting is then
- * cleared. Pass NULL to clear it explicitly.
+ * cleared. Pass NULL to clear it explicitly. On the single-kernel decode
+ * path events[0] is recorded right before that kernel and events[1..] right
+ * after it, so stage 0 -> 1 times the kernel alone.
  *
  * moe_kernel_launches: number of kernels this library has launched in this
  * process so far (all threads).
@@ -345,6 +406,30 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream);
 #define MOE_STAGE_COUNT 8
 moe_status moe_set_stage_events(void* const* events, int n);
 unsigned long long moe_kernel_launches(void);
+
+/* ------------------------------------------------------------------------
+ * Test hooks (no counterpart in the pages). Process-wide settings that let
+ * the test suite reach paths a correct run never takes; production callers
+ * leave them at their defaults.
+ *
+ * MOE_DEBUG_WAIT_LIMIT (default 4000000000): the number of GPU clock cycles
+ *   after which a bounded device wait gives up (about 2 s at 2 GHz). On a
+ *   timeout the kernel records MOE_ERR_TIMEOUT in the workspace status word,
+ *   lets its copies and tensor-core work drain, frees its tensor memory and
+ *   returns. value <= 0 restores the default.
+ * MOE_DEBUG_EXTRA_ARRIVALS (default 0): the single-kernel decode path waits
+ *   for this many more arrivals per gate/up tile than happen, so its down
+ *   phase times out (exercises the timeout path without any fault).
+ * MOE_DEBUG_DISABLE_DECODE_FUSED (default 0): nonzero makes
+ *   moe_nvfp4_forward take the multi-kernel path for decode batches too.
+ * Errors: an unknown key -> MOE_ERR_INVALID_ARG.
+ */
+typedef enum {
+  MOE_DEBUG_WAIT_LIMIT = 1,
+  MOE_DEBUG_EXTRA_ARRIVALS = 2,
+  MOE_DEBUG_DISABLE_DECODE_FUSED = 3
+} moe_debug_key;
+moe_status moe_debug_set(int key, long long value);
 
 /* ------------------------------------------------------------------------
  * moe_permute_noalloc: the permutation of moe_permute for callers that
@@ -365,8 +450,10 @@ unsigned long long moe_kernel_launches(void);
  * anything is enqueued.
  *
  * The first call on a device looks up the array's device address for that
- * device (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture. Every call on a device shares the one array and
+ * device (cudaGetSymbolAddress) and caches it for the life of the process;
+ * make that first call before any stream capture. A device reset
+ * (cudaDeviceReset) invalidates the cached address: after one, this entry
+ * point must not be called again in the same process. Every call on a device shares the one array and
  * leaves its contents behind; each call clears the status word it needs.
  * Calls that overlap on the GPU (on different streams, say) race on the
  * array: order them on one stream or with events.

@@ -5,5 +5,5 @@ The compute lives in the CUDA library ``_lib/libmoe_nvfp4.so`` (C ABI in
 and ``layer`` keeps one layer's prepared weights resident on the device.
 """
 from . import binding  # noqa: F401
-from .binding import MoeError, MOE_W4A16, MOE_W4A4  # noqa: F401
-from .layer import Nvfp4MoeLayer, quantize_bf16  # noqa: F401
+from .binding import MoeError, MOE_W4A16, MOE_W4A4, MOE_MXFP4  # noqa: F401
+from .layer import Nvfp4MoeLayer, quantize_bf16, quantize_mx  # noqa: F401

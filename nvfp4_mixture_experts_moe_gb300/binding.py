@@ -18,8 +18,9 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_nvfp4.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_ERR_WORKSPACE, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
-MOE_W4A16, MOE_W4A4 = 0, 1
+MOE_W4A16, MOE_W4A4, MOE_MXFP4 = 0, 1, 2
 MOE_SCALE_QUANT, MOE_SCALE_DEQUANT = 0, 1
+MOE_DEBUG_WAIT_LIMIT, MOE_DEBUG_EXTRA_ARRIVALS, MOE_DEBUG_DISABLE_DECODE_FUSED = 1, 2, 3
 
 _lib = None
 
@@ -38,7 +39,8 @@ class MoeLayerDesc(ctypes.Structure):
                 ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("w13_shared", ctypes.c_void_p), ("w2_shared", ctypes.c_void_p),
                 ("w_router", ctypes.c_void_p),
-                ("x_global_scale", ctypes.c_float), ("h_global_scale", ctypes.c_float)]
+                ("x_global_scale", ctypes.c_float), ("h_global_scale", ctypes.c_float),
+                ("expert_offset", ctypes.c_int), ("local_experts", ctypes.c_int)]
 
 
 class MoeGemmArgs(ctypes.Structure):
@@ -60,6 +62,7 @@ _SIGS = {
     "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_router_gemm": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_nvfp4_quantize_static": (_I, [_P, _I, _I, ctypes.c_float, _P, _P, _P]),
+    "moe_mxfp4_quantize": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_import_global_scale": (_I, [ctypes.c_float, _I, ctypes.POINTER(ctypes.c_float)]),
     "moe_nvfp4_fold_scales": (_I, [_P, _Z, ctypes.c_float, _P, _P]),
     "moe_permute_workspace_size": (_Z, [_I, _I, _I]),
@@ -71,13 +74,14 @@ _SIGS = {
     "moe_gemm_workspace_size": (_Z, [_I]),
     "moe_nvfp4_grouped_gemm": (_I, [ctypes.POINTER(MoeGemmArgs), _P, _Z, _P]),
     "moe_swiglu": (_I, [_P, _I, _I, _P, _P]),
-    "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_size": (_Z, [ctypes.POINTER(MoeLayerDesc)]),
     "moe_nvfp4_forward": (_I, [ctypes.POINTER(MoeLayerDesc), _P, _P, _P, _P, _P, _Z, _P]),
     "moe_get_device_status": (_I, [_P, _P]),
     "moe_set_stage_events": (_I, [ctypes.POINTER(ctypes.c_void_p), _I]),
     "moe_kernel_launches": (ctypes.c_ulonglong, []),
     "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_debug_set": (_I, [_I, ctypes.c_longlong]),
 }
 
 MOE_STAGE_COUNT = 8
@@ -165,6 +169,10 @@ def moe_nvfp4_quantize_static(x, rows, K, gs, q, sf, stream=None):
            "moe_nvfp4_quantize_static")
 
 
+def moe_mxfp4_quantize(x, rows, K, q, sf, stream=None):
+    _check(lib().moe_mxfp4_quantize(_ptr(x), rows, K, _ptr(q), _ptr(sf), _stream(stream)), "moe_mxfp4_quantize")
+
+
 def moe_import_global_scale(stored, fmt):
     """A checkpoint's stored global scale -> the quant-convention gs (host only)."""
     out = ctypes.c_float(0.0)
@@ -182,10 +190,13 @@ def moe_prepare_size(N, K, mode, gate_up):
 
 
 def moe_nvfp4_prepare_weights(codes, sf, gs, N, K, mode, gate_up, out, stream=None):
-    """``gs`` is a sequence of host floats (one, or gate and up)."""
-    arr = (ctypes.c_float * len(gs))(*[float(v) for v in gs])
-    _check(lib().moe_nvfp4_prepare_weights(_ptr(codes), _ptr(sf), ctypes.cast(arr, ctypes.c_void_p), N, K,
-                                           mode, gate_up, _ptr(out), _stream(stream)),
+    """``gs`` is a sequence of host floats (one, or gate and up); None for MXFP4."""
+    gp = None
+    if gs is not None:
+        arr = (ctypes.c_float * len(gs))(*[float(v) for v in gs])
+        gp = ctypes.cast(arr, ctypes.c_void_p)
+    _check(lib().moe_nvfp4_prepare_weights(_ptr(codes), _ptr(sf), gp, N, K, mode, gate_up, _ptr(out),
+                                           _stream(stream)),
            "moe_nvfp4_prepare_weights")
 
 
@@ -203,8 +214,8 @@ def moe_swiglu(gu, rows, I, h, stream=None):
     _check(lib().moe_swiglu(_ptr(gu), rows, I, _ptr(h), _stream(stream)), "moe_swiglu")
 
 
-def moe_combine(y, inv_perm, topk_w, y_shared_rows, T, k, H, out, stream=None):
-    _check(lib().moe_combine(_ptr(y), _ptr(inv_perm), _ptr(topk_w), int(y_shared_rows), T, k, H, _ptr(out),
+def moe_combine(y, inv_perm, topk_w, y_shared, T, k, H, out, stream=None):
+    _check(lib().moe_combine(_ptr(y), _ptr(inv_perm), _ptr(topk_w), _ptr(y_shared), T, k, H, _ptr(out),
                              _stream(stream)),
            "moe_combine")
 
@@ -243,3 +254,8 @@ def moe_permute_noalloc(topk_ids, T, k, E, counts, offsets, perm, inv_perm, devi
     _check(lib().moe_permute_noalloc(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm),
                                      _ptr(inv_perm), _ptr(device_status), _stream(stream)),
            "moe_permute_noalloc")
+
+
+def moe_debug_set(key, value):
+    """Test hook (process-wide): see MOE_DEBUG_* in include/moe_nvfp4.h."""
+    _check(lib().moe_debug_set(int(key), int(value)), "moe_debug_set")

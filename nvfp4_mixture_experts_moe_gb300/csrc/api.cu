@@ -15,6 +15,15 @@
 namespace moe {
 
 static thread_local char g_last_cuda_error[256] = "no CUDA error";
+constexpr long long kDefaultWaitLimit = 4ll * 1000 * 1000 * 1000;
+static std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+static std::atomic<int> g_extra_arrivals{0};
+static std::atomic<int> g_fused_disabled{0};
+
+
+long long debug_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+int debug_extra_arrivals() { return g_extra_arrivals.load(std::memory_order_relaxed); }
+bool debug_decode_fused_disabled() { return g_fused_disabled.load(std::memory_order_relaxed) != 0; }
 static std::atomic<unsigned long long> g_launches{0};
 static thread_local cudaEvent_t g_stage_events[MOE_STAGE_COUNT];
 static thread_local bool g_stage_events_set = false;
@@ -84,7 +93,8 @@ struct ForwardWs {
   float* row_weight;
   void* perm_scratch;
   uint16_t* h;        // [rows, I]
-  uint16_t* y;        // [rows, H]
+  uint16_t* y;        // [T*k, H] routed rows of GEMM 2, bf16
+  float* ys;          // [T, H] the shared expert's rows of GEMM 2, fp32 (null without one)
   uint16_t* xf;       // W4A16, T above the small-group limit: f16 copy of x [T, H]
   float* xmul;        // [T]
   uint16_t* hf;       // f16 copy of h [rows, I]
@@ -96,8 +106,19 @@ struct ForwardWs {
   uint8_t* hsf;       // W4A4: [tiles, I/256, 2048]
   int tiles;          // W4A4: bound on the 128-row tiles of all groups
   float* hgs;
+  int* fused_counters;      // decode micro path: gu_done [E+1], cmb_cnt [T * H/16], hmax [rows]
+  size_t fused_counter_ints;
   size_t bytes;
 };
+
+// Experts this forward computes (expert parallelism: a contiguous shard).
+static int local_experts(const moe_layer_desc& L) { return L.local_experts > 0 ? L.local_experts : L.E; }
+
+// The single-kernel decode path applies to this layer.
+static bool use_decode_fused(const moe_layer_desc& L) {
+  return L.mode == MOE_W4A16 && decode_fused_supported(L.T, L.H, L.I, local_experts(L), L.k) &&
+         local_experts(L) == L.E;
+}
 
 static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
   const size_t P = (size_t)L.T * L.k;
@@ -118,7 +139,8 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
   f.row_weight = c.take<float>(P + L.T);
   f.perm_scratch = c.take<uint8_t>(permute_scratch_bytes(L.T, L.k, L.E));
   f.h = c.take<uint16_t>(rows * L.I);
-  f.y = c.take<uint16_t>(rows * L.H);
+  f.y = c.take<uint16_t>(P * L.H);
+  f.ys = shared ? c.take<float>(shared * L.H) : nullptr;
   if (L.mode == MOE_W4A16 && L.T > kSmallGroupRows) {
     f.xf = c.take<uint16_t>(rows * L.H);  // x rows in group order
     f.xmul = c.take<float>(rows);
@@ -128,18 +150,26 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
     f.xf = f.hf = nullptr;
     f.xmul = f.hmul = nullptr;
   }
-  if (L.mode == MOE_W4A4) {
+  if (L.mode == MOE_W4A4 || L.mode == MOE_MXFP4) {
+    const size_t sf_stage = L.mode == MOE_MXFP4 ? 1024 : 2048;  // scale-atom bytes per (tile, 256-wide K stage)
     f.tiles = (int)(rows / 128) + L.E + 1;  // sum over groups of ceil(rows_g / 128)
     f.xq = c.take<uint8_t>(rows * L.H / 2);
-    f.xsf = c.take<uint8_t>((size_t)f.tiles * (L.H / 256) * 2048);
+    f.xsf = c.take<uint8_t>((size_t)f.tiles * (L.H / 256) * sf_stage);
     f.xgs = c.take<float>(1);
     f.hq = c.take<uint8_t>(rows * L.I / 2);
-    f.hsf = c.take<uint8_t>((size_t)f.tiles * (L.I / 256) * 2048);
+    f.hsf = c.take<uint8_t>((size_t)f.tiles * (L.I / 256) * sf_stage);
     f.hgs = c.take<float>(1);
   } else {
     f.xq = f.xsf = f.hq = f.hsf = nullptr;
     f.xgs = f.hgs = nullptr;
     f.tiles = 0;
+  }
+  if (use_decode_fused(L)) {
+    f.fused_counter_ints = (size_t)(L.E + 1) + (size_t)L.T * (L.H / 16) + rows;
+    f.fused_counters = c.take<int>(f.fused_counter_ints);
+  } else {
+    f.fused_counters = nullptr;
+    f.fused_counter_ints = 0;
   }
   f.bytes = c.off;
   return f;
@@ -148,16 +178,17 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
 static size_t prep_size(int N, int K, moe_mode mode, int gate_up) {
   (void)gate_up;
   if (mode == MOE_W4A16) return sizeof(PrepHeader) + w4a16_bytes(N, K);
+  if (mode == MOE_MXFP4) return sizeof(PrepHeader) + (size_t)N * K / 2 + (size_t)N * K / 32;
   return sizeof(PrepHeader) + (size_t)N * K / 2 + prepare_w4a4_sf_bytes(N, K);
 }
 
 static moe_status validate_layer(const moe_layer_desc* L) {
   if (!L) return MOE_ERR_INVALID_ARG;
   if (L->T < 0 || L->H <= 0 || L->I <= 0 || L->E < 1 || L->k < 1) return MOE_ERR_INVALID_ARG;
-  if (L->mode != MOE_W4A16 && L->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (L->mode != MOE_W4A16 && L->mode != MOE_W4A4 && L->mode != MOE_MXFP4) return MOE_ERR_INVALID_ARG;
   if (L->E > 1024 || L->k > 32 || L->k > L->E) return MOE_ERR_UNSUPPORTED;
   if (L->H % 128 || L->I % 64) return MOE_ERR_UNSUPPORTED;
-  if (L->mode == MOE_W4A4 && (L->H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
+  if (L->mode != MOE_W4A16 && (L->H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
   if (L->w13 == nullptr || L->w2 == nullptr) return MOE_ERR_INVALID_ARG;
   if ((L->w13_shared == nullptr) != (L->w2_shared == nullptr)) return MOE_ERR_INVALID_ARG;
   if (L->w13_shared && L->I_shared != L->I) return MOE_ERR_UNSUPPORTED;
@@ -165,10 +196,13 @@ static moe_status validate_layer(const moe_layer_desc* L) {
   if (L->w13_shared && (!aligned(L->w13_shared, kAlign) || !aligned(L->w2_shared, kAlign)))
     return MOE_ERR_INVALID_ARG;
   if ((long long)L->T * L->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  if (L->local_experts < 0 || L->expert_offset < 0) return MOE_ERR_INVALID_ARG;
+  if (L->local_experts == 0 && L->expert_offset != 0) return MOE_ERR_INVALID_ARG;
+  if ((long long)L->expert_offset + L->local_experts > L->E) return MOE_ERR_INVALID_ARG;
   if (L->w_router && !aligned(L->w_router, 16)) return MOE_ERR_INVALID_ARG;
   const float sx = L->x_global_scale, sh = L->h_global_scale;
   if (!(sx >= 0.0f) || !(sh >= 0.0f) || !std::isfinite(sx) || !std::isfinite(sh)) return MOE_ERR_INVALID_ARG;
-  if (L->mode == MOE_W4A16 && (sx != 0.0f || sh != 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (L->mode != MOE_W4A4 && (sx != 0.0f || sh != 0.0f)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -267,6 +301,15 @@ moe_status moe_nvfp4_quantize_static(const uint16_t* x, int rows, int K, float g
   return launch_quantize_bf16(x, rows, K, nullptr, q, sf, nullptr, gs, (cudaStream_t)stream);
 }
 
+moe_status moe_mxfp4_quantize(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t* sf, moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !sf || !aligned(x, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_quantize_mx(x, rows, K, q, sf, (cudaStream_t)stream);
+}
+
 moe_status moe_import_global_scale(float stored, moe_scale_format format, float* gs_out) {
   if (!gs_out) return MOE_ERR_INVALID_ARG;
   if (!(stored > 0.0f) || !std::isfinite(stored)) return MOE_ERR_INVALID_ARG;
@@ -314,12 +357,13 @@ static __device__ int g_prepare_flag;
 
 moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf, const float* gs, int N, int K,
                                      moe_mode mode, int gate_up, void* out, moe_stream_t stream) {
-  if (!codes || !sf || !gs || !out) return MOE_ERR_INVALID_ARG;
-  if (mode != MOE_W4A16 && mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (!codes || !sf || !out || (mode != MOE_MXFP4 && !gs)) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_W4A16 && mode != MOE_W4A4 && mode != MOE_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (mode == MOE_MXFP4 && K % 256) return MOE_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0 || K % 64 || N % 128) return MOE_ERR_INVALID_ARG;
   if (gate_up && (N / 2) % 64) return MOE_ERR_INVALID_ARG;
   if (!aligned(out, kAlign)) return MOE_ERR_INVALID_ARG;
-  const int ngs = gate_up ? 2 : 1;
+  const int ngs = mode == MOE_MXFP4 ? 0 : (gate_up ? 2 : 1);  // MXFP4 has no global scale
   for (int i = 0; i < ngs; ++i)
     if (!(gs[i] > 0.0f) || !std::isfinite(gs[i])) return MOE_ERR_INVALID_ARG;
   moe_status st = check_device();
@@ -332,8 +376,8 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf, co
   h.gate_up = gate_up;
   h.N = N;
   h.K = K;
-  h.alpha[0] = 1.0f / gs[0];
-  h.alpha[1] = gate_up ? 1.0f / gs[1] : 0.0f;
+  h.alpha[0] = mode == MOE_MXFP4 ? 1.0f : 1.0f / gs[0];
+  h.alpha[1] = gate_up ? (mode == MOE_MXFP4 ? 1.0f : 1.0f / gs[1]) : 0.0f;
   uint8_t* o = static_cast<uint8_t*>(out);
   st = cuda_ok(cudaMemcpyAsync(o, &h, sizeof(h), cudaMemcpyHostToDevice, s));
   if (st != MOE_OK) return st;
@@ -346,7 +390,7 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf, co
   if (mode == MOE_W4A16)
     st = launch_prepare_w4a16(codes, sf, N, K, gate_up, data, flag, s);
   else
-    st = launch_prepare_w4a4(codes, sf, N, K, gate_up, data, data + (size_t)N * K / 2, flag, s);
+    st = launch_prepare_w4a4(codes, sf, N, K, gate_up, data, data + (size_t)N * K / 2, flag, s, mode == MOE_MXFP4);
   if (st != MOE_OK) return st;
   int hflag = 0;
   st = cuda_ok(cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -374,6 +418,7 @@ static moe_status run_gemm(const GemmPlan& p, long long max_group_rows, cudaStre
 
 moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!a) return MOE_ERR_INVALID_ARG;
+  if (a->mode == MOE_MXFP4) return MOE_ERR_UNSUPPORTED;  // the fused forward runs MXFP4 layers
   if (a->mode != MOE_W4A16 && a->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
   if (a->num_groups < 0) return MOE_ERR_INVALID_ARG;
   if (a->num_groups == 0) return MOE_OK;
@@ -390,6 +435,7 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   moe_status st = check_device();
   if (st != MOE_OK) return st;
   GemmPlan p;
+  std::memset(&p, 0, sizeof(p));
   p.mode = a->mode;
   p.gate_up = a->gate_up;
   p.num_groups = a->num_groups;
@@ -424,15 +470,15 @@ moe_status moe_swiglu(const float* gu, int rows, int I, uint16_t* h, moe_stream_
   return launch_swiglu(gu, rows, I, h, (cudaStream_t)stream);
 }
 
-moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int y_shared_rows,
+moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, const float* y_shared,
                        int T, int k, int H, uint16_t* out, moe_stream_t stream) {
   if (T < 0 || k < 1 || H <= 0 || H % 8) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!y || !inv_perm || !out) return MOE_ERR_INVALID_ARG;
-  if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(out, 16) || (y_shared && !aligned(y_shared, 16))) return MOE_ERR_INVALID_ARG;
   moe_status st = check_device();
   if (st != MOE_OK) return st;
-  return launch_combine(y, inv_perm, topk_w, y_shared_rows ? 1 : 0, T, k, H, out, (cudaStream_t)stream);
+  return launch_combine(y, inv_perm, topk_w, y_shared, T, k, H, out, (cudaStream_t)stream);
 }
 
 size_t moe_workspace_size(const moe_layer_desc* L) {
@@ -454,11 +500,13 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   st = check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const bool fp4 = L->mode == MOE_W4A4;
+  const bool mx = L->mode == MOE_MXFP4;
+  const bool fp4 = L->mode == MOE_W4A4 || mx;   // FP4 activations, block-scaled FP4 MMA
   const int T = L->T, k = L->k, E = L->E, H = L->H, I = L->I;
   const int P = T * k;
   const bool has_shared = L->w13_shared != nullptr;
   const int rows = P + (has_shared ? T : 0);
+  const int EL = local_experts(*L), lo = L->expert_offset;   // this forward's expert shard
   int32_t* ids = topk_ids_out ? topk_ids_out : f.ids;
   struct StageGuard {  // the events apply to one forward call only
     ~StageGuard() { g_stage_events_set = false; }
@@ -473,31 +521,67 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     if (st != MOE_OK) return st;
     logits = f.logits;
   }
+  if (f.fused_counters != nullptr && !debug_decode_fused_disabled()) {
+    // decode micro path: the whole layer in one cooperative kernel
+    st = cuda_ok(cudaMemsetAsync(f.fused_counters, 0, f.fused_counter_ints * sizeof(int), s));
+    if (st != MOE_OK) return st;
+    stage_mark(0, s);  // recorded again: stage 0 -> 1 is the fused kernel alone
+    DecodeFusedPlan q;
+    q.logits = logits;
+    q.x = x;
+    q.w13 = static_cast<const uint8_t*>(L->w13);
+    q.s13 = prep_size(2 * I, H, L->mode, 1);
+    q.w13_shared = static_cast<const uint8_t*>(L->w13_shared);
+    q.w2 = static_cast<const uint8_t*>(L->w2);
+    q.s2 = prep_size(H, I, L->mode, 0);
+    q.w2_shared = static_cast<const uint8_t*>(L->w2_shared);
+    q.T = T;
+    q.H = H;
+    q.I = I;
+    q.E = E;
+    q.k = k;
+    q.out = out;
+    q.topk_ids_out = topk_ids_out;
+    q.h = f.h;
+    q.y = f.y;
+    q.y_shared = f.ys;
+    q.gu_done = f.fused_counters;
+    q.cmb_cnt = f.fused_counters + (E + 1);
+    q.hmax = reinterpret_cast<unsigned*>(f.fused_counters + (E + 1) + (size_t)T * (H / 16));
+    q.status = &f.hdr->status;
+    q.wait_limit = debug_wait_limit();
+    q.extra_arrivals = debug_extra_arrivals();
+    st = launch_decode_fused(q, s);
+    if (st != MOE_OK) return st;
+    for (int i = 1; i < MOE_STAGE_COUNT; ++i) stage_mark(i, s);
+    return MOE_OK;
+  }
   if (P <= kFusedRoutePermuteMax) {  // route + permute in one CTA
     st = launch_route_permute_small(logits, T, E, k, ids, f.w, f.counts, f.offsets, f.perm, f.inv_perm,
-                                    &f.hdr->status, f.row_token, f.row_weight, f.gofs, s);
+                                    &f.hdr->status, f.row_token, f.row_weight, f.gofs, s, lo, EL);
     if (st != MOE_OK) return st;
     stage_mark(1, s);
   } else {
     st = launch_route_topk(logits, T, E, k, ids, f.w, s);
     if (st != MOE_OK) return st;
     stage_mark(1, s);
-    st = launch_permute(ids, T, k, E, f.counts, f.offsets, f.perm, f.inv_perm, &f.hdr->status, f.perm_scratch,
-                        f.row_token, f.row_weight, f.w, f.gofs, s, pdl);
+    st = launch_permute(ids, T, k, EL, f.counts, f.offsets, f.perm, f.inv_perm, &f.hdr->status, f.perm_scratch,
+                        f.row_token, f.row_weight, f.w, f.gofs, s, pdl, lo, E);
     if (st != MOE_OK) return st;
   }
   stage_mark(2, s);
   const float x_static = L->x_global_scale, h_static = L->h_global_scale;
-  if (fp4) {  // per-tensor quantisation of x (W4A4): dynamic amax, or a static scale
+  const size_t sf_stage = mx ? 1024 : 2048;  // scale-atom bytes per (tile, 256-wide K stage)
+  if (fp4) {  // x -> FP4 in group order: W4A4 with a per-tensor scale (dynamic amax or static); MXFP4 per 32
     st = cuda_ok(cudaMemsetAsync(&f.hdr->amax[0], 0, 2 * sizeof(float), s));
     if (st != MOE_OK) return st;
-    if (x_static == 0.0f) {
+    if (!mx && x_static == 0.0f) {
       st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s, pdl);
       if (st != MOE_OK) return st;
     }
-    st = launch_quantize_tiles(x, T, H, f.inv_perm, k, has_shared ? P : -1, f.gofs, E + (has_shared ? 1 : 0),
-                               &f.hdr->amax[0], f.xq, f.xsf, (size_t)f.tiles * (H / 256) * 2048, f.xgs,
-                               x_static, s, pdl);
+    st = launch_quantize_tiles(x, T, H, f.inv_perm, k, has_shared ? 1 : -1, f.gofs, EL + (has_shared ? 1 : 0),
+                               &f.hdr->amax[0], f.xq, f.xsf, (size_t)f.tiles * (H / 256) * sf_stage, f.xgs,
+                               x_static, s, pdl, mx);
     if (st != MOE_OK) return st;
   }
   if (f.xf) {  // f16 copy of x, rows in group order, for the large-group tensor-core GEMM
@@ -506,7 +590,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   }
   stage_mark(3, s);
 
-  const int G = E + (has_shared ? 1 : 0);
+  const int G = EL + (has_shared ? 1 : 0);
   GemmPlan g1;
   std::memset(&g1, 0, sizeof(g1));
   g1.mode = L->mode;
@@ -523,7 +607,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g1.a_gs = fp4 ? f.xgs : nullptr;
   g1.a_row_index = f.row_token;
   g1.out = f.h;
-  g1.out_amax = (fp4 && h_static == 0.0f) ? &f.hdr->amax[1] : nullptr;
+  g1.out_amax = (fp4 && !mx && h_static == 0.0f) ? &f.hdr->amax[1] : nullptr;
   g1.a_f16 = f.xf;
   g1.a_mul = f.xmul;
   g1.a_rows = rows;
@@ -534,9 +618,9 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   st = fp4 ? launch_gemm_tc_fp4(g1, s) : run_gemm(g1, T, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
-  if (fp4) {  // h -> NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue)
+  if (fp4) {  // h -> FP4: NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue); MXFP4 per 32
     st = launch_quantize_tiles(f.h, rows, I, nullptr, 0, -1, f.gofs, G, &f.hdr->amax[1], f.hq, f.hsf,
-                               (size_t)f.tiles * (I / 256) * 2048, f.hgs, h_static, s, pdl);
+                               (size_t)f.tiles * (I / 256) * sf_stage, f.hgs, h_static, s, pdl, mx);
     if (st != MOE_OK) return st;
   } else if (f.hf) {
     st = launch_rows_to_f16(f.h, nullptr, rows, I, f.hf, f.hmul, s, pdl);
@@ -561,10 +645,11 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   g2.a_row_index = nullptr;
   g2.row_scale = f.row_weight;
   g2.out = f.y;
+  g2.out_last_f32 = f.ys;  // the shared expert's rows stay fp32 until the combine
   st = fp4 ? launch_gemm_tc_fp4(g2, s) : run_gemm(g2, T, s);
   if (st != MOE_OK) return st;
   stage_mark(6, s);
-  st = launch_combine(f.y, f.inv_perm, nullptr, has_shared ? 1 : 0, T, k, H, out, s, pdl);
+  st = launch_combine(f.y, f.inv_perm, nullptr, f.ys, T, k, H, out, s, pdl);
   if (st != MOE_OK) return st;
   stage_mark(7, s);
   return MOE_OK;
@@ -585,6 +670,22 @@ moe_status moe_set_stage_events(void* const* events, int n) {
 }
 
 unsigned long long moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_debug_set(int key, long long value) {
+  switch (key) {
+    case MOE_DEBUG_WAIT_LIMIT:
+      g_wait_limit.store(value > 0 ? value : kDefaultWaitLimit, std::memory_order_relaxed);
+      return MOE_OK;
+    case MOE_DEBUG_EXTRA_ARRIVALS:
+      g_extra_arrivals.store(value > 0 ? (int)std::min<long long>(value, 1 << 20) : 0, std::memory_order_relaxed);
+      return MOE_OK;
+    case MOE_DEBUG_DISABLE_DECODE_FUSED:
+      g_fused_disabled.store(value != 0 ? 1 : 0, std::memory_order_relaxed);
+      return MOE_OK;
+
+  }
+  return MOE_ERR_INVALID_ARG;
+}
 
 moe_status moe_get_device_status(void* ws, moe_stream_t stream) {
   if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;

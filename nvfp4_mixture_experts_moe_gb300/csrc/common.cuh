@@ -54,6 +54,18 @@ constexpr int kW16SfOff = 4096;   // scale blocks within a chunk
 __host__ __device__ inline size_t w4a16_bytes(int N, int K) { return (size_t)N * K / 2 + (size_t)N * K / 16; }
 __host__ __device__ inline size_t w4a16_chunk(int mt, int kb, int KB) { return ((size_t)mt * KB + kb) * kW16Chunk; }
 
+// 64-wide K blocks per streamed stage of the small-group (decode) GEMMs: the
+// largest count <= 8 that gives every 128-row tile an even number of stages
+// (KB = K / 64 blocks per tile). The two halves of the MMA warps take
+// alternate stages, so with an even count every tile splits its K blocks
+// between the halves the same way wherever it falls in a CTA's sequence,
+// and every kernel that runs this loop sums in the same order.
+__host__ __device__ inline int w16_stage_kb(int KB) {
+  for (int kb = 8; kb > 1; --kb)
+    if (((KB + kb - 1) / kb) % 2 == 0) return kb;
+  return 1;
+}
+
 // ---------------------------------------------------------------------------
 // Small device helpers.
 __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
@@ -104,6 +116,12 @@ __device__ __forceinline__ uint2 ldg_stream2(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
+
+// A bf16 magnitude bit pattern with the NaN patterns (above 0x7f80, the
+// infinity) mapped to 0. NaN activations are outside the contract; this keeps
+// them from becoming a tensor's or a row's maximum (an infinite amax would
+// make a global scale 0 and zero every code).
+__device__ __forceinline__ uint32_t finite_mag(uint32_t mag_bits) { return mag_bits > 0x7f80u ? 0u : mag_bits; }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);

@@ -1,0 +1,691 @@
+// The whole layer in one kernel for decode batches (W4A16, up to 8 tokens):
+// route, permute, gate/up GEMM + SwiGLU, down GEMM + routing weight and the
+// combine, in one persistent launch ("micro path").
+//
+// "Serving Solar Open 2 on DGX Spark", "The fix" (a separate micro path for
+// small decode batches); "vLLM on the NVIDIA DGX Spark: A Complete Technical
+// Guide", section 4.3 (dispatch, both expert GEMMs, SwiGLU and the top-k
+// weight reduction fused into one kernel), section 5 (weight-only NVFP4:
+// 4-bit weights dequantised to 16-bit inside the GEMM) and section 6.1
+// (alpha = 1/gs).
+//
+// At a few tokens the layer is bound by the bytes of the touched experts'
+// weights; everything else is latency. One CTA per SM (cooperative launch, so
+// all CTAs are resident and may wait on one another with bounded spins):
+//
+// * Routing and the permutation are computed by every CTA in shared memory
+//   (a few hundred logits per token); the x rows are converted once per CTA to
+//   f16 with a power-of-two row scale and stay resident for the gate/up phase.
+// * Work items are (active expert group, 128-row weight tile): gate/up items
+//   first, then down items, taken by the CTAs in a strided order (gate/up
+//   items ascending, down items descending over the CTAs, so the CTAs with
+//   one gate/up item more get one down item fewer).
+// * One producer warp streams every item's weight tiles (stages of up to 8
+//   64-wide K blocks, 36 KB, in a ring of 4) with bulk copies from the
+//   gate/up phase straight into the down phase, so the down weights are
+//   already in flight when the gate/up items end.
+// * Sixteen MMA warps (8 row blocks x 2 halves that take alternate stages)
+//   turn the e2m1 codes into f16 with the hardware conversion, multiply in
+//   the E4M3 block scales and run mma.sync m16n8k16 with the group's rows as
+//   N; the second half hands its partial sums to the first at the end of an
+//   item. Stage sizes give every item an even number of stages, so the
+//   arithmetic (and the result, bit for bit) is that of the multi-kernel
+//   path's decode GEMM.
+// * Gate/up epilogue: SwiGLU, h stored bf16 in the workspace with a running
+//   per-row max |h|. Down epilogue: y = h W2^T * alpha * routing weight,
+//   stored bf16 (the shared expert's rows fp32). Neither waits on a global
+//   fence: the MMA warps hand each finished item to a signal warp through an
+//   mbarrier.
+// * The signal warp counts a gate/up item in gu_done[group] (one release at
+//   gpu scope, cumulative over the MMA warps' stores); a helper warp stages
+//   a down item's h rows (as f16 with a row scale) once all gate/up tiles of
+//   the group are counted (acquire). For a down item the signal warp counts
+//   each (token, 16 output columns) contribution; the one that completes the
+//   k + 1 of a token sums the token's rows in the fixed order j = 0..k-1,
+//   then the shared row, in fp32 and writes the bf16 output. The sum order
+//   never depends on which CTA does it: the result is deterministic.
+//
+// Every wait (mbarriers, the gate/up counters) is bounded; on a timeout the
+// kernel records MOE_ERR_TIMEOUT, lets its bulk copies land and exits.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "route.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int kMaxT = kDecodeFusedMaxT;           // tokens (each group has at most this many rows)
+constexpr int kMaxK = 32;
+constexpr int kBlockWarps = 8;                     // one per 16-row block of a 128-row tile
+constexpr int kHalves = 2;                         // halves of a stage's K blocks
+constexpr int kMmaWarps = kBlockWarps * kHalves;
+constexpr int kProducerWarp = kMmaWarps;
+constexpr int kHelperWarp = kMmaWarps + 1;
+constexpr int kSignalWarp = kMmaWarps + 2;
+constexpr int kThreads = (kMmaWarps + 3) * 32;
+constexpr int kTile = 128;
+constexpr int kMaxSlots = 8;
+constexpr int kStageBytes = 8 * kW16Chunk;         // ring slot: up to 8 K blocks (36 KB)
+constexpr int kHSlots = 2;                         // staged h row sets (down items)
+constexpr int kMaxRows = kMaxT * kMaxK + kMaxT;    // routed pairs + shared rows
+constexpr int kMaxGroups = kMaxT * kMaxK + 1;      // active groups: at most one per pair, + shared
+
+struct Args {
+  const float* logits;
+  const uint16_t* x;
+  const uint8_t* w13;
+  size_t s13;
+  const uint8_t* w13_shared;
+  const uint8_t* w2;
+  size_t s2;
+  const uint8_t* w2_shared;
+  int T, H, I, E, k, has_shared;
+  uint16_t* out;
+  int32_t* topk_ids_out;
+  uint16_t* h;          // [rows, I] bf16
+  uint16_t* y;          // [T*k, H] routed rows, bf16
+  float* y_shared;      // [T, H] the shared expert's rows, fp32
+  int* gu_done;         // [groups] (zeroed by the caller)
+  int* cmb_cnt;         // [T][H/16] (zeroed)
+  unsigned* hmax;       // [rows] bf16 magnitude bits of max |h| (zeroed)
+  int* status;
+  int slots;
+  long long wait_limit;
+  int extra_arrivals;   // test hook: arrivals expected per gate/up tile beyond the real ones
+};
+
+struct Smem {
+  uint64_t full[kMaxSlots];
+  uint64_t empty[kMaxSlots];
+  uint64_t hfull[kHSlots];
+  uint64_t hempty[kHSlots];
+  uint64_t xfree;                // every MMA warp is done with the resident x rows
+  uint64_t done[2];              // an item's epilogue stores are issued (the 8 first-half warps)
+  uint64_t done_free[2];         // the signal warp has taken that item over
+  uint64_t red_full[kBlockWarps];
+  uint64_t red_empty[kBlockWarps];
+  int abort;
+  int A;                         // active groups
+  int32_t ids[kMaxT * kMaxK];
+  float w[kMaxT * kMaxK];
+  int32_t inv[kMaxT * kMaxK];    // pair -> grouped row
+  int32_t row_tok[kMaxRows];
+  float row_w[kMaxRows];
+  int32_t grp_e[kMaxGroups];     // expert of active group a (E = shared)
+  int32_t grp_r0[kMaxGroups];
+  int32_t grp_n[kMaxGroups];
+  float xmul[kMaxT];
+  float hmul[kHSlots][kMaxT];
+  float4 red[kBlockWarps][32];
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Power-of-two row scale from a row's largest bf16 magnitude (bit pattern m):
+// 2^sh brings the maximum into [2^14, 2^15), where every bf16 value down to
+// 2^-24 of the maximum is exact in f16. Returns sh.
+__device__ __forceinline__ int row_shift(uint32_t m) {
+  const int e = (int)(m >> 7);
+  int sh = (m == 0) ? 0 : 141 - max(e, 1);
+  return max(-113, min(sh, 126));
+}
+
+// bf16 row [K] (global) -> f16 row [K] (shared) times 2^sh.
+__device__ __forceinline__ void stage_row(const uint16_t* src, uint16_t* dst, int K, int sh, int lane, bool l2) {
+  const float up = __int_as_float((127 + sh) << 23);
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = l2 ? __ldcg(s + i) : __ldg(s + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 hh = __floats2half2_rn(__uint_as_float(w[q] << 16) * up, __uint_as_float(w[q] & 0xffff0000u) * up);
+      o[q] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Bounded wait for *ctr >= target (another CTA's release increments), or abort.
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatile int* abort, long long limit) {
+  const long long t0 = clock64();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+__device__ __forceinline__ void release_add(int* ctr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int acq_rel_add(int* ctr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(v) : "memory");
+  return old;
+}
+
+// One stage of one item: this warp's K blocks (kb % 2 == half) of its 16-row
+// block, four accumulator chains (one per k16 step of a block).
+__device__ __forceinline__ void mma_stage(const uint8_t* sd, int nkb, int kb_first, int kb_step, int blk, int lane,
+                                          uint32_t xa0, float (&acc4)[4][4]) {
+  const int g8 = lane >> 2;
+  const uint8_t* my_data = sd + blk * 512 + lane * 16;
+  const uint8_t* my_sf = sd + kW16SfOff + blk * 64 + g8 * 8;
+#pragma unroll 2
+  for (int kb = kb_first; kb < nkb; kb += kb_step) {
+    const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * kW16Chunk);
+    const uint2 sq = *reinterpret_cast<const uint2*>(my_sf + kb * kW16Chunk);
+    const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+    uint32_t bf[8];
+    const uint32_t xa = xa0 + (uint32_t)(kb * 64) * 2;
+    ldsm_x4(xa, bf[0], bf[1], bf[2], bf[3]);
+    ldsm_x4(xa + 64, bf[4], bf[5], bf[6], bf[7]);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t a[4];
+      cvt_e2m1x8_f16(wv[s], a);
+      const uint32_t pr = cvt_e4m3x2_f16x2(((s < 2 ? sq.x : sq.y) >> (16 * (s & 1))) & 0xffffu);
+      const __half2 sp = *reinterpret_cast<const __half2*>(&pr);
+      const __half2 sg = __low2half2(sp), s8 = __high2half2(sp);
+      __half2* ah = reinterpret_cast<__half2*>(a);
+      ah[0] = __hmul2(ah[0], sg);
+      ah[1] = __hmul2(ah[1], s8);
+      ah[2] = __hmul2(ah[2], sg);
+      ah[3] = __hmul2(ah[3], s8);
+      mma_f16_16816(acc4[s], a, bf[2 * s], bf[2 * s + 1]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const int T = p.T, H = p.H, I = p.I, E = p.E, k = p.k;
+  const int S = p.slots;
+  const int P = T * k;
+  const int KB1 = H / 64, KB2 = I / 64;
+  const int MT1 = (2 * I) / kTile, MT2 = H / kTile;
+  const int KBS1 = w16_stage_kb(KB1), KBS2 = w16_stage_kb(KB2);   // K blocks per stage of each phase
+  const int NST1 = (KB1 + KBS1 - 1) / KBS1, NST2 = (KB2 + KBS2 - 1) / KBS2;
+  const int xs_stride = H + 8;    // f16 per resident x row (16-byte pad: conflict-free ldmatrix)
+  const int hs_stride = I + 8;
+  uint8_t* ring = smem_raw;
+  uint16_t* act = reinterpret_cast<uint16_t*>(ring + (size_t)S * kStageBytes);
+  const size_t act_elems = max((size_t)T * xs_stride, (size_t)kHSlots * kMaxT * hs_stride);
+  Smem* sm = reinterpret_cast<Smem*>(act + act_elems);
+  int* cnt = reinterpret_cast<int*>(sm + 1);   // [E] expert histogram, then offsets
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nC = gridDim.x, b = blockIdx.x;
+  volatile int* abort = &sm->abort;
+  const long long limit = p.wait_limit;
+
+  // ------------------------------------------------------------ phase 0
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&sm->full[i], 1);
+      mbar_init(&sm->empty[i], kBlockWarps);  // the half that reads the stage
+    }
+    for (int i = 0; i < kHSlots; ++i) {
+      mbar_init(&sm->hfull[i], 1);
+      mbar_init(&sm->hempty[i], kMmaWarps);
+    }
+    for (int i = 0; i < kBlockWarps; ++i) {
+      mbar_init(&sm->red_full[i], 1);
+      mbar_init(&sm->red_empty[i], 1);
+    }
+    mbar_init(&sm->xfree, kMmaWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm->done[i], kBlockWarps);
+      mbar_init(&sm->done_free[i], 1);
+    }
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
+  if (warp < T) {
+    route_token<kMaxK>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
+  } else if (warp >= kBlockWarps && warp < kBlockWarps + T) {
+    // x row t -> f16 with its row scale, resident for the gate/up items
+    const int t = warp - kBlockWarps;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H);
+    uint32_t m = 0;
+    for (int i = lane; i < H / 8; i += 32) {
+      const uint4 v = __ldg(src + i);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m = max(m, max(finite_mag(wv[q] & 0x7fffu), finite_mag((wv[q] >> 16) & 0x7fffu)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const int sh = row_shift(m);
+    stage_row(p.x + (size_t)t * H, act + (size_t)t * xs_stride, H, sh, lane, false);
+    if (lane == 0) sm->xmul[t] = __int_as_float((127 - sh) << 23);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // stable counting sort of the pairs by expert, active groups in expert order
+    for (int q = lane; q < P; q += 32) atomicAdd(&cnt[sm->ids[q]], 1);
+    __syncwarp();
+    int base = 0, na = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? cnt[e] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned act_mask = __ballot_sync(0xffffffffu, c > 0);
+      if (c > 0) {
+        const int a = na + __popc(act_mask & ((1u << lane) - 1u));
+        sm->grp_e[a] = e;
+        sm->grp_r0[a] = base + incl - c;
+        // top-k picks distinct experts, so a group holds at most one row per
+        // token (<= kMaxT); the clamp keeps any input inside the staging buffers
+        sm->grp_n[a] = min(c, kMaxT);
+      }
+      if (e < E) cnt[e] = base + incl - c;   // becomes the group's cursor
+      base += __shfl_sync(0xffffffffu, incl, 31);
+      na += __popc(act_mask);
+    }
+    __syncwarp();
+    for (int q0 = 0; q0 < P; q0 += 32) {   // pairs in order: a pair's row grows with its index
+      const int q = q0 + lane;
+      const int e = q < P ? sm->ids[q] : -1 - lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int r = 0;
+      if (q < P) r = cnt[e] + rank;
+      __syncwarp();
+      if (q < P) {
+        sm->inv[q] = r;
+        sm->row_tok[r] = q / k;
+        sm->row_w[r] = sm->w[q];
+        if ((peers >> lane) == 1u) cnt[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
+    if (p.has_shared) {
+      if (lane == 0) {
+        sm->grp_e[na] = E;
+        sm->grp_r0[na] = P;
+        sm->grp_n[na] = T;
+      }
+      for (int t = lane; t < T; t += 32) {
+        sm->row_tok[P + t] = t;
+        sm->row_w[P + t] = 1.0f;
+      }
+      ++na;
+    }
+    if (lane == 0) sm->A = na;
+    if (b == 0 && p.topk_ids_out != nullptr)
+      for (int q = lane; q < P; q += 32) p.topk_ids_out[q] = sm->ids[q];
+  }
+  __syncthreads();
+  const int A = sm->A;
+  const int N1 = A * MT1, N2 = A * MT2;
+  // down items of this CTA: i = (nC - 1 - b) + m * nC
+  const int d0 = nC - 1 - b;
+
+  if (warp == kProducerWarp) {
+    // --------------------------------------------------------------- producer
+    if (lane == 0) {
+      int j = 0;
+      bool ok = true;
+      for (int ph = 0; ph < 2 && ok; ++ph) {
+        const int first = ph == 0 ? b : d0, N = ph == 0 ? N1 : N2;
+        const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
+        const int KBS = ph == 0 ? KBS1 : KBS2;
+        for (int i = first; i < N && ok; i += nC) {
+          const int a = i / MT, mt = i % MT;
+          const int e = sm->grp_e[a];
+          const uint8_t* blk = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
+                                       : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
+          const uint8_t* data = blk + sizeof(PrepHeader);
+          for (int st = 0; st < NST; ++st, ++j) {
+            const int slot = j % S;
+            if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, limit)) { ok = false; break; }
+            const int kb0 = st * KBS;
+            const uint32_t bytes = (uint32_t)(min(KBS, KB - kb0) * kW16Chunk);
+            mbar_arrive_expect_tx(&sm->full[slot], bytes);
+            bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, KB), bytes,
+                     &sm->full[slot]);
+          }
+        }
+      }
+      // copies still in flight land before the CTA's shared memory is released
+      for (int i = max(0, j - S); i < j; ++i) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&sm->full[i % S], (i / S) & 1) && clock64() - t0 < limit) {
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == kHelperWarp) {
+    // ------------------------------------- h rows of the down items -> f16
+    // (the h slots reuse the x rows' shared memory: wait until no MMA warp
+    // reads x any more)
+    int m = 0;
+    const bool xok = mbar_wait(&sm->xfree, 0, abort, limit);
+    for (int i = d0; i < N2 && xok; i += nC, ++m) {
+      const int slot = m % kHSlots;
+      if (!mbar_wait(&sm->hempty[slot], ((m / kHSlots) & 1) ^ 1, abort, limit)) break;
+      const int a = i / MT2;
+      if (!wait_counter(p.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
+      const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
+      uint16_t* dst = act + (size_t)slot * kMaxT * hs_stride;
+      for (int q = 0; q < n; ++q) {
+        const unsigned mx = __ldcg(p.hmax + r0 + q);
+        const int sh = row_shift(mx);
+        stage_row(p.h + (size_t)(r0 + q) * I, dst + (size_t)q * hs_stride, I, sh, lane, true);
+        if (lane == 0) sm->hmul[slot][q] = __int_as_float((127 - sh) << 23);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->hfull[slot]);
+    }
+    if (lane == 0 && *abort) set_status(p.status, MOE_ERR_TIMEOUT);
+    return;
+  }
+
+  if (warp == kSignalWarp) {
+    // ------------------------------------------------------------ signal
+    // Takes each finished item over from the MMA warps, so that no MMA warp
+    // ever waits on a global fence: gate/up items are counted in
+    // gu_done[group] (release, gpu scope; cumulative over the MMA warps'
+    // stores of h, which the done barrier ordered before it); down items
+    // count their (token, 16 columns) contributions, and the contribution
+    // that completes one sums the token's rows in the fixed order j = 0..k-1,
+    // then the shared row, and writes the bf16 output.
+    const int need = k + (p.has_shared ? 1 : 0);
+    int cnt_items = 0;
+    bool ok = true;
+    for (int ph = 0; ph < 2 && ok; ++ph) {
+      const int first = ph == 0 ? b : d0, N = ph == 0 ? N1 : N2;
+      const int MT = ph == 0 ? MT1 : MT2;
+      for (int i = first; i < N; i += nC, ++cnt_items) {
+        const int ds = cnt_items & 1;
+        if (!mbar_wait(&sm->done[ds], (cnt_items >> 1) & 1, abort, limit)) { ok = false; break; }
+        const int a = i / MT, mt = i % MT;
+        if (ph == 0) {
+          if (lane == 0) release_add(p.gu_done + a, 1);
+        } else {
+          const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
+          for (int base = 0; base < n * kBlockWarps; base += 32) {
+            const int idx = base + lane;           // (row, 16-column block) of this item
+            int last = 0, tok = 0, cb = 0;
+            if (idx < n * kBlockWarps) {
+              tok = sm->row_tok[r0 + idx / kBlockWarps];
+              cb = mt * kBlockWarps + idx % kBlockWarps;
+              last = acq_rel_add(p.cmb_cnt + (size_t)tok * (H / 16) + cb, 1) == need - 1;
+            }
+            unsigned todo = __ballot_sync(0xffffffffu, last);
+            __threadfence();
+            while (todo) {  // two completed (token, 16 columns) at a time, 16 lanes each
+              const int s0 = __ffs(todo) - 1;
+              todo &= todo - 1;
+              const int s1 = todo ? __ffs(todo) - 1 : -1;
+              if (s1 >= 0) todo &= todo - 1;
+              const int src = lane < 16 ? s0 : s1;
+              const int t = __shfl_sync(0xffffffffu, tok, src < 0 ? 0 : src);
+              const int c16 = __shfl_sync(0xffffffffu, cb, src < 0 ? 0 : src);
+              if (src >= 0) {
+                const int col = c16 * 16 + (lane & 15);
+                float acc = 0.0f;
+                for (int jj = 0; jj < k; ++jj)
+                  acc += bf16_bits_to_float(__ldcg(p.y + (size_t)sm->inv[t * k + jj] * H + col));
+                if (p.has_shared) acc += __ldcg(p.y_shared + (size_t)t * H + col);
+                p.out[(size_t)t * H + col] = float_to_bf16_bits(acc);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->done_free[ds]);
+      }
+    }
+    if (lane == 0 && *abort) set_status(p.status, MOE_ERR_TIMEOUT);
+    return;
+  }
+
+  // -------------------------------------------------------------- MMA warps
+  const int blk = warp % kBlockWarps, half = warp / kBlockWarps;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int lrow = lane & 7, lq = lane >> 3;
+  int j = 0, m = 0, cnt_items = 0;
+  uint32_t rphase = 0;
+  bool ok = true;
+  bool x_released = false;
+  for (int ph = 0; ph < 2 && ok; ++ph) {
+    const int first = ph == 0 ? b : d0, N = ph == 0 ? N1 : N2;
+    const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
+    const int KBS = ph == 0 ? KBS1 : KBS2;
+    if (ph == 1 && !x_released) {  // this CTA had no gate/up item
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->xfree);
+      x_released = true;
+    }
+    for (int i = first; i < N; i += nC, ++cnt_items) {
+      const int a = i / MT, mt = i % MT;
+      const int e = sm->grp_e[a], r0 = sm->grp_r0[a], n = sm->grp_n[a];
+      const int hslot = m % kHSlots;
+      // ldmatrix row of this lane: the group's row lrow (rows past the group
+      // repeat row 0; their columns are computed and dropped)
+      const int rsel = lrow < n ? lrow : 0;
+      uint32_t xa0;
+      if (ph == 0) {
+        xa0 = smem_u32(act + (size_t)sm->row_tok[r0 + rsel] * xs_stride + 8 * lq);
+      } else {
+        if (!mbar_wait(&sm->hfull[hslot], (m / kHSlots) & 1, abort, limit)) { ok = false; break; }
+        xa0 = smem_u32(act + (size_t)hslot * kMaxT * hs_stride + (size_t)rsel * hs_stride + 8 * lq);
+      }
+      float acc4[4][4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) acc4[s][0] = acc4[s][1] = acc4[s][2] = acc4[s][3] = 0.f;
+      // the two halves take alternate stages (j counts every stage of this
+      // CTA); with an even number of stages per item each half sums the same
+      // K blocks of every item
+      for (int st = 0; st < NST; ++st, ++j) {
+        if ((j & 1) != half) continue;
+        const int slot = j % S;
+        if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, limit)) { ok = false; break; }
+        const int kb0 = st * KBS;
+        mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), 0, 1, blk, lane,
+                  xa0 + (uint32_t)(kb0 * 64) * 2, acc4);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[slot]);
+      }
+      if (!ok) break;
+      float hm[2] = {1.0f, 1.0f};   // row multipliers of this lane's two token columns
+      if (ph == 0) {
+        if (i + nC >= N) {  // last gate/up item of this CTA: x is no longer read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->xfree);
+          x_released = true;
+        }
+      } else {  // the staged h rows (and their multipliers) are no longer read
+#pragma unroll
+        for (int q = 0; q < 2; ++q) hm[q] = sm->hmul[hslot][min(2 * t4 + q, kMaxT - 1)];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->hempty[hslot]);
+        ++m;
+      }
+      float acc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = (acc4[0][q] + acc4[1][q]) + (acc4[2][q] + acc4[3][q]);
+      // the second half hands its partial sums to the first, which adds them
+      if (half != 0) {
+        if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, limit)) { ok = false; break; }
+        sm->red[blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->red_full[blk]);
+        rphase ^= 1u;
+        continue;
+      }
+      if (!mbar_wait(&sm->red_full[blk], rphase, abort, limit)) { ok = false; break; }
+      {
+        const float4 o = sm->red[blk][lane];
+        acc[0] += o.x;
+        acc[1] += o.y;
+        acc[2] += o.z;
+        acc[3] += o.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->red_empty[blk]);
+      rphase ^= 1u;
+
+      const uint8_t* wb = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
+                                  : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wb);
+      const int mb = mt * kBlockWarps + blk;
+      if (ph == 0) {
+        // SwiGLU: lane pair (row g8 gate, row g8 + 8 up) of feature 8 * mb + g8
+        const int f = 8 * mb + g8;
+        uint32_t hb2[2] = {0u, 0u};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int c = 2 * t4 + q;
+          if (c < n) {
+            const float rm = sm->xmul[sm->row_tok[r0 + c]];
+            const float hv = silu(acc[q] * rm * hdr->alpha[0]) * (acc[2 + q] * rm * hdr->alpha[1]);
+            const uint16_t bits = float_to_bf16_bits(hv);
+            p.h[(size_t)(r0 + c) * I + f] = bits;
+            hb2[q] = bits & 0x7fffu;
+          }
+        }
+        // per-row max |h| over this warp's 8 features, then one atomic per row
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t v = finite_mag(hb2[q]);
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+          const int c = 2 * t4 + q;
+          if (g8 == 0 && c < n) atomicMax(p.hmax + r0 + c, v);
+        }
+      } else {
+        // y = acc * 2^-s * alpha * routing weight
+        const int col = mt * kTile + 16 * blk;   // this warp's 16 output columns
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int c = 2 * t4 + q;
+          if (c < n) {
+            const int r = r0 + c;
+            // the multi-kernel path's order of operations, so the two paths agree bit for bit
+            const float rw = sm->row_w[r];
+            const float v0 = acc[q] * hm[q] * hdr->alpha[0] * rw, v1 = acc[2 + q] * hm[q] * hdr->alpha[0] * rw;
+            if (e == E) {  // shared expert: kept fp32 for the combine
+              p.y_shared[(size_t)(r - P) * H + col + g8] = v0;
+              p.y_shared[(size_t)(r - P) * H + col + g8 + 8] = v1;
+            } else {
+              p.y[(size_t)r * H + col + g8] = float_to_bf16_bits(v0);
+              p.y[(size_t)r * H + col + g8 + 8] = float_to_bf16_bits(v1);
+            }
+          }
+        }
+      }
+      // hand the item to the signal warp (its slot must be free: taken over
+      // two items ago)
+      const int ds = cnt_items & 1;
+      if (!mbar_wait(&sm->done_free[ds], ((cnt_items >> 1) & 1) ^ 1, abort, limit)) { ok = false; break; }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->done[ds]);
+    }
+  }
+  if (lane == 0 && *abort) set_status(p.status, MOE_ERR_TIMEOUT);
+}
+
+}  // namespace
+
+static size_t fused_smem_bytes(int T, int H, int I, int E, int slots) {
+  const size_t act = std::max((size_t)T * (H + 8), (size_t)kHSlots * kMaxT * (I + 8)) * 2;
+  return (size_t)slots * kStageBytes + act + sizeof(Smem) + (size_t)E * sizeof(int);
+}
+
+bool decode_fused_supported(int T, int H, int I, int E, int k) {
+  if (T < 1 || T > kMaxT || k > kMaxK || E > 1024) return false;
+  if (H % kTile || (2 * I) % kTile || I % 64) return false;
+  return fused_smem_bytes(T, H, I, E, 4) <= 227 * 1024;
+}
+
+moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s) {
+  if (!decode_fused_supported(q.T, q.H, q.I, q.E, q.k)) return MOE_ERR_UNSUPPORTED;
+  Args a;
+  a.logits = q.logits;
+  a.x = q.x;
+  a.w13 = q.w13;
+  a.s13 = q.s13;
+  a.w13_shared = q.w13_shared;
+  a.w2 = q.w2;
+  a.s2 = q.s2;
+  a.w2_shared = q.w2_shared;
+  a.T = q.T;
+  a.H = q.H;
+  a.I = q.I;
+  a.E = q.E;
+  a.k = q.k;
+  a.has_shared = q.w13_shared != nullptr ? 1 : 0;
+  a.out = q.out;
+  a.topk_ids_out = q.topk_ids_out;
+  a.h = q.h;
+  a.y = q.y;
+  a.y_shared = q.y_shared;
+  a.gu_done = q.gu_done;
+  a.cmb_cnt = q.cmb_cnt;
+  a.hmax = q.hmax;
+  a.status = q.status;
+  a.wait_limit = q.wait_limit;
+  a.extra_arrivals = q.extra_arrivals;
+  int slots = kMaxSlots;
+  while (slots > 4 && fused_smem_bytes(q.T, q.H, q.I, q.E, slots) > 227 * 1024) --slots;
+  if (fused_smem_bytes(q.T, q.H, q.I, q.E, slots) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+  a.slots = slots;
+  const size_t smem = fused_smem_bytes(q.T, q.H, q.I, q.E, slots);
+  int dev = 0, sms = 0;
+  moe_status st = cuda_ok(cudaGetDevice(&dev));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (st != MOE_OK) return st;
+  st = cuda_ok(cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  if (st != MOE_OK) return st;
+  // every CTA must be resident (they wait on one another): one per SM, launched cooperatively
+  int per_sm = 0;
+  st = cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kThreads, smem));
+  if (st != MOE_OK) return st;
+  if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  st = cuda_ok(cudaLaunchKernelEx(&cfg, decode_fused_kernel, a));
+  if (st != MOE_OK) return st;
+  count_launches(1);
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -10,8 +10,8 @@
 // experts' weights ("Seven Months of GB10 Field Notes": decode re-reads the
 // active weights). Each weight byte is read from HBM once. One producer warp
 // streams the weight tiles with bulk copies (cp.async.bulk, one 36 KB copy
-// per stage, completion on mbarriers) into a ring of shared-memory stages,
-// keeping ~140 KB in flight per SM. Sixteen MMA warps: warp b of part h owns
+// per stage of up to 8 K blocks, completion on mbarriers) into a ring of
+// 36 KB shared-memory stages. Sixteen MMA warps: warp b of part h owns
 // the 16-row block b of a 128-row item for the stages j with j % 2 == h, and
 // part 1 hands its partial sums to part 0 at the end of the item (more warps
 // per scheduler hide the conversion -> multiply -> MMA latency chains). A
@@ -28,7 +28,8 @@
 //
 // Work item = (group, chunk of 8 rows, 128 weight rows). CTAs are persistent
 // (one per SM) and take contiguous item ranges. Every wait is bounded; on a
-// timeout the kernel records MOE_ERR_TIMEOUT and returns.
+// timeout the kernel records MOE_ERR_TIMEOUT, lets its copies land and
+// returns.
 #include <algorithm>
 
 #include "common.cuh"
@@ -53,8 +54,8 @@ constexpr int kThreads = (kMmaWarps + 1) * 32;  // + one producer warp
 constexpr int kRowsPerPass = 8;
 constexpr int kTileRows = 128;                   // weight rows per item
 constexpr int kMaxGroups = 1025;
-constexpr int kBlocksPerStage = 8;               // 64-wide K blocks per stage (512 K)
-constexpr int kStageBytes = kBlocksPerStage * kW16Chunk;     // 36 KB: the item's chunks of 8 K blocks
+constexpr int kMaxBlocksPerStage = 8;            // 64-wide K blocks per stage (up to 512 K)
+constexpr int kStageBytes = kMaxBlocksPerStage * kW16Chunk;  // 36 KB ring slots: an item's chunks of up to 8 K blocks
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
 
 struct SmallArgs {
@@ -67,10 +68,12 @@ struct SmallArgs {
   const int32_t* a_row_index;
   const float* row_scale;
   uint16_t* out;
+  float* out_last_f32;
   int rows_limit;
   int stages;
   int early_weights;  // stream weights before the dependency wait (offsets already final)
   int* status;
+  long long wait_limit;  // cycles per bounded wait (a timeout aborts the kernel)
 };
 
 struct SmallSmem {
@@ -108,10 +111,11 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
 
 // Barrier over the MMA warps (the producer never joins) on an mbarrier, with
 // a bounded wait: every warp arrives once per use and waits for the phase.
-__device__ __forceinline__ bool mma_warps_sync(uint64_t* bar, uint32_t& phase, volatile int* abort) {
+__device__ __forceinline__ bool mma_warps_sync(uint64_t* bar, uint32_t& phase, volatile int* abort,
+                                               long long limit) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase, abort, kWaitLimit);
+  const bool ok = mbar_wait(bar, phase, abort, limit);
   phase ^= 1u;
   __syncwarp();
   return ok;
@@ -132,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
   const int mt_count = N / kTileRows;
   const int G = p.G;
   const int kblocks = K / 64;
+  const int kBlocksPerStage = w16_stage_kb(kblocks);
   const int nstage = (kblocks + kBlocksPerStage - 1) / kBlocksPerStage;
   if (!p.early_weights) pdl_wait();
 
@@ -183,13 +188,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
         const uint8_t* data = blk + sizeof(PrepHeader);
         for (int st = 0; st < nstage; ++st, ++j) {
           const int slot = j % S;
-          if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, kWaitLimit)) break;
+          if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, p.wait_limit)) break;
           const int kb0 = st * kBlocksPerStage;
           const int nkb = min(kBlocksPerStage, kblocks - kb0);
           const uint32_t bytes = (uint32_t)(nkb * kW16Chunk);
           mbar_arrive_expect_tx(&sm->full[slot], bytes);
           bulk_g2s(smem_u32(stages + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, kblocks), bytes,
                    &sm->full[slot]);
+        }
+      }
+      // the copies still in flight land before the CTA's shared memory is
+      // released (after a timeout the MMA warps may already have left)
+      for (int i = max(0, j - S); i < j; ++i) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&sm->full[i % S], (i / S) & 1) && clock64() - t0 < kWaitLimit) {
         }
       }
     }
@@ -214,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     const int nrows = min(kRowsPerPass, p.group_offsets[g + 1] - row0);
 
     if (g != cur_g || c != cur_c) {
-      if (!mma_warps_sync(&sm->xsync, xphase, abort)) break;  // everyone is done with the previous rows
+      if (!mma_warps_sync(&sm->xsync, xphase, abort, p.wait_limit)) break;  // everyone is done with the previous rows
       if (warp < kRowsPerPass) {
         const int r = warp;  // warp w stages row w
         uint16_t* dst = xs + (size_t)r * xs_stride;
@@ -227,11 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
             const uint4 v = __ldg(src + i);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
+            for (int q = 0; q < 4; ++q) m = max(m, max(finite_mag(w[q] & 0x7fffu), finite_mag((w[q] >> 16) & 0x7fffu)));
           }
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-          if (m > 0x7f80u) m = 0x7f80u;  // NaN patterns are outside the contract
           // m = bf16 bits of the row max; its exponent e puts the max in [2^(e-127), 2^(e-126))
           const int e = (int)(m >> 7);
           int sh = (m == 0) ? 0 : 141 - max(e, 1);  // 2^(e-127+sh) = 2^14
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       }
       cur_g = g;
       cur_c = c;
-      if (!mma_warps_sync(&sm->xsync, xphase, abort)) break;
+      if (!mma_warps_sync(&sm->xsync, xphase, abort, p.wait_limit)) break;
     }
 
     // one accumulator per k16 step of a block: four independent MMA chains
@@ -275,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     for (int st = 0; st < nstage; ++st, ++j) {
       if ((j % kHalves) != half) continue;  // another part's stage
       const int slot = j % S;
-      if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, kWaitLimit)) { ok = false; break; }
+      if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, p.wait_limit)) { ok = false; break; }
       const int kb0 = st * kBlocksPerStage;
       const int nkb = min(kBlocksPerStage, kblocks - kb0);
       const uint8_t* sd = stages + (size_t)slot * kStageBytes;
@@ -318,14 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     // split-K reduction: parts 1.. hand their partial sums to part 0, which
     // adds them in a fixed order (part 0, 1, 2, ...)
     if (half != 0) {
-      if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, kWaitLimit)) break;
+      if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, p.wait_limit)) break;
       sm->red[half - 1][blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->red_full[blk]);
       rphase ^= 1u;
       continue;
     }
-    if (!mbar_wait(&sm->red_full[blk], rphase, abort, kWaitLimit)) break;
+    if (!mbar_wait(&sm->red_full[blk], rphase, abort, p.wait_limit)) break;
 #pragma unroll
     for (int h = 0; h < kHalves - 1; ++h) {
       const float4 o = sm->red[h][blk][lane];
@@ -360,8 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       } else {
         const float rs = p.row_scale ? p.row_scale[orow] : 1.0f;
         const int hr = 16 * mb + g8;
-        p.out[(size_t)orow * N + hr] = float_to_bf16_bits(acc[q] * rm * hdr->alpha[0] * rs);
-        p.out[(size_t)orow * N + hr + 8] = float_to_bf16_bits(acc[2 + q] * rm * hdr->alpha[0] * rs);
+        const float v0 = acc[q] * rm * hdr->alpha[0] * rs, v1 = acc[2 + q] * rm * hdr->alpha[0] * rs;
+        if (p.out_last_f32 != nullptr && g == G - 1) {  // shared expert: kept fp32 for the combine
+          float* o = p.out_last_f32 + (size_t)(orow - p.group_offsets[G - 1]) * N;
+          o[hr] = v0;
+          o[hr + 8] = v1;
+        } else {
+          p.out[(size_t)orow * N + hr] = float_to_bf16_bits(v0);
+          p.out[(size_t)orow * N + hr + 8] = float_to_bf16_bits(v1);
+        }
       }
     }
   }
@@ -389,8 +407,10 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStrea
   a.a_row_index = pl.a_row_index;
   a.row_scale = pl.row_scale;
   a.out = pl.out;
+  a.out_last_f32 = pl.out_last_f32;
   a.rows_limit = rows_limit;
   a.status = pl.status;
+  a.wait_limit = debug_wait_limit();
   a.early_weights = pl.pdl && pl.early_weights ? 1 : 0;
   const size_t limit = 227 * 1024;
   int S = 6;

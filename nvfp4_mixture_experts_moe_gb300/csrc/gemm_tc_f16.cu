@@ -92,14 +92,17 @@ struct Args {
   const float* a_mul;      // per A row multiplier (2^-s), group order
   const float* row_scale;
   uint16_t* out;
+  float* out_last_f32;
   int rows_min;
   int* status;
+  long long wait_limit;      // cycles per bounded wait (a timeout aborts the kernel)
 };
 
 struct Smem {
   uint64_t w_full[kRawSlots];   // raw weights of the stage landed
   uint64_t w_empty[kRawSlots];  // the dequant set is done reading them
-  uint64_t ready[kStages];      // activation rows landed (bytes) and the four dequant warps done
+  uint64_t bfull[kStages];      // activation rows of the stage landed
+  uint64_t ready[kStages];      // the four dequant warps wrote the stage's A columns
   uint64_t empty[kStages];      // the stage's MMAs completed (activation tile and TMEM A free)
   uint64_t tfull;
   uint64_t tempty;
@@ -169,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
       mbar_init(&sm->w_empty[i], 4);
     }
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm->ready[i], 4 + 1);
+      mbar_init(&sm->bfull[i], 1);
+      mbar_init(&sm->ready[i], 4);
       mbar_init(&sm->empty[i], 1);
     }
     mbar_init(&sm->tfull, 1);
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int rs = j % kRawSlots;
-          if (!mbar_wait(&sm->w_empty[rs], ((j / kRawSlots) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->w_empty[rs], ((j / kRawSlots) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
           const uint32_t bytes = (uint32_t)(min(2, KB64 - 2 * ks) * kW16Chunk);
           mbar_arrive_expect_tx(&sm->w_full[rs], bytes);
           bulk_g2s(smem_u32(raw + rs * kRawStage), wdata + w4a16_chunk(it.mt, 2 * ks, KB64), bytes, &sm->w_full[rs]);
@@ -234,20 +238,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
           const int nh = min(2, KB64 - 2 * ks);
-          mbar_arrive_expect_tx(&sm->ready[slot], nh * half_bytes);
+          mbar_arrive_expect_tx(&sm->bfull[slot], nh * half_bytes);
           const uint32_t dst = smem_u32(b_tiles + slot * kBStage);
           for (int h = 0; h < nh; ++h)
-            tma_load_2d(dst + h * kBHalf, &maps.m[q], (2 * ks + h) * kHalf, it.row0, &sm->ready[slot]);
+            tma_load_2d(dst + h * kBHalf, &maps.m[q], (2 * ks + h) * kHalf, it.row0, &sm->bfull[slot]);
         }
         if (!ok) break;
       }
-      if (*abort) {  // the boxes share their barrier with the dequant warps: allow them ~0.1 ms to land
-        const long long t0 = clock64();
-        while (clock64() - t0 < 200000) {
-        }
-      }
+      // the boxes this warp issued land before the shared memory is released
+      for (int i = max(0, j - kStages); i < j; ++i) drain_wait(&sm->bfull[i % kStages], (i / kStages) & 1);
     }
     __syncwarp();
   } else if (warp >= kDeqWarp0) {
@@ -267,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
       for (int ks = 0; ks < KS; ++ks, ++j) {
         if ((j & 1) != set) continue;
         const int slot = j % kStages, rslot = j % kRawSlots;
-        if (!mbar_wait(&sm->w_full[rslot], (j / kRawSlots) & 1, abort, kWaitLimit) ||
-            !mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) {
+        if (!mbar_wait(&sm->w_full[rslot], (j / kRawSlots) & 1, abort, p.wait_limit) ||
+            !mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, p.wait_limit)) {
           ok = false;
           break;
         }
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
         rowmul[n] = m;
       }
       __syncwarp();
-      if (!mbar_wait(&sm->tfull, itc & 1, abort, kWaitLimit)) break;
+      if (!mbar_wait(&sm->tfull, itc & 1, abort, p.wait_limit)) break;
       tc_fence_after();
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
       const float a0 = hdr->alpha[0], a1 = hdr->alpha[1];
@@ -375,6 +376,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
               if (n + 1 < it.rows) o[N / 2] = (uint16_t)(hb >> 16);
             }
           }
+        } else if (p.out_last_f32 != nullptr && it.g == G - 1) {
+          // shared expert: kept fp32 for the combine
+          float* o32 = p.out_last_f32 + (size_t)(it.row0 - p.group_offsets[G - 1]) * N + it.mt * kM + rho;
+#pragma unroll
+          for (int c4 = 0; c4 < 32; c4 += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + c4);  // broadcast read
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int n = c0 + c4 + t;
+              if (n < it.rows) o32[(size_t)n * N] = __uint_as_float(r[c4 + t]) * mv[t] * a0;
+            }
+          }
         } else {
 #pragma unroll
           for (int c4 = 0; c4 < 32; c4 += 4) {
@@ -402,14 +416,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
       int j = 0, itc = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
         const Item it = decode_item(item, pref, G, MT, p.group_offsets);
-        if (!mbar_wait(&sm->tempty, (itc & 1) ^ 1, abort, kWaitLimit)) break;
+        if (!mbar_wait(&sm->tempty, (itc & 1) ^ 1, abort, p.wait_limit)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(kM, it.bn, 0);
         const uint32_t d = tmem;
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, kWaitLimit)) {
+          if (!mbar_wait(&sm->bfull[slot], (j / kStages) & 1, abort, p.wait_limit) ||
+              !mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, p.wait_limit)) {
             ok = false;
             break;
           }
@@ -488,8 +503,10 @@ moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) 
   a.a_mul = pl.a_mul;
   a.row_scale = pl.row_scale;
   a.out = pl.out;
+  a.out_last_f32 = pl.out_last_f32;
   a.rows_min = rows_min;
   a.status = pl.status;
+  a.wait_limit = debug_wait_limit();
   const size_t smem = smem_bytes(pl.num_groups);
   if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
   int dev = 0, sms = 148;

@@ -86,12 +86,15 @@ struct Args {
   const float* b_gs;           // activation global scale
   const float* row_scale;
   uint16_t* out;
+  float* out_last_f32;
   float* out_amax;
   int* status;
+  long long wait_limit;        // cycles per bounded wait (a timeout aborts the kernel)
 };
 
 struct Smem {
-  uint64_t ready[kMaxStages];    // both loaders' bytes landed (two expect_tx arrivals)
+  uint64_t wready[kMaxStages];   // the weight loader's bytes of the stage landed
+  uint64_t bready[kMaxStages];   // the activation loader's bytes of the stage landed
   uint64_t sf_full[kMaxStages];  // the stage's scale factors are in tensor memory
   uint64_t empty[kMaxStages];    // the stage's MMAs completed
   uint64_t tfull[2];
@@ -137,8 +140,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <bool GATE_UP, int CTAS>
+// MX: MXFP4 operands (E8M0 scales per 32, kind::mxf4, two scale atoms per
+// operand and stage, no global scales); otherwise NVFP4 (E4M3 per 16,
+// kind::mxf4nvf4, four atoms per operand and stage).
+template <bool GATE_UP, int CTAS, bool MX>
 __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __grid_constant__ BoxMaps maps, Args p) {
+  constexpr int kSfBytes = MX ? kSfStage / 2 : kSfStage;   // scale bytes per operand and stage
+  constexpr int kAtoms = kSfBytes / 512;
   constexpr int kStages = Shape<CTAS>::kStages;
   constexpr int kAcc = Shape<CTAS>::kAcc;
   constexpr int kTmemCols = Shape<CTAS>::kTmemCols;
@@ -166,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
     pref[0] = 0;
     tb[0] = 0;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm->ready[i], 2);
+      mbar_init(&sm->wready[i], 1);
+      mbar_init(&sm->bready[i], 1);
       mbar_init(&sm->sf_full[i], 1);
       mbar_init(&sm->empty[i], 1);
     }
@@ -214,20 +223,17 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
           uint8_t* st = base + slot * kStageBytes;
           const size_t tile = (size_t)it.mt * KS + ks;
-          mbar_arrive_expect_tx(&sm->ready[slot], kTile + kSfStage);
-          bulk_g2s(smem_u32(st), wdata + tile * kTile, kTile, &sm->ready[slot]);
-          bulk_g2s(smem_u32(st + 2 * kTile), wsf + tile * kSfStage, kSfStage, &sm->ready[slot]);
+          mbar_arrive_expect_tx(&sm->wready[slot], kTile + kSfBytes);
+          bulk_g2s(smem_u32(st), wdata + tile * kTile, kTile, &sm->wready[slot]);
+          bulk_g2s(smem_u32(st + 2 * kTile), wsf + tile * kSfBytes, kSfBytes, &sm->wready[slot]);
         }
         if (!ok) break;
       }
-      if (*abort) {  // copies in flight land before the shared memory is released
-        const long long t0 = clock64();
-        while (clock64() - t0 < 200000) {
-        }
-      }
+      // the copies this warp issued land before the shared memory is released
+      for (int i = max(0, j - kStages); i < j; ++i) drain_wait(&sm->wready[i % kStages], (i / kStages) & 1);
     }
     __syncwarp();
   } else if (warp == kBLoadWarp) {
@@ -238,24 +244,21 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
         const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
         const int q = 32 - __clz((it.bn >> 4) - 1);   // box of 16 << q >= bn rows
-        const uint32_t bytes = (uint32_t)((16 << q) * kRowBytes + kSfStage);
+        const uint32_t bytes = (uint32_t)((16 << q) * kRowBytes + kSfBytes);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->empty[slot], ((j / kStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
           uint8_t* st = base + slot * kStageBytes;
-          mbar_arrive_expect_tx(&sm->ready[slot], bytes);
-          tma_load_2d(smem_u32(st + kTile), &maps.m[q], ks * kRowBytes, it.row0, &sm->ready[slot]);
-          bulk_g2s(smem_u32(st + 2 * kTile + kSfStage), p.b_sf_tiles + ((size_t)it.tile * KS + ks) * kSfStage,
-                   kSfStage, &sm->ready[slot]);
+          mbar_arrive_expect_tx(&sm->bready[slot], bytes);
+          tma_load_2d(smem_u32(st + kTile), &maps.m[q], ks * kRowBytes, it.row0, &sm->bready[slot]);
+          bulk_g2s(smem_u32(st + 2 * kTile + kSfStage), p.b_sf_tiles + ((size_t)it.tile * KS + ks) * kSfBytes,
+                   kSfBytes, &sm->bready[slot]);
         }
         if (!ok) break;
       }
-      if (*abort) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < 200000) {
-        }
-      }
+      // the copies this warp issued land before the shared memory is released
+      for (int i = max(0, j - kStages); i < j; ++i) drain_wait(&sm->bready[i % kStages], (i / kStages) & 1);
     }
     __syncwarp();
   } else if (warp == kSfWarp) {
@@ -268,13 +271,17 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
           const int slot = j % kStages;
           // the slot's previous MMAs completed before its loads were issued, so
           // its TMEM columns are free once the new data has landed
-          if (!mbar_wait(&sm->ready[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->wready[slot], (j / kStages) & 1, abort, p.wait_limit) ||
+              !mbar_wait(&sm->bready[slot], (j / kStages) & 1, abort, p.wait_limit)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sfa = smem_u32(base + slot * kStageBytes) + 2 * kTile;
           const uint32_t sfb = sfa + kSfStage;
           const uint32_t sf_col = tmem + kSfCol0 + slot * 32;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < kAtoms; ++kk) {
             tc_cp_32x128b_warpx4(sf_col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
             tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
           }
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int rho = q * 32 + lane;
-    const float inv_gs_b = 1.0f / *p.b_gs;
+    const float inv_gs_b = MX ? 1.0f : 1.0f / *p.b_gs;
     float amax = 0.0f;
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
         rsv[i] = (!GATE_UP && p.row_scale && n < it.rows) ? __ldg(p.row_scale + it.row0 + n) : 1.0f;
       }
       const int acc = itc % kAcc;
-      if (!mbar_wait(&sm->tfull[acc], (itc / kAcc) & 1, abort, kWaitLimit)) break;
+      if (!mbar_wait(&sm->tfull[acc], (itc / kAcc) & 1, abort, p.wait_limit)) break;
       tc_fence_after();
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
       const float a0 = hdr->alpha[0] * inv_gs_b, a1 = hdr->alpha[1] * inv_gs_b;
@@ -346,16 +353,23 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
 #pragma unroll
           for (int i = 0; i < kMaxBN / 32; ++i)
             if ((c0 >> 5) == i) rs_chunk = rsv[i];
+          const bool last_f32 = p.out_last_f32 != nullptr && it.g == G - 1;  // shared expert: fp32
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {  // two tokens per bf16 conversion
             const int n = c0 + c;
             const float rs0 = __shfl_sync(0xffffffffu, rs_chunk, c);
             const float rs1 = __shfl_sync(0xffffffffu, rs_chunk, c + 1);
-            const uint32_t yb = float2_to_bf16x2_bits(__uint_as_float(r[c]) * a0 * rs0,
-                                                      __uint_as_float(r[c + 1]) * a0 * rs1);
-            uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
-            if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
-            if (n + 1 < it.rows) o[N] = (uint16_t)(yb >> 16);
+            const float v0 = __uint_as_float(r[c]) * a0 * rs0, v1 = __uint_as_float(r[c + 1]) * a0 * rs1;
+            if (last_f32) {
+              float* o32 = p.out_last_f32 + (size_t)(it.row0 - p.group_offsets[G - 1] + n) * N + it.mt * kM + rho;
+              if (n < it.rows) o32[0] = v0;
+              if (n + 1 < it.rows) o32[N] = v1;
+            } else {
+              const uint32_t yb = float2_to_bf16x2_bits(v0, v1);
+              uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
+              if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
+              if (n + 1 < it.rows) o[N] = (uint16_t)(yb >> 16);
+            }
           }
         }
       }
@@ -374,14 +388,15 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
         const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
         const int acc = itc % kAcc;
-        if (!mbar_wait(&sm->tempty[acc], ((itc / kAcc) & 1) ^ 1, abort, kWaitLimit)) break;
+        if (!mbar_wait(&sm->tempty[acc], ((itc / kAcc) & 1) ^ 1, abort, p.wait_limit)) break;
         const uint32_t d = tmem + acc * 128;
         tc_fence_after();
         const uint32_t idesc = idesc_nvf4(kM, it.bn);
+        const uint32_t idesc_mx0 = idesc_mxf4(kM, it.bn, 0), idesc_mx2 = idesc_mxf4(kM, it.bn, 2);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
-          if (!mbar_wait(&sm->sf_full[slot], (j / kStages) & 1, abort, kWaitLimit)) { ok = false; break; }
+          if (!mbar_wait(&sm->sf_full[slot], (j / kStages) & 1, abort, p.wait_limit)) { ok = false; break; }
           tc_fence_after();
           const uint32_t as = smem_u32(base + slot * kStageBytes);
           const uint32_t bs = as + kTile;
@@ -390,7 +405,11 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
-            mma_nvf4(d, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4, (ks | kk) != 0);
+            if (MX)  // atom kk / 2, byte pair 2 * (kk % 2)
+              mma_mxf4(d, ad, bd, (kk & 1) ? idesc_mx2 : idesc_mx0, sf_col + (kk >> 1) * 4,
+                       sf_col + 16 + (kk >> 1) * 4, (ks | kk) != 0);
+            else
+              mma_nvf4(d, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4, (ks | kk) != 0);
           }
           tc_commit(&sm->empty[slot]);
         }
@@ -432,7 +451,9 @@ static size_t fp4_smem_bytes(int G, int stages) {
 moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   if (pl.num_groups <= 0) return MOE_OK;
   if (pl.K % kBK || pl.N % kM) return MOE_ERR_UNSUPPORTED;
-  if (pl.a == nullptr || pl.a_sf == nullptr || pl.a_gs == nullptr || pl.a_rows <= 0) return MOE_ERR_INVALID_ARG;
+  const bool mx = pl.mode == MOE_MXFP4;
+  if (pl.a == nullptr || pl.a_sf == nullptr || (!mx && pl.a_gs == nullptr) || pl.a_rows <= 0)
+    return MOE_ERR_INVALID_ARG;
   auto encode = encode_tiled();
   if (encode == nullptr) return MOE_ERR_CUDA;
   // the FP4 activation codes [a_rows, K/2] in group order: boxes of 16..128 rows x 128 bytes, 128-byte swizzle
@@ -459,16 +480,20 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   a.b_gs = pl.a_gs;
   a.row_scale = pl.row_scale;
   a.out = pl.out;
+  a.out_last_f32 = pl.out_last_f32;
   a.out_amax = pl.out_amax;
   a.status = pl.status;
+  a.wait_limit = debug_wait_limit();
   const int ctas = pl.ctas_per_sm == 1 ? 1 : 2;
   const size_t smem = fp4_smem_bytes(pl.num_groups, ctas == 2 ? Shape<2>::kStages : Shape<1>::kStages);
   if (smem > (ctas == 2 ? 113 : 227) * 1024) return MOE_ERR_UNSUPPORTED;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  auto k = ctas == 2 ? (pl.gate_up ? gemm_tc_fp4_kernel<true, 2> : gemm_tc_fp4_kernel<false, 2>)
-                     : (pl.gate_up ? gemm_tc_fp4_kernel<true, 1> : gemm_tc_fp4_kernel<false, 1>);
+  auto k = mx ? (ctas == 2 ? (pl.gate_up ? gemm_tc_fp4_kernel<true, 2, true> : gemm_tc_fp4_kernel<false, 2, true>)
+                           : (pl.gate_up ? gemm_tc_fp4_kernel<true, 1, true> : gemm_tc_fp4_kernel<false, 1, true>))
+              : (ctas == 2 ? (pl.gate_up ? gemm_tc_fp4_kernel<true, 2, false> : gemm_tc_fp4_kernel<false, 2, false>)
+                           : (pl.gate_up ? gemm_tc_fp4_kernel<true, 1, false> : gemm_tc_fp4_kernel<false, 1, false>));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * ctas), dim3(kThreads), smem, s, maps, a);
   if (e != cudaSuccess) return cuda_ok(e);

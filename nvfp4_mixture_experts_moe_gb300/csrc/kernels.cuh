@@ -39,10 +39,15 @@ constexpr int kFusedRoutePermuteMax = 2048;  // pairs routed and permuted by one
 // returns at once.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Expert sharding (expert parallelism): the permutations group only the
+// pairs of experts [shard_lo, shard_lo + n) (n = the E they are given, the
+// routing covering E_global experts); other valid pairs are dropped without
+// an error and get inv_perm = -1; the kept routed rows come first
+// (offsets[n] of them) and the shared rows follow at [offsets[n], offsets[n] + T).
 moe_status launch_route_permute_small(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                                       int* status, int32_t* row_token, float* row_weight, int32_t* gofs,
-                                      cudaStream_t s);
+                                      cudaStream_t s, int shard_lo, int shard_n);
 
 moe_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                              cudaStream_t s);
@@ -51,7 +56,7 @@ size_t permute_scratch_bytes(int T, int k, int E);
 moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* inv_perm, int* status, void* scratch,
                           int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
-                          cudaStream_t s, bool pdl = false);
+                          cudaStream_t s, bool pdl = false, int shard_lo = 0, int E_global = 0);
 
 // Quantisation: amax into *amax (must be zeroed first), then codes. A
 // gs_static > 0 replaces the dynamic 2688 / amax (amax is then not read).
@@ -70,14 +75,14 @@ moe_status launch_router_gemm(const uint16_t* x, const uint16_t* w, int T, int H
 
 moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStream_t s);
 moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
-                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s,
+                          const float* y_shared, int T, int k, int H, uint16_t* out, cudaStream_t s,
                           bool pdl = false);
 
 // Weight preparation (device part; the host validates sizes and scales).
 moe_status launch_prepare_w4a16(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
                                 uint8_t* out, int* flag, cudaStream_t s);
 moe_status launch_prepare_w4a4(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
-                               uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s);
+                               uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s, bool mx = false);
 size_t prepare_w4a4_sf_bytes(int N, int K);
 
 // Grouped GEMMs.
@@ -96,6 +101,8 @@ struct GemmPlan {
   const int32_t* a_row_index;
   const float* row_scale;
   uint16_t* out;
+  float* out_last_f32;      // nullable: rows of the last group (the shared expert) are written here
+                            // as fp32, row (r - group_offsets[G-1]), instead of bf16 into out
   float* out_amax;
   const uint16_t* a_f16;    // W4A16 large groups: f16 copy of the A rows in group order
                             // (row r of the grouped layout; rows_to_f16), or null
@@ -125,12 +132,19 @@ moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
 // atoms per (128-row tile of a group, 256-wide K stage), zeroed first
 // (sf_bytes); gs = 2688 / amax as moe_nvfp4_quantize, or gs_static when it is
 // > 0. With `dest` (inverse
-// permutation, [src_rows * k]) token t's row goes to dest[t*k + j] and, with
-// shared_base >= 0, to shared_base + t; without it source row r is row r.
+// permutation, [src_rows * k]) token t's row goes to dest[t*k + j] (pairs with
+// dest -1 are skipped) and, with shared_base >= 0 (a flag), to row
+// gofs[G-1] + t of the shared group; without it source row r is row r.
 moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
                                  int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
                                  uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, float gs_static,
-                                 cudaStream_t s, bool pdl = false);
+                                 cudaStream_t s, bool pdl = false, bool mx = false);
+
+// MXFP4: bf16 [rows, K] -> codes [rows, K/2] and E8M0 scales [rows, K/32]
+// (K % 32 == 0). With mx = true launch_quantize_tiles writes MXFP4 codes and
+// the E8M0 scale atoms of the kind::mxf4 GEMM (four 32-blocks per atom word;
+// amax, gs_out and gs_static are not used).
+moe_status launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t* sf, cudaStream_t s);
 
 // bf16 rows -> f16 rows scaled by a power of two so that each row's largest
 // magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it. Row r of dst is
@@ -148,5 +162,38 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& p, cudaStream_t s);
 
 // Groups with at most this many rows take the small-group path.
 constexpr int kSmallGroupRows = 32;
+
+// Single-kernel decode path (W4A16, T <= kDecodeFusedMaxT): routing,
+// permutation, both GEMMs and the combine in one cooperative launch.
+constexpr int kDecodeFusedMaxT = 8;
+struct DecodeFusedPlan {
+  const float* logits;       // [T, E]
+  const uint16_t* x;         // [T, H]
+  const uint8_t* w13;        // E prepared gate/up blocks, s13 bytes apart
+  size_t s13;
+  const uint8_t* w13_shared; // nullable (no shared expert)
+  const uint8_t* w2;
+  size_t s2;
+  const uint8_t* w2_shared;
+  int T, H, I, E, k;
+  uint16_t* out;             // [T, H]
+  int32_t* topk_ids_out;     // nullable
+  uint16_t* h;               // [T*k + T, I]
+  uint16_t* y;               // [T*k, H] routed rows, bf16
+  float* y_shared;           // [T, H] the shared expert's rows, fp32
+  int* gu_done;              // [E + 1], zero at launch
+  int* cmb_cnt;              // [T * H/16], zero at launch
+  unsigned* hmax;            // [T*k + T], zero at launch
+  int* status;
+  long long wait_limit;      // cycles per bounded wait
+  int extra_arrivals;        // test hook (0): extra arrivals a gate/up tile is expected to make
+};
+bool decode_fused_supported(int T, int H, int I, int E, int k);
+moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s);
+
+// Test hooks set through moe_debug_set (process-wide).
+long long debug_wait_limit();     // cycles per bounded device wait (default 4e9, about 2 s)
+int debug_extra_arrivals();       // 0 normally
+bool debug_decode_fused_disabled();
 
 }  // namespace moe

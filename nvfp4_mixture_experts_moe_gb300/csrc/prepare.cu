@@ -115,12 +115,39 @@ __global__ void prepare_w4a4_sf_kernel(const uint8_t* __restrict__ sf, int N, in
   }
 }
 
+// MXFP4 ("vLLM on the NVIDIA DGX Spark", section 6.4): the same tile images;
+// E8M0 scales, one per 32 along K, in 512-byte atoms that each hold four
+// consecutive scales of the tile's 128 rows (K 128: two K=64 MMAs, the
+// kind::mxf4 .scale_vec::2X layout, which picks bytes 0-1 or 2-3 of a row's
+// word per MMA). Per (tile mt, 256-wide K stage ks): two atoms. Code 0xFF
+// (NaN) is refused.
+__global__ void prepare_mx_sf_kernel(const uint8_t* __restrict__ sf, int N, int K, int gate_up,
+                                     uint8_t* __restrict__ out, int* flag) {
+  const size_t total = (size_t)N * K / 32;
+  const int KS = K / 256;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t tile = i / 1024;
+    const int within = (int)(i % 1024);
+    const int mt = (int)(tile / KS), ks = (int)(tile % KS);
+    const int c = within / 512, a = within % 512;
+    const int m0 = a / 16, m1 = (a % 16) / 4, jj = a % 4;
+    const int o = mt * 128 + 32 * m1 + m0;
+    const uint8_t v = sf[(size_t)src_row(o, N, gate_up) * (K / 32) + ks * 8 + c * 4 + jj];
+    if (v == 0xffu) atomicOr(flag, 1);
+    out[i] = v;
+  }
+}
+
 moe_status launch_prepare_w4a4(const uint8_t* codes, const uint8_t* sf, int N, int K, int gate_up,
-                               uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s) {
+                               uint8_t* out_data, uint8_t* out_sf, int* flag, cudaStream_t s, bool mx) {
   if (K % 256) return MOE_ERR_INVALID_ARG;
   prepare_w4a4_data_kernel<<<1024, 256, 0, s>>>(codes, N, K, gate_up, out_data);
   count_launches(1);
-  prepare_w4a4_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out_sf, flag);
+  if (mx)
+    prepare_mx_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out_sf, flag);
+  else
+    prepare_w4a4_sf_kernel<<<512, 256, 0, s>>>(sf, N, K, gate_up, out_sf, flag);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }

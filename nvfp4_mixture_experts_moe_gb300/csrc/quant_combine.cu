@@ -32,13 +32,13 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restri
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      m = max(m, w[j] & 0x7fffu);
-      m = max(m, (w[j] >> 16) & 0x7fffu);
+      m = max(m, finite_mag(w[j] & 0x7fffu));
+      m = max(m, finite_mag((w[j] >> 16) & 0x7fffu));
     }
   }
   for (size_t i = nvec * 8 + blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x)
-    m = max(m, (uint32_t)(x[i] & 0x7fffu));
+    m = max(m, finite_mag((uint32_t)(x[i] & 0x7fffu)));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
   __shared__ uint32_t red[8];
@@ -46,9 +46,6 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restri
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = max(m, red[i]);
-    // NaN bit patterns (> 0x7f80) are outside the contract; keep them out of
-    // the max so the scale stays finite.
-    if (m > 0x7f80u) m = 0x7f80u;
     atomic_max_nonneg(amax, __uint_as_float(m << 16));
   }
 }
@@ -152,6 +149,85 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
 }
 
 // ---------------------------------------------------------------------------
+// MXFP4 ("vLLM on the NVIDIA DGX Spark", section 6.4 "NVFP4 vs MXFP4"): e2m1
+// elements with one power-of-two E8M0 scale per 32 along K and no global
+// scale. Per block: e = floor(log2 amax) - 2 (6 = 1.5 * 2^2 is e2m1's
+// largest value, so amax / 2^e lies in [4, 8)), clamped to [-127, 127], an
+// all-zero block takes e = -127 and zero codes; the scale code is e + 127 and
+// code_i = e2m1(x_i * 2^-e), nearest even, saturating at 6, sign kept. The
+// multiply by 2^-e is exact.
+
+// floor(log2 a) for a positive finite fp32 a, from its bits (subnormals too).
+__device__ __forceinline__ int floor_log2_pos(float a) {
+  const uint32_t bits = __float_as_uint(a);
+  const int ex = (int)((bits >> 23) & 0xffu);
+  if (ex > 0) return ex - 127;
+  return (31 - __clz((int)(bits & 0x7fffffu))) - 149;
+}
+
+// 32 bf16 values (64 bytes, 16-byte aligned) -> 16 bytes of codes and the
+// E8M0 scale code.
+__device__ __forceinline__ void quant_block32_mx(const uint16_t* src, uint4& codes, uint32_t& scale_code) {
+  const uint4* v = reinterpret_cast<const uint4*>(src);
+  uint32_t wv[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = ldg_stream(v + i);
+    wv[4 * i] = q.x;
+    wv[4 * i + 1] = q.y;
+    wv[4 * i + 2] = q.z;
+    wv[4 * i + 3] = q.w;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[i] << 16)), fabsf(__uint_as_float(wv[i] & 0xffff0000u))));
+  if (!(amax > 0.0f)) {  // all zeros (a NaN block, outside the contract, also lands here)
+    codes = make_uint4(0u, 0u, 0u, 0u);
+    scale_code = 0u;
+    return;
+  }
+  const int e = max(-127, min(127, floor_log2_pos(amax) - 2));
+  const float mul = __int_as_float((127 - e) << 23);  // 2^-e, a normal float for e in [-127, 126]
+  uint32_t out[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t x = wv[4 * w + b];
+      word |= e2m1x2_rn(__fmul_rn(__uint_as_float(x << 16), mul), __fmul_rn(__uint_as_float(x & 0xffff0000u), mul))
+              << (8 * b);
+    }
+    out[w] = word;
+  }
+  codes = make_uint4(out[0], out[1], out[2], out[3]);
+  scale_code = (uint32_t)(e + 127);
+}
+
+// One thread per 32-element block: codes [rows, K/2], scales [rows, K/32].
+__global__ void __launch_bounds__(256) quantize_mx_bf16_kernel(const uint16_t* __restrict__ x, int rows, int K,
+                                                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const size_t nblk = (size_t)rows * (K / 32);
+  const size_t b = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  uint4 codes;
+  uint32_t code;
+  quant_block32_mx(x + b * 32, codes, code);
+  *reinterpret_cast<uint4*>(q + b * 16) = codes;
+  sf[b] = (uint8_t)code;
+}
+
+moe_status launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t* sf, cudaStream_t s) {
+  const size_t nblk = (size_t)rows * (K / 32);
+  if (nblk == 0) return MOE_OK;
+  const int blocks = (int)((nblk + 255) / 256);
+  quantize_mx_bf16_kernel<<<blocks, 256, 0, s>>>(x, rows, K, q, sf);
+  count_launches(1);
+  return cuda_ok(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
 // Quantisation of the block-scaled GEMM's activation rows straight into the
 // layout its loaders copy. Row r of the grouped layout gets its codes at
 // q[r][K/2] (row-major, so 2-D tensor-map boxes of a group's rows are plain
@@ -166,8 +242,9 @@ moe_status launch_quantize_bf16(const uint16_t* x, int rows, int K, const float*
 //
 // One warp per source row, quantised once: with `dest` (the inverse
 // permutation, [rows_src * k]) the row of token t goes to dest[t*k + j] for
-// each j with a valid slot and, with `shared_base` >= 0, to row
-// shared_base + t; without it, source row r is row r. A lane takes one
+// each j with a valid slot and, with `shared_base` >= 0 (a flag), to row
+// gofs[G-1] + t of the shared group (the last group); without it, source
+// row r is row r. A lane takes one
 // 16-block per round of 32 (coalesced loads and code stores; four lanes'
 // scales make one 4-byte atom word). The group offsets and the tile prefix
 // sit in shared memory. The arithmetic per 16-block is quantize_bf16_kernel's.
@@ -203,6 +280,7 @@ __device__ __forceinline__ void quant_block16(const uint16_t* src, float gs, uin
   }
 }
 
+template <bool MX>
 __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
     const uint16_t* __restrict__ x, int src_rows, int K, const int32_t* __restrict__ dest, int k, int shared_base,
     const int32_t* __restrict__ gofs, int G, const float* __restrict__ amax_p, uint8_t* __restrict__ q,
@@ -229,7 +307,7 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
     }
   }
   __syncthreads();
-  const float gs = global_scale_of(amax_p, gs_static);
+  const float gs = MX ? 1.0f : global_scale_of(amax_p, gs_static);
   if (blockIdx.x == 0 && threadIdx.x == 0 && gs_out != nullptr) *gs_out = gs;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kQtWarps + (threadIdx.x >> 5);
@@ -238,7 +316,8 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
   const int ndest = dest ? k + (shared_base >= 0 ? 1 : 0) : 1;
   int my_r = -1, my_t = 0, my_m = 0;
   if (lane < ndest) {
-    my_r = dest ? (lane < k ? dest[(size_t)row * k + lane] : shared_base + row) : row;
+    // the shared group (the last one) starts right after the routed rows that were kept
+    my_r = dest ? (lane < k ? dest[(size_t)row * k + lane] : s_gofs[G - 1] + row) : row;
     if (my_r >= 0) {
       int lo = 0, hi = G - 1;  // group of row my_r: the last g with gofs[g] <= my_r
       while (lo < hi) {
@@ -250,29 +329,41 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
       my_m = local % 128;
     }
   }
-  const int KB16 = K / 16, KS = K / 256;
+  // blocks of 16 (NVFP4) or 32 (MXFP4) elements; a scale atom holds four
+  // consecutive blocks' scales of 128 rows: one K=64 MMA (NVFP4) or two (MXFP4)
+  constexpr int BLK = MX ? 32 : 16;
+  const int NB = K / BLK, atoms_per_tile = K / (4 * BLK);
   const uint16_t* src = x + (size_t)row * K;
-  // 32 consecutive 16-blocks per round, one per lane: the warp's loads and
-  // code stores are contiguous; the four scales of lanes 4i..4i+3 (one
-  // 4-byte word of a scale atom) are gathered into lane 4i, which stores it
+  // 32 consecutive blocks per round, one per lane: the warp's loads and code
+  // stores are contiguous; the four scales of lanes 4i..4i+3 (one 4-byte word
+  // of a scale atom) are gathered into lane 4i, which stores it
 #pragma unroll 2
-  for (int kb0 = 0; kb0 < KB16; kb0 += 32) {
+  for (int kb0 = 0; kb0 < NB; kb0 += 32) {
     const int kb = kb0 + lane;
-    const bool valid = kb < KB16;
-    uint32_t lo = 0, hi = 0, code = 0;
-    if (valid) quant_block16(src + (size_t)kb * 16, gs, lo, hi, code);
+    const bool valid = kb < NB;
+    uint32_t code = 0;
+    uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      if (MX) {
+        quant_block32_mx(src + (size_t)kb * 32, c4, code);
+      } else {
+        quant_block16(src + (size_t)kb * 16, gs, c4.x, c4.y, code);
+      }
+    }
     uint32_t sw = code << (8 * (lane & 3));
     sw |= __shfl_xor_sync(0xffffffffu, sw, 1);
     sw |= __shfl_xor_sync(0xffffffffu, sw, 2);
-    const int ks = kb >> 4, kk = (kb >> 2) & 3;
     for (int d = 0; d < ndest; ++d) {
       const int r = __shfl_sync(0xffffffffu, my_r, d);
       const int t = __shfl_sync(0xffffffffu, my_t, d);
       const int m = __shfl_sync(0xffffffffu, my_m, d);
       if (r < 0 || !valid) continue;
-      *reinterpret_cast<uint2*>(q + (size_t)r * (K / 2) + (size_t)kb * 8) = make_uint2(lo, hi);
+      if (MX)
+        *reinterpret_cast<uint4*>(q + (size_t)r * (K / 2) + (size_t)kb * 16) = c4;
+      else
+        *reinterpret_cast<uint2*>(q + (size_t)r * (K / 2) + (size_t)kb * 8) = make_uint2(c4.x, c4.y);
       if ((lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(sf_tiles + (((size_t)t * KS + ks) * 4 + kk) * 512 + (m & 31) * 16 +
+        *reinterpret_cast<uint32_t*>(sf_tiles + ((size_t)t * atoms_per_tile + (kb >> 2)) * 512 + (m & 31) * 16 +
                                      (m >> 5) * 4) = sw;
     }
   }
@@ -281,7 +372,7 @@ __global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
 moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
                                  int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
                                  uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, float gs_static,
-                                 cudaStream_t s, bool pdl) {
+                                 cudaStream_t s, bool pdl, bool mx) {
   if (K % 256 || G <= 0 || (dest && k + 1 > kQtMaxDest)) return MOE_ERR_UNSUPPORTED;
   if (src_rows == 0) return MOE_OK;
   moe_status st = cuda_ok(cudaMemsetAsync(sf_tiles, 0, sf_bytes, s));
@@ -290,7 +381,8 @@ moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const i
   const size_t smem = (size_t)2 * (G + 1) * sizeof(int);
   // after the memset the kernel is an ordinary stream successor (no programmatic launch)
   (void)pdl;
-  cudaError_t e = launch_ex(false, quantize_tiles_kernel, dim3(blocks), dim3(kQtWarps * 32), smem, s, x, src_rows, K,
+  cudaError_t e = launch_ex(false, mx ? quantize_tiles_kernel<true> : quantize_tiles_kernel<false>, dim3(blocks),
+                            dim3(kQtWarps * 32), smem, s, x, src_rows, K,
                             dest, k, shared_base, gofs, G, amax, q, sf_tiles, gs_out, gs_static);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
@@ -350,11 +442,10 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __rest
     const uint4 v = __ldg(s + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
+    for (int q = 0; q < 4; ++q) m = max(m, max(finite_mag(w[q] & 0x7fffu), finite_mag((w[q] >> 16) & 0x7fffu)));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (m > 0x7f80u) m = 0x7f80u;
   const int e = (int)(m >> 7);
   int sh = (m == 0) ? 0 : 141 - max(e, 1);
   sh = max(-113, min(sh, 126));
@@ -407,21 +498,12 @@ moe_status launch_swiglu(const float* gu, int rows, int I, uint16_t* h, cudaStre
 }
 
 // ---------------------------------------------------------------------------
-// out[t] = sum_j y[inv_perm[t*k + j]] (* topk_w[t, j]) + y[T*k + t], fp32 in
-// that fixed order, rounded once to bf16. One thread per 8 outputs (16-byte
-// loads and stores); a grid of (H/8/64) x T blocks of 64 threads.
-__global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict__ y,
-                                                     const int32_t* __restrict__ inv_perm,
-                                                     const float* __restrict__ topk_w, int shared, int T,
-                                                     int k, int H, uint16_t* __restrict__ out) {
-  pdl_wait();
-  const int t = blockIdx.y;
-  const int c8 = blockIdx.x * blockDim.x + threadIdx.x;  // chunk of 8 columns
-  if (c8 * 8 >= H) return;
+__device__ __forceinline__ void combine_token(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_perm,
+                                              const float* __restrict__ topk_w, const float* __restrict__ y_shared,
+                                              int k, int H, uint16_t* __restrict__ out, int t, int c8) {
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  const size_t P = (size_t)T * k;
   for (int j = 0; j < k; ++j) {
     const int row = __ldg(inv_perm + (size_t)t * k + j);
     if (row < 0) continue;
@@ -434,14 +516,12 @@ __global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict_
       acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u) * wt;
     }
   }
-  if (shared) {
-    const uint4 v = ldg_stream(y + (P + t) * H + (size_t)c8 * 8);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (y_shared != nullptr) {
+    const float4* ys = reinterpret_cast<const float4*>(y_shared + (size_t)t * H + (size_t)c8 * 8);
+    const float4 a = __ldg(ys), b = __ldg(ys + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += __uint_as_float(w[i] << 16);
-      acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
   }
   uint32_t o[4];
 #pragma unroll
@@ -450,13 +530,28 @@ __global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict_
   *reinterpret_cast<uint4*>(out + (size_t)t * H + (size_t)c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// out[t] = sum_j y[inv_perm[t*k + j]] (* topk_w[t, j]) + y_shared[t], fp32 in
+// that fixed order, rounded once to bf16 (routed rows bf16, the shared
+// expert's rows fp32). One thread per 8 outputs (16-byte loads and stores); a
+// grid of (H/8/64) x min(T, 65535) blocks of 64 threads, the y blocks
+// stepping over the tokens (grid.y is capped at 65535).
+__global__ void __launch_bounds__(64) combine_kernel(const uint16_t* __restrict__ y,
+                                                     const int32_t* __restrict__ inv_perm,
+                                                     const float* __restrict__ topk_w,
+                                                     const float* __restrict__ y_shared, int T, int k, int H,
+                                                     uint16_t* __restrict__ out) {
+  pdl_wait();
+  const int c8 = blockIdx.x * blockDim.x + threadIdx.x;  // chunk of 8 columns
+  if (c8 * 8 >= H) return;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) combine_token(y, inv_perm, topk_w, y_shared, k, H, out, t, c8);
+}
 moe_status launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
-                          int y_shared_rows, int T, int k, int H, uint16_t* out, cudaStream_t s, bool pdl) {
+                          const float* y_shared, int T, int k, int H, uint16_t* out, cudaStream_t s, bool pdl) {
   if (T == 0) return MOE_OK;
   const int chunks = H / 8;
-  dim3 grid((chunks + 63) / 64, T);
-  cudaError_t e = launch_ex(pdl, combine_kernel, grid, dim3(64), 0, s, y, inv_perm, topk_w, y_shared_rows, T, k,
-                            H, out);
+  dim3 grid((chunks + 63) / 64, T < 65535 ? T : 65535);
+  cudaError_t e = launch_ex(pdl, combine_kernel, grid, dim3(64), 0, s, y, inv_perm, topk_w, y_shared, T, k, H,
+                            out);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());

@@ -7,76 +7,9 @@
 // ([Permute-Experts-Unpermute]).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "route.cuh"
 
 namespace moe {
-
-// ---------------------------------------------------------------------------
-// One warp per token. Lane l holds logits l, l+32, l+64, ... in registers.
-// k rounds of a warp-wide argmax pick the experts by rank: a larger logit
-// wins, equal logits go to the lower expert index. The weights are
-// exp(l_j - l_max) / sum over the chosen j (fp32), i.e. the softmax
-// probabilities renormalised over the top k.
-template <int PER_LANE>
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, int token, int E, int k,
-                                            int32_t* __restrict__ ids, float* __restrict__ w,
-                                            int32_t* sids = nullptr, float* sw = nullptr) {
-  const int lane = threadIdx.x & 31;
-  const float* row = logits + (size_t)token * E;
-  float v[PER_LANE];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? __ldg(row + e) : 0.0f;
-    if (e >= E) taken |= 1u << i;
-  }
-  float my_val = 0.0f;
-  int my_id = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      if (!(taken & (1u << i))) {
-        // ascending index within a lane: strict '>' keeps the lower index on ties
-        if (bi == 0x7fffffff || v[i] > bv) {
-          bv = v[i];
-          bi = lane + 32 * i;
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      const bool other_valid = oi != 0x7fffffff;
-      const bool mine_valid = bi != 0x7fffffff;
-      if (other_valid && (!mine_valid || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi == 0x7fffffff) bi = 0;  // only reachable with NaN logits (outside the contract)
-    if ((bi & 31) == lane && bi < E) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_val = bv;
-      my_id = bi;
-    }
-  }
-  const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
-  float ex = lane < k ? expf(my_val - vmax) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane < k) {
-    ids[(size_t)token * k + lane] = my_id;
-    w[(size_t)token * k + lane] = ex / sum;
-    if (sids != nullptr) {  // shared-memory copies for the fused single-CTA kernel
-      sids[token * k + lane] = my_id;
-      sw[token * k + lane] = ex / sum;
-    }
-  }
-}
 
 template <int PER_LANE>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
@@ -125,18 +58,31 @@ moe_status launch_route_topk(const float* logits, int T, int E, int k, int32_t* 
 
 constexpr int kPermChunk = 4096;  // pairs per chunk in the multi-CTA path
 
+// Expert parallelism ("Serving Solar Open 2 on DGX Spark", "Adding Expert
+// Parallelism to b12x": each node holds a contiguous shard of the experts,
+// global ids are remapped to shard-local ones and out-of-shard pairs are
+// filtered out). A global id in [lo, lo + n) maps to local group id - lo; a
+// valid id of another shard gives -1 (the pair is dropped without an error:
+// another shard computes it); an id outside [0, E_global) gives -2 (an error).
+// Without sharding lo = 0 and n = E_global.
+__device__ __forceinline__ int shard_local(int id, int lo, int n, int E_global) {
+  if (id < 0 || id >= E_global) return -2;
+  const int e = id - lo;
+  return (e >= 0 && e < n) ? e : -1;
+}
+
 __device__ __forceinline__ void scatter_warp(const int32_t* __restrict__ ids, int p0, int p1, int E,
                                              int* cursor /* smem [E] */, int32_t* perm,
-                                             int32_t* inv_perm, int* status, const int32_t* lids = nullptr,
-                                             int32_t* lperm = nullptr) {
+                                             int32_t* inv_perm, int* status, int lo, int E_global,
+                                             const int32_t* lids = nullptr, int32_t* lperm = nullptr) {
   const int lane = threadIdx.x & 31;
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     const bool in = p < p1;
     // ids written earlier in the same kernel: the shared copy, else an L2 load
-    int e = in ? (lids ? lids[p] : __ldcg(ids + p)) : -1;
-    const bool valid = in && e >= 0 && e < E;
-    if (in && !valid) set_status(status, MOE_ERR_DEVICE);
+    const int e = in ? shard_local(lids ? lids[p] : __ldcg(ids + p), lo, E, E_global) : -1;
+    const bool valid = in && e >= 0;
+    if (in && e == -2) set_status(status, MOE_ERR_DEVICE);
     const int key = valid ? e : -1 - lane;  // invalid lanes never match each other
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     const unsigned lt = (1u << lane) - 1u;
@@ -158,28 +104,41 @@ __device__ __forceinline__ void scatter_warp(const int32_t* __restrict__ ids, in
 }
 
 // Extra per-row outputs for the fused forward: the A-row (token) of each
-// sorted row and its routing weight; shared rows follow the routed ones.
+// sorted row and its routing weight. The Pu routed rows that were kept (all
+// P = T*k of them unless a shard or bad ids dropped some) come first, then
+// the T shared rows at [Pu, Pu + T); rows past Pu + T are unused.
 struct RowInfoOut {
   int32_t* row_token;    // [P + T] or nullptr
   float* row_weight;     // [P + T] or nullptr
   const float* topk_w;   // [P]
   int k, T;
-  int32_t* gofs;         // [E+2] or nullptr: offsets[0..E-1], then P, then P + T
+  int32_t* gofs;         // [E+2] or nullptr: offsets[0..E] (offsets[E] = Pu), then Pu + T
 };
 
-__device__ void write_row_info(const RowInfoOut& ri, const int32_t* perm, int P, const int32_t* lperm = nullptr,
-                               const float* lw = nullptr) {
+__device__ __forceinline__ void row_info_one(const RowInfoOut& ri, int r, int Pu, int p, float wp) {
+  if (r < Pu) {
+    const bool ok = p >= 0;
+    ri.row_token[r] = ok ? p / ri.k : 0;
+    ri.row_weight[r] = ok ? wp : 0.0f;
+  } else if (r < Pu + ri.T) {
+    ri.row_token[r] = r - Pu;
+    ri.row_weight[r] = 1.0f;
+  } else {
+    ri.row_token[r] = 0;
+    ri.row_weight[r] = 0.0f;
+  }
+}
+
+__device__ void write_row_info(const RowInfoOut& ri, const int32_t* perm, int P, int Pu,
+                               const int32_t* lperm = nullptr, const float* lw = nullptr) {
   if (ri.row_token == nullptr) return;
   for (int r = threadIdx.x; r < P + ri.T; r += blockDim.x) {
-    if (r < P) {
-      const int p = lperm ? lperm[r] : perm[r];
-      const bool ok = p >= 0 && p < P;
-      ri.row_token[r] = ok ? p / ri.k : 0;
-      ri.row_weight[r] = ok ? (lw ? lw[p] : ri.topk_w[p]) : 0.0f;
-    } else {
-      ri.row_token[r] = r - P;
-      ri.row_weight[r] = 1.0f;
+    int p = -1;
+    if (r < Pu) {
+      p = lperm ? lperm[r] : perm[r];
+      if (p < 0 || p >= P) p = -1;
     }
+    row_info_one(ri, r, Pu, p, p >= 0 ? (lw ? lw[p] : ri.topk_w[p]) : 0.0f);
   }
 }
 
@@ -226,8 +185,8 @@ __device__ void block_exclusive_scan(int* data, int n, int* tmp /* smem [32] */)
 
 __device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int E, int32_t* counts,
                                     int32_t* offsets, int32_t* perm, int32_t* inv_perm, int* status,
-                                    const RowInfoOut& ri, const int32_t* lids = nullptr, const float* lw = nullptr,
-                                    int32_t* lperm = nullptr) {
+                                    const RowInfoOut& ri, int lo, int E_global, const int32_t* lids = nullptr,
+                                    const float* lw = nullptr, int32_t* lperm = nullptr) {
   extern __shared__ int smem[];
   int* cnt = smem;            // [E]
   int* cursor = smem + E;     // [E]
@@ -240,8 +199,8 @@ __device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int 
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
     // ids written earlier in the same kernel: the shared copy, else an L2 load
-    const int e = lids ? lids[p] : __ldcg(ids + p);
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    const int e = shard_local(lids ? lids[p] : __ldcg(ids + p), lo, E, E_global);
+    if (e >= 0) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -254,36 +213,39 @@ __device__ void permute_single_body(const int32_t* __restrict__ ids, int P, int 
     offsets[e] = cursor[e];
     if (ri.gofs) ri.gofs[e] = cursor[e];
   }
+  const int Pu = cursor[E - 1] + cnt[E - 1];  // routed pairs kept (this shard's, valid ids)
   if (threadIdx.x == 0) {
-    offsets[E] = cursor[E - 1] + cnt[E - 1];
+    offsets[E] = Pu;
     if (ri.gofs) {
-      ri.gofs[E] = P;
-      ri.gofs[E + 1] = P + ri.T;
+      ri.gofs[E] = Pu;
+      ri.gofs[E + 1] = Pu + ri.T;
     }
   }
   __syncthreads();
-  if (threadIdx.x < 32) scatter_warp(ids, 0, P, E, cursor, perm, inv_perm, status, lids, lperm);
+  if (threadIdx.x < 32) scatter_warp(ids, 0, P, E, cursor, perm, inv_perm, status, lo, E_global, lids, lperm);
   __syncthreads();
   __threadfence_block();
-  write_row_info(ri, perm, P, lperm, lw);
+  write_row_info(ri, perm, P, Pu, lperm, lw);
 }
 
 __global__ void __launch_bounds__(1024) permute_single_kernel(const int32_t* __restrict__ ids, int P,
                                                               int E, int32_t* counts, int32_t* offsets,
                                                               int32_t* perm, int32_t* inv_perm,
-                                                              int* status, RowInfoOut ri) {
+                                                              int* status, RowInfoOut ri, int lo, int E_global) {
   pdl_wait();
-  permute_single_body(ids, P, E, counts, offsets, perm, inv_perm, status, ri);
+  permute_single_body(ids, P, E, counts, offsets, perm, inv_perm, status, ri, lo, E_global);
 }
 
 // Small batches: route and permute in one CTA (one launch). Warp w routes
 // tokens w, w + 32, ...; the permutation starts once every id is written.
+// E_global experts are routed; the permutation groups the pairs of the E
+// experts [lo, lo + E) of this shard (E = E_global, lo = 0 without sharding).
 template <int PER_LANE>
 __global__ void __launch_bounds__(1024) route_permute_small_kernel(const float* __restrict__ logits, int T,
-                                                                   int E, int k, int32_t* ids, float* w,
+                                                                   int E_global, int k, int32_t* ids, float* w,
                                                                    int32_t* counts, int32_t* offsets,
                                                                    int32_t* perm, int32_t* inv_perm,
-                                                                   int* status, RowInfoOut ri) {
+                                                                   int* status, RowInfoOut ri, int lo, int E) {
   extern __shared__ int smem_rp[];
   const int P = T * k;
   // after the permutation's own shared arrays ([2E + 32] ints): ids, weights, perm of the pairs
@@ -291,23 +253,23 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(const float* 
   float* sw = reinterpret_cast<float*>(sids + P);
   int32_t* sperm = reinterpret_cast<int32_t*>(sw + P);
   for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5)
-    route_token<PER_LANE>(logits, t, E, k, ids, w, sids, sw);
+    route_token<PER_LANE>(logits, t, E_global, k, ids, w, sids, sw);
   __syncthreads();
-  permute_single_body(ids, P, E, counts, offsets, perm, inv_perm, status, ri, sids, sw, sperm);
+  permute_single_body(ids, P, E, counts, offsets, perm, inv_perm, status, ri, lo, E_global, sids, sw, sperm);
 }
 
 moe_status launch_route_permute_small(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                                       int* status, int32_t* row_token, float* row_weight, int32_t* gofs,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, int shard_lo, int shard_n) {
   RowInfoOut ri{row_token, row_weight, w, k, T, gofs};
-  const size_t smem = (2 * (size_t)E + 32 + 3 * (size_t)T * k) * sizeof(int);
+  const size_t smem = (2 * (size_t)shard_n + 32 + 3 * (size_t)T * k) * sizeof(int);
   if (smem > 48 * 1024) return MOE_ERR_UNSUPPORTED;
   const int per = (E + 31) / 32;
 #define MOE_RP_CASE(PL)                                                                                  \
   if (per <= PL) {                                                                                       \
     route_permute_small_kernel<PL><<<1, 1024, smem, s>>>(logits, T, E, k, ids, w, counts, offsets, perm, \
-                                                         inv_perm, status, ri);                          \
+                                                         inv_perm, status, ri, shard_lo, shard_n);       \
     count_launches(1);                                                                                   \
     return cuda_ok(cudaGetLastError());                                                                  \
   }
@@ -324,7 +286,7 @@ moe_status launch_route_permute_small(const float* logits, int T, int E, int k, 
 
 __global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                              int32_t* chunk_hist /* [nchunks][E] */,
-                                                             int32_t* perm) {
+                                                             int32_t* perm, int lo, int E_global) {
   pdl_wait();
   extern __shared__ int cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
@@ -332,9 +294,9 @@ __global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __re
   const int p0 = blockIdx.x * kPermChunk;
   const int p1 = min(P, p0 + kPermChunk);
   for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    const int e = __ldg(ids + p);
+    const int e = shard_local(__ldg(ids + p), lo, E, E_global);
     perm[p] = -1;
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    if (e >= 0) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + e] = cnt[e];
@@ -367,10 +329,11 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* chunk_hist,
     for (int b = 0; b < nchunks; ++b) chunk_hist[(size_t)b * E + e] += tot[e];
   }
   if (threadIdx.x == 0) {
-    offsets[E] = tot[E - 1] + last;
+    const int Pu = tot[E - 1] + last;   // routed pairs kept; the shared rows follow them
+    offsets[E] = Pu;
     if (gofs) {
-      gofs[E] = P;
-      gofs[E + 1] = P + T;
+      gofs[E] = Pu;
+      gofs[E + 1] = Pu + T;
     }
   }
 }
@@ -384,7 +347,7 @@ constexpr int kScatterWarps = 8;
 __global__ void __launch_bounds__(kScatterWarps * 32) permute_scatter_kernel(const int32_t* __restrict__ ids, int P,
                                                                             int E, const int32_t* chunk_base,
                                                                             int32_t* perm, int32_t* inv_perm,
-                                                                            int* status) {
+                                                                            int* status, int lo, int E_global) {
   pdl_wait();
   extern __shared__ int cursor[];  // [kScatterWarps][E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -395,8 +358,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32) permute_scatter_kernel(con
   constexpr int kSub = kPermChunk / kScatterWarps;
   const int q0 = min(p1, p0 + warp * kSub), q1 = min(p1, q0 + kSub);
   for (int p = q0 + lane; p < q1; p += 32) {
-    const int e = __ldg(ids + p);
-    if (e >= 0 && e < E) atomicAdd(&cursor[warp * E + e], 1);
+    const int e = shard_local(__ldg(ids + p), lo, E, E_global);
+    if (e >= 0) atomicAdd(&cursor[warp * E + e], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -408,23 +371,18 @@ __global__ void __launch_bounds__(kScatterWarps * 32) permute_scatter_kernel(con
     }
   }
   __syncthreads();
-  if (q0 < q1) scatter_warp(ids, q0, q1, E, cursor + warp * E, perm, inv_perm, status);
+  if (q0 < q1) scatter_warp(ids, q0, q1, E, cursor + warp * E, perm, inv_perm, status, lo, E_global);
 }
 
-__global__ void row_info_kernel(const int32_t* perm, int P, RowInfoOut ri) {
+__global__ void row_info_kernel(const int32_t* perm, int P, const int32_t* offsets_end, RowInfoOut ri) {
   pdl_wait();
-  // grid-stride version of write_row_info
+  // grid-stride version of write_row_info; the kept routed rows end at offsets[E]
+  const int Pu = __ldcg(offsets_end);
   const int n = P + ri.T;
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
-    if (r < P) {
-      const int p = perm[r];
-      const bool ok = p >= 0 && p < P;
-      ri.row_token[r] = ok ? p / ri.k : 0;
-      ri.row_weight[r] = ok ? ri.topk_w[p] : 0.0f;
-    } else {
-      ri.row_token[r] = r - P;
-      ri.row_weight[r] = 1.0f;
-    }
+    int p = r < Pu ? perm[r] : -1;
+    if (p >= P) p = -1;
+    row_info_one(ri, r, Pu, p, p >= 0 ? ri.topk_w[p] : 0.0f);
   }
 }
 
@@ -438,13 +396,14 @@ size_t permute_scratch_bytes(int T, int k, int E) {
 moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* inv_perm, int* status, void* scratch,
                           int32_t* row_token, float* row_weight, const float* topk_w, int32_t* gofs,
-                          cudaStream_t s, bool pdl) {
+                          cudaStream_t s, bool pdl, int shard_lo, int E_global) {
   const int P = T * k;
+  if (E_global <= 0) E_global = E;
   RowInfoOut ri{row_token, row_weight, topk_w, k, T, gofs};
   if (P <= kPermSingleMax) {
     const size_t smem = (2 * (size_t)E + 32) * sizeof(int);
     cudaError_t e = launch_ex(pdl, permute_single_kernel, dim3(1), dim3(1024), smem, s, ids, P, E, counts,
-                              offsets, perm, inv_perm, status, ri);
+                              offsets, perm, inv_perm, status, ri, shard_lo, E_global);
     if (e != cudaSuccess) return cuda_ok(e);
     count_launches(1);
     return cuda_ok(cudaGetLastError());
@@ -452,7 +411,7 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
   const int nchunks = (P + kPermChunk - 1) / kPermChunk;
   int32_t* hist = static_cast<int32_t*>(scratch);
   cudaError_t e = launch_ex(pdl, permute_count_kernel, dim3(nchunks), dim3(1024), (size_t)E * sizeof(int), s,
-                            ids, P, E, hist, perm);
+                            ids, P, E, hist, perm, shard_lo, E_global);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   e = launch_ex(pdl, permute_scan_kernel, dim3(1), dim3(1024), ((size_t)E + 32) * sizeof(int), s, hist,
@@ -460,12 +419,14 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   e = launch_ex(pdl, permute_scatter_kernel, dim3(nchunks), dim3(kScatterWarps * 32),
-                (size_t)kScatterWarps * E * sizeof(int), s, ids, P, E, (const int32_t*)hist, perm, inv_perm, status);
+                (size_t)kScatterWarps * E * sizeof(int), s, ids, P, E, (const int32_t*)hist, perm, inv_perm, status,
+                shard_lo, E_global);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   if (row_token != nullptr) {
     const int n = P + T;
-    e = launch_ex(pdl, row_info_kernel, dim3((n + 255) / 256), dim3(256), 0, s, (const int32_t*)perm, P, ri);
+    e = launch_ex(pdl, row_info_kernel, dim3((n + 255) / 256), dim3(256), 0, s, (const int32_t*)perm, P,
+                  (const int32_t*)(offsets + E), ri);
     if (e != cudaSuccess) return cuda_ok(e);
     count_launches(1);
   }

@@ -172,6 +172,20 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Block-scaled FP4 x FP4 MMA with UE8M0 (power-of-two) scales, one per 32
+// elements (kind::mxf4, scale_vec::2X: MXFP4); each 32-bit scale column
+// holds four consecutive scales of a row, and the instruction descriptor's
+// scale-factor IDs pick the byte pair (0 or 2) this K=64 MMA uses.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // SMEM (32 rows x 16 bytes) -> TMEM (32 lanes x 4 columns), replicated into
 // all four lane quarters.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
@@ -223,6 +237,14 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16) {
 // scales, K-major, M x N, dense K = 64.
 __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (0u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4 block-scaled: A and B e2m1, UE8M0
+// scales (bit 23), K-major, M x N, dense K = 64; sf_id (0 or 2) selects the
+// scale bytes of A (bits 29-30) and B (bits 4-5) within their 32-bit columns.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
 }
 
 }  // namespace tc

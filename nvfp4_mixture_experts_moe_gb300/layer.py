@@ -1,7 +1,8 @@
 """Device-side setup of one MoE layer through the C ABI.
 
 ``Nvfp4MoeLayer`` quantises bf16 weight matrices to NVFP4 with the
-library's own quantiser (``moe_nvfp4_quantize``) or takes pre-quantised
+library's own quantiser (``moe_nvfp4_quantize``; MXFP4 layers with
+``moe_mxfp4_quantize``) or takes pre-quantised
 checkpoint matrices (``import_expert``: the stored global scale is converted
 with ``moe_import_global_scale``), converts them into the kernels' tile
 layout (``moe_nvfp4_prepare_weights``), keeps them resident in device memory
@@ -33,19 +34,37 @@ def quantize_bf16(x, device="cuda"):
     return q, sf, gs
 
 
+def quantize_mx(x, device="cuda"):
+    """bf16 ``[rows, K]`` on the device -> MXFP4 (packed codes, E8M0 scales)."""
+    rows, K = x.shape
+    q = torch.empty(rows, K // 2, dtype=torch.uint8, device=device)
+    sf = torch.empty(rows, K // 32, dtype=torch.uint8, device=device)
+    B.moe_mxfp4_quantize(x, rows, K, q, sf)
+    return q, sf
+
+
 class Nvfp4MoeLayer:
     """NVFP4 weights of E routed experts (+ optional shared expert) on one GPU."""
 
-    def __init__(self, T, H, I, E, k, mode=B.MOE_W4A16, I_shared=None, shared=True, device="cuda"):
+    def __init__(self, T, H, I, E, k, mode=B.MOE_W4A16, I_shared=None, shared=True, device="cuda",
+                 expert_offset=0, local_experts=None):
+        """``expert_offset`` / ``local_experts``: expert parallelism, this layer
+        holds (and computes) only the experts ``[expert_offset, expert_offset +
+        local_experts)`` of the E the router ranks; its output is then the
+        shard's partial output (see ``ep``)."""
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         self.I_shared = I if I_shared is None else I_shared
         self.mode = mode
         self.shared = shared
         self.device = device
+        self.expert_offset = expert_offset
+        self.local_experts = E if local_experts is None else local_experts
+        if not (0 <= expert_offset and expert_offset + self.local_experts <= E):
+            raise ValueError("expert shard outside [0, E)")
         self.s13 = B.moe_prepare_size(2 * I, H, mode, 1)
         self.s2 = B.moe_prepare_size(H, I, mode, 0)
-        self.w13 = _empty_bytes(E * self.s13, device)
-        self.w2 = _empty_bytes(E * self.s2, device)
+        self.w13 = _empty_bytes(self.local_experts * self.s13, device)
+        self.w2 = _empty_bytes(self.local_experts * self.s2, device)
         if shared:
             self.w13_s = _empty_bytes(B.moe_prepare_size(2 * self.I_shared, H, mode, 1), device)
             self.w2_s = _empty_bytes(B.moe_prepare_size(H, self.I_shared, mode, 0), device)
@@ -58,14 +77,24 @@ class Nvfp4MoeLayer:
     def _slot(self, expert, which):
         if expert == self.E:
             return self.w13_s if which == 13 else self.w2_s
+        e = expert - self.expert_offset  # this shard's block of the (global) expert
+        if not 0 <= e < self.local_experts:
+            raise ValueError(f"expert {expert} is not in this layer's shard")
         if which == 13:
-            return self.w13[expert * self.s13:(expert + 1) * self.s13]
-        return self.w2[expert * self.s2:(expert + 1) * self.s2]
+            return self.w13[e * self.s13:(e + 1) * self.s13]
+        return self.w2[e * self.s2:(e + 1) * self.s2]
 
     def set_expert(self, expert, gate, up, down):
         """bf16 gate ``[I, H]``, up ``[I, H]``, down ``[H, I]`` (any device); expert E = shared."""
         dev = self.device
         gate, up, down = (t.to(dev, torch.bfloat16).contiguous() for t in (gate, up, down))
+        if self.mode == B.MOE_MXFP4:  # E8M0 scales per 32, no global scale
+            (qg, sg), (qu, su), (qd, sd) = (quantize_mx(m, dev) for m in (gate, up, down))
+            inter = gate.shape[0]
+            B.moe_nvfp4_prepare_weights(torch.cat([qg, qu]), torch.cat([sg, su]), None, 2 * inter, self.H,
+                                        self.mode, 1, self._slot(expert, 13))
+            B.moe_nvfp4_prepare_weights(qd, sd, None, self.H, inter, self.mode, 0, self._slot(expert, 2))
+            return (qg, sg), (qu, su), (qd, sd)
         qg, sg, gg = quantize_bf16(gate, dev)
         qu, su, gu = quantize_bf16(up, dev)
         qd, sd, gd = quantize_bf16(down, dev)
@@ -117,6 +146,9 @@ class Nvfp4MoeLayer:
         d.w2_shared = self.w2_s.data_ptr() if self.shared else None
         d.w_router = None if self.w_router is None else self.w_router.data_ptr()
         d.x_global_scale, d.h_global_scale = self.x_gs, self.h_gs
+        sharded = self.local_experts != self.E
+        d.expert_offset = self.expert_offset if sharded else 0
+        d.local_experts = self.local_experts if sharded else 0
         return d
 
     def workspace(self, T=None):

@@ -24,7 +24,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import nvfp4
+from . import mxfp4, nvfp4
 
 F32 = np.float32
 
@@ -125,6 +125,23 @@ class QuantWeight:
         return nvfp4.dequantize(self.codes, self.sf, self.gs)
 
 
+class QuantWeightMX:
+    """One MXFP4 weight matrix ``[N, K]``: unpacked e2m1 codes and E8M0 scale
+    codes (one per 32 along K); no per-tensor global scale ("vLLM on the
+    NVIDIA DGX Spark", section 6.4 "NVFP4 vs MXFP4")."""
+
+    def __init__(self, codes, sc):
+        self.codes = np.asarray(codes, dtype=np.uint8)
+        self.sc = np.asarray(sc, dtype=np.uint8)
+
+    @classmethod
+    def from_dense(cls, w):
+        return cls(*mxfp4.quantize(np.asarray(w, dtype=F32)))
+
+    def dequantize(self):
+        return mxfp4.dequantize(self.codes, self.sc)
+
+
 def gate_up_swiglu(x_rows, gate, up):
     """First GEMM pair and SwiGLU on a block of rows: ``h = silu(x Wg^T) * (x Wu^T)``.
 
@@ -159,7 +176,8 @@ def router_logits(x, w_router):
     return x @ w.T
 
 
-def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=None, h_gs=None):
+def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=None, h_gs=None,
+          experts_range=None):
     """The whole layer for ``T`` tokens, float64.
 
     ``x`` ``[T, H]`` (bf16 values), ``logits`` ``[T, E]`` fp32, ``experts`` a
@@ -173,11 +191,21 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=
     scale) and dequantised first; ``h`` is rounded to bf16, quantised over all
     rows with one global scale, and dequantised before the down GEMM. The two
     W4A4 global scales are dynamic (from the tensors' amax) unless ``x_gs`` /
-    ``h_gs`` give static calibrated ones (quant convention).
+    ``h_gs`` give static calibrated ones (quant convention). MXFP4 (the
+    experts are ``QuantWeightMX``): as W4A4 with MXFP4 for x and h (E8M0
+    scales per 32, no global scale).
+    ``experts_range=(lo, hi)`` computes one shard of expert parallelism
+    ("Serving Solar Open 2 on DGX Spark", "Adding Expert Parallelism to b12x":
+    each node holds a contiguous shard of the experts and filters out the
+    pairs of other shards): the router still ranks all E experts, only the
+    pairs routed to experts lo..hi-1 are computed (W4A4: the global scale of h
+    is taken over those rows and the shared rows), and the result is that
+    shard's partial output (plus the shared expert when ``shared`` is given).
     Pinned by: a dense formulation (every expert on every token, weighted by a
     T x E routing matrix) on tiny sizes, the identical-experts invariant, the
-    one-expert dense reduction, and (static scales) the dynamic result when
-    the static scales equal the dynamic ones (tests).
+    one-expert dense reduction, (static scales) the dynamic result when the
+    static scales equal the dynamic ones, and (shards) the shards' partial
+    outputs summing to the whole layer (tests).
     """
     x = np.asarray(x, dtype=np.float64)
     T, H = x.shape
@@ -190,13 +218,22 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=
         xq, xsf, xgs = nvfp4.quantize(x.astype(F32), gs=x_gs)
         parts.update(xq=xq, xsf=xsf, xgs=xgs)
         x_in = nvfp4.dequantize(xq, xsf, xgs)
+    elif mode == "mxfp4":
+        xq, xsc = mxfp4.quantize(x.astype(F32))
+        parts.update(xq=xq, xsc=xsc)
+        x_in = mxfp4.dequantize(xq, xsc)
     elif mode == "w4a16":
         x_in = x
     else:
         raise ValueError(mode)
+    lo, hi = (0, E) if experts_range is None else experts_range
+    if not 0 <= lo <= hi <= E:
+        raise ValueError("expert range outside [0, E]")
     # Rows in the order the layer lays them out: routed pairs grouped by
-    # expert (sorted order), then the shared expert's rows in token order.
-    groups = [(experts[e], perm[offsets[e]:offsets[e + 1]] // k) for e in range(E)]
+    # expert (sorted order; this shard's experts only), then the shared
+    # expert's rows in token order.
+    groups = [(experts[e], perm[offsets[e]:offsets[e + 1]] // k) for e in range(lo, hi)]
+    E_local = hi - lo
     if shared is not None:
         groups.append((shared, np.arange(T)))
     hs = [gate_up_swiglu(x_in[toks], gate, up) for (gate, up, _), toks in groups]
@@ -207,18 +244,74 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=
         hq, hsf, hgs = nvfp4.quantize(allh_bf, gs=h_gs)
         parts.update(h_bf16=allh_bf, hq=hq, hsf=hsf, hgs=hgs)
         hs = np.split(nvfp4.dequantize(hq, hsf, hgs), np.cumsum(sizes)[:-1], axis=0)
+    if mode == "mxfp4":
+        # h rounded to bf16, then every row quantised on its own (block scales
+        # per 32; MXFP4 has no per-tensor scale)
+        q = [mxfp4.quantize(bf16_round(h)) if h.shape[0] else (h, None) for h in hs]
+        hs = [mxfp4.dequantize(c, sc) if sc is not None else h for (c, sc), h in zip(q, hs)]
     ys = [down_proj(h, trip[2]) for h, (trip, _) in zip(hs, groups)]
-    y_routed = np.concatenate(ys[:E], axis=0) if E else np.zeros((0, H))
+    y_routed = np.concatenate(ys[:E_local], axis=0) if E_local else np.zeros((0, H))
     out = np.zeros((T, H), dtype=np.float64)
     for t in range(T):
         for j in range(k):
-            out[t] += np.float64(w[t, j]) * y_routed[inv_perm[t * k + j]]
+            if lo <= ids[t, j] < hi:
+                out[t] += np.float64(w[t, j]) * y_routed[inv_perm[t * k + j] - offsets[lo]]
     if shared is not None:
-        out += ys[E]
+        out += ys[E_local]
     parts.update(h=hs, y_routed=y_routed)
     if return_parts:
         return out, parts
     return out
+
+
+def _bf16_neighbour(h):
+    """The bf16 value adjacent to bf16_round(h) on the other side of h (h
+    float64, finite): with bf16_round(h) it brackets h."""
+    b0 = bf16_round(h).astype(np.float64)
+    bits = b0.astype(np.float32).view(np.uint32).astype(np.int64)
+    # one bf16 ulp away from zero is +0x10000 in the fp32 bit pattern of the magnitude
+    away = ((h > b0) == (b0 >= 0)) | (b0 == 0)
+    nb = np.where(away, bits + 0x10000, bits - 0x10000)
+    nb = np.where((b0 == 0) & (h < 0), (np.uint32(0x80000000).astype(np.int64) | 0x10000), nb)
+    return nb.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def requant_flip_bound(h_exact, gs, down_abs, rel_delta=2.0 ** -14):
+    """How much FP4 re-quantisation of h can move one row's down projection
+    when h is known only to within ``rel_delta`` (relative) of ``h_exact``.
+
+    The layer rounds h to bf16 and quantises it (W4A4). A computation of h
+    that differs from ``h_exact`` by less than ``rel_delta * |h|`` (plus a
+    floor of ``2**-20`` times the row's largest |h|) can round to either bf16
+    value next to ``h_exact`` when ``h_exact`` lies that close to the midpoint
+    between them. For every such element the block is quantised with each of
+    the two values (the other elements as the oracle has them, global scale
+    ``gs``); where the dequantised block differs, the absolute differences are
+    added up element by element. ``down_abs`` is ``|Wd|``, the element-wise
+    absolute value of the dequantised down matrix ``[H, I]``. Returns
+    ``down_abs @ sum_of_differences`` (the largest change of each output
+    element of this row, by the triangle inequality), float64 ``[H]``.
+    Pinned by: zero for a row far from every bf16 midpoint; an element put on
+    a midpoint that straddles an e2m1 decision gives exactly one step times
+    |Wd column| (tests).
+    """
+    h = np.asarray(h_exact, dtype=np.float64).reshape(1, -1)
+    b0 = bf16_round(h).astype(np.float64)
+    b1 = _bf16_neighbour(h)
+    mid = 0.5 * (b0 + b1)
+    tol = rel_delta * np.abs(h) + 2.0 ** -20 * np.abs(h).max()
+    amb = np.abs(h - mid) <= tol
+    diff = np.zeros_like(h)
+    if amb.any():
+        base = nvfp4.dequantize(*nvfp4.quantize(b0.astype(F32), gs=gs)[:2], gs)
+        for i in np.nonzero(amb[0])[0]:
+            alt = b0.copy()
+            alt[0, i] = b1[0, i]
+            blk = slice(16 * (i // 16), 16 * (i // 16) + 16)
+            q = nvfp4.quantize(alt[:, blk].astype(F32), gs=gs)
+            d = nvfp4.dequantize(q[0], q[1], gs)
+            diff[0, blk] += np.abs(d - base[:, blk])[0]
+    return down_abs @ diff[0]
 
 
 def token_outputs_w4a16(x_tokens, ids, w, expert_weights, shared):

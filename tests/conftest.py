@@ -27,3 +27,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # the achieved output errors of every parity check of this session
+    try:
+        from tests.tolerance import ACHIEVED
+    except ImportError:  # pragma: no cover
+        return
+    if not ACHIEVED:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "achieved output errors (bar: max abs <= max(2e-2, 2^-7 |ref|), rel Frobenius <= 1e-2)")
+    for what, err, rel, amax in ACHIEVED:
+        tr.write_line(f"{what:48s} max abs {err:.3e}  rel fro {rel:.3e}  max |ref| {amax:.3g}")

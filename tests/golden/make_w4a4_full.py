@@ -12,7 +12,14 @@ generators in ``synthetic_inputs``; nothing from the CUDA path), and stores:
 * ``amax_h``, ``gs_h``: the amax of the bf16-rounded h over all rows and its
   global scale;
 * ``tokens``: 64 token indices spread over the batch, with their routing
-  (``ids``, ``w``) and their float64 layer outputs ``out`` stored as float32.
+  (``ids``, ``w``) and their float64 layer outputs ``out`` stored as float32;
+* ``flip``: per output element of those tokens, how far FP4 re-quantisation
+  of h can move it when h is computed to within 2^-14 (relative) of the
+  oracle's float64 value (``oracle.moe.requant_flip_bound``): a GPU computes
+  h in fp32 in another summation order, so an h element lying that close to
+  a bf16 rounding midpoint may round the other way, and where the two bf16
+  values quantise to different FP4 codes (or block scales) the token's whole
+  output row moves by one FP4 step times the down-projection column.
 
 Given ``gs_x`` and ``gs_h`` every token's output depends on that token alone,
 so the stored rows are exactly the rows of ``oracle.moe.layer(..., mode="w4a4")``
@@ -79,16 +86,17 @@ def golden_rows(cfg, tokens, threads=8, log=print):
         sampled = {}
         for c0 in range(0, len(toks), 2048):  # bounded memory for the shared expert's 16384 rows
             tk = toks[c0:c0 + 2048]
-            h = omoe.bf16_round(omoe.gate_up_swiglu(x_deq[tk], gq, uq))
+            h_exact = omoe.gate_up_swiglu(x_deq[tk], gq, uq)
+            h = omoe.bf16_round(h_exact)
             if h.size:
                 amax = max(amax, float(np.max(np.abs(h))))
             for i, t in enumerate(tk):
                 if int(t) in want:
-                    sampled[int(t)] = h[i].copy()
+                    sampled[int(t)] = (h[i].copy(), h_exact[i].copy())
         return e, amax, sampled, (dq if sampled else None)
 
     amax_h = 0.0
-    h_rows = {}        # (token, expert) -> bf16-rounded h row
+    h_rows = {}        # (token, expert) -> (bf16-rounded h row, float64 h row)
     downs = {}
     done = 0
     with ThreadPoolExecutor(threads) as ex:
@@ -105,26 +113,37 @@ def golden_rows(cfg, tokens, threads=8, log=print):
     log(f"gate/up + SwiGLU over all rows: {time.time() - t0:.0f} s; amax_h = {amax_h!r}, gs_h = {gs_h!r}")
 
     def y_of(t, e):
-        h = h_rows[(t, e)][None, :].astype(np.float32)
+        h = h_rows[(t, e)][0][None, :].astype(np.float32)
         hq, hsf, _ = onv.quantize(h, gs=gs_h)
         return omoe.down_proj(onv.dequantize(hq, hsf, gs_h), downs[e])[0]
 
+    down_abs = {}
+
+    def flip_of(t, e):
+        if e not in down_abs:
+            down_abs[e] = np.abs(downs[e].dequantize())
+        return omoe.requant_flip_bound(h_rows[(t, e)][1], gs_h, down_abs[e])
+
     out = np.zeros((len(tokens), H), dtype=np.float64)
+    flip = np.zeros((len(tokens), H), dtype=np.float64)
     for i, t in enumerate(tokens):
         for j in range(k):
             out[i] += np.float64(w[t, j]) * y_of(int(t), int(ids[t, j]))
+            flip[i] += np.float64(w[t, j]) * flip_of(int(t), int(ids[t, j]))
         out[i] += y_of(int(t), E)
-    return out, gs_x, np.float32(amax_h), gs_h, ids, w
+        flip[i] += flip_of(int(t), E)
+    return out, gs_x, np.float32(amax_h), gs_h, ids, w, flip
 
 
 def main(threads=8):
     cfg = si.CONFIGS["w4a4"]
     t0 = time.time()
     tokens = sample_tokens(cfg.T, N_TOKENS)
-    out, gs_x, amax_h, gs_h, ids, w = golden_rows(cfg, tokens, threads,
-                                                  log=lambda m: print(m, flush=True))
+    out, gs_x, amax_h, gs_h, ids, w, flip = golden_rows(cfg, tokens, threads,
+                                                        log=lambda m: print(m, flush=True))
     np.savez_compressed(OUT, tokens=tokens, out=out.astype(np.float32), ids=ids[tokens], w=w[tokens],
-                        gs_x=np.float32(gs_x), amax_h=np.float32(amax_h), gs_h=np.float32(gs_h))
+                        gs_x=np.float32(gs_x), amax_h=np.float32(amax_h), gs_h=np.float32(gs_h),
+                        flip=flip.astype(np.float32))
     print(f"wrote {OUT} ({os.path.getsize(OUT)} bytes) in {time.time() - t0:.0f} s")
 
 

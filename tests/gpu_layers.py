@@ -16,11 +16,11 @@ def device_layer(name, T=None):
     key or a LayerConfig) prepared on the device."""
     import __graft_entry__
     __graft_entry__.build()
-    from nvfp4_mixture_experts_moe_gb300 import Nvfp4MoeLayer, MOE_W4A16, MOE_W4A4
+    from nvfp4_mixture_experts_moe_gb300 import Nvfp4MoeLayer, MOE_MXFP4, MOE_W4A16, MOE_W4A4
     cfg = si.CONFIGS[name] if isinstance(name, str) else name
     if T is not None:
         cfg = cfg.with_tokens(T)
-    mode = MOE_W4A4 if cfg.mode == "w4a4" else MOE_W4A16
+    mode = {"w4a4": MOE_W4A4, "mxfp4": MOE_MXFP4}.get(cfg.mode, MOE_W4A16)
     layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mode=mode, I_shared=cfg.I_s, device="cuda")
     chunk = 32
     for e0 in range(0, cfg.E + 1, chunk):
@@ -32,16 +32,18 @@ def device_layer(name, T=None):
 
 
 class OracleWeights:
-    """Lazily quantised (by the oracle) experts of a workload, cached."""
+    """Lazily quantised (by the oracle) experts of a workload, cached: NVFP4,
+    or MXFP4 for an "mxfp4" workload."""
 
     def __init__(self, cfg):
         self.cfg = cfg
         self.cache = {}
+        self.kind = omoe.QuantWeightMX if cfg.mode == "mxfp4" else omoe.QuantWeight
 
     def __call__(self, e):
         if e not in self.cache:
             mats = [si.make_expert_weight(self.cfg, e, m) for m in ("gate", "up", "down")]
-            self.cache[e] = tuple(omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats)
+            self.cache[e] = tuple(self.kind.from_dense(m.float().numpy()) for m in mats)
         return self.cache[e]
 
     def all(self):
@@ -53,7 +55,7 @@ class OracleWeights:
 
         def one(e):
             mats = [si.make_expert_weight(self.cfg, e, m) for m in ("gate", "up", "down")]
-            return e, tuple(omoe.QuantWeight.from_dense(m.float().numpy()) for m in mats)
+            return e, tuple(self.kind.from_dense(m.float().numpy()) for m in mats)
 
         with ThreadPoolExecutor(threads) as ex:
             for e, w in ex.map(one, todo):

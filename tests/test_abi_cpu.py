@@ -59,7 +59,8 @@ def test_host_validation_before_device_work(lib):
     assert L.moe_nvfp4_prepare_weights(256, 256, ctypes.cast(gs, ctypes.c_void_p), 100, 64, 0, 0, 256,
                                        None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_nvfp4_quantize(256, 4, 24, 256, 256, 256, 256, 256, None) == B.MOE_ERR_INVALID_ARG
-    assert L.moe_combine(256, 256, None, 1, 4, 2, 12, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(256, 256, None, None, 4, 2, 12, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(256, 256, None, 8, 4, 2, 16, 256, None) == B.MOE_ERR_INVALID_ARG  # misaligned
 
 
 def test_sizes(lib):
@@ -137,5 +138,11 @@ def test_empty_batches_are_host_no_ops(lib):
                        w13_shared=256, w2_shared=256)
     assert lib.moe_nvfp4_forward(ctypes.byref(d), None, None, None, None, None, 0, None) == B.MOE_OK
     assert lib.moe_nvfp4_quantize_static(None, 0, 64, 1.0, None, None, None) == B.MOE_OK
-    assert lib.moe_combine(None, None, None, 1, 0, 8, 4096, None, None) == B.MOE_OK
+    assert lib.moe_combine(None, None, None, None, 0, 8, 4096, None, None) == B.MOE_OK
     assert lib.moe_swiglu(None, 0, 128, None, None) == B.MOE_OK
+
+
+def test_debug_hooks_validate_keys(lib):
+    assert lib.moe_debug_set(99, 1) == B.MOE_ERR_INVALID_ARG
+    for key in (B.MOE_DEBUG_WAIT_LIMIT, B.MOE_DEBUG_EXTRA_ARRIVALS, B.MOE_DEBUG_DISABLE_DECODE_FUSED):
+        assert lib.moe_debug_set(key, 0) == B.MOE_OK   # 0 restores every default

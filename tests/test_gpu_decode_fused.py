@@ -1,0 +1,137 @@
+"""The single-kernel decode path ("micro path": routing, permutation, both
+expert GEMMs and the combine in one cooperative launch; "Serving Solar Open 2
+on DGX Spark", "The fix") against the multi-kernel path and the oracle.
+
+The two paths share their arithmetic (the same MMA inner loop, accumulation
+order, row scales, epilogue operations and combine order), so their outputs
+must agree bit for bit; the oracle check of the decode workload itself runs
+in test_gpu_parity.py through whichever path the forward takes (this one).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic_inputs as si
+from oracle import moe as omoe
+from tests.gpu_layers import OracleWeights, device_layer
+from tests.tolerance import check_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def B():
+    from nvfp4_mixture_experts_moe_gb300 import binding
+    return binding
+
+
+@pytest.fixture(autouse=True)
+def default_hooks():
+    yield
+    for key in (B().MOE_DEBUG_WAIT_LIMIT, B().MOE_DEBUG_EXTRA_ARRIVALS, B().MOE_DEBUG_DISABLE_DECODE_FUSED):
+        B().moe_debug_set(key, 0)
+
+
+def _both_paths(layer, x, logits, T, k):
+    outs = []
+    for disable in (0, 1):
+        B().moe_debug_set(B().MOE_DEBUG_DISABLE_DECODE_FUSED, disable)
+        ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+        ws = layer.workspace(T)
+        launches0 = B().moe_kernel_launches()
+        out = layer.forward(x, logits, topk_ids=ids, ws=ws)
+        torch.cuda.synchronize()
+        launches = B().moe_kernel_launches() - launches0
+        assert B().moe_get_device_status(ws) == 0
+        outs.append((out.clone(), ids.clone(), launches))
+    return outs
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_fused_equals_multi_kernel_path(T):
+    cfg, layer = device_layer("decode")
+    c = cfg.with_tokens(T)
+    x = si.make_x(c).cuda()
+    logits = si.make_logits(c).cuda()
+    (fo, fi, fl), (mo, mi, ml) = _both_paths(layer, x, logits, T, cfg.k)
+    assert fl == 1 and ml > 1           # one kernel against the chain
+    assert torch.equal(fi, mi)
+    assert torch.equal(fo, mo)
+    rids, _ = omoe.route(logits.cpu().numpy(), cfg.k)
+    assert (fi.cpu().numpy() == rids).all()
+
+
+def test_fused_tiny_layer_against_oracle():
+    cfg, layer = device_layer("tiny", T=8)
+    x = si.make_x(cfg)
+    logits = si.make_logits(cfg)
+    (fo, fi, fl), (mo, _, _) = _both_paths(layer, x.cuda(), logits.cuda(), cfg.T, cfg.k)
+    assert fl == 1 and torch.equal(fo, mo)
+    experts, shared = OracleWeights(cfg).all()
+    ref = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k)
+    check_outputs(fo.float().cpu().numpy(), ref, what="tiny T=8, single-kernel decode")
+
+
+def test_fused_without_shared_expert():
+    from nvfp4_mixture_experts_moe_gb300 import Nvfp4MoeLayer
+    cfg = si.LayerConfig("noshared_dec", T=6, H=512, I=256, I_s=256, E=16, k=4)
+    layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, shared=False, device="cuda")
+    W = si.make_layer_weights(cfg, experts=list(range(cfg.E)))
+    for e in range(cfg.E):
+        layer.set_expert(e, *W[e])
+    x = si.make_x(cfg)
+    logits = si.make_logits(cfg)
+    (fo, _, fl), (mo, _, _) = _both_paths(layer, x.cuda(), logits.cuda(), cfg.T, cfg.k)
+    assert fl == 1 and torch.equal(fo, mo)
+    ow = OracleWeights(cfg)
+    ref = omoe.layer(x.float().numpy(), logits.numpy(), [ow(e) for e in range(cfg.E)], None, cfg.k)
+    check_outputs(fo.float().cpu().numpy(), ref, what="no shared expert, single-kernel decode")
+
+
+def test_fused_with_router_gemm():
+    cfg, layer = device_layer("decode")
+    x = si.make_x(cfg).cuda()
+    layer.set_router(si.make_router_weight(cfg))
+    try:
+        (fo, fi, _), (mo, mi, _) = _both_paths(layer, x, None, cfg.T, cfg.k)
+    finally:
+        layer.set_router(None)
+    assert torch.equal(fi, mi) and torch.equal(fo, mo)
+
+
+def test_fused_is_deterministic():
+    cfg, layer = device_layer("decode")
+    x = si.make_x(cfg).cuda()
+    logits = si.make_logits(cfg).cuda()
+    outs = [layer.forward(x, logits).clone() for _ in range(5)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_fused_timeout_is_reported_and_recovers():
+    """The down phase waits for arrivals that never come: every wait gives up
+    after the (shortened) limit, the status word reads MOE_ERR_TIMEOUT, and the
+    next forward on the same workspace is correct again."""
+    cfg, layer = device_layer("tiny", T=8)
+    x = si.make_x(cfg).cuda()
+    logits = si.make_logits(cfg).cuda()
+    ws = layer.workspace()
+    good = layer.forward(x, logits, ws=ws).clone()
+    torch.cuda.synchronize()
+    assert B().moe_get_device_status(ws) == 0
+    B().moe_debug_set(B().MOE_DEBUG_WAIT_LIMIT, 2_000_000)      # ~1 ms
+    B().moe_debug_set(B().MOE_DEBUG_EXTRA_ARRIVALS, 1)
+    layer.forward(x, logits, ws=ws)
+    torch.cuda.synchronize()
+    assert B().moe_get_device_status(ws) == B().MOE_ERR_TIMEOUT
+    B().moe_debug_set(B().MOE_DEBUG_EXTRA_ARRIVALS, 0)
+    B().moe_debug_set(B().MOE_DEBUG_WAIT_LIMIT, 0)
+    again = layer.forward(x, logits, ws=ws)
+    torch.cuda.synchronize()
+    assert B().moe_get_device_status(ws) == 0
+    assert torch.equal(good, again)

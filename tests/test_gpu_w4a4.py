@@ -1,5 +1,7 @@
 """W4A4 path (NVFP4 weights and activations, block-scaled FP4 MMA on tcgen05)
 against the CPU oracle through the C ABI."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -8,7 +10,7 @@ import synthetic_inputs as si
 from oracle import moe as omoe
 from oracle import nvfp4 as onv
 from tests.gpu_layers import OracleWeights, device_layer
-from tests.tolerance import check_outputs
+from tests.tolerance import TOPK_W_ABS, check_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -134,39 +136,36 @@ def test_w4a4_grouped_gemm_tile_edges(gate_up):
         assert amax.item() == float(np.abs(got).max())
 
 
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "w4a4_full_tokens.npz")
+
+
 @pytest.mark.slow
-def test_w4a4_full_size_properties():
-    """The W4A4 workload at full size (16384 tokens, hidden 7168, 256 experts):
-    routing exact; X quantisation bit-exact; sampled tokens within the bound
-    that NVFP4 quantisation of h can introduce (valid for any global scale of
-    h): |out - out_h_unquantised| <= sum_i |W2 col i| * delta_i, where delta_i
-    = (block amax / 6) * (1 + 2**-4) is the round-trip bound of one element."""
+def test_w4a4_full_size_against_golden():
+    """The W4A4 workload at full size (16384 tokens, hidden 7168, 256 experts
+    top-8 + shared): routing exact; X quantisation bit-exact over the whole
+    tensor with the oracle's global scale; and 64 tokens spread over the batch
+    element by element against the oracle's outputs at the stated bars plus
+    the oracle's allowance for FP4 re-quantisation of h. The global scale of
+    h depends on all 147,456 rows, so those outputs were computed once by the
+    oracle alone (tests/golden/make_w4a4_full.py) and stored with the scales
+    and the allowance."""
+    ref = np.load(GOLDEN)
     cfg, layer, x, logits, out, ids = _run("w4a4")
     rids, rw = omoe.route(logits.numpy(), cfg.k)
     assert (ids == rids).all()
+    toks = ref["tokens"]
+    # the stored routing was computed on another machine: ids bit for bit, weights
+    # within the routing-weight bar (numpy's exp may differ in the last place)
+    assert (rids[toks] == ref["ids"]).all() and np.abs(rw[toks] - ref["w"]).max() <= TOPK_W_ABS
     from nvfp4_mixture_experts_moe_gb300 import quantize_bf16
     q, sf, gs = quantize_bf16(x.cuda())
     xs = x.float().numpy()
     rq, rsf, rgs = onv.quantize(xs)
-    assert np.float32(gs.item()) == rgs
+    assert np.float32(gs.item()) == rgs == ref["gs_x"]
     assert (sf.cpu().numpy() == rsf).all() and (q.cpu().numpy() == onv.pack(rq)).all()
-    xd = onv.dequantize(rq, rsf, rgs)
-    tokens = [0, 9999]
-    ow = OracleWeights(cfg)
-    ow.prefetch([int(e) for t in tokens for e in rids[t]] + [cfg.E])
-    for t in tokens:
-        ref = np.zeros(cfg.H)
-        bound = np.zeros(cfg.H)
-        slots = [(int(rids[t, j]), float(rw[t, j])) for j in range(cfg.k)] + [(cfg.E, 1.0)]
-        for e, wt in slots:
-            g_, u_, d_ = ow(e)
-            h = omoe.bf16_round(omoe.gate_up_swiglu(xd[t:t + 1], g_, u_)).astype(np.float64)
-            blocks = np.abs(h.reshape(-1, 16)).max(axis=1)
-            delta = np.repeat(blocks / 6 * (1 + 2 ** -4), 16)
-            wd = d_.dequantize()
-            ref += wt * (h @ wd.T)[0]
-            bound += wt * (np.abs(wd) @ delta)
-        err = np.abs(out[t] - ref)
-        assert (err <= bound + 2e-2 + 2 ** -7 * np.abs(ref)).all(), (t, float((err - bound).max()))
-        # the quantisation error is random in sign: far below the worst case
-        assert np.linalg.norm(out[t] - ref) <= 0.25 * np.linalg.norm(bound)
+    # the bar plus, per element, how far FP4 re-quantisation of h can move it when
+    # h (fp32 on the GPU, float64 in the oracle) rounds the other way to bf16 at
+    # elements that lie on a bf16 midpoint straddling an FP4 decision (computed
+    # by the oracle alone; tests/golden/make_w4a4_full.py)
+    check_outputs(out[toks], ref["out"].astype(np.float64), extra=ref["flip"].astype(np.float64),
+                  what="w4a4 full size (64 stored tokens)")

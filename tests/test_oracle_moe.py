@@ -216,7 +216,8 @@ def test_w4a4_golden_script_equals_layer():
     spec.loader.exec_module(mk)
     cfg = si.LayerConfig("w4a4_pin", T=64, H=512, I=256, I_s=256, E=8, k=2, mode="w4a4", outliers=True)
     toks = np.array([0, 5, 17, 40, 63])
-    out, gs_x, amax_h, gs_h, ids, w = mk.golden_rows(cfg, toks, threads=4, log=lambda m: None)
+    out, gs_x, amax_h, gs_h, ids, w, flip = mk.golden_rows(cfg, toks, threads=4, log=lambda m: None)
+    assert flip.shape == out.shape and (flip >= 0).all()
     W = {e: tuple(moe.QuantWeight.from_dense(si.make_expert_weight(cfg, e, m).float().numpy())
                   for m in ("gate", "up", "down")) for e in range(cfg.E + 1)}
     ref, parts = moe.layer(si.make_x(cfg).float().numpy(), si.make_logits(cfg).numpy(),
@@ -224,3 +225,87 @@ def test_w4a4_golden_script_equals_layer():
     assert gs_x == parts["xgs"] and gs_h == parts["hgs"]
     assert amax_h == np.float32(np.max(np.abs(parts["h_bf16"])))
     assert np.abs(out - ref[toks]).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_layer_matches_dense_formulation_mxfp4():
+    """MXFP4 layer ("vLLM on the NVIDIA DGX Spark", section 6.4): every expert
+    on every token weighted by the routing matrix, with x quantised once and
+    each h row quantised on its own (no global scale), against the grouped
+    layer."""
+    from oracle import mxfp4
+    cfg = si.LayerConfig("tiny_mx", T=16, H=256, I=128, I_s=128, E=8, k=2, mode="mxfp4")
+    W = si.make_layer_weights(cfg)
+    trips = {e: tuple(moe.QuantWeightMX.from_dense(m.float().numpy()) for m in W[e]) for e in W}
+    x = si.make_x(cfg).float().numpy().astype(np.float64)
+    logits = si.make_logits(cfg).numpy()
+    experts, shared = [trips[e] for e in range(cfg.E)], trips[cfg.E]
+    out = moe.layer(x, logits, experts, shared, cfg.k, mode="mxfp4")
+    ids, w = moe.route(logits, cfg.k)
+    xd = mxfp4.dequantize(*mxfp4.quantize(x.astype(np.float32)))
+
+    def ffn(rows, trip):
+        g, u, d = (torch.tensor(m.dequantize()) for m in trip)
+        xt = torch.tensor(rows)
+        h = torch.nn.functional.silu(xt @ g.T) * (xt @ u.T)
+        hb = h.to(torch.float32).to(torch.bfloat16).float().numpy()
+        hd = mxfp4.dequantize(*mxfp4.quantize(hb))
+        return (torch.tensor(hd) @ d.T).numpy()
+
+    dense = np.zeros_like(out)
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            dense[t] += w[t, j] * ffn(xd[t:t + 1], experts[ids[t, j]])[0]
+        dense[t] += ffn(xd[t:t + 1], shared)[0]
+    assert np.abs(out - dense).max() <= 1e-12 * max(1.0, np.abs(dense).max())
+    # and MXFP4 is not NVFP4: the same layer through the W4A4 path differs
+    nv = {e: tuple(moe.QuantWeight.from_dense(m.float().numpy()) for m in W[e]) for e in W}
+    out_nv = moe.layer(x, logits, [nv[e] for e in range(cfg.E)], nv[cfg.E], cfg.k, mode="w4a4")
+    assert np.abs(out - out_nv).max() > 1e-3
+
+
+@pytest.mark.parametrize("mode", ["w4a16", "mxfp4"])
+def test_expert_shards_sum_to_the_layer(mode):
+    """Expert parallelism: contiguous shards of the experts, each computing
+    only its own pairs (the shared expert on one shard), add up to the whole
+    layer. Modes without a per-tensor activation scale only (with dynamic
+    W4A4 scales every shard quantises h with its own scale)."""
+    cfg = si.LayerConfig("shards", T=24, H=256, I=128, I_s=128, E=10, k=3, mode=mode)
+    W = si.make_layer_weights(cfg)
+    kind = moe.QuantWeightMX if mode == "mxfp4" else moe.QuantWeight
+    trips = {e: tuple(kind.from_dense(m.float().numpy()) for m in W[e]) for e in W}
+    x = si.make_x(cfg).float().numpy().astype(np.float64)
+    logits = si.make_logits(cfg).numpy()
+    experts, shared = [trips[e] for e in range(cfg.E)], trips[cfg.E]
+    full = moe.layer(x, logits, experts, shared, cfg.k, mode=mode)
+    bounds = [0, 3, 7, 10]  # uneven shards
+    parts = [moe.layer(x, logits, experts, shared if i == 0 else None, cfg.k, mode=mode,
+                       experts_range=(bounds[i], bounds[i + 1])) for i in range(3)]
+    assert np.abs(sum(parts) - full).max() <= 1e-12 * max(1.0, np.abs(full).max())
+    # a shard without experts and without the shared expert contributes nothing
+    empty = moe.layer(x, logits, experts, None, cfg.k, mode=mode, experts_range=(4, 4))
+    assert not empty.any()
+
+
+def test_requant_flip_bound_pins():
+    """The W4A4 flip allowance: zero when no element of h can round to another
+    bf16 value; exactly one dequantised step times |Wd column| for one element
+    put on a bf16 midpoint whose two neighbours quantise differently."""
+    rng = np.random.default_rng(3)
+    H, I = 8, 32
+    down_abs = np.abs(rng.standard_normal((H, I)))
+    gs = np.float32(1.0)
+    # bf16 values are a half ulp away from every midpoint: never ambiguous
+    h = moe.bf16_round(rng.standard_normal((1, I))).astype(np.float64)[0]
+    assert not moe.requant_flip_bound(h, gs, down_abs).any()
+    # block 0 with amax 6 -> scale 1 (at gs = 1): e2m1 decides 2.5 between 2 and 3;
+    # 2.5 is a bf16 value, so put h midway between 2.5 and its bf16 neighbour 2.515625
+    h = np.zeros(I)
+    h[0] = 6.0
+    h[5] = 0.5 * (2.5 + 2.515625)
+    got = moe.requant_flip_bound(h, gs, down_abs)
+    d0 = nvfp4.dequantize(*nvfp4.quantize(np.array([[6.0, 0, 0, 0, 0, 2.5] + [0] * 10], np.float32), gs=gs)[:2], gs)
+    d1 = nvfp4.dequantize(*nvfp4.quantize(np.array([[6.0, 0, 0, 0, 0, 2.515625] + [0] * 10], np.float32), gs=gs)[:2],
+                          gs)
+    step = np.abs(d1 - d0)[0]
+    assert step[5] == 1.0 and step.sum() == 1.0        # 2.5 -> code of 2, 2.515625 -> code of 3
+    assert np.array_equal(got, down_abs[:, 5] * 1.0)

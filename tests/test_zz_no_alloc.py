@@ -67,3 +67,30 @@ def test_noalloc_rejects_oversized_problems():
     with pytest.raises(B.MoeError) as ei:
         B.moe_permute_noalloc(dummy, T, k, E, dummy, dummy, dummy, dummy)
     assert ei.value.status == B.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T,k,E", [(4096, 8, 320), (8, 8, 320), (2048, 8, 320)])
+def test_noalloc_matches_oracle_two_calls(T, k, E):
+    """Bit for bit against the oracle's stable counting sort, on two calls in a
+    row (the second reuses the scratch the first one left behind)."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as B
+    from oracle import moe as omoe
+    P = T * k
+    for call in range(2):
+        g = torch.Generator().manual_seed(7 * call + T)
+        ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+        if call == 1:
+            ids[: T // 2, 1] = E - 1  # a skewed histogram on the second call
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        perm = torch.empty(P, dtype=torch.int32, device="cuda")
+        inv = torch.empty(P, dtype=torch.int32, device="cuda")
+        status = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+        B.moe_permute_noalloc(ids.cuda(), T, k, E, counts, offsets, perm, inv, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        rc, ro, rp, ri = omoe.permute(ids.numpy(), E)
+        assert (counts.cpu().numpy() == rc).all()
+        assert (offsets.cpu().numpy() == ro).all()
+        assert (perm.cpu().numpy() == rp).all()
+        assert (inv.cpu().numpy() == ri).all()

@@ -2,18 +2,28 @@
 
 The layer's specification bounds the float outputs by a max absolute error of
 2e-2 and a relative Frobenius error of 1e-2 against the float64 oracle. The
-layer's output is bf16, whose own rounding error is up to 2**-8 * |ref|; for
-|ref| below 2.56 that fits inside 2e-2. Above it the absolute bar alone cannot
-be met by any bf16 output, so the per-element bar becomes
-``max(2e-2, 2**-7 * |ref|)``: the bf16 output rounding plus the same again for
-the bf16 intermediate ``h``. Integer results (routing ids, permutation,
-quantised codes and scales) are compared bit for bit elsewhere.
+layer's output is bf16: rounding to bf16 alone can move a value by up to
+half an ulp, 2**-8 * |ref|, which exceeds 2e-2 once |ref| > 5.12 (the W4A4
+workload's outputs reach ~17), so no bf16 output can meet a flat 2e-2 there.
+The per-element bar is therefore ``max(2e-2, 2**-7 * |ref|)``: twice the
+output rounding, the second half for the bf16 intermediate ``h`` between the
+two GEMMs. It equals 2e-2 exactly for |ref| <= 2.56 (every output of the
+decode, prefill and skewed workloads) and is wider above that. Integer results
+(routing ids, permutation, quantised codes and scales) are compared bit for
+bit elsewhere.
+
+Every ``check_outputs`` call records the achieved max absolute and relative
+Frobenius errors; the test session prints them at the end (tests/conftest.py)
+so that how much of the bar a workload uses is visible in every run.
 """
 import numpy as np
 
 MAX_ABS = 2e-2
 REL_FRO = 1e-2
 TOPK_W_ABS = 1e-6
+
+#: (what, max abs error, relative Frobenius error, largest |ref|) per check
+ACHIEVED = []
 
 
 def elementwise_bar(ref, extra=None):
@@ -40,4 +50,6 @@ def check_outputs(got, ref, extra=None, what="output"):
             f"{what}: {int(bad.sum())} elements over the bar; worst at {idx}: "
             f"got {got[idx]!r} ref {ref[idx]!r} err {err[idx]:.3g} bar {bar[idx]:.3g}")
     assert rel <= REL_FRO, f"{what}: relative Frobenius error {rel:.3g} > {REL_FRO}"
-    return float(err.max()) if err.size else 0.0, rel
+    max_err = float(err.max()) if err.size else 0.0
+    ACHIEVED.append((what, max_err, rel, float(np.abs(ref).max()) if ref.size else 0.0))
+    return max_err, rel
