@@ -264,54 +264,112 @@ def layer(x, logits, experts, shared, k, mode="w4a16", return_parts=False, x_gs=
     return out
 
 
-def _bf16_neighbour(h):
-    """The bf16 value adjacent to bf16_round(h) on the other side of h (h
-    float64, finite): with bf16_round(h) it brackets h."""
-    b0 = bf16_round(h).astype(np.float64)
-    bits = b0.astype(np.float32).view(np.uint32).astype(np.int64)
-    # one bf16 ulp away from zero is +0x10000 in the fp32 bit pattern of the magnitude
-    away = ((h > b0) == (b0 >= 0)) | (b0 == 0)
-    nb = np.where(away, bits + 0x10000, bits - 0x10000)
-    nb = np.where((b0 == 0) & (h < 0), (np.uint32(0x80000000).astype(np.int64) | 0x10000), nb)
-    return nb.astype(np.uint32).view(np.float32).astype(np.float64)
+#: Lipschitz constant of silu: max |silu'(z)| = 1.0998 (at z = 2.40)
+SILU_LIP = 1.1
 
 
-def requant_flip_bound(h_exact, gs, down_abs, rel_delta=2.0 ** -14):
+def gate_up_window(x_rows, gate, up):
+    """Bound on how far an fp32 computation of ``h = silu(g) * u`` can lie
+    from the float64 ``h`` of ``gate_up_swiglu`` (same inputs), per element.
+
+    A dot product of K terms summed in fp32 in any order, with r roundings on
+    the path of every term, is within ``r * 2**-24 * sum |terms|`` of the exact
+    sum (the standard recursive-summation bound, first order). Reading taken
+    for a block-scaled tensor-core GEMM that accumulates one 64-wide K block
+    at a time into an fp32 accumulator: at most 6 roundings inside a block
+    (a pairwise tree over 64 products) and one per block added, plus 2 for the
+    global-scale product, so ``r = K / 64 + 8``. Then, with ``dg``, ``du``
+    the bounds of g and u and silu 1.1-Lipschitz,
+    ``|h' - h| <= 1.1 dg (|u| + du) + |silu(g)| du`` plus ``2**-20`` relative
+    for evaluating silu and the product in fp32 (exp, a division, two
+    multiplies, each a few ulps).
+
+    ``x_rows`` float64 ``[n, K]`` (the GEMM's input values), ``gate``/``up``
+    ``QuantWeight``. Returns float64 ``[n, I]``.
+    Pinned by: zero for zero rows; it contains the actual error of float32
+    evaluations of h in several summation orders (tests).
+    """
+    x = np.abs(np.asarray(x_rows, dtype=np.float64))
+    K = x.shape[1]
+    r = K / 64.0 + 8.0
+    gd, ud = gate.dequantize(), up.dequantize()
+    xr = np.asarray(x_rows, dtype=np.float64)
+    g, u = xr @ gd.T, xr @ ud.T
+    dg = r * 2.0 ** -24 * (x @ np.abs(gd).T)
+    du = r * 2.0 ** -24 * (x @ np.abs(ud).T)
+    sg = np.abs(silu(g))
+    w = SILU_LIP * dg * (np.abs(u) + du) + sg * du
+    return w + 2.0 ** -20 * (sg + SILU_LIP * dg) * (np.abs(u) + du)
+
+
+def _bf16_values_between(lo, hi):
+    """All bf16 values v with lo <= v <= hi (lo, hi bf16 values, lo <= hi)."""
+    def key(v):  # monotone integer key of a bf16 value (sign-magnitude -> ordered)
+        b = int(np.float32(v).view(np.uint32)) >> 16
+        return -(b & 0x7FFF) if b & 0x8000 else b
+    def val(k):
+        b = (0x8000 | -k) if k < 0 else k
+        return float(np.uint32(b << 16).view(np.float32))
+    return [val(k) for k in range(key(lo), key(hi) + 1)]
+
+
+def requant_flip_bound(h_exact, gs, down_abs, window):
     """How much FP4 re-quantisation of h can move one row's down projection
-    when h is known only to within ``rel_delta`` (relative) of ``h_exact``.
+    when h is known only to within ``window`` (absolute, per element, e.g.
+    ``gate_up_window``) of ``h_exact``.
 
     The layer rounds h to bf16 and quantises it (W4A4). A computation of h
-    that differs from ``h_exact`` by less than ``rel_delta * |h|`` (plus a
-    floor of ``2**-20`` times the row's largest |h|) can round to either bf16
-    value next to ``h_exact`` when ``h_exact`` lies that close to the midpoint
-    between them. For every such element the block is quantised with each of
-    the two values (the other elements as the oracle has them, global scale
-    ``gs``); where the dequantised block differs, the absolute differences are
-    added up element by element. ``down_abs`` is ``|Wd|``, the element-wise
-    absolute value of the dequantised down matrix ``[H, I]``. Returns
-    ``down_abs @ sum_of_differences`` (the largest change of each output
-    element of this row, by the triangle inequality), float64 ``[H]``.
-    Pinned by: zero for a row far from every bf16 midpoint; an element put on
-    a midpoint that straddles an e2m1 decision gives exactly one step times
-    |Wd column| (tests).
+    within the window rounds to some bf16 value between ``bf16(h - window)``
+    and ``bf16(h + window)``. For every element where that is not just
+    ``bf16(h)``, the element's block is quantised with each other such value
+    (up to 8 of them; beyond that the two ends) and the rest of the row as the
+    oracle has it (global scale ``gs``); the largest absolute change of each
+    dequantised block element is added up over the ambiguous elements.
+    ``down_abs`` is ``|Wd|``, the element-wise absolute value of the
+    dequantised down matrix ``[H, I]``. Returns ``down_abs @ changes`` (the
+    largest change of each output element of this row, by the triangle
+    inequality, counting the flips one at a time), float64 ``[H]``.
+    Pinned by: zero when no element can round to another bf16 value; an
+    element put on a midpoint that straddles an e2m1 decision gives exactly
+    one step times |Wd column| (tests).
     """
-    h = np.asarray(h_exact, dtype=np.float64).reshape(1, -1)
+    h = np.asarray(h_exact, dtype=np.float64).reshape(-1)
+    win = np.broadcast_to(np.asarray(window, dtype=np.float64).reshape(-1), h.shape)
     b0 = bf16_round(h).astype(np.float64)
-    b1 = _bf16_neighbour(h)
-    mid = 0.5 * (b0 + b1)
-    tol = rel_delta * np.abs(h) + 2.0 ** -20 * np.abs(h).max()
-    amb = np.abs(h - mid) <= tol
+    lo = bf16_round(h - win).astype(np.float64)
+    hi = bf16_round(h + win).astype(np.float64)
+    amb = np.nonzero((lo != b0) | (hi != b0))[0]
     diff = np.zeros_like(h)
-    if amb.any():
-        base = nvfp4.dequantize(*nvfp4.quantize(b0.astype(F32), gs=gs)[:2], gs)
-        for i in np.nonzero(amb[0])[0]:
-            alt = b0.copy()
-            alt[0, i] = b1[0, i]
-            blk = slice(16 * (i // 16), 16 * (i // 16) + 16)
-            q = nvfp4.quantize(alt[:, blk].astype(F32), gs=gs)
+    if amb.size:
+        base = nvfp4.dequantize(*nvfp4.quantize(b0[None, :].astype(F32), gs=gs)[:2], gs)[0]
+        rows, owner = [], []
+        for i in amb:
+            vals = _bf16_values_between(lo[i], hi[i])
+            if len(vals) > 9:
+                vals = [vals[0], vals[-1]]
+            s0 = 16 * (i // 16)
+            for v in vals:
+                if v == b0[i]:
+                    continue
+                blk = b0[s0:s0 + 16].copy()
+                blk[i - s0] = v
+                rows.append(blk)
+                owner.append(i)
+        if rows:
+            alt = np.stack(rows).astype(F32)
+            q = nvfp4.quantize(alt, gs=gs)
             d = nvfp4.dequantize(q[0], q[1], gs)
-            diff[0, blk] += np.abs(d - base[:, blk])[0]
-    return down_abs @ diff[0]
+            owner = np.asarray(owner)
+            starts = 16 * (owner // 16)
+            delta = np.abs(d - base[starts[:, None] + np.arange(16)[None, :]])
+            # largest change per ambiguous element over its alternatives
+            best = {}
+            for r_, i in enumerate(owner):
+                best[i] = delta[r_] if i not in best else np.maximum(best[i], delta[r_])
+            for i, dl in best.items():
+                s0 = 16 * (i // 16)
+                diff[s0:s0 + 16] += dl
+    return down_abs @ diff
 
 
 def token_outputs_w4a16(x_tokens, ids, w, expert_weights, shared):

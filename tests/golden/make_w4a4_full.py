@@ -14,12 +14,13 @@ generators in ``synthetic_inputs``; nothing from the CUDA path), and stores:
 * ``tokens``: 64 token indices spread over the batch, with their routing
   (``ids``, ``w``) and their float64 layer outputs ``out`` stored as float32;
 * ``flip``: per output element of those tokens, how far FP4 re-quantisation
-  of h can move it when h is computed to within 2^-14 (relative) of the
-  oracle's float64 value (``oracle.moe.requant_flip_bound``): a GPU computes
-  h in fp32 in another summation order, so an h element lying that close to
-  a bf16 rounding midpoint may round the other way, and where the two bf16
-  values quantise to different FP4 codes (or block scales) the token's whole
-  output row moves by one FP4 step times the down-projection column.
+  of h can move it when h is computed in fp32 (``oracle.moe.requant_flip_bound``
+  with the window ``oracle.moe.gate_up_window``, the fp32 summation bound of
+  the gate/up GEMM): a GPU computes h in another summation order, so an h
+  element lying within that window of a bf16 rounding midpoint may round the
+  other way, and where the bf16 values quantise to different FP4 codes (or
+  block scales) the token's whole output row moves by the FP4 steps times
+  the down-projection column.
 
 Given ``gs_x`` and ``gs_h`` every token's output depends on that token alone,
 so the stored rows are exactly the rows of ``oracle.moe.layer(..., mode="w4a4")``
@@ -65,7 +66,8 @@ def sample_tokens(T, n):
 def golden_rows(cfg, tokens, threads=8, log=print):
     """Oracle outputs ``[len(tokens), H]`` (float64) of the W4A4 layer ``cfg``
     for the given tokens, with the scales: returns (out, gs_x, amax_h, gs_h,
-    ids, w) where ids/w are the whole batch's routing."""
+    ids, w, flip) where ids/w are the whole batch's routing and flip the
+    re-quantisation allowance of the tokens' outputs."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     t0 = time.time()
     x = si.make_x(cfg).float().numpy()
@@ -90,13 +92,15 @@ def golden_rows(cfg, tokens, threads=8, log=print):
             h = omoe.bf16_round(h_exact)
             if h.size:
                 amax = max(amax, float(np.max(np.abs(h))))
-            for i, t in enumerate(tk):
-                if int(t) in want:
-                    sampled[int(t)] = (h[i].copy(), h_exact[i].copy())
+            pick = [i for i, t in enumerate(tk) if int(t) in want]
+            if pick:
+                win = omoe.gate_up_window(x_deq[tk[pick]], gq, uq)
+                for n, i in enumerate(pick):
+                    sampled[int(tk[i])] = (h[i].copy(), h_exact[i].copy(), win[n])
         return e, amax, sampled, (dq if sampled else None)
 
     amax_h = 0.0
-    h_rows = {}        # (token, expert) -> (bf16-rounded h row, float64 h row)
+    h_rows = {}        # (token, expert) -> (bf16-rounded h row, float64 h row, fp32 window)
     downs = {}
     done = 0
     with ThreadPoolExecutor(threads) as ex:
@@ -122,7 +126,7 @@ def golden_rows(cfg, tokens, threads=8, log=print):
     def flip_of(t, e):
         if e not in down_abs:
             down_abs[e] = np.abs(downs[e].dequantize())
-        return omoe.requant_flip_bound(h_rows[(t, e)][1], gs_h, down_abs[e])
+        return omoe.requant_flip_bound(h_rows[(t, e)][1], gs_h, down_abs[e], h_rows[(t, e)][2])
 
     out = np.zeros((len(tokens), H), dtype=np.float64)
     flip = np.zeros((len(tokens), H), dtype=np.float64)

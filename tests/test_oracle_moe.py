@@ -294,18 +294,71 @@ def test_requant_flip_bound_pins():
     H, I = 8, 32
     down_abs = np.abs(rng.standard_normal((H, I)))
     gs = np.float32(1.0)
-    # bf16 values are a half ulp away from every midpoint: never ambiguous
+    # bf16 values are a half ulp away from every midpoint: a window below
+    # that never reaches another bf16 value
     h = moe.bf16_round(rng.standard_normal((1, I))).astype(np.float64)[0]
-    assert not moe.requant_flip_bound(h, gs, down_abs).any()
+    assert not moe.requant_flip_bound(h, gs, down_abs, 1e-6 * np.abs(h)).any()
     # block 0 with amax 6 -> scale 1 (at gs = 1): e2m1 decides 2.5 between 2 and 3;
     # 2.5 is a bf16 value, so put h midway between 2.5 and its bf16 neighbour 2.515625
     h = np.zeros(I)
     h[0] = 6.0
     h[5] = 0.5 * (2.5 + 2.515625)
-    got = moe.requant_flip_bound(h, gs, down_abs)
+    got = moe.requant_flip_bound(h, gs, down_abs, 1e-6)
     d0 = nvfp4.dequantize(*nvfp4.quantize(np.array([[6.0, 0, 0, 0, 0, 2.5] + [0] * 10], np.float32), gs=gs)[:2], gs)
     d1 = nvfp4.dequantize(*nvfp4.quantize(np.array([[6.0, 0, 0, 0, 0, 2.515625] + [0] * 10], np.float32), gs=gs)[:2],
                           gs)
     step = np.abs(d1 - d0)[0]
     assert step[5] == 1.0 and step.sum() == 1.0        # 2.5 -> code of 2, 2.515625 -> code of 3
     assert np.array_equal(got, down_abs[:, 5] * 1.0)
+    # a wide window on the block's maximum reaches another block scale: every
+    # element of the block may move, and the bound covers the recomputed block
+    h = np.zeros(I)
+    h[:16] = moe.bf16_round(np.linspace(0.3, 5.9, 16)).astype(np.float64)
+    win = np.zeros(I)
+    win[15] = 0.2                                      # 5.90625 may be anything in [5.70625, 6.10625]
+    got = moe.requant_flip_bound(h, gs, down_abs, win)
+    base = nvfp4.dequantize(*nvfp4.quantize(h[None, :16].astype(np.float32), gs=gs)[:2], gs)[0]
+    alt = h[:16].copy()
+    alt[15] = 5.75                                     # in the window: 5.75 / 6 -> E4M3 scale 0.9375, not 1
+    moved = np.abs(nvfp4.dequantize(*nvfp4.quantize(alt[None].astype(np.float32), gs=gs)[:2], gs)[0] - base)
+    assert (moved[:15] > 0).any()                      # another block scale moves the other elements
+    assert np.all(got >= down_abs[:, :16] @ moved - 1e-12)
+
+
+def test_gate_up_window_contains_fp32_errors():
+    """The fp32 window of h is zero for zero rows and contains the actual
+    error of float32 evaluations of h in several summation orders (forward,
+    reversed, blocked by 64 with a float32 accumulator across blocks)."""
+    rng = np.random.default_rng(11)
+    K, I = 1024, 64
+    g = moe.QuantWeight.from_dense((rng.standard_normal((I, K)) * 0.02).astype(np.float32))
+    u = moe.QuantWeight.from_dense((rng.standard_normal((I, K)) * 0.02).astype(np.float32))
+    assert not moe.gate_up_window(np.zeros((2, K)), g, u).any()
+    x = moe.bf16_round(rng.standard_normal((4, K)) * np.where(rng.random((4, K)) < 0.01, 20.0, 1.0)).astype(np.float64)
+    exact = moe.gate_up_swiglu(x, g, u)
+    win = moe.gate_up_window(x, g, u)
+    gd, ud = g.dequantize().astype(np.float32), u.dequantize().astype(np.float32)
+    x32 = x.astype(np.float32)
+
+    def h32(order):
+        gg = np.zeros((4, I), np.float32)
+        uu = np.zeros((4, I), np.float32)
+        if order == "blocked":
+            for k0 in range(0, K, 64):
+                gg = gg + (x32[:, k0:k0 + 64] @ gd[:, k0:k0 + 64].T).astype(np.float32)
+                uu = uu + (x32[:, k0:k0 + 64] @ ud[:, k0:k0 + 64].T).astype(np.float32)
+        else:
+            ks = range(K) if order == "forward" else range(K - 1, -1, -1)
+            for kk in ks:
+                gg = gg + x32[:, kk:kk + 1] * gd[None, :, kk]
+                uu = uu + x32[:, kk:kk + 1] * ud[None, :, kk]
+        sg = (gg / (np.float32(1) + np.exp(-gg))).astype(np.float32)
+        return (sg * uu).astype(np.float64)
+
+    for order in ("forward", "reversed", "blocked"):
+        err = np.abs(h32(order) - exact)
+        assert np.all(err <= win), (order, float(np.max(err - win)))
+    # and the window is not vacuous: well below |h| for most elements
+    assert np.median(win / np.maximum(np.abs(exact), 1e-30)) < 2.0 ** -8
+
+
