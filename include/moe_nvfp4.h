@@ -422,12 +422,19 @@ unsigned long long moe_kernel_launches(void);
  *   phase times out (exercises the timeout path without any fault).
  * MOE_DEBUG_DISABLE_DECODE_FUSED (default 0): nonzero makes
  *   moe_nvfp4_forward take the multi-kernel path for decode batches too.
- * Errors: an unknown key -> MOE_ERR_INVALID_ARG.
+ * MOE_DEBUG_DECODE_STAGE_KB (default 8, range 1..8; 0 restores the default):
+ *   the largest number of 64-wide K blocks per streamed shared-memory stage
+ *   of the W4A16 decode GEMMs (multi-kernel and single-kernel paths alike).
+ *   It sets how the two halves of the MMA warps split K, so results can
+ *   differ in the last bits from one setting to another (never between the
+ *   two decode paths at one setting). Used to tune the stage size.
+ * Errors: an unknown key, or a value out of range -> MOE_ERR_INVALID_ARG.
  */
 typedef enum {
   MOE_DEBUG_WAIT_LIMIT = 1,
   MOE_DEBUG_EXTRA_ARRIVALS = 2,
-  MOE_DEBUG_DISABLE_DECODE_FUSED = 3
+  MOE_DEBUG_DISABLE_DECODE_FUSED = 3,
+  MOE_DEBUG_DECODE_STAGE_KB = 4
 } moe_debug_key;
 moe_status moe_debug_set(int key, long long value);
 

@@ -54,14 +54,19 @@ constexpr int kW16SfOff = 4096;   // scale blocks within a chunk
 __host__ __device__ inline size_t w4a16_bytes(int N, int K) { return (size_t)N * K / 2 + (size_t)N * K / 16; }
 __host__ __device__ inline size_t w4a16_chunk(int mt, int kb, int KB) { return ((size_t)mt * KB + kb) * kW16Chunk; }
 
-// 64-wide K blocks per streamed stage of the small-group (decode) GEMMs: the
-// largest count <= 8 that gives every 128-row tile an even number of stages
-// (KB = K / 64 blocks per tile). The two halves of the MMA warps take
+// 64-wide K blocks per streamed stage of the small-group (decode) GEMMs
+// (KB = K / 64 blocks per 128-row tile): the largest count <= kmax (at most
+// 8) that divides KB into an even number of equal stages, else the largest
+// that gives an even number of stages. The two halves of the MMA warps take
 // alternate stages, so with an even count every tile splits its K blocks
-// between the halves the same way wherever it falls in a CTA's sequence,
-// and every kernel that runs this loop sums in the same order.
-__host__ __device__ inline int w16_stage_kb(int KB) {
-  for (int kb = 8; kb > 1; --kb)
+// between the halves the same way wherever it falls in a CTA's sequence (and
+// every kernel that runs this loop with the same kmax sums in the same
+// order); with equal stages the two halves also get the same work.
+constexpr int kW16MaxStageKb = 8;
+__host__ __device__ inline int w16_stage_kb(int KB, int kmax) {
+  for (int kb = kmax; kb > 1; --kb)
+    if (KB % kb == 0 && (KB / kb) % 2 == 0) return kb;
+  for (int kb = kmax; kb > 1; --kb)
     if (((KB + kb - 1) / kb) % 2 == 0) return kb;
   return 1;
 }

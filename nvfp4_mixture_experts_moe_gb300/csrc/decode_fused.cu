@@ -14,23 +14,25 @@
 // all CTAs are resident and may wait on one another with bounded spins):
 //
 // * Routing and the permutation are computed by every CTA in shared memory
-//   (a few hundred logits per token); the x rows are converted once per CTA to
-//   f16 with a power-of-two row scale and stay resident for the gate/up phase.
+//   (a few hundred logits per token); meanwhile the x rows arrive by bulk
+//   copy and are converted in place to f16 with a power-of-two row scale;
+//   they stay resident for the gate/up phase.
 // * Work items are (active expert group, 128-row weight tile): gate/up items
 //   first, then down items, taken by the CTAs in a strided order (gate/up
 //   items ascending, down items descending over the CTAs, so the CTAs with
 //   one gate/up item more get one down item fewer).
 // * One producer warp streams every item's weight tiles (stages of up to 8
-//   64-wide K blocks, 36 KB, in a ring of 4) with bulk copies from the
+//   64-wide K blocks, 36 KB, in a ring of as many as fit) with bulk copies from the
 //   gate/up phase straight into the down phase, so the down weights are
 //   already in flight when the gate/up items end.
 // * Sixteen MMA warps (8 row blocks x 2 halves that take alternate stages)
 //   turn the e2m1 codes into f16 with the hardware conversion, multiply in
 //   the E4M3 block scales and run mma.sync m16n8k16 with the group's rows as
-//   N; the second half hands its partial sums to the first at the end of an
+//   N; at the end of an item the half that finishes second adds the other's
+//   partial sums and runs the epilogue, while the first goes on to the next
 //   item. Stage sizes give every item an even number of stages, so the
 //   arithmetic (and the result, bit for bit) is that of the multi-kernel
-//   path's decode GEMM.
+//   path's decode GEMM (the same stage loop and join, decode_mma.cuh).
 // * Gate/up epilogue: SwiGLU, h stored bf16 in the workspace with a running
 //   per-row max |h|. Down epilogue: y = h W2^T * alpha * routing weight,
 //   stored bf16 (the shared expert's rows fp32). Neither waits on a global
@@ -50,6 +52,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "decode_mma.cuh"
 #include "kernels.cuh"
 #include "route.cuh"
 #include "tc_ptx.cuh"
@@ -61,19 +64,19 @@ using namespace tc;
 
 constexpr int kMaxT = kDecodeFusedMaxT;           // tokens (each group has at most this many rows)
 constexpr int kMaxK = 32;
-constexpr int kBlockWarps = 8;                     // one per 16-row block of a 128-row tile
-constexpr int kHalves = 2;                         // halves of a stage's K blocks
+using decode::kBlockWarps;                         // one per 16-row block of a 128-row tile
+using decode::kHalves;                             // halves that take alternate stages
 constexpr int kMmaWarps = kBlockWarps * kHalves;
 constexpr int kProducerWarp = kMmaWarps;
 constexpr int kHelperWarp = kMmaWarps + 1;
 constexpr int kSignalWarp = kMmaWarps + 2;
 constexpr int kThreads = (kMmaWarps + 3) * 32;
 constexpr int kTile = 128;
-constexpr int kMaxSlots = 8;
-constexpr int kStageBytes = 8 * kW16Chunk;         // ring slot: up to 8 K blocks (36 KB)
+constexpr int kMaxSlots = 16;                      // ring slots of stage_kb K blocks (stage_kb * 4608 bytes)
 constexpr int kHSlots = 2;                         // staged h row sets (down items)
 constexpr int kMaxRows = kMaxT * kMaxK + kMaxT;    // routed pairs + shared rows
 constexpr int kMaxGroups = kMaxT * kMaxK + 1;      // active groups: at most one per pair, + shared
+constexpr long long kDrainLimit = 4ll * 1000 * 1000 * 1000;  // cycles for in-flight copies to land
 
 struct Args {
   const float* logits;
@@ -95,6 +98,8 @@ struct Args {
   unsigned* hmax;       // [rows] bf16 magnitude bits of max |h| (zeroed)
   int* status;
   int slots;
+  int stage_kb;         // K blocks per ring slot (the larger of the two phases' stages)
+  int kmax;             // max 64-wide K blocks per stage (1..8)
   long long wait_limit;
   int extra_arrivals;   // test hook: arrivals expected per gate/up tile beyond the real ones
 };
@@ -103,12 +108,12 @@ struct Smem {
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   uint64_t hfull[kHSlots];
+  uint64_t hland[kHSlots];       // the helper's bulk copies of a slot's h rows have landed
   uint64_t hempty[kHSlots];
+  uint64_t xfull;                // the x rows (bf16) have landed in shared memory
   uint64_t xfree;                // every MMA warp is done with the resident x rows
-  uint64_t done[2];              // an item's epilogue stores are issued (the 8 first-half warps)
-  uint64_t done_free[2];         // the signal warp has taken that item over
-  uint64_t red_full[kBlockWarps];
-  uint64_t red_empty[kBlockWarps];
+  uint64_t done[2];              // an item's epilogue stores are issued (one warp per row block)
+  int released;                  // items the signal warp has taken over (counts up; no parity aliasing)
   int abort;
   int A;                         // active groups
   int32_t ids[kMaxT * kMaxK];
@@ -121,14 +126,8 @@ struct Smem {
   int32_t grp_n[kMaxGroups];
   float xmul[kMaxT];
   float hmul[kHSlots][kMaxT];
-  float4 red[kBlockWarps][32];
+  decode::HalfJoin join;         // the two halves' partial sums of an item
 };
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
 
 // Power-of-two row scale from a row's largest bf16 magnitude (bit pattern m):
 // 2^sh brings the maximum into [2^14, 2^15), where every bf16 value down to
@@ -137,23 +136,6 @@ __device__ __forceinline__ int row_shift(uint32_t m) {
   const int e = (int)(m >> 7);
   int sh = (m == 0) ? 0 : 141 - max(e, 1);
   return max(-113, min(sh, 126));
-}
-
-// bf16 row [K] (global) -> f16 row [K] (shared) times 2^sh.
-__device__ __forceinline__ void stage_row(const uint16_t* src, uint16_t* dst, int K, int sh, int lane, bool l2) {
-  const float up = __int_as_float((127 + sh) << 23);
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  for (int i = lane; i < K / 8; i += 32) {
-    const uint4 v = l2 ? __ldcg(s + i) : __ldg(s + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __half2 hh = __floats2half2_rn(__uint_as_float(w[q] << 16) * up, __uint_as_float(w[q] & 0xffff0000u) * up);
-      o[q] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    *reinterpret_cast<uint4*>(dst + i * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
 }
 
 // Bounded wait for *ctr >= target (another CTA's release increments), or abort.
@@ -182,37 +164,43 @@ __device__ __forceinline__ int acq_rel_add(int* ctr, int v) {
   return old;
 }
 
-// One stage of one item: this warp's K blocks (kb % 2 == half) of its 16-row
-// block, four accumulator chains (one per k16 step of a block).
-__device__ __forceinline__ void mma_stage(const uint8_t* sd, int nkb, int kb_first, int kb_step, int blk, int lane,
-                                          uint32_t xa0, float (&acc4)[4][4]) {
-  const int g8 = lane >> 2;
-  const uint8_t* my_data = sd + blk * 512 + lane * 16;
-  const uint8_t* my_sf = sd + kW16SfOff + blk * 64 + g8 * 8;
-#pragma unroll 2
-  for (int kb = kb_first; kb < nkb; kb += kb_step) {
-    const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * kW16Chunk);
-    const uint2 sq = *reinterpret_cast<const uint2*>(my_sf + kb * kW16Chunk);
-    const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
-    uint32_t bf[8];
-    const uint32_t xa = xa0 + (uint32_t)(kb * 64) * 2;
-    ldsm_x4(xa, bf[0], bf[1], bf[2], bf[3]);
-    ldsm_x4(xa + 64, bf[4], bf[5], bf[6], bf[7]);
+// out[t, col .. col+8) = sum_j y[inv[t, j]] (j = 0..k-1 in order) + y_shared[t]
+// in fp32, rounded once to bf16: the same sum, in the same order, as the
+// multi-kernel path's combine. All of the token's row loads are issued
+// before the first add (no chain of dependent loads).
+__device__ __forceinline__ void combine_cols8(const Args& p, const int32_t* inv, int t, int k, int H, int col) {
+  float acc[8];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t a[4];
-      cvt_e2m1x8_f16(wv[s], a);
-      const uint32_t pr = cvt_e4m3x2_f16x2(((s < 2 ? sq.x : sq.y) >> (16 * (s & 1))) & 0xffffu);
-      const __half2 sp = *reinterpret_cast<const __half2*>(&pr);
-      const __half2 sg = __low2half2(sp), s8 = __high2half2(sp);
-      __half2* ah = reinterpret_cast<__half2*>(a);
-      ah[0] = __hmul2(ah[0], sg);
-      ah[1] = __hmul2(ah[1], s8);
-      ah[2] = __hmul2(ah[2], sg);
-      ah[3] = __hmul2(ah[3], s8);
-      mma_f16_16816(acc4[s], a, bf[2 * s], bf[2 * s + 1]);
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = j0 + u < k ? __ldcg(reinterpret_cast<const uint4*>(p.y + (size_t)inv[t * k + j0 + u] * H + col))
+                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (j0 + u >= k) break;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+      }
     }
   }
+  if (p.has_shared) {
+    const float4* ys = reinterpret_cast<const float4*>(p.y_shared + (size_t)t * H + col);
+    const float4 a = __ldcg(ys), b = __ldcg(ys + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = (uint32_t)float_to_bf16_bits(acc[2 * i]) | ((uint32_t)float_to_bf16_bits(acc[2 * i + 1]) << 16);
+  *reinterpret_cast<uint4*>(p.out + (size_t)t * H + col) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
@@ -222,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   const int P = T * k;
   const int KB1 = H / 64, KB2 = I / 64;
   const int MT1 = (2 * I) / kTile, MT2 = H / kTile;
-  const int KBS1 = w16_stage_kb(KB1), KBS2 = w16_stage_kb(KB2);   // K blocks per stage of each phase
+  const size_t kStageBytes = (size_t)p.stage_kb * kW16Chunk;   // ring slot: the larger phase's stage
+  const int KBS1 = w16_stage_kb(KB1, p.kmax), KBS2 = w16_stage_kb(KB2, p.kmax);   // K blocks per stage
   const int NST1 = (KB1 + KBS1 - 1) / KBS1, NST2 = (KB2 + KBS2 - 1) / KBS2;
   const int xs_stride = H + 8;    // f16 per resident x row (16-byte pad: conflict-free ldmatrix)
   const int hs_stride = I + 8;
@@ -243,40 +232,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       mbar_init(&sm->empty[i], kBlockWarps);  // the half that reads the stage
     }
     for (int i = 0; i < kHSlots; ++i) {
+      mbar_init(&sm->hland[i], 1);
       mbar_init(&sm->hfull[i], 1);
       mbar_init(&sm->hempty[i], kMmaWarps);
     }
-    for (int i = 0; i < kBlockWarps; ++i) {
-      mbar_init(&sm->red_full[i], 1);
-      mbar_init(&sm->red_empty[i], 1);
-    }
+    decode::half_join_init(&sm->join, 0, 1);
     mbar_init(&sm->xfree, kMmaWarps);
+    mbar_init(&sm->xfull, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm->done[i], kBlockWarps);
-      mbar_init(&sm->done_free[i], 1);
     }
     sm->abort = 0;
+    sm->released = 0;
     fence_barrier_init();
   }
   for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
+  __syncthreads();   // barriers initialised
+  if (warp == kProducerWarp && lane == 0) {
+    // the T x rows (bf16) into the activation area, one bulk copy per row
+    mbar_arrive_expect_tx(&sm->xfull, (uint32_t)(T * H * 2));
+    for (int t = 0; t < T; ++t)
+      bulk_g2s(smem_u32(act + (size_t)t * xs_stride), p.x + (size_t)t * H, (uint32_t)(H * 2), &sm->xfull);
+  }
   if (warp < T) {
     route_token<kMaxK>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
   } else if (warp >= kBlockWarps && warp < kBlockWarps + T) {
-    // x row t -> f16 with its row scale, resident for the gate/up items
+    // x row t -> f16 in place with its row scale, resident for the gate/up items
     const int t = warp - kBlockWarps;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H);
-    uint32_t m = 0;
-    for (int i = lane; i < H / 8; i += 32) {
-      const uint4 v = __ldg(src + i);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    if (mbar_wait(&sm->xfull, 0, abort, limit)) {
+      uint4* row = reinterpret_cast<uint4*>(act + (size_t)t * xs_stride);
+      uint32_t m = 0;
+      for (int i = lane; i < H / 8; i += 32) {
+        const uint4 v = row[i];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) m = max(m, max(finite_mag(wv[q] & 0x7fffu), finite_mag((wv[q] >> 16) & 0x7fffu)));
+        for (int q = 0; q < 4; ++q)
+          m = max(m, max(finite_mag(wv[q] & 0x7fffu), finite_mag((wv[q] >> 16) & 0x7fffu)));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const int sh = row_shift(m);
+      const float up = __int_as_float((127 + sh) << 23);
+      for (int i = lane; i < H / 8; i += 32) {
+        const uint4 v = row[i];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(wv[q] << 16) * up,
+                                               __uint_as_float(wv[q] & 0xffff0000u) * up);
+          o[q] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        row[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (lane == 0) sm->xmul[t] = __int_as_float((127 - sh) << 23);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-    const int sh = row_shift(m);
-    stage_row(p.x + (size_t)t * H, act + (size_t)t * xs_stride, H, sh, lane, false);
-    if (lane == 0) sm->xmul[t] = __int_as_float((127 - sh) << 23);
   }
   __syncthreads();
   if (warp == 0) {
@@ -372,10 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         }
       }
       // copies still in flight land before the CTA's shared memory is released
+      // (a fixed limit: the test hook's short wait limit must not cut this short)
       for (int i = max(0, j - S); i < j; ++i) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(&sm->full[i % S], (i / S) & 1) && clock64() - t0 < limit) {
+        while (!mbar_try_wait(&sm->full[i % S], (i / S) & 1) && clock64() - t0 < kDrainLimit) {
         }
+      }
+      const long long t0 = clock64();   // and the x rows (their wait may have given up)
+      while (!mbar_try_wait(&sm->xfull, 0) && clock64() - t0 < kDrainLimit) {
       }
     }
     return;
@@ -385,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // ------------------------------------- h rows of the down items -> f16
     // (the h slots reuse the x rows' shared memory: wait until no MMA warp
     // reads x any more)
-    int m = 0;
+    // The group's h rows (bf16, written by other CTAs and published by the
+    // gu_done release) arrive by bulk copy into the slot and are converted
+    // there in place, as the x rows are.
+    int m = 0, issued = 0;
     const bool xok = mbar_wait(&sm->xfree, 0, abort, limit);
     for (int i = d0; i < N2 && xok; i += nC, ++m) {
       const int slot = m % kHSlots;
@@ -394,14 +411,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       if (!wait_counter(p.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
       const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
       uint16_t* dst = act + (size_t)slot * kMaxT * hs_stride;
+      if (lane == 0) {
+        // the other CTAs' generic stores of h, acquired above, before the copy engine reads them
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_expect_tx(&sm->hland[slot], (uint32_t)(n * I * 2));
+        for (int q = 0; q < n; ++q)
+          bulk_g2s(smem_u32(dst + (size_t)q * hs_stride), p.h + (size_t)(r0 + q) * I, (uint32_t)(I * 2),
+                   &sm->hland[slot]);
+      }
+      ++issued;
+      const unsigned mx = lane < n ? __ldcg(p.hmax + r0 + lane) : 0u;
+      if (!mbar_wait(&sm->hland[slot], (m / kHSlots) & 1, abort, limit)) break;
       for (int q = 0; q < n; ++q) {
-        const unsigned mx = __ldcg(p.hmax + r0 + q);
-        const int sh = row_shift(mx);
-        stage_row(p.h + (size_t)(r0 + q) * I, dst + (size_t)q * hs_stride, I, sh, lane, true);
+        const int sh = row_shift(__shfl_sync(0xffffffffu, mx, q));
+        const float up = __int_as_float((127 + sh) << 23);
+        uint4* row = reinterpret_cast<uint4*>(dst + (size_t)q * hs_stride);
+        for (int c = lane; c < I / 8; c += 32) {
+          const uint4 v = row[c];
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 hh = __floats2half2_rn(__uint_as_float(wv[e] << 16) * up,
+                                                 __uint_as_float(wv[e] & 0xffff0000u) * up);
+            o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+          row[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
         if (lane == 0) sm->hmul[slot][q] = __int_as_float((127 - sh) << 23);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->hfull[slot]);
+    }
+    if (lane == 0 && issued > 0) {
+      // the last slot's copies land before the shared memory is released (its
+      // wait may have given up); earlier slots were waited for before reuse
+      const int lm = issued - 1;
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&sm->hland[lm % kHSlots], (lm / kHSlots) & 1) && clock64() - t0 < kDrainLimit) {
+      }
     }
     if (lane == 0 && *abort) set_status(p.status, MOE_ERR_TIMEOUT);
     return;
@@ -440,27 +488,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
             }
             unsigned todo = __ballot_sync(0xffffffffu, last);
             __threadfence();
-            while (todo) {  // two completed (token, 16 columns) at a time, 16 lanes each
-              const int s0 = __ffs(todo) - 1;
-              todo &= todo - 1;
-              const int s1 = todo ? __ffs(todo) - 1 : -1;
-              if (s1 >= 0) todo &= todo - 1;
-              const int src = lane < 16 ? s0 : s1;
-              const int t = __shfl_sync(0xffffffffu, tok, src < 0 ? 0 : src);
-              const int c16 = __shfl_sync(0xffffffffu, cb, src < 0 ? 0 : src);
-              if (src >= 0) {
-                const int col = c16 * 16 + (lane & 15);
-                float acc = 0.0f;
-                for (int jj = 0; jj < k; ++jj)
-                  acc += bf16_bits_to_float(__ldcg(p.y + (size_t)sm->inv[t * k + jj] * H + col));
-                if (p.has_shared) acc += __ldcg(p.y_shared + (size_t)t * H + col);
-                p.out[(size_t)t * H + col] = float_to_bf16_bits(acc);
+            while (todo) {  // up to 16 completed (token, 16 columns) at a time, two lanes (8 columns) each
+              const int nb = __popc(todo);
+              const int sub = lane >> 1;
+              unsigned m = todo;
+              for (int q = 0; q < sub && m; ++q) m &= m - 1;   // this lane pair's set bit: the sub-th
+              const int src = (sub < nb) ? __ffs(m) - 1 : 0;
+              const int t = __shfl_sync(0xffffffffu, tok, src);
+              const int c16 = __shfl_sync(0xffffffffu, cb, src);
+              if (sub < nb) combine_cols8(p, sm->inv, t, k, H, c16 * 16 + (lane & 1) * 8);
+              if (nb <= 16) {
+                todo = 0;
+              } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) todo &= todo - 1;
               }
             }
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->done_free[ds]);
+        if (lane == 0) {
+          __threadfence_block();
+          *reinterpret_cast<volatile int*>(&sm->released) = cnt_items + 1;
+        }
       }
     }
     if (lane == 0 && *abort) set_status(p.status, MOE_ERR_TIMEOUT);
@@ -472,7 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   const int g8 = lane >> 2, t4 = lane & 3;
   const int lrow = lane & 7, lq = lane >> 3;
   int j = 0, m = 0, cnt_items = 0;
-  uint32_t rphase = 0;
   bool ok = true;
   bool x_released = false;
   for (int ph = 0; ph < 2 && ok; ++ph) {
@@ -509,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         const int slot = j % S;
         if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, limit)) { ok = false; break; }
         const int kb0 = st * KBS;
-        mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), 0, 1, blk, lane,
+        decode::mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), 0, 1, blk, lane,
                   xa0 + (uint32_t)(kb0 * 64) * 2, acc4);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[slot]);
@@ -532,26 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       float acc[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[q] = (acc4[0][q] + acc4[1][q]) + (acc4[2][q] + acc4[3][q]);
-      // the second half hands its partial sums to the first, which adds them
-      if (half != 0) {
-        if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, limit)) { ok = false; break; }
-        sm->red[blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->red_full[blk]);
-        rphase ^= 1u;
-        continue;
-      }
-      if (!mbar_wait(&sm->red_full[blk], rphase, abort, limit)) { ok = false; break; }
-      {
-        const float4 o = sm->red[blk][lane];
-        acc[0] += o.x;
-        acc[1] += o.y;
-        acc[2] += o.z;
-        acc[3] += o.w;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->red_empty[blk]);
-      rphase ^= 1u;
+      // the half that comes second sums and runs the epilogue
+      bool second = false;
+      if (!decode::half_join(&sm->join, blk, lane, cnt_items, acc, second, abort, limit)) { ok = false; break; }
+      if (!second) continue;
 
       const uint8_t* wb = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
                                   : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
@@ -606,7 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       // hand the item to the signal warp (its slot must be free: taken over
       // two items ago)
       const int ds = cnt_items & 1;
-      if (!mbar_wait(&sm->done_free[ds], ((cnt_items >> 1) & 1) ^ 1, abort, limit)) { ok = false; break; }
+      int freed = 1;
+      if (lane == 0) freed = decode::spin_ge(&sm->released, cnt_items - 1, abort, limit);
+      if (!__shfl_sync(0xffffffffu, freed, 0)) { ok = false; break; }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->done[ds]);
     }
@@ -616,15 +651,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
 
 }  // namespace
 
-static size_t fused_smem_bytes(int T, int H, int I, int E, int slots) {
+static size_t fused_smem_bytes(int T, int H, int I, int E, int slots, int stage_kb) {
   const size_t act = std::max((size_t)T * (H + 8), (size_t)kHSlots * kMaxT * (I + 8)) * 2;
-  return (size_t)slots * kStageBytes + act + sizeof(Smem) + (size_t)E * sizeof(int);
+  return (size_t)slots * stage_kb * kW16Chunk + act + sizeof(Smem) + (size_t)E * sizeof(int);
+}
+
+// Ring slots for a stage size: as many as fit, at most 144 KB of ring (four
+// 36 KB stages, eight 18 KB ones), never fewer than 4, and always even. The
+// halves take alternate stages, so with an even ring a slot's previous stage
+// belongs to the same half, which consumed it before it waits on the slot
+// again; with an odd ring the previous stage is the other half's, and a half
+// running ahead could find that earlier phase still incomplete and take the
+// parity of the phase before it as its own.
+static int fused_slots(int T, int H, int I, int E, int stage_kb) {
+  int slots = std::min(kMaxSlots, (int)((144 * 1024) / ((size_t)stage_kb * kW16Chunk)));
+  slots -= slots % kHalves;
+  while (slots > 4 && fused_smem_bytes(T, H, I, E, slots, stage_kb) > 227 * 1024) slots -= kHalves;
+  return slots;
+}
+
+// Ring slot size in K blocks: the larger stage of the two phases.
+static int fused_stage_kb(int H, int I) {
+  return std::max(w16_stage_kb(H / 64, decode_stage_kb()), w16_stage_kb(I / 64, decode_stage_kb()));
 }
 
 bool decode_fused_supported(int T, int H, int I, int E, int k) {
   if (T < 1 || T > kMaxT || k > kMaxK || E > 1024) return false;
   if (H % kTile || (2 * I) % kTile || I % 64) return false;
-  return fused_smem_bytes(T, H, I, E, 4) <= 227 * 1024;
+  const int skb = fused_stage_kb(H, I);
+  return fused_smem_bytes(T, H, I, E, fused_slots(T, H, I, E, skb), skb) <= 227 * 1024;
 }
 
 moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s) {
@@ -655,11 +710,13 @@ moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s) {
   a.status = q.status;
   a.wait_limit = q.wait_limit;
   a.extra_arrivals = q.extra_arrivals;
-  int slots = kMaxSlots;
-  while (slots > 4 && fused_smem_bytes(q.T, q.H, q.I, q.E, slots) > 227 * 1024) --slots;
-  if (fused_smem_bytes(q.T, q.H, q.I, q.E, slots) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+  const int skb = fused_stage_kb(q.H, q.I);
+  const int slots = fused_slots(q.T, q.H, q.I, q.E, skb);
+  if (fused_smem_bytes(q.T, q.H, q.I, q.E, slots, skb) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
   a.slots = slots;
-  const size_t smem = fused_smem_bytes(q.T, q.H, q.I, q.E, slots);
+  a.stage_kb = skb;
+  a.kmax = decode_stage_kb();
+  const size_t smem = fused_smem_bytes(q.T, q.H, q.I, q.E, slots, skb);
   int dev = 0, sms = 0;
   moe_status st = cuda_ok(cudaGetDevice(&dev));
   if (st != MOE_OK) return st;

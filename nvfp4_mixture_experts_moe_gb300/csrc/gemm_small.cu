@@ -9,12 +9,13 @@
 // At a few rows per expert the layer is bound by the bytes of the touched
 // experts' weights ("Seven Months of GB10 Field Notes": decode re-reads the
 // active weights). Each weight byte is read from HBM once. One producer warp
-// streams the weight tiles with bulk copies (cp.async.bulk, one 36 KB copy
-// per stage of up to 8 K blocks, completion on mbarriers) into a ring of
-// 36 KB shared-memory stages. Sixteen MMA warps: warp b of part h owns
-// the 16-row block b of a 128-row item for the stages j with j % 2 == h, and
-// part 1 hands its partial sums to part 0 at the end of the item (more warps
-// per scheduler hide the conversion -> multiply -> MMA latency chains). A
+// streams the weight tiles with bulk copies (cp.async.bulk, one copy per
+// stage of up to 8 K blocks (36 KB), completion on mbarriers) into a ring of
+// shared-memory stages. Sixteen MMA warps: warp b of part h owns
+// the 16-row block b of a 128-row item for the stages j with j % 2 == h (more
+// warps per scheduler hide the conversion -> multiply -> MMA latency chains);
+// at the end of an item the part that finishes second adds the other's
+// partial sums and runs the epilogue, while the first goes on. A
 // warp loads its 16-byte A fragment per 64-wide K block from shared memory,
 // turns the e2m1 codes into f16 with the hardware e2m1x2 conversion, multiplies in the E4M3 block scales (e2m1 * e4m3 is exact in
 // f16) and feeds mma.sync m16n8k16 with the group's rows (up to 8) as N.
@@ -33,6 +34,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "decode_mma.cuh"
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,20 +44,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBlockWarps = 8;                   // one per 16-row block of a 128-row item
+using decode::kBlockWarps;   // one per 16-row block of a 128-row item
 // K split: part h takes the ring stages j with j % kHalves == h (j counts the
-// stages of all items in order). A part waits for stage j only after it
-// consumed stage j - kHalves, so with at least kHalves ring slots it never
-// waits on a slot two phases ahead (an mbarrier parity wait cannot tell those
-// apart).
-constexpr int kHalves = 2;
+// stages of all items in order). The ring has a multiple of kHalves slots, so
+// the previous stage of a slot (j - S) belongs to the same part, which
+// consumed it before it waits for stage j: the slot's barrier is then never
+// a phase behind (an mbarrier parity wait cannot tell phase n from n - 2).
+using decode::kHalves;
 constexpr int kMmaWarps = kBlockWarps * kHalves;
 constexpr int kThreads = (kMmaWarps + 1) * 32;  // + one producer warp
 constexpr int kRowsPerPass = 8;
 constexpr int kTileRows = 128;                   // weight rows per item
 constexpr int kMaxGroups = 1025;
-constexpr int kMaxBlocksPerStage = 8;            // 64-wide K blocks per stage (up to 512 K)
-constexpr int kStageBytes = kMaxBlocksPerStage * kW16Chunk;  // 36 KB ring slots: an item's chunks of up to 8 K blocks
+constexpr int kMaxSlots = 16;                    // ring slots of stage_kb K blocks (stage_kb * 4608 bytes)
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
 
 struct SmallArgs {
@@ -71,21 +72,20 @@ struct SmallArgs {
   float* out_last_f32;
   int rows_limit;
   int stages;
+  int stage_kb;       // max 64-wide K blocks per ring stage (1..8)
   int early_weights;  // stream weights before the dependency wait (offsets already final)
   int* status;
   long long wait_limit;  // cycles per bounded wait (a timeout aborts the kernel)
 };
 
 struct SmallSmem {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t full[kMaxSlots];
+  uint64_t empty[kMaxSlots];
   uint64_t xsync;                  // the MMA warps' barrier around x staging (one arrival per warp)
-  uint64_t red_full[kBlockWarps];  // parts 1.. -> part 0: partial sums of block b written
-  uint64_t red_empty[kBlockWarps]; // part 0 -> parts 1..: read
   int abort;
   float row_mul[kRowsPerPass];
   int row_out[kRowsPerPass];
-  float4 red[kHalves - 1][kBlockWarps][32];  // parts 1..'s partial sums (per lane: rows g, g+8 x 2 columns)
+  decode::HalfJoin join;           // the two parts' partial sums of an item
 };
 
 __device__ __forceinline__ int group_items(const int32_t* off, int g, int mt_count, int limit) {
@@ -101,12 +101,6 @@ __device__ __forceinline__ int find_group(const int* pref, int G, int item) {
     if (pref[mid] <= item) lo = mid; else hi = mid - 1;
   }
   return lo;
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
 }
 
 // Barrier over the MMA warps (the producer never joins) on an mbarrier, with
@@ -126,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int K = p.K, N = p.N;
   const int S = p.stages;
+  const size_t kStageBytes = (size_t)p.stage_kb * kW16Chunk;
   const int xs_stride = K + 8;  // f16 elements per staged row (16-byte pad: conflict-free ldmatrix)
   uint8_t* stages = smem_raw;                                                   // S x kStageBytes
   uint16_t* xs = reinterpret_cast<uint16_t*>(stages + (size_t)S * kStageBytes);  // [8][K+8]
@@ -136,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
   const int mt_count = N / kTileRows;
   const int G = p.G;
   const int kblocks = K / 64;
-  const int kBlocksPerStage = w16_stage_kb(kblocks);
+  const int kBlocksPerStage = w16_stage_kb(kblocks, p.stage_kb);
   const int nstage = (kblocks + kBlocksPerStage - 1) / kBlocksPerStage;
   if (!p.early_weights) pdl_wait();
 
@@ -148,10 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       mbar_init(&sm->empty[i], kBlockWarps);  // the eight warps of the half that read the stage
     }
     mbar_init(&sm->xsync, kMmaWarps);
-    for (int b = 0; b < kBlockWarps; ++b) {
-      mbar_init(&sm->red_full[b], kHalves - 1);
-      mbar_init(&sm->red_empty[b], 1);
-    }
+    decode::half_join_init(&sm->join, 0, 1);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -213,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
   const int blk = warp % kBlockWarps, half = warp / kBlockWarps;
   const int g8 = lane >> 2, t4 = lane & 3;
   int cur_g = -1, cur_c = -1;
-  int j = 0;
-  uint32_t xphase = 0, rphase = 0;
+  int j = 0, tile = 0;
+  uint32_t xphase = 0;
   // ldmatrix row address of this lane: matrix q = lane / 8 covers the 8
   // staged rows at k offset 8 * q (two k16 steps per ldmatrix.x4)
   const int lrow = lane & 7, lq = lane >> 3;
@@ -288,36 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       const int slot = j % S;
       if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, p.wait_limit)) { ok = false; break; }
       const int kb0 = st * kBlocksPerStage;
-      const int nkb = min(kBlocksPerStage, kblocks - kb0);
-      const uint8_t* sd = stages + (size_t)slot * kStageBytes;
-      const uint8_t* my_data = sd + blk * 512 + lane * 16;
-      const uint8_t* my_sf = sd + kW16SfOff + blk * 64 + g8 * 8;
-#pragma unroll 2
-      for (int kb = 0; kb < nkb; ++kb) {
-        const uint4 wq = *reinterpret_cast<const uint4*>(my_data + kb * kW16Chunk);
-        const uint2 sq = *reinterpret_cast<const uint2*>(my_sf + kb * kW16Chunk);
-        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
-        // B fragments of the 4 k16 steps: two ldmatrix.x4 (steps 0-1, 2-3)
-        uint32_t bf[8];
-        const uint32_t xa = xbase + (uint32_t)((kb0 + kb) * 64) * 2;
-        ldsm_x4(xa, bf[0], bf[1], bf[2], bf[3]);
-        ldsm_x4(xa + 64, bf[4], bf[5], bf[6], bf[7]);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint32_t a[4];
-          cvt_e2m1x8_f16(wv[s], a);
-          // (scale of row g, scale of row g+8) for step s
-          const uint32_t pr = cvt_e4m3x2_f16x2(((s < 2 ? sq.x : sq.y) >> (16 * (s & 1))) & 0xffffu);
-          const __half2 sp = *reinterpret_cast<const __half2*>(&pr);
-          const __half2 sg = __low2half2(sp), s8 = __high2half2(sp);
-          __half2* ah = reinterpret_cast<__half2*>(a);
-          ah[0] = __hmul2(ah[0], sg);
-          ah[1] = __hmul2(ah[1], s8);
-          ah[2] = __hmul2(ah[2], sg);
-          ah[3] = __hmul2(ah[3], s8);
-          mma_f16_16816(acc4[s], a, bf[2 * s], bf[2 * s + 1]);
-        }
-      }
+      decode::mma_stage(stages + (size_t)slot * kStageBytes, min(kBlocksPerStage, kblocks - kb0), 0, 1, blk, lane,
+                        xbase + (uint32_t)(kb0 * 64) * 2, acc4);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->empty[slot]);
     }
@@ -326,28 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = (acc4[0][q] + acc4[1][q]) + (acc4[2][q] + acc4[3][q]);
 
-    // split-K reduction: parts 1.. hand their partial sums to part 0, which
-    // adds them in a fixed order (part 0, 1, 2, ...)
-    if (half != 0) {
-      if (!mbar_wait(&sm->red_empty[blk], rphase ^ 1u, abort, p.wait_limit)) break;
-      sm->red[half - 1][blk][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->red_full[blk]);
-      rphase ^= 1u;
-      continue;
-    }
-    if (!mbar_wait(&sm->red_full[blk], rphase, abort, p.wait_limit)) break;
-#pragma unroll
-    for (int h = 0; h < kHalves - 1; ++h) {
-      const float4 o = sm->red[h][blk][lane];
-      acc[0] += o.x;
-      acc[1] += o.y;
-      acc[2] += o.z;
-      acc[3] += o.w;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->red_empty[blk]);
-    rphase ^= 1u;
+    // split-K join: the part that comes second sums and runs the epilogue
+    bool second = false;
+    if (!decode::half_join(&sm->join, blk, lane, tile++, acc, second, abort, p.wait_limit)) break;
+    if (!second) continue;
 
     // Epilogue: c0,c1 = row g (tokens 2t, 2t+1); c2,c3 = row g+8.
     const uint8_t* wb = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
@@ -388,8 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
 
 }  // namespace
 
-static size_t small_smem_bytes(int K, int G, int S) {
-  return (size_t)S * kStageBytes + (size_t)kRowsPerPass * (K + 8) * 2 + sizeof(SmallSmem) + (size_t)(G + 1) * 4;
+static size_t small_smem_bytes(int K, int G, int S, int stage_kb) {
+  return (size_t)S * stage_kb * kW16Chunk + (size_t)kRowsPerPass * (K + 8) * 2 + sizeof(SmallSmem) +
+         (size_t)(G + 1) * 4;
 }
 
 moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStream_t s) {
@@ -413,9 +360,14 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStrea
   a.wait_limit = debug_wait_limit();
   a.early_weights = pl.pdl && pl.early_weights ? 1 : 0;
   const size_t limit = 227 * 1024;
-  int S = 6;
-  while (S > kHalves && small_smem_bytes(pl.K, pl.num_groups, S) > limit) --S;
-  const size_t smem = small_smem_bytes(pl.K, pl.num_groups, S);
+  // ring slots of one stage of this K; as many as fit, up to 216 KB of ring
+  // (eight 27 KB stages, or six 36 KB ones)
+  const int skb = w16_stage_kb(pl.K / 64, decode_stage_kb());
+  a.stage_kb = skb;
+  int S = std::min(kMaxSlots, (int)((216 * 1024) / ((size_t)skb * kW16Chunk)));
+  S -= S % kHalves;
+  while (S > kHalves && small_smem_bytes(pl.K, pl.num_groups, S, skb) > limit) S -= kHalves;
+  const size_t smem = small_smem_bytes(pl.K, pl.num_groups, S, skb);
   if (smem > limit) return MOE_ERR_UNSUPPORTED;  // K too large for the staged rows and kHalves slots
   a.stages = S;
   int dev = 0, sms = 148;

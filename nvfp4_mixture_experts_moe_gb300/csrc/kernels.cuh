@@ -195,5 +195,6 @@ moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s);
 long long debug_wait_limit();     // cycles per bounded device wait (default 4e9, about 2 s)
 int debug_extra_arrivals();       // 0 normally
 bool debug_decode_fused_disabled();
+int decode_stage_kb();             // max 64-wide K blocks per ring stage of the decode GEMMs (1..8)
 
 }  // namespace moe

@@ -504,16 +504,31 @@ __device__ __forceinline__ void combine_token(const uint16_t* __restrict__ y, co
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int row = __ldg(inv_perm + (size_t)t * k + j);
-    if (row < 0) continue;
-    const float wt = topk_w != nullptr ? __ldg(topk_w + (size_t)t * k + j) : 1.0f;
-    const uint4 v = ldg_stream(y + (size_t)row * H + (size_t)c8 * 8);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // the token's rows eight at a time: every index, then every row load, is
+  // issued before the first use (no chain of dependent loads per row); the
+  // sum still runs j = 0, 1, ... in order
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int row[8];
+    float wt[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += __uint_as_float(w[i] << 16) * wt;
-      acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u) * wt;
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      row[u] = j < k ? __ldg(inv_perm + (size_t)t * k + j) : -1;
+      wt[u] = (j < k && topk_w != nullptr) ? __ldg(topk_w + (size_t)t * k + j) : 1.0f;
+    }
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = row[u] >= 0 ? ldg_stream(y + (size_t)row[u] * H + (size_t)c8 * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (row[u] < 0) continue;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16) * wt[u];
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u) * wt[u];
+      }
     }
   }
   if (y_shared != nullptr) {

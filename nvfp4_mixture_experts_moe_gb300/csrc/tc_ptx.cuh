@@ -43,19 +43,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of one phase (try_wait may suspend the thread for a
+// while before it reports an incomplete phase; test_wait never does).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on one phase of an mbarrier. Gives up after `limit` clock
-// cycles or as soon as *abort is set, sets *abort and returns false.
+// cycles or as soon as *abort is set, sets *abort and returns false. The
+// clock is checked before every blocking try, so a wait that is not already
+// complete at the first (non-blocking) test gives up at once when `limit` is
+// a few cycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           long long limit) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
   }
 }
 
