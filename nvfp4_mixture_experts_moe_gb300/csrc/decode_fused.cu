@@ -18,13 +18,17 @@
 //   copy and are converted in place to f16 with a power-of-two row scale;
 //   they stay resident for the gate/up phase.
 // * Work items are (active expert group, 128-row weight tile): gate/up items
-//   first, then down items, taken by the CTAs in a strided order (gate/up
-//   items ascending, down items descending over the CTAs, so the CTAs with
-//   one gate/up item more get one down item fewer).
-// * One producer warp streams every item's weight tiles (stages of up to 8
-//   64-wide K blocks, 36 KB, in a ring of as many as fit) with bulk copies from the
-//   gate/up phase straight into the down phase, so the down weights are
-//   already in flight when the gate/up items end.
+//   0..N1-1, then down items. Each CTA's producer takes the next item from a
+//   grid-wide counter when it is about to stream the last stage of its
+//   current one, so CTAs that stream faster take more items and all finish
+//   within about one item of each other. A CTA's items increase, so a down
+//   item's group has had all its gate/up items taken before (long before, in
+//   all but the last groups). The producer publishes each item in a small
+//   per-CTA queue that the other warps read in order.
+// * The producer streams every item's weight tiles (stages of up to 8
+//   64-wide K blocks, 36 KB, in a ring of as many as fit) with bulk copies
+//   from the gate/up phase straight into the down phase, so the down weights
+//   are already in flight when the gate/up items end.
 // * Sixteen MMA warps (8 row blocks x 2 halves that take alternate stages)
 //   turn the e2m1 codes into f16 with the hardware conversion, multiply in
 //   the E4M3 block scales and run mma.sync m16n8k16 with the group's rows as
@@ -76,6 +80,7 @@ constexpr int kMaxSlots = 16;                      // ring slots of stage_kb K b
 constexpr int kHSlots = 2;                         // staged h row sets (down items)
 constexpr int kMaxRows = kMaxT * kMaxK + kMaxT;    // routed pairs + shared rows
 constexpr int kMaxGroups = kMaxT * kMaxK + 1;      // active groups: at most one per pair, + shared
+constexpr int kQueue = 8;                          // the CTA's published items not yet taken over
 constexpr long long kDrainLimit = 4ll * 1000 * 1000 * 1000;  // cycles for in-flight copies to land
 
 struct Args {
@@ -95,6 +100,7 @@ struct Args {
   float* y_shared;      // [T, H] the shared expert's rows, fp32
   int* gu_done;         // [groups] (zeroed by the caller)
   int* cmb_cnt;         // [T][H/16] (zeroed)
+  int* next_item;       // grid-wide item counter (zeroed)
   unsigned* hmax;       // [rows] bf16 magnitude bits of max |h| (zeroed)
   int* status;
   int slots;
@@ -114,12 +120,16 @@ struct Smem {
   uint64_t xfree;                // every MMA warp is done with the resident x rows
   uint64_t done[2];              // an item's epilogue stores are issued (one warp per row block)
   int released;                  // items the signal warp has taken over (counts up; no parity aliasing)
+  int q_item[kQueue];            // the CTA's c-th item at c % kQueue (-1: no more items)
+  int q_count;                   // items published
+  int first_down;                // index c of the CTA's first down item (or of the end)
   int abort;
   int A;                         // active groups
   int32_t ids[kMaxT * kMaxK];
   float w[kMaxT * kMaxK];
   int32_t inv[kMaxT * kMaxK];    // pair -> grouped row
   int32_t row_tok[kMaxRows];
+  int32_t row_e[kMaxT * kMaxK];  // expert of grouped row r (routed rows)
   float row_w[kMaxRows];
   int32_t grp_e[kMaxGroups];     // expert of active group a (E = shared)
   int32_t grp_r0[kMaxGroups];
@@ -136,6 +146,27 @@ __device__ __forceinline__ int row_shift(uint32_t m) {
   const int e = (int)(m >> 7);
   int sh = (m == 0) ? 0 : 141 - max(e, 1);
   return max(-113, min(sh, 126));
+}
+
+// The CTA's c-th item from its queue (lane 0 waits, bounded; broadcast):
+// >= 0 an item, -1 no more items, -2 the wait gave up.
+__device__ __forceinline__ int queue_get(Smem* sm, int c, volatile int* abort, long long limit, int lane) {
+  int v = -2;
+  if (lane == 0 && decode::spin_ge(&sm->q_count, c + 1, abort, limit)) {
+    __threadfence_block();
+    v = *reinterpret_cast<volatile int*>(&sm->q_item[c % kQueue]);
+  }
+  return __shfl_sync(0xffffffffu, v, 0);
+}
+
+// The c-th item if it is published already, else -3 (no wait).
+__device__ __forceinline__ int queue_peek(Smem* sm, int c, int lane) {
+  int v = -3;
+  if (lane == 0 && *reinterpret_cast<volatile int*>(&sm->q_count) > c) {
+    __threadfence_block();
+    v = *reinterpret_cast<volatile int*>(&sm->q_item[c % kQueue]);
+  }
+  return __shfl_sync(0xffffffffu, v, 0);
 }
 
 // Bounded wait for *ctr >= target (another CTA's release increments), or abort.
@@ -219,9 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   uint16_t* act = reinterpret_cast<uint16_t*>(ring + (size_t)S * kStageBytes);
   const size_t act_elems = max((size_t)T * xs_stride, (size_t)kHSlots * kMaxT * hs_stride);
   Smem* sm = reinterpret_cast<Smem*>(act + act_elems);
-  int* cnt = reinterpret_cast<int*>(sm + 1);   // [E] expert histogram, then offsets
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nC = gridDim.x, b = blockIdx.x;
+  const int b = blockIdx.x;
   volatile int* abort = &sm->abort;
   const long long limit = p.wait_limit;
 
@@ -244,10 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     }
     sm->abort = 0;
     sm->released = 0;
+    sm->q_count = 0;
+    sm->first_down = 0;
     fence_barrier_init();
   }
-  for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
   __syncthreads();   // barriers initialised
+  int first_item = 0;
+  if (warp == kProducerWarp && lane == 0) first_item = atomicAdd(p.next_item, 1);   // latency hidden by phase 0
   if (warp == kProducerWarp && lane == 0) {
     // the T x rows (bf16) into the activation area, one bulk copy per row
     mbar_arrive_expect_tx(&sm->xfull, (uint32_t)(T * H * 2));
@@ -255,7 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       bulk_g2s(smem_u32(act + (size_t)t * xs_stride), p.x + (size_t)t * H, (uint32_t)(H * 2), &sm->xfull);
   }
   if (warp < T) {
-    route_token<kMaxK>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
+    // registers per lane sized to E (E <= 32, 128, 320, 1024)
+    if (E <= 32)
+      route_token<1>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
+    else if (E <= 128)
+      route_token<4>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
+    else if (E <= 320)
+      route_token<10>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
+    else
+      route_token<32>(p.logits, warp, E, k, nullptr, nullptr, sm->ids, sm->w);
   } else if (warp >= kBlockWarps && warp < kBlockWarps + T) {
     // x row t -> f16 in place with its row scale, resident for the gate/up items
     const int t = warp - kBlockWarps;
@@ -289,50 +330,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     }
   }
   __syncthreads();
+  if (tid < P) {
+    // rank of pair q in the order (expert, pair index): its grouped row, so
+    // the rows of an expert keep the pairs' order (a stable sort, the same
+    // permutation as the multi-kernel path's)
+    const int q = tid, e = sm->ids[q];
+    int r = 0;
+    for (int q2 = 0; q2 < P; ++q2) {
+      const int e2 = sm->ids[q2];
+      r += (e2 < e || (e2 == e && q2 < q)) ? 1 : 0;
+    }
+    sm->inv[q] = r;
+    sm->row_tok[r] = q / k;
+    sm->row_w[r] = sm->w[q];
+    sm->row_e[r] = e;
+  }
+  __syncthreads();
   if (warp == 0) {
-    // stable counting sort of the pairs by expert, active groups in expert order
-    for (int q = lane; q < P; q += 32) atomicAdd(&cnt[sm->ids[q]], 1);
-    __syncwarp();
-    int base = 0, na = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int c = e < E ? cnt[e] : 0;
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
+    // active groups in expert order: a group starts where the expert changes
+    int na = 0;
+    for (int r0 = 0; r0 < P; r0 += 32) {
+      const int r = r0 + lane;
+      const bool start = r < P && (r == 0 || sm->row_e[r] != sm->row_e[r - 1]);
+      const unsigned starts = __ballot_sync(0xffffffffu, start);
+      if (start) {
+        const int a = na + __popc(starts & ((1u << lane) - 1u));
+        sm->grp_e[a] = sm->row_e[r];
+        sm->grp_r0[a] = r;
       }
-      const unsigned act_mask = __ballot_sync(0xffffffffu, c > 0);
-      if (c > 0) {
-        const int a = na + __popc(act_mask & ((1u << lane) - 1u));
-        sm->grp_e[a] = e;
-        sm->grp_r0[a] = base + incl - c;
-        // top-k picks distinct experts, so a group holds at most one row per
-        // token (<= kMaxT); the clamp keeps any input inside the staging buffers
-        sm->grp_n[a] = min(c, kMaxT);
-      }
-      if (e < E) cnt[e] = base + incl - c;   // becomes the group's cursor
-      base += __shfl_sync(0xffffffffu, incl, 31);
-      na += __popc(act_mask);
+      na += __popc(starts);
     }
     __syncwarp();
-    for (int q0 = 0; q0 < P; q0 += 32) {   // pairs in order: a pair's row grows with its index
-      const int q = q0 + lane;
-      const int e = q < P ? sm->ids[q] : -1 - lane;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      int r = 0;
-      if (q < P) r = cnt[e] + rank;
-      __syncwarp();
-      if (q < P) {
-        sm->inv[q] = r;
-        sm->row_tok[r] = q / k;
-        sm->row_w[r] = sm->w[q];
-        if ((peers >> lane) == 1u) cnt[e] += __popc(peers);
-      }
-      __syncwarp();
-    }
+    // top-k picks distinct experts, so a group holds at most one row per
+    // token (<= kMaxT); the clamp keeps any input inside the staging buffers
+    for (int a = lane; a < na; a += 32) sm->grp_n[a] = min((a + 1 < na ? sm->grp_r0[a + 1] : P) - sm->grp_r0[a], kMaxT);
+    __syncwarp();
     if (p.has_shared) {
       if (lane == 0) {
         sm->grp_e[na] = E;
@@ -351,35 +383,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   }
   __syncthreads();
   const int A = sm->A;
-  const int N1 = A * MT1, N2 = A * MT2;
-  // down items of this CTA: i = (nC - 1 - b) + m * nC
-  const int d0 = nC - 1 - b;
+  const int N1 = A * MT1, N2 = A * MT2;   // items: gate/up 0..N1-1, then down N1..N1+N2-1
+  // Items take the groups in the order shared expert first, then the routed
+  // groups by expert: the shared expert's rows are the contributions every
+  // token waits for, and taking them first leaves the last items of the
+  // kernel (whose signal warps sum the finished tokens) few rows each.
+  const int rot = p.has_shared ? A - 1 : 0;
 
   if (warp == kProducerWarp) {
     // --------------------------------------------------------------- producer
+    // Takes the CTA's items one at a time from the grid-wide counter (the
+    // first was taken at entry), publishes each in the CTA's queue for the
+    // other warps, then streams its stages; the next item is taken while
+    // the last stage of the current one streams.
     if (lane == 0) {
-      int j = 0;
-      bool ok = true;
-      for (int ph = 0; ph < 2 && ok; ++ph) {
-        const int first = ph == 0 ? b : d0, N = ph == 0 ? N1 : N2;
+      int j = 0, item = first_item, c = 0;
+      for (;; ++c) {
+        // a queue entry is reused once the signal warp has taken over the
+        // item kQueue places before it (every warp is past that item)
+        if (!decode::spin_ge(&sm->released, c - kQueue + 1, abort, limit)) break;
+        const int pub = item < N1 + N2 ? item : -1;
+        *reinterpret_cast<volatile int*>(&sm->q_item[c % kQueue]) = pub;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&sm->q_count) = c + 1;
+        if (pub < 0) break;
+        const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
         const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
         const int KBS = ph == 0 ? KBS1 : KBS2;
-        for (int i = first; i < N && ok; i += nC) {
-          const int a = i / MT, mt = i % MT;
-          const int e = sm->grp_e[a];
-          const uint8_t* blk = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
-                                       : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
-          const uint8_t* data = blk + sizeof(PrepHeader);
-          for (int st = 0; st < NST; ++st, ++j) {
-            const int slot = j % S;
-            if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, limit)) { ok = false; break; }
-            const int kb0 = st * KBS;
-            const uint32_t bytes = (uint32_t)(min(KBS, KB - kb0) * kW16Chunk);
-            mbar_arrive_expect_tx(&sm->full[slot], bytes);
-            bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, KB), bytes,
-                     &sm->full[slot]);
-          }
+        const int a = (i / MT + rot) % A, mt = i % MT;
+        const int e = sm->grp_e[a];
+        const uint8_t* blk = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
+                                     : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
+        const uint8_t* data = blk + sizeof(PrepHeader);
+        bool ok = true;
+        int next = N1 + N2;
+        for (int st = 0; st < NST; ++st, ++j) {
+          const int slot = j % S;
+          if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, limit)) { ok = false; break; }
+          const int kb0 = st * KBS;
+          const uint32_t bytes = (uint32_t)(min(KBS, KB - kb0) * kW16Chunk);
+          mbar_arrive_expect_tx(&sm->full[slot], bytes);
+          bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, KB), bytes,
+                   &sm->full[slot]);
+          if (st == NST - 1) next = atomicAdd(p.next_item, 1);
         }
+        if (!ok) break;
+        item = next;
       }
       // copies still in flight land before the CTA's shared memory is released
       // (a fixed limit: the test hook's short wait limit must not cut this short)
@@ -402,12 +451,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // The group's h rows (bf16, written by other CTAs and published by the
     // gu_done release) arrive by bulk copy into the slot and are converted
     // there in place, as the x rows are.
+    // The CTA takes its items in increasing order, so every item from its
+    // first down item on is a down item.
     int m = 0, issued = 0;
     const bool xok = mbar_wait(&sm->xfree, 0, abort, limit);
-    for (int i = d0; i < N2 && xok; i += nC, ++m) {
+    for (int c = xok ? sm->first_down : 0; xok; ++c, ++m) {
+      const int item = queue_get(sm, c, abort, limit, lane);
+      if (item < 0) break;   // no more items (-1) or a timeout (-2)
       const int slot = m % kHSlots;
       if (!mbar_wait(&sm->hempty[slot], ((m / kHSlots) & 1) ^ 1, abort, limit)) break;
-      const int a = i / MT2;
+      const int a = ((item - N1) / MT2 + rot) % A;
       if (!wait_counter(p.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
       const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
       uint16_t* dst = act + (size_t)slot * kMaxT * hs_stride;
@@ -465,15 +518,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // that completes one sums the token's rows in the fixed order j = 0..k-1,
     // then the shared row, and writes the bf16 output.
     const int need = k + (p.has_shared ? 1 : 0);
-    int cnt_items = 0;
-    bool ok = true;
-    for (int ph = 0; ph < 2 && ok; ++ph) {
-      const int first = ph == 0 ? b : d0, N = ph == 0 ? N1 : N2;
-      const int MT = ph == 0 ? MT1 : MT2;
-      for (int i = first; i < N; i += nC, ++cnt_items) {
+    for (int cnt_items = 0;; ++cnt_items) {
+      {
+        const int item = queue_get(sm, cnt_items, abort, limit, lane);
+        if (item < 0) break;
+        const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
+        const int MT = ph == 0 ? MT1 : MT2;
         const int ds = cnt_items & 1;
-        if (!mbar_wait(&sm->done[ds], (cnt_items >> 1) & 1, abort, limit)) { ok = false; break; }
-        const int a = i / MT, mt = i % MT;
+        if (!mbar_wait(&sm->done[ds], (cnt_items >> 1) & 1, abort, limit)) break;
+        const int a = (i / MT + rot) % A, mt = i % MT;
         if (ph == 0) {
           if (lane == 0) release_add(p.gu_done + a, 1);
         } else {
@@ -521,20 +574,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   const int blk = warp % kBlockWarps, half = warp / kBlockWarps;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int lrow = lane & 7, lq = lane >> 3;
-  int j = 0, m = 0, cnt_items = 0;
+  int j = 0, m = 0;
   bool ok = true;
   bool x_released = false;
-  for (int ph = 0; ph < 2 && ok; ++ph) {
-    const int first = ph == 0 ? b : d0, N = ph == 0 ? N1 : N2;
-    const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
-    const int KBS = ph == 0 ? KBS1 : KBS2;
-    if (ph == 1 && !x_released) {  // this CTA had no gate/up item
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->xfree);
-      x_released = true;
-    }
-    for (int i = first; i < N; i += nC, ++cnt_items) {
-      const int a = i / MT, mt = i % MT;
+  // x (and the slot of the first down item's h rows, which reuses its shared
+  // memory) is released at the CTA's first down item, or earlier: after the
+  // stage loop of a gate/up item whose successor in the queue is already
+  // known to be a down item (or the end)
+  auto release_x = [&](int c) {
+    if (x_released) return;
+    if (warp == 0 && lane == 0) sm->first_down = c;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->xfree);
+    x_released = true;
+  };
+  for (int cnt_items = 0; ok; ++cnt_items) {
+    {
+      const int item = queue_get(sm, cnt_items, abort, limit, lane);
+      if (item == -2) { ok = false; break; }
+      if (item < 0 || item >= N1) release_x(cnt_items);
+      if (item < 0) break;
+      const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
+      const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
+      const int KBS = ph == 0 ? KBS1 : KBS2;
+      const int a = (i / MT + rot) % A, mt = i % MT;
       const int e = sm->grp_e[a], r0 = sm->grp_r0[a], n = sm->grp_n[a];
       const int hslot = m % kHSlots;
       // ldmatrix row of this lane: the group's row lrow (rows past the group
@@ -566,11 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       if (!ok) break;
       float hm[2] = {1.0f, 1.0f};   // row multipliers of this lane's two token columns
       if (ph == 0) {
-        if (i + nC >= N) {  // last gate/up item of this CTA: x is no longer read
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm->xfree);
-          x_released = true;
-        }
+        const int nx = queue_peek(sm, cnt_items + 1, lane);   // -3: not published yet
+        if (nx == -1 || nx >= N1) release_x(cnt_items + 1);
       } else {  // the staged h rows (and their multipliers) are no longer read
 #pragma unroll
         for (int q = 0; q < 2; ++q) hm[q] = sm->hmul[hslot][min(2 * t4 + q, kMaxT - 1)];
@@ -653,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
 
 static size_t fused_smem_bytes(int T, int H, int I, int E, int slots, int stage_kb) {
   const size_t act = std::max((size_t)T * (H + 8), (size_t)kHSlots * kMaxT * (I + 8)) * 2;
-  return (size_t)slots * stage_kb * kW16Chunk + act + sizeof(Smem) + (size_t)E * sizeof(int);
+  return (size_t)slots * stage_kb * kW16Chunk + act + sizeof(Smem);
 }
 
 // Ring slots for a stage size: as many as fit, at most 144 KB of ring (four
@@ -706,6 +766,7 @@ moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s) {
   a.y_shared = q.y_shared;
   a.gu_done = q.gu_done;
   a.cmb_cnt = q.cmb_cnt;
+  a.next_item = q.next_item;
   a.hmax = q.hmax;
   a.status = q.status;
   a.wait_limit = q.wait_limit;

@@ -184,6 +184,7 @@ struct DecodeFusedPlan {
   int* gu_done;              // [E + 1], zero at launch
   int* cmb_cnt;              // [T * H/16], zero at launch
   unsigned* hmax;            // [T*k + T], zero at launch
+  int* next_item;            // one int, zero at launch (the grid's item counter)
   int* status;
   long long wait_limit;      // cycles per bounded wait
   int extra_arrivals;        // test hook (0): extra arrivals a gate/up tile is expected to make
