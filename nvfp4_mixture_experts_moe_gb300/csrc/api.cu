@@ -109,7 +109,7 @@ struct ForwardWs {
   uint8_t* hsf;       // W4A4: [tiles, I/256, 2048]
   int tiles;          // W4A4: bound on the 128-row tiles of all groups
   float* hgs;
-  int* fused_counters;      // decode micro path: gu_done [E+1], cmb_cnt [T * H/16], hmax [rows], next item
+  int* fused_counters;      // decode micro path: gu_done [E+1], cmb_cnt [T * H/128], hmax [rows], next item
   size_t fused_counter_ints;
   size_t bytes;
 };
@@ -168,7 +168,7 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
     f.tiles = 0;
   }
   if (use_decode_fused(L)) {
-    f.fused_counter_ints = (size_t)(L.E + 1) + (size_t)L.T * (L.H / 16) + rows + 1;
+    f.fused_counter_ints = (size_t)(L.E + 1) + (size_t)L.T * (L.H / 128) + rows + 1;
     f.fused_counters = c.take<int>(f.fused_counter_ints);
   } else {
     f.fused_counters = nullptr;
@@ -550,8 +550,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     q.y_shared = f.ys;
     q.gu_done = f.fused_counters;
     q.cmb_cnt = f.fused_counters + (E + 1);
-    q.hmax = reinterpret_cast<unsigned*>(f.fused_counters + (E + 1) + (size_t)T * (H / 16));
-    q.next_item = f.fused_counters + (E + 1) + (size_t)T * (H / 16) + rows;
+    q.hmax = reinterpret_cast<unsigned*>(f.fused_counters + (E + 1) + (size_t)T * (H / 128));
+    q.next_item = f.fused_counters + (E + 1) + (size_t)T * (H / 128) + rows;
     q.status = &f.hdr->status;
     q.wait_limit = debug_wait_limit();
     q.extra_arrivals = debug_extra_arrivals();

@@ -56,19 +56,15 @@ __host__ __device__ inline size_t w4a16_chunk(int mt, int kb, int KB) { return (
 
 // 64-wide K blocks per streamed stage of the small-group (decode) GEMMs
 // (KB = K / 64 blocks per 128-row tile): the largest count <= kmax (at most
-// 8) that divides KB into an even number of equal stages, else the largest
-// that gives an even number of stages. The two halves of the MMA warps take
-// alternate stages, so with an even count every tile splits its K blocks
-// between the halves the same way wherever it falls in a CTA's sequence (and
-// every kernel that runs this loop with the same kmax sums in the same
-// order); with equal stages the two halves also get the same work.
+// 8) that divides KB into equal stages, else kmax itself (a short last
+// stage). Both halves of the MMA warps read every stage, half h taking the
+// stage's blocks h, h + 2, ...; every kernel that runs this loop with the
+// same kmax therefore sums in the same order.
 constexpr int kW16MaxStageKb = 8;
 __host__ __device__ inline int w16_stage_kb(int KB, int kmax) {
   for (int kb = kmax; kb > 1; --kb)
-    if (KB % kb == 0 && (KB / kb) % 2 == 0) return kb;
-  for (int kb = kmax; kb > 1; --kb)
-    if (((KB + kb - 1) / kb) % 2 == 0) return kb;
-  return 1;
+    if (KB % kb == 0) return kb;
+  return kmax < KB ? kmax : (KB > 0 ? KB : 1);
 }
 
 // ---------------------------------------------------------------------------

@@ -29,14 +29,15 @@
 //   64-wide K blocks, 36 KB, in a ring of as many as fit) with bulk copies
 //   from the gate/up phase straight into the down phase, so the down weights
 //   are already in flight when the gate/up items end.
-// * Sixteen MMA warps (8 row blocks x 2 halves that take alternate stages)
+// * Sixteen MMA warps (8 row blocks x 2 halves; in every stage half h takes
+//   the K blocks h, h + 2, ...)
 //   turn the e2m1 codes into f16 with the hardware conversion, multiply in
 //   the E4M3 block scales and run mma.sync m16n8k16 with the group's rows as
 //   N; at the end of an item the half that finishes second adds the other's
 //   partial sums and runs the epilogue, while the first goes on to the next
-//   item. Stage sizes give every item an even number of stages, so the
-//   arithmetic (and the result, bit for bit) is that of the multi-kernel
-//   path's decode GEMM (the same stage loop and join, decode_mma.cuh).
+//   item. The stage sizes and the split are those of the multi-kernel
+//   path's decode GEMM, so the arithmetic (and the result, bit for bit) is
+//   the same (the same stage loop and join, decode_mma.cuh).
 // * Gate/up epilogue: SwiGLU, h stored bf16 in the workspace with a running
 //   per-row max |h|. Down epilogue: y = h W2^T * alpha * routing weight,
 //   stored bf16 (the shared expert's rows fp32). Neither waits on a global
@@ -46,7 +47,7 @@
 //   gpu scope, cumulative over the MMA warps' stores); a helper warp stages
 //   a down item's h rows (as f16 with a row scale) once all gate/up tiles of
 //   the group are counted (acquire). For a down item the signal warp counts
-//   each (token, 16 output columns) contribution; the one that completes the
+//   each (token, 128 output columns) contribution; the one that completes the
 //   k + 1 of a token sums the token's rows in the fixed order j = 0..k-1,
 //   then the shared row, in fp32 and writes the bf16 output. The sum order
 //   never depends on which CTA does it: the result is deterministic.
@@ -69,7 +70,7 @@ using namespace tc;
 constexpr int kMaxT = kDecodeFusedMaxT;           // tokens (each group has at most this many rows)
 constexpr int kMaxK = 32;
 using decode::kBlockWarps;                         // one per 16-row block of a 128-row tile
-using decode::kHalves;                             // halves that take alternate stages
+using decode::kHalves;                             // halves: alternate K blocks of every stage
 constexpr int kMmaWarps = kBlockWarps * kHalves;
 constexpr int kProducerWarp = kMmaWarps;
 constexpr int kHelperWarp = kMmaWarps + 1;
@@ -80,7 +81,8 @@ constexpr int kMaxSlots = 16;                      // ring slots of stage_kb K b
 constexpr int kHSlots = 2;                         // staged h row sets (down items)
 constexpr int kMaxRows = kMaxT * kMaxK + kMaxT;    // routed pairs + shared rows
 constexpr int kMaxGroups = kMaxT * kMaxK + 1;      // active groups: at most one per pair, + shared
-constexpr int kQueue = 8;                          // the CTA's published items not yet taken over
+constexpr int kQueue = 8;
+constexpr int kDoneSlots = 4;                      // finished items the signal warp may lag behind                          // the CTA's published items not yet taken over
 constexpr long long kDrainLimit = 4ll * 1000 * 1000 * 1000;  // cycles for in-flight copies to land
 
 struct Args {
@@ -99,7 +101,7 @@ struct Args {
   uint16_t* y;          // [T*k, H] routed rows, bf16
   float* y_shared;      // [T, H] the shared expert's rows, fp32
   int* gu_done;         // [groups] (zeroed by the caller)
-  int* cmb_cnt;         // [T][H/16] (zeroed)
+  int* cmb_cnt;         // [T][H/128] (zeroed)
   int* next_item;       // grid-wide item counter (zeroed)
   unsigned* hmax;       // [rows] bf16 magnitude bits of max |h| (zeroed)
   int* status;
@@ -118,7 +120,7 @@ struct Smem {
   uint64_t hempty[kHSlots];
   uint64_t xfull;                // the x rows (bf16) have landed in shared memory
   uint64_t xfree;                // every MMA warp is done with the resident x rows
-  uint64_t done[2];              // an item's epilogue stores are issued (one warp per row block)
+  uint64_t done[kDoneSlots];     // an item's epilogue stores are issued (one warp per row block)
   int released;                  // items the signal warp has taken over (counts up; no parity aliasing)
   int q_item[kQueue];            // the CTA's c-th item at c % kQueue (-1: no more items)
   int q_count;                   // items published
@@ -189,11 +191,6 @@ __device__ __forceinline__ void release_add(int* ctr, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ int acq_rel_add(int* ctr, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(v) : "memory");
-  return old;
-}
 
 // out[t, col .. col+8) = sum_j y[inv[t, j]] (j = 0..k-1 in order) + y_shared[t]
 // in fp32, rounded once to bf16: the same sum, in the same order, as the
@@ -259,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&sm->full[i], 1);
-      mbar_init(&sm->empty[i], kBlockWarps);  // the half that reads the stage
+      mbar_init(&sm->empty[i], kMmaWarps);  // both halves read every stage
     }
     for (int i = 0; i < kHSlots; ++i) {
       mbar_init(&sm->hland[i], 1);
@@ -269,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     decode::half_join_init(&sm->join, 0, 1);
     mbar_init(&sm->xfree, kMmaWarps);
     mbar_init(&sm->xfull, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDoneSlots; ++i) {
       mbar_init(&sm->done[i], kBlockWarps);
     }
     sm->abort = 0;
@@ -514,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // ever waits on a global fence: gate/up items are counted in
     // gu_done[group] (release, gpu scope; cumulative over the MMA warps'
     // stores of h, which the done barrier ordered before it); down items
-    // count their (token, 16 columns) contributions, and the contribution
-    // that completes one sums the token's rows in the fixed order j = 0..k-1,
-    // then the shared row, and writes the bf16 output.
+    // count their (token, 128-column tile) contributions, and the
+    // contribution that completes one sums the token's rows in the fixed
+    // order j = 0..k-1, then the shared row, and writes the bf16 output.
     const int need = k + (p.has_shared ? 1 : 0);
     for (int cnt_items = 0;; ++cnt_items) {
       {
@@ -524,38 +521,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         if (item < 0) break;
         const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
         const int MT = ph == 0 ? MT1 : MT2;
-        const int ds = cnt_items & 1;
-        if (!mbar_wait(&sm->done[ds], (cnt_items >> 1) & 1, abort, limit)) break;
+        const int ds = cnt_items % kDoneSlots;
+        if (!mbar_wait(&sm->done[ds], (cnt_items / kDoneSlots) & 1, abort, limit)) break;
         const int a = (i / MT + rot) % A, mt = i % MT;
         if (ph == 0) {
           if (lane == 0) release_add(p.gu_done + a, 1);
         } else {
           const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
-          for (int base = 0; base < n * kBlockWarps; base += 32) {
-            const int idx = base + lane;           // (row, 16-column block) of this item
-            int last = 0, tok = 0, cb = 0;
-            if (idx < n * kBlockWarps) {
-              tok = sm->row_tok[r0 + idx / kBlockWarps];
-              cb = mt * kBlockWarps + idx % kBlockWarps;
-              last = acq_rel_add(p.cmb_cnt + (size_t)tok * (H / 16) + cb, 1) == need - 1;
-            }
-            unsigned todo = __ballot_sync(0xffffffffu, last);
+          // count the item's rows: one per (token, 128-column tile). The fence
+          // publishes the MMA warps' y stores (ordered before by the done
+          // barrier) ahead of the counts; the count that completes a token's
+          // tile (k routed rows + the shared row) is followed by a fence
+          // before the rows are read back.
+          __threadfence();
+          int last = 0, tok = 0;
+          if (lane < n) {
+            tok = sm->row_tok[r0 + lane];
+            last = atomicAdd(p.cmb_cnt + (size_t)tok * MT2 + mt, 1) == need - 1;
+          }
+          unsigned todo = __ballot_sync(0xffffffffu, last);
+          if (todo) {
             __threadfence();
-            while (todo) {  // up to 16 completed (token, 16 columns) at a time, two lanes (8 columns) each
-              const int nb = __popc(todo);
-              const int sub = lane >> 1;
-              unsigned m = todo;
-              for (int q = 0; q < sub && m; ++q) m &= m - 1;   // this lane pair's set bit: the sub-th
-              const int src = (sub < nb) ? __ffs(m) - 1 : 0;
-              const int t = __shfl_sync(0xffffffffu, tok, src);
-              const int c16 = __shfl_sync(0xffffffffu, cb, src);
-              if (sub < nb) combine_cols8(p, sm->inv, t, k, H, c16 * 16 + (lane & 1) * 8);
-              if (nb <= 16) {
-                todo = 0;
-              } else {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) todo &= todo - 1;
-              }
+            while (todo) {  // two finished (token, tile) at a time, 16 lanes of 8 columns each
+              const int s0 = __ffs(todo) - 1;
+              todo &= todo - 1;
+              const int s1 = todo ? __ffs(todo) - 1 : -1;
+              if (s1 >= 0) todo &= todo - 1;
+              const int src = lane < 16 ? s0 : s1;
+              const int t = __shfl_sync(0xffffffffu, tok, src < 0 ? 0 : src);
+              if (src >= 0) combine_cols8(p, sm->inv, t, k, H, mt * kTile + (lane & 15) * 8);
             }
           }
         }
@@ -610,19 +604,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         if (!mbar_wait(&sm->hfull[hslot], (m / kHSlots) & 1, abort, limit)) { ok = false; break; }
         xa0 = smem_u32(act + (size_t)hslot * kMaxT * hs_stride + (size_t)rsel * hs_stride + 8 * lq);
       }
+      // the epilogue's alpha, loaded now so that it arrives during the stage loop
+      const uint8_t* wb = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
+                                  : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wb);
+      const float al0 = __ldg(&hdr->alpha[0]), al1 = __ldg(&hdr->alpha[1]);
       float acc4[4][4];
 #pragma unroll
       for (int s = 0; s < 4; ++s) acc4[s][0] = acc4[s][1] = acc4[s][2] = acc4[s][3] = 0.f;
-      // the two halves take alternate stages (j counts every stage of this
-      // CTA); with an even number of stages per item each half sums the same
-      // K blocks of every item
+      // both halves read every stage: half h sums its K blocks h, h + 2, ...
+      // (j counts every stage of this CTA)
       for (int st = 0; st < NST; ++st, ++j) {
-        if ((j & 1) != half) continue;
         const int slot = j % S;
         if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, limit)) { ok = false; break; }
         const int kb0 = st * KBS;
-        decode::mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), 0, 1, blk, lane,
-                  xa0 + (uint32_t)(kb0 * 64) * 2, acc4);
+        decode::mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), half, kHalves, blk, lane,
+                          xa0 + (uint32_t)(kb0 * 64) * 2, acc4);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[slot]);
       }
@@ -646,9 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       if (!decode::half_join(&sm->join, blk, lane, cnt_items, acc, second, abort, limit)) { ok = false; break; }
       if (!second) continue;
 
-      const uint8_t* wb = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
-                                  : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
-      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wb);
       const int mb = mt * kBlockWarps + blk;
       if (ph == 0) {
         // SwiGLU: lane pair (row g8 gate, row g8 + 8 up) of feature 8 * mb + g8
@@ -659,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
           const int c = 2 * t4 + q;
           if (c < n) {
             const float rm = sm->xmul[sm->row_tok[r0 + c]];
-            const float hv = silu(acc[q] * rm * hdr->alpha[0]) * (acc[2 + q] * rm * hdr->alpha[1]);
+            const float hv = silu(acc[q] * rm * al0) * (acc[2 + q] * rm * al1);
             const uint16_t bits = float_to_bf16_bits(hv);
             p.h[(size_t)(r0 + c) * I + f] = bits;
             hb2[q] = bits & 0x7fffu;
@@ -685,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
             const int r = r0 + c;
             // the multi-kernel path's order of operations, so the two paths agree bit for bit
             const float rw = sm->row_w[r];
-            const float v0 = acc[q] * hm[q] * hdr->alpha[0] * rw, v1 = acc[2 + q] * hm[q] * hdr->alpha[0] * rw;
+            const float v0 = acc[q] * hm[q] * al0 * rw, v1 = acc[2 + q] * hm[q] * al0 * rw;
             if (e == E) {  // shared expert: kept fp32 for the combine
               p.y_shared[(size_t)(r - P) * H + col + g8] = v0;
               p.y_shared[(size_t)(r - P) * H + col + g8 + 8] = v1;
@@ -696,11 +690,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
           }
         }
       }
-      // hand the item to the signal warp (its slot must be free: taken over
-      // two items ago)
-      const int ds = cnt_items & 1;
+      // hand the item to the signal warp (its slot must be free: the item
+      // kDoneSlots before it taken over)
+      const int ds = cnt_items % kDoneSlots;
       int freed = 1;
-      if (lane == 0) freed = decode::spin_ge(&sm->released, cnt_items - 1, abort, limit);
+      if (lane == 0) freed = decode::spin_ge(&sm->released, cnt_items - kDoneSlots + 1, abort, limit);
       if (!__shfl_sync(0xffffffffu, freed, 0)) { ok = false; break; }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->done[ds]);
@@ -717,16 +711,12 @@ static size_t fused_smem_bytes(int T, int H, int I, int E, int slots, int stage_
 }
 
 // Ring slots for a stage size: as many as fit, at most 144 KB of ring (four
-// 36 KB stages, eight 18 KB ones), never fewer than 4, and always even. The
-// halves take alternate stages, so with an even ring a slot's previous stage
-// belongs to the same half, which consumed it before it waits on the slot
-// again; with an odd ring the previous stage is the other half's, and a half
-// running ahead could find that earlier phase still incomplete and take the
-// parity of the phase before it as its own.
+// 36 KB stages, eight 18 KB ones), never fewer than 4. Every MMA warp reads
+// every stage in order, so a slot's previous stage was consumed by each
+// waiter before it waits on the slot again.
 static int fused_slots(int T, int H, int I, int E, int stage_kb) {
   int slots = std::min(kMaxSlots, (int)((144 * 1024) / ((size_t)stage_kb * kW16Chunk)));
-  slots -= slots % kHalves;
-  while (slots > 4 && fused_smem_bytes(T, H, I, E, slots, stage_kb) > 227 * 1024) slots -= kHalves;
+  while (slots > 4 && fused_smem_bytes(T, H, I, E, slots, stage_kb) > 227 * 1024) --slots;
   return slots;
 }
 

@@ -14,7 +14,7 @@ namespace moe {
 namespace decode {
 
 constexpr int kBlockWarps = 8;   // one per 16-row block of a 128-row weight tile
-constexpr int kHalves = 2;       // two halves of the MMA warps take alternate stages
+constexpr int kHalves = 2;       // two halves of the MMA warps: alternate K blocks of every stage
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -23,7 +23,8 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
 }
 
 // One stage of one 128-row tile: this warp's 16-row block over the stage's
-// K blocks kb_first, kb_first + kb_step, ... < nkb, with four accumulator
+// K blocks kb_first, kb_first + kb_step, ... < nkb (half h of the MMA warps
+// takes h, h + 2, ...), with four accumulator
 // chains (one per k16 step of a block). The stage holds the tile's prepared
 // chunks (4608 bytes per 64-wide K block: eight 512-byte blocks of codes in
 // m16n8k16 A-fragment order, then eight 64-byte blocks of E4M3 scales); xa0

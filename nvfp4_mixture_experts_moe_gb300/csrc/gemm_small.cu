@@ -11,13 +11,15 @@
 // active weights). Each weight byte is read from HBM once. One producer warp
 // streams the weight tiles with bulk copies (cp.async.bulk, one copy per
 // stage of up to 8 K blocks (36 KB), completion on mbarriers) into a ring of
-// shared-memory stages. Sixteen MMA warps: warp b of part h owns
-// the 16-row block b of a 128-row item for the stages j with j % 2 == h (more
-// warps per scheduler hide the conversion -> multiply -> MMA latency chains);
-// at the end of an item the part that finishes second adds the other's
-// partial sums and runs the epilogue, while the first goes on. A
-// warp loads its 16-byte A fragment per 64-wide K block from shared memory,
-// turns the e2m1 codes into f16 with the hardware e2m1x2 conversion, multiplies in the E4M3 block scales (e2m1 * e4m3 is exact in
+// shared-memory stages. Sixteen MMA warps: warp b of part h owns the 16-row
+// block b of a 128-row item and, in every stage, the K blocks h, h + 2, ...
+// (more warps per scheduler hide the conversion -> multiply -> MMA latency
+// chains, and with both parts on every stage a slot is freed for the next
+// copy as soon as the stage is done); at the end of an item the part that
+// finishes second adds the other's partial sums and runs the epilogue, while
+// the first goes on. A warp loads its 16-byte A fragment per 64-wide K block
+// from shared memory, turns the e2m1 codes into f16 with the hardware e2m1x2
+// conversion, multiplies in the E4M3 block scales (e2m1 * e4m3 is exact in
 // f16) and feeds mma.sync m16n8k16 with the group's rows (up to 8) as N.
 //
 // Activations enter as f16: each row is scaled by a power of two 2^s so that
@@ -45,11 +47,10 @@ namespace {
 using namespace tc;
 
 using decode::kBlockWarps;   // one per 16-row block of a 128-row item
-// K split: part h takes the ring stages j with j % kHalves == h (j counts the
-// stages of all items in order). The ring has a multiple of kHalves slots, so
-// the previous stage of a slot (j - S) belongs to the same part, which
-// consumed it before it waits for stage j: the slot's barrier is then never
-// a phase behind (an mbarrier parity wait cannot tell phase n from n - 2).
+// K split: part h takes the K blocks h, h + 2, ... of every ring stage. Every
+// MMA warp consumes every stage in order, so it has consumed a slot's previous
+// stage (j - S) before it waits for stage j: the slot's barrier is never a
+// phase behind (an mbarrier parity wait cannot tell phase n from n - 2).
 using decode::kHalves;
 constexpr int kMmaWarps = kBlockWarps * kHalves;
 constexpr int kThreads = (kMmaWarps + 1) * 32;  // + one producer warp
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     pref[0] = 0;
     for (int i = 0; i < S; ++i) {
       mbar_init(&sm->full[i], 1);
-      mbar_init(&sm->empty[i], kBlockWarps);  // the eight warps of the half that read the stage
+      mbar_init(&sm->empty[i], kMmaWarps);  // both parts read every stage
     }
     mbar_init(&sm->xsync, kMmaWarps);
     decode::half_join_init(&sm->join, 0, 1);
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
 
   // ------------------------------------------------------------- MMA warps
   if (p.early_weights) pdl_wait();  // the activation rows come from the predecessor
+  const int row_last0 = p.group_offsets[G - 1];   // first row of the last group
   const int blk = warp % kBlockWarps, half = warp / kBlockWarps;
   const int g8 = lane >> 2, t4 = lane & 3;
   int cur_g = -1, cur_c = -1;
@@ -269,6 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       if (!mma_warps_sync(&sm->xsync, xphase, abort, p.wait_limit)) break;
     }
 
+    // the epilogue's alpha and routing weights, loaded now so that they
+    // arrive during the stage loop
+    const uint8_t* wb = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
+                                                                 : p.weights + (size_t)g * p.stride;
+    const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wb);
+    const float al0 = __ldg(&hdr->alpha[0]), al1 = __ldg(&hdr->alpha[1]);
+    float rs2[2] = {1.0f, 1.0f};
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (!GATE_UP && p.row_scale != nullptr && 2 * t4 + q < nrows) rs2[q] = __ldg(p.row_scale + row0 + 2 * t4 + q);
     // one accumulator per k16 step of a block: four independent MMA chains
     float acc4[4][4];
 #pragma unroll
@@ -276,12 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     const uint32_t xbase = smem_u32(xs) + (uint32_t)(lrow * xs_stride + 8 * lq) * 2;
     bool ok = true;
     for (int st = 0; st < nstage; ++st, ++j) {
-      if ((j % kHalves) != half) continue;  // another part's stage
       const int slot = j % S;
       if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, p.wait_limit)) { ok = false; break; }
       const int kb0 = st * kBlocksPerStage;
-      decode::mma_stage(stages + (size_t)slot * kStageBytes, min(kBlocksPerStage, kblocks - kb0), 0, 1, blk, lane,
-                        xbase + (uint32_t)(kb0 * 64) * 2, acc4);
+      decode::mma_stage(stages + (size_t)slot * kStageBytes, min(kBlocksPerStage, kblocks - kb0), half, kHalves,
+                        blk, lane, xbase + (uint32_t)(kb0 * 64) * 2, acc4);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->empty[slot]);
     }
@@ -296,9 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     if (!second) continue;
 
     // Epilogue: c0,c1 = row g (tokens 2t, 2t+1); c2,c3 = row g+8.
-    const uint8_t* wb = (g == G - 1 && p.last_weights != nullptr) ? p.last_weights
-                                                                 : p.weights + (size_t)g * p.stride;
-    const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(wb);
     const int mb = mt * 8 + blk;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -311,15 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
       }
       const float rm = sm->row_mul[n];
       if (GATE_UP) {
-        const float gv = acc[q] * rm * hdr->alpha[0];
-        const float uv = acc[2 + q] * rm * hdr->alpha[1];
+        const float gv = acc[q] * rm * al0;
+        const float uv = acc[2 + q] * rm * al1;
         p.out[(size_t)orow * (N / 2) + 8 * mb + g8] = float_to_bf16_bits(silu(gv) * uv);
       } else {
-        const float rs = p.row_scale ? p.row_scale[orow] : 1.0f;
+        const float rs = rs2[q];
         const int hr = 16 * mb + g8;
-        const float v0 = acc[q] * rm * hdr->alpha[0] * rs, v1 = acc[2 + q] * rm * hdr->alpha[0] * rs;
+        const float v0 = acc[q] * rm * al0 * rs, v1 = acc[2 + q] * rm * al0 * rs;
         if (p.out_last_f32 != nullptr && g == G - 1) {  // shared expert: kept fp32 for the combine
-          float* o = p.out_last_f32 + (size_t)(orow - p.group_offsets[G - 1]) * N;
+          float* o = p.out_last_f32 + (size_t)(orow - row_last0) * N;
           o[hr] = v0;
           o[hr + 8] = v1;
         } else {
@@ -365,10 +373,9 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& pl, int rows_limit, cudaStrea
   const int skb = w16_stage_kb(pl.K / 64, decode_stage_kb());
   a.stage_kb = skb;
   int S = std::min(kMaxSlots, (int)((216 * 1024) / ((size_t)skb * kW16Chunk)));
-  S -= S % kHalves;
-  while (S > kHalves && small_smem_bytes(pl.K, pl.num_groups, S, skb) > limit) S -= kHalves;
+  while (S > 2 && small_smem_bytes(pl.K, pl.num_groups, S, skb) > limit) --S;
   const size_t smem = small_smem_bytes(pl.K, pl.num_groups, S, skb);
-  if (smem > limit) return MOE_ERR_UNSUPPORTED;  // K too large for the staged rows and kHalves slots
+  if (smem > limit) return MOE_ERR_UNSUPPORTED;  // K too large for the staged rows and two slots
   a.stages = S;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);

@@ -182,7 +182,7 @@ struct DecodeFusedPlan {
   uint16_t* y;               // [T*k, H] routed rows, bf16
   float* y_shared;           // [T, H] the shared expert's rows, fp32
   int* gu_done;              // [E + 1], zero at launch
-  int* cmb_cnt;              // [T * H/16], zero at launch
+  int* cmb_cnt;              // [T * H/128], zero at launch
   unsigned* hmax;            // [T*k + T], zero at launch
   int* next_item;            // one int, zero at launch (the grid's item counter)
   int* status;
