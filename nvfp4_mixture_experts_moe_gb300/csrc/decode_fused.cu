@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   } else if (warp >= kBlockWarps && warp < kBlockWarps + T) {
     // x row t -> f16 in place with its row scale, resident for the gate/up items
     const int t = warp - kBlockWarps;
-    if (mbar_wait(&sm->xfull, 0, abort, limit)) {
+    // (the warp decides as one: the conversion below uses warp shuffles)
+    if (__all_sync(0xffffffffu, mbar_wait(&sm->xfull, 0, abort, limit))) {
       uint4* row = reinterpret_cast<uint4*>(act + (size_t)t * xs_stride);
       uint32_t m = 0;
       for (int i = lane; i < H / 8; i += 32) {
@@ -451,12 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // The CTA takes its items in increasing order, so every item from its
     // first down item on is a down item.
     int m = 0, issued = 0;
-    const bool xok = mbar_wait(&sm->xfree, 0, abort, limit);
+    const bool xok = __all_sync(0xffffffffu, mbar_wait(&sm->xfree, 0, abort, limit));
     for (int c = xok ? sm->first_down : 0; xok; ++c, ++m) {
       const int item = queue_get(sm, c, abort, limit, lane);
       if (item < 0) break;   // no more items (-1) or a timeout (-2)
       const int slot = m % kHSlots;
-      if (!mbar_wait(&sm->hempty[slot], ((m / kHSlots) & 1) ^ 1, abort, limit)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm->hempty[slot], ((m / kHSlots) & 1) ^ 1, abort, limit))) break;
       const int a = ((item - N1) / MT2 + rot) % A;
       if (!wait_counter(p.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
       const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       }
       ++issued;
       const unsigned mx = lane < n ? __ldcg(p.hmax + r0 + lane) : 0u;
-      if (!mbar_wait(&sm->hland[slot], (m / kHSlots) & 1, abort, limit)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm->hland[slot], (m / kHSlots) & 1, abort, limit))) break;
       for (int q = 0; q < n; ++q) {
         const int sh = row_shift(__shfl_sync(0xffffffffu, mx, q));
         const float up = __int_as_float((127 + sh) << 23);
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
         const int MT = ph == 0 ? MT1 : MT2;
         const int ds = cnt_items % kDoneSlots;
-        if (!mbar_wait(&sm->done[ds], (cnt_items / kDoneSlots) & 1, abort, limit)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm->done[ds], (cnt_items / kDoneSlots) & 1, abort, limit))) break;
         const int a = (i / MT + rot) % A, mt = i % MT;
         if (ph == 0) {
           if (lane == 0) release_add(p.gu_done + a, 1);
@@ -601,7 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       if (ph == 0) {
         xa0 = smem_u32(act + (size_t)sm->row_tok[r0 + rsel] * xs_stride + 8 * lq);
       } else {
-        if (!mbar_wait(&sm->hfull[hslot], (m / kHSlots) & 1, abort, limit)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm->hfull[hslot], (m / kHSlots) & 1, abort, limit))) {
+          ok = false;
+          break;
+        }
         xa0 = smem_u32(act + (size_t)hslot * kMaxT * hs_stride + (size_t)rsel * hs_stride + 8 * lq);
       }
       // the epilogue's alpha, loaded now so that it arrives during the stage loop
@@ -616,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       // (j counts every stage of this CTA)
       for (int st = 0; st < NST; ++st, ++j) {
         const int slot = j % S;
-        if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, limit)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm->full[slot], (j / S) & 1, abort, limit))) { ok = false; break; }
         const int kb0 = st * KBS;
         decode::mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), half, kHalves, blk, lane,
                           xa0 + (uint32_t)(kb0 * 64) * 2, acc4);

@@ -110,7 +110,7 @@ __device__ __forceinline__ bool mma_warps_sync(uint64_t* bar, uint32_t& phase, v
                                                long long limit) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase, abort, limit);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase, abort, limit));   // the warp decides as one
   phase ^= 1u;
   __syncwarp();
   return ok;
@@ -289,7 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_small_kernel(SmallArgs p) {
     bool ok = true;
     for (int st = 0; st < nstage; ++st, ++j) {
       const int slot = j % S;
-      if (!mbar_wait(&sm->full[slot], (j / S) & 1, abort, p.wait_limit)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm->full[slot], (j / S) & 1, abort, p.wait_limit))) {
+        ok = false;
+        break;
+      }
       const int kb0 = st * kBlocksPerStage;
       decode::mma_stage(stages + (size_t)slot * kStageBytes, min(kBlocksPerStage, kblocks - kb0), half, kHalves,
                         blk, lane, xbase + (uint32_t)(kb0 * 64) * 2, acc4);
