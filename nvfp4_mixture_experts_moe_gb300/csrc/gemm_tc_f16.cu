@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int rho = q * 32 + lane;
+    const int row_last0 = p.out_last_f32 != nullptr ? p.group_offsets[G - 1] : 0;   // first shared row
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
       const Item it = decode_item(item, pref, G, MT, p.group_offsets);
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
           }
         } else if (p.out_last_f32 != nullptr && it.g == G - 1) {
           // shared expert: kept fp32 for the combine
-          float* o32 = p.out_last_f32 + (size_t)(it.row0 - p.group_offsets[G - 1]) * N + it.mt * kM + rho;
+          float* o32 = p.out_last_f32 + (size_t)(it.row0 - row_last0) * N + it.mt * kM + rho;
 #pragma unroll
           for (int c4 = 0; c4 < 32; c4 += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + c4);  // broadcast read

@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
     const int q = warp & 3;
     const int rho = q * 32 + lane;
     const float inv_gs_b = MX ? 1.0f : 1.0f / *p.b_gs;
+    const int row_last0 = p.out_last_f32 != nullptr ? p.group_offsets[G - 1] : 0;   // first shared row
     float amax = 0.0f;
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
             const float rs1 = __shfl_sync(0xffffffffu, rs_chunk, c + 1);
             const float v0 = __uint_as_float(r[c]) * a0 * rs0, v1 = __uint_as_float(r[c + 1]) * a0 * rs1;
             if (last_f32) {
-              float* o32 = p.out_last_f32 + (size_t)(it.row0 - p.group_offsets[G - 1] + n) * N + it.mt * kM + rho;
+              float* o32 = p.out_last_f32 + (size_t)(it.row0 - row_last0 + n) * N + it.mt * kM + rho;
               if (n < it.rows) o32[0] = v0;
               if (n + 1 < it.rows) o32[N] = v1;
             } else {
