@@ -122,7 +122,7 @@ struct Smem {
   uint64_t xfree;                // every MMA warp is done with the resident x rows
   uint64_t done[kDoneSlots];     // an item's epilogue stores are issued (one warp per row block)
   int released;                  // items the signal warp has taken over (counts up; no parity aliasing)
-  int q_item[kQueue];            // the CTA's c-th item at c % kQueue (-1: no more items)
+  int q_item[kQueue];            // the CTA's c-th item (its descriptor) at c % kQueue (-1: no more items)
   int q_count;                   // items published
   int first_down;                // index c of the CTA's first down item (or of the end)
   int abort;
@@ -149,6 +149,14 @@ __device__ __forceinline__ int row_shift(uint32_t m) {
   int sh = (m == 0) ? 0 : 141 - max(e, 1);
   return max(-113, min(sh, 126));
 }
+
+// A queue entry describes an item by its phase (bit 30: down), its group a
+// (bits 12..29) and its 128-row weight tile mt (bits 0..11), so that no warp
+// divides to decode it; -1 is the end of the CTA's items.
+__device__ __forceinline__ int item_desc(int ph, int a, int mt) { return (ph << 30) | (a << 12) | mt; }
+__device__ __forceinline__ int desc_ph(int d) { return (d >> 30) & 1; }
+__device__ __forceinline__ int desc_a(int d) { return (d >> 12) & 0x3ffff; }
+__device__ __forceinline__ int desc_mt(int d) { return d & 0xfff; }
 
 // The CTA's c-th item from its queue (lane 0 waits, bounded; broadcast):
 // >= 0 an item, -1 no more items, -2 the wait gave up.
@@ -283,6 +291,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     mbar_arrive_expect_tx(&sm->xfull, (uint32_t)(T * H * 2));
     for (int t = 0; t < T; ++t)
       bulk_g2s(smem_u32(act + (size_t)t * xs_stride), p.x + (size_t)t * H, (uint32_t)(H * 2), &sm->xfull);
+    // The shared expert's gate/up tiles are the first items; while the CTAs
+    // route (HBM otherwise idle), each brings its slice of them into L2.
+    if (p.has_shared) {
+      const size_t tot = (size_t)MT1 * KB1 * kW16Chunk;   // the prepared tiles after the header
+      const size_t per = ((tot + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+      const size_t off = per * blockIdx.x;
+      if (off < tot) {
+        const uint32_t n = (uint32_t)min(per, tot - off);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.w13_shared + sizeof(PrepHeader) + off),
+                     "r"(n)
+                     : "memory");
+      }
+    }
   }
   if (warp < T) {
     // registers per lane sized to E (E <= 32, 128, 320, 1024)
@@ -395,20 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // other warps, then streams its stages; the next item is taken while
     // the last stage of the current one streams.
     if (lane == 0) {
-      int j = 0, item = first_item, c = 0;
+      int j = 0, slot = 0, par = 0, item = first_item, c = 0;
       for (;; ++c) {
         // a queue entry is reused once the signal warp has taken over the
         // item kQueue places before it (every warp is past that item)
         if (!decode::spin_ge(&sm->released, c - kQueue + 1, abort, limit)) break;
-        const int pub = item < N1 + N2 ? item : -1;
-        *reinterpret_cast<volatile int*>(&sm->q_item[c % kQueue]) = pub;
-        __threadfence_block();
-        *reinterpret_cast<volatile int*>(&sm->q_count) = c + 1;
-        if (pub < 0) break;
         const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
         const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
         const int KBS = ph == 0 ? KBS1 : KBS2;
         const int a = (i / MT + rot) % A, mt = i % MT;
+        const int pub = item < N1 + N2 ? item_desc(ph, a, mt) : -1;
+        *reinterpret_cast<volatile int*>(&sm->q_item[c % kQueue]) = pub;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&sm->q_count) = c + 1;
+        if (pub < 0) break;
         const int e = sm->grp_e[a];
         const uint8_t* blk = ph == 0 ? (e == E ? p.w13_shared : p.w13 + (size_t)e * p.s13)
                                      : (e == E ? p.w2_shared : p.w2 + (size_t)e * p.s2);
@@ -416,14 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         bool ok = true;
         int next = N1 + N2;
         for (int st = 0; st < NST; ++st, ++j) {
-          const int slot = j % S;
-          if (!mbar_wait(&sm->empty[slot], ((j / S) & 1) ^ 1, abort, limit)) { ok = false; break; }
+          if (!mbar_wait(&sm->empty[slot], par ^ 1, abort, limit)) { ok = false; break; }
           const int kb0 = st * KBS;
           const uint32_t bytes = (uint32_t)(min(KBS, KB - kb0) * kW16Chunk);
           mbar_arrive_expect_tx(&sm->full[slot], bytes);
           bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, KB), bytes,
                    &sm->full[slot]);
           if (st == NST - 1) next = atomicAdd(p.next_item, 1);
+          if (++slot == S) {
+            slot = 0;
+            par ^= 1;
+          }
         }
         if (!ok) break;
         item = next;
@@ -458,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       if (item < 0) break;   // no more items (-1) or a timeout (-2)
       const int slot = m % kHSlots;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm->hempty[slot], ((m / kHSlots) & 1) ^ 1, abort, limit))) break;
-      const int a = ((item - N1) / MT2 + rot) % A;
+      const int a = desc_a(item);
       if (!wait_counter(p.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
       const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
       uint16_t* dst = act + (size_t)slot * kMaxT * hs_stride;
@@ -520,11 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       {
         const int item = queue_get(sm, cnt_items, abort, limit, lane);
         if (item < 0) break;
-        const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
-        const int MT = ph == 0 ? MT1 : MT2;
+        const int ph = desc_ph(item);
         const int ds = cnt_items % kDoneSlots;
         if (!__all_sync(0xffffffffu, mbar_wait(&sm->done[ds], (cnt_items / kDoneSlots) & 1, abort, limit))) break;
-        const int a = (i / MT + rot) % A, mt = i % MT;
+        const int a = desc_a(item), mt = desc_mt(item);
         if (ph == 0) {
           if (lane == 0) release_add(p.gu_done + a, 1);
         } else {
@@ -569,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   const int blk = warp % kBlockWarps, half = warp / kBlockWarps;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int lrow = lane & 7, lq = lane >> 3;
-  int j = 0, m = 0;
+  int slot = 0, par = 0, m = 0;   // ring slot and phase parity of the next stage
   bool ok = true;
   bool x_released = false;
   // x (and the slot of the first down item's h rows, which reuses its shared
@@ -587,12 +610,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     {
       const int item = queue_get(sm, cnt_items, abort, limit, lane);
       if (item == -2) { ok = false; break; }
-      if (item < 0 || item >= N1) release_x(cnt_items);
+      if (item < 0 || desc_ph(item) == 1) release_x(cnt_items);
       if (item < 0) break;
-      const int ph = item < N1 ? 0 : 1, i = ph ? item - N1 : item;
-      const int MT = ph == 0 ? MT1 : MT2, KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
+      const int ph = desc_ph(item);
+      const int KB = ph == 0 ? KB1 : KB2, NST = ph == 0 ? NST1 : NST2;
       const int KBS = ph == 0 ? KBS1 : KBS2;
-      const int a = (i / MT + rot) % A, mt = i % MT;
+      const int a = desc_a(item), mt = desc_mt(item);
       const int e = sm->grp_e[a], r0 = sm->grp_r0[a], n = sm->grp_n[a];
       const int hslot = m % kHSlots;
       // ldmatrix row of this lane: the group's row lrow (rows past the group
@@ -618,20 +641,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       for (int s = 0; s < 4; ++s) acc4[s][0] = acc4[s][1] = acc4[s][2] = acc4[s][3] = 0.f;
       // both halves read every stage: half h sums its K blocks h, h + 2, ...
       // (j counts every stage of this CTA)
-      for (int st = 0; st < NST; ++st, ++j) {
-        const int slot = j % S;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm->full[slot], (j / S) & 1, abort, limit))) { ok = false; break; }
+      for (int st = 0; st < NST; ++st) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm->full[slot], par, abort, limit))) { ok = false; break; }
         const int kb0 = st * KBS;
         decode::mma_stage(ring + (size_t)slot * kStageBytes, min(KBS, KB - kb0), half, kHalves, blk, lane,
                           xa0 + (uint32_t)(kb0 * 64) * 2, acc4);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[slot]);
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1;
+        }
       }
       if (!ok) break;
       float hm[2] = {1.0f, 1.0f};   // row multipliers of this lane's two token columns
       if (ph == 0) {
         const int nx = queue_peek(sm, cnt_items + 1, lane);   // -3: not published yet
-        if (nx == -1 || nx >= N1) release_x(cnt_items + 1);
+        if (nx == -1 || (nx >= 0 && desc_ph(nx) == 1)) release_x(cnt_items + 1);
       } else {  // the staged h rows (and their multipliers) are no longer read
 #pragma unroll
         for (int q = 0; q < 2; ++q) hm[q] = sm->hmul[hslot][min(2 * t4 + q, kMaxT - 1)];
