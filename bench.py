@@ -415,26 +415,36 @@ def measure(cfg, layer, args, dev, dist, world, rank, headline):
         raise RuntimeError(f"{cfg.name}: device status set during the timed steps")
     value = job_tokens_per_s(cfg.T, world, ms)
 
-    # end to end: pinned host inputs copied in, result read back, every step
-    hx = [b[0].cpu().pin_memory() for b in batches]
-    hl = [b[1].cpu().pin_memory() for b in batches]
+    # end to end: pinned host inputs copied in (x and the logits packed in one
+    # pinned buffer, one copy), result read back, every step
+    xb = batches[0][0].numel() * batches[0][0].element_size()
+    lb = batches[0][1].numel() * batches[0][1].element_size()
+    loff = (xb + 255) // 256 * 256
+    hbuf = []
+    for bx, bl in batches:
+        hb = torch.empty(loff + lb, dtype=torch.uint8).pin_memory()
+        hb[:xb].view(bx.dtype).view(bx.shape).copy_(bx.cpu())
+        hb[loff:].view(bl.dtype).view(bl.shape).copy_(bl.cpu())
+        hbuf.append(hb)
     hout = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty_like(batches[0][0])
-    dl = torch.empty_like(batches[0][1])
+    dbuf = torch.empty(loff + lb, dtype=torch.uint8, device=dev)
+    dx = dbuf[:xb].view(batches[0][0].dtype).view(batches[0][0].shape)
+    dl = dbuf[loff:].view(batches[0][1].dtype).view(batches[0][1].shape)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(args.warmup + K):
         flush.zero_()
         if i >= args.warmup:
             e2e_ev[i - args.warmup][0].record(stream)
-        dx.copy_(hx[i % nb], non_blocking=True)
-        dl.copy_(hl[i % nb], non_blocking=True)
+        dbuf.copy_(hbuf[i % nb], non_blocking=True)
         B.moe_nvfp4_forward(desc, dx, dl, out, None, ws, stream)
         hout.copy_(out, non_blocking=True)
         if i >= args.warmup:
             e2e_ev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
+    if not torch.equal(hout.to(dev), out):
+        raise RuntimeError(f"{cfg.name}: end-to-end output differs from the device output")
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dist, dev)
-    h2d = dx.numel() * dx.element_size() + dl.numel() * dl.element_size()
+    h2d = loff + lb
     d2h = hout.numel() * hout.element_size()
 
     pk = peaks()
@@ -488,6 +498,8 @@ def measure(cfg, layer, args, dev, dist, world, rank, headline):
     if headline:
         res["graph_replay"] = graph_replay(desc, batches, out, ws, flush, stream, args, dist, dev, world, cfg)
         res["router_gemm"] = router_gemm(cfg, layer, batches, out, flush, stream, args, dev, pk)
+    if cfg.T > 64 and cfg.mode in ("w4a16", "w4a4") and layer.shared:
+        res["public_grouped_gemm"] = public_grouped_gemm(cfg, layer, batches, flush, stream, args, dev, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_tok = {"tiny": 16, "w4a4": 1}.get(cfg.name, args.cpu_sample_tokens)
         res["cpu_baseline"] = cpu_baseline(cfg, batches[0][0].cpu(), batches[0][1].cpu(), n_tok)
@@ -577,6 +589,71 @@ def router_gemm(cfg, layer, batches, out, flush, stream, args, dev, pk):
     return dict(ms=r_ms, bytes=r_bytes, flops=r_flops, **r_roof, forward_with_router_ms=fr_ms,
                 note="logits = x W_router^T (bf16 [E, H] router, seeded N(0, 1/H)); timed alone and inside "
                      "moe_nvfp4_forward (x only), L2 flushed between launches")
+
+
+def public_grouped_gemm(cfg, layer, batches, flush, stream, args, dev, pk):
+    """The public grouped GEMM entry point (moe_nvfp4_grouped_gemm) on this
+    workload's gate/up GEMM: the same routed and shared rows, the activations
+    row-major with a row index (W4A4: quantised by moe_nvfp4_quantize), timed
+    alone with L2 flushed between launches. The forward runs its own GEMM
+    kernels on activations it has put in group order."""
+    import torch
+
+    from nvfp4_mixture_experts_moe_gb300 import binding as B
+    K, k, T, E = args.steps, cfg.k, cfg.T, cfg.E
+    x, logits = batches[0]
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    B.moe_route_topk(logits, T, E, k, ids, w, stream)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pws = torch.zeros(B.moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    B.moe_permute(ids, T, k, E, counts, offsets, perm, inv, pws, stream)
+    torch.cuda.synchronize()
+    # groups: the E routed experts, then the shared expert's T rows
+    offs = torch.cat([offsets, torch.tensor([T * k + T], dtype=torch.int32, device=dev)])
+    row_tok = torch.cat([(perm.long() // k).to(torch.int32), torch.arange(T, dtype=torch.int32, device=dev)])
+    rows = T * k + T
+    h = torch.empty(rows, cfg.I, dtype=torch.bfloat16, device=dev)
+    w4a4 = cfg.mode == "w4a4"
+    args_g = B.MoeGemmArgs(mode=1 if w4a4 else 0, gate_up=1, num_groups=E + 1, N=2 * cfg.I, K=cfg.H)
+    args_g.weights = layer.w13.data_ptr()
+    args_g.last_weights = layer.w13_s.data_ptr()
+    args_g.group_offsets = offs.data_ptr()
+    args_g.a_row_index = row_tok.data_ptr()
+    args_g.out = h.data_ptr()
+    if w4a4:
+        from nvfp4_mixture_experts_moe_gb300 import quantize_bf16
+        q, sf, gs = quantize_bf16(x)
+        keep = (q, sf, gs)
+        args_g.a, args_g.a_sf, args_g.a_gs = q.data_ptr(), sf.data_ptr(), gs.data_ptr()
+    else:
+        keep = (x,)
+        args_g.a = x.data_ptr()
+    gws = torch.zeros(B.moe_gemm_workspace_size(E + 1), dtype=torch.uint8, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(args.warmup + K):
+        flush.zero_()
+        if i >= args.warmup:
+            ev[i - args.warmup][0].record(stream)
+        B.moe_nvfp4_grouped_gemm(args_g, gws, stream)
+        if i >= args.warmup:
+            ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    del keep
+    if B.moe_get_device_status(gws) != 0:
+        raise RuntimeError("device status set in the public grouped GEMM")
+    g_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flops = rows * 2 * (2 * cfg.I) * cfg.H
+    peak = pk["bf16"] * (6.0 if w4a4 else 1.0)
+    achieved = flops / (g_ms / 1e3) / 1e12
+    return {"ms": g_ms, "flops": flops, "achieved": achieved, "unit": "TFLOP/s", "peak": peak,
+            "frac": achieved / peak,
+            "kernel": "gemm_tc_w4a4_kernel (gather)" if w4a4 else "gemm_tc_w4a16_kernel / gemm_small_kernel",
+            "note": "moe_nvfp4_grouped_gemm, gate/up + SwiGLU, the workload's routed and shared rows, "
+                    "activations row-major with a row index; L2 flushed between launches"}
 
 
 def run_ours(args):
