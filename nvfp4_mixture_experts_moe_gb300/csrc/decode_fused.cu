@@ -158,6 +158,11 @@ __device__ __forceinline__ int desc_ph(int d) { return (d >> 30) & 1; }
 __device__ __forceinline__ int desc_a(int d) { return (d >> 12) & 0x3ffff; }
 __device__ __forceinline__ int desc_mt(int d) { return d & 0xfff; }
 
+// Barrier over the first n threads of the CTA (named barrier id, not 0).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // The CTA's c-th item from its queue (lane 0 waits, bounded; broadcast):
 // >= 0 an item, -1 no more items, -2 the wait gave up.
 __device__ __forceinline__ int queue_get(Smem* sm, int c, volatile int* abort, long long limit, int lane) {
@@ -348,7 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       if (lane == 0) sm->xmul[t] = __int_as_float((127 - sh) << 23);
     }
   }
-  __syncthreads();
+  // The permutation needs only the routing: warps 0..7 (which route, and hold
+  // the P <= 256 pairs) sort among themselves on a named barrier while warps
+  // 8.. still convert x.
+  if (warp < kBlockWarps) named_sync(1, kBlockWarps * 32);
   if (tid < P) {
     // rank of pair q in the order (expert, pair index): its grouped row, so
     // the rows of an expert keep the pairs' order (a stable sort, the same
@@ -364,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     sm->row_w[r] = sm->w[q];
     sm->row_e[r] = e;
   }
-  __syncthreads();
+  if (warp < kBlockWarps) named_sync(1, kBlockWarps * 32);
   if (warp == 0) {
     // active groups in expert order: a group starts where the expert changes
     int na = 0;
