@@ -428,13 +428,21 @@ unsigned long long moe_kernel_launches(void);
  *   It sets how the two halves of the MMA warps split K, so results can
  *   differ in the last bits from one setting to another (never between the
  *   two decode paths at one setting). Used to tune the stage size.
+ * MOE_DEBUG_FP4_TILE (default 0 = the library's choice): the tile shape of
+ *   the W4A4 / MXFP4 GEMMs as two decimal digits, tens for the gate/up GEMM
+ *   and units for the down GEMM: 1 = one CTA per SM (two accumulators, six
+ *   stages) with the weight rows on the MMA's M side; 2 = two CTAs per SM
+ *   (one accumulator and three stages each), weight rows on M; 3 = two CTAs
+ *   per SM with the group's rows on M; 0 keeps the library's choice for that
+ *   GEMM. Results agree to the last bit across shapes. Used to compare them.
  * Errors: an unknown key, or a value out of range -> MOE_ERR_INVALID_ARG.
  */
 typedef enum {
   MOE_DEBUG_WAIT_LIMIT = 1,
   MOE_DEBUG_EXTRA_ARRIVALS = 2,
   MOE_DEBUG_DISABLE_DECODE_FUSED = 3,
-  MOE_DEBUG_DECODE_STAGE_KB = 4
+  MOE_DEBUG_DECODE_STAGE_KB = 4,
+  MOE_DEBUG_FP4_TILE = 5
 } moe_debug_key;
 moe_status moe_debug_set(int key, long long value);
 

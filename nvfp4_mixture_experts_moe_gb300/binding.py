@@ -21,6 +21,7 @@ MOE_ERR_WORKSPACE, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
 MOE_W4A16, MOE_W4A4, MOE_MXFP4 = 0, 1, 2
 MOE_SCALE_QUANT, MOE_SCALE_DEQUANT = 0, 1
 MOE_DEBUG_WAIT_LIMIT, MOE_DEBUG_EXTRA_ARRIVALS, MOE_DEBUG_DISABLE_DECODE_FUSED, MOE_DEBUG_DECODE_STAGE_KB = 1, 2, 3, 4
+MOE_DEBUG_FP4_TILE = 5
 
 _lib = None
 

@@ -21,12 +21,17 @@ static std::atomic<int> g_extra_arrivals{0};
 static std::atomic<int> g_fused_disabled{0};
 constexpr int kDefaultDecodeStageKb = 8;
 static std::atomic<int> g_decode_stage_kb{kDefaultDecodeStageKb};
+static std::atomic<int> g_fp4_tile{0};
 
 
 long long debug_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 int debug_extra_arrivals() { return g_extra_arrivals.load(std::memory_order_relaxed); }
 bool debug_decode_fused_disabled() { return g_fused_disabled.load(std::memory_order_relaxed) != 0; }
 int decode_stage_kb() { return g_decode_stage_kb.load(std::memory_order_relaxed); }
+int debug_fp4_tile(bool gate_up) {
+  const int v = g_fp4_tile.load(std::memory_order_relaxed);
+  return gate_up ? v / 10 : v % 10;
+}
 static std::atomic<unsigned long long> g_launches{0};
 static thread_local cudaEvent_t g_stage_events[MOE_STAGE_COUNT];
 static thread_local bool g_stage_events_set = false;
@@ -689,6 +694,10 @@ moe_status moe_debug_set(int key, long long value) {
     case MOE_DEBUG_DECODE_STAGE_KB:
       if (value < 0 || value > kW16MaxStageKb) return MOE_ERR_INVALID_ARG;
       g_decode_stage_kb.store(value > 0 ? (int)value : kDefaultDecodeStageKb, std::memory_order_relaxed);
+      return MOE_OK;
+    case MOE_DEBUG_FP4_TILE:
+      if (value < 0 || value > 33 || value % 10 > 3) return MOE_ERR_INVALID_ARG;
+      g_fp4_tile.store((int)value, std::memory_order_relaxed);
       return MOE_OK;
 
   }

@@ -122,6 +122,13 @@ __device__ __forceinline__ uint2 ldg_stream2(const void* p) {
 // infinity) mapped to 0. NaN activations are outside the contract; this keeps
 // them from becoming a tensor's or a row's maximum (an infinite amax would
 // make a global scale 0 and zero every code).
+// One 32-byte global store (p 32-byte aligned): one L2 sector per thread.
+__device__ __forceinline__ void stg_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t finite_mag(uint32_t mag_bits) { return mag_bits > 0x7f80u ? 0u : mag_bits; }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

@@ -143,7 +143,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // MX: MXFP4 operands (E8M0 scales per 32, kind::mxf4, two scale atoms per
 // operand and stage, no global scales); otherwise NVFP4 (E4M3 per 16,
 // kind::mxf4nvf4, four atoms per operand and stage).
-template <bool GATE_UP, int CTAS, bool MX>
+// TOK_M: the group's rows on the MMA's M side (always 128: rows past the
+// group only reach accumulator lanes that are never stored) and 128 weight
+// rows on N, so each epilogue thread owns one row of the output tile and
+// stores it in 16-byte pieces; otherwise (swap-AB) the weight rows on M and
+// the group's rows on N (rounded up to 16), each thread owning one output
+// column. The same stage images and scale atoms serve both.
+template <bool GATE_UP, int CTAS, bool MX, bool TOK_M>
 __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __grid_constant__ BoxMaps maps, Args p) {
   constexpr int kSfBytes = MX ? kSfStage / 2 : kSfStage;   // scale bytes per operand and stage
   constexpr int kAtoms = kSfBytes / 512;
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
       int j = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
         const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
-        const int q = 32 - __clz((it.bn >> 4) - 1);   // box of 16 << q >= bn rows
+        const int q = TOK_M ? 3 : 32 - __clz((it.bn >> 4) - 1);   // box of 16 << q >= bn rows
         const uint32_t bytes = (uint32_t)((16 << q) * kRowBytes + kSfBytes);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
@@ -296,80 +302,133 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
   } else if (warp < kEpiWarp0 + 4) {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;
-    const int rho = q * 32 + lane;
+    const int rho = q * 32 + lane;   // this thread's TMEM lane
     const float inv_gs_b = MX ? 1.0f : 1.0f / *p.b_gs;
     const int row_last0 = p.out_last_f32 != nullptr ? p.group_offsets[G - 1] : 0;   // first shared row
     float amax = 0.0f;
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
       const Item it = decode_item(item, pref, tb, G, MT, p.group_offsets);
-      float rsv[kMaxBN / 32];
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
+      const float a0 = hdr->alpha[0] * inv_gs_b, a1 = hdr->alpha[1] * inv_gs_b;
+      const bool last_f32 = !GATE_UP && p.out_last_f32 != nullptr && it.g == G - 1;  // shared expert: fp32
+      // down: y = acc * (alpha * routing weight), one factor per row of the group
+      float fac[TOK_M ? 1 : kMaxBN / 32];
 #pragma unroll
-      for (int i = 0; i < kMaxBN / 32; ++i) {
-        const int n = 32 * i + lane;
-        rsv[i] = (!GATE_UP && p.row_scale && n < it.rows) ? __ldg(p.row_scale + it.row0 + n) : 1.0f;
+      for (int i = 0; i < (TOK_M ? 1 : kMaxBN / 32); ++i) {
+        const int n = TOK_M ? rho : 32 * i + lane;
+        fac[i] = (!GATE_UP && p.row_scale && n < it.rows) ? a0 * __ldg(p.row_scale + it.row0 + n) : a0;
       }
       const int acc = itc % kAcc;
       if (!mbar_wait(&sm->tfull[acc], (itc / kAcc) & 1, abort, p.wait_limit)) break;
       tc_fence_after();
-      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
-      const float a0 = hdr->alpha[0] * inv_gs_b, a1 = hdr->alpha[1] * inv_gs_b;
-      const bool gate_lane = (rho & 8) == 0;  // rows 16j..16j+7 gate, 16j+8..16j+15 up (interleave by 8)
-      const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
-      for (int c0 = 0; c0 < it.bn; c0 += 32) {  // columns past bn are read (within the buffer) and not stored
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * 128 + c0, r);
-        tmem_ld_wait();
-        if (GATE_UP) {
-          // the gate lane finishes columns c0..c0+15, its up partner (lane ^ 8) c0+16..c0+31
-          const int cb = gate_lane ? 0 : 16;
-          float other[16];
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * 128;
+      if (TOK_M) {
+        // lane rho = row rho of the tile; TMEM column c = weight row c of tile mt
+        const bool valid = rho < it.rows;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kM; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tacc + c0, r);
+          tmem_ld_wait();
+          if (!valid) continue;
+          if (GATE_UP) {
+            // columns c0..c0+31: gate of features F0..F0+7, their up, gate of
+            // F0+8..F0+15, their up (weight rows interleaved by 8)
+            const int F0 = 64 * it.mt + (c0 >> 1);
+            uint32_t hb[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            other[c] = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? r[16 + c] : r[c]), 8);
+            for (int i = 0; i < 16; i += 2) {
+              float h2[2];
 #pragma unroll
-          for (int c = 0; c < 16; c += 2) {  // two tokens per bf16 conversion
-            float h2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float own = __uint_as_float(gate_lane ? r[c + e] : r[16 + c + e]);
-              const float g = gate_lane ? own : other[c + e];
-              const float u = gate_lane ? other[c + e] : own;
-              h2[e] = silu(g * a0) * (u * a1);
+              for (int e = 0; e < 2; ++e) {
+                const int j = i + e, gc = j < 8 ? j : j + 8;
+                h2[e] = silu(__uint_as_float(r[gc]) * a0) * (__uint_as_float(r[gc + 8]) * a1);
+              }
+              hb[i >> 1] = float2_to_bf16x2_bits(h2[0], h2[1]);
+              amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb[i >> 1] << 16)),
+                                       fabsf(__uint_as_float(hb[i >> 1] & 0xffff0000u))));
             }
-            const uint32_t hb = float2_to_bf16x2_bits(h2[0], h2[1]);
-            const int n = c0 + cb + c;
-            uint16_t* o = p.out + (size_t)(it.row0 + n) * (N / 2) + f;
-            if (n < it.rows) {
-              o[0] = (uint16_t)(hb & 0xffffu);
-              amax = fmaxf(amax, fabsf(__uint_as_float(hb << 16)));
+            stg_v8(p.out + (size_t)(it.row0 + rho) * (N / 2) + F0, hb);
+          } else if (last_f32) {   // the shared expert's rows stay fp32
+            float* o = p.out_last_f32 + (size_t)(it.row0 - row_last0 + rho) * N + it.mt * kM + c0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(r[8 * v + e]) * fac[0]);
+              stg_v8(o + 8 * v, w);
             }
-            if (n + 1 < it.rows) {
-              o[N / 2] = (uint16_t)(hb >> 16);
-              amax = fmaxf(amax, fabsf(__uint_as_float(hb & 0xffff0000u)));
+          } else {
+            uint16_t* o = p.out + (size_t)(it.row0 + rho) * N + it.mt * kM + c0;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint32_t yb[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                yb[e] = float2_to_bf16x2_bits(__uint_as_float(r[16 * v + 2 * e]) * fac[0],
+                                              __uint_as_float(r[16 * v + 2 * e + 1]) * fac[0]);
+              stg_v8(o + 16 * v, yb);
             }
           }
-        } else {
-          float rs_chunk = 1.0f;
+        }
+      } else {
+        // lane rho = weight row rho of tile mt; TMEM column n = row n of the tile
+        const bool gate_lane = (rho & 8) == 0;  // rows 16j..16j+7 gate, 16j+8..16j+15 up (interleave by 8)
+        const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
+        for (int c0 = 0; c0 < it.bn; c0 += 32) {  // columns past bn are read (within the buffer) and not stored
+          uint32_t r[32];
+          tmem_ld32(tacc + c0, r);
+          tmem_ld_wait();
+          if (GATE_UP) {
+            // the gate lane finishes columns c0..c0+15, its up partner (lane ^ 8) c0+16..c0+31
+            const int cb = gate_lane ? 0 : 16;
+            float other[16];
 #pragma unroll
-          for (int i = 0; i < kMaxBN / 32; ++i)
-            if ((c0 >> 5) == i) rs_chunk = rsv[i];
-          const bool last_f32 = p.out_last_f32 != nullptr && it.g == G - 1;  // shared expert: fp32
+            for (int c = 0; c < 16; ++c)
+              other[c] = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? r[16 + c] : r[c]), 8);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {  // two tokens per bf16 conversion
-            const int n = c0 + c;
-            const float rs0 = __shfl_sync(0xffffffffu, rs_chunk, c);
-            const float rs1 = __shfl_sync(0xffffffffu, rs_chunk, c + 1);
-            const float v0 = __uint_as_float(r[c]) * a0 * rs0, v1 = __uint_as_float(r[c + 1]) * a0 * rs1;
-            if (last_f32) {
-              float* o32 = p.out_last_f32 + (size_t)(it.row0 - row_last0 + n) * N + it.mt * kM + rho;
-              if (n < it.rows) o32[0] = v0;
-              if (n + 1 < it.rows) o32[N] = v1;
-            } else {
-              const uint32_t yb = float2_to_bf16x2_bits(v0, v1);
-              uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
-              if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
-              if (n + 1 < it.rows) o[N] = (uint16_t)(yb >> 16);
+            for (int c = 0; c < 16; c += 2) {  // two tokens per bf16 conversion
+              float h2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float own = __uint_as_float(gate_lane ? r[c + e] : r[16 + c + e]);
+                const float g = gate_lane ? own : other[c + e];
+                const float u = gate_lane ? other[c + e] : own;
+                h2[e] = silu(g * a0) * (u * a1);
+              }
+              const uint32_t hb = float2_to_bf16x2_bits(h2[0], h2[1]);
+              const int n = c0 + cb + c;
+              uint16_t* o = p.out + (size_t)(it.row0 + n) * (N / 2) + f;
+              if (n < it.rows) {
+                o[0] = (uint16_t)(hb & 0xffffu);
+                amax = fmaxf(amax, fabsf(__uint_as_float(hb << 16)));
+              }
+              if (n + 1 < it.rows) {
+                o[N / 2] = (uint16_t)(hb >> 16);
+                amax = fmaxf(amax, fabsf(__uint_as_float(hb & 0xffff0000u)));
+              }
+            }
+          } else {
+            float fac_chunk = fac[0];
+#pragma unroll
+            for (int i = 1; i < (TOK_M ? 1 : kMaxBN / 32); ++i)
+              if ((c0 >> 5) == i) fac_chunk = fac[i];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {  // two tokens per bf16 conversion
+              const int n = c0 + c;
+              const float v0 = __uint_as_float(r[c]) * __shfl_sync(0xffffffffu, fac_chunk, c);
+              const float v1 = __uint_as_float(r[c + 1]) * __shfl_sync(0xffffffffu, fac_chunk, c + 1);
+              if (last_f32) {
+                float* o32 = p.out_last_f32 + (size_t)(it.row0 - row_last0 + n) * N + it.mt * kM + rho;
+                if (n < it.rows) o32[0] = v0;
+                if (n + 1 < it.rows) o32[N] = v1;
+              } else {
+                const uint32_t yb = float2_to_bf16x2_bits(v0, v1);
+                uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
+                if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
+                if (n + 1 < it.rows) o[N] = (uint16_t)(yb >> 16);
+              }
             }
           }
         }
@@ -392,25 +451,29 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
         if (!mbar_wait(&sm->tempty[acc], ((itc / kAcc) & 1) ^ 1, abort, p.wait_limit)) break;
         const uint32_t d = tmem + acc * 128;
         tc_fence_after();
-        const uint32_t idesc = idesc_nvf4(kM, it.bn);
-        const uint32_t idesc_mx0 = idesc_mxf4(kM, it.bn, 0), idesc_mx2 = idesc_mxf4(kM, it.bn, 2);
+        const int mma_n = TOK_M ? kM : it.bn;
+        const uint32_t idesc = idesc_nvf4(kM, mma_n);
+        const uint32_t idesc_mx0 = idesc_mxf4(kM, mma_n, 0), idesc_mx2 = idesc_mxf4(kM, mma_n, 2);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
           if (!mbar_wait(&sm->sf_full[slot], (j / kStages) & 1, abort, p.wait_limit)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t as = smem_u32(base + slot * kStageBytes);
-          const uint32_t bs = as + kTile;
+          // stage: weight tile | activation tile; TMEM: weight atoms at +0, activation atoms at +16
+          const uint32_t ws_ = smem_u32(base + slot * kStageBytes);
+          const uint32_t as = TOK_M ? ws_ + kTile : ws_;
+          const uint32_t bs = TOK_M ? ws_ : ws_ + kTile;
           const uint32_t sf_col = tmem + kSfCol0 + slot * 32;
+          const uint32_t sfa_col = sf_col + (TOK_M ? 16 : 0), sfb_col = sf_col + (TOK_M ? 0 : 16);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
             if (MX)  // atom kk / 2, byte pair 2 * (kk % 2)
-              mma_mxf4(d, ad, bd, (kk & 1) ? idesc_mx2 : idesc_mx0, sf_col + (kk >> 1) * 4,
-                       sf_col + 16 + (kk >> 1) * 4, (ks | kk) != 0);
+              mma_mxf4(d, ad, bd, (kk & 1) ? idesc_mx2 : idesc_mx0, sfa_col + (kk >> 1) * 4,
+                       sfb_col + (kk >> 1) * 4, (ks | kk) != 0);
             else
-              mma_nvf4(d, ad, bd, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4, (ks | kk) != 0);
+              mma_nvf4(d, ad, bd, idesc, sfa_col + kk * 4, sfb_col + kk * 4, (ks | kk) != 0);
           }
           tc_commit(&sm->empty[slot]);
         }
@@ -485,16 +548,28 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   a.out_amax = pl.out_amax;
   a.status = pl.status;
   a.wait_limit = debug_wait_limit();
-  const int ctas = pl.ctas_per_sm == 1 ? 1 : 2;
+  // tile shape: 1 = one CTA per SM, weight rows on M; 2 = two CTAs per SM,
+  // weight rows on M; 3 = two CTAs per SM, the group's rows on M
+  const int forced = debug_fp4_tile(pl.gate_up != 0);
+  const int shape = forced != 0 ? forced : pl.ctas_per_sm == 1 ? 1 : 3;
+  const int ctas = shape == 1 ? 1 : 2;
   const size_t smem = fp4_smem_bytes(pl.num_groups, ctas == 2 ? Shape<2>::kStages : Shape<1>::kStages);
   if (smem > (ctas == 2 ? 113 : 227) * 1024) return MOE_ERR_UNSUPPORTED;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  auto k = mx ? (ctas == 2 ? (pl.gate_up ? gemm_tc_fp4_kernel<true, 2, true> : gemm_tc_fp4_kernel<false, 2, true>)
-                           : (pl.gate_up ? gemm_tc_fp4_kernel<true, 1, true> : gemm_tc_fp4_kernel<false, 1, true>))
-              : (ctas == 2 ? (pl.gate_up ? gemm_tc_fp4_kernel<true, 2, false> : gemm_tc_fp4_kernel<false, 2, false>)
-                           : (pl.gate_up ? gemm_tc_fp4_kernel<true, 1, false> : gemm_tc_fp4_kernel<false, 1, false>));
+  using KernelFn = void (*)(const BoxMaps, Args);
+  // [mx][gate_up][shape - 1]
+  static const KernelFn table[2][2][3] = {
+      {{gemm_tc_fp4_kernel<false, 1, false, false>, gemm_tc_fp4_kernel<false, 2, false, false>,
+        gemm_tc_fp4_kernel<false, 2, false, true>},
+       {gemm_tc_fp4_kernel<true, 1, false, false>, gemm_tc_fp4_kernel<true, 2, false, false>,
+        gemm_tc_fp4_kernel<true, 2, false, true>}},
+      {{gemm_tc_fp4_kernel<false, 1, true, false>, gemm_tc_fp4_kernel<false, 2, true, false>,
+        gemm_tc_fp4_kernel<false, 2, true, true>},
+       {gemm_tc_fp4_kernel<true, 1, true, false>, gemm_tc_fp4_kernel<true, 2, true, false>,
+        gemm_tc_fp4_kernel<true, 2, true, true>}}};
+  const KernelFn k = table[mx ? 1 : 0][pl.gate_up ? 1 : 0][shape - 1];
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * ctas), dim3(kThreads), smem, s, maps, a);
   if (e != cudaSuccess) return cuda_ok(e);

@@ -113,7 +113,8 @@ struct GemmPlan {
   bool pdl;                 // programmatic dependent launch (inside the fused forward)
   bool early_weights;       // group offsets are final before the predecessor ends: weights may
                             // stream before the dependency wait (only with pdl)
-  int ctas_per_sm;          // W4A4 tile GEMM shape: 2 (default) or 1 (two accumulators)
+  int ctas_per_sm;          // W4A4 tile GEMM: 1 = one CTA per SM (two accumulators); otherwise
+                            // two CTAs per SM with the group's rows on the MMA's M side
 };
 
 // Small-group path: mma.sync m16n8k16 over register-dequantised weights; one
@@ -196,6 +197,7 @@ moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s);
 long long debug_wait_limit();     // cycles per bounded device wait (default 4e9, about 2 s)
 int debug_extra_arrivals();       // 0 normally
 bool debug_decode_fused_disabled();
+int debug_fp4_tile(bool gate_up);   // W4A4/MXFP4 tile shape: 0 (library's choice), 1, 2 or 3
 int decode_stage_kb();             // max 64-wide K blocks per ring stage of the decode GEMMs (1..8)
 
 }  // namespace moe

@@ -64,6 +64,34 @@ def test_w4a4_skewed_groups_full_check():
     check_outputs(out, ref, what="w4a4 skewed groups")
 
 
+MX_GROUPS = si.LayerConfig("mx_groups", T=300, H=512, I=256, I_s=256, E=24, k=4, mode="mxfp4", logits="zipf")
+
+
+@pytest.mark.parametrize("cfg", [GROUPS, MX_GROUPS], ids=["nvfp4", "mxfp4"])
+def test_fp4_tile_shapes_agree(cfg):
+    """Every tile shape of the block-scaled FP4 GEMMs (one or two CTAs per SM;
+    weight rows or the group's rows on the MMA's M side) gives the library
+    default's bits, on skewed routing with empty groups, groups of several
+    128-row tiles and ragged last tiles (the default is checked against the
+    oracle above)."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd
+    cfg, layer = device_layer(cfg)
+    x = si.make_x(cfg).cuda()
+    lg = si.make_logits(cfg).cuda()
+    ws = layer.workspace()
+    outs = {}
+    try:
+        for shape in (0, 11, 12, 13, 21, 22, 23, 31, 32, 33):
+            Bd.moe_debug_set(Bd.MOE_DEBUG_FP4_TILE, shape)
+            outs[shape] = layer.forward(x, lg, ws=ws).clone()
+            torch.cuda.synchronize()
+            assert Bd.moe_get_device_status(ws) == 0, shape
+    finally:
+        Bd.moe_debug_set(Bd.MOE_DEBUG_FP4_TILE, 0)
+    differ = [shape for shape, o in outs.items() if not torch.equal(o, outs[0])]
+    assert not differ, f"tile shapes {differ} differ from the default"
+
+
 def test_w4a4_small_deterministic():
     cfg, layer = device_layer(SMALL)
     x = si.make_x(cfg).cuda()
