@@ -140,13 +140,70 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Drains one 128 x 128 accumulator whose lanes are the rows of the item's
+// tile (lane rho = row rho) and whose columns are the rows of weight tile
+// mt: SwiGLU to bf16 h (gate/up) or y = acc * fac to bf16 (down; the shared
+// expert's rows to fp32), 32 columns at a time, 32-byte stores.
+template <bool GATE_UP>
+__device__ __forceinline__ void drain_rows(const Args& p, uint32_t tacc, const Item& it, int mt, int rho, int N,
+                                           float a0, float a1, float fac, bool last_f32, int row_last0,
+                                           float& amax) {
+  const bool valid = rho < it.rows;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kM; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(tacc + c0, r);
+    tmem_ld_wait();
+    if (!valid) continue;
+    if (GATE_UP) {
+      // columns c0..c0+31: gate of features F0..F0+7, their up, gate of
+      // F0+8..F0+15, their up (weight rows interleaved by 8)
+      const int F0 = 64 * mt + (c0 >> 1);
+      uint32_t hb[8];
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        float h2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = i + e, gc = j < 8 ? j : j + 8;
+          h2[e] = silu(__uint_as_float(r[gc]) * a0) * (__uint_as_float(r[gc + 8]) * a1);
+        }
+        hb[i >> 1] = float2_to_bf16x2_bits(h2[0], h2[1]);
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb[i >> 1] << 16)),
+                                 fabsf(__uint_as_float(hb[i >> 1] & 0xffff0000u))));
+      }
+      stg_v8(p.out + (size_t)(it.row0 + rho) * (N / 2) + F0, hb);
+    } else if (last_f32) {   // the shared expert's rows stay fp32
+      float* o = p.out_last_f32 + (size_t)(it.row0 - row_last0 + rho) * N + mt * kM + c0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(r[8 * v + e]) * fac);
+        stg_v8(o + 8 * v, w);
+      }
+    } else {
+      uint16_t* o = p.out + (size_t)(it.row0 + rho) * N + mt * kM + c0;
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        uint32_t yb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          yb[e] = float2_to_bf16x2_bits(__uint_as_float(r[16 * v + 2 * e]) * fac,
+                                        __uint_as_float(r[16 * v + 2 * e + 1]) * fac);
+        stg_v8(o + 16 * v, yb);
+      }
+    }
+  }
+}
+
 // MX: MXFP4 operands (E8M0 scales per 32, kind::mxf4, two scale atoms per
 // operand and stage, no global scales); otherwise NVFP4 (E4M3 per 16,
 // kind::mxf4nvf4, four atoms per operand and stage).
 // TOK_M: the group's rows on the MMA's M side (always 128: rows past the
 // group only reach accumulator lanes that are never stored) and 128 weight
 // rows on N, so each epilogue thread owns one row of the output tile and
-// stores it in 16-byte pieces; otherwise (swap-AB) the weight rows on M and
+// stores it in 32-byte pieces; otherwise (swap-AB) the weight rows on M and
 // the group's rows on N (rounded up to 16), each thread owning one output
 // column. The same stage images and scale atoms serve both.
 template <bool GATE_UP, int CTAS, bool MX, bool TOK_M>
@@ -324,54 +381,7 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + acc * 128;
       if (TOK_M) {
-        // lane rho = row rho of the tile; TMEM column c = weight row c of tile mt
-        const bool valid = rho < it.rows;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kM; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tacc + c0, r);
-          tmem_ld_wait();
-          if (!valid) continue;
-          if (GATE_UP) {
-            // columns c0..c0+31: gate of features F0..F0+7, their up, gate of
-            // F0+8..F0+15, their up (weight rows interleaved by 8)
-            const int F0 = 64 * it.mt + (c0 >> 1);
-            uint32_t hb[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              float h2[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int j = i + e, gc = j < 8 ? j : j + 8;
-                h2[e] = silu(__uint_as_float(r[gc]) * a0) * (__uint_as_float(r[gc + 8]) * a1);
-              }
-              hb[i >> 1] = float2_to_bf16x2_bits(h2[0], h2[1]);
-              amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb[i >> 1] << 16)),
-                                       fabsf(__uint_as_float(hb[i >> 1] & 0xffff0000u))));
-            }
-            stg_v8(p.out + (size_t)(it.row0 + rho) * (N / 2) + F0, hb);
-          } else if (last_f32) {   // the shared expert's rows stay fp32
-            float* o = p.out_last_f32 + (size_t)(it.row0 - row_last0 + rho) * N + it.mt * kM + c0;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(r[8 * v + e]) * fac[0]);
-              stg_v8(o + 8 * v, w);
-            }
-          } else {
-            uint16_t* o = p.out + (size_t)(it.row0 + rho) * N + it.mt * kM + c0;
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              uint32_t yb[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                yb[e] = float2_to_bf16x2_bits(__uint_as_float(r[16 * v + 2 * e]) * fac[0],
-                                              __uint_as_float(r[16 * v + 2 * e + 1]) * fac[0]);
-              stg_v8(o + 16 * v, yb);
-            }
-          }
-        }
+        drain_rows<GATE_UP>(p, tacc, it, it.mt, rho, N, a0, a1, fac[0], last_f32, row_last0, amax);
       } else {
         // lane rho = weight row rho of tile mt; TMEM column n = row n of the tile
         const bool gate_lane = (rho & 8) == 0;  // rows 16j..16j+7 gate, 16j+8..16j+15 up (interleave by 8)
@@ -492,6 +502,269 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
   if (tid == 0 && sm->abort) set_status(p.status, MOE_ERR_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// Wide tile: one CTA per SM, the group's rows on M (128) and 256 weight rows
+// on N as two halves of 128 (weight tiles 2m and 2m+1), each half with its
+// own accumulator (TMEM columns 0-127, 128-255), MMA-issuing thread and
+// scale-copy thread. The activation tile and its scale atoms come into shared
+// memory once per stage for both halves: 54 KB per 16.8 MFLOP instead of
+// 36 KB per 8.4 MFLOP, a quarter fewer bytes per FLOP through the SM's
+// L2 -> shared-memory path, which is what bounds the 128 x 128 tiles.
+namespace wide {
+constexpr int kWStages = 4;
+constexpr int kSfSlot = kSfStage;                         // one operand's atoms per stage (NVFP4 size)
+constexpr int kWStageBytes = 3 * kTile + 3 * kSfSlot;      // A | B0 | B1 | SFA | SFB0 | SFB1
+constexpr uint32_t kWSfCol0 = 256;                         // after the two accumulators
+constexpr int kSfCols = 48;                               // per stage: SFA, SFB0, SFB1 (16 columns each)
+constexpr int kWTmemCols = 512;
+static_assert(kWSfCol0 + kSfCols * kWStages <= kWTmemCols, "TMEM columns");
+static_assert(kWStageBytes % 1024 == 0, "stage alignment");
+constexpr int kEpiWarps = 8;    // warps 0..7: TMEM lane quarter w % 4, half w / 4
+constexpr int kMmaWarp0 = 8;    // 8, 9: MMA issuer of half 0, 1
+constexpr int kSfWarp0 = 10;    // 10, 11: scale copies of half 0, 1
+constexpr int kWALoadWarp = 12;  // the group's rows
+constexpr int kWBLoadWarp = 13;  // the two weight tiles
+constexpr int kWThreads = 14 * 32;
+
+struct WSmem {
+  uint64_t aready[kWStages];   // the activation tile and its atoms landed
+  uint64_t bready[kWStages];   // both weight tiles and their atoms landed
+  uint64_t sf_full[kWStages];  // both halves' scale copies completed
+  uint64_t empty[kWStages];    // both halves' MMAs completed
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;             // both MMA issuers' last commits
+  uint64_t drain_sf;          // both scale-copy threads' last commits
+  uint32_t tmem_base;
+  int abort;
+};
+}  // namespace wide
+
+template <bool GATE_UP, bool MX>
+__global__ void __launch_bounds__(wide::kWThreads, 1)
+    gemm_tc_fp4_wide_kernel(const __grid_constant__ BoxMaps maps, Args p) {
+  using namespace wide;
+  constexpr int kSfBytes = MX ? kSfStage / 2 : kSfStage;   // scale bytes per operand tile and stage
+  constexpr int kAtoms = kSfBytes / 512;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  WSmem* sm = reinterpret_cast<WSmem*>(base + kWStages * kWStageBytes);
+  int* pref = reinterpret_cast<int*>(sm + 1);   // [G + 1]
+  int* tb = pref + (p.G + 1);                   // [G + 1]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.G, K = p.K, N = p.N;
+  const int MT2 = N / (2 * kM);   // items per 128-row tile of a group: pairs of weight tiles
+  const int KS = K / kBK;
+  pdl_wait();
+
+  for (int g = tid; g < G; g += kWThreads) {
+    const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
+    const int nt = rows > 0 ? (rows + kMaxBN - 1) / kMaxBN : 0;
+    pref[g + 1] = nt * MT2;
+    tb[g + 1] = nt;
+  }
+  if (tid == 0) {
+    pref[0] = 0;
+    tb[0] = 0;
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(&sm->aready[i], 1);
+      mbar_init(&sm->bready[i], 1);
+      mbar_init(&sm->sf_full[i], 2);
+      mbar_init(&sm->empty[i], 2);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm->tfull[i], 1);
+      mbar_init(&sm->tempty[i], 128);
+    }
+    mbar_init(&sm->drain, 2);
+    mbar_init(&sm->drain_sf, 2);
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp < 2) {  // inclusive scans of pref (warp 0) and tb (warp 1)
+    int* arr = warp == 0 ? pref : tb;
+    int carry = 0;
+    for (int b0 = 1; b0 <= G; b0 += 32) {
+      const int i = b0 + lane;
+      int v = i <= G ? arr[i] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (i <= G) arr[i] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  if (warp == kMmaWarp0) tmem_alloc(&sm->tmem_base, kWTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  const int total = pref[G];
+  volatile int* abort = &sm->abort;
+
+  if (warp == kWALoadWarp) {
+    // ------------------------------------------------ activation (row) loader
+    if (lane == 0) {
+      tma_prefetch_map(&maps.m[3]);
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        const Item it = decode_item(item, pref, tb, G, MT2, p.group_offsets);
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kWStages;
+          if (!mbar_wait(&sm->empty[slot], ((j / kWStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
+          uint8_t* st = base + slot * kWStageBytes;
+          mbar_arrive_expect_tx(&sm->aready[slot], kTile + kSfBytes);
+          tma_load_2d(smem_u32(st), &maps.m[3], ks * kRowBytes, it.row0, &sm->aready[slot]);
+          bulk_g2s(smem_u32(st + 3 * kTile), p.b_sf_tiles + ((size_t)it.tile * KS + ks) * kSfBytes, kSfBytes,
+                   &sm->aready[slot]);
+        }
+        if (!ok) break;
+      }
+      for (int i = max(0, j - kWStages); i < j; ++i) drain_wait(&sm->aready[i % kWStages], (i / kWStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kWBLoadWarp) {
+    // ------------------------------------------------------- weight loader
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        const Item it = decode_item(item, pref, tb, G, MT2, p.group_offsets);
+        const uint8_t* wdata = weight_block(p, it.g) + sizeof(PrepHeader);
+        const uint8_t* wsf = wdata + (size_t)N * K / 2;
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kWStages;
+          if (!mbar_wait(&sm->empty[slot], ((j / kWStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
+          uint8_t* st = base + slot * kWStageBytes;
+          mbar_arrive_expect_tx(&sm->bready[slot], 2 * (kTile + kSfBytes));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const size_t tile = (size_t)(2 * it.mt + h) * KS + ks;
+            bulk_g2s(smem_u32(st + (1 + h) * kTile), wdata + tile * kTile, kTile, &sm->bready[slot]);
+            bulk_g2s(smem_u32(st + 3 * kTile + (1 + h) * kSfSlot), wsf + tile * kSfBytes, kSfBytes,
+                     &sm->bready[slot]);
+          }
+        }
+        if (!ok) break;
+      }
+      for (int i = max(0, j - kWStages); i < j; ++i) drain_wait(&sm->bready[i % kWStages], (i / kWStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kSfWarp0 || warp == kSfWarp0 + 1) {
+    // ------------------------- scale factors -> TMEM: half h's weight atoms
+    // and every other activation atom (the two threads split the shared ones)
+    const int h = warp - kSfWarp0;
+    if (lane == 0) {
+      int j = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kWStages;
+          // the slot's previous MMAs (both halves) completed before its loads
+          // were issued, so its TMEM columns are free once the data landed
+          if (!mbar_wait(&sm->aready[slot], (j / kWStages) & 1, abort, p.wait_limit) ||
+              !mbar_wait(&sm->bready[slot], (j / kWStages) & 1, abort, p.wait_limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = smem_u32(base + slot * kWStageBytes) + 3 * kTile;
+          const uint32_t sfb = sfa + (1 + h) * kSfSlot;
+          const uint32_t col = tmem + kWSfCol0 + slot * kSfCols;
+#pragma unroll
+          for (int kk = h; kk < kAtoms; kk += 2)
+            tc_cp_32x128b_warpx4(col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
+#pragma unroll
+          for (int kk = 0; kk < kAtoms; ++kk)
+            tc_cp_32x128b_warpx4(col + 16 + 16 * h + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
+          tc_commit(&sm->sf_full[slot]);
+        }
+        if (!ok) break;
+      }
+      tc_commit(&sm->drain_sf);
+      drain_wait(&sm->drain_sf, 0);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+    // ------------------------------------------------- MMA issuer of half h
+    const int h = warp - kMmaWarp0;
+    if (lane == 0) {
+      int j = 0, itc = 0;
+      for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
+        if (!mbar_wait(&sm->tempty[h], (itc & 1) ^ 1, abort, p.wait_limit)) break;
+        const uint32_t d = tmem + 128 * h;
+        tc_fence_after();
+        const uint32_t idesc = idesc_nvf4(kM, kM);
+        const uint32_t idesc_mx0 = idesc_mxf4(kM, kM, 0), idesc_mx2 = idesc_mxf4(kM, kM, 2);
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++j) {
+          const int slot = j % kWStages;
+          if (!mbar_wait(&sm->sf_full[slot], (j / kWStages) & 1, abort, p.wait_limit)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t as = smem_u32(base + slot * kWStageBytes);
+          const uint32_t bs = as + (1 + h) * kTile;
+          const uint32_t sfa_col = tmem + kWSfCol0 + slot * kSfCols;
+          const uint32_t sfb_col = sfa_col + 16 + 16 * h;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
+            if (MX)  // atom kk / 2, byte pair 2 * (kk % 2)
+              mma_mxf4(d, ad, bd, (kk & 1) ? idesc_mx2 : idesc_mx0, sfa_col + (kk >> 1) * 4,
+                       sfb_col + (kk >> 1) * 4, (ks | kk) != 0);
+            else
+              mma_nvf4(d, ad, bd, idesc, sfa_col + kk * 4, sfb_col + kk * 4, (ks | kk) != 0);
+          }
+          tc_commit(&sm->empty[slot]);
+        }
+        if (!ok) break;
+        tc_commit(&sm->tfull[h]);
+      }
+      tc_commit(&sm->drain);
+      drain_wait(&sm->drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------- epilogue (warps 0..7)
+    const int q = warp & 3, h = warp >> 2;
+    const int rho = q * 32 + lane;   // TMEM lane = row of the item's tile
+    const float inv_gs_b = MX ? 1.0f : 1.0f / *p.b_gs;
+    const int row_last0 = p.out_last_f32 != nullptr ? p.group_offsets[G - 1] : 0;   // first shared row
+    float amax = 0.0f;
+    int itc = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
+      const Item it = decode_item(item, pref, tb, G, MT2, p.group_offsets);
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
+      const float a0 = hdr->alpha[0] * inv_gs_b, a1 = hdr->alpha[1] * inv_gs_b;
+      const bool last_f32 = !GATE_UP && p.out_last_f32 != nullptr && it.g == G - 1;  // shared expert: fp32
+      // down: y = acc * (alpha * routing weight)
+      const float fac =
+          (!GATE_UP && p.row_scale && rho < it.rows) ? a0 * __ldg(p.row_scale + it.row0 + rho) : a0;
+      if (!mbar_wait(&sm->tfull[h], itc & 1, abort, p.wait_limit)) break;
+      tc_fence_after();
+      drain_rows<GATE_UP>(p, tmem + ((uint32_t)(q * 32) << 16) + 128 * h, it, 2 * it.mt + h, rho, N, a0, a1, fac,
+                          last_f32, row_last0, amax);
+      tc_fence_before();
+      mbar_arrive(&sm->tempty[h]);
+    }
+    if (GATE_UP && p.out_amax != nullptr) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) atomic_max_nonneg(p.out_amax, amax);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp0) tmem_dealloc(tmem, kWTmemCols);
+  if (tid == 0 && sm->abort) set_status(p.status, MOE_ERR_TIMEOUT);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -549,16 +822,32 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   a.status = pl.status;
   a.wait_limit = debug_wait_limit();
   // tile shape: 1 = one CTA per SM, weight rows on M; 2 = two CTAs per SM,
-  // weight rows on M; 3 = two CTAs per SM, the group's rows on M
+  // weight rows on M; 3 = two CTAs per SM, the group's rows on M; 4 = one CTA
+  // per SM, the group's rows on M, 256 weight rows per tile (N a multiple of 256)
   const int forced = debug_fp4_tile(pl.gate_up != 0);
-  const int shape = forced != 0 ? forced : pl.ctas_per_sm == 1 ? 1 : 3;
-  const int ctas = shape == 1 ? 1 : 2;
-  const size_t smem = fp4_smem_bytes(pl.num_groups, ctas == 2 ? Shape<2>::kStages : Shape<1>::kStages);
-  if (smem > (ctas == 2 ? 113 : 227) * 1024) return MOE_ERR_UNSUPPORTED;
+  int shape = forced != 0 ? forced : pl.ctas_per_sm == 1 ? 1 : 4;
+  if (shape == 4 && pl.N % (2 * kM) != 0) shape = 3;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   using KernelFn = void (*)(const BoxMaps, Args);
+  if (shape == 4) {
+    const size_t smem = 1024 + (size_t)wide::kWStages * wide::kWStageBytes + sizeof(wide::WSmem) +
+                        (size_t)(pl.num_groups + 1) * 8;
+    if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    static const KernelFn wtable[2][2] = {
+        {gemm_tc_fp4_wide_kernel<false, false>, gemm_tc_fp4_wide_kernel<true, false>},
+        {gemm_tc_fp4_wide_kernel<false, true>, gemm_tc_fp4_wide_kernel<true, true>}};
+    const KernelFn k = wtable[mx ? 1 : 0][pl.gate_up ? 1 : 0];
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(wide::kWThreads), smem, s, maps, a);
+    if (e != cudaSuccess) return cuda_ok(e);
+    count_launches(1);
+    return MOE_OK;
+  }
+  const int ctas = shape == 1 ? 1 : 2;
+  const size_t smem = fp4_smem_bytes(pl.num_groups, ctas == 2 ? Shape<2>::kStages : Shape<1>::kStages);
+  if (smem > (ctas == 2 ? 113 : 227) * 1024) return MOE_ERR_UNSUPPORTED;
   // [mx][gate_up][shape - 1]
   static const KernelFn table[2][2][3] = {
       {{gemm_tc_fp4_kernel<false, 1, false, false>, gemm_tc_fp4_kernel<false, 2, false, false>,

@@ -70,7 +70,8 @@ MX_GROUPS = si.LayerConfig("mx_groups", T=300, H=512, I=256, I_s=256, E=24, k=4,
 @pytest.mark.parametrize("cfg", [GROUPS, MX_GROUPS], ids=["nvfp4", "mxfp4"])
 def test_fp4_tile_shapes_agree(cfg):
     """Every tile shape of the block-scaled FP4 GEMMs (one or two CTAs per SM;
-    weight rows or the group's rows on the MMA's M side) gives the library
+    weight rows or the group's rows on the MMA's M side; 128 or 256 weight
+    rows per tile) gives the library
     default's bits, on skewed routing with empty groups, groups of several
     128-row tiles and ragged last tiles (the default is checked against the
     oracle above)."""
@@ -81,7 +82,7 @@ def test_fp4_tile_shapes_agree(cfg):
     ws = layer.workspace()
     outs = {}
     try:
-        for shape in (0, 11, 12, 13, 21, 22, 23, 31, 32, 33):
+        for shape in (0, 11, 12, 13, 14, 21, 22, 23, 24, 31, 32, 33, 34, 41, 42, 43, 44):
             Bd.moe_debug_set(Bd.MOE_DEBUG_FP4_TILE, shape)
             outs[shape] = layer.forward(x, lg, ws=ws).clone()
             torch.cuda.synchronize()
