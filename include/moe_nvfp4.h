@@ -434,9 +434,10 @@ unsigned long long moe_kernel_launches(void);
  *   stages) with the weight rows on the MMA's M side; 2 = two CTAs per SM
  *   (one accumulator and three stages each), weight rows on M; 3 = two CTAs
  *   per SM with the group's rows on M; 4 = one CTA per SM, the group's rows
- *   on M and 256 weight rows per tile (two halves with their own MMA
- *   issuers; a GEMM whose N is not a multiple of 256 takes 3 instead); 0
- *   keeps the library's choice for that GEMM. Results agree to the last bit
+ *   on M and 256 weight rows per tile (two N = 128 halves with their own
+ *   MMA issuers); 5 = the same tile as one N = 256 MMA per K block (one
+ *   issuer); a GEMM whose N is not a multiple of 256 takes 3 instead of 4 or
+ *   5; 0 keeps the library's choice for that GEMM. Results agree to the last bit
  *   across shapes. Used to compare them.
  * Errors: an unknown key, or a value out of range -> MOE_ERR_INVALID_ARG.
  */

@@ -696,7 +696,7 @@ moe_status moe_debug_set(int key, long long value) {
       g_decode_stage_kb.store(value > 0 ? (int)value : kDefaultDecodeStageKb, std::memory_order_relaxed);
       return MOE_OK;
     case MOE_DEBUG_FP4_TILE:
-      if (value < 0 || value > 44 || value % 10 > 4) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 55 || value % 10 > 5) return MOE_ERR_INVALID_ARG;
       g_fp4_tile.store((int)value, std::memory_order_relaxed);
       return MOE_OK;
 

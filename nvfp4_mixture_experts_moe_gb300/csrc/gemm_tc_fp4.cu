@@ -197,6 +197,65 @@ __device__ __forceinline__ void drain_rows(const Args& p, uint32_t tacc, const I
   }
 }
 
+// The same drain with the whole 128-column row in registers first: the
+// accumulator is read and converted, `release` hands it back to the next
+// tile's MMAs, and only then the row is stored (bf16 outputs only).
+template <bool GATE_UP, typename Release>
+__device__ __forceinline__ void drain_rows_release(const Args& p, uint32_t tacc, const Item& it, int mt, int rho,
+                                                   int N, float a0, float a1, float fac, float& amax,
+                                                   Release release) {
+  const bool valid = rho < it.rows;
+  constexpr int kPk = GATE_UP ? 8 : 16;   // bf16 pairs per 32 columns
+  uint32_t pk[4 * kPk];
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    if (!GATE_UP) {   // 16 columns per load: the 64 packed words and one load fit the registers
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t r[16];
+        tmem_ld16(tacc + 32 * ch + 16 * hf, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          pk[ch * kPk + 8 * hf + v] =
+              float2_to_bf16x2_bits(__uint_as_float(r[2 * v]) * fac, __uint_as_float(r[2 * v + 1]) * fac);
+      }
+      continue;
+    }
+    uint32_t r[32];
+    tmem_ld32(tacc + 32 * ch, r);
+    tmem_ld_wait();
+    {
+      // columns 32ch..32ch+31: gate of features 64 mt + 16 ch + 0..7, their
+      // up, gate of the next 8, their up (weight rows interleaved by 8)
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        float h2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = i + e, gc = j < 8 ? j : j + 8;
+          h2[e] = silu(__uint_as_float(r[gc]) * a0) * (__uint_as_float(r[gc + 8]) * a1);
+        }
+        const uint32_t hb = float2_to_bf16x2_bits(h2[0], h2[1]);
+        pk[ch * kPk + (i >> 1)] = hb;
+        if (valid)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb << 16)), fabsf(__uint_as_float(hb & 0xffff0000u))));
+      }
+    }
+  }
+  release();
+  if (!valid) return;
+  uint16_t* o = GATE_UP ? p.out + (size_t)(it.row0 + rho) * (N / 2) + 64 * mt
+                        : p.out + (size_t)(it.row0 + rho) * N + mt * kM;
+#pragma unroll
+  for (int v = 0; v < kPk / 2; ++v) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = pk[8 * v + e];
+    stg_v8(o + 16 * v, w);
+  }
+}
+
 // MX: MXFP4 operands (E8M0 scales per 32, kind::mxf4, two scale atoms per
 // operand and stage, no global scales); otherwise NVFP4 (E4M3 per 16,
 // kind::mxf4nvf4, four atoms per operand and stage).
@@ -540,8 +599,12 @@ struct WSmem {
 };
 }  // namespace wide
 
-template <bool GATE_UP, bool MX>
-__global__ void __launch_bounds__(wide::kWThreads, 1)
+// N256: one N = 256 MMA per K block into one 256-column accumulator (one
+// issuing thread; three scale-copy threads: the activation atoms and each
+// weight tile's atoms); otherwise two N = 128 halves, each with its own
+// issuing thread, scale-copy thread and accumulator.
+template <bool GATE_UP, bool MX, bool N256>
+__global__ void __maxnreg__(128)
     gemm_tc_fp4_wide_kernel(const __grid_constant__ BoxMaps maps, Args p) {
   using namespace wide;
   constexpr int kSfBytes = MX ? kSfStage / 2 : kSfStage;   // scale bytes per operand tile and stage
@@ -570,15 +633,15 @@ __global__ void __launch_bounds__(wide::kWThreads, 1)
     for (int i = 0; i < kWStages; ++i) {
       mbar_init(&sm->aready[i], 1);
       mbar_init(&sm->bready[i], 1);
-      mbar_init(&sm->sf_full[i], 2);
-      mbar_init(&sm->empty[i], 2);
+      mbar_init(&sm->sf_full[i], N256 ? 3 : 2);
+      mbar_init(&sm->empty[i], N256 ? 1 : 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm->tfull[i], 1);
-      mbar_init(&sm->tempty[i], 128);
+      mbar_init(&sm->tempty[i], N256 ? 256 : 128);
     }
-    mbar_init(&sm->drain, 2);
-    mbar_init(&sm->drain_sf, 2);
+    mbar_init(&sm->drain, N256 ? 1 : 2);
+    mbar_init(&sm->drain_sf, N256 ? 3 : 2);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -655,10 +718,11 @@ __global__ void __launch_bounds__(wide::kWThreads, 1)
       for (int i = max(0, j - kWStages); i < j; ++i) drain_wait(&sm->bready[i % kWStages], (i / kWStages) & 1);
     }
     __syncwarp();
-  } else if (warp == kSfWarp0 || warp == kSfWarp0 + 1) {
-    // ------------------------- scale factors -> TMEM: half h's weight atoms
-    // and every other activation atom (the two threads split the shared ones)
-    const int h = warp - kSfWarp0;
+  } else if (warp == kSfWarp0 || warp == kSfWarp0 + 1 || (N256 && warp == kMmaWarp0 + 1)) {
+    // ------------------------- scale factors -> TMEM. Two halves: thread h
+    // copies weight tile h's atoms and every other activation atom. N256:
+    // thread h copies weight tile h's atoms, the third the activation atoms.
+    const int h = warp == kMmaWarp0 + 1 ? 2 : warp - kSfWarp0;
     if (lane == 0) {
       int j = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
@@ -674,14 +738,28 @@ __global__ void __launch_bounds__(wide::kWThreads, 1)
           }
           tc_fence_after();
           const uint32_t sfa = smem_u32(base + slot * kWStageBytes) + 3 * kTile;
-          const uint32_t sfb = sfa + (1 + h) * kSfSlot;
+          const uint32_t sfb = sfa + (1 + (h & 1)) * kSfSlot;
           const uint32_t col = tmem + kWSfCol0 + slot * kSfCols;
+          if (N256) {
+            // activation atoms at columns 4 kk; the weight atoms of a K block
+            // side by side (rows 0-127, then 128-255): 16 + 8 kk + 4 h
+            if (h == 2) {
 #pragma unroll
-          for (int kk = h; kk < kAtoms; kk += 2)
-            tc_cp_32x128b_warpx4(col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
+              for (int kk = 0; kk < kAtoms; ++kk)
+                tc_cp_32x128b_warpx4(col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
+            } else {
 #pragma unroll
-          for (int kk = 0; kk < kAtoms; ++kk)
-            tc_cp_32x128b_warpx4(col + 16 + 16 * h + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
+              for (int kk = 0; kk < kAtoms; ++kk)
+                tc_cp_32x128b_warpx4(col + 16 + 8 * kk + 4 * h, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
+            }
+          } else {
+#pragma unroll
+            for (int kk = h; kk < kAtoms; kk += 2)
+              tc_cp_32x128b_warpx4(col + kk * 4, smem_desc(sfa + kk * 512, 16, 128, kSwizzleNone));
+#pragma unroll
+            for (int kk = 0; kk < kAtoms; ++kk)
+              tc_cp_32x128b_warpx4(col + 16 + 16 * h + kk * 4, smem_desc(sfb + kk * 512, 16, 128, kSwizzleNone));
+          }
           tc_commit(&sm->sf_full[slot]);
         }
         if (!ok) break;
@@ -692,15 +770,16 @@ __global__ void __launch_bounds__(wide::kWThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
     // ------------------------------------------------- MMA issuer of half h
-    const int h = warp - kMmaWarp0;
-    if (lane == 0) {
+    const int h = warp - kMmaWarp0;   // N256: only half 0's thread issues (N = 256)
+    if (lane == 0 && !(N256 && h == 1)) {
       int j = 0, itc = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
-        if (!mbar_wait(&sm->tempty[h], (itc & 1) ^ 1, abort, p.wait_limit)) break;
+        if (!mbar_wait(&sm->tempty[h], (itc & 1) ^ 1, abort, p.wait_limit)) break;   // h = 0 with N256
         const uint32_t d = tmem + 128 * h;
         tc_fence_after();
-        const uint32_t idesc = idesc_nvf4(kM, kM);
-        const uint32_t idesc_mx0 = idesc_mxf4(kM, kM, 0), idesc_mx2 = idesc_mxf4(kM, kM, 2);
+        constexpr int kN = N256 ? 2 * kM : kM;
+        const uint32_t idesc = idesc_nvf4(kM, kN);
+        const uint32_t idesc_mx0 = idesc_mxf4(kM, kN, 0), idesc_mx2 = idesc_mxf4(kM, kN, 2);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kWStages;
@@ -709,16 +788,17 @@ __global__ void __launch_bounds__(wide::kWThreads, 1)
           const uint32_t as = smem_u32(base + slot * kWStageBytes);
           const uint32_t bs = as + (1 + h) * kTile;
           const uint32_t sfa_col = tmem + kWSfCol0 + slot * kSfCols;
-          const uint32_t sfb_col = sfa_col + 16 + 16 * h;
+          const uint32_t sfb_col = sfa_col + 16 + (N256 ? 0 : 16 * h);
+          constexpr int kSfbStep = N256 ? 8 : 4;   // columns per weight atom index
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc(as + kk * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(bs + kk * 32, 16, 1024, kSwizzle128B);
             if (MX)  // atom kk / 2, byte pair 2 * (kk % 2)
               mma_mxf4(d, ad, bd, (kk & 1) ? idesc_mx2 : idesc_mx0, sfa_col + (kk >> 1) * 4,
-                       sfb_col + (kk >> 1) * 4, (ks | kk) != 0);
+                       sfb_col + (kk >> 1) * kSfbStep, (ks | kk) != 0);
             else
-              mma_nvf4(d, ad, bd, idesc, sfa_col + kk * 4, sfb_col + kk * 4, (ks | kk) != 0);
+              mma_nvf4(d, ad, bd, idesc, sfa_col + kk * 4, sfb_col + kk * kSfbStep, (ks | kk) != 0);
           }
           tc_commit(&sm->empty[slot]);
         }
@@ -745,12 +825,20 @@ __global__ void __launch_bounds__(wide::kWThreads, 1)
       // down: y = acc * (alpha * routing weight)
       const float fac =
           (!GATE_UP && p.row_scale && rho < it.rows) ? a0 * __ldg(p.row_scale + it.row0 + rho) : a0;
-      if (!mbar_wait(&sm->tfull[h], itc & 1, abort, p.wait_limit)) break;
+      if (!mbar_wait(&sm->tfull[N256 ? 0 : h], itc & 1, abort, p.wait_limit)) break;
       tc_fence_after();
-      drain_rows<GATE_UP>(p, tmem + ((uint32_t)(q * 32) << 16) + 128 * h, it, 2 * it.mt + h, rho, N, a0, a1, fac,
-                          last_f32, row_last0, amax);
-      tc_fence_before();
-      mbar_arrive(&sm->tempty[h]);
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + 128 * h;
+      uint64_t* tempty = &sm->tempty[N256 ? 0 : h];
+      if (last_f32) {
+        drain_rows<GATE_UP>(p, tacc, it, 2 * it.mt + h, rho, N, a0, a1, fac, true, row_last0, amax);
+        tc_fence_before();
+        mbar_arrive(tempty);
+      } else {
+        drain_rows_release<GATE_UP>(p, tacc, it, 2 * it.mt + h, rho, N, a0, a1, fac, amax, [&] {
+          tc_fence_before();
+          mbar_arrive(tempty);
+        });
+      }
     }
     if (GATE_UP && p.out_amax != nullptr) {
 #pragma unroll
@@ -825,21 +913,28 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   // weight rows on M; 3 = two CTAs per SM, the group's rows on M; 4 = one CTA
   // per SM, the group's rows on M, 256 weight rows per tile (N a multiple of 256)
   const int forced = debug_fp4_tile(pl.gate_up != 0);
-  int shape = forced != 0 ? forced : pl.ctas_per_sm == 1 ? 1 : 4;
-  if (shape == 4 && pl.N % (2 * kM) != 0) shape = 3;
+  int shape = forced != 0 ? forced : pl.ctas_per_sm == 1 ? 1 : 5;
+  if (shape >= 4 && pl.N % (2 * kM) != 0) shape = 3;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   using KernelFn = void (*)(const BoxMaps, Args);
-  if (shape == 4) {
-    const size_t smem = 1024 + (size_t)wide::kWStages * wide::kWStageBytes + sizeof(wide::WSmem) +
-                        (size_t)(pl.num_groups + 1) * 8;
-    if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
-    static const KernelFn wtable[2][2] = {
-        {gemm_tc_fp4_wide_kernel<false, false>, gemm_tc_fp4_wide_kernel<true, false>},
-        {gemm_tc_fp4_wide_kernel<false, true>, gemm_tc_fp4_wide_kernel<true, true>}};
-    const KernelFn k = wtable[mx ? 1 : 0][pl.gate_up ? 1 : 0];
+  const size_t wide_smem = 1024 + (size_t)wide::kWStages * wide::kWStageBytes + sizeof(wide::WSmem) +
+                           (size_t)(pl.num_groups + 1) * 8;
+  if ((shape == 4 || shape == 5) && wide_smem > 227 * 1024) shape = 3;
+  if (shape == 4 || shape == 5) {
+    const size_t smem = wide_smem;
+    // [n256][mx][gate_up]
+    static const KernelFn wtable[2][2][2] = {
+        {{gemm_tc_fp4_wide_kernel<false, false, false>, gemm_tc_fp4_wide_kernel<true, false, false>},
+         {gemm_tc_fp4_wide_kernel<false, true, false>, gemm_tc_fp4_wide_kernel<true, true, false>}},
+        {{gemm_tc_fp4_wide_kernel<false, false, true>, gemm_tc_fp4_wide_kernel<true, false, true>},
+         {gemm_tc_fp4_wide_kernel<false, true, true>, gemm_tc_fp4_wide_kernel<true, true, true>}}};
+    const KernelFn k = wtable[shape == 5 ? 1 : 0][mx ? 1 : 0][pl.gate_up ? 1 : 0];
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int fit = 0;   // one CTA of this kernel must fit an SM (registers and shared memory)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k, wide::kWThreads, smem) != cudaSuccess || fit < 1)
+      return MOE_ERR_UNSUPPORTED;
     cudaError_t e = launch_ex(pl.pdl, k, dim3(sms), dim3(wide::kWThreads), smem, s, maps, a);
     if (e != cudaSuccess) return cuda_ok(e);
     count_launches(1);

@@ -147,7 +147,7 @@ def test_debug_hooks_validate_keys(lib):
     for key in (B.MOE_DEBUG_WAIT_LIMIT, B.MOE_DEBUG_EXTRA_ARRIVALS, B.MOE_DEBUG_DISABLE_DECODE_FUSED,
                 B.MOE_DEBUG_DECODE_STAGE_KB, B.MOE_DEBUG_FP4_TILE):
         assert lib.moe_debug_set(key, 0) == B.MOE_OK   # 0 restores every default
-    for bad in (-1, 5, 15, 45, 50, 100):   # FP4 tile shapes: two digits, each 0..4
+    for bad in (-1, 6, 16, 56, 60, 100):   # FP4 tile shapes: two digits, each 0..5
         assert lib.moe_debug_set(B.MOE_DEBUG_FP4_TILE, bad) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_set(B.MOE_DEBUG_FP4_TILE, 23) == B.MOE_OK
     assert lib.moe_debug_set(B.MOE_DEBUG_FP4_TILE, 0) == B.MOE_OK

@@ -71,7 +71,7 @@ MX_GROUPS = si.LayerConfig("mx_groups", T=300, H=512, I=256, I_s=256, E=24, k=4,
 def test_fp4_tile_shapes_agree(cfg):
     """Every tile shape of the block-scaled FP4 GEMMs (one or two CTAs per SM;
     weight rows or the group's rows on the MMA's M side; 128 or 256 weight
-    rows per tile) gives the library
+    rows per tile, the latter as two N = 128 MMAs or one N = 256) gives the library
     default's bits, on skewed routing with empty groups, groups of several
     128-row tiles and ragged last tiles (the default is checked against the
     oracle above)."""
@@ -82,7 +82,8 @@ def test_fp4_tile_shapes_agree(cfg):
     ws = layer.workspace()
     outs = {}
     try:
-        for shape in (0, 11, 12, 13, 14, 21, 22, 23, 24, 31, 32, 33, 34, 41, 42, 43, 44):
+        for shape in (0, 11, 12, 13, 14, 15, 21, 22, 23, 24, 25, 31, 32, 33, 34, 35, 41, 42, 43, 44, 45, 51, 52,
+                      53, 54, 55):
             Bd.moe_debug_set(Bd.MOE_DEBUG_FP4_TILE, shape)
             outs[shape] = layer.forward(x, lg, ws=ws).clone()
             torch.cuda.synchronize()
