@@ -586,8 +586,10 @@ constexpr int kWBLoadWarp = 13;  // the two weight tiles
 constexpr int kWThreads = 14 * 32;
 
 struct WSmem {
-  uint64_t aready[kWStages];   // the activation tile and its atoms landed
-  uint64_t bready[kWStages];   // both weight tiles and their atoms landed
+  uint64_t aready[kWStages];   // the activation tile landed
+  uint64_t bready[kWStages];   // both weight tiles landed
+  uint64_t sfready[kWStages];  // the stage's scale atoms landed (copied first, so the
+                               // moves into TMEM overlap the tiles' flight)
   uint64_t sf_full[kWStages];  // both halves' scale copies completed
   uint64_t empty[kWStages];    // both halves' MMAs completed
   uint64_t tfull[2];
@@ -633,6 +635,7 @@ __global__ void __maxnreg__(128)
     for (int i = 0; i < kWStages; ++i) {
       mbar_init(&sm->aready[i], 1);
       mbar_init(&sm->bready[i], 1);
+      mbar_init(&sm->sfready[i], 2);
       mbar_init(&sm->sf_full[i], N256 ? 3 : 2);
       mbar_init(&sm->empty[i], N256 ? 1 : 2);
     }
@@ -681,14 +684,18 @@ __global__ void __maxnreg__(128)
           const int slot = j % kWStages;
           if (!mbar_wait(&sm->empty[slot], ((j / kWStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
           uint8_t* st = base + slot * kWStageBytes;
-          mbar_arrive_expect_tx(&sm->aready[slot], kTile + kSfBytes);
-          tma_load_2d(smem_u32(st), &maps.m[3], ks * kRowBytes, it.row0, &sm->aready[slot]);
+          mbar_arrive_expect_tx(&sm->sfready[slot], kSfBytes);
           bulk_g2s(smem_u32(st + 3 * kTile), p.b_sf_tiles + ((size_t)it.tile * KS + ks) * kSfBytes, kSfBytes,
-                   &sm->aready[slot]);
+                   &sm->sfready[slot]);
+          mbar_arrive_expect_tx(&sm->aready[slot], kTile);
+          tma_load_2d(smem_u32(st), &maps.m[3], ks * kRowBytes, it.row0, &sm->aready[slot]);
         }
         if (!ok) break;
       }
-      for (int i = max(0, j - kWStages); i < j; ++i) drain_wait(&sm->aready[i % kWStages], (i / kWStages) & 1);
+      for (int i = max(0, j - kWStages); i < j; ++i) {
+        drain_wait(&sm->aready[i % kWStages], (i / kWStages) & 1);
+        drain_wait(&sm->sfready[i % kWStages], (i / kWStages) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == kWBLoadWarp) {
@@ -704,18 +711,26 @@ __global__ void __maxnreg__(128)
           const int slot = j % kWStages;
           if (!mbar_wait(&sm->empty[slot], ((j / kWStages) & 1) ^ 1, abort, p.wait_limit)) { ok = false; break; }
           uint8_t* st = base + slot * kWStageBytes;
-          mbar_arrive_expect_tx(&sm->bready[slot], 2 * (kTile + kSfBytes));
+          mbar_arrive_expect_tx(&sm->sfready[slot], 2 * kSfBytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const size_t tile = (size_t)(2 * it.mt + h) * KS + ks;
+            bulk_g2s(smem_u32(st + 3 * kTile + (1 + h) * kSfSlot), wsf + tile * kSfBytes, kSfBytes,
+                     &sm->sfready[slot]);
+          }
+          mbar_arrive_expect_tx(&sm->bready[slot], 2 * kTile);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const size_t tile = (size_t)(2 * it.mt + h) * KS + ks;
             bulk_g2s(smem_u32(st + (1 + h) * kTile), wdata + tile * kTile, kTile, &sm->bready[slot]);
-            bulk_g2s(smem_u32(st + 3 * kTile + (1 + h) * kSfSlot), wsf + tile * kSfBytes, kSfBytes,
-                     &sm->bready[slot]);
           }
         }
         if (!ok) break;
       }
-      for (int i = max(0, j - kWStages); i < j; ++i) drain_wait(&sm->bready[i % kWStages], (i / kWStages) & 1);
+      for (int i = max(0, j - kWStages); i < j; ++i) {
+        drain_wait(&sm->bready[i % kWStages], (i / kWStages) & 1);
+        drain_wait(&sm->sfready[i % kWStages], (i / kWStages) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == kSfWarp0 || warp == kSfWarp0 + 1 || (N256 && warp == kMmaWarp0 + 1)) {
@@ -729,10 +744,9 @@ __global__ void __maxnreg__(128)
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kWStages;
-          // the slot's previous MMAs (both halves) completed before its loads
-          // were issued, so its TMEM columns are free once the data landed
-          if (!mbar_wait(&sm->aready[slot], (j / kWStages) & 1, abort, p.wait_limit) ||
-              !mbar_wait(&sm->bready[slot], (j / kWStages) & 1, abort, p.wait_limit)) {
+          // the slot's previous MMAs completed before its loads were issued,
+          // so its TMEM columns are free once the atoms landed
+          if (!mbar_wait(&sm->sfready[slot], (j / kWStages) & 1, abort, p.wait_limit)) {
             ok = false;
             break;
           }
@@ -783,7 +797,12 @@ __global__ void __maxnreg__(128)
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kWStages;
-          if (!mbar_wait(&sm->sf_full[slot], (j / kWStages) & 1, abort, p.wait_limit)) { ok = false; break; }
+          if (!mbar_wait(&sm->sf_full[slot], (j / kWStages) & 1, abort, p.wait_limit) ||
+              !mbar_wait(&sm->aready[slot], (j / kWStages) & 1, abort, p.wait_limit) ||
+              !mbar_wait(&sm->bready[slot], (j / kWStages) & 1, abort, p.wait_limit)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t as = smem_u32(base + slot * kWStageBytes);
           const uint32_t bs = as + (1 + h) * kTile;
