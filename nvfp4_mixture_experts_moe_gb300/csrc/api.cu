@@ -114,6 +114,7 @@ struct ForwardWs {
   uint8_t* hsf;       // W4A4: [tiles, I/256, 2048]
   int tiles;          // W4A4: bound on the 128-row tiles of all groups
   float* hgs;
+  int* fused_region;        // kFusedRegionInts ints right after the header (every shape)
   int* fused_counters;      // decode micro path: gu_done [E+1], cmb_cnt [T * H/128], hmax [rows], next item
   size_t fused_counter_ints;
   size_t bytes;
@@ -123,9 +124,15 @@ struct ForwardWs {
 static int local_experts(const moe_layer_desc& L) { return L.local_experts > 0 ? L.local_experts : L.E; }
 
 // The single-kernel decode path applies to this layer.
+// gu_done [E+1], cmb_cnt [T * H/128], hmax [rows], next item
+static size_t fused_counter_ints(const moe_layer_desc& L) {
+  const size_t rows = (size_t)L.T * L.k + (L.w13_shared ? (size_t)L.T : 0);
+  return (size_t)(L.E + 1) + (size_t)L.T * (L.H / 128) + rows + 1;
+}
+
 static bool use_decode_fused(const moe_layer_desc& L) {
   return L.mode == MOE_W4A16 && decode_fused_supported(L.T, L.H, L.I, local_experts(L), L.k) &&
-         local_experts(L) == L.E;
+         local_experts(L) == L.E && fused_counter_ints(L) <= kFusedSetInts;
 }
 
 static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
@@ -135,6 +142,7 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
   Carver c{static_cast<uint8_t*>(ws), 0};
   ForwardWs f;
   f.hdr = c.take<WsHeader>(1);
+  f.fused_region = c.take<int>(kFusedRegionInts);   // fixed place for every shape
   f.ids = c.take<int32_t>(P);
   f.w = c.take<float>(P);
   f.logits = L.w_router ? c.take<float>((size_t)L.T * L.E) : nullptr;
@@ -173,8 +181,8 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
     f.tiles = 0;
   }
   if (use_decode_fused(L)) {
-    f.fused_counter_ints = (size_t)(L.E + 1) + (size_t)L.T * (L.H / 128) + rows + 1;
-    f.fused_counters = c.take<int>(f.fused_counter_ints);
+    f.fused_counter_ints = fused_counter_ints(L);
+    f.fused_counters = f.fused_region;
   } else {
     f.fused_counters = nullptr;
     f.fused_counter_ints = 0;
@@ -273,6 +281,10 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* co
   moe_status st = check_device();
   if (st != MOE_OK) return st;
   auto* hdr = static_cast<WsHeader*>(ws);
+  // the scratch below overlaps a forward workspace's decode counters: they
+  // are no longer known to be zero
+  st = cuda_ok(cudaMemsetAsync(&hdr->fused_clean, 0, sizeof(int), (cudaStream_t)stream));
+  if (st != MOE_OK) return st;
   return launch_permute(topk_ids, T, k, E, counts, offsets, perm, inv_perm, &hdr->status,
                         static_cast<uint8_t*>(ws) + sizeof(WsHeader), nullptr, nullptr, nullptr, nullptr,
                         (cudaStream_t)stream);
@@ -530,10 +542,9 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     logits = f.logits;
   }
   if (f.fused_counters != nullptr && !debug_decode_fused_disabled()) {
-    // decode micro path: the whole layer in one cooperative kernel
-    st = cuda_ok(cudaMemsetAsync(f.fused_counters, 0, f.fused_counter_ints * sizeof(int), s));
-    if (st != MOE_OK) return st;
-    stage_mark(0, s);  // recorded again: stage 0 -> 1 is the fused kernel alone
+    // decode micro path: the whole layer in one cooperative kernel (its
+    // counters alternate between two sets in the workspace; each launch
+    // zeroes the set the next one uses, so no memset precedes it)
     DecodeFusedPlan q;
     q.logits = logits;
     q.x = x;
@@ -553,10 +564,12 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     q.h = f.h;
     q.y = f.y;
     q.y_shared = f.ys;
-    q.gu_done = f.fused_counters;
-    q.cmb_cnt = f.fused_counters + (E + 1);
-    q.hmax = reinterpret_cast<unsigned*>(f.fused_counters + (E + 1) + (size_t)T * (H / 128));
-    q.next_item = f.fused_counters + (E + 1) + (size_t)T * (H / 128) + rows;
+    q.counters = f.fused_region;   // set 0; set 1 kFusedSetInts further
+    q.set_ints = (int)kFusedSetInts;
+    q.counter_ints = (int)f.fused_counter_ints;
+    q.clean = &f.hdr->fused_clean;
+    q.ticket = &f.hdr->fused_ticket;
+    q.gbar = &f.hdr->fused_gbar;
     q.status = &f.hdr->status;
     q.wait_limit = debug_wait_limit();
     q.extra_arrivals = debug_extra_arrivals();

@@ -18,9 +18,22 @@ struct WsHeader {
   int status;
   int pad0;
   float amax[4];     // atomic-max slots for dynamic global scales
-  int pad[58];
+  // the single-kernel decode path's counters (two sets in the fused region
+  // after this header): 1 once both sets are known to be zero; launch ticket
+  // (one per CTA; launch n = ticket / grid uses set n % 2 and zeroes the
+  // other); first-use grid barrier (counts up, never reset)
+  int fused_clean;
+  int pad1;
+  unsigned long long fused_ticket;
+  unsigned long long fused_gbar;
+  int pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+// A forward workspace keeps this many ints right after the header for the
+// single-kernel decode path's two counter sets (kFusedSetInts each),
+// whatever the call's shape, so no other buffer ever overlaps them.
+constexpr size_t kFusedSetInts = 2048;
+constexpr size_t kFusedRegionInts = 2 * kFusedSetInts;
 
 constexpr size_t kAlign = 256;
 __host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }

@@ -100,10 +100,15 @@ struct Args {
   uint16_t* h;          // [rows, I] bf16
   uint16_t* y;          // [T*k, H] routed rows, bf16
   float* y_shared;      // [T, H] the shared expert's rows, fp32
-  int* gu_done;         // [groups] (zeroed by the caller)
-  int* cmb_cnt;         // [T][H/128] (zeroed)
-  int* next_item;       // grid-wide item counter (zeroed)
-  unsigned* hmax;       // [rows] bf16 magnitude bits of max |h| (zeroed)
+  // two counter sets (set 1 set_ints ints after set 0), each: gu_done
+  // [groups], cmb_cnt [T][H/128], hmax [rows] (bf16 magnitude bits of max
+  // |h|), the grid's item counter
+  int* counters;
+  int set_ints;
+  int counter_ints;
+  int* clean;                    // header: 1 = both sets were zeroed once
+  unsigned long long* ticket;    // header: one per CTA per launch
+  unsigned long long* gbar;      // header: first-use grid barrier (counts up)
   int* status;
   int slots;
   int stage_kb;         // K blocks per ring slot (the larger of the two phases' stages)
@@ -125,6 +130,7 @@ struct Smem {
   int q_item[kQueue];            // the CTA's c-th item (its descriptor) at c % kQueue (-1: no more items)
   int q_count;                   // items published
   int first_down;                // index c of the CTA's first down item (or of the end)
+  int* ctr;                      // this launch's counter set
   int abort;
   int A;                         // active groups
   int32_t ids[kMaxT * kMaxK];
@@ -140,6 +146,23 @@ struct Smem {
   float hmul[kHSlots][kMaxT];
   decode::HalfJoin join;         // the two halves' partial sums of an item
 };
+
+// This launch's counters inside its set.
+struct Ctr {
+  int* gu_done;
+  int* cmb_cnt;
+  unsigned* hmax;
+  int* next_item;
+};
+__device__ __forceinline__ Ctr ctr_of(int* base, const Args& p) {
+  Ctr c;
+  const int rows = p.T * p.k + (p.has_shared ? p.T : 0);
+  c.gu_done = base;
+  c.cmb_cnt = base + p.E + 1;
+  c.hmax = reinterpret_cast<unsigned*>(c.cmb_cnt + p.T * (p.H / 128));
+  c.next_item = reinterpret_cast<int*>(c.hmax + rows);
+  return c;
+}
 
 // Power-of-two row scale from a row's largest bf16 magnitude (bit pattern m):
 // 2^sh brings the maximum into [2^14, 2^15), where every bf16 value down to
@@ -190,6 +213,22 @@ __device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatil
   while (true) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+__device__ __forceinline__ bool wait_counter64(const unsigned long long* ctr, unsigned long long target,
+                                               volatile int* abort, long long limit) {
+  const long long t0 = clock64();
+  while (true) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
     if (v >= target) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
@@ -290,7 +329,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   }
   __syncthreads();   // barriers initialised
   int first_item = 0;
-  if (warp == kProducerWarp && lane == 0) first_item = atomicAdd(p.next_item, 1);   // latency hidden by phase 0
+  if (warp == kProducerWarp && lane == 0) {
+    // Launch n (tickets n*grid .. n*grid + grid-1, one per CTA) counts in set
+    // n % 2, which launch n-1's helper zeroed. The first launch that finds
+    // the sets not known to be zero has CTA 0 zero both while the grid waits
+    // at a barrier (all CTAs are co-resident: cooperative launch).
+    const unsigned long long tk = atomicAdd(p.ticket, 1ull);
+    int clean;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(clean) : "l"(p.clean) : "memory");
+    if (clean == 0) {
+      if (b == 0) {
+        for (int i = 0; i < 2 * p.set_ints; i += 4) *reinterpret_cast<int4*>(p.counters + i) = make_int4(0, 0, 0, 0);
+        __threadfence();
+      }
+      const unsigned long long g = gridDim.x, arrived = atomicAdd(p.gbar, 1ull);
+      wait_counter64(p.gbar, (arrived / g + 1) * g, abort, limit);   // a timeout sets abort
+      __threadfence();
+      if (b == 0) atomicExch(p.clean, 1);   // every CTA has read the flag (it reached the barrier)
+    }
+    int* ctr = p.counters + (size_t)((tk / gridDim.x) & 1) * p.set_ints;
+    sm->ctr = ctr;
+    first_item = atomicAdd(ctr_of(ctr, p).next_item, 1);   // latency hidden by phase 0
+  }
   if (warp == kProducerWarp && lane == 0) {
     // the T x rows (bf16) into the activation area, one bulk copy per row
     mbar_arrive_expect_tx(&sm->xfull, (uint32_t)(T * H * 2));
@@ -410,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
   }
   __syncthreads();
   const int A = sm->A;
+  const Ctr cc = ctr_of(sm->ctr, p);
   const int N1 = A * MT1, N2 = A * MT2;   // items: gate/up 0..N1-1, then down N1..N1+N2-1
   // Items take the groups in the order shared expert first, then the routed
   // groups by expert: the shared expert's rows are the contributions every
@@ -451,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
           mbar_arrive_expect_tx(&sm->full[slot], bytes);
           bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), data + w4a16_chunk(mt, kb0, KB), bytes,
                    &sm->full[slot]);
-          if (st == NST - 1) next = atomicAdd(p.next_item, 1);
+          if (st == NST - 1) next = atomicAdd(cc.next_item, 1);
           if (++slot == S) {
             slot = 0;
             par ^= 1;
@@ -483,6 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
     // there in place, as the x rows are.
     // The CTA takes its items in increasing order, so every item from its
     // first down item on is a down item.
+    if (b == (int)gridDim.x - 1) {
+      // the other counter set, which the previous launch used, zeroed for the next
+      int* other = sm->ctr == p.counters ? p.counters + p.set_ints : p.counters;
+      for (int i = 4 * lane; i < p.set_ints; i += 128) *reinterpret_cast<int4*>(other + i) = make_int4(0, 0, 0, 0);
+    }
     int m = 0, issued = 0;
     const bool xok = __all_sync(0xffffffffu, mbar_wait(&sm->xfree, 0, abort, limit));
     for (int c = xok ? sm->first_down : 0; xok; ++c, ++m) {
@@ -491,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
       const int slot = m % kHSlots;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm->hempty[slot], ((m / kHSlots) & 1) ^ 1, abort, limit))) break;
       const int a = desc_a(item);
-      if (!wait_counter(p.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
+      if (!wait_counter(cc.gu_done + a, MT1 * (1 + p.extra_arrivals), abort, limit)) break;
       const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
       uint16_t* dst = act + (size_t)slot * kMaxT * hs_stride;
       if (lane == 0) {
@@ -503,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
                    &sm->hland[slot]);
       }
       ++issued;
-      const unsigned mx = lane < n ? __ldcg(p.hmax + r0 + lane) : 0u;
+      const unsigned mx = lane < n ? __ldcg(cc.hmax + r0 + lane) : 0u;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm->hland[slot], (m / kHSlots) & 1, abort, limit))) break;
       for (int q = 0; q < n; ++q) {
         const int sh = row_shift(__shfl_sync(0xffffffffu, mx, q));
@@ -557,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
         if (!__all_sync(0xffffffffu, mbar_wait(&sm->done[ds], (cnt_items / kDoneSlots) & 1, abort, limit))) break;
         const int a = desc_a(item), mt = desc_mt(item);
         if (ph == 0) {
-          if (lane == 0) release_add(p.gu_done + a, 1);
+          if (lane == 0) release_add(cc.gu_done + a, 1);
         } else {
           const int r0 = sm->grp_r0[a], n = sm->grp_n[a];
           // count the item's rows: one per (token, 128-column tile). The fence
@@ -569,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
           int last = 0, tok = 0;
           if (lane < n) {
             tok = sm->row_tok[r0 + lane];
-            last = atomicAdd(p.cmb_cnt + (size_t)tok * MT2 + mt, 1) == need - 1;
+            last = atomicAdd(cc.cmb_cnt + (size_t)tok * MT2 + mt, 1) == need - 1;
           }
           unsigned todo = __ballot_sync(0xffffffffu, last);
           if (todo) {
@@ -705,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Args p) {
           v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
           v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
           const int c = 2 * t4 + q;
-          if (g8 == 0 && c < n) atomicMax(p.hmax + r0 + c, v);
+          if (g8 == 0 && c < n) atomicMax(cc.hmax + r0 + c, v);
         }
       } else {
         // y = acc * 2^-s * alpha * routing weight
@@ -792,10 +858,12 @@ moe_status launch_decode_fused(const DecodeFusedPlan& q, cudaStream_t s) {
   a.h = q.h;
   a.y = q.y;
   a.y_shared = q.y_shared;
-  a.gu_done = q.gu_done;
-  a.cmb_cnt = q.cmb_cnt;
-  a.next_item = q.next_item;
-  a.hmax = q.hmax;
+  a.counters = q.counters;
+  a.set_ints = q.set_ints;
+  a.counter_ints = q.counter_ints;
+  a.clean = q.clean;
+  a.ticket = q.ticket;
+  a.gbar = q.gbar;
   a.status = q.status;
   a.wait_limit = q.wait_limit;
   a.extra_arrivals = q.extra_arrivals;

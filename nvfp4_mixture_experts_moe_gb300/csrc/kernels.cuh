@@ -182,10 +182,17 @@ struct DecodeFusedPlan {
   uint16_t* h;               // [T*k + T, I]
   uint16_t* y;               // [T*k, H] routed rows, bf16
   float* y_shared;           // [T, H] the shared expert's rows, fp32
-  int* gu_done;              // [E + 1], zero at launch
-  int* cmb_cnt;              // [T * H/128], zero at launch
-  unsigned* hmax;            // [T*k + T], zero at launch
-  int* next_item;            // one int, zero at launch (the grid's item counter)
+  // Two counter sets of set_ints ints (counters, then set 1): each holds
+  // gu_done [E+1], cmb_cnt [T * H/128], hmax [T*k + T] and the grid's item
+  // counter (counter_ints ints). A launch uses one set, found zero, and
+  // zeroes the other for the next launch; both sets are zeroed by the first
+  // launch that finds *clean == 0.
+  int* counters;
+  int set_ints;
+  int counter_ints;
+  int* clean;                          // workspace header words
+  unsigned long long* ticket;
+  unsigned long long* gbar;
   int* status;
   long long wait_limit;      // cycles per bounded wait
   int extra_arrivals;        // test hook (0): extra arrivals a gate/up tile is expected to make

@@ -135,3 +135,33 @@ def test_fused_timeout_is_reported_and_recovers():
     torch.cuda.synchronize()
     assert B().moe_get_device_status(ws) == 0
     assert torch.equal(good, again)
+
+
+def test_fused_counters_survive_workspace_reuse():
+    """The single-kernel path keeps its counters in a fixed region after the
+    workspace header and leaves them zero at the end of every launch. A
+    workspace whose bytes past the header start as garbage, then serves a
+    multi-kernel (larger T) forward and a standalone permutation (whose
+    scratch overlaps the region), still gives the decode call's exact bits."""
+    cfg, layer = device_layer("decode")
+    x = si.make_x(cfg).cuda()
+    logits = si.make_logits(cfg).cuda()
+    ref = layer.forward(x, logits).clone()              # fresh workspace
+    big = cfg.with_tokens(64)                           # multi-kernel path
+    ws = layer.workspace(big.T)
+    ws[256:].fill_(0xFF)                                # garbage past the zeroed header
+    first = layer.forward(x, logits, ws=ws).clone()     # first use: the region is zeroed
+    again = layer.forward(x, logits, ws=ws).clone()     # steady state: counters left zero
+    layer.forward(si.make_x(big).cuda(), si.make_logits(big).cuda(), ws=ws)
+    after_big = layer.forward(x, logits, ws=ws).clone()
+    ids = torch.randint(0, cfg.E, (big.T, cfg.k), dtype=torch.int32, device="cuda")
+    counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(big.T * cfg.k, dtype=torch.int32, device="cuda")
+    inv = torch.empty_like(perm)
+    B().moe_permute(ids, big.T, cfg.k, cfg.E, counts, offsets, perm, inv, ws)
+    after_permute = layer.forward(x, logits, ws=ws).clone()
+    torch.cuda.synchronize()
+    assert B().moe_get_device_status(ws) == 0
+    for name, o in (("first", first), ("again", again), ("after_big", after_big), ("after_permute", after_permute)):
+        assert torch.equal(o, ref), name
