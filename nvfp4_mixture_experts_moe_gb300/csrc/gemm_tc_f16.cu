@@ -107,6 +107,8 @@ struct Smem {
   uint64_t tfull;
   uint64_t tempty;
   float rowmul[4][kMaxBN];      // epilogue: per-row factors of the tile, one copy per epilogue warp
+                                // (gate/up: 2^-s * alpha_gate; down: 2^-s * routing weight * alpha)
+  float rowmul_up[4][kMaxBN];   // gate/up: 2^-s * alpha_up
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -322,8 +324,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
       const Item it = decode_item(item, pref, G, MT, p.group_offsets);
-      // per-row factors of the tile into this warp's shared copy (no cross-warp sync)
+      // per-row factors of the tile, alpha folded in, into this warp's shared
+      // copy (no cross-warp sync)
+      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
+      const float a0 = hdr->alpha[0], a1 = hdr->alpha[1];
       float* rowmul = sm->rowmul[q];
+      float* rowmul_up = sm->rowmul_up[q];
       __syncwarp();  // done reading the previous item's factors
 #pragma unroll
       for (int i = 0; i < kMaxBN / 32; ++i) {
@@ -334,13 +340,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
           m = __ldg(p.a_mul + r);
           if (!GATE_UP && p.row_scale) m *= __ldg(p.row_scale + r);
         }
-        rowmul[n] = m;
+        rowmul[n] = m * a0;
+        if (GATE_UP) rowmul_up[n] = m * a1;
       }
       __syncwarp();
       if (!mbar_wait(&sm->tfull, itc & 1, abort, p.wait_limit)) break;
       tc_fence_after();
-      const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
-      const float a0 = hdr->alpha[0], a1 = hdr->alpha[1];
       const bool gate_lane = (rho & 8) == 0;   // rows 16j..16j+7 gate, 16j+8..16j+15 up (interleave by 8)
       const int f = 64 * it.mt + 8 * (rho >> 4) + (rho & 7);
       for (int c0 = 0; c0 < it.bn; c0 += 32) {  // columns past bn are read (within the buffer) and not stored
@@ -357,8 +362,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
             other[c] = __shfl_xor_sync(0xffffffffu, __uint_as_float(gate_lane ? r[16 + c] : r[c]), 8);
 #pragma unroll
           for (int c4 = 0; c4 < 16; c4 += 4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(rowmul + c0 + cb + c4);  // broadcast read
-            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+            const float4 g4 = *reinterpret_cast<const float4*>(rowmul + c0 + cb + c4);     // broadcast reads
+            const float4 u4 = *reinterpret_cast<const float4*>(rowmul_up + c0 + cb + c4);
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
             for (int t = 0; t < 4; t += 2) {  // two tokens per bf16 conversion
               float h2[2];
@@ -366,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
               for (int e = 0; e < 2; ++e) {
                 const int c = c4 + t + e;
                 const float own = __uint_as_float(gate_lane ? r[c] : r[16 + c]);
-                const float g = (gate_lane ? own : other[c]) * mv[t + e];
-                const float u = (gate_lane ? other[c] : own) * mv[t + e];
-                h2[e] = silu(g * a0) * (u * a1);
+                const float g = (gate_lane ? own : other[c]) * gv[t + e];
+                const float u = (gate_lane ? other[c] : own) * uv[t + e];
+                h2[e] = silu(g) * u;
               }
               const uint32_t hb = float2_to_bf16x2_bits(h2[0], h2[1]);
               const int n = c0 + cb + c4 + t;
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const int n = c0 + c4 + t;
-              if (n < it.rows) o32[(size_t)n * N] = __uint_as_float(r[c4 + t]) * mv[t] * a0;
+              if (n < it.rows) o32[(size_t)n * N] = __uint_as_float(r[c4 + t]) * mv[t];
             }
           }
         } else {
@@ -397,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
             const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
             for (int t = 0; t < 4; t += 2) {  // two tokens per bf16 conversion
-              const uint32_t yb = float2_to_bf16x2_bits(__uint_as_float(r[c4 + t]) * mv[t] * a0,
-                                                        __uint_as_float(r[c4 + t + 1]) * mv[t + 1] * a0);
+              const uint32_t yb = float2_to_bf16x2_bits(__uint_as_float(r[c4 + t]) * mv[t],
+                                                        __uint_as_float(r[c4 + t + 1]) * mv[t + 1]);
               const int n = c0 + c4 + t;
               uint16_t* o = p.out + (size_t)(it.row0 + n) * N + it.mt * kM + rho;
               if (n < it.rows) o[0] = (uint16_t)(yb & 0xffffu);
