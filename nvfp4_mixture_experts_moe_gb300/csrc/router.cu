@@ -8,13 +8,14 @@
 // The product is small next to the experts (E x H weights, T x E x H
 // multiply-adds: 2.6 MB and 10.7 GFLOP for E = 320, H = 4096 at 4096 tokens),
 // and two kernels cover it:
-// * few tokens (T <= 16): the weight rows stream from HBM once; one CTA per
-//   expert row, its four warps take a quarter of K each, every lane holds one
-//   fp32 sum per token (its chunks in a fixed order), and the partial sums
-//   are added in a fixed order (lanes by a shuffle tree, then warps 0..3).
-//   Measured at 8 tokens, E = 320, H = 4096: about 11 us per launch after an
-//   L2 flush, far from the 0.4 us the 2.7 MB would take at HBM speed; the
-//   kernel is latency-bound (sixteen warps per row measured no faster);
+// * few tokens (T <= 16): the weight rows stream from HBM once; two expert
+//   rows per CTA of eight warps, the threads striding over K in 16-byte
+//   chunks with every load of a round (both rows' weights, every token's x)
+//   issued before any is used, one fp32 sum per (row, token) per thread, and
+//   the partial sums added in a fixed order (lanes by a shuffle tree, then
+//   warps 0..7). The 2.7 MB at 8 tokens, E = 320, H = 4096 would take 0.4 us
+//   at HBM speed; a launch is bound by its latency (one CTA per row with
+//   four dependent rounds of x loads measured about 10 us);
 // * more tokens: tcgen05.mma (bf16 in, fp32 accumulate in TMEM) over
 //   128-expert x 128-token tiles, described below.
 // Both reduce in an order fixed by the shapes, so the logits are the same
@@ -34,8 +35,8 @@ using tc::smem_u32;
 // ---------------------------------------------------------------------------
 // Few tokens.
 constexpr int kGemvMaxT = 16;
-constexpr int kGemvWarps = 4;
-constexpr int kGemvBatch = 4;
+constexpr int kGemvWarps = 8;
+constexpr int kGemvRows = 2;   // expert rows per CTA
 
 __device__ __forceinline__ void bf16x8_to_float(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -46,65 +47,73 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& v, float (&f)[8]) {
   }
 }
 
+// MAXT tokens at most; BATCH 16-byte chunks of K per thread per round, whose
+// weight loads (HBM) and x loads (L2) for every row and token are all issued
+// before any is used, so a round costs one memory latency. Each thread keeps
+// one fp32 sum per (row, token) over its chunks in increasing order; lanes
+// are added by a shuffle tree, then warps 0..7 in order.
+template <int MAXT, int BATCH>
 __global__ void __launch_bounds__(kGemvWarps * 32) router_gemv_kernel(const uint16_t* __restrict__ x,
                                                                       const uint16_t* __restrict__ w, int T,
                                                                       int H, int E, float* __restrict__ logits) {
   pdl_wait();
-  const int e = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = H / 8;  // 16-byte chunks of a row
-  const int per = (C + kGemvWarps - 1) / kGemvWarps;
-  const int c0 = min(C, warp * per), c1 = min(C, c0 + per);
-  float acc[kGemvMaxT];
+  const int e0 = blockIdx.x * kGemvRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = H / 8;   // 16-byte chunks of a row
+  float acc[kGemvRows][MAXT];
 #pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.0f;
-  const uint4* wrow = reinterpret_cast<const uint4*>(w + (size_t)e * H);
-  // kGemvBatch chunks per lane per round: their weight loads (HBM) are issued
-  // together; then, chunk by chunk, the matching x chunks of every token (L2)
-  // are issued together before they are used, so a round costs one HBM
-  // latency plus one L2 latency per chunk instead of one per chunk and token
-  for (int cb = c0 + lane; cb < c1; cb += 32 * kGemvBatch) {
-    uint4 wv[kGemvBatch];
+  for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
-    for (int u = 0; u < kGemvBatch; ++u) {
-      const int c = cb + 32 * u;
-      wv[u] = c < c1 ? ldg_stream(wrow + c) : make_uint4(0, 0, 0, 0);
+    for (int t = 0; t < MAXT; ++t) acc[r][t] = 0.0f;
+  for (int cb = tid; cb < C; cb += kGemvWarps * 32 * BATCH) {
+    uint4 wv[kGemvRows][BATCH], xv[BATCH][MAXT];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int c = cb + kGemvWarps * 32 * u;
+#pragma unroll
+      for (int r = 0; r < kGemvRows; ++r)
+        wv[r][u] = (c < C && e0 + r < E) ? ldg_stream(reinterpret_cast<const uint4*>(w + (size_t)(e0 + r) * H) + c)
+                                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int t = 0; t < MAXT; ++t)
+        xv[u][t] = (c < C && t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c)
+                                    : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kGemvBatch; ++u) {
-      const int c = cb + 32 * u;
-      if (c >= c1) break;
-      uint4 xv[kGemvMaxT];
+    for (int u = 0; u < BATCH; ++u) {
 #pragma unroll
-      for (int t = 0; t < kGemvMaxT; ++t)
-        xv[t] = t < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c) : make_uint4(0, 0, 0, 0);
-      float wf[8];
-      bf16x8_to_float(wv[u], wf);
+      for (int r = 0; r < kGemvRows; ++r) {
+        float wf[8];
+        bf16x8_to_float(wv[r][u], wf);
 #pragma unroll
-      for (int t = 0; t < kGemvMaxT; ++t) {
-        if (t < T) {
+        for (int t = 0; t < MAXT; ++t) {
           float xf[8];
-          bf16x8_to_float(xv[t], xf);
+          bf16x8_to_float(xv[u][t], xf);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[t] = fmaf(xf[i], wf[i], acc[t]);
+          for (int i = 0; i < 8; ++i) acc[r][t] = fmaf(xf[i], wf[i], acc[r][t]);
         }
       }
     }
   }
-  __shared__ float part[kGemvWarps][kGemvMaxT];
+  __shared__ float part[kGemvWarps][kGemvRows][MAXT];
 #pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) {
-    float v = acc[t];
+  for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) part[warp][t] = v;
-  }
+    for (int t = 0; t < MAXT; ++t) {
+      float v = acc[r][t];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) part[warp][r][t] = v;
+    }
   __syncthreads();
-  if ((int)threadIdx.x < T) {
-    float v = part[0][threadIdx.x];
+  if (tid < kGemvRows * MAXT) {
+    const int r = tid / MAXT, t = tid % MAXT;
+    if (t < T && e0 + r < E) {
+      float v = part[0][r][t];
 #pragma unroll
-    for (int q = 1; q < kGemvWarps; ++q) v += part[q][threadIdx.x];
-    logits[(size_t)threadIdx.x * E + e] = v;
+      for (int q = 1; q < kGemvWarps; ++q) v += part[q][r][t];
+      logits[(size_t)t * E + e0 + r] = v;
+    }
   }
 }
 
@@ -258,7 +267,9 @@ moe_status launch_router_gemm_status(const uint16_t* x, const uint16_t* w, int T
   if (T == 0) return MOE_OK;
   cudaError_t e;
   if (T <= kGemvMaxT) {
-    e = launch_ex(pdl, router_gemv_kernel, dim3(E), dim3(kGemvWarps * 32), 0, s, x, w, T, H, E, logits);
+    const dim3 grid((E + kGemvRows - 1) / kGemvRows), block(kGemvWarps * 32);
+    e = T <= 8 ? launch_ex(pdl, router_gemv_kernel<8, 2>, grid, block, 0, s, x, w, T, H, E, logits)
+               : launch_ex(pdl, router_gemv_kernel<kGemvMaxT, 1>, grid, block, 0, s, x, w, T, H, E, logits);
   } else {
     const int ntiles = (T + kTcN - 1) / kTcN;
     if (ntiles > 65535) return MOE_ERR_UNSUPPORTED;
