@@ -112,6 +112,9 @@ struct ForwardWs {
   float* xgs;
   uint8_t* hq;        // W4A4: [rows, I/2]
   uint8_t* hsf;       // W4A4: [tiles, I/256, 2048]
+  uint8_t* xq_tok;    // W4A4: x quantised token by token: codes [T, H/2]
+  uint8_t* xsf_tok;   //   and scales [T, H/BLK] (BLK = 16 NVFP4, 32 MXFP4), before the per-tile assembly
+  uint8_t* hsf_lin;   // W4A4: h's scales row by row [rows, I/BLK] (its codes go straight to hq)
   int tiles;          // W4A4: bound on the 128-row tiles of all groups
   float* hgs;
   int* fused_region;        // kFusedRegionInts ints right after the header (every shape)
@@ -175,7 +178,12 @@ static ForwardWs carve_forward(const moe_layer_desc& L, void* ws) {
     f.hq = c.take<uint8_t>(rows * L.I / 2);
     f.hsf = c.take<uint8_t>((size_t)f.tiles * (L.I / 256) * sf_stage);
     f.hgs = c.take<float>(1);
+    const int blk = L.mode == MOE_MXFP4 ? 32 : 16;
+    f.xq_tok = c.take<uint8_t>((size_t)L.T * L.H / 2);
+    f.xsf_tok = c.take<uint8_t>((size_t)L.T * (L.H / blk));
+    f.hsf_lin = c.take<uint8_t>(rows * (L.I / blk));
   } else {
+    f.xq_tok = f.xsf_tok = f.hsf_lin = nullptr;
     f.xq = f.xsf = f.hq = f.hsf = nullptr;
     f.xgs = f.hgs = nullptr;
     f.tiles = 0;
@@ -593,7 +601,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   }
   stage_mark(2, s);
   const float x_static = L->x_global_scale, h_static = L->h_global_scale;
-  const size_t sf_stage = mx ? 1024 : 2048;  // scale-atom bytes per (tile, 256-wide K stage)
+
   if (fp4) {  // x -> FP4 in group order: W4A4 with a per-tensor scale (dynamic amax or static); MXFP4 per 32
     st = cuda_ok(cudaMemsetAsync(&f.hdr->amax[0], 0, 2 * sizeof(float), s));
     if (st != MOE_OK) return st;
@@ -601,9 +609,13 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
       st = launch_amax_bf16(x, (size_t)T * H, &f.hdr->amax[0], s, pdl);
       if (st != MOE_OK) return st;
     }
-    st = launch_quantize_tiles(x, T, H, f.inv_perm, k, has_shared ? 1 : -1, f.gofs, EL + (has_shared ? 1 : 0),
-                               &f.hdr->amax[0], f.xq, f.xsf, (size_t)f.tiles * (H / 256) * sf_stage, f.xgs,
-                               x_static, s, pdl, mx);
+    // token by token (coalesced codes and scales), then per 128-row tile:
+    // each token's codes to its grouped rows, the scale atoms assembled
+    st = mx ? launch_quantize_mx(x, T, H, f.xq_tok, f.xsf_tok, s)
+            : launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq_tok, f.xsf_tok, f.xgs, x_static, s, pdl);
+    if (st != MOE_OK) return st;
+    st = launch_tile_gather(f.xq_tok, f.xsf_tok, f.row_token, H, f.gofs, EL + (has_shared ? 1 : 0), f.tiles, f.xq,
+                            f.xsf, mx, s);
     if (st != MOE_OK) return st;
   }
   if (f.xf) {  // f16 copy of x, rows in group order, for the large-group tensor-core GEMM
@@ -641,8 +653,12 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
   if (st != MOE_OK) return st;
   stage_mark(4, s);
   if (fp4) {  // h -> FP4: NVFP4 with one global scale over all rows (amax from GEMM 1's epilogue); MXFP4 per 32
-    st = launch_quantize_tiles(f.h, rows, I, nullptr, 0, -1, f.gofs, G, &f.hdr->amax[1], f.hq, f.hsf,
-                               (size_t)f.tiles * (I / 256) * sf_stage, f.hgs, h_static, s, pdl, mx);
+    // row by row (h is in group order: the codes land in place), then the
+    // scale atoms per 128-row tile
+    st = mx ? launch_quantize_mx(f.h, rows, I, f.hq, f.hsf_lin, s)
+            : launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf_lin, f.hgs, h_static, s, pdl);
+    if (st != MOE_OK) return st;
+    st = launch_tile_gather(nullptr, f.hsf_lin, nullptr, I, f.gofs, G, f.tiles, nullptr, f.hsf, mx, s);
     if (st != MOE_OK) return st;
   } else if (f.hf) {
     st = launch_rows_to_f16(f.h, nullptr, rows, I, f.hf, f.hmul, s, pdl);

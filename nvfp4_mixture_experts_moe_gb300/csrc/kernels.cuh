@@ -129,23 +129,18 @@ moe_status launch_gemm_tc_w4a16(const GemmPlan& p, int rows_min, cudaStream_t s)
 // copy of the activation rows (a_f16, a_mul).
 moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
 
-// bf16 rows -> NVFP4 codes [rows, K/2] of the grouped layout and scale-factor
-// atoms per (128-row tile of a group, 256-wide K stage), zeroed first
-// (sf_bytes); gs = 2688 / amax as moe_nvfp4_quantize, or gs_static when it is
-// > 0. With `dest` (inverse
-// permutation, [src_rows * k]) token t's row goes to dest[t*k + j] (pairs with
-// dest -1 are skipped) and, with shared_base >= 0 (a flag), to row
-// gofs[G-1] + t of the shared group; without it source row r is row r.
-moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
-                                 int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
-                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, float gs_static,
-                                 cudaStream_t s, bool pdl = false, bool mx = false);
-
 // MXFP4: bf16 [rows, K] -> codes [rows, K/2] and E8M0 scales [rows, K/32]
-// (K % 32 == 0). With mx = true launch_quantize_tiles writes MXFP4 codes and
-// the E8M0 scale atoms of the kind::mxf4 GEMM (four 32-blocks per atom word;
-// amax, gs_out and gs_static are not used).
+// (K % 32 == 0).
 moe_status launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* q, uint8_t* sf, cudaStream_t s);
+// Per-tile assembly of the block-scaled GEMMs' activation codes (gathered
+// through src_row, or left in place when it is null) and scale atoms from
+// row-by-row quantised codes and scales; one CTA per 128-row tile of a group.
+// The atoms: per (tile, 256-wide K stage) four (NVFP4, E4M3 per 16) or two
+// (MXFP4, E8M0 per 32) 512-byte tcgen05 scale-factor atoms; rows past a
+// group's end carry scale 0.
+moe_status launch_tile_gather(const uint8_t* q_src, const uint8_t* sf_src, const int32_t* src_row, int K,
+                              const int32_t* gofs, int G, int tiles_max, uint8_t* q, uint8_t* sf_tiles, bool mx,
+                              cudaStream_t s);
 
 // bf16 rows -> f16 rows scaled by a power of two so that each row's largest
 // magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it. Row r of dst is
@@ -158,7 +153,7 @@ moe_status launch_gemm_tc_w4a4(const GemmPlan& p, cudaStream_t s);
 
 // W4A4 GEMM of the fused forward: activation codes in group order (a, a_rows
 // rows) loaded as tensor-map boxes, their scales as per-tile atoms (a_sf, from
-// launch_quantize_tiles), two CTAs per SM.
+// launch_tile_gather).
 moe_status launch_gemm_tc_fp4(const GemmPlan& p, cudaStream_t s);
 
 // Groups with at most this many rows take the small-group path.

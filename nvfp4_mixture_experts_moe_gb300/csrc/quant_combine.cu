@@ -228,166 +228,110 @@ moe_status launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* q, ui
 }
 
 // ---------------------------------------------------------------------------
-// Quantisation of the block-scaled GEMM's activation rows straight into the
-// layout its loaders copy. Row r of the grouped layout gets its codes at
-// q[r][K/2] (row-major, so 2-D tensor-map boxes of a group's rows are plain
-// tiles) and its E4M3 scales in the scale-factor atoms of its 128-row tile:
-// the tiles of group g are numbered from tile_base[g] = sum over g' < g of
-// ceil(rows(g') / 128), and tile t, 256-wide K stage ks, 64-wide step kk hold
-// one 512-byte atom at ((t * K/256 + ks) * 4 + kk) * 512 whose byte
-// m0 * 16 + m1 * 4 + j is scale j of tile row 32 * m1 + m0 (the layout
-// tcgen05.cp 32x128b.warpx4 moves into tensor memory). The atoms start zeroed
-// (tile rows past a group's end keep scale 0, so whatever codes a box brings
-// for them contribute nothing).
-//
-// One warp per source row, quantised once: with `dest` (the inverse
-// permutation, [rows_src * k]) the row of token t goes to dest[t*k + j] for
-// each j with a valid slot and, with `shared_base` >= 0 (a flag), to row
-// gofs[G-1] + t of the shared group (the last group); without it, source
-// row r is row r. A lane takes one
-// 16-block per round of 32 (coalesced loads and code stores; four lanes'
-// scales make one 4-byte atom word). The group offsets and the tile prefix
-// sit in shared memory. The arithmetic per 16-block is quantize_bf16_kernel's.
-constexpr int kQtWarps = 8;
-constexpr int kQtMaxDest = 33;
-
-__device__ __forceinline__ void quant_block16(const uint16_t* src, float gs, uint32_t& lo4, uint32_t& hi4,
-                                              uint32_t& code) {
-  const uint4 v0 = ldg_stream(reinterpret_cast<const uint4*>(src));
-  const uint4 v1 = ldg_stream(reinterpret_cast<const uint4*>(src) + 1);
-  const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  float f[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    f[2 * j] = __uint_as_float(wv[j] << 16);
-    f[2 * j + 1] = __uint_as_float(wv[j] & 0xffff0000u);
-  }
-  float bmax = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
-  const float sc = __fmul_rn(__fdiv_rn(bmax, 6.0f), gs);
-  code = e4m3_encode_sat(sc);
-  const float sval = e4m3_decode(code);
-  lo4 = hi4 = 0;
-  if (sval > 0.0f) {
-    const float rr = __fdiv_rn(gs, sval);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t b = e2m1x2_rn(__fmul_rn(f[2 * j], rr), __fmul_rn(f[2 * j + 1], rr));
-      if (j < 4) lo4 |= b << (8 * j);
-      else hi4 |= b << (8 * (j - 4));
-    }
-  }
-}
-
-template <bool MX>
-__global__ void __launch_bounds__(kQtWarps * 32) quantize_tiles_kernel(
-    const uint16_t* __restrict__ x, int src_rows, int K, const int32_t* __restrict__ dest, int k, int shared_base,
-    const int32_t* __restrict__ gofs, int G, const float* __restrict__ amax_p, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ sf_tiles, float* __restrict__ gs_out, float gs_static) {
+// Per-tile assembly of the block-scaled GEMMs' activation operands from rows
+// quantised one by one (quantize_bf16_kernel / quantize_mx_bf16_kernel:
+// codes [src_rows, K/2], scales [src_rows, K/BLK]). One CTA per 128-row tile
+// of a group (tiles numbered group by group, ceil(rows_g / 128) each):
+// * with `src_row` (the grouped row's source row: x's token), each tile row's
+//   codes are copied from its source row — a token's codes reach its k+1
+//   grouped rows; without it the codes are already in place (h, quantised in
+//   group order) and only the scales move;
+// * the tile's scale atoms (the tcgen05 scale-factor layout: one 512-byte
+//   atom per four consecutive blocks, row m's 4 bytes at (m % 32) * 16 +
+//   (m / 32) * 4) are assembled in shared memory, rows past the group's end
+//   left 0, and written out whole, 16 bytes per thread.
+// So the scattered 4-byte writes of a token-major pass become coalesced ones.
+template <int BLK>
+__global__ void __launch_bounds__(256) tile_gather_kernel(const uint8_t* __restrict__ q_src,
+                                                          const uint8_t* __restrict__ sf_src,
+                                                          const int32_t* __restrict__ src_row, int K,
+                                                          const int32_t* __restrict__ gofs, int G,
+                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf_tiles) {
   pdl_wait();
-  extern __shared__ int smem_i[];
-  int* s_gofs = smem_i;               // [G + 1] group offsets
-  int* tile_base = smem_i + (G + 1);  // [G + 1] first tile of each group
-  for (int g = threadIdx.x; g <= G; g += blockDim.x) s_gofs[g] = gofs[g];
-  __syncthreads();
-  if (threadIdx.x < 32) {  // exclusive prefix of ceil(rows / 128) over the groups
+  extern __shared__ __align__(16) uint8_t smem_tg[];
+  const int atoms = K / (4 * BLK), NB = K / BLK, W = NB / 4;   // atoms per tile; scale bytes and words per row
+  uint8_t* at = smem_tg;                                                   // [atoms * 512]
+  int* s_tb = reinterpret_cast<int*>(smem_tg + (size_t)atoms * 512);     // [G + 1] first tile of each group
+  const int tid = threadIdx.x;
+  if (tid < 32) {  // exclusive prefix of ceil(rows / 128) over the groups
     int carry = 0;
     for (int g0 = 0; g0 <= G; g0 += 32) {
-      const int g = g0 + (int)threadIdx.x;
-      const int v = g < G ? (s_gofs[g + 1] - s_gofs[g] + 127) / 128 : 0;
+      const int g = g0 + tid;
+      const int v = g < G ? (__ldg(gofs + g + 1) - __ldg(gofs + g) + 127) / 128 : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if ((int)threadIdx.x >= o) incl += t;
+        if (tid >= o) incl += t;
       }
-      if (g <= G) tile_base[g] = carry + incl - v;
+      if (g <= G) s_tb[g] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  for (int i = tid; i < atoms * 32; i += 256) reinterpret_cast<uint4*>(at)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  const float gs = MX ? 1.0f : global_scale_of(amax_p, gs_static);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && gs_out != nullptr) *gs_out = gs;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kQtWarps + (threadIdx.x >> 5);
-  if (row >= src_rows) return;
-  // destinations of this source row: lane d < ndest holds (row r, tile t, tile row m)
-  const int ndest = dest ? k + (shared_base >= 0 ? 1 : 0) : 1;
-  int my_r = -1, my_t = 0, my_m = 0;
-  if (lane < ndest) {
-    // the shared group (the last one) starts right after the routed rows that were kept
-    my_r = dest ? (lane < k ? dest[(size_t)row * k + lane] : s_gofs[G - 1] + row) : row;
-    if (my_r >= 0) {
-      int lo = 0, hi = G - 1;  // group of row my_r: the last g with gofs[g] <= my_r
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_gofs[mid] <= my_r) lo = mid; else hi = mid - 1;
-      }
-      const int local = my_r - s_gofs[lo];
-      my_t = tile_base[lo] + local / 128;
-      my_m = local % 128;
+  const int t = blockIdx.x;
+  if (t >= s_tb[G]) return;   // past the tiles this routing has (the grid is an upper bound)
+  int lo = 0, hi = G - 1;     // group of tile t: the last g with s_tb[g] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tb[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int row0 = __ldg(gofs + lo) + (t - s_tb[lo]) * 128;
+  const int nrows = min(128, __ldg(gofs + lo + 1) - row0);
+  // scales: thread (row m, four words of it); consecutive threads take
+  // consecutive rows, so their shared-memory words are 16 bytes apart
+  const int W4 = (W + 3) / 4;
+  for (int i = tid; i < 128 * W4; i += 256) {
+    const int m = i & 127, c = i >> 7;
+    if (m >= nrows) continue;
+    const int src = src_row ? __ldg(src_row + row0 + m) : row0 + m;
+    const uint8_t* rowp = sf_src + (size_t)src * NB;
+    const int w0 = 4 * c;
+    uint32_t wv[4];
+    if (w0 + 4 <= W && (NB & 15) == 0) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(rowp) + c);
+      wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) wv[e] = w0 + e < W ? __ldg(reinterpret_cast<const uint32_t*>(rowp) + w0 + e) : 0u;
+    }
+    const int off = (m & 31) * 16 + (m >> 5) * 4;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (w0 + e < W) *reinterpret_cast<uint32_t*>(at + (size_t)(w0 + e) * 512 + off) = wv[e];
+  }
+  // codes: a warp per row, 16 bytes per lane
+  if (src_row != nullptr) {
+    const int n16 = K / 32;   // 16-byte pieces of a row's codes
+    for (int m = tid >> 5; m < nrows; m += 8) {
+      const uint4* from = reinterpret_cast<const uint4*>(q_src + (size_t)__ldg(src_row + row0 + m) * (K / 2));
+      uint4* to = reinterpret_cast<uint4*>(q + (size_t)(row0 + m) * (K / 2));
+      for (int j = tid & 31; j < n16; j += 32) to[j] = __ldg(from + j);   // read by up to k+1 tiles: keep in L2
     }
   }
-  // blocks of 16 (NVFP4) or 32 (MXFP4) elements; a scale atom holds four
-  // consecutive blocks' scales of 128 rows: one K=64 MMA (NVFP4) or two (MXFP4)
-  constexpr int BLK = MX ? 32 : 16;
-  const int NB = K / BLK, atoms_per_tile = K / (4 * BLK);
-  const uint16_t* src = x + (size_t)row * K;
-  // 32 consecutive blocks per round, one per lane: the warp's loads and code
-  // stores are contiguous; the four scales of lanes 4i..4i+3 (one 4-byte word
-  // of a scale atom) are gathered into lane 4i, which stores it
-#pragma unroll 2
-  for (int kb0 = 0; kb0 < NB; kb0 += 32) {
-    const int kb = kb0 + lane;
-    const bool valid = kb < NB;
-    uint32_t code = 0;
-    uint4 c4 = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) {
-      if (MX) {
-        quant_block32_mx(src + (size_t)kb * 32, c4, code);
-      } else {
-        quant_block16(src + (size_t)kb * 16, gs, c4.x, c4.y, code);
-      }
-    }
-    uint32_t sw = code << (8 * (lane & 3));
-    sw |= __shfl_xor_sync(0xffffffffu, sw, 1);
-    sw |= __shfl_xor_sync(0xffffffffu, sw, 2);
-    for (int d = 0; d < ndest; ++d) {
-      const int r = __shfl_sync(0xffffffffu, my_r, d);
-      const int t = __shfl_sync(0xffffffffu, my_t, d);
-      const int m = __shfl_sync(0xffffffffu, my_m, d);
-      if (r < 0 || !valid) continue;
-      if (MX)
-        *reinterpret_cast<uint4*>(q + (size_t)r * (K / 2) + (size_t)kb * 16) = c4;
-      else
-        *reinterpret_cast<uint2*>(q + (size_t)r * (K / 2) + (size_t)kb * 8) = make_uint2(c4.x, c4.y);
-      if ((lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(sf_tiles + ((size_t)t * atoms_per_tile + (kb >> 2)) * 512 + (m & 31) * 16 +
-                                     (m >> 5) * 4) = sw;
-    }
-  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(sf_tiles + (size_t)t * atoms * 512);
+  for (int i = tid; i < atoms * 32; i += 256) dst[i] = reinterpret_cast<const uint4*>(at)[i];
 }
 
-moe_status launch_quantize_tiles(const uint16_t* x, int src_rows, int K, const int32_t* dest, int k,
-                                 int shared_base, const int32_t* gofs, int G, const float* amax, uint8_t* q,
-                                 uint8_t* sf_tiles, size_t sf_bytes, float* gs_out, float gs_static,
-                                 cudaStream_t s, bool pdl, bool mx) {
-  if (K % 256 || G <= 0 || (dest && k + 1 > kQtMaxDest)) return MOE_ERR_UNSUPPORTED;
-  if (src_rows == 0) return MOE_OK;
-  moe_status st = cuda_ok(cudaMemsetAsync(sf_tiles, 0, sf_bytes, s));
-  if (st != MOE_OK) return st;
-  const int blocks = (src_rows + kQtWarps - 1) / kQtWarps;
-  const size_t smem = (size_t)2 * (G + 1) * sizeof(int);
-  // after the memset the kernel is an ordinary stream successor (no programmatic launch)
-  (void)pdl;
-  cudaError_t e = launch_ex(false, mx ? quantize_tiles_kernel<true> : quantize_tiles_kernel<false>, dim3(blocks),
-                            dim3(kQtWarps * 32), smem, s, x, src_rows, K,
-                            dest, k, shared_base, gofs, G, amax, q, sf_tiles, gs_out, gs_static);
+moe_status launch_tile_gather(const uint8_t* q_src, const uint8_t* sf_src, const int32_t* src_row, int K,
+                              const int32_t* gofs, int G, int tiles_max, uint8_t* q, uint8_t* sf_tiles, bool mx,
+                              cudaStream_t s) {
+  if (K % 256 || G <= 0) return MOE_ERR_UNSUPPORTED;
+  if (tiles_max <= 0) return MOE_OK;
+  const int atoms = K / (4 * (mx ? 32 : 16));
+  const size_t smem = (size_t)atoms * 512 + (size_t)(G + 1) * sizeof(int);
+  if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+  auto k = mx ? tile_gather_kernel<32> : tile_gather_kernel<16>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_ok(e);
+  e = launch_ex(false, k, dim3(tiles_max), dim3(256), smem, s, q_src, sf_src, src_row, K, gofs, G, q, sf_tiles);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
 }
+
 
 // ---------------------------------------------------------------------------
 // Re-rounding E4M3 block scales by a global-scale ratio (checkpoint import,

@@ -47,7 +47,7 @@ def test_w4a4_small_layer_full_check():
 
 
 # skewed routing at a small size: empty groups, groups of several 128-row
-# tiles and ragged last tiles through the fused forward's tile quantiser and
+# tiles and ragged last tiles through the fused forward's per-tile operand assembly and
 # its block-scaled GEMMs
 GROUPS = si.LayerConfig("w4a4_groups", T=300, H=512, I=256, I_s=256, E=24, k=4, mode="w4a4", logits="zipf")
 
