@@ -293,8 +293,8 @@ def build_layer(cfg, dev):
     import torch
 
     import synthetic_inputs as si
-    from nvfp4_mixture_experts_moe_gb300 import MOE_W4A4, MOE_W4A16, Nvfp4MoeLayer
-    mode = MOE_W4A4 if cfg.mode == "w4a4" else MOE_W4A16
+    from nvfp4_mixture_experts_moe_gb300 import MOE_MXFP4, MOE_W4A4, MOE_W4A16, Nvfp4MoeLayer
+    mode = {"w4a4": MOE_W4A4, "mxfp4": MOE_MXFP4}.get(cfg.mode, MOE_W4A16)
     layer = Nvfp4MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mode=mode, I_shared=cfg.I_s, device=dev)
     for e0 in range(0, cfg.E + 1, 32):
         W = si.make_layer_weights(cfg, experts=list(range(e0, min(cfg.E + 1, e0 + 32))), threads=16)
