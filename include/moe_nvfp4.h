@@ -29,7 +29,12 @@
  *    before anything is enqueued. Anomalies only visible on the device
  *    (an expert id out of range, say) set an error word inside the
  *    workspace; moe_get_device_status() reads it. A workspace's first 256
- *    bytes must be zero before its first use; the library keeps them so.
+ *    bytes must be zero before its first use; afterwards the library
+ *    maintains them (the status word, scale slots and the single-kernel
+ *    decode path's launch ticket and flags), so they need not be cleared
+ *    again, and the rest of a workspace needs no initialisation. A
+ *    workspace serves one call at a time: calls that may run at the same
+ *    time (on different streams, say) need different workspaces.
  *  - Only sm_103 devices are supported; anything else returns
  *    MOE_ERR_UNSUPPORTED. No call traps or aborts the process.
  *  - Matrices are row-major with the contraction dimension K contiguous.
