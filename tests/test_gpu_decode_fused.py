@@ -165,3 +165,34 @@ def test_fused_counters_survive_workspace_reuse():
     assert B().moe_get_device_status(ws) == 0
     for name, o in (("first", first), ("again", again), ("after_big", after_big), ("after_permute", after_permute)):
         assert torch.equal(o, ref), name
+
+
+def test_fused_counter_sets_alternate_across_shapes_and_graph_replays():
+    """Launches alternate between the workspace's two counter sets (a ticket
+    per launch): decode batches of different sizes interleaved on one
+    workspace, and one forward captured in a CUDA graph and replayed (every
+    replay takes new tickets), each give the bits of a forward on a fresh
+    workspace."""
+    cfg, layer = device_layer("decode")
+    xs = {T: si.make_x(cfg.with_tokens(T)).cuda() for T in (1, 2, 5, 8)}
+    ls = {T: si.make_logits(cfg.with_tokens(T)).cuda() for T in (1, 2, 5, 8)}
+    ref = {T: layer.forward(xs[T], ls[T]).clone() for T in xs}   # fresh workspaces
+    ws = layer.workspace(8)
+    for T in (8, 2, 8, 5, 8, 1, 8, 8, 2):
+        got = layer.forward(xs[T], ls[T], ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref[T]), T
+    out = torch.empty_like(ref[8])
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        layer.forward(xs[8], ls[8], out=out, ws=ws)      # warm-up on the capture stream
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        layer.forward(xs[8], ls[8], out=out, ws=ws, stream=stream)
+    for _ in range(5):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[8])
+    assert B().moe_get_device_status(ws) == 0
