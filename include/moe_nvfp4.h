@@ -444,6 +444,10 @@ unsigned long long moe_kernel_launches(void);
  *   issuer); a GEMM whose N is not a multiple of 256 takes 3 instead of 4 or
  *   5; 0 keeps the library's choice for that GEMM. Results agree to the last bit
  *   across shapes. Used to compare them.
+ * MOE_DEBUG_F16_TILE (default 0): 1 = the W4A16 tensor-core GEMMs compute
+ *   every group above the small-group limit in tiles of 128 token rows (two
+ *   CTAs per SM); 0 = groups of more than 128 rows in tiles of 256 (one CTA
+ *   per SM). Results agree to the last bit across the two. Used to compare them.
  * Errors: an unknown key, or a value out of range -> MOE_ERR_INVALID_ARG.
  */
 typedef enum {
@@ -451,7 +455,8 @@ typedef enum {
   MOE_DEBUG_EXTRA_ARRIVALS = 2,
   MOE_DEBUG_DISABLE_DECODE_FUSED = 3,
   MOE_DEBUG_DECODE_STAGE_KB = 4,
-  MOE_DEBUG_FP4_TILE = 5
+  MOE_DEBUG_FP4_TILE = 5,
+  MOE_DEBUG_F16_TILE = 6
 } moe_debug_key;
 moe_status moe_debug_set(int key, long long value);
 

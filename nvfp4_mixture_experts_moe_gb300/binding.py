@@ -22,6 +22,7 @@ MOE_W4A16, MOE_W4A4, MOE_MXFP4 = 0, 1, 2
 MOE_SCALE_QUANT, MOE_SCALE_DEQUANT = 0, 1
 MOE_DEBUG_WAIT_LIMIT, MOE_DEBUG_EXTRA_ARRIVALS, MOE_DEBUG_DISABLE_DECODE_FUSED, MOE_DEBUG_DECODE_STAGE_KB = 1, 2, 3, 4
 MOE_DEBUG_FP4_TILE = 5
+MOE_DEBUG_F16_TILE = 6
 
 _lib = None
 

@@ -3,6 +3,7 @@
 // of every call are in include/moe_nvfp4.h.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -22,12 +23,14 @@ static std::atomic<int> g_fused_disabled{0};
 constexpr int kDefaultDecodeStageKb = 8;
 static std::atomic<int> g_decode_stage_kb{kDefaultDecodeStageKb};
 static std::atomic<int> g_fp4_tile{0};
+static std::atomic<int> g_f16_tile{0};
 
 
 long long debug_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 int debug_extra_arrivals() { return g_extra_arrivals.load(std::memory_order_relaxed); }
 bool debug_decode_fused_disabled() { return g_fused_disabled.load(std::memory_order_relaxed) != 0; }
 int decode_stage_kb() { return g_decode_stage_kb.load(std::memory_order_relaxed); }
+bool debug_f16_narrow_only() { return g_f16_tile.load(std::memory_order_relaxed) == 1; }
 int debug_fp4_tile(bool gate_up) {
   const int v = g_fp4_tile.load(std::memory_order_relaxed);
   return gate_up ? v / 10 : v % 10;
@@ -440,7 +443,14 @@ static moe_status run_gemm(const GemmPlan& p, long long max_group_rows, cudaStre
   if (p.mode == MOE_W4A4) return launch_gemm_tc_w4a4(p, s);
   moe_status st = launch_gemm_small_w4a16(p, kSmallGroupRows, s);
   if (st != MOE_OK || max_group_rows <= kSmallGroupRows) return st;
-  if (p.a_f16 != nullptr) return launch_gemm_tc_f16(p, kSmallGroupRows, s);
+  if (p.a_f16 != nullptr) {
+    // groups of up to 128 rows in 128-row tiles, larger ones in 256-row tiles
+    const bool wide = !debug_f16_narrow_only() && gemm_tc_f16_wide_fits(p.num_groups);
+    const int narrow_max = wide ? kWideGroupRows : INT_MAX;
+    st = launch_gemm_tc_f16(p, kSmallGroupRows, narrow_max, false, s);
+    if (st != MOE_OK || !wide || max_group_rows <= kWideGroupRows) return st;
+    return launch_gemm_tc_f16(p, kWideGroupRows, INT_MAX, true, s);
+  }
   return launch_gemm_tc_w4a16(p, kSmallGroupRows, s);
 }
 
@@ -727,6 +737,10 @@ moe_status moe_debug_set(int key, long long value) {
     case MOE_DEBUG_FP4_TILE:
       if (value < 0 || value > 55 || value % 10 > 5) return MOE_ERR_INVALID_ARG;
       g_fp4_tile.store((int)value, std::memory_order_relaxed);
+      return MOE_OK;
+    case MOE_DEBUG_F16_TILE:
+      if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+      g_f16_tile.store((int)value, std::memory_order_relaxed);
       return MOE_OK;
 
   }

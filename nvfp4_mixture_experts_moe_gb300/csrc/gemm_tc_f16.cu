@@ -32,8 +32,8 @@
 //   activation row's 2^-s (the f16 copy's power-of-two scale), alpha and the
 //   routing weight (GEMM 2) or apply SwiGLU (GEMM 1), and store bf16.
 //
-// Two CTAs share an SM (kCtasPerSm). TMEM per CTA: one accumulator of 128
-// columns and two A stages of 64 columns. Every wait is bounded; on a timeout the kernel records
+// Two tile shapes (F16Shape below): 128 token rows, two CTAs per SM, or 256
+// token rows, one CTA per SM. Every wait is bounded; on a timeout the kernel records
 // MOE_ERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -53,15 +53,32 @@ constexpr int kM = 128;
 constexpr int kBK = 128;                     // K per stage
 constexpr int kHalf = 64;                    // K per box / per 128-byte swizzled row
 constexpr int kRowBytes = 128;
-// Two CTAs per SM: one thread issues a CTA's MMAs and each stage costs that
-// thread a few hundred cycles of barrier and commit latency in which its
-// tensor core would idle; two independent issuers keep it fed, and while one
-// CTA drains its accumulator in the epilogue the other one's MMAs run.
-constexpr int kCtasPerSm = 2;
-constexpr int kStages = 2;                   // activation tiles and TMEM A stages
-constexpr int kRawSlots = 4;                 // raw weight stages
-constexpr int kTmemCols = 256;               // per CTA
-constexpr int kMaxBN = 128;
+// Two tile shapes.
+// Narrow (groups of up to 128 rows): up to 128 token rows per tile, two CTAs
+//   per SM, two stages of activation tiles and TMEM A columns, four raw weight
+//   slots. One thread issues a CTA's MMAs and each stage costs that thread a
+//   few hundred cycles of barrier and commit latency in which its tensor core
+//   would idle; two independent issuers keep it fed, and while one CTA drains
+//   its accumulator in the epilogue the other one's MMAs run.
+// Wide (groups of more than 128 rows): up to 256 token rows per tile (one
+//   N = 256 MMA per K step, so each dequantised weight tile serves twice the
+//   tokens), one CTA per SM, three stages, two raw weight slots (one per
+//   dequant set).
+// TMEM: the accumulator in columns [0, kBN), the A stages of 64 columns after it.
+template <bool WIDE>
+struct F16Shape {
+  static constexpr int kBN = WIDE ? 256 : 128;
+  static constexpr int kCtas = WIDE ? 1 : 2;
+  static constexpr int kTmemCols = WIDE ? 512 : 256;
+  static constexpr uint32_t kAcol0 = kBN;
+  static constexpr int kBHalf = kBN * 128;   // one 64-wide K half of the activation tile (128-byte rows)
+  static constexpr int kBStage = 2 * kBHalf;
+  static constexpr int kStages = WIDE ? 3 : 2;
+  static constexpr int kRawSlots = WIDE ? 2 : 4;
+  static_assert(kAcol0 + 64 * kStages <= kTmemCols, "TMEM columns");
+  static_assert(kRawSlots % 2 == 0, "each dequant set owns whole raw slots");
+};
+constexpr int kStagesMax = 3, kRawSlotsMax = 4;
 // Warp roles. The epilogue warps are the oldest: the schedulers favour them
 // over the ALU-heavy dequant warps, so an accumulator drains quickly.
 constexpr int kEpiWarp0 = 0;                 // warps 0..3
@@ -70,12 +87,8 @@ constexpr int kWLoadWarp = 5;
 constexpr int kBLoadWarp = 6;
 constexpr int kDeqWarp0 = 7;                 // warps 7..14: two dequant sets
 constexpr int kThreads = (kDeqWarp0 + 8) * 32;
-constexpr int kBHalf = kMaxBN * kRowBytes;   // 16 KB: one K half of the activation tile
-constexpr int kBStage = 2 * kBHalf;
 constexpr int kRawStage = 2 * kW16Chunk;     // two (128-row, 64-K) chunks
-constexpr uint32_t kAcol0 = 128;             // accumulator: columns [0, 128); A stages from 128
 constexpr long long kWaitLimit = 4ll * 1000 * 1000 * 1000;
-static_assert(kAcol0 + 64 * kStages <= kTmemCols, "TMEM columns");
 
 // Tensor maps over the f16 activation matrix with boxes of 16, 32, 64 and
 // 128 rows (64 columns each).
@@ -93,22 +106,24 @@ struct Args {
   const float* row_scale;
   uint16_t* out;
   float* out_last_f32;
-  int rows_min;
+  int rows_min, rows_max;   // the groups this launch computes: rows_min < rows <= rows_max
   int* status;
   long long wait_limit;      // cycles per bounded wait (a timeout aborts the kernel)
 };
 
+template <int BN>
 struct Smem {
-  uint64_t w_full[kRawSlots];   // raw weights of the stage landed
-  uint64_t w_empty[kRawSlots];  // the dequant set is done reading them
-  uint64_t bfull[kStages];      // activation rows of the stage landed
-  uint64_t ready[kStages];      // the four dequant warps wrote the stage's A columns
-  uint64_t empty[kStages];      // the stage's MMAs completed (activation tile and TMEM A free)
+  uint64_t w_full[kRawSlotsMax];   // raw weights of the stage landed
+  uint64_t w_empty[kRawSlotsMax];  // the dequant set is done reading them
+  uint64_t bfull[kStagesMax];      // activation rows of the stage landed
+  uint64_t ready[kStagesMax];      // the four dequant warps wrote the stage's A columns
+  uint64_t empty[kStagesMax];      // the stage's MMAs completed (activation tile and TMEM A free)
   uint64_t tfull;
   uint64_t tempty;
-  float rowmul[4][kMaxBN];      // epilogue: per-row factors of the tile, one copy per epilogue warp
-                                // (gate/up: 2^-s * alpha_gate; down: 2^-s * routing weight * alpha)
-  float rowmul_up[4][kMaxBN];   // gate/up: 2^-s * alpha_up
+  // epilogue: per-row factors of the tile, one copy per epilogue warp, read
+  // as float4 (gate/up: 2^-s * alpha_gate; down: 2^-s * routing weight * alpha)
+  alignas(16) float rowmul[4][BN];
+  alignas(16) float rowmul_up[4][BN];   // gate/up: 2^-s * alpha_up
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -118,7 +133,7 @@ struct Item {
   int g, row0, rows, bn, mt;
 };
 
-__device__ __forceinline__ Item decode_item(int idx, const int* pref, int G, int MT, const int32_t* off) {
+__device__ __forceinline__ Item decode_item(int idx, const int* pref, int G, int MT, const int32_t* off, int BN) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -130,8 +145,8 @@ __device__ __forceinline__ Item decode_item(int idx, const int* pref, int G, int
   const int nt = local / MT;
   it.mt = local % MT;
   const int grows = off[lo + 1] - off[lo];
-  it.row0 = off[lo] + nt * kMaxBN;
-  it.rows = min(kMaxBN, grows - nt * kMaxBN);
+  it.row0 = off[lo] + nt * BN;
+  it.rows = min(BN, grows - nt * BN);
   it.bn = (it.rows + 15) & ~15;
   return it;
 }
@@ -147,8 +162,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const __grid_constant__ BoxMaps maps, Args p) {
+template <bool GATE_UP, bool WIDE>
+__global__ void __launch_bounds__(kThreads, F16Shape<WIDE>::kCtas)
+    gemm_tc_f16_kernel(const __grid_constant__ BoxMaps maps, Args p) {
+  using Sh = F16Shape<WIDE>;
+  constexpr int kBN = Sh::kBN, kBHalf = Sh::kBHalf, kBStage = Sh::kBStage, kTmemCols = Sh::kTmemCols;
+  constexpr int kStages = Sh::kStages, kRawSlots = Sh::kRawSlots;
+  constexpr uint32_t kAcol0 = Sh::kAcol0;
+  using Smem = ::moe::Smem<kBN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* b_tiles = base;                               // kStages x 32 KB
@@ -165,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
 
   for (int g = tid; g < G; g += kThreads) {
     const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
-    pref[g + 1] = rows > p.rows_min ? ((rows + kMaxBN - 1) / kMaxBN) * MT : 0;
+    pref[g + 1] = rows > p.rows_min && rows <= p.rows_max ? ((rows + kBN - 1) / kBN) * MT : 0;
   }
   if (tid == 0) {
     pref[0] = 0;
@@ -212,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
     if (lane == 0) {
       int j = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-        const Item it = decode_item(item, pref, G, MT, p.group_offsets);
+        const Item it = decode_item(item, pref, G, MT, p.group_offsets, kBN);
         const uint8_t* wdata = weight_block(p, it.g) + sizeof(PrepHeader);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
@@ -234,9 +255,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
     if (lane == 0) {
       int j = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-        const Item it = decode_item(item, pref, G, MT, p.group_offsets);
-        const int q = 32 - __clz((it.bn >> 4) - 1);   // box of 16 << q >= bn rows
-        const uint32_t half_bytes = (uint32_t)((16 << q) * kRowBytes);
+        const Item it = decode_item(item, pref, G, MT, p.group_offsets, kBN);
+        // one box of 16 << q >= bn rows, or two boxes of 128 rows for bn > 128
+        const int nbox = it.bn > 128 ? 2 : 1;
+        const int q = nbox == 2 ? 3 : 32 - __clz((it.bn >> 4) - 1);
+        const uint32_t half_bytes = (uint32_t)(nbox * (16 << q) * kRowBytes);
         bool ok = true;
         for (int ks = 0; ks < KS; ++ks, ++j) {
           const int slot = j % kStages;
@@ -245,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
           mbar_arrive_expect_tx(&sm->bfull[slot], nh * half_bytes);
           const uint32_t dst = smem_u32(b_tiles + slot * kBStage);
           for (int h = 0; h < nh; ++h)
-            tma_load_2d(dst + h * kBHalf, &maps.m[q], (2 * ks + h) * kHalf, it.row0, &sm->bfull[slot]);
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d(dst + h * kBHalf + bx * 128 * kRowBytes, &maps.m[q], (2 * ks + h) * kHalf,
+                          it.row0 + 128 * bx, &sm->bfull[slot]);
         }
         if (!ok) break;
       }
@@ -277,14 +302,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
         }
         tc_fence_after();
         const int nh = min(2, KB64 - 2 * ks);
+        // Releasing the raw slot. Its refill is a bulk copy, an async-proxy
+        // write, and the reads here are generic loads: a load still in flight
+        // when the slot is released could see the refill's bytes. The narrow
+        // shape (two slots per set) releases the slot after the TMEM stores
+        // have consumed the loaded words, so no read is in flight. The
+        // wide shape (one slot per set) reads both halves up front and
+        // releases at once, so that the refill overlaps the conversion; the
+        // proxy fence orders those reads before the refill. (Without it the
+        // wide shape computed a few wrong weight rows in some launches.)
+        uint4 pwa[2], pwb[2];
+        uint2 psc[2];
+        if (WIDE) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h < nh) {
+              const uint8_t* rs = raw + rslot * kRawStage + h * kW16Chunk;
+              pwa[h] = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16);
+              pwb[h] = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16 + 16);
+              psc[h] = *reinterpret_cast<const uint2*>(rs + kW16SfOff + blk * 64 + g8 * 8);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->w_empty[rslot]);
+        }
         for (int h = 0; h < nh; ++h) {
-          const uint8_t* rs = raw + rslot * kRawStage + h * kW16Chunk;
-          const uint4 wa4 = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16);
-          const uint4 wb4 = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16 + 16);
-          const uint2 sc = *reinterpret_cast<const uint2*>(rs + kW16SfOff + blk * 64 + g8 * 8);
-          if (h == nh - 1) {  // raw slot read completely
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm->w_empty[rslot]);
+          uint4 wa4, wb4;
+          uint2 sc;
+          if (WIDE) {
+            wa4 = h ? pwa[1] : pwa[0];
+            wb4 = h ? pwb[1] : pwb[0];
+            sc = h ? psc[1] : psc[0];
+          } else {
+            const uint8_t* rs = raw + rslot * kRawStage + h * kW16Chunk;
+            wa4 = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16);
+            wb4 = *reinterpret_cast<const uint4*>(rs + blk * 512 + (4 * g8 + 2 * hi) * 16 + 16);
+            sc = *reinterpret_cast<const uint2*>(rs + kW16SfOff + blk * 64 + g8 * 8);
           }
           const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
           const uint32_t wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
@@ -312,7 +366,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->ready[slot]);
+        if (lane == 0) {
+          // narrow: the TMEM stores above (asm statements, kept in order with
+          // the arrive) consumed every word loaded from the slot
+          if (!WIDE) mbar_arrive(&sm->w_empty[rslot]);
+          mbar_arrive(&sm->ready[slot]);
+        }
       }
       if (!ok) break;
     }
@@ -323,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
     const int row_last0 = p.out_last_f32 != nullptr ? p.group_offsets[G - 1] : 0;   // first shared row
     int itc = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++itc) {
-      const Item it = decode_item(item, pref, G, MT, p.group_offsets);
+      const Item it = decode_item(item, pref, G, MT, p.group_offsets, kBN);
       // per-row factors of the tile, alpha folded in, into this warp's shared
       // copy (no cross-warp sync)
       const PrepHeader* hdr = reinterpret_cast<const PrepHeader*>(weight_block(p, it.g));
@@ -332,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
       float* rowmul_up = sm->rowmul_up[q];
       __syncwarp();  // done reading the previous item's factors
 #pragma unroll
-      for (int i = 0; i < kMaxBN / 32; ++i) {
+      for (int i = 0; i < kBN / 32; ++i) {
         const int n = 32 * i + lane;
         float m = 0.0f;
         if (n < it.rows) {
@@ -422,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_tc_f16_kernel(const
       const uint64_t bdesc0 = smem_desc(smem_u32(b_tiles), 16, 1024, kSwizzle128B);  // + 2 per 32-byte K step
       int j = 0, itc = 0;
       for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x, ++itc) {
-        const Item it = decode_item(item, pref, G, MT, p.group_offsets);
+        const Item it = decode_item(item, pref, G, MT, p.group_offsets, kBN);
         if (!mbar_wait(&sm->tempty, (itc & 1) ^ 1, abort, p.wait_limit)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(kM, it.bn, 0);
@@ -478,11 +537,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 
 }  // namespace
 
+template <bool WIDE>
 static size_t smem_bytes(int G) {
-  return 1024 + (size_t)kStages * kBStage + (size_t)kRawSlots * kRawStage + sizeof(Smem) + (size_t)(G + 1) * 4;
+  using Sh = F16Shape<WIDE>;
+  return 1024 + (size_t)Sh::kStages * Sh::kBStage + (size_t)Sh::kRawSlots * kRawStage +
+         sizeof(Smem<Sh::kBN>) + (size_t)(G + 1) * 4;
 }
 
-moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) {
+bool gemm_tc_f16_wide_fits(int num_groups) { return smem_bytes<true>(num_groups) <= 227 * 1024; }
+
+moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, int rows_max, bool wide, cudaStream_t s) {
   if (pl.num_groups <= 0) return MOE_OK;
   if (pl.a_f16 == nullptr || pl.a_mul == nullptr || pl.a_rows <= 0) return MOE_ERR_INVALID_ARG;
   auto encode = encode_tiled();
@@ -512,16 +576,19 @@ moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, cudaStream_t s) 
   a.out = pl.out;
   a.out_last_f32 = pl.out_last_f32;
   a.rows_min = rows_min;
+  a.rows_max = rows_max;
   a.status = pl.status;
   a.wait_limit = debug_wait_limit();
-  const size_t smem = smem_bytes(pl.num_groups);
+  const size_t smem = wide ? smem_bytes<true>(pl.num_groups) : smem_bytes<false>(pl.num_groups);
+  const int ctas = wide ? F16Shape<true>::kCtas : F16Shape<false>::kCtas;
   if (smem > 227 * 1024) return MOE_ERR_UNSUPPORTED;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  auto k = pl.gate_up ? gemm_tc_f16_kernel<true> : gemm_tc_f16_kernel<false>;
+  auto k = wide ? (pl.gate_up ? gemm_tc_f16_kernel<true, true> : gemm_tc_f16_kernel<false, true>)
+                : (pl.gate_up ? gemm_tc_f16_kernel<true, false> : gemm_tc_f16_kernel<false, false>);
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * kCtasPerSm), dim3(kThreads), smem, s, maps, a);
+  cudaError_t e = launch_ex(pl.pdl, k, dim3(sms * ctas), dim3(kThreads), smem, s, maps, a);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;

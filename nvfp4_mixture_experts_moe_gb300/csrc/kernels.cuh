@@ -126,8 +126,14 @@ moe_status launch_gemm_small_w4a16(const GemmPlan& p, int rows_limit, cudaStream
 moe_status launch_gemm_tc_w4a16(const GemmPlan& p, int rows_min, cudaStream_t s);
 
 // Large-group W4A16 path with the dequantised weights in TMEM; needs the f16
-// copy of the activation rows (a_f16, a_mul).
-moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, cudaStream_t s);
+// copy of the activation rows (a_f16, a_mul). Computes the groups with
+// rows_min < rows <= rows_max, in tiles of up to 128 token rows (two CTAs per
+// SM) or, with `wide`, of up to 256 (one CTA per SM).
+moe_status launch_gemm_tc_f16(const GemmPlan& p, int rows_min, int rows_max, bool wide, cudaStream_t s);
+// The wide tiles' shared memory (which grows with the group count) fits a CTA.
+bool gemm_tc_f16_wide_fits(int num_groups);
+// MOE_DEBUG_F16_TILE: 1 = 128-row tiles for every group of the W4A16 GEMMs.
+bool debug_f16_narrow_only();
 
 // MXFP4: bf16 [rows, K] -> codes [rows, K/2] and E8M0 scales [rows, K/32]
 // (K % 32 == 0).
@@ -158,6 +164,8 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& p, cudaStream_t s);
 
 // Groups with at most this many rows take the small-group path.
 constexpr int kSmallGroupRows = 32;
+// Groups of more than this many rows take the W4A16 GEMMs' 256-row tiles.
+constexpr int kWideGroupRows = 128;
 
 // Single-kernel decode path (W4A16, T <= kDecodeFusedMaxT): routing,
 // permutation, both GEMMs and the combine in one cooperative launch.

@@ -145,9 +145,13 @@ def test_empty_batches_are_host_no_ops(lib):
 def test_debug_hooks_validate_keys(lib):
     assert lib.moe_debug_set(99, 1) == B.MOE_ERR_INVALID_ARG
     for key in (B.MOE_DEBUG_WAIT_LIMIT, B.MOE_DEBUG_EXTRA_ARRIVALS, B.MOE_DEBUG_DISABLE_DECODE_FUSED,
-                B.MOE_DEBUG_DECODE_STAGE_KB, B.MOE_DEBUG_FP4_TILE):
+                B.MOE_DEBUG_DECODE_STAGE_KB, B.MOE_DEBUG_FP4_TILE, B.MOE_DEBUG_F16_TILE):
         assert lib.moe_debug_set(key, 0) == B.MOE_OK   # 0 restores every default
     for bad in (-1, 6, 16, 56, 60, 100):   # FP4 tile shapes: two digits, each 0..5
         assert lib.moe_debug_set(B.MOE_DEBUG_FP4_TILE, bad) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_set(B.MOE_DEBUG_FP4_TILE, 23) == B.MOE_OK
     assert lib.moe_debug_set(B.MOE_DEBUG_FP4_TILE, 0) == B.MOE_OK
+    for bad in (-1, 2, 10):   # W4A16 tile shapes: 0 (default) or 1 (128-row tiles only)
+        assert lib.moe_debug_set(B.MOE_DEBUG_F16_TILE, bad) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_set(B.MOE_DEBUG_F16_TILE, 1) == B.MOE_OK
+    assert lib.moe_debug_set(B.MOE_DEBUG_F16_TILE, 0) == B.MOE_OK

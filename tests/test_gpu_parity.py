@@ -177,10 +177,12 @@ def test_forward_mid_full_check(cfg):
 
 
 def test_forward_group_sizes_cover_tile_shapes():
-    # top-1 routing forced by the logits: groups of 33..200 rows give every
-    # 16-row residue of the 128-row token tiles of the large-group GEMMs
-    sizes = [33, 40, 70, 90, 100, 128, 129, 200]
-    cfg = si.LayerConfig("groups8", T=sum(sizes), H=256, I=128, I_s=128, E=len(sizes), k=1)
+    # top-1 routing forced by the logits: groups of 33..128 rows give every
+    # 16-row residue of the 128-row token tiles of the large-group GEMMs;
+    # 129..513 rows the 256-row tiles (two 128-row boxes, one box for a short
+    # tail, exact multiples)
+    sizes = [33, 40, 70, 90, 100, 128, 129, 200, 256, 300, 513]
+    cfg = si.LayerConfig("groups11", T=sum(sizes), H=256, I=128, I_s=128, E=len(sizes), k=1)
     _, layer = device_layer(cfg)
     rng = np.random.default_rng(7)
     expert_of = rng.permutation(np.repeat(np.arange(len(sizes)), sizes))
@@ -196,7 +198,9 @@ def test_forward_group_sizes_cover_tile_shapes():
     assert (ids.cpu().numpy()[:, 0] == expert_of).all()
     experts, shared = OracleWeights(cfg).all()
     ref = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k)
-    check_outputs(out.float().cpu().numpy(), ref, what="groups8")
+    check_outputs(out.float().cpu().numpy(), ref, what="groups11")
+    narrow = _forward_narrow_tiles(layer, x.cuda(), logits.cuda(), ws)
+    assert torch.equal(narrow, out), "128-row tiles differ from the default tiles"
 
 
 def test_forward_decode_full_check():
@@ -206,6 +210,20 @@ def test_forward_decode_full_check():
     assert (ids == rids).all()
     ref = omoe.token_outputs_w4a16(x.float().numpy(), rids, rw, ow, ow(cfg.E))
     check_outputs(out, ref, what="decode")
+
+
+def _forward_narrow_tiles(layer, x, logits, ws):
+    """The forward with every large group in 128-row tiles (the W4A16 GEMMs'
+    other tile shape)."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd
+    try:
+        Bd.moe_debug_set(Bd.MOE_DEBUG_F16_TILE, 1)
+        out = layer.forward(x, logits, ws=ws).clone()
+        torch.cuda.synchronize()
+        assert Bd.moe_get_device_status(ws) == 0
+    finally:
+        Bd.moe_debug_set(Bd.MOE_DEBUG_F16_TILE, 0)
+    return out
 
 
 _SHARED_WEIGHTS = {}
@@ -238,6 +256,18 @@ def test_forward_large_full_check(name):
     experts, shared = ow.all()
     ref = omoe.layer(x.float().numpy(), logits.numpy(), experts, shared, cfg.k)
     check_outputs(out, ref, what=f"{name} (all {cfg.T} tokens)")
+    # the checked bits again from the 128-row tiles alone and from repeated
+    # launches of the default tiles (a race between a stage's readers and its
+    # refill shows as a few wrong weight rows in some launches)
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd
+    xd, ld = x.cuda(), logits.cuda()
+    ws = layer.workspace()
+    runs = [_forward_narrow_tiles(layer, xd, ld, ws)]
+    runs += [layer.forward(xd, ld, ws=ws).clone() for _ in range(4)]
+    torch.cuda.synchronize()
+    assert Bd.moe_get_device_status(ws) == 0
+    differ = [i for i, r in enumerate(runs) if not np.array_equal(r.float().cpu().numpy(), out)]
+    assert not differ, f"runs {differ} (0: 128-row tiles, 1..4: repeats) differ from the checked output"
 
 
 def _prepared_groups(G, N, K, gate_up, seed):
