@@ -262,8 +262,17 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf,
  *   [rows, N] (row_scale NULL means 1).
  * W4A16: a is bf16 [a_rows, K]. W4A4: a is packed NVFP4 [a_rows, K/2] with
  *   E4M3 scales a_sf [a_rows, K/16] and device global scale a_gs.
- * out_amax (nullable, device fp32, must start at 0): atomically maxed with
- *   |out| (as stored), to feed the next quantisation.
+ * out_amax (nullable, device fp32, must start at 0): W4A4 gate/up only (the
+ *   W4A16 kernels do not write it): atomically maxed with |out| (as stored),
+ *   to feed the next quantisation.
+ * rows: the number of output rows, group_offsets[num_groups], or 0. A W4A16
+ *   call that gives it (it must be exact) together with a workspace of at
+ *   least moe_gemm_workspace_size_rows(num_groups, rows, K) bytes runs the
+ *   kernels of moe_nvfp4_forward for the groups of more than 32 rows: the
+ *   activation rows are first copied, gathered through a_row_index, into the
+ *   workspace as f16 with a power-of-two scale per row, which the TMA-fed
+ *   tensor-core GEMM reads. Otherwise (rows = 0 or a smaller workspace) those
+ *   groups run a tensor-core kernel that reads a directly, at a lower rate.
  * ws: scratch of at least moe_gemm_workspace_size(num_groups) bytes.
  * Limits: K % 64 == 0, N % 128 == 0, num_groups <= 1025. MOE_MXFP4 ->
  * MOE_ERR_UNSUPPORTED here (MXFP4 layers run through moe_nvfp4_forward).
@@ -283,9 +292,13 @@ typedef struct {
   const float* row_scale;
   uint16_t* out;
   float* out_amax;
+  int rows;
 } moe_gemm_args;
 
 size_t moe_gemm_workspace_size(int num_groups);
+/* Workspace bytes for the f16 activation copy described under `rows` above
+ * (0 for a negative argument or K <= 0). */
+size_t moe_gemm_workspace_size_rows(int num_groups, int rows, int K);
 moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 

@@ -52,7 +52,7 @@ class MoeGemmArgs(ctypes.Structure):
                 ("group_offsets", ctypes.c_void_p), ("a", ctypes.c_void_p),
                 ("a_sf", ctypes.c_void_p), ("a_gs", ctypes.c_void_p),
                 ("a_row_index", ctypes.c_void_p), ("row_scale", ctypes.c_void_p),
-                ("out", ctypes.c_void_p), ("out_amax", ctypes.c_void_p)]
+                ("out", ctypes.c_void_p), ("out_amax", ctypes.c_void_p), ("rows", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -74,6 +74,7 @@ _SIGS = {
     "moe_prepare_size": (_Z, [_I, _I, _I, _I]),
     "moe_nvfp4_prepare_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_gemm_workspace_size": (_Z, [_I]),
+    "moe_gemm_workspace_size_rows": (_Z, [_I, _I, _I]),
     "moe_nvfp4_grouped_gemm": (_I, [ctypes.POINTER(MoeGemmArgs), _P, _Z, _P]),
     "moe_swiglu": (_I, [_P, _I, _I, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -204,6 +205,10 @@ def moe_nvfp4_prepare_weights(codes, sf, gs, N, K, mode, gate_up, out, stream=No
 
 def moe_gemm_workspace_size(num_groups):
     return lib().moe_gemm_workspace_size(num_groups)
+
+
+def moe_gemm_workspace_size_rows(num_groups, rows, K):
+    return lib().moe_gemm_workspace_size_rows(num_groups, rows, K)
 
 
 def moe_nvfp4_grouped_gemm(args: MoeGemmArgs, ws, stream=None):

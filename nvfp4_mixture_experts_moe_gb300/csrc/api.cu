@@ -454,11 +454,17 @@ static moe_status run_gemm(const GemmPlan& p, long long max_group_rows, cudaStre
   return launch_gemm_tc_w4a16(p, kSmallGroupRows, s);
 }
 
+size_t moe_gemm_workspace_size_rows(int num_groups, int rows, int K) {
+  if (num_groups < 0 || rows < 0 || K <= 0) return 0;
+  // header, the f16 rows [rows, K], their power-of-two multipliers [rows]
+  return moe_gemm_workspace_size(num_groups) + align_up((size_t)rows * K * 2) + align_up((size_t)rows * 4);
+}
+
 moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!a) return MOE_ERR_INVALID_ARG;
   if (a->mode == MOE_MXFP4) return MOE_ERR_UNSUPPORTED;  // the fused forward runs MXFP4 layers
   if (a->mode != MOE_W4A16 && a->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
-  if (a->num_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (a->num_groups < 0 || a->rows < 0) return MOE_ERR_INVALID_ARG;
   if (a->num_groups == 0) return MOE_OK;
   if (a->num_groups > 1025) return MOE_ERR_UNSUPPORTED;
   if (a->K <= 0 || a->N <= 0 || a->K % 64 || a->N % 128) return MOE_ERR_UNSUPPORTED;
@@ -496,7 +502,21 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   p.early_weights = false;
   p.a_f16 = nullptr;
   p.a_mul = nullptr;
-  return run_gemm(p, 1LL << 30, (cudaStream_t)stream);
+  cudaStream_t s = (cudaStream_t)stream;
+  // W4A16 with the row count and room for the f16 copy: the forward's kernels
+  const bool f16_path = a->mode == MOE_W4A16 && a->rows > kSmallGroupRows &&
+                        ws_bytes >= moe_gemm_workspace_size_rows(a->num_groups, a->rows, a->K);
+  if (!f16_path) return run_gemm(p, 1LL << 30, s);
+  uint8_t* base = static_cast<uint8_t*>(ws) + moe_gemm_workspace_size(a->num_groups);
+  uint16_t* xf = reinterpret_cast<uint16_t*>(base);
+  float* xmul = reinterpret_cast<float*>(base + align_up((size_t)a->rows * a->K * 2));
+  st = launch_rows_to_f16(static_cast<const uint16_t*>(a->a), a->a_row_index, a->rows, a->K, xf, xmul, s);
+  if (st != MOE_OK) return st;
+  p.a_f16 = xf;
+  p.a_mul = xmul;
+  p.a_rows = a->rows;
+  p.max_rows = a->rows;
+  return run_gemm(p, a->rows, s);
 }
 
 moe_status moe_swiglu(const float* gu, int rows, int I, uint16_t* h, moe_stream_t stream) {

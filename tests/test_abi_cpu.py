@@ -58,6 +58,9 @@ def test_host_validation_before_device_work(lib):
     gs = (ctypes.c_float * 1)(1.0)
     assert L.moe_nvfp4_prepare_weights(256, 256, ctypes.cast(gs, ctypes.c_void_p), 100, 64, 0, 0, 256,
                                        None) == B.MOE_ERR_INVALID_ARG
+    # grouped GEMM: a negative row count is refused on the host
+    ga = B.MoeGemmArgs(mode=0, gate_up=1, num_groups=2, N=256, K=64, rows=-1)
+    assert L.moe_nvfp4_grouped_gemm(ctypes.byref(ga), 256, 4096, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_nvfp4_quantize(256, 4, 24, 256, 256, 256, 256, 256, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(256, 256, None, None, 4, 2, 12, 256, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(256, 256, None, 8, 4, 2, 16, 256, None) == B.MOE_ERR_INVALID_ARG  # misaligned
@@ -73,6 +76,12 @@ def test_sizes(lib):
     assert 0 < n8 < n4096
     d.H = 100
     assert B.moe_workspace_size(d) == 0
+    # grouped GEMM: header, then the f16 rows and their multipliers (256-byte aligned pieces)
+    base = B.moe_gemm_workspace_size(9)
+    assert B.moe_gemm_workspace_size_rows(9, 0, 64) == base
+    assert B.moe_gemm_workspace_size_rows(9, 100, 64) == base + 12800 + 512
+    assert B.moe_gemm_workspace_size_rows(9, -1, 64) == 0
+    assert B.moe_gemm_workspace_size_rows(9, 100, 0) == 0
 
 
 def test_import_global_scale_host_only(lib):

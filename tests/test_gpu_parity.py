@@ -291,8 +291,13 @@ def _prepared_groups(G, N, K, gate_up, seed):
     return buf, oracle_w
 
 
+@pytest.mark.parametrize("f16_copy", [False, True], ids=["direct", "f16_copy"])
 @pytest.mark.parametrize("gate_up", [1, 0])
-def test_grouped_gemm_entry_tile_edges(gate_up):
+def test_grouped_gemm_entry_tile_edges(gate_up, f16_copy):
+    """The public grouped GEMM against the oracle on empty, small, ragged and
+    multi-tile groups, both without the row count (the kernel that reads the
+    bf16 rows directly) and with it and room for the f16 copy (the forward's
+    128-row and 256-row tile kernels)."""
     from nvfp4_mixture_experts_moe_gb300 import binding as Bd
     rows = [0, 40, 300, 7, 129, 33, 1, 256]
     G = len(rows)
@@ -316,7 +321,11 @@ def test_grouped_gemm_entry_tile_edges(gate_up):
     args.a_row_index = idx_d.data_ptr()
     args.row_scale = None if gate_up else rs_d.data_ptr()
     args.out = out.data_ptr()
-    ws = torch.zeros(Bd.moe_gemm_workspace_size(G), dtype=torch.uint8, device="cuda")
+    if f16_copy:
+        args.rows = total
+        ws = torch.zeros(Bd.moe_gemm_workspace_size_rows(G, total, K), dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.zeros(Bd.moe_gemm_workspace_size(G), dtype=torch.uint8, device="cuda")
     Bd.moe_nvfp4_grouped_gemm(args, ws)
     assert Bd.moe_get_device_status(ws) == 0
     got = out.float().cpu().numpy()
