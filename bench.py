@@ -624,7 +624,7 @@ def public_grouped_gemm(cfg, layer, batches, flush, stream, args, dev, pk):
     args_g.group_offsets = offs.data_ptr()
     args_g.a_row_index = row_tok.data_ptr()
     args_g.out = h.data_ptr()
-    args_g.rows = rows   # W4A16: the row count and room for the f16 copy select the forward's kernels
+    args_g.rows = rows   # the row count and room for the copies select the forward's kernels
     if w4a4:
         from nvfp4_mixture_experts_moe_gb300 import quantize_bf16
         q, sf, gs = quantize_bf16(x)
@@ -633,8 +633,7 @@ def public_grouped_gemm(cfg, layer, batches, flush, stream, args, dev, pk):
     else:
         keep = (x,)
         args_g.a = x.data_ptr()
-    gws = torch.zeros(B.moe_gemm_workspace_size(E + 1) if w4a4 else
-                      B.moe_gemm_workspace_size_rows(E + 1, rows, cfg.H), dtype=torch.uint8, device=dev)
+    gws = torch.zeros(B.moe_gemm_workspace_size_rows(E + 1, rows, cfg.H), dtype=torch.uint8, device=dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(args.warmup + K):
         flush.zero_()
@@ -653,13 +652,11 @@ def public_grouped_gemm(cfg, layer, batches, flush, stream, args, dev, pk):
     achieved = flops / (g_ms / 1e3) / 1e12
     return {"ms": g_ms, "flops": flops, "achieved": achieved, "unit": "TFLOP/s", "peak": peak,
             "frac": achieved / peak,
-            "kernel": "gemm_tc_w4a4_kernel (gather)" if w4a4 else
+            "kernel": "tile_gather_kernel + gemm_tc_fp4_wide_kernel" if w4a4 else
                       "rows_to_f16_kernel + gemm_small_kernel + gemm_tc_f16_kernel (128- and 256-row tiles)",
             "note": "moe_nvfp4_grouped_gemm, gate/up + SwiGLU, the workload's routed and shared rows, "
-                    "activations row-major with a row index"
-                    + ("" if w4a4 else " (row count given: the f16 copy of the rows is made inside the call "
-                                       "and timed)")
-                    + "; L2 flushed between launches"}
+                    "activations row-major with a row index (row count given: the copy of the rows into "
+                    "group order is made inside the call and timed); L2 flushed between launches"}
 
 
 def run_ours(args):

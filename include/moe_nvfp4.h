@@ -265,14 +265,17 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf,
  * out_amax (nullable, device fp32, must start at 0): W4A4 gate/up only (the
  *   W4A16 kernels do not write it): atomically maxed with |out| (as stored),
  *   to feed the next quantisation.
- * rows: the number of output rows, group_offsets[num_groups], or 0. A W4A16
- *   call that gives it (it must be exact) together with a workspace of at
- *   least moe_gemm_workspace_size_rows(num_groups, rows, K) bytes runs the
- *   kernels of moe_nvfp4_forward for the groups of more than 32 rows: the
- *   activation rows are first copied, gathered through a_row_index, into the
- *   workspace as f16 with a power-of-two scale per row, which the TMA-fed
- *   tensor-core GEMM reads. Otherwise (rows = 0 or a smaller workspace) those
- *   groups run a tensor-core kernel that reads a directly, at a lower rate.
+ * rows: the number of output rows, group_offsets[num_groups], or 0. A call
+ *   that gives it (it must be exact) together with a workspace of at least
+ *   moe_gemm_workspace_size_rows(num_groups, rows, K) bytes runs the kernels
+ *   of moe_nvfp4_forward, which read the activations in group order as
+ *   tensor-map tiles: W4A16 first copies the rows, gathered through
+ *   a_row_index, into the workspace as f16 with a power-of-two scale per row
+ *   (groups of more than 32 rows then run the TMA-fed tensor-core GEMM);
+ *   W4A4 gathers the codes into the workspace (without a_row_index they are
+ *   read in place) and assembles the scales into per-tile tcgen05 atoms.
+ *   Otherwise (rows = 0 or a smaller workspace) the large groups run
+ *   tensor-core kernels that gather rows inside the GEMM, at a lower rate.
  * ws: scratch of at least moe_gemm_workspace_size(num_groups) bytes.
  * Limits: K % 64 == 0, N % 128 == 0, num_groups <= 1025. MOE_MXFP4 ->
  * MOE_ERR_UNSUPPORTED here (MXFP4 layers run through moe_nvfp4_forward).
@@ -296,8 +299,8 @@ typedef struct {
 } moe_gemm_args;
 
 size_t moe_gemm_workspace_size(int num_groups);
-/* Workspace bytes for the f16 activation copy described under `rows` above
- * (0 for a negative argument or K <= 0). */
+/* Workspace bytes for the activation copies described under `rows` above,
+ * enough for either mode (0 for a negative argument or K <= 0). */
 size_t moe_gemm_workspace_size_rows(int num_groups, int rows, int K);
 moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);

@@ -454,10 +454,19 @@ static moe_status run_gemm(const GemmPlan& p, long long max_group_rows, cudaStre
   return launch_gemm_tc_w4a16(p, kSmallGroupRows, s);
 }
 
+// W4A4 calls with a row count: a bound on the groups' 128-row tiles
+static int gemm_fp4_tiles(int num_groups, int rows) { return rows / 128 + num_groups; }
+
 size_t moe_gemm_workspace_size_rows(int num_groups, int rows, int K) {
   if (num_groups < 0 || rows < 0 || K <= 0) return 0;
-  // header, the f16 rows [rows, K], their power-of-two multipliers [rows]
-  return moe_gemm_workspace_size(num_groups) + align_up((size_t)rows * K * 2) + align_up((size_t)rows * 4);
+  // W4A16: the f16 rows [rows, K] and their power-of-two multipliers [rows]
+  const size_t f16 = align_up((size_t)rows * K * 2) + align_up((size_t)rows * 4);
+  // W4A4: the codes in group order [rows, K/2] and the scale atoms, 2048 bytes
+  // per (128-row tile, 256-wide K stage)
+  const size_t fp4 = K % 256 ? 0
+                             : align_up((size_t)rows * (K / 2)) +
+                                   align_up((size_t)gemm_fp4_tiles(num_groups, rows) * (K / 256) * 2048);
+  return moe_gemm_workspace_size(num_groups) + std::max(f16, fp4);
 }
 
 moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -503,11 +512,27 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   p.a_f16 = nullptr;
   p.a_mul = nullptr;
   cudaStream_t s = (cudaStream_t)stream;
-  // W4A16 with the row count and room for the f16 copy: the forward's kernels
-  const bool f16_path = a->mode == MOE_W4A16 && a->rows > kSmallGroupRows &&
-                        ws_bytes >= moe_gemm_workspace_size_rows(a->num_groups, a->rows, a->K);
-  if (!f16_path) return run_gemm(p, 1LL << 30, s);
+  const bool copy_path = a->rows > 0 && ws_bytes >= moe_gemm_workspace_size_rows(a->num_groups, a->rows, a->K);
   uint8_t* base = static_cast<uint8_t*>(ws) + moe_gemm_workspace_size(a->num_groups);
+  if (a->mode == MOE_W4A4) {
+    if (!copy_path) return run_gemm(p, 1LL << 30, s);
+    // the forward's layout: codes in group order (gathered through the row
+    // index, or read in place without one) and per-tile scale atoms
+    const bool gather = a->a_row_index != nullptr;
+    uint8_t* q = gather ? base : nullptr;
+    uint8_t* atoms = base + align_up((size_t)a->rows * (a->K / 2));
+    st = launch_tile_gather(gather ? static_cast<const uint8_t*>(a->a) : nullptr, a->a_sf, a->a_row_index, a->K,
+                            a->group_offsets, a->num_groups, gemm_fp4_tiles(a->num_groups, a->rows), q, atoms,
+                            false, s);
+    if (st != MOE_OK) return st;
+    p.a = gather ? static_cast<const void*>(q) : a->a;
+    p.a_sf = atoms;
+    p.a_rows = a->rows;
+    p.max_rows = a->rows;
+    return launch_gemm_tc_fp4(p, s);
+  }
+  // W4A16 with the row count and room for the f16 copy: the forward's kernels
+  if (!copy_path || a->rows <= kSmallGroupRows) return run_gemm(p, 1LL << 30, s);
   uint16_t* xf = reinterpret_cast<uint16_t*>(base);
   float* xmul = reinterpret_cast<float*>(base + align_up((size_t)a->rows * a->K * 2));
   st = launch_rows_to_f16(static_cast<const uint16_t*>(a->a), a->a_row_index, a->rows, a->K, xf, xmul, s);

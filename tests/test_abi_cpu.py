@@ -82,6 +82,9 @@ def test_sizes(lib):
     assert B.moe_gemm_workspace_size_rows(9, 100, 64) == base + 12800 + 512
     assert B.moe_gemm_workspace_size_rows(9, -1, 64) == 0
     assert B.moe_gemm_workspace_size_rows(9, 100, 0) == 0
+    # K % 256 == 0: also room for the W4A4 codes and per-tile scale atoms; the larger need counts
+    assert B.moe_gemm_workspace_size_rows(9, 100, 256) == base + 51200 + 512
+    assert B.moe_gemm_workspace_size_rows(1000, 100, 256) == B.moe_gemm_workspace_size(1000) + 12800 + 1000 * 2048
 
 
 def test_import_global_scale_host_only(lib):

@@ -120,8 +120,13 @@ def _fp4_groups(G, N, K, gate_up, seed):
     return buf, ow
 
 
+@pytest.mark.parametrize("path", ["gather", "tiles", "tiles_in_place"])
 @pytest.mark.parametrize("gate_up", [1, 0])
-def test_w4a4_grouped_gemm_tile_edges(gate_up):
+def test_w4a4_grouped_gemm_tile_edges(gate_up, path):
+    """The public W4A4 grouped GEMM against the oracle on empty, small,
+    ragged and multi-tile groups: without the row count (the kernel that
+    gathers rows inside the GEMM), and with it (the forward's tile kernels),
+    the codes gathered through the row index or read in place in group order."""
     from nvfp4_mixture_experts_moe_gb300 import binding as Bd, quantize_bf16
     rows = [0, 40, 300, 7, 129, 128, 1]
     G = len(rows)
@@ -143,10 +148,17 @@ def test_w4a4_grouped_gemm_tile_edges(gate_up):
     args.group_offsets = offs_d.data_ptr()
     args.a, args.a_sf, args.a_gs = aq.data_ptr(), asf.data_ptr(), ags.data_ptr()
     args.a_row_index = idx_d.data_ptr()
+    if path == "tiles_in_place":   # the rows already in group order, no row index
+        aq_g, asf_g = aq[idx_d.long()].contiguous(), asf[idx_d.long()].contiguous()
+        args.a, args.a_sf, args.a_row_index = aq_g.data_ptr(), asf_g.data_ptr(), None
     args.row_scale = None if gate_up else rs_d.data_ptr()
     args.out = out.data_ptr()
     args.out_amax = amax.data_ptr() if gate_up else None
-    ws = torch.zeros(Bd.moe_gemm_workspace_size(G), dtype=torch.uint8, device="cuda")
+    if path == "gather":
+        ws = torch.zeros(Bd.moe_gemm_workspace_size(G), dtype=torch.uint8, device="cuda")
+    else:
+        args.rows = total
+        ws = torch.zeros(Bd.moe_gemm_workspace_size_rows(G, total, K), dtype=torch.uint8, device="cuda")
     Bd.moe_nvfp4_grouped_gemm(args, ws)
     assert Bd.moe_get_device_status(ws) == 0
     got = out.float().cpu().numpy()
