@@ -266,7 +266,7 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf,
  *   W4A16 kernels do not write it): atomically maxed with |out| (as stored),
  *   to feed the next quantisation.
  * rows: the number of output rows, group_offsets[num_groups], or 0. A call
- *   that gives it (it must be exact) together with a workspace of at least
+ *   that gives it together with a workspace of at least
  *   moe_gemm_workspace_size_rows(num_groups, rows, K) bytes runs the kernels
  *   of moe_nvfp4_forward, which read the activations in group order as
  *   tensor-map tiles: W4A16 first copies the rows, gathered through
@@ -276,6 +276,10 @@ moe_status moe_nvfp4_prepare_weights(const uint8_t* codes, const uint8_t* sf,
  *   read in place) and assembles the scales into per-tile tcgen05 atoms.
  *   Otherwise (rows = 0 or a smaller workspace) the large groups run
  *   tensor-core kernels that gather rows inside the GEMM, at a lower rate.
+ *   A larger rows value only costs workspace (rows past group_offsets[
+ *   num_groups] are neither read nor computed); a smaller one makes the
+ *   large-group GEMM record MOE_ERR_DEVICE in the workspace status word and
+ *   write nothing.
  * ws: scratch of at least moe_gemm_workspace_size(num_groups) bytes.
  * Limits: K % 64 == 0, N % 128 == 0, num_groups <= 1025. MOE_MXFP4 ->
  * MOE_ERR_UNSUPPORTED here (MXFP4 layers run through moe_nvfp4_forward).

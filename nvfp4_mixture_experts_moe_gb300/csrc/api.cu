@@ -522,8 +522,8 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
     uint8_t* q = gather ? base : nullptr;
     uint8_t* atoms = base + align_up((size_t)a->rows * (a->K / 2));
     st = launch_tile_gather(gather ? static_cast<const uint8_t*>(a->a) : nullptr, a->a_sf, a->a_row_index, a->K,
-                            a->group_offsets, a->num_groups, gemm_fp4_tiles(a->num_groups, a->rows), q, atoms,
-                            false, s);
+                            a->group_offsets, a->num_groups, gemm_fp4_tiles(a->num_groups, a->rows), a->rows, q,
+                            atoms, false, s);
     if (st != MOE_OK) return st;
     p.a = gather ? static_cast<const void*>(q) : a->a;
     p.a_sf = atoms;
@@ -535,7 +535,9 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
   if (!copy_path || a->rows <= kSmallGroupRows) return run_gemm(p, 1LL << 30, s);
   uint16_t* xf = reinterpret_cast<uint16_t*>(base);
   float* xmul = reinterpret_cast<float*>(base + align_up((size_t)a->rows * a->K * 2));
-  st = launch_rows_to_f16(static_cast<const uint16_t*>(a->a), a->a_row_index, a->rows, a->K, xf, xmul, s);
+  // (rows past group_offsets[G] are not read: the caller's arrays may end there)
+  st = launch_rows_to_f16(static_cast<const uint16_t*>(a->a), a->a_row_index, a->rows, a->K, xf, xmul, s, false,
+                          a->group_offsets + a->num_groups);
   if (st != MOE_OK) return st;
   p.a_f16 = xf;
   p.a_mul = xmul;
@@ -669,8 +671,8 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     st = mx ? launch_quantize_mx(x, T, H, f.xq_tok, f.xsf_tok, s)
             : launch_quantize_bf16(x, T, H, &f.hdr->amax[0], f.xq_tok, f.xsf_tok, f.xgs, x_static, s, pdl);
     if (st != MOE_OK) return st;
-    st = launch_tile_gather(f.xq_tok, f.xsf_tok, f.row_token, H, f.gofs, EL + (has_shared ? 1 : 0), f.tiles, f.xq,
-                            f.xsf, mx, s);
+    st = launch_tile_gather(f.xq_tok, f.xsf_tok, f.row_token, H, f.gofs, EL + (has_shared ? 1 : 0), f.tiles, rows,
+                            f.xq, f.xsf, mx, s);
     if (st != MOE_OK) return st;
   }
   if (f.xf) {  // f16 copy of x, rows in group order, for the large-group tensor-core GEMM
@@ -713,7 +715,7 @@ moe_status moe_nvfp4_forward(const moe_layer_desc* L, const uint16_t* x, const f
     st = mx ? launch_quantize_mx(f.h, rows, I, f.hq, f.hsf_lin, s)
             : launch_quantize_bf16(f.h, rows, I, &f.hdr->amax[1], f.hq, f.hsf_lin, f.hgs, h_static, s, pdl);
     if (st != MOE_OK) return st;
-    st = launch_tile_gather(nullptr, f.hsf_lin, nullptr, I, f.gofs, G, f.tiles, nullptr, f.hsf, mx, s);
+    st = launch_tile_gather(nullptr, f.hsf_lin, nullptr, I, f.gofs, G, f.tiles, 0, nullptr, f.hsf, mx, s);
     if (st != MOE_OK) return st;
   } else if (f.hf) {
     st = launch_rows_to_f16(f.h, nullptr, rows, I, f.hf, f.hmul, s, pdl);

@@ -107,6 +107,7 @@ struct Args {
   uint16_t* out;
   float* out_last_f32;
   int rows_min, rows_max;   // the groups this launch computes: rows_min < rows <= rows_max
+  int a_rows;               // rows of the f16 copy and of a_mul
   int* status;
   long long wait_limit;      // cycles per bounded wait (a timeout aborts the kernel)
 };
@@ -183,6 +184,10 @@ __global__ void __launch_bounds__(kThreads, F16Shape<WIDE>::kCtas)
   const int KS = (K + kBK - 1) / kBK;     // the last stage has one half when K % 128 == 64
   const int KB64 = K / kHalf;
   pdl_wait();
+  if (p.group_offsets[G] > p.a_rows) {   // the copied rows do not cover the groups: compute nothing
+    if (tid == 0) set_status(p.status, MOE_ERR_DEVICE);
+    return;
+  }
 
   for (int g = tid; g < G; g += kThreads) {
     const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
@@ -577,6 +582,7 @@ moe_status launch_gemm_tc_f16(const GemmPlan& pl, int rows_min, int rows_max, bo
   a.out_last_f32 = pl.out_last_f32;
   a.rows_min = rows_min;
   a.rows_max = rows_max;
+  a.a_rows = pl.a_rows;
   a.status = pl.status;
   a.wait_limit = debug_wait_limit();
   const size_t smem = wide ? smem_bytes<true>(pl.num_groups) : smem_bytes<false>(pl.num_groups);

@@ -88,6 +88,7 @@ struct Args {
   uint16_t* out;
   float* out_last_f32;
   float* out_amax;
+  int a_rows;                  // rows of the activation codes (group order)
   int* status;
   long long wait_limit;        // cycles per bounded wait (a timeout aborts the kernel)
 };
@@ -285,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, CTAS) gemm_tc_fp4_kernel(const __gri
   const int MT = N / kM;
   const int KS = K / kBK;
   pdl_wait();
+  if (p.group_offsets[G] > p.a_rows) {   // the codes do not cover the groups: compute nothing
+    if (tid == 0) set_status(p.status, MOE_ERR_DEVICE);
+    return;
+  }
 
   for (int g = tid; g < G; g += kThreads) {
     const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
@@ -584,6 +589,7 @@ constexpr int kSfWarp0 = 10;    // 10, 11: scale copies of half 0, 1
 constexpr int kWALoadWarp = 12;  // the group's rows
 constexpr int kWBLoadWarp = 13;  // the two weight tiles
 constexpr int kWThreads = 14 * 32;
+static_assert(kEpiWarps == kMmaWarp0, "the epilogue warps are warps 0 .. kMmaWarp0 - 1");
 
 struct WSmem {
   uint64_t aready[kWStages];   // the activation tile landed
@@ -622,6 +628,10 @@ __global__ void __maxnreg__(128)
   const int MT2 = N / (2 * kM);   // items per 128-row tile of a group: pairs of weight tiles
   const int KS = K / kBK;
   pdl_wait();
+  if (p.group_offsets[G] > p.a_rows) {   // the codes do not cover the groups: compute nothing
+    if (tid == 0) set_status(p.status, MOE_ERR_DEVICE);
+    return;
+  }
 
   for (int g = tid; g < G; g += kWThreads) {
     const int rows = p.group_offsets[g + 1] - p.group_offsets[g];
@@ -926,6 +936,7 @@ moe_status launch_gemm_tc_fp4(const GemmPlan& pl, cudaStream_t s) {
   a.out = pl.out;
   a.out_last_f32 = pl.out_last_f32;
   a.out_amax = pl.out_amax;
+  a.a_rows = pl.a_rows;
   a.status = pl.status;
   a.wait_limit = debug_wait_limit();
   // tile shape: 1 = one CTA per SM, weight rows on M; 2 = two CTAs per SM,

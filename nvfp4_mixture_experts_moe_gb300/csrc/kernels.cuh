@@ -144,22 +144,26 @@ moe_status launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* q, ui
 // The atoms: per (tile, 256-wide K stage) four (NVFP4, E4M3 per 16) or two
 // (MXFP4, E8M0 per 32) 512-byte tcgen05 scale-factor atoms; rows past a
 // group's end carry scale 0.
+// q has room for q_rows rows (codes of rows past it are not copied).
 moe_status launch_tile_gather(const uint8_t* q_src, const uint8_t* sf_src, const int32_t* src_row, int K,
-                              const int32_t* gofs, int G, int tiles_max, uint8_t* q, uint8_t* sf_tiles, bool mx,
-                              cudaStream_t s);
+                              const int32_t* gofs, int G, int tiles_max, int q_rows, uint8_t* q, uint8_t* sf_tiles,
+                              bool mx, cudaStream_t s);
 
 // bf16 rows -> f16 rows scaled by a power of two so that each row's largest
 // magnitude lies in [2^14, 2^15); mul[r] = 2^-s undoes it. Row r of dst is
 // row src_index[r] of src (row r when src_index is null).
+// rows_limit (nullable, device): rows at or past *rows_limit are skipped (a
+// caller's row count that may exceed its arrays).
 moe_status launch_rows_to_f16(const uint16_t* src, const int32_t* src_index, int rows, int K, uint16_t* dst,
-                              float* mul, cudaStream_t s, bool pdl = false);
+                              float* mul, cudaStream_t s, bool pdl = false, const int32_t* rows_limit = nullptr);
 
 // W4A4: block-scaled FP4 tcgen05 kernel (every non-empty group).
 moe_status launch_gemm_tc_w4a4(const GemmPlan& p, cudaStream_t s);
 
 // W4A4 GEMM of the fused forward: activation codes in group order (a, a_rows
 // rows) loaded as tensor-map boxes, their scales as per-tile atoms (a_sf, from
-// launch_tile_gather).
+// launch_tile_gather). The large-group GEMMs record MOE_ERR_DEVICE and compute
+// nothing when group_offsets[G] exceeds a_rows.
 moe_status launch_gemm_tc_fp4(const GemmPlan& p, cudaStream_t s);
 
 // Groups with at most this many rows take the small-group path.

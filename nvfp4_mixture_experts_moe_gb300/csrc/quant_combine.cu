@@ -245,7 +245,7 @@ template <int BLK>
 __global__ void __launch_bounds__(256) tile_gather_kernel(const uint8_t* __restrict__ q_src,
                                                           const uint8_t* __restrict__ sf_src,
                                                           const int32_t* __restrict__ src_row, int K,
-                                                          const int32_t* __restrict__ gofs, int G,
+                                                          const int32_t* __restrict__ gofs, int G, int q_rows,
                                                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf_tiles) {
   pdl_wait();
   extern __shared__ __align__(16) uint8_t smem_tg[];
@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(256) tile_gather_kernel(const uint8_t* __restr
   // codes: a warp per row, 16 bytes per lane
   if (src_row != nullptr) {
     const int n16 = K / 32;   // 16-byte pieces of a row's codes
-    for (int m = tid >> 5; m < nrows; m += 8) {
+    const int nq = min(nrows, q_rows - row0);   // rows q has room for
+    for (int m = tid >> 5; m < nq; m += 8) {
       const uint4* from = reinterpret_cast<const uint4*>(q_src + (size_t)__ldg(src_row + row0 + m) * (K / 2));
       uint4* to = reinterpret_cast<uint4*>(q + (size_t)(row0 + m) * (K / 2));
       for (int j = tid & 31; j < n16; j += 32) to[j] = __ldg(from + j);   // read by up to k+1 tiles: keep in L2
@@ -316,8 +317,8 @@ __global__ void __launch_bounds__(256) tile_gather_kernel(const uint8_t* __restr
 }
 
 moe_status launch_tile_gather(const uint8_t* q_src, const uint8_t* sf_src, const int32_t* src_row, int K,
-                              const int32_t* gofs, int G, int tiles_max, uint8_t* q, uint8_t* sf_tiles, bool mx,
-                              cudaStream_t s) {
+                              const int32_t* gofs, int G, int tiles_max, int q_rows, uint8_t* q, uint8_t* sf_tiles,
+                              bool mx, cudaStream_t s) {
   if (K % 256 || G <= 0) return MOE_ERR_UNSUPPORTED;
   if (tiles_max <= 0) return MOE_OK;
   const int atoms = K / (4 * (mx ? 32 : 16));
@@ -326,7 +327,8 @@ moe_status launch_tile_gather(const uint8_t* q_src, const uint8_t* sf_src, const
   auto k = mx ? tile_gather_kernel<32> : tile_gather_kernel<16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_ok(e);
-  e = launch_ex(false, k, dim3(tiles_max), dim3(256), smem, s, q_src, sf_src, src_row, K, gofs, G, q, sf_tiles);
+  e = launch_ex(false, k, dim3(tiles_max), dim3(256), smem, s, q_src, sf_src, src_row, K, gofs, G, q_rows, q,
+                sf_tiles);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return cuda_ok(cudaGetLastError());
@@ -373,11 +375,12 @@ moe_status launch_fold_scales(const uint8_t* in, size_t n, float ratio, uint8_t*
 // in f16 except magnitudes below 2^-24 of that maximum, which flush.
 __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __restrict__ src,
                                                           const int32_t* __restrict__ src_index, int rows, int K,
-                                                          uint16_t* __restrict__ dst, float* __restrict__ mul) {
+                                                          uint16_t* __restrict__ dst, float* __restrict__ mul,
+                                                          const int32_t* __restrict__ rows_limit) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-  if (row >= rows) return;
+  if (row >= rows || (rows_limit != nullptr && row >= __ldg(rows_limit))) return;
   const int srow = src_index ? __ldg(src_index + row) : row;
   const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)srow * K);
   uint4* d = reinterpret_cast<uint4*>(dst + (size_t)row * K);
@@ -409,11 +412,11 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __rest
 }
 
 moe_status launch_rows_to_f16(const uint16_t* src, const int32_t* src_index, int rows, int K, uint16_t* dst,
-                              float* mul, cudaStream_t s, bool pdl) {
+                              float* mul, cudaStream_t s, bool pdl, const int32_t* rows_limit) {
   if (rows == 0) return MOE_OK;
   const int blocks = (int)(((size_t)rows * 32 + 255) / 256);
   cudaError_t e = launch_ex(pdl, rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, src_index, rows, K, dst,
-                            mul);
+                            mul, rows_limit);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;

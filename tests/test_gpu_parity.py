@@ -226,6 +226,39 @@ def _forward_narrow_tiles(layer, x, logits, ws):
     return out
 
 
+def test_grouped_gemm_row_count_checked():
+    """The public W4A16 grouped GEMM's row count: a larger one than the
+    groups hold gives the exact count's bits (rows past the groups are
+    neither read nor computed); a smaller one makes the large-group GEMM
+    record MOE_ERR_DEVICE and compute nothing."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd
+    rows = [40, 300, 7, 129]
+    G, N, K = len(rows), 256, 512
+    buf, _ = _prepared_groups(G, N, K, 1, seed=31)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    total = int(off[-1])
+    g = torch.Generator().manual_seed(6)
+    a = torch.randn(total + 3, K, generator=g).to(torch.bfloat16).cuda()
+    idx = torch.randperm(total + 3, generator=g)[:total].to(torch.int32).cuda()
+    offs = torch.from_numpy(off).cuda()
+
+    def run(count):
+        out = torch.full((total, N // 2), float("nan"), dtype=torch.bfloat16, device="cuda")
+        args = Bd.MoeGemmArgs(mode=0, gate_up=1, num_groups=G, N=N, K=K, rows=count)
+        args.weights, args.group_offsets = buf.data_ptr(), offs.data_ptr()
+        args.a, args.a_row_index, args.out = a.data_ptr(), idx.data_ptr(), out.data_ptr()
+        ws = torch.zeros(Bd.moe_gemm_workspace_size_rows(G, count, K), dtype=torch.uint8, device="cuda")
+        Bd.moe_nvfp4_grouped_gemm(args, ws)
+        return out, Bd.moe_get_device_status(ws)
+
+    exact, st = run(total)
+    assert st == 0
+    more, st = run(total + 37)
+    assert st == 0 and torch.equal(more, exact)
+    _, st = run(total - 1)
+    assert st == Bd.MOE_ERR_DEVICE
+
+
 _SHARED_WEIGHTS = {}
 
 

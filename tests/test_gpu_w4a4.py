@@ -178,6 +178,41 @@ def test_w4a4_grouped_gemm_tile_edges(gate_up, path):
         assert amax.item() == float(np.abs(got).max())
 
 
+def test_w4a4_grouped_gemm_row_count_checked():
+    """The public W4A4 grouped GEMM's row count: a larger one than the groups
+    hold gives the exact count's bits; a smaller one makes the GEMM record
+    MOE_ERR_DEVICE and compute nothing (the code gather stays within the
+    workspace)."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd, quantize_bf16
+    rows = [40, 300, 7, 129]
+    G, N, K = len(rows), 256, 512
+    buf, _ = _fp4_groups(G, N, K, 1, seed=33)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    total = int(off[-1])
+    g = torch.Generator().manual_seed(8)
+    a = torch.randn(total + 5, K, generator=g).to(torch.bfloat16)
+    aq, asf, ags = quantize_bf16(a.cuda())
+    idx = torch.randperm(total + 5, generator=g)[:total].to(torch.int32).cuda()
+    offs = torch.from_numpy(off).cuda()
+
+    def run(count):
+        out = torch.full((total, N // 2), float("nan"), dtype=torch.bfloat16, device="cuda")
+        args = Bd.MoeGemmArgs(mode=1, gate_up=1, num_groups=G, N=N, K=K, rows=count)
+        args.weights, args.group_offsets = buf.data_ptr(), offs.data_ptr()
+        args.a, args.a_sf, args.a_gs = aq.data_ptr(), asf.data_ptr(), ags.data_ptr()
+        args.a_row_index, args.out = idx.data_ptr(), out.data_ptr()
+        ws = torch.zeros(Bd.moe_gemm_workspace_size_rows(G, count, K), dtype=torch.uint8, device="cuda")
+        Bd.moe_nvfp4_grouped_gemm(args, ws)
+        return out, Bd.moe_get_device_status(ws)
+
+    exact, st = run(total)
+    assert st == 0
+    more, st = run(total + 37)
+    assert st == 0 and torch.equal(more, exact)
+    _, st = run(total - 1)
+    assert st == Bd.MOE_ERR_DEVICE
+
+
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "w4a4_full_tokens.npz")
 
 
