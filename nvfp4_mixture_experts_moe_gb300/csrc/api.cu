@@ -525,11 +525,15 @@ moe_status moe_nvfp4_grouped_gemm(const moe_gemm_args* a, void* ws, size_t ws_by
                             a->group_offsets, a->num_groups, gemm_fp4_tiles(a->num_groups, a->rows), a->rows, q,
                             atoms, false, s);
     if (st != MOE_OK) return st;
-    p.a = gather ? static_cast<const void*>(q) : a->a;
-    p.a_sf = atoms;
-    p.a_rows = a->rows;
-    p.max_rows = a->rows;
-    return launch_gemm_tc_fp4(p, s);
+    GemmPlan t = p;
+    t.a = gather ? static_cast<const void*>(q) : a->a;
+    t.a_sf = atoms;
+    t.a_rows = a->rows;
+    t.max_rows = a->rows;
+    st = launch_gemm_tc_fp4(t, s);
+    // a tile shape whose shared memory cannot hold this many groups: the
+    // gather kernel instead (the copies above are then unused)
+    return st == MOE_ERR_UNSUPPORTED ? run_gemm(p, 1LL << 30, s) : st;
   }
   // W4A16 with the row count and room for the f16 copy: the forward's kernels
   if (!copy_path || a->rows <= kSmallGroupRows) return run_gemm(p, 1LL << 30, s);

@@ -213,6 +213,44 @@ def test_w4a4_grouped_gemm_row_count_checked():
     assert st == Bd.MOE_ERR_DEVICE
 
 
+def test_w4a4_grouped_gemm_many_groups_fall_back():
+    """600 groups with N = 384 (not a multiple of 256): the tile kernel's
+    shape for that N cannot hold the groups in shared memory, so a call with
+    the row count runs the gather kernel, with its exact bits."""
+    from nvfp4_mixture_experts_moe_gb300 import binding as Bd, quantize_bf16
+    G, N, K = 600, 384, 256
+    size = Bd.moe_prepare_size(N, K, 1, 0)
+    g = torch.Generator().manual_seed(12)
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    wq, wsf, wgs = quantize_bf16(w.cuda())
+    buf = torch.empty(G * size, dtype=torch.uint8, device="cuda")
+    Bd.moe_nvfp4_prepare_weights(wq, wsf, [wgs.item()], N, K, 1, 0, buf[:size])
+    buf.view(G, size)[1:] = buf[:size]   # every group the same prepared block
+    rows = torch.randint(0, 3, (G,), generator=g).tolist()
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    total = int(off[-1])
+    a = torch.randn(total, K, generator=g).to(torch.bfloat16)
+    aq, asf, ags = quantize_bf16(a.cuda())
+    rs = (torch.rand(total, generator=g) + 0.5).cuda()
+    offs = torch.from_numpy(off).cuda()
+
+    def run(count):
+        out = torch.full((total, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        args = Bd.MoeGemmArgs(mode=1, gate_up=0, num_groups=G, N=N, K=K, rows=count)
+        args.weights, args.group_offsets = buf.data_ptr(), offs.data_ptr()
+        args.a, args.a_sf, args.a_gs = aq.data_ptr(), asf.data_ptr(), ags.data_ptr()
+        args.row_scale, args.out = rs.data_ptr(), out.data_ptr()
+        n = Bd.moe_gemm_workspace_size_rows(G, count, K) if count else Bd.moe_gemm_workspace_size(G)
+        ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        Bd.moe_nvfp4_grouped_gemm(args, ws)
+        assert Bd.moe_get_device_status(ws) == 0
+        return out
+
+    ref = run(0)
+    assert not torch.isnan(ref.float()).any()
+    assert torch.equal(run(total), ref)
+
+
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "w4a4_full_tokens.npz")
 
 
