@@ -373,6 +373,9 @@ moe_status launch_fold_scales(const uint8_t* in, size_t n, float ratio, uint8_t*
 // dst row r comes from src row src_index[r] (r when src_index is null).
 // With the row's largest magnitude in [2^14, 2^15) every bf16 value is exact
 // in f16 except magnitudes below 2^-24 of that maximum, which flush.
+// V > 0: the row (at most V 16-byte pieces per lane) stays in registers
+// between the max and the conversion, so it is read once; V = 0 reads it twice.
+template <int V>
 __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __restrict__ src,
                                                           const int32_t* __restrict__ src_index, int rows, int K,
                                                           uint16_t* __restrict__ dst, float* __restrict__ mul,
@@ -384,12 +387,24 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __rest
   const int srow = src_index ? __ldg(src_index + row) : row;
   const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)srow * K);
   uint4* d = reinterpret_cast<uint4*>(dst + (size_t)row * K);
-  uint32_t m = 0;
-  for (int i = lane; i < K / 8; i += 32) {
-    const uint4 v = __ldg(s + i);
+  const int n16 = K / 8;
+  auto row_max = [](uint32_t m, const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) m = max(m, max(finite_mag(w[q] & 0x7fffu), finite_mag((w[q] >> 16) & 0x7fffu)));
+    return m;
+  };
+  uint32_t m = 0;
+  uint4 keep[V > 0 ? V : 1];
+  if (V > 0) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = lane + 32 * j;
+      keep[j] = i < n16 ? __ldg(s + i) : make_uint4(0u, 0u, 0u, 0u);
+      m = row_max(m, keep[j]);
+    }
+  } else {
+    for (int i = lane; i < n16; i += 32) m = row_max(m, __ldg(s + i));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -397,8 +412,7 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __rest
   int sh = (m == 0) ? 0 : 141 - max(e, 1);
   sh = max(-113, min(sh, 126));
   const float up = __int_as_float((127 + sh) << 23);
-  for (int i = lane; i < K / 8; i += 32) {
-    const uint4 v = __ldg(s + i);
+  auto convert = [up](const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
@@ -406,7 +420,16 @@ __global__ void __launch_bounds__(256) rows_to_f16_kernel(const uint16_t* __rest
       const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * up, __uint_as_float(w[q] & 0xffff0000u) * up);
       o[q] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    d[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  if (V > 0) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = lane + 32 * j;
+      if (i < n16) d[i] = convert(keep[j]);
+    }
+  } else {
+    for (int i = lane; i < n16; i += 32) d[i] = convert(__ldg(s + i));
   }
   if (lane == 0) mul[row] = __int_as_float((127 - sh) << 23);
 }
@@ -415,8 +438,11 @@ moe_status launch_rows_to_f16(const uint16_t* src, const int32_t* src_index, int
                               float* mul, cudaStream_t s, bool pdl, const int32_t* rows_limit) {
   if (rows == 0) return MOE_OK;
   const int blocks = (int)(((size_t)rows * 32 + 255) / 256);
-  cudaError_t e = launch_ex(pdl, rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, src_index, rows, K, dst,
-                            mul, rows_limit);
+  const int per = (K / 8 + 31) / 32;   // 16-byte pieces of a row per lane
+  // (keeping up to 16 pieces per lane in registers halved the resident warps
+  // and doubled the time at K = 4096; up to 8 pieces the single read pays)
+  auto k = per <= 8 ? rows_to_f16_kernel<8> : rows_to_f16_kernel<0>;
+  cudaError_t e = launch_ex(pdl, k, dim3(blocks), dim3(256), 0, s, src, src_index, rows, K, dst, mul, rows_limit);
   if (e != cudaSuccess) return cuda_ok(e);
   count_launches(1);
   return MOE_OK;
