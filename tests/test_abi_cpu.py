@@ -167,3 +167,33 @@ def test_debug_hooks_validate_keys(lib):
         assert lib.moe_debug_set(B.MOE_DEBUG_F16_TILE, bad) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_set(B.MOE_DEBUG_F16_TILE, 1) == B.MOE_OK
     assert lib.moe_debug_set(B.MOE_DEBUG_F16_TILE, 0) == B.MOE_OK
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """The binding's ctypes structs have the C header's field offsets and
+    sizes (compiled here with the host C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    structs = {"moe_gemm_args": B.MoeGemmArgs, "moe_layer_desc": B.MoeLayerDesc}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "moe_nvfp4.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for name, _ in py._fields_:
+            lines.append(f'  printf("{cname} {name} %zu\\n", offsetof({cname}, {name}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([cc, "-std=c99", "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        cname, field, value = line.split()
+        got[(cname, field)] = int(value)
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for name, _ in py._fields_:
+            assert got[(cname, name)] == getattr(py, name).offset, (cname, name)
